@@ -1,0 +1,151 @@
+"""fp64 CPU oracle for causal linear self-attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It shares no code with the CUDA
+library in ``sub_linear_memory_gb300`` and never imports it.
+
+Two independent formulations of "Sub-Linear Memory: How to Make Performers
+SLiM", section 2.1:
+  * ``recurrence_forward`` / ``recurrence_backward``: the per-step prefix-sum
+    recurrence, eq. (3)-(4), in plain C (``slim_oracle.c``), fp64, OpenMP over
+    heads;
+  * ``quadratic.forward`` / ``quadratic.backward``: the explicit quadratic form
+    of eq. (2), numpy fp64;
+  * ``quadratic.softmax_forward``: eq. (1), the exponential attention that the
+    randomized feature map approximates.
+"""
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+from . import quadratic  # noqa: F401  (re-exported)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "slim_oracle.c")
+_LIB = os.path.join(_HERE, "libslim_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+MAP_FAVOR = 0
+MAP_ELU = 1
+
+
+def build(force=False):
+    """Compile the C oracle with gcc (plain C99 + OpenMP; no target flags)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + ".tmp%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            lib.oracle_forward.argtypes = [dp] * 5 + [ctypes.c_long] * 3 + [ctypes.c_int] * 4
+            lib.oracle_backward.argtypes = [dp] * 10 + [ctypes.c_long] * 3 + [ctypes.c_int] * 4
+            lib.oracle_feature_map.argtypes = [dp] * 3 + [ctypes.c_long] + [ctypes.c_int] * 3
+            for fn in (lib.oracle_forward, lib.oracle_backward, lib.oracle_feature_map):
+                fn.restype = ctypes.c_int
+            lib.oracle_max_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _check_w(w, d):
+    if w is not None and (np.ndim(w) != 2 or np.shape(w)[0] != d):
+        raise ValueError("W must be [d, M] with d = %d, got %s" % (d, np.shape(w)))
+
+
+def _as4d(x):
+    x = _f64(x)
+    if x.ndim == 2:
+        x = x[None, None]
+    if x.ndim != 4:
+        raise ValueError("expected [B, H, L, d] or [L, d]")
+    return x
+
+
+def max_threads():
+    return int(_load().oracle_max_threads())
+
+
+def feature_map(x, w):
+    """g applied to every row of x ([rows, d]); w None selects elu+1."""
+    x = _f64(x)
+    rows, d = x.reshape(-1, x.shape[-1]).shape
+    _check_w(w, d)
+    m = d if w is None else int(np.shape(w)[1])
+    wf = None if w is None else _f64(w)
+    out = np.empty((rows, m), dtype=np.float64)
+    rc = _load().oracle_feature_map(_ptr(x), _ptr(wf), _ptr(out), rows, d, m,
+                                     MAP_ELU if w is None else MAP_FAVOR)
+    if rc:
+        raise ValueError("oracle_feature_map failed (%d)" % rc)
+    return out.reshape(x.shape[:-1] + (m,))
+
+
+def recurrence_forward(q, k, v, w, threads=0):
+    """Y = Att^lin(Q, K, V) by the per-step recurrence; arrays [B, H, L, d]
+    (or [L, d]).  w None selects elu+1, else W is [d, M]."""
+    shape = np.shape(q)
+    q, k, v = _as4d(q), _as4d(k), _as4d(v)
+    b, h, length, d = q.shape
+    _check_w(w, d)
+    m = d if w is None else int(np.shape(w)[1])
+    wf = None if w is None else _f64(w)
+    y = np.empty_like(q)
+    rc = _load().oracle_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(wf), _ptr(y), b, h, length,
+                                d, m, MAP_ELU if w is None else MAP_FAVOR, int(threads))
+    if rc:
+        raise ValueError("oracle_forward failed (%d)" % rc)
+    return y.reshape(shape)
+
+
+def recurrence_backward(q, k, v, w, dy, threads=0, want_dw=True, want_y=False):
+    """Gradients of sum(dy * Y): returns (dq, dk, dv, dw[, y]); dw is None for
+    elu+1 or when ``want_dw`` is False."""
+    shape = np.shape(q)
+    q, k, v, dy = _as4d(q), _as4d(k), _as4d(v), _as4d(dy)
+    b, h, length, d = q.shape
+    _check_w(w, d)
+    m = d if w is None else int(np.shape(w)[1])
+    wf = None if w is None else _f64(w)
+    dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
+    dw = np.empty((d, m), dtype=np.float64) if (w is not None and want_dw) else None
+    y = np.empty_like(q) if want_y else None
+    rc = _load().oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(wf), _ptr(dy), _ptr(dq),
+                                 _ptr(dk), _ptr(dv), _ptr(dw), _ptr(y), b, h, length, d, m,
+                                 MAP_ELU if w is None else MAP_FAVOR, int(threads))
+    if rc:
+        raise ValueError("oracle_backward failed (%d)" % rc)
+    out = (dq.reshape(shape), dk.reshape(shape), dv.reshape(shape), dw)
+    if want_y:
+        out = out + (y.reshape(shape),)
+    return out
+
+
+def rel_l2(x, ref):
+    """Relative L2 error ||x - ref||_2 / ||ref||_2 over the whole tensor, in fp64
+    (the discrepancy measure the paper uses for gradients, section 4)."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    return float(np.linalg.norm((x - ref).ravel()) / np.linalg.norm(ref.ravel()))
