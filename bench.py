@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""Benchmark: causal linear attention (SLiM chunked form), forward + backward.
+
+One step = slim_attn_fwd + slim_attn_bwd over one synthetic batch of the
+workload (default ``l32k``: B=2, H=16, L=32768, d=64, M=256, chunk 128, bf16
+I/O, FAVOR+ with block-orthogonal W).  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+``--impl reference`` times the fp64 CPU oracle on this machine's host cores
+on a bounded sample of the same workload (the reference arm).  Multi-GPU runs
+(torchrun) are independent replicas: heads are independent problems, so every
+rank runs its own copy of the workload and no data crosses ranks.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal linear-attn fwd+bwd tokens/s on 1 GB300; % of roofline; peak mem vs L"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"],
+                "bf16_tflops_sustained": pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def work_per_token_head(wl):
+    """Algorithmic FLOPs and bytes per (token, head): a multiply-add counts 2,
+    the causal C x C block counts its triangle, d' = d + 1 carries the
+    normaliser, recomputation is excluded."""
+    d, M, C = wl.d, wl.M, wl.chunk
+    dp = d + 1
+    s = 4 if wl.dtype == "fp32" else 2
+    feat = 4 * d * M if wl.feature == "favor" else 0
+    fwd = feat + M * (C + 1) + dp * (C + 1) + 4 * M * dp + d
+    bwd = dp * (C + 1) + 2 * M * (C + 1) + d * (C + 1) + 8 * M * dp + 2 * M * d + feat
+    return {"fwd_flops": fwd, "bwd_flops": bwd, "fwd_bytes": 4 * d * s, "bwd_bytes": 7 * d * s}
+
+
+KERNEL_WORK = {
+    # kernel name -> which algorithmic unit one launch of it processes in full
+    "gen_forward": "fwd", "tc_forward": "fwd",
+    "gen_backward": "bwd", "tc_backward": "bwd",
+}
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms (read only)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        return rank, world, local, dist
+    return rank, world, local, None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(x, dist):
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_sample(wl, row_frac=1.0, threads=0):
+    """Time the oracle (fwd + bwd) on min(cores, B*H) heads of the workload,
+    optionally on the first ``row_frac`` of the rows; returns (seconds,
+    heads, rows, cores).  Inputs follow the workload recipe on the CPU."""
+    import oracle
+    from sub_linear_memory_gb300 import inputs
+
+    cores = threads or len(os.sched_getaffinity(0))
+    heads = min(cores, wl.B * wl.H)
+    rows = max(1, int(wl.L * row_frac))
+    small = wl.with_(L=rows)
+    q, k, v, dy, w = inputs.make_inputs(small, heads=(1, heads))
+    qn, kn, vn, dyn = (t.to(torch.float64).numpy() for t in (q, k, v, dy))
+    wn = None if w is None else w.to(torch.float64).numpy()
+    t0 = time.perf_counter()
+    oracle.recurrence_forward(qn, kn, vn, wn, threads=cores)
+    oracle.recurrence_backward(qn, kn, vn, wn, dyn, threads=cores, want_dw=False)
+    return time.perf_counter() - t0, heads, rows, cores
+
+
+def tokens_per_s_from_sample(wl, secs, heads, rows, cores):
+    rounds = math.ceil(wl.B * wl.H / heads)
+    full_secs = secs * rounds * (wl.L / rows)
+    return wl.B * wl.L / full_secs
+
+
+def run_reference(args, wl):
+    rank, world, _, dist = dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    row_frac = args.ref_row_frac
+    for _ in range(args.warmup):
+        cpu_oracle_sample(wl, row_frac)
+    times = []
+    for _ in range(args.steps):
+        secs, heads, rows, cores = cpu_oracle_sample(wl, row_frac)
+        times.append(secs)
+    secs = sum(times) / len(times)
+    value = tokens_per_s_from_sample(wl, secs, heads, rows, cores)
+    sample = "%d of %d heads x first %d of %d rows per step, fp64 recurrence fwd+bwd, scaled to the full workload" % (
+        heads, wl.B * wl.H, rows, wl.L)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * wl.B * wl.L / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl, args.gpus),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(wl, n_gpus):
+    io = 4 * wl.B * wl.H * wl.L * wl.d * (4 if wl.dtype == "fp32" else 2)
+    return {"workload": wl.name, "B": wl.B, "H": wl.H, "L": wl.L, "d": wl.d, "M": wl.M,
+            "chunk": wl.chunk, "feature": "FAVOR+ (block-orthogonal W)" if wl.feature == "favor" and wl.w_kind == "orf"
+            else ("FAVOR+ (iid W)" if wl.feature == "favor" else "elu+1"),
+            "io_dtype": wl.dtype, "global_batch": wl.B * n_gpus, "seq_len": wl.L,
+            "parallelism": "replicas x%d" % n_gpus if n_gpus > 1 else "single GPU",
+            "l2": "inputs larger than L2 (%.0f MB of Q,K,V,dY vs 129 MB L2); no flush" % (io / 2**20)
+            if io > L2_BYTES else "L2 flushed between steps"}
+
+
+def memory_sweep(binding, inputs, exps=(16, 18, 20)):
+    """Peak device memory of one fwd + bwd on the 1M workload's head shape at
+    L = 2^e, from torch.cuda.max_memory_allocated (the workspace is a torch
+    allocation), split into the Theta(L) I/O tensors and the rest."""
+    base = inputs.WORKLOADS["l1m"]
+    out = {"L": [], "peak_bytes": [], "io_bytes": [], "workspace_bytes": [], "non_io_bytes": []}
+    for e in exps:
+        wl = base.with_(L=1 << e)
+        binding.release_workspace()
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        torch.cuda.reset_peak_memory_stats()
+        before = torch.cuda.memory_allocated()
+        q, k, v, dy, w = inputs.make_inputs(wl, device="cuda")
+        y = binding.slim_attn_fwd(q, k, v, w, wl.chunk)
+        dq, dk, dv, _ = binding.slim_attn_bwd(q, k, v, w, dy, wl.chunk)
+        torch.cuda.synchronize()
+        peak = torch.cuda.max_memory_allocated() - before
+        io = sum(t.numel() * t.element_size() for t in (q, k, v, dy, y, dq, dk, dv))
+        ws = max(binding.workspace_bytes(wl.B, wl.H, wl.L, wl.d, wl.M, wl.chunk, b) for b in (0, 1))
+        out["L"].append(wl.L)
+        out["peak_bytes"].append(int(peak))
+        out["io_bytes"].append(int(io))
+        out["workspace_bytes"].append(int(ws))
+        out["non_io_bytes"].append(int(peak - io))
+        del q, k, v, dy, w, y, dq, dk, dv
+    binding.release_workspace()
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_native(args, wl):
+    rank, world, local, dist = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    from sub_linear_memory_gb300 import binding, inputs
+
+    peaks = load_peaks()
+    q, k, v, dy, w = inputs.make_inputs(wl, device="cuda")
+    y = torch.empty_like(q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    out = (dq, dk, dv, None)
+
+    def step():
+        binding.slim_attn_fwd(q, k, v, w, wl.chunk, y=y)
+        binding.slim_attn_bwd(q, k, v, w, dy, wl.chunk, out=out)
+
+    for _ in range(args.warmup):
+        step()
+    binding.sync_status()
+    torch.cuda.synchronize()
+
+    # timed region: K steps, barrier + synchronize on both sides, CUDA events
+    stream = torch.cuda.current_stream()
+    binding.profile_reset()
+    binding.profile_enable(True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(dist)
+    binding.profile_enable(False)
+    kernels = binding.profile_read()
+    binding.sync_status()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), dist)
+    ms_per_step = ms / args.steps
+    tokens = wl.B * wl.L
+    value = world * tokens * args.steps / (ms / 1e3)
+
+    # forward alone (same inputs), for the forward tokens/s figure
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        binding.slim_attn_fwd(q, k, v, w, wl.chunk, y=y)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    fwd_ms = f0.elapsed_time(f1) / args.steps
+
+    # end to end through the public API with pinned host buffers
+    hq, hk, hv, hdy = (t.cpu().pin_memory() for t in (q, k, v, dy))
+    hy, hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(4))
+    dev_in = [torch.empty_like(q) for _ in range(4)]
+    e2e_steps = max(1, min(args.steps, 10))
+
+    def e2e_step():
+        for dst, src in zip(dev_in, (hq, hk, hv, hdy)):
+            dst.copy_(src, non_blocking=True)
+        yy = binding.slim_attn_fwd(dev_in[0], dev_in[1], dev_in[2], w, wl.chunk, y=y)
+        binding.slim_attn_bwd(dev_in[0], dev_in[1], dev_in[2], w, dev_in[3], wl.chunk, out=out)
+        for dst, src in zip((hy, hdq, hdk, hdv), (yy, dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist) / e2e_steps
+    nbytes = q.numel() * q.element_size()
+
+    # roofline of the dominant kernel (largest share of the timed region)
+    work = work_per_token_head(wl)
+    th = wl.B * wl.H * wl.L
+    dom = max(kernels.items(), key=lambda kv: kv[1][1]) if kernels else None
+    roofline = None
+    if dom is not None:
+        name, (launches, total_ms) = dom
+        unit = KERNEL_WORK.get(name)
+        avg_s = total_ms / launches / 1e3
+        if unit is not None:
+            flops = work[unit + "_flops"] * th
+            nb = work[unit + "_bytes"] * th
+            t_tensor = flops / (peaks["bf16_tflops_sustained"] * 1e12)
+            t_hbm = nb / (peaks["hbm_gbs"] * 1e9)
+            if t_tensor >= t_hbm:
+                roofline = {"bound": "tensor", "achieved": flops / avg_s / 1e12,
+                            "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
+            else:
+                roofline = {"bound": "hbm", "achieved": nb / avg_s / 1e9,
+                            "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+            roofline["frac"] = roofline["achieved"] / roofline["peak"]
+            roofline["traffic"] = None
+            roofline["kernel"] = name
+            roofline["avg_launch_ms"] = total_ms / launches
+            roofline["peak_source"] = peaks["source"] + " (sustained bf16 / copy bandwidth)"
+    # the whole step against its roofline (max of FLOPs at tensor peak, bytes at HBM)
+    step_flops = (work["fwd_flops"] + work["bwd_flops"]) * th
+    step_bytes = (work["fwd_bytes"] + work["bwd_bytes"]) * th
+    t_roof = max(step_flops / (peaks["bf16_tflops_sustained"] * 1e12), step_bytes / (peaks["hbm_gbs"] * 1e9))
+    fwd_roof = max(work["fwd_flops"] * th / (peaks["bf16_tflops_sustained"] * 1e12),
+                   work["fwd_bytes"] * th / (peaks["hbm_gbs"] * 1e9))
+
+    launches = sum(n for n, _ in kernels.values())
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Gaussian Q, K, V, dY; block-orthogonal random W)",
+        "config": config_of(wl, world),
+        "clocks": clocks.summary(),
+        "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": 4 * nbytes, "d2h_bytes_per_step": 4 * nbytes,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "roofline": roofline,
+        "step_roofline": {"roofline_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_per_step,
+                          "fwd_roofline_ms": fwd_roof * 1e3, "fwd_ms": fwd_ms,
+                          "fwd_frac": fwd_roof * 1e3 / fwd_ms,
+                          "fwd_tokens_per_s": world * tokens / (fwd_ms / 1e3)},
+        "kernels": {n: {"launches": c, "total_ms": t, "share": t / max(sum(x[1] for x in kernels.values()), 1e-12)}
+                    for n, (c, t) in sorted(kernels.items(), key=lambda kv: -kv[1][1])},
+    }
+    if args.memory and rank == 0:
+        del hq, hk, hv, hdy, hy, hdq, hdk, hdv, dev_in
+        line["memory"] = memory_sweep(binding, inputs)
+    if rank == 0 and world == 1 and args.cpu_baseline:
+        secs, heads, rows, cores = cpu_oracle_sample(wl, args.cpu_row_frac)
+        line["cpu_baseline"] = {
+            "value": tokens_per_s_from_sample(wl, secs, heads, rows, cores), "unit": "tokens/s",
+            "cores": cores, "kind": "oracle",
+            "sample": "%d of %d heads x first %d of %d rows, fp64 recurrence fwd+bwd (%.1f s), scaled to the full workload"
+                      % (heads, wl.B * wl.H, rows, wl.L, secs)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="l32k")
+    ap.add_argument("--no-memory", dest="memory", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-row-frac", type=float, default=0.5,
+                    help="fraction of the rows the CPU-baseline sample covers")
+    ap.add_argument("--ref-row-frac", type=float, default=0.125,
+                    help="fraction of the rows each reference-arm step covers")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "native":
+        ap.error("--warmup must be >= 3")
+    from sub_linear_memory_gb300 import inputs
+
+    wl = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_native(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,150 @@
+/*
+ * slim_attn.h -- C ABI of the GB300 (sm_103a) causal linear self-attention
+ * library, computed in SLiM's chunked, sub-linear-memory form.
+ *
+ * Operation (from "Sub-Linear Memory: How to Make Performers SLiM"):
+ *   section 2.1, eq. (2)-(4): for every (batch b, head h) independently,
+ *       Y_l = (PS(R)_l x g(Q_l)) / (PS(S)_l . g(Q_l)),
+ *       R_l = V_l (x) g(K_l)  (d x M),   S_l = g(K_l)  (M),
+ *   i.e. Y_l = sum_{j<=l} (g(Q_l).g(K_j)) V_j / sum_{j<=l} g(Q_l).g(K_j)
+ *   (causal, diagonal included, no epsilon in the division).
+ *   section 3.2, eq. (14)-(18): the sequence is cut into N = ceil(L/chunk)
+ *   slices of `chunk` rows (the last one may be shorter); the prefix-sum
+ *   state is carried only across slice boundaries.
+ *   section 3.3, eq. (19)-(21): the backward pass walks the slices in
+ *   reverse, recovering each slice's incoming state by subtracting the slice's
+ *   own contribution and carrying the reverse (gradient) state; the gradient
+ *   through a prefix sum is a prefix sum taken backwards.
+ *
+ * Feature map g (the page names a randomized positive map and an elementwise
+ * one without printing formulas):
+ *   w != NULL: FAVOR+ positive random features
+ *       g(x)_m = exp(w_m . x - |x|^2 / 2) / sqrt(M),  w_m = column m of W,
+ *       W fp32, row-major [d][M], shared by every batch and head;
+ *   w == NULL: g(x) = elu(x) + 1 elementwise; requires M == d.
+ *
+ * Layout: Q, K, V, Y, dY, dQ, dK, dV are dense row-major [B][H][L][d] device
+ * tensors (bf16 for slim_attn_fwd/bwd, fp32 for the _f32 variants); all
+ * arithmetic is fp32 (products on the tensor cores take bf16 operands on the
+ * bf16 path), outputs are rounded to the I/O type (round-to-nearest-even).
+ * Supported: d in {16, 32, 64, 128}; M a multiple of 16 in [16, 256];
+ * chunk a power of two in [16, 256]; any L >= 0 (a ragged last slice is
+ * fine); B, H >= 0.  Other shapes return SLIM_ERR_UNSUPPORTED.
+ *
+ * Ownership: the caller owns every buffer.  The library never allocates
+ * device memory on these entry points: the fp32 workspace (slice-boundary
+ * states, per-CTA scratch, dW partials) is a caller-provided device buffer
+ * registered with slim_attn_set_workspace() and sized by
+ * slim_attn_workspace_bytes(); its size does not grow with L beyond the
+ * point where every SM already has a segment of its own.
+ *
+ * Execution: every call only enqueues work on `stream` (a cudaStream_t; NULL
+ * is the legacy default stream) and returns; no host synchronisation.  Calls
+ * that share the registered workspace must not overlap on the GPU (use one
+ * stream, or one workspace per stream, re-registered before each call).
+ *
+ * Errors: no exception or abort crosses this ABI.  Argument problems are
+ * detected on the host and returned before anything is enqueued.  Launch
+ * failures return SLIM_ERR_CUDA.  Kernels that wait on on-chip barriers give
+ * up after a bounded number of polls and record SLIM_ERR_TIMEOUT in a device
+ * status word, which slim_attn_sync_status() reads back (and clears).
+ */
+#ifndef SLIM_ATTN_H
+#define SLIM_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Identical to cudaStream_t. */
+typedef struct CUstream_st *slim_stream_t;
+
+typedef enum {
+  SLIM_OK = 0,
+  SLIM_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, M != d for elu+1 */
+  SLIM_ERR_UNSUPPORTED = 2,  /* shape outside the supported set, misaligned */
+  SLIM_ERR_WORKSPACE = 3,    /* no workspace registered, or too small */
+  SLIM_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  SLIM_ERR_TIMEOUT = 5       /* a device-side bounded wait gave up */
+} slim_status;
+
+/* Options for slim_attn_set_option(). */
+typedef enum {
+  /* Segments per (b, h): 0 = automatic (fill the SMs), else the requested
+   * count, clamped to [1, ceil(L/chunk)]. */
+  SLIM_OPT_SEGMENTS = 1,
+  /* Kernel family: 0 = automatic, 1 = CUDA-core kernels only,
+   * 2 = tensor-core (tcgen05) kernels where the shape allows. */
+  SLIM_OPT_PATH = 2,
+  /* Per-kernel timing: 1 = record a CUDA event pair around every kernel
+   * launch, on the launch stream (read with slim_attn_profile_get), 0 = off. */
+  SLIM_OPT_PROFILE = 3
+} slim_option;
+
+/* Forward, bf16 I/O: y = Att^lin(q, k, v) (section 2.1, eq. (2)-(4); slices
+ * of section 3.2).  q, k, v: const bf16 [B][H][L][d]; w: fp32 [d][M] or NULL
+ * (elu+1); y: bf16 [B][H][L][d], written in full. */
+slim_status slim_attn_fwd(const void *q, const void *k, const void *v, const float *w,
+                          void *y, int B, int H, int L, int d, int M, int chunk,
+                          slim_stream_t stream);
+
+/* Backward, bf16 I/O: gradients of the scalar sum(dy * y) (section 3.3).
+ * dq, dk, dv: bf16 [B][H][L][d], written in full.  dw: fp32 [d][M],
+ * overwritten with the W-gradient summed over every b, h and row, or NULL
+ * when W is not learned (must be NULL for elu+1). */
+slim_status slim_attn_bwd(const void *q, const void *k, const void *v, const float *w,
+                          const void *dy, void *dq, void *dk, void *dv, float *dw, int B,
+                          int H, int L, int d, int M, int chunk, slim_stream_t stream);
+
+/* The same two operations with fp32 I/O. */
+slim_status slim_attn_fwd_f32(const float *q, const float *k, const float *v,
+                              const float *w, float *y, int B, int H, int L, int d, int M,
+                              int chunk, slim_stream_t stream);
+slim_status slim_attn_bwd_f32(const float *q, const float *k, const float *v,
+                              const float *w, const float *dy, float *dq, float *dk,
+                              float *dv, float *dw, int B, int H, int L, int d, int M,
+                              int chunk, slim_stream_t stream);
+
+/* Bytes of workspace slim_attn_fwd (is_bwd = 0) or slim_attn_bwd (is_bwd = 1)
+ * need for this shape on the current device (either I/O type).  0 for an
+ * unsupported shape or an empty problem. */
+size_t slim_attn_workspace_bytes(int B, int H, int L, int d, int M, int chunk, int is_bwd);
+
+/* Register the device workspace used by later calls (process-wide; ptr must
+ * be 256-byte aligned).  The library keeps the pointer only; the caller keeps
+ * ownership and must keep it alive until the calls that use it complete.
+ * ptr = NULL, bytes = 0 unregisters. */
+slim_status slim_attn_set_workspace(void *ptr, size_t bytes);
+
+/* Process-wide tuning / testing knobs (see slim_option). */
+slim_status slim_attn_set_option(int option, int value);
+
+/* Segments per (b, h) that a call with this shape uses on the current device. */
+int slim_attn_segments(int B, int H, int L, int d, int M, int chunk);
+
+/* Per-kernel profile (SLIM_OPT_PROFILE): waits for every recorded event,
+ * folds them into per-kernel totals and returns how many distinct kernels
+ * have been seen since the last reset. */
+int slim_attn_profile_count(void);
+
+/* Kernel i of the profile: its name (static storage), number of launches and
+ * summed device time in milliseconds. */
+slim_status slim_attn_profile_get(int i, const char **name, long long *launches,
+                                  double *total_ms);
+
+/* Drop every recorded profile entry. */
+void slim_attn_profile_reset(void);
+
+/* Wait for `stream`, then read and clear the device status word. */
+slim_status slim_attn_sync_status(slim_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *slim_status_string(slim_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SLIM_ATTN_H */

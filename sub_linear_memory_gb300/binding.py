@@ -1,0 +1,193 @@
+"""Thin ctypes binding over ``libslim_attn.so``: argument marshalling only.
+
+Every step of the attention runs in the library's CUDA kernels; this module
+checks tensor dtypes/devices/contiguity, owns the caller-side workspace (a
+torch allocation, so ``torch.cuda.max_memory_allocated`` sees it) and passes
+raw device pointers and the current torch stream.  There is no fallback: if
+the shared library is missing, importing this module raises.
+"""
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libslim_attn.so")
+
+if not os.path.exists(library_path):
+    raise ImportError(
+        "libslim_attn.so is not built (run sub_linear_memory_gb300.build.build() "
+        "or __graft_entry__.build()); there is no non-CUDA fallback")
+
+_lib = ctypes.CDLL(library_path)
+_vp, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+
+_lib.slim_attn_fwd.argtypes = [_vp] * 5 + [_i] * 6 + [_vp]
+_lib.slim_attn_fwd_f32.argtypes = _lib.slim_attn_fwd.argtypes
+_lib.slim_attn_bwd.argtypes = [_vp] * 9 + [_i] * 6 + [_vp]
+_lib.slim_attn_bwd_f32.argtypes = _lib.slim_attn_bwd.argtypes
+for _f in (_lib.slim_attn_fwd, _lib.slim_attn_fwd_f32, _lib.slim_attn_bwd, _lib.slim_attn_bwd_f32):
+    _f.restype = _i
+_lib.slim_attn_workspace_bytes.argtypes = [_i] * 7
+_lib.slim_attn_workspace_bytes.restype = _sz
+_lib.slim_attn_set_workspace.argtypes = [_vp, _sz]
+_lib.slim_attn_set_workspace.restype = _i
+_lib.slim_attn_set_option.argtypes = [_i, _i]
+_lib.slim_attn_set_option.restype = _i
+_lib.slim_attn_segments.argtypes = [_i] * 6
+_lib.slim_attn_segments.restype = _i
+_lib.slim_attn_sync_status.argtypes = [_vp]
+_lib.slim_attn_sync_status.restype = _i
+_lib.slim_attn_profile_count.argtypes = []
+_lib.slim_attn_profile_count.restype = _i
+_lib.slim_attn_profile_get.argtypes = [_i, ctypes.POINTER(ctypes.c_char_p),
+                                       ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_double)]
+_lib.slim_attn_profile_get.restype = _i
+_lib.slim_attn_profile_reset.argtypes = []
+_lib.slim_attn_profile_reset.restype = None
+_lib.slim_status_string.argtypes = [_i]
+_lib.slim_status_string.restype = ctypes.c_char_p
+
+OPT_SEGMENTS = 1
+OPT_PATH = 2
+OPT_PROFILE = 3
+EXPORTED = (
+    "slim_attn_fwd", "slim_attn_bwd", "slim_attn_fwd_f32", "slim_attn_bwd_f32",
+    "slim_attn_workspace_bytes", "slim_attn_set_workspace", "slim_attn_set_option",
+    "slim_attn_segments", "slim_attn_sync_status", "slim_status_string",
+    "slim_attn_profile_count", "slim_attn_profile_get", "slim_attn_profile_reset",
+)
+
+
+class SlimError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__("%s: %s" % (what, _lib.slim_status_string(code).decode()))
+        self.code = code
+
+
+def _check(code, what):
+    if code != 0:
+        raise SlimError(code, what)
+
+
+_ws_lock = threading.Lock()
+_ws = {}
+
+
+def workspace(nbytes, device):
+    """A cached torch uint8 device buffer of at least ``nbytes`` (256-B aligned)."""
+    dev = torch.device(device)
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    with _ws_lock:
+        buf = _ws.get(key)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=dev)
+            _ws[key] = buf
+        return buf
+
+
+def release_workspace():
+    with _ws_lock:
+        _ws.clear()
+    _check(_lib.slim_attn_set_workspace(None, 0), "slim_attn_set_workspace")
+
+
+def set_option(option, value):
+    _check(_lib.slim_attn_set_option(option, value), "slim_attn_set_option")
+
+
+def segments(B, H, L, d, M, chunk):
+    return _lib.slim_attn_segments(B, H, L, d, M, chunk)
+
+
+def workspace_bytes(B, H, L, d, M, chunk, is_bwd):
+    return _lib.slim_attn_workspace_bytes(B, H, L, d, M, chunk, int(is_bwd))
+
+
+def sync_status(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    _check(_lib.slim_attn_sync_status(_vp(s.cuda_stream)), "slim_attn_sync_status")
+
+
+def profile_enable(on=True):
+    set_option(OPT_PROFILE, 1 if on else 0)
+
+
+def profile_reset():
+    _lib.slim_attn_profile_reset()
+
+
+def profile_read():
+    """{kernel name: (launches, total ms)} since the last reset (waits for the GPU)."""
+    out = {}
+    for i in range(_lib.slim_attn_profile_count()):
+        name, n, ms = ctypes.c_char_p(), ctypes.c_longlong(), ctypes.c_double()
+        _check(_lib.slim_attn_profile_get(i, ctypes.byref(name), ctypes.byref(n), ctypes.byref(ms)),
+               "slim_attn_profile_get")
+        out[name.value.decode()] = (n.value, ms.value)
+    return out
+
+
+def _ptr(t):
+    return None if t is None else _vp(t.data_ptr())
+
+
+def _validate(q, k, v, w, extra=()):
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, L, d]")
+    for t in (q, k, v) + tuple(extra):
+        if t.shape != q.shape or t.dtype != q.dtype or t.device != q.device:
+            raise ValueError("q, k, v (and dy) must share shape, dtype and device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous [B, H, L, d]")
+    if q.dtype not in (torch.bfloat16, torch.float32) or q.device.type != "cuda":
+        raise ValueError("tensors must be CUDA bf16 or fp32")
+    if w is not None:
+        if w.dtype != torch.float32 or w.device != q.device or w.dim() != 2 or not w.is_contiguous():
+            raise ValueError("w must be a contiguous fp32 [d, M] tensor on q's device")
+        if w.shape[0] != q.shape[3]:
+            raise ValueError("w must be [d, M]")
+    b, h, length, d = q.shape
+    m = d if w is None else w.shape[1]
+    return b, h, length, d, m
+
+
+def _prepare(shape, is_bwd, device):
+    nbytes = workspace_bytes(*shape, is_bwd)
+    buf = workspace(nbytes, device)
+    _check(_lib.slim_attn_set_workspace(_vp(buf.data_ptr()), buf.numel()), "slim_attn_set_workspace")
+
+
+def slim_attn_fwd(q, k, v, w, chunk, y=None):
+    """Y = Att^lin(Q, K, V) through the library (bf16 or fp32 I/O by q's dtype)."""
+    b, h, length, d, m = _validate(q, k, v, w)
+    if y is None:
+        y = torch.empty_like(q)
+    _prepare((b, h, length, d, m, chunk), False, q.device)
+    fn = _lib.slim_attn_fwd if q.dtype == torch.bfloat16 else _lib.slim_attn_fwd_f32
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(y), b, h, length, d, m, chunk, _vp(stream)),
+           "slim_attn_fwd")
+    return y
+
+
+def slim_attn_bwd(q, k, v, w, dy, chunk, want_dw=False, out=None):
+    """Gradients of sum(dy * Y): returns (dq, dk, dv, dw or None)."""
+    b, h, length, d, m = _validate(q, k, v, w, (dy,))
+    if out is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        dw = torch.empty((d, m), dtype=torch.float32, device=q.device) if (want_dw and w is not None) else None
+    else:
+        dq, dk, dv, dw = out
+    _prepare((b, h, length, d, m, chunk), True, q.device)
+    fn = _lib.slim_attn_bwd if q.dtype == torch.bfloat16 else _lib.slim_attn_bwd_f32
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(dy), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dw),
+              b, h, length, d, m, chunk, _vp(stream)), "slim_attn_bwd")
+    return dq, dk, dv, dw
+
+
+def raw():
+    """The loaded ctypes library (for tests that call the C ABI directly)."""
+    return _lib

@@ -1,0 +1,54 @@
+// common.cuh -- shared host/device definitions of the slim_attn library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/slim_attn.h"
+
+namespace slim {
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// One (b, h) problem is cut into N = ceil(L / C) slices ("chunks") of C rows
+// ("Sub-Linear Memory: How to Make Performers SLiM", section 3.2, eq. (14)-(15));
+// consecutive chunks are grouped into P segments that run on different CTAs.
+// Segment s covers chunks [s * cps, min((s + 1) * cps, N)).
+struct Plan {
+  int B, H, L, d, M, C;
+  int BH;       // B * H
+  int nchunks;  // N
+  int P;        // segments per (b, h)
+  int cps;      // chunks per segment
+  int favor;    // 1: FAVOR+ random features, 0: elu + 1
+  int dp;       // d + 1: rows of the stacked state R' = [R ; S^T]
+  int path;     // 1 = CUDA-core kernels, 2 = tensor-core kernels
+  // workspace layout, in floats from the registered base
+  size_t states_off;   // fp64 [BH][P][dp][M]: inclusive segment-end states R'
+  size_t gstates_off;  // fp64 [BH][P][dp][M]: reverse states G (backward only)
+  size_t scratch_off;  // [BH * P][scratch_stride]
+  size_t dwpart_off;   // [BH * P][d][M] (backward with dW only)
+  size_t scratch_stride;
+  size_t total_floats;
+};
+
+// Kernel arguments shared by every kernel family.
+struct Args {
+  const void *q, *k, *v, *dy;
+  void *y, *dq, *dk, *dv;
+  const float *w;
+  float *dw;
+  float *ws;       // workspace base
+  int *status;     // device status word (SLIM_OK or the first error recorded)
+};
+
+__host__ __device__ inline size_t align_floats(size_t n) { return (n + 63) & ~size_t(63); }  // 256 B
+
+}  // namespace slim

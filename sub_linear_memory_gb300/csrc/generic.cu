@@ -1,0 +1,559 @@
+// generic.cu -- CUDA-core kernels (fp32 arithmetic) for every supported shape.
+//
+// This family is the fp32-I/O path and the fallback for shapes the
+// tensor-core kernels do not take.  One CTA owns one segment of consecutive
+// chunks of one (b, h) problem; chunk-sized intermediates (features, the
+// masked C x C score block, gradients) live in a per-CTA slice of the
+// workspace, which stays resident in L2.
+//
+// Notation ("Sub-Linear Memory: How to Make Performers SLiM", sections 2.1,
+// 3.2, 3.3): phi_q = g(Q_c), phi_k = g(K_c) for the chunk's rows;
+// V' = [V, 1]; the state R' = [R ; S^T] is (d+1) x M; A = tril(phi_q phi_k^T)
+// including the diagonal; num' = A V' + phi_q R'^T; Y = num / den.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace slim {
+namespace gen {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ float warp_sum(float s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return s;
+}
+
+struct Chunk {
+  int row0, rows;
+};
+
+__device__ __forceinline__ Chunk chunk_rows(const Plan &p, int c) {
+  Chunk ch;
+  ch.row0 = c * p.C;
+  ch.rows = min(p.C, p.L - ch.row0);
+  return ch;
+}
+
+// ---- feature map g (section 2.1) ----------------------------------------
+
+template <typename T>
+__device__ void row_sqnorms(const T *x, int rows, int d, float *sq) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int r = warp; r < rows; r += kWarps) {
+    float s = 0.f;
+    for (int i = lane; i < d; i += 32) {
+      const float t = to_f32(x[(size_t)r * d + i]);
+      s = fmaf(t, t, s);
+    }
+    s = warp_sum(s);
+    if (lane == 0) sq[r] = s;
+  }
+}
+
+// phi[r][m] = exp(x_r . w_m - |x_r|^2 / 2) / sqrt(M)   or   elu(x_r)_m + 1.
+template <typename T>
+__device__ void feature_rows(const Plan &p, const T *x, int rows, const float *w,
+                             const float *sq, float *phi) {
+  const int d = p.d, M = p.M;
+  const float inv_sqrt_m = 1.0f / sqrtf((float)M);
+  for (int idx = threadIdx.x; idx < rows * M; idx += kThreads) {
+    const int r = idx / M, m = idx - r * M;
+    const T *xr = x + (size_t)r * d;
+    float f;
+    if (p.favor) {
+      float dot = 0.f;
+      for (int i = 0; i < d; ++i) dot = fmaf(to_f32(xr[i]), w[(size_t)i * M + m], dot);
+      f = expf(dot - 0.5f * sq[r]) * inv_sqrt_m;
+    } else {
+      const float t = to_f32(xr[m]);
+      f = t > 0.f ? t + 1.f : expf(t);
+    }
+    phi[idx] = f;
+  }
+}
+
+// A[l][j] = phi_q[l] . phi_k[j] for j <= l, else 0 (row stride C).
+__device__ void causal_scores(const Plan &p, const float *phq, const float *phk, int rows,
+                              float *A) {
+  const int M = p.M, C = p.C;
+  for (int idx = threadIdx.x; idx < rows * rows; idx += kThreads) {
+    const int l = idx / rows, j = idx - l * rows;
+    float s = 0.f;
+    if (j <= l) {
+      const float *a = phq + (size_t)l * M, *b = phk + (size_t)j * M;
+      for (int m = 0; m < M; ++m) s = fmaf(a[m], b[m], s);
+    }
+    A[(size_t)l * C + j] = s;
+  }
+}
+
+// den[l] = sum_j A[l][j] + phi_q[l] . S, then Y[l][e] = num[l][e] / den[l]
+// with num = A V + phi_q R^T (R' holds the state before this chunk).
+template <typename T>
+__device__ void chunk_outputs(const Plan &p, const float *A, const float *phq, const double *R,
+                              const T *v, int rows, float *den, float *yc, T *y) {
+  const int d = p.d, M = p.M, C = p.C;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int l = warp; l < rows; l += kWarps) {
+    float s = 0.f;
+    for (int j = lane; j <= l; j += 32) s += A[(size_t)l * C + j];
+    for (int m = lane; m < M; m += 32) s = fmaf(phq[(size_t)l * M + m], (float)R[(size_t)d * M + m], s);
+    s = warp_sum(s);
+    if (lane == 0) den[l] = s;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < rows * d; idx += kThreads) {
+    const int l = idx / d, e = idx - l * d;
+    float num = 0.f;
+    for (int j = 0; j <= l; ++j) num = fmaf(A[(size_t)l * C + j], to_f32(v[(size_t)j * d + e]), num);
+    const float *a = phq + (size_t)l * M;
+    const double *r = R + (size_t)e * M;
+    for (int m = 0; m < M; ++m) num = fmaf(a[m], (float)r[m], num);
+    const float val = num / den[l];
+    if (yc) yc[idx] = val;
+    if (y) y[idx] = from_f32<T>(val);
+  }
+}
+
+// R'[e][m] += sign * sum_j V'[j][e] phi_k[j][m]   (V'[j][d] = 1).
+// The chunk's contribution is summed in fp32 in a fixed order, so the forward
+// sweep and the backward's reversal (eq. (19)) add and remove bit-identical
+// values; the master state is fp64, so removing them recovers the incoming
+// state to ~1e-16 of |R'| instead of accumulating fp32 cancellation error.
+template <typename T>
+__device__ void state_add(const Plan &p, double *R, const float *phk, const T *v, int rows,
+                          float sign) {
+  const int d = p.d, M = p.M, dp = p.dp;
+  for (int idx = threadIdx.x; idx < dp * M; idx += kThreads) {
+    const int e = idx / M, m = idx - e * M;
+    float s = 0.f;
+    if (e < d) {
+      for (int j = 0; j < rows; ++j) s = fmaf(to_f32(v[(size_t)j * d + e]), phk[(size_t)j * M + m], s);
+    } else {
+      for (int j = 0; j < rows; ++j) s += phk[(size_t)j * M + m];
+    }
+    R[idx] += (double)(sign * s);
+  }
+}
+
+// dN'[l] = [dY_l / den_l ; -(dY_l . Y_l) / den_l]
+template <typename T>
+__device__ void output_grads(const Plan &p, const T *dy, const float *yc, const float *den,
+                             int rows, float *dNp) {
+  const int d = p.d, dp = p.dp;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int l = warp; l < rows; l += kWarps) {
+    const float inv = 1.0f / den[l];
+    float s = 0.f;
+    for (int e = lane; e < d; e += 32) {
+      const float g = to_f32(dy[(size_t)l * d + e]);
+      dNp[(size_t)l * dp + e] = g * inv;
+      s = fmaf(g, yc[(size_t)l * d + e], s);
+    }
+    s = warp_sum(s);
+    if (lane == 0) dNp[(size_t)l * dp + d] = -s * inv;
+  }
+}
+
+// G[e][m] += sum_l dN'[l][e] phi_q[l][m]
+__device__ void reverse_state_add(const Plan &p, double *G, const float *dNp, const float *phq,
+                                  int rows) {
+  const int M = p.M, dp = p.dp;
+  for (int idx = threadIdx.x; idx < dp * M; idx += kThreads) {
+    const int e = idx / M, m = idx - e * M;
+    float s = 0.f;
+    for (int l = 0; l < rows; ++l) s = fmaf(dNp[(size_t)l * dp + e], phq[(size_t)l * M + m], s);
+    G[idx] += (double)s;
+  }
+}
+
+// Chain rule through g for `rows` rows of x: dphi is consumed (overwritten by
+// u = phi * dphi for FAVOR+); dx rows written as T; dW partial accumulated.
+template <typename T>
+__device__ void feature_backward(const Plan &p, const T *x, int rows, const float *w,
+                                 const float *phi, float *dphi, float *usum, T *dx,
+                                 float *dwp) {
+  const int d = p.d, M = p.M;
+  if (!p.favor) {
+    for (int idx = threadIdx.x; idx < rows * d; idx += kThreads) {
+      const float t = to_f32(x[idx]);
+      dx[idx] = from_f32<T>(dphi[idx] * (t > 0.f ? 1.f : phi[idx]));
+    }
+    return;
+  }
+  for (int idx = threadIdx.x; idx < rows * M; idx += kThreads) dphi[idx] *= phi[idx];
+  __syncthreads();
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int r = warp; r < rows; r += kWarps) {
+    float s = 0.f;
+    for (int m = lane; m < M; m += 32) s += dphi[(size_t)r * M + m];
+    s = warp_sum(s);
+    if (lane == 0) usum[r] = s;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < rows * d; idx += kThreads) {
+    const int r = idx / d, i = idx - r * d;
+    const float *u = dphi + (size_t)r * M, *wi = w + (size_t)i * M;
+    float s = 0.f;
+    for (int m = 0; m < M; ++m) s = fmaf(wi[m], u[m], s);
+    dx[idx] = from_f32<T>(s - to_f32(x[idx]) * usum[r]);
+  }
+  if (dwp) {
+    for (int idx = threadIdx.x; idx < d * M; idx += kThreads) {
+      const int i = idx / M, m = idx - i * M;
+      float s = 0.f;
+      for (int r = 0; r < rows; ++r) s = fmaf(to_f32(x[(size_t)r * d + i]), dphi[(size_t)r * M + m], s);
+      dwp[idx] += s;
+    }
+  }
+}
+
+// ---- kernels ------------------------------------------------------------
+
+struct FwdScratch {
+  double *R;
+  float *phq, *phk, *A, *yc, *dNp;
+};
+
+// Master states are fp64: a state of dp x M numbers takes 2 * dp * M floats.
+__device__ __forceinline__ FwdScratch fwd_scratch(const Plan &p, float *base) {
+  FwdScratch s;
+  s.R = reinterpret_cast<double *>(base);
+  s.phq = base + align_floats((size_t)2 * p.dp * p.M);
+  s.phk = s.phq + align_floats((size_t)p.C * p.M);
+  s.A = s.phk + align_floats((size_t)p.C * p.M);
+  s.yc = s.A + align_floats((size_t)p.C * p.C);
+  s.dNp = s.yc + align_floats((size_t)p.C * p.d);
+  return s;
+}
+
+__device__ __forceinline__ float *cta_scratch(const Plan &p, const Args &a) {
+  const size_t cta = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
+  return a.ws + p.scratch_off + cta * p.scratch_stride;
+}
+
+__device__ __forceinline__ double *state_ptr(const Plan &p, const Args &a, size_t off, int bh,
+                                             int s) {
+  return reinterpret_cast<double *>(a.ws + off) + ((size_t)bh * p.P + s) * p.dp * p.M;
+}
+
+template <typename T>
+__device__ __forceinline__ const T *head_ptr(const void *base, const Plan &p, int bh, int row0) {
+  return static_cast<const T *>(base) + ((size_t)bh * p.L + row0) * p.d;
+}
+template <typename T>
+__device__ __forceinline__ T *head_ptr_mut(void *base, const Plan &p, int bh, int row0) {
+  return static_cast<T *>(base) + ((size_t)bh * p.L + row0) * p.d;
+}
+
+// Segment totals dR'_s = sum over the segment's rows of V'_j (x) g(K_j)
+// (the rows the prefix sum of eq. (3) adds), written to states[bh][s].
+template <typename T>
+__global__ void __launch_bounds__(kThreads) segment_state_kernel(Plan p, Args a) {
+  __shared__ float sq[256];
+  const int s = blockIdx.x, bh = blockIdx.y;
+  double *out = state_ptr(p, a, p.states_off, bh, s);
+  FwdScratch sc = fwd_scratch(p, cta_scratch(p, a));
+  for (int i = threadIdx.x; i < p.dp * p.M; i += kThreads) out[i] = 0.0;
+  const int c0 = s * p.cps, c1 = min(c0 + p.cps, p.nchunks);
+  for (int c = c0; c < c1; ++c) {
+    const Chunk ch = chunk_rows(p, c);
+    const T *k = head_ptr<T>(a.k, p, bh, ch.row0), *v = head_ptr<T>(a.v, p, bh, ch.row0);
+    if (p.favor) row_sqnorms(k, ch.rows, p.d, sq);
+    __syncthreads();
+    feature_rows(p, k, ch.rows, a.w, sq, sc.phk);
+    __syncthreads();
+    state_add(p, out, sc.phk, v, ch.rows, 1.f);
+    __syncthreads();
+  }
+}
+
+// In-place inclusive scan of segment states over s (forward: R'; reverse: G).
+__global__ void scan_states_kernel(Plan p, double *st, int nseg, int reverse) {
+  const size_t per = (size_t)p.dp * p.M;
+  const size_t n = (size_t)p.BH * per;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t bh = i / per, e = i - bh * per;
+    double *b = st + bh * p.P * per + e;
+    if (!reverse) {
+      double acc = b[0];
+      for (int s = 1; s < nseg; ++s) { acc += b[s * per]; b[s * per] = acc; }
+    } else {
+      double acc = b[(size_t)(nseg - 1) * per];
+      for (int s = nseg - 2; s >= 0; --s) { acc += b[s * per]; b[s * per] = acc; }
+    }
+  }
+}
+
+// Forward over one segment, starting from the state left by the segments
+// before it (section 3.2: only the boundary state is carried).
+template <typename T>
+__global__ void __launch_bounds__(kThreads) forward_kernel(Plan p, Args a) {
+  __shared__ float sq[256], den[256];
+  const int s = blockIdx.x, bh = blockIdx.y;
+  FwdScratch sc = fwd_scratch(p, cta_scratch(p, a));
+  const double *R0 = s > 0 ? state_ptr(p, a, p.states_off, bh, s - 1) : nullptr;
+  for (int i = threadIdx.x; i < p.dp * p.M; i += kThreads) sc.R[i] = R0 ? R0[i] : 0.0;
+  __syncthreads();
+  const int c0 = s * p.cps, c1 = min(c0 + p.cps, p.nchunks);
+  for (int c = c0; c < c1; ++c) {
+    const Chunk ch = chunk_rows(p, c);
+    const T *q = head_ptr<T>(a.q, p, bh, ch.row0), *k = head_ptr<T>(a.k, p, bh, ch.row0);
+    const T *v = head_ptr<T>(a.v, p, bh, ch.row0);
+    T *y = head_ptr_mut<T>(a.y, p, bh, ch.row0);
+    if (p.favor) {
+      row_sqnorms(q, ch.rows, p.d, sq);
+      row_sqnorms(k, ch.rows, p.d, den);  // den[] doubles as |k|^2 here
+    }
+    __syncthreads();
+    feature_rows(p, q, ch.rows, a.w, sq, sc.phq);
+    feature_rows(p, k, ch.rows, a.w, den, sc.phk);
+    __syncthreads();
+    causal_scores(p, sc.phq, sc.phk, ch.rows, sc.A);
+    __syncthreads();
+    chunk_outputs(p, sc.A, sc.phq, sc.R, v, ch.rows, den, (float *)nullptr, y);
+    __syncthreads();
+    state_add(p, sc.R, sc.phk, v, ch.rows, 1.f);
+    __syncthreads();
+  }
+}
+
+// Backward pre-pass for segment s >= 1: replay the segment's forward from its
+// incoming state to get dN' and accumulate dG_s = sum_l dN'_l (x) g(Q_l)
+// (the rows the backward prefix sum of section 3.3 adds).
+template <typename T>
+__global__ void __launch_bounds__(kThreads) segment_dg_kernel(Plan p, Args a) {
+  __shared__ float sq[256], den[256];
+  const int s = blockIdx.x, bh = blockIdx.y;
+  if (s == 0) return;
+  double *out = state_ptr(p, a, p.gstates_off, bh, s);
+  FwdScratch sc = fwd_scratch(p, cta_scratch(p, a));
+  const double *R0 = state_ptr(p, a, p.states_off, bh, s - 1);
+  for (int i = threadIdx.x; i < p.dp * p.M; i += kThreads) {
+    sc.R[i] = R0[i];
+    out[i] = 0.0;
+  }
+  __syncthreads();
+  const int c0 = s * p.cps, c1 = min(c0 + p.cps, p.nchunks);
+  for (int c = c0; c < c1; ++c) {
+    const Chunk ch = chunk_rows(p, c);
+    const T *q = head_ptr<T>(a.q, p, bh, ch.row0), *k = head_ptr<T>(a.k, p, bh, ch.row0);
+    const T *v = head_ptr<T>(a.v, p, bh, ch.row0), *dy = head_ptr<T>(a.dy, p, bh, ch.row0);
+    if (p.favor) {
+      row_sqnorms(q, ch.rows, p.d, sq);
+      row_sqnorms(k, ch.rows, p.d, den);
+    }
+    __syncthreads();
+    feature_rows(p, q, ch.rows, a.w, sq, sc.phq);
+    feature_rows(p, k, ch.rows, a.w, den, sc.phk);
+    __syncthreads();
+    causal_scores(p, sc.phq, sc.phk, ch.rows, sc.A);
+    __syncthreads();
+    chunk_outputs(p, sc.A, sc.phq, sc.R, v, ch.rows, den, sc.yc, (T *)nullptr);
+    __syncthreads();
+    output_grads(p, dy, sc.yc, den, ch.rows, sc.dNp);
+    __syncthreads();
+    reverse_state_add(p, out, sc.dNp, sc.phq, ch.rows);
+    state_add(p, sc.R, sc.phk, v, ch.rows, 1.f);
+    __syncthreads();
+  }
+}
+
+struct BwdScratch {
+  double *R, *G;
+  float *phq, *phk, *dphq, *dphk, *A, *dA, *dNp, *yc;
+};
+
+__device__ __forceinline__ BwdScratch bwd_scratch(const Plan &p, float *base) {
+  BwdScratch s;
+  const size_t st = align_floats((size_t)2 * p.dp * p.M), cm = align_floats((size_t)p.C * p.M);
+  const size_t cc = align_floats((size_t)p.C * p.C);
+  s.R = reinterpret_cast<double *>(base);
+  s.G = reinterpret_cast<double *>(base + st);
+  s.phq = base + 2 * st;
+  s.phk = s.phq + cm;
+  s.dphq = s.phk + cm;
+  s.dphk = s.dphq + cm;
+  s.A = s.dphk + cm;
+  s.dA = s.A + cc;
+  s.dNp = s.dA + cc;
+  s.yc = s.dNp + align_floats((size_t)p.C * p.dp);
+  return s;
+}
+
+// The SLiM backward over one segment, chunks in reverse (section 3.3):
+//   R'(n-1) = R'(n) - sum_{j in chunk n} V'_j (x) g(K_j)        (eq. (19))
+//   recompute g, A, Y, dN' for the chunk from R'(n-1)
+//   dA     = tril(dN' V'^T)
+//   dg(Q)  = dA g(K) + dN' R'(n-1)
+//   dg(K)  = dA^T g(Q) + V' G(n)
+//   dV     = A^T dN + g(K) G(n)[0:d]^T
+//   G(n-1) = G(n) + dN'^T g(Q)                                   (eq. (20))
+// then the feature-map chain rule gives dQ, dK (and the dW partial).
+template <typename T>
+__global__ void __launch_bounds__(kThreads) backward_kernel(Plan p, Args a) {
+  __shared__ float sq[256], sk[256], den[256];
+  const int s = blockIdx.x, bh = blockIdx.y;
+  const int d = p.d, M = p.M, C = p.C, dp = p.dp;
+  BwdScratch sc = bwd_scratch(p, cta_scratch(p, a));
+  float *dwp = a.dw ? a.ws + p.dwpart_off + ((size_t)bh * p.P + s) * d * M : nullptr;
+  const double *Rend = state_ptr(p, a, p.states_off, bh, s);
+  const double *Gend = s + 1 < p.P ? state_ptr(p, a, p.gstates_off, bh, s + 1) : nullptr;
+  for (int i = threadIdx.x; i < dp * M; i += kThreads) {
+    sc.R[i] = Rend[i];
+    sc.G[i] = Gend ? Gend[i] : 0.0;
+  }
+  if (dwp)
+    for (int i = threadIdx.x; i < d * M; i += kThreads) dwp[i] = 0.f;
+  __syncthreads();
+  const int c0 = s * p.cps, c1 = min(c0 + p.cps, p.nchunks);
+  for (int c = c1 - 1; c >= c0; --c) {
+    const Chunk ch = chunk_rows(p, c);
+    const int rows = ch.rows;
+    const T *q = head_ptr<T>(a.q, p, bh, ch.row0), *k = head_ptr<T>(a.k, p, bh, ch.row0);
+    const T *v = head_ptr<T>(a.v, p, bh, ch.row0), *dy = head_ptr<T>(a.dy, p, bh, ch.row0);
+    T *dq = head_ptr_mut<T>(a.dq, p, bh, ch.row0), *dk = head_ptr_mut<T>(a.dk, p, bh, ch.row0);
+    T *dv = head_ptr_mut<T>(a.dv, p, bh, ch.row0);
+    if (p.favor) {
+      row_sqnorms(q, rows, d, sq);
+      row_sqnorms(k, rows, d, sk);
+    }
+    __syncthreads();
+    feature_rows(p, q, rows, a.w, sq, sc.phq);
+    feature_rows(p, k, rows, a.w, sk, sc.phk);
+    __syncthreads();
+    state_add(p, sc.R, sc.phk, v, rows, -1.f);  // eq. (19): state before this chunk
+    causal_scores(p, sc.phq, sc.phk, rows, sc.A);
+    __syncthreads();
+    chunk_outputs(p, sc.A, sc.phq, sc.R, v, rows, den, sc.yc, (T *)nullptr);
+    __syncthreads();
+    output_grads(p, dy, sc.yc, den, rows, sc.dNp);
+    __syncthreads();
+    // dA[l][j] = dN'_l . V'_j for j <= l
+    for (int idx = threadIdx.x; idx < rows * rows; idx += kThreads) {
+      const int l = idx / rows, j = idx - l * rows;
+      float t = 0.f;
+      if (j <= l) {
+        t = sc.dNp[(size_t)l * dp + d];
+        for (int e = 0; e < d; ++e) t = fmaf(sc.dNp[(size_t)l * dp + e], to_f32(v[(size_t)j * d + e]), t);
+      }
+      sc.dA[(size_t)l * C + j] = t;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < rows * M; idx += kThreads) {
+      const int r = idx / M, m = idx - r * M;
+      // dg(Q_r)_m = sum_{j<=r} dA[r][j] g(K_j)_m + sum_e dN'[r][e] R'[e][m]
+      float t = 0.f;
+      for (int j = 0; j <= r; ++j) t = fmaf(sc.dA[(size_t)r * C + j], sc.phk[(size_t)j * M + m], t);
+      for (int e = 0; e < dp; ++e) t = fmaf(sc.dNp[(size_t)r * dp + e], (float)sc.R[(size_t)e * M + m], t);
+      sc.dphq[idx] = t;
+      // dg(K_r)_m = sum_{l>=r} dA[l][r] g(Q_l)_m + sum_e V'[r][e] G[e][m]
+      float u = (float)sc.G[(size_t)d * M + m];
+      for (int l = r; l < rows; ++l) u = fmaf(sc.dA[(size_t)l * C + r], sc.phq[(size_t)l * M + m], u);
+      for (int e = 0; e < d; ++e) u = fmaf(to_f32(v[(size_t)r * d + e]), (float)sc.G[(size_t)e * M + m], u);
+      sc.dphk[idx] = u;
+    }
+    // dV[j][e] = sum_{l>=j} A[l][j] dN[l][e] + sum_m G[e][m] g(K_j)_m
+    for (int idx = threadIdx.x; idx < rows * d; idx += kThreads) {
+      const int j = idx / d, e = idx - j * d;
+      float t = 0.f;
+      for (int l = j; l < rows; ++l) t = fmaf(sc.A[(size_t)l * C + j], sc.dNp[(size_t)l * dp + e], t);
+      const double *g = sc.G + (size_t)e * M;
+      const float *f = sc.phk + (size_t)j * M;
+      for (int m = 0; m < M; ++m) t = fmaf((float)g[m], f[m], t);
+      dv[idx] = from_f32<T>(t);
+    }
+    __syncthreads();
+    reverse_state_add(p, sc.G, sc.dNp, sc.phq, rows);  // eq. (20)
+    feature_backward(p, q, rows, a.w, sc.phq, sc.dphq, sq, dq, dwp);
+    __syncthreads();
+    feature_backward(p, k, rows, a.w, sc.phk, sc.dphk, sk, dk, dwp);
+    __syncthreads();
+  }
+}
+
+// dw[i] = sum over CTAs of the per-CTA partials (fixed order: deterministic).
+__global__ void reduce_dw_kernel(Plan p, const float *parts, float *dw) {
+  const size_t n = (size_t)p.d * p.M;
+  const int nparts = p.BH * p.P;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    float s = 0.f;
+    for (int c = 0; c < nparts; ++c) s += parts[(size_t)c * n + i];
+    dw[i] = s;
+  }
+}
+
+}  // namespace gen
+
+size_t generic_scratch_floats(const Plan &p, bool bwd) {
+  const size_t st = align_floats((size_t)2 * p.dp * p.M), cm = align_floats((size_t)p.C * p.M);
+  const size_t cc = align_floats((size_t)p.C * p.C);
+  const size_t cd = align_floats((size_t)p.C * p.d), cdp = align_floats((size_t)p.C * p.dp);
+  if (!bwd) return st + 2 * cm + cc + cd + cdp;
+  return 2 * st + 4 * cm + 2 * cc + cdp + cd;
+}
+
+static int scan_blocks(const Plan &p) {
+  const size_t n = (size_t)p.BH * p.dp * p.M;
+  return (int)std::min<size_t>((n + 255) / 256, 4096);
+}
+
+template <typename T>
+cudaError_t generic_forward(const Plan &p, const Args &a, cudaStream_t st) {
+  if (p.P > 1) {
+    {
+      ProfScope ps("gen_segment_state", st);
+      gen::segment_state_kernel<T><<<dim3(p.P - 1, p.BH), gen::kThreads, 0, st>>>(p, a);
+    }
+    ProfScope ps("gen_scan_states", st);
+    gen::scan_states_kernel<<<scan_blocks(p), 256, 0, st>>>(
+        p, reinterpret_cast<double *>(a.ws + p.states_off), p.P - 1, 0);
+  }
+  ProfScope ps("gen_forward", st);
+  gen::forward_kernel<T><<<dim3(p.P, p.BH), gen::kThreads, 0, st>>>(p, a);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t generic_backward(const Plan &p, const Args &a, cudaStream_t st) {
+  {
+    ProfScope ps("gen_segment_state", st);
+    gen::segment_state_kernel<T><<<dim3(p.P, p.BH), gen::kThreads, 0, st>>>(p, a);
+  }
+  {
+    ProfScope ps("gen_scan_states", st);
+    gen::scan_states_kernel<<<scan_blocks(p), 256, 0, st>>>(
+        p, reinterpret_cast<double *>(a.ws + p.states_off), p.P, 0);
+  }
+  if (p.P > 1) {
+    {
+      ProfScope ps("gen_segment_dg", st);
+      gen::segment_dg_kernel<T><<<dim3(p.P, p.BH), gen::kThreads, 0, st>>>(p, a);
+    }
+    // G_end(s) = sum_{s' > s} dG_s': reverse inclusive scan over s = 1..P-1
+    ProfScope ps("gen_scan_states", st);
+    gen::scan_states_kernel<<<scan_blocks(p), 256, 0, st>>>(
+        p, reinterpret_cast<double *>(a.ws + p.gstates_off) + (size_t)p.dp * p.M, p.P - 1, 1);
+  }
+  {
+    ProfScope ps("gen_backward", st);
+    gen::backward_kernel<T><<<dim3(p.P, p.BH), gen::kThreads, 0, st>>>(p, a);
+  }
+  if (a.dw) {
+    const int n = p.d * p.M;
+    ProfScope ps("gen_reduce_dw", st);
+    gen::reduce_dw_kernel<<<(n + 255) / 256, 256, 0, st>>>(p, a.ws + p.dwpart_off, a.dw);
+  }
+  return cudaGetLastError();
+}
+
+template cudaError_t generic_forward<float>(const Plan &, const Args &, cudaStream_t);
+template cudaError_t generic_forward<__nv_bfloat16>(const Plan &, const Args &, cudaStream_t);
+template cudaError_t generic_backward<float>(const Plan &, const Args &, cudaStream_t);
+template cudaError_t generic_backward<__nv_bfloat16>(const Plan &, const Args &, cudaStream_t);
+
+}  // namespace slim

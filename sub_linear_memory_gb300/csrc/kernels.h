@@ -1,0 +1,28 @@
+// kernels.h -- host-side entry points of the kernel families.
+#pragma once
+
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace slim {
+
+// Brackets one kernel launch with a CUDA event pair on the launch stream when
+// profiling is enabled (SLIM_OPT_PROFILE); free otherwise.
+class ProfScope {
+ public:
+  ProfScope(const char *name, cudaStream_t stream);
+  ~ProfScope();
+
+ private:
+  const char *name_;
+  cudaStream_t stream_;
+  void *start_;
+};
+
+// CUDA-core family (generic.cu): any supported shape, fp32 arithmetic.
+size_t generic_scratch_floats(const Plan &p, bool bwd);
+template <typename T> cudaError_t generic_forward(const Plan &p, const Args &a, cudaStream_t st);
+template <typename T> cudaError_t generic_backward(const Plan &p, const Args &a, cudaStream_t st);
+
+}  // namespace slim

@@ -1,0 +1,294 @@
+// slim_attn_api.cu -- the C ABI declared in include/slim_attn.h: argument
+// validation, the segment plan, workspace layout and kernel dispatch.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace slim {
+
+// Device status word: SLIM_OK, or the first device-side error recorded.
+__device__ int g_device_status = 0;
+
+namespace {
+
+std::mutex g_mu;
+void *g_ws = nullptr;
+size_t g_ws_bytes = 0;
+int g_opt_segments = 0;
+int g_opt_path = 0;
+
+// ---- per-kernel profiling ----
+std::mutex g_prof_mu;
+std::atomic<int> g_prof_on{0};
+struct PendingEvent {
+  const char *name;
+  cudaEvent_t start, stop;
+};
+std::vector<PendingEvent> g_pending;
+std::vector<cudaEvent_t> g_event_pool;
+struct ProfTotal {
+  long long launches = 0;
+  double ms = 0.0;
+};
+std::vector<std::pair<std::string, ProfTotal>> g_prof_totals;
+
+cudaEvent_t take_event() {
+  cudaEvent_t e = nullptr;
+  if (!g_event_pool.empty()) {
+    e = g_event_pool.back();
+    g_event_pool.pop_back();
+  } else if (cudaEventCreate(&e) != cudaSuccess) {
+    e = nullptr;
+  }
+  return e;
+}
+
+void fold_pending() {
+  for (auto &pe : g_pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(pe.stop) == cudaSuccess &&
+        cudaEventElapsedTime(&ms, pe.start, pe.stop) == cudaSuccess) {
+      auto it = g_prof_totals.begin();
+      for (; it != g_prof_totals.end(); ++it)
+        if (it->first == pe.name) break;
+      if (it == g_prof_totals.end()) {
+        g_prof_totals.emplace_back(pe.name, ProfTotal{});
+        it = g_prof_totals.end() - 1;
+      }
+      it->second.launches += 1;
+      it->second.ms += ms;
+    }
+    g_event_pool.push_back(pe.start);
+    g_event_pool.push_back(pe.stop);
+  }
+  g_pending.clear();
+}
+
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+slim_status check_shape(int B, int H, int L, int d, int M, int chunk, bool favor) {
+  if (B < 0 || H < 0 || L < 0 || d <= 0 || M <= 0 || chunk <= 0) return SLIM_ERR_INVALID_ARG;
+  if (!favor && M != d) return SLIM_ERR_INVALID_ARG;
+  if (!(d == 16 || d == 32 || d == 64 || d == 128)) return SLIM_ERR_UNSUPPORTED;
+  if (M % 16 != 0 || M > 256) return SLIM_ERR_UNSUPPORTED;
+  if (!pow2(chunk) || chunk < 16 || chunk > 256) return SLIM_ERR_UNSUPPORTED;
+  if ((long long)B * H > (1LL << 30)) return SLIM_ERR_UNSUPPORTED;
+  return SLIM_OK;
+}
+
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return 148;
+  return sms;
+}
+
+// Segments per (b, h): enough CTAs to cover every SM once, never more
+// segments than chunks, and no empty segment.
+void choose_segments(Plan &p, int requested) {
+  const int sms = device_sms();
+  int P = requested > 0 ? requested : (sms + p.BH - 1) / std::max(p.BH, 1);
+  P = std::max(1, std::min(P, p.nchunks));
+  p.cps = (p.nchunks + P - 1) / P;
+  p.P = (p.nchunks + p.cps - 1) / p.cps;
+}
+
+Plan make_plan(int B, int H, int L, int d, int M, int chunk, bool favor, bool bwd, bool want_dw) {
+  Plan p{};
+  p.B = B; p.H = H; p.L = L; p.d = d; p.M = M; p.C = chunk;
+  p.BH = B * H;
+  p.nchunks = (L + chunk - 1) / chunk;
+  p.favor = favor ? 1 : 0;
+  p.dp = d + 1;
+  p.path = 1;
+  choose_segments(p, g_opt_segments);
+  const size_t state = 2 * (size_t)p.BH * p.P * p.dp * p.M;  // fp64 master states
+  size_t off = 0;
+  p.states_off = off; off += align_floats(state);
+  p.gstates_off = off; if (bwd) off += align_floats(state);
+  p.scratch_stride = align_floats(generic_scratch_floats(p, bwd));
+  p.scratch_off = off; off += p.scratch_stride * p.BH * p.P;
+  p.dwpart_off = off; if (bwd && want_dw) off += align_floats((size_t)p.BH * p.P * d * M);
+  p.total_floats = off;
+  return p;
+}
+
+template <typename T>
+slim_status run(bool bwd, const void *q, const void *k, const void *v, const float *w,
+                const void *dy, void *y, void *dq, void *dk, void *dv, float *dw, int B, int H,
+                int L, int d, int M, int chunk, cudaStream_t stream) {
+  const bool favor = w != nullptr;
+  slim_status st = check_shape(B, H, L, d, M, chunk, favor);
+  if (st != SLIM_OK) return st;
+  if (!favor && dw) return SLIM_ERR_INVALID_ARG;
+  if ((long long)B * H * L == 0) {
+    if (dw && cudaMemsetAsync(dw, 0, sizeof(float) * d * M, stream) != cudaSuccess) return SLIM_ERR_CUDA;
+    return SLIM_OK;
+  }
+  if (!q || !k || !v) return SLIM_ERR_INVALID_ARG;
+  if (!bwd && !y) return SLIM_ERR_INVALID_ARG;
+  if (bwd && (!dy || !dq || !dk || !dv)) return SLIM_ERR_INVALID_ARG;
+  Plan p = make_plan(B, H, L, d, M, chunk, favor, bwd, dw != nullptr);
+  Args a{};
+  a.q = q; a.k = k; a.v = v; a.dy = dy; a.y = y; a.dq = dq; a.dk = dk; a.dv = dv;
+  a.w = w; a.dw = dw;
+  if (cudaGetSymbolAddress((void **)&a.status, g_device_status) != cudaSuccess) return SLIM_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_ws || g_ws_bytes < p.total_floats * sizeof(float)) return SLIM_ERR_WORKSPACE;
+    a.ws = static_cast<float *>(g_ws);
+  }
+  cudaError_t err = bwd ? generic_backward<T>(p, a, stream) : generic_forward<T>(p, a, stream);
+  return err == cudaSuccess ? SLIM_OK : SLIM_ERR_CUDA;
+}
+
+}  // namespace
+
+ProfScope::ProfScope(const char *name, cudaStream_t stream)
+    : name_(name), stream_(stream), start_(nullptr) {
+  if (!g_prof_on.load()) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  cudaEvent_t e = take_event();
+  if (e && cudaEventRecord(e, stream) == cudaSuccess) start_ = e;
+}
+
+ProfScope::~ProfScope() {
+  if (!start_) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  cudaEvent_t e = take_event();
+  if (e && cudaEventRecord(e, stream_) == cudaSuccess) {
+    g_pending.push_back(PendingEvent{name_, static_cast<cudaEvent_t>(start_), e});
+  } else {
+    g_event_pool.push_back(static_cast<cudaEvent_t>(start_));
+    if (e) g_event_pool.push_back(e);
+  }
+}
+
+}  // namespace slim
+
+using slim::run;
+
+extern "C" {
+
+slim_status slim_attn_fwd(const void *q, const void *k, const void *v, const float *w, void *y,
+                          int B, int H, int L, int d, int M, int chunk, slim_stream_t stream) {
+  return run<__nv_bfloat16>(false, q, k, v, w, nullptr, y, nullptr, nullptr, nullptr, nullptr, B,
+                            H, L, d, M, chunk, (cudaStream_t)stream);
+}
+
+slim_status slim_attn_bwd(const void *q, const void *k, const void *v, const float *w,
+                          const void *dy, void *dq, void *dk, void *dv, float *dw, int B, int H,
+                          int L, int d, int M, int chunk, slim_stream_t stream) {
+  return run<__nv_bfloat16>(true, q, k, v, w, dy, nullptr, dq, dk, dv, dw, B, H, L, d, M, chunk,
+                            (cudaStream_t)stream);
+}
+
+slim_status slim_attn_fwd_f32(const float *q, const float *k, const float *v, const float *w,
+                              float *y, int B, int H, int L, int d, int M, int chunk,
+                              slim_stream_t stream) {
+  return run<float>(false, q, k, v, w, nullptr, y, nullptr, nullptr, nullptr, nullptr, B, H, L,
+                    d, M, chunk, (cudaStream_t)stream);
+}
+
+slim_status slim_attn_bwd_f32(const float *q, const float *k, const float *v, const float *w,
+                              const float *dy, float *dq, float *dk, float *dv, float *dw, int B,
+                              int H, int L, int d, int M, int chunk, slim_stream_t stream) {
+  return run<float>(true, q, k, v, w, dy, nullptr, dq, dk, dv, dw, B, H, L, d, M, chunk,
+                    (cudaStream_t)stream);
+}
+
+size_t slim_attn_workspace_bytes(int B, int H, int L, int d, int M, int chunk, int is_bwd) {
+  // elu+1 has M == d; the plan does not depend on the feature map otherwise
+  if (slim::check_shape(B, H, L, d, M, chunk, M != d || true) != SLIM_OK) return 0;
+  if ((long long)B * H * L == 0) return 0;
+  slim::Plan p = slim::make_plan(B, H, L, d, M, chunk, true, is_bwd != 0, is_bwd != 0);
+  return p.total_floats * sizeof(float);
+}
+
+slim_status slim_attn_set_workspace(void *ptr, size_t bytes) {
+  if ((ptr == nullptr) != (bytes == 0)) return SLIM_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(ptr) % 256 != 0) return SLIM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(slim::g_mu);
+  slim::g_ws = ptr;
+  slim::g_ws_bytes = bytes;
+  return SLIM_OK;
+}
+
+slim_status slim_attn_set_option(int option, int value) {
+  std::lock_guard<std::mutex> lk(slim::g_mu);
+  switch (option) {
+    case SLIM_OPT_SEGMENTS:
+      if (value < 0) return SLIM_ERR_INVALID_ARG;
+      slim::g_opt_segments = value;
+      return SLIM_OK;
+    case SLIM_OPT_PROFILE:
+      slim::g_prof_on.store(value ? 1 : 0);
+      return SLIM_OK;
+    case SLIM_OPT_PATH:
+      if (value < 0 || value > 2) return SLIM_ERR_INVALID_ARG;
+      slim::g_opt_path = value;
+      return SLIM_OK;
+    default:
+      return SLIM_ERR_INVALID_ARG;
+  }
+}
+
+int slim_attn_segments(int B, int H, int L, int d, int M, int chunk) {
+  if (slim::check_shape(B, H, L, d, M, chunk, true) != SLIM_OK) return 0;
+  if ((long long)B * H * L == 0) return 0;
+  return slim::make_plan(B, H, L, d, M, chunk, true, false, false).P;
+}
+
+int slim_attn_profile_count(void) {
+  std::lock_guard<std::mutex> lk(slim::g_prof_mu);
+  slim::fold_pending();
+  return (int)slim::g_prof_totals.size();
+}
+
+slim_status slim_attn_profile_get(int i, const char **name, long long *launches, double *total_ms) {
+  std::lock_guard<std::mutex> lk(slim::g_prof_mu);
+  slim::fold_pending();
+  if (i < 0 || i >= (int)slim::g_prof_totals.size()) return SLIM_ERR_INVALID_ARG;
+  const auto &e = slim::g_prof_totals[i];
+  if (name) *name = e.first.c_str();
+  if (launches) *launches = e.second.launches;
+  if (total_ms) *total_ms = e.second.ms;
+  return SLIM_OK;
+}
+
+void slim_attn_profile_reset(void) {
+  std::lock_guard<std::mutex> lk(slim::g_prof_mu);
+  slim::fold_pending();
+  slim::g_prof_totals.clear();
+}
+
+slim_status slim_attn_sync_status(slim_stream_t stream) {
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return SLIM_ERR_CUDA;
+  int host = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&host, slim::g_device_status, sizeof(int)) != cudaSuccess) return SLIM_ERR_CUDA;
+  if (host != 0 && cudaMemcpyToSymbol(slim::g_device_status, &zero, sizeof(int)) != cudaSuccess)
+    return SLIM_ERR_CUDA;
+  return (slim_status)host;
+}
+
+const char *slim_status_string(slim_status status) {
+  switch (status) {
+    case SLIM_OK: return "SLIM_OK";
+    case SLIM_ERR_INVALID_ARG: return "SLIM_ERR_INVALID_ARG: invalid argument";
+    case SLIM_ERR_UNSUPPORTED: return "SLIM_ERR_UNSUPPORTED: shape or alignment not supported";
+    case SLIM_ERR_WORKSPACE: return "SLIM_ERR_WORKSPACE: workspace missing or too small";
+    case SLIM_ERR_CUDA: return "SLIM_ERR_CUDA: CUDA runtime error";
+    case SLIM_ERR_TIMEOUT: return "SLIM_ERR_TIMEOUT: device-side wait gave up";
+    default: return "unknown slim_status";
+  }
+}
+
+}  // extern "C"

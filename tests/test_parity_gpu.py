@@ -1,0 +1,186 @@
+"""GPU parity: the CUDA library against the fp64 oracle, element by element.
+
+Bars (relative L2 over the whole tensor, computed in fp64, as the gradient
+discrepancy of "Sub-Linear Memory: How to Make Performers SLiM", section 4):
+  fp32 I/O: <= 1e-4 on Y, dQ, dK, dV and dW;
+  bf16 I/O with fp32 accumulation: <= 2e-2 on the same tensors.
+Small cases compare every head against the oracle; the full-size workloads
+run at full size on the GPU, exactly as the benchmark calls them, and compare
+sampled (b, h) heads (heads are independent, so a head is an exact unit).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sub_linear_memory_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from sub_linear_memory_gb300 import binding
+
+    binding.set_option(binding.OPT_SEGMENTS, 0)
+    binding.set_option(binding.OPT_PATH, 0)
+    yield binding
+    binding.set_option(binding.OPT_SEGMENTS, 0)
+    binding.set_option(binding.OPT_PATH, 0)
+
+
+def _np(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def _wnp(w):
+    return None if w is None else _np(w)
+
+
+def run_library(q, k, v, w, dy, chunk, want_dw=True):
+    from sub_linear_memory_gb300 import binding
+
+    y = binding.slim_attn_fwd(q, k, v, w, chunk)
+    dq, dk, dv, dw = binding.slim_attn_bwd(q, k, v, w, dy, chunk, want_dw=want_dw)
+    binding.sync_status()
+    return y, dq, dk, dv, dw
+
+
+def check(name, got, ref, tol, floor=0.0):
+    """Relative L2 error; ``floor`` bounds the denominator from below for
+    gradients that vanish identically (e.g. dQ, dK at L = 1, where Y_1 = V_1)."""
+    den = max(float(np.linalg.norm(np.ravel(ref))), floor)
+    err = float(np.linalg.norm(np.ravel(np.asarray(got, np.float64) - ref))) / den
+    print("%s rel L2 %.3e (tol %.0e)" % (name, err, tol))
+    assert np.isfinite(err) and err <= tol, "%s: rel L2 %.3e > %.1e" % (name, err, tol)
+    return err
+
+
+def small_case(B, H, L, d, M, C, dtype, feature, seed=0):
+    base = inputs.WORKLOADS["tiny" if dtype == torch.float32 else "l4k"]
+    wl = base.with_(B=B, H=H, L=L, d=d, M=M, chunk=C, index=100 + seed,
+                    dtype="fp32" if dtype == torch.float32 else "bf16", feature=feature,
+                    qk_scale=(1.0 if feature == "elu" else d ** -0.25),
+                    w_kind=("none" if feature == "elu" else base.w_kind))
+    q, k, v, dy, w = inputs.make_inputs(wl)
+    dev = "cuda"
+    return (q.to(dev), k.to(dev), v.to(dev), dy.to(dev), None if w is None else w.to(dev))
+
+
+def compare_all(q, k, v, w, dy, chunk, tol, want_dw=True):
+    y, dq, dk, dv, dw = run_library(q, k, v, w, dy, chunk, want_dw)
+    qn, kn, vn, dyn, wn = _np(q), _np(k), _np(v), _np(dy), _wnp(w)
+    y_ref = oracle.recurrence_forward(qn, kn, vn, wn)
+    dq_ref, dk_ref, dv_ref, dw_ref = oracle.recurrence_backward(qn, kn, vn, wn, dyn,
+                                                                want_dw=want_dw)
+    floor = 1e-2 * float(np.linalg.norm(dyn.ravel()))
+    errs = {"Y": check("Y", _np(y), y_ref, tol)}
+    errs["dQ"] = check("dQ", _np(dq), dq_ref, tol, floor)
+    errs["dK"] = check("dK", _np(dk), dk_ref, tol, floor)
+    errs["dV"] = check("dV", _np(dv), dv_ref, tol, floor)
+    if want_dw and w is not None:
+        errs["dW"] = check("dW", _np(dw), dw_ref, tol)
+    return errs
+
+
+SMALL = [
+    # (B, H, L, d, M, C, feature)    -- several chunks + a ragged tail
+    (1, 1, 256, 16, 32, 32, "favor"),      # the tiny workload, full size
+    (1, 1, 250, 16, 32, 32, "favor"),      # ragged last chunk
+    (1, 1, 20, 16, 32, 32, "favor"),       # L < chunk
+    (1, 3, 17, 16, 16, 16, "favor"),       # one full chunk + a 1-row tail
+    (2, 2, 1000, 64, 128, 64, "favor"),    # the 4k workload's head shape
+    (1, 2, 700, 64, 256, 128, "favor"),    # the 32k workload's head shape
+    (1, 1, 1500, 64, 64, 256, "favor"),    # the 1M workload's head shape
+    (1, 2, 300, 128, 128, 64, "elu"),      # elu+1, M = d = 128
+    (1, 1, 200, 32, 32, 16, "elu"),
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "x".join(map(str, c)))
+def test_small_against_oracle(case, dtype):
+    B, H, L, d, M, C, feature = case
+    q, k, v, dy, w = small_case(B, H, L, d, M, C, dtype, feature)
+    compare_all(q, k, v, w, dy, C, TOL[dtype])
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_single_row(dtype):
+    """L = 1: Y_1 = V_1, dV_1 = dY_1, and dQ = dK = dW = 0 (Y_1 does not depend
+    on Q or K), so only rounding noise may remain there."""
+    q, k, v, dy, w = small_case(2, 3, 1, 16, 32, 16, dtype, "favor", seed=6)
+    y, dq, dk, dv, dw = run_library(q, k, v, w, dy, 16)
+    tol = TOL[dtype]
+    check("Y", _np(y), _np(v), tol)
+    check("dV", _np(dv), _np(dy), tol)
+    scale = float(np.linalg.norm(_np(dy).ravel())) * (1.0 + float(np.linalg.norm(_np(w))))
+    for name, t in (("dQ", dq), ("dK", dk), ("dW", dw)):
+        assert float(np.linalg.norm(_np(t).ravel())) <= tol * scale, name
+
+
+@pytest.mark.parametrize("segments", [1, 2, 3, 7])
+def test_segment_count_does_not_change_results(segments, _lib):
+    q, k, v, dy, w = small_case(1, 2, 900, 32, 64, 32, torch.float32, "favor", seed=3)
+    _lib.set_option(_lib.OPT_SEGMENTS, segments)
+    try:
+        compare_all(q, k, v, w, dy, 32, 1e-4)
+    finally:
+        _lib.set_option(_lib.OPT_SEGMENTS, 0)
+
+
+@pytest.mark.parametrize("chunk", [16, 32, 64, 128, 256])
+def test_chunk_invariance(chunk):
+    """Any slice size C gives the same attention (the paper's Algorithm 1 is
+    exact for every C; section 3.4)."""
+    q, k, v, dy, w = small_case(1, 2, 600, 32, 64, chunk, torch.float32, "favor", seed=4)
+    compare_all(q, k, v, w, dy, chunk, 1e-4)
+
+
+def test_outputs_do_not_depend_on_stale_workspace(_lib):
+    q, k, v, dy, w = small_case(1, 1, 300, 16, 32, 32, torch.float32, "favor", seed=5)
+    first = run_library(q, k, v, w, dy, 32)
+    second = run_library(q, k, v, w, dy, 32)
+    for a, b in zip(first, second):
+        assert torch.equal(a, b)
+
+
+# ---- full-size workloads: sampled heads ----------------------------------
+
+FULL = {
+    # name: sampled (b, h) heads; None = every head
+    "l4k": None,
+    "l32k": [(0, 0), (1, 15)],
+    "l1m": [(0, 3)],
+    "elu16k": [(0, 0), (3, 11)],
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_workload(name):
+    wl = inputs.WORKLOADS[name]
+    q, k, v, dy, w = inputs.make_inputs(wl, device="cuda")
+    want_dw = FULL[name] is None and w is not None
+    y, dq, dk, dv, dw = run_library(q, k, v, w, dy, wl.chunk, want_dw=want_dw)
+    tol = TOL[wl.torch_dtype]
+    heads = FULL[name]
+    if heads is None:
+        sel = lambda t: _np(t)
+    else:
+        idx_b = torch.tensor([b for b, _ in heads])
+        idx_h = torch.tensor([h for _, h in heads])
+        sel = lambda t: _np(t[idx_b, idx_h].unsqueeze(0))
+    qn, kn, vn, dyn, wn = sel(q), sel(k), sel(v), sel(dy), _wnp(w)
+    y_ref = oracle.recurrence_forward(qn, kn, vn, wn)
+    check("Y", sel(y), y_ref, tol)
+    del y_ref
+    dq_ref, dk_ref, dv_ref, dw_ref = oracle.recurrence_backward(qn, kn, vn, wn, dyn, want_dw=want_dw)
+    check("dQ", sel(dq), dq_ref, tol)
+    check("dK", sel(dk), dk_ref, tol)
+    check("dV", sel(dv), dv_ref, tol)
+    if want_dw:
+        check("dW", _np(dw), dw_ref, tol)
