@@ -107,6 +107,27 @@ slim_status slim_attn_bwd_f32(const float *q, const float *k, const float *v,
                               float *dv, float *dw, int B, int H, int L, int d, int M,
                               int chunk, slim_stream_t stream);
 
+/* Size of the fixed device scratch array behind slim_attn_fwd_noalloc. */
+#define SLIM_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* Forward, bf16 I/O, for callers that cannot allocate device memory (a
+ * memory-capped pool, an allocation-free real-time loop, code that must not
+ * risk the device synchronisation an allocation can cause).  Same arguments
+ * and result as slim_attn_fwd, but no workspace is registered or used: the
+ * scratch is a 64 MiB array compiled into the library, resident on every GPU
+ * that loads the library until the process exits.  The paper has no
+ * counterpart; this is a deployment convenience.
+ *   - Problems whose slim_attn_workspace_bytes(..., 0) exceeds
+ *     SLIM_NOALLOC_SCRATCH_BYTES return SLIM_ERR_WORKSPACE before any launch.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make it before any
+ *     stream capture.  It calls no allocator itself.
+ *   - Every call shares the one array: calls that overlap on the GPU race.
+ *     No value is carried from one call to the next. */
+slim_status slim_attn_fwd_noalloc(const void *q, const void *k, const void *v, const float *w,
+                                  void *y, int B, int H, int L, int d, int M, int chunk,
+                                  slim_stream_t stream);
+
 /* Bytes of workspace slim_attn_fwd (is_bwd = 0) or slim_attn_bwd (is_bwd = 1)
  * need for this shape on the current device (either I/O type).  0 for an
  * unsupported shape or an empty problem. */

@@ -20,6 +20,12 @@ class ProfScope {
   void *start_;
 };
 
+// Shape validation and the segment plan of slim_attn_api.cu.
+slim_status shape_status(int B, int H, int L, int d, int M, int chunk, bool favor);
+Plan plan_for(int B, int H, int L, int d, int M, int chunk, bool favor, bool bwd, bool want_dw);
+// Device address of the status word (nullptr on failure).
+int *device_status_ptr();
+
 // CUDA-core family (generic.cu): any supported shape, fp32 arithmetic.
 size_t generic_scratch_floats(const Plan &p, bool bwd);
 template <typename T> cudaError_t generic_forward(const Plan &p, const Args &a, cudaStream_t st);

@@ -152,6 +152,21 @@ slim_status run(bool bwd, const void *q, const void *k, const void *v, const flo
 
 }  // namespace
 
+// Accessors for entry points that live in other translation units.
+slim_status shape_status(int B, int H, int L, int d, int M, int chunk, bool favor) {
+  return check_shape(B, H, L, d, M, chunk, favor);
+}
+
+Plan plan_for(int B, int H, int L, int d, int M, int chunk, bool favor, bool bwd, bool want_dw) {
+  return make_plan(B, H, L, d, M, chunk, favor, bwd, want_dw);
+}
+
+int *device_status_ptr() {
+  int *ptr = nullptr;
+  if (cudaGetSymbolAddress((void **)&ptr, g_device_status) != cudaSuccess) return nullptr;
+  return ptr;
+}
+
 ProfScope::ProfScope(const char *name, cudaStream_t stream)
     : name_(name), stream_(stream), start_(nullptr) {
   if (!g_prof_on.load()) return;
