@@ -26,12 +26,14 @@ struct Plan {
   int BH;       // B * H
   int nchunks;  // N
   int P;        // segments per (b, h)
-  int cps;      // chunks per segment
+  int cps;      // chunks (CUDA-core path) or 128-row tiles (tensor path) per segment
   int favor;    // 1: FAVOR+ random features, 0: elu + 1
   int dp;       // d + 1: rows of the stacked state R' = [R ; S^T]
   int path;     // 1 = CUDA-core kernels, 2 = tensor-core kernels
+  int tc_tiles; // 128-row tiles per (b, h) (tensor-core path)
   // workspace layout, in floats from the registered base
-  size_t states_off;   // fp64 [BH][P][dp][M]: inclusive segment-end states R'
+  size_t states_off;   // inclusive segment-end states R': CUDA-core path fp64
+                       // [BH][P][dp][M]; tensor path fp32 [BH][P][M][dp]
   size_t gstates_off;  // fp64 [BH][P][dp][M]: reverse states G (backward only)
   size_t scratch_off;  // [BH * P][scratch_stride]
   size_t dwpart_off;   // [BH * P][d][M] (backward with dW only)

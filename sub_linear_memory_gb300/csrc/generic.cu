@@ -271,18 +271,19 @@ __global__ void __launch_bounds__(kThreads) segment_state_kernel(Plan p, Args a)
 }
 
 // In-place inclusive scan of segment states over s (forward: R'; reverse: G).
-__global__ void scan_states_kernel(Plan p, double *st, int nseg, int reverse) {
+template <typename S>
+__global__ void scan_states_kernel(Plan p, S *st, int nseg, int reverse) {
   const size_t per = (size_t)p.dp * p.M;
   const size_t n = (size_t)p.BH * per;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x) {
     const size_t bh = i / per, e = i - bh * per;
-    double *b = st + bh * p.P * per + e;
+    S *b = st + bh * p.P * per + e;
     if (!reverse) {
-      double acc = b[0];
+      S acc = b[0];
       for (int s = 1; s < nseg; ++s) { acc += b[s * per]; b[s * per] = acc; }
     } else {
-      double acc = b[(size_t)(nseg - 1) * per];
+      S acc = b[(size_t)(nseg - 1) * per];
       for (int s = nseg - 2; s >= 0; --s) { acc += b[s * per]; b[s * per] = acc; }
     }
   }
@@ -548,6 +549,11 @@ cudaError_t generic_backward(const Plan &p, const Args &a, cudaStream_t st) {
     ProfScope ps("gen_reduce_dw", st);
     gen::reduce_dw_kernel<<<(n + 255) / 256, 256, 0, st>>>(p, a.ws + p.dwpart_off, a.dw);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t scan_states_f32(const Plan &p, float *states, int nseg, cudaStream_t st) {
+  gen::scan_states_kernel<float><<<scan_blocks(p), 256, 0, st>>>(p, states, nseg, 0);
   return cudaGetLastError();
 }
 

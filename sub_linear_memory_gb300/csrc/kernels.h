@@ -30,5 +30,12 @@ int *device_status_ptr();
 size_t generic_scratch_floats(const Plan &p, bool bwd);
 template <typename T> cudaError_t generic_forward(const Plan &p, const Args &a, cudaStream_t st);
 template <typename T> cudaError_t generic_backward(const Plan &p, const Args &a, cudaStream_t st);
+// In-place inclusive scan over the first nseg segment states (fp32 layout).
+cudaError_t scan_states_f32(const Plan &p, float *states, int nseg, cudaStream_t st);
+
+// Tensor-core family (tc_forward.cu): bf16 I/O, 128-row tiles.
+bool tc_forward_supported(int d, int M, int chunk, bool favor);
+size_t tc_smem_bytes(int d, int M, bool favor);
+cudaError_t tc_forward(const Plan &p, const Args &a, cudaStream_t st);
 
 }  // namespace slim

@@ -71,6 +71,8 @@ void fold_pending() {
   g_pending.clear();
 }
 
+bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
 bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 slim_status check_shape(int B, int H, int L, int d, int M, int chunk, bool favor) {
@@ -92,29 +94,34 @@ int device_sms() {
 }
 
 // Segments per (b, h): enough CTAs to cover every SM once, never more
-// segments than chunks, and no empty segment.
-void choose_segments(Plan &p, int requested) {
+// segments than work units (chunks, or 128-row tiles on the tensor path), and
+// no empty segment.
+void choose_segments(Plan &p, int requested, int units) {
   const int sms = device_sms();
   int P = requested > 0 ? requested : (sms + p.BH - 1) / std::max(p.BH, 1);
-  P = std::max(1, std::min(P, p.nchunks));
-  p.cps = (p.nchunks + P - 1) / P;
-  p.P = (p.nchunks + p.cps - 1) / p.cps;
+  P = std::max(1, std::min(P, units));
+  p.cps = (units + P - 1) / P;
+  p.P = (units + p.cps - 1) / p.cps;
 }
 
-Plan make_plan(int B, int H, int L, int d, int M, int chunk, bool favor, bool bwd, bool want_dw) {
+// path: 1 = CUDA-core kernels, 2 = tensor-core kernels.
+Plan make_plan(int B, int H, int L, int d, int M, int chunk, bool favor, bool bwd, bool want_dw,
+               int path = 1) {
   Plan p{};
   p.B = B; p.H = H; p.L = L; p.d = d; p.M = M; p.C = chunk;
   p.BH = B * H;
   p.nchunks = (L + chunk - 1) / chunk;
+  p.tc_tiles = (L + 127) / 128;
   p.favor = favor ? 1 : 0;
   p.dp = d + 1;
-  p.path = 1;
-  choose_segments(p, g_opt_segments);
-  const size_t state = 2 * (size_t)p.BH * p.P * p.dp * p.M;  // fp64 master states
+  p.path = path;
+  choose_segments(p, g_opt_segments, path == 2 ? p.tc_tiles : p.nchunks);
+  // master states: fp64 on the CUDA-core path, fp32 on the tensor path
+  const size_t state = (path == 2 ? 1 : 2) * (size_t)p.BH * p.P * p.dp * p.M;
   size_t off = 0;
   p.states_off = off; off += align_floats(state);
   p.gstates_off = off; if (bwd) off += align_floats(state);
-  p.scratch_stride = align_floats(generic_scratch_floats(p, bwd));
+  p.scratch_stride = path == 2 ? 0 : align_floats(generic_scratch_floats(p, bwd));
   p.scratch_off = off; off += p.scratch_stride * p.BH * p.P;
   p.dwpart_off = off; if (bwd && want_dw) off += align_floats((size_t)p.BH * p.P * d * M);
   p.total_floats = off;
@@ -136,7 +143,10 @@ slim_status run(bool bwd, const void *q, const void *k, const void *v, const flo
   if (!q || !k || !v) return SLIM_ERR_INVALID_ARG;
   if (!bwd && !y) return SLIM_ERR_INVALID_ARG;
   if (bwd && (!dy || !dq || !dk || !dv)) return SLIM_ERR_INVALID_ARG;
-  Plan p = make_plan(B, H, L, d, M, chunk, favor, bwd, dw != nullptr);
+  const bool tc = !bwd && sizeof(T) == 2 && g_opt_path != 1 &&
+                  tc_forward_supported(d, M, chunk, favor) && aligned16(q) && aligned16(k) &&
+                  aligned16(v) && aligned16(y);
+  Plan p = make_plan(B, H, L, d, M, chunk, favor, bwd, dw != nullptr, tc ? 2 : 1);
   Args a{};
   a.q = q; a.k = k; a.v = v; a.dy = dy; a.y = y; a.dq = dq; a.dk = dk; a.dv = dv;
   a.w = w; a.dw = dw;
@@ -146,7 +156,9 @@ slim_status run(bool bwd, const void *q, const void *k, const void *v, const flo
     if (!g_ws || g_ws_bytes < p.total_floats * sizeof(float)) return SLIM_ERR_WORKSPACE;
     a.ws = static_cast<float *>(g_ws);
   }
-  cudaError_t err = bwd ? generic_backward<T>(p, a, stream) : generic_forward<T>(p, a, stream);
+  cudaError_t err = bwd  ? generic_backward<T>(p, a, stream)
+                    : tc ? tc_forward(p, a, stream)
+                         : generic_forward<T>(p, a, stream);
   return err == cudaSuccess ? SLIM_OK : SLIM_ERR_CUDA;
 }
 
@@ -224,8 +236,12 @@ size_t slim_attn_workspace_bytes(int B, int H, int L, int d, int M, int chunk, i
   // elu+1 has M == d; the plan does not depend on the feature map otherwise
   if (slim::check_shape(B, H, L, d, M, chunk, M != d || true) != SLIM_OK) return 0;
   if ((long long)B * H * L == 0) return 0;
-  slim::Plan p = slim::make_plan(B, H, L, d, M, chunk, true, is_bwd != 0, is_bwd != 0);
-  return p.total_floats * sizeof(float);
+  size_t floats = 0;
+  for (int path = 1; path <= 2; ++path) {
+    slim::Plan p = slim::make_plan(B, H, L, d, M, chunk, true, is_bwd != 0, is_bwd != 0, path);
+    floats = std::max(floats, p.total_floats);
+  }
+  return floats * sizeof(float);
 }
 
 slim_status slim_attn_set_workspace(void *ptr, size_t bytes) {

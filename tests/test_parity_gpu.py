@@ -109,6 +109,61 @@ def test_small_against_oracle(case, dtype):
     compare_all(q, k, v, w, dy, C, TOL[dtype])
 
 
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "x".join(map(str, c)))
+def test_small_bf16_cuda_core_family(case, _lib):
+    """The CUDA-core kernels on bf16 I/O (the tensor-core kernels take the
+    supported shapes by default)."""
+    B, H, L, d, M, C, feature = case
+    q, k, v, dy, w = small_case(B, H, L, d, M, C, torch.bfloat16, feature)
+    _lib.set_option(_lib.OPT_PATH, 1)
+    try:
+        compare_all(q, k, v, w, dy, C, TOL[torch.bfloat16])
+    finally:
+        _lib.set_option(_lib.OPT_PATH, 0)
+
+
+TC_SHAPES = [
+    # (B, H, L, d, M, C, feature): shapes the tensor-core forward takes
+    (1, 2, 700, 64, 256, 128, "favor"),
+    (2, 1, 1000, 64, 128, 64, "favor"),
+    (1, 1, 1500, 64, 64, 256, "favor"),
+    (1, 2, 300, 128, 128, 64, "elu"),
+    (1, 1, 333, 64, 64, 128, "elu"),
+    (1, 3, 128, 64, 256, 128, "favor"),   # exactly one tile
+    (1, 1, 1, 64, 128, 64, "favor"),      # one row
+]
+
+
+@pytest.mark.parametrize("case", TC_SHAPES, ids=lambda c: "x".join(map(str, c)))
+def test_tensor_core_forward_is_used_and_matches(case, _lib):
+    B, H, L, d, M, C, feature = case
+    q, k, v, dy, w = small_case(B, H, L, d, M, C, torch.bfloat16, feature, seed=7)
+    _lib.profile_reset()
+    _lib.profile_enable(True)
+    try:
+        y = _lib.slim_attn_fwd(q, k, v, w, C)
+        _lib.sync_status()
+        names = set(_lib.profile_read())
+    finally:
+        _lib.profile_enable(False)
+    assert "tc_forward" in names, names
+    y_ref = oracle.recurrence_forward(_np(q), _np(k), _np(v), _wnp(w))
+    check("Y", _np(y), y_ref, TOL[torch.bfloat16])
+
+
+@pytest.mark.parametrize("segments", [1, 2, 3, 5])
+def test_tensor_core_segments(segments, _lib):
+    q, k, v, dy, w = small_case(1, 2, 1100, 64, 256, 128, torch.bfloat16, "favor", seed=8)
+    _lib.set_option(_lib.OPT_SEGMENTS, segments)
+    try:
+        y = _lib.slim_attn_fwd(q, k, v, w, 128)
+        _lib.sync_status()
+    finally:
+        _lib.set_option(_lib.OPT_SEGMENTS, 0)
+    y_ref = oracle.recurrence_forward(_np(q), _np(k), _np(v), _wnp(w))
+    check("Y", _np(y), y_ref, TOL[torch.bfloat16])
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
 def test_single_row(dtype):
     """L = 1: Y_1 = V_1, dV_1 = dY_1, and dQ = dK = dW = 0 (Y_1 does not depend
