@@ -34,7 +34,9 @@ struct Plan {
   // workspace layout, in floats from the registered base
   size_t states_off;   // inclusive segment-end states R': CUDA-core path fp64
                        // [BH][P][dp][M]; tensor path fp32 [BH][P][M][dp]
-  size_t gstates_off;  // fp64 [BH][P][dp][M]: reverse states G (backward only)
+  size_t states_lo_off;  // tensor path: low parts of the double-float states
+  size_t gstates_off;  // reverse states G (backward): fp64 [BH][P][dp][M] on the
+                       // CUDA-core path, fp32 [BH][P][M][dp] on the tensor path
   size_t scratch_off;  // [BH * P][scratch_stride]
   size_t dwpart_off;   // [BH * P][d][M] (backward with dW only)
   size_t scratch_stride;

@@ -476,6 +476,25 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(Plan p, Args a) {
   }
 }
 
+// Inclusive scan over segments of double-float states: acc = sum in fp64,
+// written back as (hi, lo) = (fl(acc), fl(acc - hi)).
+__global__ void scan_states_df_kernel(Plan p, float *hi, float *lo, int nseg) {
+  const size_t per = (size_t)p.dp * p.M;
+  const size_t n = (size_t)p.BH * per;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t bh = i / per, e = i - bh * per;
+    float *h = hi + bh * p.P * per + e, *l = lo + bh * p.P * per + e;
+    double acc = 0.0;
+    for (int s = 0; s < nseg; ++s) {
+      acc += (double)h[s * per] + (double)l[s * per];
+      const float fh = (float)acc;
+      h[s * per] = fh;
+      l[s * per] = (float)(acc - (double)fh);
+    }
+  }
+}
+
 // dw[i] = sum over CTAs of the per-CTA partials (fixed order: deterministic).
 __global__ void reduce_dw_kernel(Plan p, const float *parts, float *dw) {
   const size_t n = (size_t)p.d * p.M;
@@ -554,6 +573,16 @@ cudaError_t generic_backward(const Plan &p, const Args &a, cudaStream_t st) {
 
 cudaError_t scan_states_f32(const Plan &p, float *states, int nseg, cudaStream_t st) {
   gen::scan_states_kernel<float><<<scan_blocks(p), 256, 0, st>>>(p, states, nseg, 0);
+  return cudaGetLastError();
+}
+
+cudaError_t scan_states_df(const Plan &p, float *hi, float *lo, int nseg, cudaStream_t st) {
+  gen::scan_states_df_kernel<<<scan_blocks(p), 256, 0, st>>>(p, hi, lo, nseg);
+  return cudaGetLastError();
+}
+
+cudaError_t scan_states_f32_rev(const Plan &p, float *states, int nseg, cudaStream_t st) {
+  gen::scan_states_kernel<float><<<scan_blocks(p), 256, 0, st>>>(p, states, nseg, 1);
   return cudaGetLastError();
 }
 

@@ -30,12 +30,22 @@ int *device_status_ptr();
 size_t generic_scratch_floats(const Plan &p, bool bwd);
 template <typename T> cudaError_t generic_forward(const Plan &p, const Args &a, cudaStream_t st);
 template <typename T> cudaError_t generic_backward(const Plan &p, const Args &a, cudaStream_t st);
-// In-place inclusive scan over the first nseg segment states (fp32 layout).
+// In-place inclusive scan over the first nseg segment states (fp32 layout),
+// forward (state s += state s-1) or reverse (state s += state s+1).
 cudaError_t scan_states_f32(const Plan &p, float *states, int nseg, cudaStream_t st);
+cudaError_t scan_states_f32_rev(const Plan &p, float *states, int nseg, cudaStream_t st);
+// The same forward scan for double-float (hi, lo) states, summed in fp64.
+cudaError_t scan_states_df(const Plan &p, float *hi, float *lo, int nseg, cudaStream_t st);
 
 // Tensor-core family (tc_forward.cu): bf16 I/O, 128-row tiles.
 bool tc_forward_supported(int d, int M, int chunk, bool favor);
 size_t tc_smem_bytes(int d, int M, bool favor);
 cudaError_t tc_forward(const Plan &p, const Args &a, cudaStream_t st);
+// K-side totals of R' for the first nseg segments, scanned (tensor path).
+cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, cudaStream_t st);
+
+// Tensor-core SLiM backward (tc_backward.cu): bf16 I/O, d = 64, M <= 128.
+bool tc_backward_supported(int d, int M, int chunk, bool favor);
+cudaError_t tc_backward(const Plan &p, const Args &a, cudaStream_t st);
 
 }  // namespace slim

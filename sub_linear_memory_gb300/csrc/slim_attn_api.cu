@@ -116,10 +116,12 @@ Plan make_plan(int B, int H, int L, int d, int M, int chunk, bool favor, bool bw
   p.dp = d + 1;
   p.path = path;
   choose_segments(p, g_opt_segments, path == 2 ? p.tc_tiles : p.nchunks);
-  // master states: fp64 on the CUDA-core path, fp32 on the tensor path
+  // master states: fp64 on the CUDA-core path; double-float (hi, lo) fp32
+  // pairs on the tensor path, whose reverse states are plain fp32
   const size_t state = (path == 2 ? 1 : 2) * (size_t)p.BH * p.P * p.dp * p.M;
   size_t off = 0;
   p.states_off = off; off += align_floats(state);
+  p.states_lo_off = off; if (path == 2) off += align_floats(state);
   p.gstates_off = off; if (bwd) off += align_floats(state);
   p.scratch_stride = path == 2 ? 0 : align_floats(generic_scratch_floats(p, bwd));
   p.scratch_off = off; off += p.scratch_stride * p.BH * p.P;
@@ -143,9 +145,10 @@ slim_status run(bool bwd, const void *q, const void *k, const void *v, const flo
   if (!q || !k || !v) return SLIM_ERR_INVALID_ARG;
   if (!bwd && !y) return SLIM_ERR_INVALID_ARG;
   if (bwd && (!dy || !dq || !dk || !dv)) return SLIM_ERR_INVALID_ARG;
-  const bool tc = !bwd && sizeof(T) == 2 && g_opt_path != 1 &&
-                  tc_forward_supported(d, M, chunk, favor) && aligned16(q) && aligned16(k) &&
-                  aligned16(v) && aligned16(y);
+  const bool io_ok = sizeof(T) == 2 && g_opt_path != 1 && aligned16(q) && aligned16(k) && aligned16(v);
+  const bool tc = io_ok && (bwd ? (dw == nullptr && tc_backward_supported(d, M, chunk, favor) &&
+                                   aligned16(dy) && aligned16(dq) && aligned16(dk) && aligned16(dv))
+                                : (tc_forward_supported(d, M, chunk, favor) && aligned16(y)));
   Plan p = make_plan(B, H, L, d, M, chunk, favor, bwd, dw != nullptr, tc ? 2 : 1);
   Args a{};
   a.q = q; a.k = k; a.v = v; a.dy = dy; a.y = y; a.dq = dq; a.dk = dk; a.dv = dv;
@@ -156,9 +159,8 @@ slim_status run(bool bwd, const void *q, const void *k, const void *v, const flo
     if (!g_ws || g_ws_bytes < p.total_floats * sizeof(float)) return SLIM_ERR_WORKSPACE;
     a.ws = static_cast<float *>(g_ws);
   }
-  cudaError_t err = bwd  ? generic_backward<T>(p, a, stream)
-                    : tc ? tc_forward(p, a, stream)
-                         : generic_forward<T>(p, a, stream);
+  cudaError_t err = tc ? (bwd ? tc_backward(p, a, stream) : tc_forward(p, a, stream))
+                      : (bwd ? generic_backward<T>(p, a, stream) : generic_forward<T>(p, a, stream));
   return err == cudaSuccess ? SLIM_OK : SLIM_ERR_CUDA;
 }
 

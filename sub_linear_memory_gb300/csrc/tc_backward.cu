@@ -1,0 +1,808 @@
+// tc_backward.cu -- tensor-core (tcgen05 + TMA) SLiM backward for bf16 I/O.
+//
+// "Sub-Linear Memory: How to Make Performers SLiM", section 3.3.  One CTA
+// walks one segment of 128-row tiles in reverse.  Per tile, with R' the
+// stacked state [R ; S^T] and G the reverse state [G_V ; G_S] (rows d and
+// d+1), both kept as fp32 masters in TMEM with features on the lanes:
+//   R' -= phi_k^T [V, 1]                      eq. (19): state before the tile
+//   A   = tril(phi_q phi_k^T),  num = A V + phi_q R^T,
+//   den = rowsum(A) + phi_q . S,  Y = num / den
+//   dN  = dY / den,  dD = -(dY . Y) / den     (dN' = [dN ; dD])
+//   dA  = tril(dN V^T + dD 1^T)
+//   dV  = A^T dN + phi_k G_V^T
+//   dphi_q = dA phi_k + dN R^T + dD S^T
+//   dphi_k = dA^T phi_q + V G_V^T + 1 G_S^T
+//   G  += phi_q^T [dN, dD]                    eq. (20)
+//   FAVOR+: u = phi * dphi, dX = u W^T - X rowsum(u);  elu+1: dX = dphi * min(phi, 1)
+// G starts at zero at the end of each segment, so dK and dV here miss the
+// later segments' G; the correction kernel adds G_end(s) (the reverse scan of
+// the segments' G totals) afterwards: both terms are linear in G.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_common.cuh"
+#include "tma_host.h"
+
+namespace slim {
+namespace tcb {
+
+using namespace slim::tc;
+
+constexpr int kThreads = 256;
+constexpr int kTile = 128;
+constexpr int D = 64;
+
+struct Params {
+  int L, M, nt, P, tps, favor;
+  __nv_bfloat16 *dq, *dk, *dv;
+  const float *w;
+  const float *states;     // fp32 [BH][P][M][D + 1]: inclusive segment-end R', high parts
+  const float *states_lo;  // low parts
+  float *gstates;          // fp32 [BH][P][M][D + 1]: segment totals of G (out) / G_end (in)
+  int *status;
+};
+
+struct Layout {
+  uint32_t w, q, k, v, dy, phq, phk, at, dn, rb, ones, ddb;
+  uint32_t s_f, gs_f, den_a, den_b, dd, usq, usk, dot, bars, total;
+  __host__ __device__ explicit Layout(int MC) {
+    uint32_t o = 0;
+    const uint32_t tile = kTile * D * 2;
+    w = o; o += (uint32_t)MC * 128u;
+    q = o; o += tile;
+    k = o; o += tile;
+    v = o; o += tile;
+    dy = o; o += tile;  // dY, then the bf16 copy of G_V
+    phq = o; o += kTile * 256;
+    phk = o; o += kTile * 256;
+    at = o; o += kTile * 256;  // masked A, then masked dA
+    dn = o; o += tile;
+    rb = o; o += (uint32_t)MC * 128u;
+    ones = o; o += 4096;
+    ddb = o; o += 4096;
+    s_f = o; o += 128 * 4;
+    gs_f = o; o += 128 * 4;
+    den_a = o; o += 2 * kTile * 4;
+    den_b = o; o += 2 * kTile * 4;
+    dd = o; o += kTile * 4;
+    usq = o; o += 2 * kTile * 4;
+    usk = o; o += 2 * kTile * 4;
+    dot = o; o += 2 * kTile * 4;
+    bars = o; o += 64;
+    total = o;
+  }
+};
+
+// TMEM columns: R' as a double-float (hi, lo) pair, G, two transients
+constexpr uint32_t kRhi = 0, kRlo = 80, kG = 160, kT = 240, kX = 368;
+
+__device__ __forceinline__ void st_bf16_scalar(unsigned char *smem, uint32_t off, float v) {
+  *reinterpret_cast<__nv_bfloat16 *>(smem + off) = __float2bfloat16_rn(v);
+}
+
+// Copy columns [0, 64) of a TMEM state (features on lanes) into a bf16
+// [MC][64] tile and column 64 into an fp32 vector.  Threads: feature
+// f = 32 * (warp % 4) + lane, column half = warp / 4.
+// (col_lo != col: the state is the double-float pair (col, col_lo).)
+__device__ __forceinline__ void state_to_smem(uint32_t tbase, uint32_t col, uint32_t col_lo, int q4,
+                                              int ch, int f, int MC, uint32_t s_tile, float *vec) {
+  float v[32];
+  tmem_ld32(tmem_addr(tbase, 32 * q4, col + 32 * ch), v);
+  if (col_lo != col) {
+    float l[32];
+    tmem_ld32(tmem_addr(tbase, 32 * q4, col_lo + 32 * ch), l);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] += l[i];
+  }
+  if (f < MC) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) st_bf16x8(s_tile + sw128_offset(f, 32 * ch + 8 * j, MC), v + 8 * j);
+  }
+  if (ch == 1) {
+    float s[16];
+    tmem_ld16(tmem_addr(tbase, 32 * q4, col + 64), s);
+    if (col_lo != col) {
+      float l[16];
+      tmem_ld16(tmem_addr(tbase, 32 * q4, col_lo + 64), l);
+      s[0] += l[0];
+    }
+    if (f < MC) vec[f] = s[0];
+  }
+}
+
+template <bool FAVOR>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDY,
+                  Params p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char *smem =
+      reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int MC = p.M;  // features per CTA (<= 128)
+  const Layout lay(MC);
+  const uint32_t sb = smem_u32(smem);
+  uint64_t *in_bar = reinterpret_cast<uint64_t *>(smem + lay.bars);
+  uint64_t *mma_bar = in_bar + 1;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(in_bar + 2);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(in_bar + 3);
+  float *s_f = reinterpret_cast<float *>(smem + lay.s_f);
+  float *gs_f = reinterpret_cast<float *>(smem + lay.gs_f);
+  float *den_a = reinterpret_cast<float *>(smem + lay.den_a);
+  float *den_b = reinterpret_cast<float *>(smem + lay.den_b);
+  float *dd = reinterpret_cast<float *>(smem + lay.dd);
+  float *usq = reinterpret_cast<float *>(smem + lay.usq);
+  float *usk = reinterpret_cast<float *>(smem + lay.usk);
+  float *dot = reinterpret_cast<float *>(smem + lay.dot);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q4 = warp & 3, ch = warp >> 2, row = 32 * q4 + lane;
+  const int seg = blockIdx.x, bh = blockIdx.y;
+  const int M = p.M, DP = D + 1;
+  const int t0 = seg * p.tps, t1 = min(t0 + p.tps, p.nt);
+  const int half = MC / 2;  // feature columns per thread (two threads per row)
+
+  if (tid == 0) {
+    mbar_init(in_bar, 1);
+    mbar_init(mma_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(tslot, 512);
+
+  if (FAVOR) {
+    for (int idx = tid; idx < MC * D; idx += kThreads) {
+      const int i = idx / MC, m = idx - i * MC;
+      st_bf16_scalar(smem, lay.w + sw128_offset(m, i, MC), p.w[(size_t)i * M + m]);
+    }
+  }
+  for (int idx = tid; idx < kTile * 16; idx += kThreads) {
+    const int r = idx >> 4, x = idx & 15;
+    st_bf16_scalar(smem, lay.ones + n16_offset(r, x), x == 0 ? 1.f : 0.f);
+    st_bf16_scalar(smem, lay.ddb + n16_offset(r, x), 0.f);
+  }
+  if (MC < 128) {  // features beyond MC stay zero in phi_q / phi_k
+    for (int idx = tid; idx < kTile * 128; idx += kThreads) {
+      const int r = idx >> 7, x = idx & 127;
+      if (x >= MC) {
+        st_bf16_scalar(smem, lay.phq + sw128_offset(r, x, kTile), 0.f);
+        st_bf16_scalar(smem, lay.phk + sw128_offset(r, x, kTile), 0.f);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = *tslot;
+
+  // R' <- inclusive state at the segment end (hi, lo); G <- 0
+  {
+    const size_t off = ((size_t)bh * p.P + seg) * (size_t)M * DP;
+    const int f = row;
+    for (int c = ch * 48; c < (ch ? 80 : 48); c += 16) {
+      float h[16], l[16], z[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int e = c + i;
+        const bool in = f < MC && e <= D;
+        h[i] = in ? p.states[off + (size_t)f * DP + e] : 0.f;
+        l[i] = in ? p.states_lo[off + (size_t)f * DP + e] : 0.f;
+        z[i] = 0.f;
+      }
+      tmem_st16(tmem_addr(tb, 32 * q4, kRhi + c), h);
+      tmem_st16(tmem_addr(tb, 32 * q4, kRlo + c), l);
+      tmem_st16(tmem_addr(tb, 32 * q4, kG + c), z);
+    }
+    tmem_st_wait();
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t s_w = sb + lay.w, s_q = sb + lay.q, s_k = sb + lay.k, s_v = sb + lay.v;
+  const uint32_t s_dy = sb + lay.dy, s_phq = sb + lay.phq, s_phk = sb + lay.phk;
+  const uint32_t s_at = sb + lay.at, s_dn = sb + lay.dn, s_rb = sb + lay.rb;
+  const uint32_t s_ones = sb + lay.ones, s_ddb = sb + lay.ddb;
+  const uint32_t tile_bytes = kTile * D * 2;
+  uint32_t in_phase = 0, mma_phase = 0;
+
+  auto issue_in = [&](int t) {
+    mbar_arrive_expect_tx(in_bar, 4 * tile_bytes);
+    tma_load_3d(smem + lay.q, &tmQ, in_bar, 0, t * kTile, bh);
+    tma_load_3d(smem + lay.k, &tmK, in_bar, 0, t * kTile, bh);
+    tma_load_3d(smem + lay.v, &tmV, in_bar, 0, t * kTile, bh);
+    tma_load_3d(smem + lay.dy, &tmDY, in_bar, 0, t * kTile, bh);
+  };
+  auto mma_done = [&]() {
+    mma_commit(mma_bar);
+  };
+  auto wait_mma = [&]() {
+    __syncwarp();
+    mbar_wait(mma_bar, mma_phase, p.status, abort_flag);
+    mma_phase ^= 1;
+    tc_fence_after();
+  };
+  auto cta_sync = [&]() {
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  };
+
+  if (tid == 0 && t0 < t1) issue_in(t1 - 1);
+
+  for (int t = t1 - 1; t >= t0; --t) {
+    const int valid = min(kTile, p.L - t * kTile);
+    const bool live = row < valid;
+    mbar_wait(in_bar, in_phase, p.status, abort_flag);
+    in_phase ^= 1;
+    float ck = 0.f, cq = 0.f;
+    if (FAVOR) {
+      ck = favor_row_const(tile_row_sqnorm(s_k, row, D), M);
+      cq = favor_row_const(tile_row_sqnorm(s_q, row, D), M);
+    }
+
+    // (b) phi_k
+    if (FAVOR) {
+      if (tid == 0) {
+        const uint32_t id = make_idesc(128, MC, false, false);
+        for (int s = 0; s < D / 16; ++s)
+          mma_bf16(tb + kT, desc_kmajor(s_k, kTile, 0, s), desc_kmajor(s_w, MC, 0, s), id, s > 0);
+        mma_done();
+      }
+      wait_mma();
+      for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 32) {
+        float v[32];
+        tmem_ld32(tmem_addr(tb, 32 * q4, kT + c0), v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = live ? favor_feature(v[i], ck) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) st_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
+      }
+    } else {
+      for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 8) {
+        float v[8];
+        ld_bf16x8(s_k + sw128_offset(row, c0, kTile), v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = live ? elu1_feature(v[i]) : 0.f;
+        st_bf16x8(s_phk + sw128_offset(row, c0, kTile), v);
+      }
+    }
+    fence_async_smem();
+    cta_sync();
+
+    // (c) eq. (19): R' -= phi_k^T [V, 1], removing exactly the increment the
+    // segment pre-pass added for this tile; then the bf16 copy of R and S
+    if (tid == 0) {
+      issue_state_delta(tb + kX, s_phk, s_v, s_ones, D);
+      mma_done();
+    }
+    wait_mma();
+    df_update_tmem(tb, 32 * q4, kX, kRhi, kRlo, ch ? 48 : 0, ch ? 80 : 48, -1.f);
+    cta_sync();
+    state_to_smem(tb, kRhi, kRlo, q4, ch, row, MC, s_rb, s_f);
+    fence_async_smem();
+    cta_sync();
+
+    // (d) phi_q and phi_q . S
+    float den_inter = 0.f;
+    if (FAVOR) {
+      if (tid == 0) {
+        const uint32_t id = make_idesc(128, MC, false, false);
+        for (int s = 0; s < D / 16; ++s)
+          mma_bf16(tb + kT, desc_kmajor(s_q, kTile, 0, s), desc_kmajor(s_w, MC, 0, s), id, s > 0);
+        mma_done();
+      }
+      wait_mma();
+      for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 32) {
+        float v[32];
+        tmem_ld32(tmem_addr(tb, 32 * q4, kT + c0), v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v[i] = live ? favor_feature(v[i], cq) : 0.f;
+          den_inter = fmaf(v[i], s_f[c0 + i], den_inter);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) st_bf16x8(s_phq + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
+      }
+    } else {
+      for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 8) {
+        float v[8];
+        ld_bf16x8(s_q + sw128_offset(row, c0, kTile), v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          v[i] = live ? elu1_feature(v[i]) : 0.f;
+          den_inter = fmaf(v[i], s_f[c0 + i], den_inter);
+        }
+        st_bf16x8(s_phq + sw128_offset(row, c0, kTile), v);
+      }
+    }
+    den_a[ch * kTile + row] = den_inter;
+    fence_async_smem();
+    cta_sync();
+
+    // (e) A = tril(phi_q phi_k^T) -> bf16 tile, row sums
+    if (tid == 0) {
+      const uint32_t id = make_idesc(128, 128, false, false);
+      for (int s = 0; s < MC / 16; ++s)
+        mma_bf16(tb + kT, desc_kmajor(s_phq, kTile, 0, s), desc_kmajor(s_phk, kTile, 0, s), id, s > 0);
+      mma_done();
+    }
+    wait_mma();
+    {
+      float rs = 0.f;
+      for (int c0 = ch * 64; c0 < ch * 64 + 64; c0 += 32) {
+        float v[32];
+        tmem_ld32(tmem_addr(tb, 32 * q4, kT + c0), v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (c0 + i > row) v[i] = 0.f;
+          rs += v[i];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
+      }
+      den_b[ch * kTile + row] = rs;
+    }
+    fence_async_smem();
+    cta_sync();
+
+    // (f) num = A V + phi_q R^T; Y, dN, dD
+    if (tid == 0) {
+      const uint32_t id = make_idesc(128, D, false, true);
+      for (int s = 0; s < kTile / 16; ++s)
+        mma_bf16(tb + kT, desc_kmajor(s_at, kTile, 0, s), desc_mnmajor(s_v, kTile, 0, s), id, s > 0);
+      for (int s = 0; s < MC / 16; ++s)
+        mma_bf16(tb + kT, desc_kmajor(s_phq, kTile, 0, s), desc_mnmajor(s_rb, MC, 0, s), id, 1);
+      mma_done();
+    }
+    wait_mma();
+    {
+      const float den = den_a[row] + den_a[kTile + row] + den_b[row] + den_b[kTile + row];
+      const float inv = 1.0f / den;
+      float v[32], g[32];
+      tmem_ld32(tmem_addr(tb, 32 * q4, kT + 32 * ch), v);
+      float dyy = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        ld_bf16x8(s_dy + sw128_offset(row, 32 * ch + 8 * j, kTile), g + 8 * j);
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float y = v[i] * inv;
+        dyy = fmaf(g[i], y, dyy);
+        g[i] = live ? g[i] * inv : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) st_bf16x8(s_dn + sw128_offset(row, 32 * ch + 8 * j, kTile), g + 8 * j);
+      dot[ch * kTile + row] = dyy;
+      __syncthreads();
+      if (ch == 0) {
+        const float dval = live ? -(dot[row] + dot[kTile + row]) * inv : 0.f;
+        dd[row] = dval;
+        st_bf16_scalar(smem, lay.ddb + n16_offset(row, 0), dval);
+      }
+    }
+    cta_sync();  // dY consumed: its buffer now takes the bf16 copy of G_V
+    state_to_smem(tb, kG, kG, q4, ch, row, MC, s_dy, gs_f);
+    fence_async_smem();
+    cta_sync();
+
+    // (g) dV = A^T dN + phi_k G_V^T ; raw dA = dN V^T
+    if (tid == 0) {
+      const uint32_t id_v1 = make_idesc(128, D, true, true);
+      const uint32_t id_v2 = make_idesc(128, D, false, true);
+      for (int s = 0; s < kTile / 16; ++s)
+        mma_bf16(tb + kX, desc_mnmajor(s_at, kTile, 0, s), desc_mnmajor(s_dn, kTile, 0, s), id_v1, s > 0);
+      for (int s = 0; s < MC / 16; ++s)
+        mma_bf16(tb + kX, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_dy, MC, 0, s), id_v2, 1);
+      const uint32_t id_a = make_idesc(128, 128, false, false);
+      for (int s = 0; s < D / 16; ++s)
+        mma_bf16(tb + kT, desc_kmajor(s_dn, kTile, 0, s), desc_kmajor(s_v, kTile, 0, s), id_a, s > 0);
+      mma_done();
+    }
+    wait_mma();
+    {
+      const float dval = dd[row];
+      for (int c0 = ch * 64; c0 < ch * 64 + 64; c0 += 32) {
+        float v[32];
+        tmem_ld32(tmem_addr(tb, 32 * q4, kT + c0), v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = (c0 + i > row) ? 0.f : v[i] + dval;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
+      }
+      float v[32];
+      tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * ch), v);
+      if (live) {
+        uint4 *dst = reinterpret_cast<uint4 *>(p.dv + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          dst[j] = make_uint4(pack_bf16(v[8 * j], v[8 * j + 1]), pack_bf16(v[8 * j + 2], v[8 * j + 3]),
+                              pack_bf16(v[8 * j + 4], v[8 * j + 5]), pack_bf16(v[8 * j + 6], v[8 * j + 7]));
+      }
+    }
+    fence_async_smem();
+    cta_sync();
+
+    // (h) dphi_q, dphi_k, G update
+    if (tid == 0) {
+      const uint32_t id_q1 = make_idesc(128, MC, false, true);
+      const uint32_t id_q2 = make_idesc(128, MC, false, false);
+      for (int s = 0; s < kTile / 16; ++s)
+        mma_bf16(tb + kT, desc_kmajor(s_at, kTile, 0, s), desc_mnmajor(s_phk, kTile, 0, s), id_q1, s > 0);
+      for (int s = 0; s < D / 16; ++s)
+        mma_bf16(tb + kT, desc_kmajor(s_dn, kTile, 0, s), desc_kmajor(s_rb, MC, 0, s), id_q2, 1);
+      const uint32_t id_k1 = make_idesc(128, MC, true, true);
+      for (int s = 0; s < kTile / 16; ++s)
+        mma_bf16(tb + kX, desc_mnmajor(s_at, kTile, 0, s), desc_mnmajor(s_phq, kTile, 0, s), id_k1, s > 0);
+      for (int s = 0; s < D / 16; ++s)
+        mma_bf16(tb + kX, desc_kmajor(s_v, kTile, 0, s), desc_kmajor(s_dy, MC, 0, s), id_q2, 1);
+      const uint32_t id_g = make_idesc(128, D, true, true);
+      const uint32_t id_g1 = make_idesc(128, 16, true, true);
+      for (int s = 0; s < kTile / 16; ++s) {
+        mma_bf16(tb + kG, desc_mnmajor(s_phq, kTile, 0, s), desc_mnmajor(s_dn, kTile, 0, s), id_g, 1);
+        mma_bf16(tb + kG + D, desc_mnmajor(s_phq, kTile, 0, s), desc_n16(s_ddb, s), id_g1, 1);
+      }
+      mma_done();
+    }
+    wait_mma();
+
+    // (i) u = phi * dphi (in place over phi), row sums; elu+1 writes dQ, dK here
+    {
+      const float dval = dd[row];
+      float uq = 0.f, uk = 0.f;
+      for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 32) {
+        float a[32], b[32];
+        tmem_ld32(tmem_addr(tb, 32 * q4, kT + c0), a);
+        tmem_ld32(tmem_addr(tb, 32 * q4, kX + c0), b);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float fq[8], fk[8];
+          ld_bf16x8(s_phq + sw128_offset(row, c0 + 8 * j, kTile), fq);
+          ld_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), fk);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int m = c0 + 8 * j + i;
+            const float dq = fmaf(dval, s_f[m], a[8 * j + i]);
+            const float dk = b[8 * j + i] + gs_f[m];
+            if (FAVOR) {
+              a[8 * j + i] = fq[i] * dq;
+              b[8 * j + i] = fk[i] * dk;
+            } else {
+              a[8 * j + i] = dq * fminf(fq[i], 1.f);
+              b[8 * j + i] = dk * fminf(fk[i], 1.f);
+            }
+            uq += a[8 * j + i];
+            uk += b[8 * j + i];
+          }
+        }
+        if (FAVOR) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            st_bf16x8(s_phq + sw128_offset(row, c0 + 8 * j, kTile), a + 8 * j);
+            st_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), b + 8 * j);
+          }
+        } else if (live) {
+          uint4 *gq = reinterpret_cast<uint4 *>(p.dq + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + c0);
+          uint4 *gk = reinterpret_cast<uint4 *>(p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + c0);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            gq[j] = make_uint4(pack_bf16(a[8 * j], a[8 * j + 1]), pack_bf16(a[8 * j + 2], a[8 * j + 3]),
+                               pack_bf16(a[8 * j + 4], a[8 * j + 5]), pack_bf16(a[8 * j + 6], a[8 * j + 7]));
+            gk[j] = make_uint4(pack_bf16(b[8 * j], b[8 * j + 1]), pack_bf16(b[8 * j + 2], b[8 * j + 3]),
+                               pack_bf16(b[8 * j + 4], b[8 * j + 5]), pack_bf16(b[8 * j + 6], b[8 * j + 7]));
+          }
+        }
+      }
+      usq[ch * kTile + row] = uq;
+      usk[ch * kTile + row] = uk;
+    }
+    fence_async_smem();
+    cta_sync();
+
+    if (FAVOR) {
+      // (j) dQ = u_q W^T - q rowsum(u_q), dK likewise
+      if (tid == 0) {
+        const uint32_t id = make_idesc(128, D, false, true);
+        for (int s = 0; s < MC / 16; ++s) {
+          mma_bf16(tb + kT, desc_kmajor(s_phq, kTile, 0, s), desc_mnmajor(s_w, MC, 0, s), id, s > 0);
+          mma_bf16(tb + kT + 64, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_w, MC, 0, s), id, s > 0);
+        }
+        mma_done();
+      }
+      wait_mma();
+      const float sq = usq[row] + usq[kTile + row], sk = usk[row] + usk[kTile + row];
+      float a[32], b[32];
+      tmem_ld32(tmem_addr(tb, 32 * q4, kT + 32 * ch), a);
+      tmem_ld32(tmem_addr(tb, 32 * q4, kT + 64 + 32 * ch), b);
+      if (live) {
+        uint4 *gq = reinterpret_cast<uint4 *>(p.dq + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch);
+        uint4 *gk = reinterpret_cast<uint4 *>(p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float xq[8], xk[8];
+          ld_bf16x8(s_q + sw128_offset(row, 32 * ch + 8 * j, kTile), xq);
+          ld_bf16x8(s_k + sw128_offset(row, 32 * ch + 8 * j, kTile), xk);
+          float oq[8], ok[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            oq[i] = a[8 * j + i] - xq[i] * sq;
+            ok[i] = b[8 * j + i] - xk[i] * sk;
+          }
+          gq[j] = make_uint4(pack_bf16(oq[0], oq[1]), pack_bf16(oq[2], oq[3]), pack_bf16(oq[4], oq[5]),
+                             pack_bf16(oq[6], oq[7]));
+          gk[j] = make_uint4(pack_bf16(ok[0], ok[1]), pack_bf16(ok[2], ok[3]), pack_bf16(ok[4], ok[5]),
+                             pack_bf16(ok[6], ok[7]));
+        }
+      }
+      cta_sync();
+    }
+    if (tid == 0 && t > t0) issue_in(t - 1);
+  }
+
+  // segment total of G -> gstates
+  {
+    float *out = p.gstates + ((size_t)bh * p.P + seg) * (size_t)M * DP;
+    const int f = row;
+    for (int c = ch * 48; c < (ch ? 80 : 48); c += 16) {
+      float v[16];
+      tmem_ld16(tmem_addr(tb, 32 * q4, kG + c), v);
+      if (f < MC) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (c + i <= D) out[(size_t)f * DP + c + i] = v[i];
+      }
+    }
+  }
+  cta_sync();
+  if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+// Correction: add G_end(s) (the G of every later segment) to dK and dV of
+// segment s:  dphi_k += V G_V^T + 1 G_S^T,  dV += phi_k G_V^T.
+template <bool FAVOR>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_bwd_fix_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      Params p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char *smem =
+      reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int MC = p.M;
+  const Layout lay(MC);  // reuses the main kernel's regions
+  const uint32_t sb = smem_u32(smem);
+  uint64_t *in_bar = reinterpret_cast<uint64_t *>(smem + lay.bars);
+  uint64_t *mma_bar = in_bar + 1;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(in_bar + 2);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(in_bar + 3);
+  float *gs_f = reinterpret_cast<float *>(smem + lay.gs_f);
+  float *usk = reinterpret_cast<float *>(smem + lay.usk);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q4 = warp & 3, ch = warp >> 2, row = 32 * q4 + lane;
+  const int seg = blockIdx.x, bh = blockIdx.y;
+  const int M = p.M, DP = D + 1;
+  const int t0 = seg * p.tps, t1 = min(t0 + p.tps, p.nt);
+  const int half = MC / 2;
+
+  if (tid == 0) {
+    mbar_init(in_bar, 1);
+    mbar_init(mma_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(tslot, 512);
+  if (FAVOR) {
+    for (int idx = tid; idx < MC * D; idx += kThreads) {
+      const int i = idx / MC, m = idx - i * MC;
+      st_bf16_scalar(smem, lay.w + sw128_offset(m, i, MC), p.w[(size_t)i * M + m]);
+    }
+  }
+  // G_end(s) = gstates[s + 1] after the reverse scan -> bf16 [MC][64] + G_S
+  {
+    const float *g = p.gstates + ((size_t)bh * p.P + seg + 1) * (size_t)M * DP;
+    for (int idx = tid; idx < MC * D; idx += kThreads) {
+      const int f = idx / D, e = idx - f * D;
+      st_bf16_scalar(smem, lay.rb + sw128_offset(f, e, MC), g[(size_t)f * DP + e]);
+    }
+    for (int f = tid; f < MC; f += kThreads) gs_f[f] = g[(size_t)f * DP + D];
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = *tslot;
+  const uint32_t s_w = sb + lay.w, s_k = sb + lay.k, s_v = sb + lay.v, s_phk = sb + lay.phk;
+  const uint32_t s_gb = sb + lay.rb;
+  const uint32_t tile_bytes = kTile * D * 2;
+  uint32_t in_phase = 0, mma_phase = 0;
+  auto wait_mma = [&]() {
+    __syncwarp();
+    mbar_wait(mma_bar, mma_phase, p.status, abort_flag);
+    mma_phase ^= 1;
+    tc_fence_after();
+  };
+  auto cta_sync = [&]() {
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  };
+
+  for (int t = t0; t < t1; ++t) {
+    const int valid = min(kTile, p.L - t * kTile);
+    const bool live = row < valid;
+    if (tid == 0) {
+      mbar_arrive_expect_tx(in_bar, 2 * tile_bytes);
+      tma_load_3d(smem + lay.k, &tmK, in_bar, 0, t * kTile, bh);
+      tma_load_3d(smem + lay.v, &tmV, in_bar, 0, t * kTile, bh);
+    }
+    mbar_wait(in_bar, in_phase, p.status, abort_flag);
+    in_phase ^= 1;
+    float ck = 0.f;
+    if (FAVOR) {
+      ck = favor_row_const(tile_row_sqnorm(s_k, row, D), M);
+      if (tid == 0) {
+        const uint32_t id = make_idesc(128, MC, false, false);
+        for (int s = 0; s < D / 16; ++s)
+          mma_bf16(tb + kT, desc_kmajor(s_k, kTile, 0, s), desc_kmajor(s_w, MC, 0, s), id, s > 0);
+        mma_commit(mma_bar);
+      }
+      wait_mma();
+      for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 32) {
+        float v[32];
+        tmem_ld32(tmem_addr(tb, 32 * q4, kT + c0), v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = live ? favor_feature(v[i], ck) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) st_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
+      }
+    } else {
+      for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 8) {
+        float v[8];
+        ld_bf16x8(s_k + sw128_offset(row, c0, kTile), v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = live ? elu1_feature(v[i]) : 0.f;
+        st_bf16x8(s_phk + sw128_offset(row, c0, kTile), v);
+      }
+    }
+    fence_async_smem();
+    cta_sync();
+    // dphi_k' = V G_V^T -> T ; dV' = phi_k G_V^T -> X
+    if (tid == 0) {
+      const uint32_t id1 = make_idesc(128, MC, false, false);
+      for (int s = 0; s < D / 16; ++s)
+        mma_bf16(tb + kT, desc_kmajor(s_v, kTile, 0, s), desc_kmajor(s_gb, MC, 0, s), id1, s > 0);
+      const uint32_t id2 = make_idesc(128, D, false, true);
+      for (int s = 0; s < MC / 16; ++s)
+        mma_bf16(tb + kX, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_gb, MC, 0, s), id2, s > 0);
+      mma_commit(mma_bar);
+    }
+    wait_mma();
+    float uk = 0.f;
+    for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 32) {
+      float b[32];
+      tmem_ld32(tmem_addr(tb, 32 * q4, kT + c0), b);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float fk[8];
+        ld_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), fk);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float dk = b[8 * j + i] + gs_f[c0 + 8 * j + i];
+          b[8 * j + i] = FAVOR ? fk[i] * dk : dk * fminf(fk[i], 1.f);
+          uk += b[8 * j + i];
+        }
+      }
+      if (FAVOR) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) st_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), b + 8 * j);
+      } else if (live) {
+        __nv_bfloat16 *gk = p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + c0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) gk[i] = __float2bfloat16_rn(__bfloat162float(gk[i]) + b[i]);
+      }
+    }
+    usk[ch * kTile + row] = uk;
+    {
+      float v[32];
+      tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * ch), v);
+      if (live) {
+        __nv_bfloat16 *gv = p.dv + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) gv[i] = __float2bfloat16_rn(__bfloat162float(gv[i]) + v[i]);
+      }
+    }
+    fence_async_smem();
+    cta_sync();
+    if (FAVOR) {
+      if (tid == 0) {
+        const uint32_t id = make_idesc(128, D, false, true);
+        for (int s = 0; s < MC / 16; ++s)
+          mma_bf16(tb + kX, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_w, MC, 0, s), id, s > 0);
+        mma_commit(mma_bar);
+      }
+      wait_mma();
+      const float sk = usk[row] + usk[kTile + row];
+      float b[32];
+      tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * ch), b);
+      if (live) {
+        __nv_bfloat16 *gk = p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float xk[8];
+          ld_bf16x8(s_k + sw128_offset(row, 32 * ch + 8 * j, kTile), xk);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int e = 8 * j + i;
+            gk[e] = __float2bfloat16_rn(__bfloat162float(gk[e]) + b[e] - xk[i] * sk);
+          }
+        }
+      }
+    }
+    cta_sync();
+  }
+  cta_sync();
+  if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+template <bool FAVOR>
+cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
+  CUtensorMap mq, mk, mv, mdy;
+  if (!make_map_bf16_3d(&mq, a.q, pl.BH, pl.L, D, kTile) || !make_map_bf16_3d(&mk, a.k, pl.BH, pl.L, D, kTile) ||
+      !make_map_bf16_3d(&mv, a.v, pl.BH, pl.L, D, kTile) || !make_map_bf16_3d(&mdy, a.dy, pl.BH, pl.L, D, kTile))
+    return cudaErrorInvalidValue;
+  cudaError_t e = tc_segment_states(pl, a, pl.P, st);  // R' totals of every segment, scanned
+  if (e != cudaSuccess) return e;
+  Params p{};
+  p.L = pl.L; p.M = pl.M; p.nt = pl.tc_tiles; p.P = pl.P; p.tps = pl.cps; p.favor = FAVOR;
+  p.dq = static_cast<__nv_bfloat16 *>(a.dq);
+  p.dk = static_cast<__nv_bfloat16 *>(a.dk);
+  p.dv = static_cast<__nv_bfloat16 *>(a.dv);
+  p.w = a.w;
+  p.states = a.ws + pl.states_off;
+  p.states_lo = a.ws + pl.states_lo_off;
+  p.gstates = a.ws + pl.gstates_off;
+  p.status = a.status;
+  const Layout lay(pl.M);
+  const int smem = (int)lay.total + 1024;
+  {
+    auto kern = tc_bwd_kernel<FAVOR>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    ProfScope ps("tc_backward", st);
+    kern<<<dim3(pl.P, pl.BH), kThreads, smem, st>>>(mq, mk, mv, mdy, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (pl.P > 1) {
+    {
+      ProfScope ps("scan_states", st);
+      // G_end(s) = sum over s' > s: reverse inclusive scan over segments 1..P-1
+      e = scan_states_f32_rev(pl, a.ws + pl.gstates_off + (size_t)pl.M * (D + 1), pl.P - 1, st);
+      if (e != cudaSuccess) return e;
+    }
+    auto kern = tc_bwd_fix_kernel<FAVOR>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    ProfScope ps("tc_backward_fix", st);
+    kern<<<dim3(pl.P - 1, pl.BH), kThreads, smem, st>>>(mk, mv, p);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace tcb
+
+bool tc_backward_supported(int d, int M, int chunk, bool favor) {
+  if (chunk < 64 || d != 64) return false;
+  return favor ? (M == 64 || M == 128) : M == 64;
+}
+
+size_t tc_backward_smem_bytes(int M) { return tcb::Layout(M).total + 1024; }
+
+cudaError_t tc_backward(const Plan &p, const Args &a, cudaStream_t st) {
+  if (p.d != 64) return cudaErrorInvalidValue;
+  return p.favor ? tcb::backward_family<true>(p, a, st) : tcb::backward_family<false>(p, a, st);
+}
+
+}  // namespace slim

@@ -325,3 +325,94 @@ __device__ __forceinline__ void ld_bf16x8(uint32_t addr, float *v) {
 
 }  // namespace tc
 }  // namespace slim
+
+namespace slim {
+namespace tc {
+
+// ---- pieces shared bit-for-bit by every tensor-core kernel ------------------
+// The backward recovers each tile's incoming state by removing exactly the
+// values the segment pre-pass added, so the feature map and the state
+// increment must round identically in both: they live here, written with
+// explicit fmaf so no kernel contracts them differently.
+
+// |x_row|^2 from a swizzled bf16 [128][D] tile.
+__device__ __forceinline__ float tile_row_sqnorm(uint32_t tile_base, int row, int D) {
+  float s = 0.f;
+  for (int c = 0; c < D / 8; ++c) {
+    float v[8];
+    ld_bf16x8(tile_base + sw128_offset(row, c * 8, 128), v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s = fmaf(v[i], v[i], s);
+  }
+  return s;
+}
+
+constexpr float kLog2eF = 1.4426950408889634f;
+
+// exp2 offset of a row: phi_m = 2^(s_m log2 e + c), c = -|x|^2 log2(e)/2 - log2(sqrt(M)).
+__device__ __forceinline__ float favor_row_const(float sqnorm, int M) {
+  return fmaf(-0.5f * kLog2eF, sqnorm, -0.5f * log2f((float)M));
+}
+
+__device__ __forceinline__ float favor_feature(float s, float c) {
+  return exp2f(fmaf(s, kLog2eF, c));
+}
+
+__device__ __forceinline__ float elu1_feature(float x) { return x > 0.f ? x + 1.f : __expf(x); }
+
+// no-swizzle MN-major operand of 16 columns: core matrices of 8 rows x 16 B,
+// K groups of 8 rows 256 B apart, the two 8-column groups 128 B apart.
+__host__ __device__ __forceinline__ uint32_t n16_offset(uint32_t k, uint32_t n) {
+  return (n >> 3) * 128u + (k >> 3) * 256u + (k & 7u) * 16u + (n & 7u) * 2u;
+}
+
+__device__ __forceinline__ uint64_t desc_n16(uint32_t base, uint32_t s) {
+  return make_desc(base + s * 512u, 256u, 128u, 0u);
+}
+
+// Increment of one 128-feature block of R'^T over one tile:
+//   delta[f][e] = sum_j phi_k[j][f] V'[j][e],  V' = [V, 1]   (columns 0..D)
+// issued by one thread; `phk` is the [128][128] swizzled phi_k tile (block
+// features in columns 0..127), `v` the [128][D] V tile, `ones` the 16-column
+// ones operand.  Accumulation restarts at zero, so the result depends only
+// on the operands.
+__device__ __forceinline__ void issue_state_delta(uint32_t t_delta, uint32_t phk, uint32_t v,
+                                                  uint32_t ones, int D) {
+  const uint32_t id = make_idesc(128, D, true, true);
+  const uint32_t id1 = make_idesc(128, 16, true, true);
+  for (int s = 0; s < 8; ++s) {
+    mma_bf16(t_delta, desc_mnmajor(phk, 128, 0, s), desc_mnmajor(v, 128, 0, s), id, s > 0);
+    mma_bf16(t_delta + D, desc_mnmajor(phk, 128, 0, s), desc_n16(ones, s), id1, s > 0);
+  }
+}
+
+// (hi, lo) += sign * x as a double-float (two-sum, then renormalise).
+__device__ __forceinline__ void df_add(float &hi, float &lo, float x) {
+  const float s = hi + x;
+  const float bp = s - hi;
+  const float e = (hi - (s - bp)) + (x - bp);
+  const float t = lo + e;
+  hi = s + t;
+  lo = t - (hi - s);
+}
+
+// Columns [c_lo, c_hi) (multiples of 16) of this warp's 32 lanes:
+// (hi, lo) += sign * delta, all three in TMEM.
+__device__ __forceinline__ void df_update_tmem(uint32_t tbase, int lane_base, uint32_t t_delta,
+                                               uint32_t t_hi, uint32_t t_lo, int c_lo, int c_hi,
+                                               float sign) {
+  for (int c = c_lo; c < c_hi; c += 16) {
+    float x[16], h[16], l[16];
+    tmem_ld16(tmem_addr(tbase, lane_base, t_delta + c), x);
+    tmem_ld16(tmem_addr(tbase, lane_base, t_hi + c), h);
+    tmem_ld16(tmem_addr(tbase, lane_base, t_lo + c), l);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) df_add(h[i], l[i], sign * x[i]);
+    tmem_st16(tmem_addr(tbase, lane_base, t_hi + c), h);
+    tmem_st16(tmem_addr(tbase, lane_base, t_lo + c), l);
+  }
+  tmem_st_wait();
+}
+
+}  // namespace tc
+}  // namespace slim

@@ -17,7 +17,9 @@
 // 64-row slices or half a 256-row slice; the paper's slice recurrence is
 // exact for any slice size (section 3.4), so the tiling only changes
 // rounding.  MODE_STATE runs only the K side and writes the segment's total
-// R' (the rows eq. (3) adds) for the segment scan.
+// R' (the rows eq. (3) adds) for the segment scan: each tile's increment is
+// formed by an MMA that restarts at zero and is added to a double-float
+// (hi, lo) total, so the backward can later remove exactly the same values.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -32,7 +34,6 @@ using namespace slim::tc;
 
 constexpr int kThreads = 256;
 constexpr int kTile = 128;
-constexpr float kLog2e = 1.4426950408889634f;
 
 enum { MODE_STATE = 0, MODE_FWD = 1 };
 
@@ -40,7 +41,8 @@ struct Params {
   int L, M, nt, P, tps, favor;
   __nv_bfloat16 *y;
   const float *w;
-  float *states;  // fp32 [BH][P][M][D + 1]
+  float *states;     // fp32 [BH][P][M][D + 1]: high parts of the segment states
+  float *states_lo;  // same layout: low parts
   int *status;
 };
 
@@ -50,6 +52,8 @@ struct Layout {
   uint32_t w, q, k, v, phk, phq, rb, ones, sf, den, bars, total;
   // TMEM columns
   uint32_t t_f, t_a, t_num, t_r;
+  // TMEM columns of the state pre-pass: increment, (hi, lo) totals
+  uint32_t s_delta, s_hi, s_lo;
   __host__ __device__ Layout(int M, bool favor) {
     const uint32_t tile = kTile * D * 2;  // one [128][D] bf16 tile
     uint32_t o = 0;
@@ -60,7 +64,7 @@ struct Layout {
     phk = o; o += kTile * 128 * 2;
     phq = o; o += kTile * 128 * 2;  // also the masked A tile
     rb = o; o += (uint32_t)M * D * 2;
-    ones = o; o += kTile * 128;
+    ones = o; o += 4096;
     sf = o; o += (uint32_t)M * 4;
     den = o; o += 2 * kTile * 4;
     bars = o; o += 64;
@@ -70,19 +74,11 @@ struct Layout {
     t_a = nh > 1 ? 128u : 0u;
     t_num = nh > 1 ? 256u : 128u;
     t_r = t_num + D + 16;
+    s_delta = 0;
+    s_hi = (D + 16 > 128) ? (uint32_t)(D + 16) : 128u;
+    s_lo = s_hi + nh * (D + 16);
   }
 };
-
-__device__ __forceinline__ float row_sqnorm(uint32_t tile_base, int row, int D) {
-  float s = 0.f;
-  for (int c = 0; c < D / 8; ++c) {
-    float v[8];
-    ld_bf16x8(tile_base + sw128_offset(row, c * 8, kTile), v);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) s = fmaf(v[i], v[i], s);
-  }
-  return s;
-}
 
 template <int D, bool FAVOR, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -129,9 +125,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           __float2bfloat16_rn(p.w[idx]);
     }
   }
-  for (int idx = tid; idx < kTile * 64; idx += kThreads) {
-    const int r = idx >> 6, x = idx & 63;
-    *reinterpret_cast<__nv_bfloat16 *>(smem + lay.ones + sw128_offset(r, x, kTile)) =
+  for (int idx = tid; idx < kTile * 16; idx += kThreads) {
+    const int r = idx >> 4, x = idx & 15;
+    *reinterpret_cast<__nv_bfloat16 *>(smem + lay.ones + n16_offset(r, x)) =
         __float2bfloat16_rn(x == 0 ? 1.f : 0.f);
   }
   if (M < 128) {
@@ -147,16 +143,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tslot;
 
   // incoming state of the segment -> TMEM master, bf16 copy and S
-  {
-    const float *st = (MODE == MODE_FWD && seg > 0)
-                          ? p.states + ((size_t)bh * p.P + seg - 1) * (size_t)M * DP
-                          : nullptr;
+  // (the pre-pass instead starts its (hi, lo) totals at zero)
+  const int ncols = D + 16, csplit = ((ncols / 16 + 1) / 2) * 16;
+  if (MODE == MODE_STATE) {
+    for (int b = 0; b < nh; ++b) {
+      float z[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) z[i] = 0.f;
+      for (int c = ch ? csplit : 0; c < (ch ? ncols : csplit); c += 16) {
+        tmem_st16(tmem_addr(tbase, 32 * q4, lay.s_hi + b * ncols + c), z);
+        tmem_st16(tmem_addr(tbase, 32 * q4, lay.s_lo + b * ncols + c), z);
+      }
+    }
+    tmem_st_wait();
+  } else {
+    const size_t off = ((size_t)bh * p.P + seg - 1) * (size_t)M * DP;
+    const float *st = seg > 0 ? p.states + off : nullptr;
+    const float *st_lo = seg > 0 ? p.states_lo + off : nullptr;
     const int blocks = nh;
     for (int b = 0; b < blocks; ++b) {
       // warps 4b..4b+3 own block b when nh == 2; all warps split columns when nh == 1
       if (nh == 2 && ch != b) continue;
       const int f = 128 * b + row;
-      const int ncols = D + 16;
       const int c_lo = (nh == 2) ? 0 : (ch == 0 ? 0 : (ncols / 32) * 16);
       const int c_hi = (nh == 2) ? ncols : (ch == 0 ? (ncols / 32) * 16 : ncols);
       for (int c = c_lo; c < c_hi; c += 16) {
@@ -164,10 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int e = c + i;
-          v[i] = (st && f < M && e <= D) ? st[(size_t)f * DP + e] : 0.f;
+          v[i] = (st && f < M && e <= D) ? st[(size_t)f * DP + e] + st_lo[(size_t)f * DP + e] : 0.f;
         }
         tmem_st16(tmem_addr(tbase, 32 * q4, lay.t_r + b * (D + 16) + c), v);
-        if (MODE == MODE_FWD && f < M) {
+        if (f < M) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int e = c + i;
@@ -228,8 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     qk_phase ^= 1;
     float ck = 0.f, cq = 0.f;  // per-row exp2 offsets
     if (FAVOR) {
-      ck = -0.5f * kLog2e * row_sqnorm(s_k, row, D) - log2_sqrt_m;
-      if (MODE == MODE_FWD) cq = -0.5f * kLog2e * row_sqnorm(s_q, row, D) - log2_sqrt_m;
+      ck = favor_row_const(tile_row_sqnorm(s_k, row, D), M);
+      if (MODE == MODE_FWD) cq = favor_row_const(tile_row_sqnorm(s_q, row, D), M);
     }
     float den_inter = 0.f;
     for (int h = 0; h < nh; ++h) {
@@ -254,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float v[32];
             tmem_ld32(tmem_addr(tbase, 32 * q4, lay.t_f + c0), v);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = live ? exp2f(fmaf(v[i], kLog2e, c_row)) : 0.f;
+            for (int i = 0; i < 32; ++i) v[i] = live ? favor_feature(v[i], c_row) : 0.f;
             if (side) {
 #pragma unroll
               for (int i = 0; i < 32; ++i) den_inter = fmaf(v[i], sf[128 * h + c0 + i], den_inter);
@@ -268,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float v[8];
             ld_bf16x8(s_x + sw128_offset(row, c0, kTile), v);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = live ? (v[i] > 0.f ? v[i] + 1.f : __expf(v[i])) : 0.f;
+            for (int i = 0; i < 8; ++i) v[i] = live ? elu1_feature(v[i]) : 0.f;
             if (side) {
 #pragma unroll
               for (int i = 0; i < 8; ++i) den_inter = fmaf(v[i], sf[c0 + i], den_inter);
@@ -296,17 +304,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(v_bar, v_phase, p.status, abort_flag);
           v_phase ^= 1;
         }
-        const uint32_t id_r = make_idesc(128, D, true, true);
-        const uint32_t id_r1 = make_idesc(128, 16, true, true);
-        const uint32_t t_r = tbase + lay.t_r + h * (D + 16);
-        for (int s = 0; s < kTile / 16; ++s) {
-          mma_bf16(t_r, desc_mnmajor(s_phk, kTile, 0, s), desc_mnmajor(s_v, kTile, 0, s), id_r, 1);
-          mma_bf16(t_r + D, desc_mnmajor(s_phk, kTile, 0, s), desc_mnmajor(s_ones, kTile, 0, s), id_r1, 1);
+        if (MODE == MODE_FWD) {
+          // the running state only moves forward here: accumulate in place
+          const uint32_t id_r = make_idesc(128, D, true, true);
+          const uint32_t id_r1 = make_idesc(128, 16, true, true);
+          const uint32_t t_r = tbase + lay.t_r + h * (D + 16);
+          for (int s = 0; s < kTile / 16; ++s) {
+            mma_bf16(t_r, desc_mnmajor(s_phk, kTile, 0, s), desc_mnmajor(s_v, kTile, 0, s), id_r, 1);
+            mma_bf16(t_r + D, desc_mnmajor(s_phk, kTile, 0, s), desc_n16(s_ones, s), id_r1, 1);
+          }
+        } else {
+          issue_state_delta(tbase + lay.s_delta, s_phk, s_v, s_ones, D);
         }
         mma_commit(mma_bar);
       }
       __syncwarp();
       mma_sync_all();
+      if (MODE == MODE_STATE) {
+        // (hi, lo) total of block h += this tile's increment
+        df_update_tmem(tbase, 32 * q4, lay.s_delta, lay.s_hi + h * ncols, lay.s_lo + h * ncols,
+                       ch ? csplit : 0, ch ? ncols : csplit, 1.f);
+        cta_sync();
+      }
     }
     if (MODE == MODE_FWD) {
       den_part[ch * kTile + row] = den_inter;
@@ -327,8 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t id_n1 = make_idesc(128, 16, false, true);
         for (int s = 0; s < kTile / 16; ++s) {
           mma_bf16(tbase + lay.t_num, desc_kmajor(s_phq, kTile, 0, s), desc_mnmajor(s_v, kTile, 0, s), id_n, 1);
-          mma_bf16(tbase + lay.t_num + D, desc_kmajor(s_phq, kTile, 0, s), desc_mnmajor(s_ones, kTile, 0, s),
-                   id_n1, s > 0);
+          mma_bf16(tbase + lay.t_num + D, desc_kmajor(s_phq, kTile, 0, s), desc_n16(s_ones, s), id_n1, s > 0);
         }
         mma_commit(mma_bar);
       }
@@ -364,7 +382,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nh == 2 && ch != b) continue;
         const int f = 128 * b + row;
         if (f >= M) continue;
-        const int ncols = D + 16;
         const int c_lo = (nh == 2) ? 0 : (ch == 0 ? 0 : (ncols / 32) * 16);
         const int c_hi = (nh == 2) ? ncols : (ch == 0 ? (ncols / 32) * 16 : ncols);
         for (int c = c_lo; c < c_hi; c += 16) {
@@ -385,21 +402,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (MODE == MODE_STATE) {
-    // segment total of R' -> fp32 [M][D + 1]
-    float *out = p.states + ((size_t)bh * p.P + seg) * (size_t)M * DP;
+    // segment total of R' -> fp32 [M][D + 1], high and low parts
+    const size_t off = ((size_t)bh * p.P + seg) * (size_t)M * DP;
     for (int b = 0; b < nh; ++b) {
-      if (nh == 2 && ch != b) continue;
       const int f = 128 * b + row;
-      const int ncols = D + 16;
-      const int c_lo = (nh == 2) ? 0 : (ch == 0 ? 0 : (ncols / 32) * 16);
-      const int c_hi = (nh == 2) ? ncols : (ch == 0 ? (ncols / 32) * 16 : ncols);
-      for (int c = c_lo; c < c_hi; c += 16) {
-        float v[16];
-        tmem_ld16(tmem_addr(tbase, 32 * q4, lay.t_r + b * (D + 16) + c), v);
+      for (int c = ch ? csplit : 0; c < (ch ? ncols : csplit); c += 16) {
+        float h[16], l[16];
+        tmem_ld16(tmem_addr(tbase, 32 * q4, lay.s_hi + b * ncols + c), h);
+        tmem_ld16(tmem_addr(tbase, 32 * q4, lay.s_lo + b * ncols + c), l);
         if (f < M) {
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            if (c + i <= D) out[(size_t)f * DP + c + i] = v[i];
+            if (c + i <= D) {
+              p.states[off + (size_t)f * DP + c + i] = h[i];
+              p.states_lo[off + (size_t)f * DP + c + i] = l[i];
+            }
         }
       }
     }
@@ -416,6 +433,7 @@ cudaError_t launch(const Plan &pl, const Args &a, const CUtensorMap &mq, const C
   p.y = static_cast<__nv_bfloat16 *>(a.y);
   p.w = a.w;
   p.states = a.ws + pl.states_off;
+  p.states_lo = a.ws + pl.states_lo_off;
   p.status = a.status;
   const Layout<D> lay(pl.M, FAVOR);
   const int smem = (int)lay.total + 1024;
@@ -426,6 +444,24 @@ cudaError_t launch(const Plan &pl, const Args &a, const CUtensorMap &mq, const C
   return cudaGetLastError();
 }
 
+// Totals of R' over the first nseg segments, then their inclusive scan:
+// states[s] = R' at the end of segment s.
+template <int D, bool FAVOR>
+cudaError_t segment_states(const Plan &pl, const Args &a, const CUtensorMap &mq,
+                           const CUtensorMap &mk, const CUtensorMap &mv, int nseg, cudaStream_t st) {
+  cudaError_t e;
+  {
+    ProfScope ps("tc_segment_state", st);
+    e = launch<D, FAVOR, MODE_STATE>(pl, a, mq, mk, mv, nseg, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (nseg > 1) {
+    ProfScope ps("scan_states", st);
+    e = scan_states_df(pl, a.ws + pl.states_off, a.ws + pl.states_lo_off, nseg, st);
+  }
+  return e;
+}
+
 template <int D, bool FAVOR>
 cudaError_t forward_family(const Plan &pl, const Args &a, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
@@ -434,13 +470,7 @@ cudaError_t forward_family(const Plan &pl, const Args &a, cudaStream_t st) {
     return cudaErrorInvalidValue;
   cudaError_t e;
   if (pl.P > 1) {
-    {
-      ProfScope ps("tc_segment_state", st);
-      e = launch<D, FAVOR, MODE_STATE>(pl, a, mq, mk, mv, pl.P - 1, st);
-      if (e != cudaSuccess) return e;
-    }
-    ProfScope ps("scan_states", st);
-    e = scan_states_f32(pl, a.ws + pl.states_off, pl.P - 1, st);
+    e = segment_states<D, FAVOR>(pl, a, mq, mk, mv, pl.P - 1, st);
     if (e != cudaSuccess) return e;
   }
   ProfScope ps("tc_forward", st);
@@ -459,6 +489,17 @@ bool tc_forward_supported(int d, int M, int chunk, bool favor) {
   if (d == 64) return favor ? (M == 64 || M == 128 || M == 256) : M == 64;
   if (d == 128) return !favor && M == 128;
   return false;
+}
+
+cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, cudaStream_t st) {
+  CUtensorMap mk, mv;
+  const int d = p.d;
+  if (!make_map_bf16_3d(&mk, a.k, p.BH, p.L, d, tcf::kTile) || !make_map_bf16_3d(&mv, a.v, p.BH, p.L, d, tcf::kTile))
+    return cudaErrorInvalidValue;
+  if (d == 64 && p.favor) return tcf::segment_states<64, true>(p, a, mk, mk, mv, nseg, st);
+  if (d == 64) return tcf::segment_states<64, false>(p, a, mk, mk, mv, nseg, st);
+  if (d == 128 && !p.favor) return tcf::segment_states<128, false>(p, a, mk, mk, mv, nseg, st);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t tc_forward(const Plan &p, const Args &a, cudaStream_t st) {

@@ -151,6 +151,77 @@ def test_tensor_core_forward_is_used_and_matches(case, _lib):
     check("Y", _np(y), y_ref, TOL[torch.bfloat16])
 
 
+TC_BWD_SHAPES = [
+    # (B, H, L, d, M, C, feature): shapes the tensor-core backward takes
+    (2, 2, 1000, 64, 128, 64, "favor"),
+    (1, 1, 1500, 64, 64, 256, "favor"),
+    (1, 2, 333, 64, 64, 128, "elu"),
+    (1, 3, 128, 64, 128, 128, "favor"),   # exactly one tile
+    (1, 2, 129, 64, 64, 128, "favor"),    # one tile + a 1-row tail
+]
+
+
+def _run_profiled(_lib, fn):
+    _lib.profile_reset()
+    _lib.profile_enable(True)
+    try:
+        out = fn()
+        _lib.sync_status()
+        names = set(_lib.profile_read())
+    finally:
+        _lib.profile_enable(False)
+    return out, names
+
+
+@pytest.mark.parametrize("case", TC_BWD_SHAPES, ids=lambda c: "x".join(map(str, c)))
+def test_tensor_core_backward_is_used_and_matches(case, _lib):
+    B, H, L, d, M, C, feature = case
+    q, k, v, dy, w = small_case(B, H, L, d, M, C, torch.bfloat16, feature, seed=9)
+    (dq, dk, dv, _), names = _run_profiled(_lib, lambda: _lib.slim_attn_bwd(q, k, v, w, dy, C))
+    assert "tc_backward" in names, names
+    qn, kn, vn, dyn, wn = _np(q), _np(k), _np(v), _np(dy), _wnp(w)
+    ref = oracle.recurrence_backward(qn, kn, vn, wn, dyn, want_dw=False)
+    floor = 1e-2 * float(np.linalg.norm(dyn.ravel()))
+    for name, got, exp in (("dQ", dq, ref[0]), ("dK", dk, ref[1]), ("dV", dv, ref[2])):
+        check(name, _np(got), exp, TOL[torch.bfloat16], floor)
+
+
+@pytest.mark.parametrize("segments", [1, 2, 3, 6])
+def test_tensor_core_backward_segments(segments, _lib):
+    """Segments > 1 exercise the correction of dK, dV by the later segments' G."""
+    q, k, v, dy, w = small_case(1, 2, 1300, 64, 128, 128, torch.bfloat16, "favor", seed=10)
+    _lib.set_option(_lib.OPT_SEGMENTS, segments)
+    try:
+        (dq, dk, dv, _), names = _run_profiled(_lib, lambda: _lib.slim_attn_bwd(q, k, v, w, dy, 128))
+    finally:
+        _lib.set_option(_lib.OPT_SEGMENTS, 0)
+    assert "tc_backward" in names
+    if segments > 1:
+        assert "tc_backward_fix" in names
+    ref = oracle.recurrence_backward(_np(q), _np(k), _np(v), _wnp(w), _np(dy), want_dw=False)
+    for name, got, exp in (("dQ", dq, ref[0]), ("dK", dk, ref[1]), ("dV", dv, ref[2])):
+        check(name, _np(got), exp, TOL[torch.bfloat16])
+
+
+def test_tensor_core_backward_long_reversal(_lib):
+    """One segment of 160 tiles: the backward removes each tile's state
+    increment in turn (eq. (19)); the double-float state keeps the early
+    tiles' small states exact."""
+    q, k, v, dy, w = small_case(1, 1, 160 * 128, 64, 64, 128, torch.bfloat16, "favor", seed=11)
+    _lib.set_option(_lib.OPT_SEGMENTS, 1)
+    try:
+        (dq, dk, dv, _), names = _run_profiled(_lib, lambda: _lib.slim_attn_bwd(q, k, v, w, dy, 128))
+    finally:
+        _lib.set_option(_lib.OPT_SEGMENTS, 0)
+    assert "tc_backward" in names
+    ref = oracle.recurrence_backward(_np(q), _np(k), _np(v), _wnp(w), _np(dy), want_dw=False)
+    for name, got, exp in (("dQ", dq, ref[0]), ("dK", dk, ref[1]), ("dV", dv, ref[2])):
+        check(name, _np(got), exp, TOL[torch.bfloat16])
+    # the first tile, where the recovered state is smallest relative to the total
+    for name, got, exp in (("dQ[:128]", dq, ref[0]), ("dK[:128]", dk, ref[1])):
+        check(name, _np(got)[..., :128, :], exp[..., :128, :], TOL[torch.bfloat16])
+
+
 @pytest.mark.parametrize("segments", [1, 2, 3, 5])
 def test_tensor_core_segments(segments, _lib):
     q, k, v, dy, w = small_case(1, 2, 1100, 64, 256, 128, torch.bfloat16, "favor", seed=8)
@@ -164,18 +235,21 @@ def test_tensor_core_segments(segments, _lib):
     check("Y", _np(y), y_ref, TOL[torch.bfloat16])
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
-def test_single_row(dtype):
+@pytest.mark.parametrize("dtype,d,M,C", [(torch.float32, 16, 32, 16), (torch.bfloat16, 16, 32, 16),
+                                         (torch.bfloat16, 64, 128, 64)],
+                         ids=["fp32", "bf16", "bf16-tensor-core"])
+def test_single_row(dtype, d, M, C):
     """L = 1: Y_1 = V_1, dV_1 = dY_1, and dQ = dK = dW = 0 (Y_1 does not depend
     on Q or K), so only rounding noise may remain there."""
-    q, k, v, dy, w = small_case(2, 3, 1, 16, 32, 16, dtype, "favor", seed=6)
-    y, dq, dk, dv, dw = run_library(q, k, v, w, dy, 16)
+    q, k, v, dy, w = small_case(2, 3, 1, d, M, C, dtype, "favor", seed=6)
+    y, dq, dk, dv, dw = run_library(q, k, v, w, dy, C, want_dw=(d == 16))
     tol = TOL[dtype]
     check("Y", _np(y), _np(v), tol)
     check("dV", _np(dv), _np(dy), tol)
     scale = float(np.linalg.norm(_np(dy).ravel())) * (1.0 + float(np.linalg.norm(_np(w))))
     for name, t in (("dQ", dq), ("dK", dk), ("dW", dw)):
-        assert float(np.linalg.norm(_np(t).ravel())) <= tol * scale, name
+        if t is not None:
+            assert float(np.linalg.norm(_np(t).ravel())) <= tol * scale, name
 
 
 @pytest.mark.parametrize("segments", [1, 2, 3, 7])
