@@ -45,7 +45,7 @@ struct Params {
 
 struct Layout {
   uint32_t w, q, k, v, dy, phq, phk, at, dn, rb, ones, ddb;
-  uint32_t s_f, gs_f, den_a, den_b, dd, usq, usk, dot, bars, total;
+  uint32_t s_f, gs_f, den_a, den_b, dd, usq, usk, dot, rx_den, rx_usq, rx_usk, bars, total;
   __host__ __device__ explicit Layout(int MC) {
     uint32_t o = 0;
     const uint32_t tile = kTile * D * 2;
@@ -69,6 +69,9 @@ struct Layout {
     usq = o; o += 2 * kTile * 4;
     usk = o; o += 2 * kTile * 4;
     dot = o; o += 2 * kTile * 4;
+    rx_den = o; o += 64 * 4;  // cluster exchange: partner's partials for my rows
+    rx_usq = o; o += 64 * 4;
+    rx_usk = o; o += 64 * 4;
     bars = o; o += 64;
     total = o;
   }
@@ -111,7 +114,14 @@ __device__ __forceinline__ void state_to_smem(uint32_t tbase, uint32_t col, uint
   }
 }
 
-template <bool FAVOR>
+// CS = 1: one CTA per segment holds all M <= 128 features.
+// CS = 2: a cluster of two CTAs per segment; CTA c owns features
+// [128c, 128c + 128) with their R' and G, computes every per-feature term
+// locally, and the two exchange through distributed shared memory the
+// cross-feature sums (num, den; dV, dQ, dK, rowsum(u)) for the 64 rows each
+// owns, plus dN' so both hold it.  Exchange buffers reuse tiles that are
+// provably idle at that point (cluster barriers mark those points).
+template <bool FAVOR, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDY,
@@ -119,13 +129,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem =
       reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int MC = p.M;  // features per CTA (<= 128)
+  const int MC = p.M / CS;  // features per CTA (<= 128)
   const Layout lay(MC);
   const uint32_t sb = smem_u32(smem);
   uint64_t *in_bar = reinterpret_cast<uint64_t *>(smem + lay.bars);
   uint64_t *mma_bar = in_bar + 1;
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(in_bar + 2);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(in_bar + 3);
+  uint64_t *rl_bar = in_bar + 2;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(in_bar + 3);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(in_bar + 4);
+  float *rx_den = reinterpret_cast<float *>(smem + lay.rx_den);
+  float *rx_usq = reinterpret_cast<float *>(smem + lay.rx_usq);
+  float *rx_usk = reinterpret_cast<float *>(smem + lay.rx_usk);
   float *s_f = reinterpret_cast<float *>(smem + lay.s_f);
   float *gs_f = reinterpret_cast<float *>(smem + lay.gs_f);
   float *den_a = reinterpret_cast<float *>(smem + lay.den_a);
@@ -137,14 +151,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q4 = warp & 3, ch = warp >> 2, row = 32 * q4 + lane;
-  const int seg = blockIdx.x, bh = blockIdx.y;
+  const int rank = CS == 2 ? (int)cluster_rank() : 0, peer = 1 - rank;
+  const int seg = blockIdx.x / CS, bh = blockIdx.y;
   const int M = p.M, DP = D + 1;
+  const int fbase = rank * MC;  // first feature of this CTA
   const int t0 = seg * p.tps, t1 = min(t0 + p.tps, p.nt);
   const int half = MC / 2;  // feature columns per thread (two threads per row)
+  const bool own = CS == 1 || (row >> 6) == rank;  // rows this CTA finalises
 
   if (tid == 0) {
     mbar_init(in_bar, 1);
     mbar_init(mma_bar, 1);
+    mbar_init(rl_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -153,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (FAVOR) {
     for (int idx = tid; idx < MC * D; idx += kThreads) {
       const int i = idx / MC, m = idx - i * MC;
-      st_bf16_scalar(smem, lay.w + sw128_offset(m, i, MC), p.w[(size_t)i * M + m]);
+      st_bf16_scalar(smem, lay.w + sw128_offset(m, i, MC), p.w[(size_t)i * M + fbase + m]);
     }
   }
   for (int idx = tid; idx < kTile * 16; idx += kThreads) {
@@ -172,6 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (CS == 2) cluster_sync();  // the peer is running before any remote store
   tc_fence_after();
   const uint32_t tb = *tslot;
 
@@ -185,8 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 16; ++i) {
         const int e = c + i;
         const bool in = f < MC && e <= D;
-        h[i] = in ? p.states[off + (size_t)f * DP + e] : 0.f;
-        l[i] = in ? p.states_lo[off + (size_t)f * DP + e] : 0.f;
+        h[i] = in ? p.states[off + (size_t)(fbase + f) * DP + e] : 0.f;
+        l[i] = in ? p.states_lo[off + (size_t)(fbase + f) * DP + e] : 0.f;
         z[i] = 0.f;
       }
       tmem_st16(tmem_addr(tb, 32 * q4, kRhi + c), h);
@@ -205,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_at = sb + lay.at, s_dn = sb + lay.dn, s_rb = sb + lay.rb;
   const uint32_t s_ones = sb + lay.ones, s_ddb = sb + lay.ddb;
   const uint32_t tile_bytes = kTile * D * 2;
-  uint32_t in_phase = 0, mma_phase = 0;
+  uint32_t in_phase = 0, mma_phase = 0, rl_phase = 0;
 
   auto issue_in = [&](int t) {
     mbar_arrive_expect_tx(in_bar, 4 * tile_bytes);
@@ -358,31 +377,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     wait_mma();
     {
-      const float den = den_a[row] + den_a[kTile + row] + den_b[row] + den_b[kTile + row];
-      const float inv = 1.0f / den;
+      float den = den_a[row] + den_a[kTile + row] + den_b[row] + den_b[kTile + row];
       float v[32], g[32];
       tmem_ld32(tmem_addr(tb, 32 * q4, kT + 32 * ch), v);
+      if (CS == 2) {
+        // both CTAs are past their features: the peer's Q tile is idle and
+        // takes my partial num and den for the rows it owns
+        cluster_sync();
+        if (!own) {
+          const uint32_t dst = map_peer(s_q + (uint32_t)(((row - 64 * peer) * 64 + 32 * ch) * 4), peer);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) st_peer_v4(dst + 16 * j, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          if (ch == 0) st_peer_f32(map_peer(sb + lay.rx_den + (row - 64 * peer) * 4, peer), den);
+        }
+        cluster_sync();
+        if (own) {
+          float r[32];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) ld_shared_v4f(s_q + (uint32_t)(((row - 64 * rank) * 64 + 32 * ch + 4 * j) * 4), r + 4 * j);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] += r[i];
+          den += rx_den[row - 64 * rank];
+        }
+      }
+      const float inv = 1.0f / den;
       float dyy = 0.f;
+      if (own) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        ld_bf16x8(s_dy + sw128_offset(row, 32 * ch + 8 * j, kTile), g + 8 * j);
+        for (int j = 0; j < 4; ++j) ld_bf16x8(s_dy + sw128_offset(row, 32 * ch + 8 * j, kTile), g + 8 * j);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float y = v[i] * inv;
+          dyy = fmaf(g[i], y, dyy);
+          g[i] = live ? g[i] * inv : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t off = sw128_offset(row, 32 * ch + 8 * j, kTile);
+          st_bf16x8(s_dn + off, g + 8 * j);
+          if (CS == 2)
+            st_peer_v4u(map_peer(s_dn + off, peer), pack_bf16(g[8 * j], g[8 * j + 1]),
+                        pack_bf16(g[8 * j + 2], g[8 * j + 3]), pack_bf16(g[8 * j + 4], g[8 * j + 5]),
+                        pack_bf16(g[8 * j + 6], g[8 * j + 7]));
+        }
+        dot[ch * kTile + row] = dyy;
       }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float y = v[i] * inv;
-        dyy = fmaf(g[i], y, dyy);
-        g[i] = live ? g[i] * inv : 0.f;
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) st_bf16x8(s_dn + sw128_offset(row, 32 * ch + 8 * j, kTile), g + 8 * j);
-      dot[ch * kTile + row] = dyy;
       __syncthreads();
-      if (ch == 0) {
+      if (own && ch == 0) {
         const float dval = live ? -(dot[row] + dot[kTile + row]) * inv : 0.f;
         dd[row] = dval;
         st_bf16_scalar(smem, lay.ddb + n16_offset(row, 0), dval);
+        if (CS == 2) {
+          st_peer_f32(map_peer(sb + lay.dd + row * 4, peer), dval);
+          const __nv_bfloat16 hb = __float2bfloat16_rn(dval);
+          st_peer_b16(map_peer(s_ddb + n16_offset(row, 0), peer), *reinterpret_cast<const uint16_t *>(&hb));
+        }
       }
     }
+    if (CS == 2) cluster_sync();  // dN', dD of all 128 rows present in both CTAs
     cta_sync();  // dY consumed: its buffer now takes the bf16 copy of G_V
     state_to_smem(tb, kG, kG, q4, ch, row, MC, s_dy, gs_f);
     fence_async_smem();
@@ -414,7 +466,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float v[32];
       tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * ch), v);
-      if (live) {
+      if (CS == 2) {
+        // park this CTA's dV partial (fp32 [128][64]) in the idle Q/K tiles
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          st_shared_v4(s_q + (uint32_t)((row * 64 + 32 * ch + 4 * j) * 4), __float_as_uint(v[4 * j]),
+                       __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+      } else if (live) {
         uint4 *dst = reinterpret_cast<uint4 *>(p.dv + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -447,6 +505,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_done();
     }
     wait_mma();
+    if (CS == 2) {
+      // V, dN, R and G copies and the dA tile are idle in both CTAs from here:
+      // bring Q and K back (into the dA tile) for the dQ, dK epilogue
+      cluster_sync();
+      if (tid == 0) {
+        mbar_arrive_expect_tx(rl_bar, 2 * tile_bytes);
+        tma_load_3d(smem + lay.at, &tmQ, rl_bar, 0, t * kTile, bh);
+        tma_load_3d(smem + lay.at + tile_bytes, &tmK, rl_bar, 0, t * kTile, bh);
+      }
+    }
 
     // (i) u = phi * dphi (in place over phi), row sums; elu+1 writes dQ, dK here
     {
@@ -512,18 +580,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_done();
       }
       wait_mma();
-      const float sq = usq[row] + usq[kTile + row], sk = usk[row] + usk[kTile + row];
+      float sq = usq[row] + usq[kTile + row], sk = usk[row] + usk[kTile + row];
       float a[32], b[32];
       tmem_ld32(tmem_addr(tb, 32 * q4, kT + 32 * ch), a);
       tmem_ld32(tmem_addr(tb, 32 * q4, kT + 64 + 32 * ch), b);
-      if (live) {
+      uint32_t s_xq = s_q, s_xk = s_k;
+      if (CS == 2) {
+        // exchange 2: my partials of the peer's rows go to its idle V (dV),
+        // dN (dQ) and R-copy (dK) tiles, fp32 [64][64] each
+        float c3[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ld_shared_v4f(s_q + (uint32_t)((row * 64 + 32 * ch + 4 * j) * 4), c3 + 4 * j);
+        if (!own) {
+          const uint32_t o = (uint32_t)(((row - 64 * peer) * 64 + 32 * ch) * 4);
+          const uint32_t dv_dst = map_peer(s_v + o, peer), dq_dst = map_peer(s_dn + o, peer);
+          const uint32_t dk_dst = map_peer(s_rb + o, peer);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            st_peer_v4(dv_dst + 16 * j, c3[4 * j], c3[4 * j + 1], c3[4 * j + 2], c3[4 * j + 3]);
+            st_peer_v4(dq_dst + 16 * j, a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]);
+            st_peer_v4(dk_dst + 16 * j, b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]);
+          }
+          if (ch == 0) {
+            st_peer_f32(map_peer(sb + lay.rx_usq + (row - 64 * peer) * 4, peer), sq);
+            st_peer_f32(map_peer(sb + lay.rx_usk + (row - 64 * peer) * 4, peer), sk);
+          }
+        }
+        cluster_sync();
+        if (own) {
+          const uint32_t o = (uint32_t)(((row - 64 * rank) * 64 + 32 * ch) * 4);
+          float r[32];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) ld_shared_v4f(s_v + o + 16 * j, r + 4 * j);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) c3[i] += r[i];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) ld_shared_v4f(s_dn + o + 16 * j, r + 4 * j);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a[i] += r[i];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) ld_shared_v4f(s_rb + o + 16 * j, r + 4 * j);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) b[i] += r[i];
+          sq += rx_usq[row - 64 * rank];
+          sk += rx_usk[row - 64 * rank];
+          if (live) {
+            uint4 *dst = reinterpret_cast<uint4 *>(p.dv + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_uint4(pack_bf16(c3[8 * j], c3[8 * j + 1]), pack_bf16(c3[8 * j + 2], c3[8 * j + 3]),
+                                  pack_bf16(c3[8 * j + 4], c3[8 * j + 5]), pack_bf16(c3[8 * j + 6], c3[8 * j + 7]));
+          }
+        }
+        mbar_wait(rl_bar, rl_phase, p.status, abort_flag);
+        rl_phase ^= 1;
+        s_xq = sb + lay.at;
+        s_xk = sb + lay.at + tile_bytes;
+      }
+      if (live && own) {
         uint4 *gq = reinterpret_cast<uint4 *>(p.dq + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch);
         uint4 *gk = reinterpret_cast<uint4 *>(p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           float xq[8], xk[8];
-          ld_bf16x8(s_q + sw128_offset(row, 32 * ch + 8 * j, kTile), xq);
-          ld_bf16x8(s_k + sw128_offset(row, 32 * ch + 8 * j, kTile), xk);
+          ld_bf16x8(s_xq + sw128_offset(row, 32 * ch + 8 * j, kTile), xq);
+          ld_bf16x8(s_xk + sw128_offset(row, 32 * ch + 8 * j, kTile), xk);
           float oq[8], ok[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -551,16 +672,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (f < MC) {
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          if (c + i <= D) out[(size_t)f * DP + c + i] = v[i];
+          if (c + i <= D) out[(size_t)(fbase + f) * DP + c + i] = v[i];
       }
     }
   }
   cta_sync();
+  if (CS == 2) cluster_sync();  // no remote store may target an exited CTA
   if (warp == 0) tmem_dealloc(tb, 512);
 }
 
 // Correction: add G_end(s) (the G of every later segment) to dK and dV of
-// segment s:  dphi_k += V G_V^T + 1 G_S^T,  dV += phi_k G_V^T.
+// segment s:  dphi_k += V G_V^T + 1 G_S^T,  dV += phi_k G_V^T, one 128-feature
+// block at a time (every term is a sum over features).
+struct FixLayout {
+  uint32_t w, k, v, phk, gb, gs, usk, bars, total;
+  __host__ __device__ explicit FixLayout(int M) {
+    uint32_t o = 0;
+    const uint32_t tile = kTile * D * 2;
+    w = o; o += (uint32_t)M * 128u;   // W^T as [M][64]
+    k = o; o += tile;
+    v = o; o += tile;
+    phk = o; o += kTile * 256;
+    gb = o; o += (uint32_t)M * 128u;  // G_end(s)[0:d] as bf16 [M][64]
+    gs = o; o += (uint32_t)M * 4u;    // G_end(s)[d] (fp32)
+    usk = o; o += 2 * kTile * 4;
+    bars = o; o += 64;
+    total = o;
+  }
+};
+
 template <bool FAVOR>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_fix_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -568,22 +708,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem =
       reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int MC = p.M;
-  const Layout lay(MC);  // reuses the main kernel's regions
+  const int M = p.M, DP = D + 1;
+  const int nb = (M + 127) / 128, MB = M < 128 ? M : 128;  // feature blocks and their width
+  const FixLayout lay(M);
   const uint32_t sb = smem_u32(smem);
   uint64_t *in_bar = reinterpret_cast<uint64_t *>(smem + lay.bars);
   uint64_t *mma_bar = in_bar + 1;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(in_bar + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(in_bar + 3);
-  float *gs_f = reinterpret_cast<float *>(smem + lay.gs_f);
+  float *gs_f = reinterpret_cast<float *>(smem + lay.gs);
   float *usk = reinterpret_cast<float *>(smem + lay.usk);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q4 = warp & 3, ch = warp >> 2, row = 32 * q4 + lane;
   const int seg = blockIdx.x, bh = blockIdx.y;
-  const int M = p.M, DP = D + 1;
   const int t0 = seg * p.tps, t1 = min(t0 + p.tps, p.nt);
-  const int half = MC / 2;
+  const int half = MB / 2;
 
   if (tid == 0) {
     mbar_init(in_bar, 1);
@@ -593,19 +733,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 0) tmem_alloc(tslot, 512);
   if (FAVOR) {
-    for (int idx = tid; idx < MC * D; idx += kThreads) {
-      const int i = idx / MC, m = idx - i * MC;
-      st_bf16_scalar(smem, lay.w + sw128_offset(m, i, MC), p.w[(size_t)i * M + m]);
+    for (int idx = tid; idx < M * D; idx += kThreads) {
+      const int i = idx / M, m = idx - i * M;
+      st_bf16_scalar(smem, lay.w + sw128_offset(m, i, M), p.w[idx]);
     }
   }
-  // G_end(s) = gstates[s + 1] after the reverse scan -> bf16 [MC][64] + G_S
   {
     const float *g = p.gstates + ((size_t)bh * p.P + seg + 1) * (size_t)M * DP;
-    for (int idx = tid; idx < MC * D; idx += kThreads) {
+    for (int idx = tid; idx < M * D; idx += kThreads) {
       const int f = idx / D, e = idx - f * D;
-      st_bf16_scalar(smem, lay.rb + sw128_offset(f, e, MC), g[(size_t)f * DP + e]);
+      st_bf16_scalar(smem, lay.gb + sw128_offset(f, e, M), g[(size_t)f * DP + e]);
     }
-    for (int f = tid; f < MC; f += kThreads) gs_f[f] = g[(size_t)f * DP + D];
+    for (int f = tid; f < M; f += kThreads) gs_f[f] = g[(size_t)f * DP + D];
+  }
+  if (MB < 128) {
+    for (int idx = tid; idx < kTile * 128; idx += kThreads) {
+      const int r = idx >> 7, x = idx & 127;
+      if (x >= MB) st_bf16_scalar(smem, lay.phk + sw128_offset(r, x, kTile), 0.f);
+    }
   }
   fence_async_smem();
   tc_fence_before();
@@ -613,8 +758,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tb = *tslot;
   const uint32_t s_w = sb + lay.w, s_k = sb + lay.k, s_v = sb + lay.v, s_phk = sb + lay.phk;
-  const uint32_t s_gb = sb + lay.rb;
+  const uint32_t s_gb = sb + lay.gb;
   const uint32_t tile_bytes = kTile * D * 2;
+  constexpr uint32_t kF = 0, kDV = 128, kDK = 192;  // TMEM columns
   uint32_t in_phase = 0, mma_phase = 0;
   auto wait_mma = [&]() {
     __syncwarp();
@@ -638,93 +784,99 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_wait(in_bar, in_phase, p.status, abort_flag);
     in_phase ^= 1;
-    float ck = 0.f;
-    if (FAVOR) {
-      ck = favor_row_const(tile_row_sqnorm(s_k, row, D), M);
+    const float ck = FAVOR ? favor_row_const(tile_row_sqnorm(s_k, row, D), M) : 0.f;
+    float uk = 0.f;
+    for (int b = 0; b < nb; ++b) {
+      if (FAVOR) {
+        if (tid == 0) {
+          const uint32_t id = make_idesc(128, MB, false, false);
+          for (int s = 0; s < D / 16; ++s)
+            mma_bf16(tb + kF, desc_kmajor(s_k, kTile, 0, s), desc_kmajor(s_w, M, 128 * b, s), id, s > 0);
+          mma_commit(mma_bar);
+        }
+        wait_mma();
+        for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 32) {
+          float v[32];
+          tmem_ld32(tmem_addr(tb, 32 * q4, kF + c0), v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = live ? favor_feature(v[i], ck) : 0.f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) st_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
+        }
+      } else {
+        for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 8) {
+          float v[8];
+          ld_bf16x8(s_k + sw128_offset(row, c0, kTile), v);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = live ? elu1_feature(v[i]) : 0.f;
+          st_bf16x8(s_phk + sw128_offset(row, c0, kTile), v);
+        }
+      }
+      fence_async_smem();
+      cta_sync();
+      // dphi_k' = V G_V^T -> F ; dV' += phi_k G_V^T -> DV
       if (tid == 0) {
-        const uint32_t id = make_idesc(128, MC, false, false);
+        const uint32_t id1 = make_idesc(128, MB, false, false);
         for (int s = 0; s < D / 16; ++s)
-          mma_bf16(tb + kT, desc_kmajor(s_k, kTile, 0, s), desc_kmajor(s_w, MC, 0, s), id, s > 0);
+          mma_bf16(tb + kF, desc_kmajor(s_v, kTile, 0, s), desc_kmajor(s_gb, M, 128 * b, s), id1, s > 0);
+        const uint32_t id2 = make_idesc(128, D, false, true);
+        for (int s = 0; s < MB / 16; ++s)
+          mma_bf16(tb + kDV, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_gb, M, 0, 8 * b + s), id2,
+                   (b > 0 || s > 0));
         mma_commit(mma_bar);
       }
       wait_mma();
       for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 32) {
-        float v[32];
-        tmem_ld32(tmem_addr(tb, 32 * q4, kT + c0), v);
+        float x[32];
+        tmem_ld32(tmem_addr(tb, 32 * q4, kF + c0), x);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = live ? favor_feature(v[i], ck) : 0.f;
+        for (int j = 0; j < 4; ++j) {
+          float fk[8];
+          ld_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), fk);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) st_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
-      }
-    } else {
-      for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 8) {
-        float v[8];
-        ld_bf16x8(s_k + sw128_offset(row, c0, kTile), v);
+          for (int i = 0; i < 8; ++i) {
+            const float dk = x[8 * j + i] + gs_f[128 * b + c0 + 8 * j + i];
+            x[8 * j + i] = FAVOR ? fk[i] * dk : dk * fminf(fk[i], 1.f);
+            uk += x[8 * j + i];
+          }
+        }
+        if (FAVOR) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = live ? elu1_feature(v[i]) : 0.f;
-        st_bf16x8(s_phk + sw128_offset(row, c0, kTile), v);
-      }
-    }
-    fence_async_smem();
-    cta_sync();
-    // dphi_k' = V G_V^T -> T ; dV' = phi_k G_V^T -> X
-    if (tid == 0) {
-      const uint32_t id1 = make_idesc(128, MC, false, false);
-      for (int s = 0; s < D / 16; ++s)
-        mma_bf16(tb + kT, desc_kmajor(s_v, kTile, 0, s), desc_kmajor(s_gb, MC, 0, s), id1, s > 0);
-      const uint32_t id2 = make_idesc(128, D, false, true);
-      for (int s = 0; s < MC / 16; ++s)
-        mma_bf16(tb + kX, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_gb, MC, 0, s), id2, s > 0);
-      mma_commit(mma_bar);
-    }
-    wait_mma();
-    float uk = 0.f;
-    for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 32) {
-      float b[32];
-      tmem_ld32(tmem_addr(tb, 32 * q4, kT + c0), b);
+          for (int j = 0; j < 4; ++j) st_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), x + 8 * j);
+        } else if (live) {
+          __nv_bfloat16 *gk = p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + c0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float fk[8];
-        ld_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), fk);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float dk = b[8 * j + i] + gs_f[c0 + 8 * j + i];
-          b[8 * j + i] = FAVOR ? fk[i] * dk : dk * fminf(fk[i], 1.f);
-          uk += b[8 * j + i];
+          for (int i = 0; i < 32; ++i) gk[i] = __float2bfloat16_rn(__bfloat162float(gk[i]) + x[i]);
         }
       }
+      fence_async_smem();
+      cta_sync();
       if (FAVOR) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) st_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), b + 8 * j);
-      } else if (live) {
-        __nv_bfloat16 *gk = p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + c0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) gk[i] = __float2bfloat16_rn(__bfloat162float(gk[i]) + b[i]);
+        if (tid == 0) {
+          const uint32_t id = make_idesc(128, D, false, true);
+          for (int s = 0; s < MB / 16; ++s)
+            mma_bf16(tb + kDK, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_w, M, 0, 8 * b + s), id,
+                     (b > 0 || s > 0));
+          mma_commit(mma_bar);
+        }
+        wait_mma();  // phi_k is overwritten by the next block's features
       }
     }
     usk[ch * kTile + row] = uk;
+    __syncthreads();
     {
       float v[32];
-      tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * ch), v);
+      tmem_ld32(tmem_addr(tb, 32 * q4, kDV + 32 * ch), v);
       if (live) {
         __nv_bfloat16 *gv = p.dv + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch;
 #pragma unroll
         for (int i = 0; i < 32; ++i) gv[i] = __float2bfloat16_rn(__bfloat162float(gv[i]) + v[i]);
       }
     }
-    fence_async_smem();
-    cta_sync();
     if (FAVOR) {
-      if (tid == 0) {
-        const uint32_t id = make_idesc(128, D, false, true);
-        for (int s = 0; s < MC / 16; ++s)
-          mma_bf16(tb + kX, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_w, MC, 0, s), id, s > 0);
-        mma_commit(mma_bar);
-      }
-      wait_mma();
       const float sk = usk[row] + usk[kTile + row];
       float b[32];
-      tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * ch), b);
+      tmem_ld32(tmem_addr(tb, 32 * q4, kDK + 32 * ch), b);
       if (live) {
         __nv_bfloat16 *gk = p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch;
 #pragma unroll
@@ -745,7 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_dealloc(tb, 512);
 }
 
-template <bool FAVOR>
+template <bool FAVOR, int CS>
 cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mdy;
   if (!make_map_bf16_3d(&mq, a.q, pl.BH, pl.L, D, kTile) || !make_map_bf16_3d(&mk, a.k, pl.BH, pl.L, D, kTile) ||
@@ -763,15 +915,30 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
   p.states_lo = a.ws + pl.states_lo_off;
   p.gstates = a.ws + pl.gstates_off;
   p.status = a.status;
-  const Layout lay(pl.M);
-  const int smem = (int)lay.total + 1024;
   {
-    auto kern = tc_bwd_kernel<FAVOR>;
+    const Layout lay(pl.M / CS);
+    const int smem = (int)lay.total + 1024;
+    auto kern = tc_bwd_kernel<FAVOR, CS>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    if (CS > 1) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      (void)e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl.P * CS, pl.BH);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     ProfScope ps("tc_backward", st);
-    kern<<<dim3(pl.P, pl.BH), kThreads, smem, st>>>(mq, mk, mv, mdy, p);
-    e = cudaGetLastError();
+    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mdy, p);
     if (e != cudaSuccess) return e;
   }
   if (pl.P > 1) {
@@ -781,6 +948,8 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
       e = scan_states_f32_rev(pl, a.ws + pl.gstates_off + (size_t)pl.M * (D + 1), pl.P - 1, st);
       if (e != cudaSuccess) return e;
     }
+    const FixLayout fl(pl.M);
+    const int smem = (int)fl.total + 1024;
     auto kern = tc_bwd_fix_kernel<FAVOR>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -795,14 +964,14 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
 
 bool tc_backward_supported(int d, int M, int chunk, bool favor) {
   if (chunk < 64 || d != 64) return false;
-  return favor ? (M == 64 || M == 128) : M == 64;
+  return favor ? (M == 64 || M == 128 || M == 256) : M == 64;
 }
-
-size_t tc_backward_smem_bytes(int M) { return tcb::Layout(M).total + 1024; }
 
 cudaError_t tc_backward(const Plan &p, const Args &a, cudaStream_t st) {
   if (p.d != 64) return cudaErrorInvalidValue;
-  return p.favor ? tcb::backward_family<true>(p, a, st) : tcb::backward_family<false>(p, a, st);
+  if (!p.favor) return tcb::backward_family<false, 1>(p, a, st);
+  if (p.M == 256) return tcb::backward_family<true, 2>(p, a, st);
+  return tcb::backward_family<true, 1>(p, a, st);
 }
 
 }  // namespace slim

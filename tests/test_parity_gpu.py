@@ -158,6 +158,8 @@ TC_BWD_SHAPES = [
     (1, 2, 333, 64, 64, 128, "elu"),
     (1, 3, 128, 64, 128, 128, "favor"),   # exactly one tile
     (1, 2, 129, 64, 64, 128, "favor"),    # one tile + a 1-row tail
+    (1, 2, 700, 64, 256, 128, "favor"),   # M = 256: a two-CTA cluster per segment
+    (2, 1, 300, 64, 256, 64, "favor"),
 ]
 
 
@@ -186,10 +188,11 @@ def test_tensor_core_backward_is_used_and_matches(case, _lib):
         check(name, _np(got), exp, TOL[torch.bfloat16], floor)
 
 
+@pytest.mark.parametrize("M", [128, 256])
 @pytest.mark.parametrize("segments", [1, 2, 3, 6])
-def test_tensor_core_backward_segments(segments, _lib):
+def test_tensor_core_backward_segments(segments, M, _lib):
     """Segments > 1 exercise the correction of dK, dV by the later segments' G."""
-    q, k, v, dy, w = small_case(1, 2, 1300, 64, 128, 128, torch.bfloat16, "favor", seed=10)
+    q, k, v, dy, w = small_case(1, 2, 1300, 64, M, 128, torch.bfloat16, "favor", seed=10)
     _lib.set_option(_lib.OPT_SEGMENTS, segments)
     try:
         (dq, dk, dv, _), names = _run_profiled(_lib, lambda: _lib.slim_attn_bwd(q, k, v, w, dy, 128))
