@@ -93,12 +93,35 @@ int device_sms() {
   return sms;
 }
 
-// Segments per (b, h): enough CTAs to cover every SM once, never more
-// segments than work units (chunks, or 128-row tiles on the tensor path), and
-// no empty segment.
-void choose_segments(Plan &p, int requested, int units) {
+// Segments per (b, h), never more than the work units (chunks, or 128-row
+// tiles on the tensor path) and with no empty segment.  The CUDA-core path
+// covers every SM once.  The tensor path runs one CTA per SM (cta_per_seg
+// CTAs per segment), so it picks the count with the shortest makespan,
+// waves x units per segment, preferring fewer segments on ties, and caps it
+// at 8 waves' worth so the boundary states stay a bounded workspace.
+void choose_segments(Plan &p, int requested, int units, int tensor_path, int cta_per_seg) {
   const int sms = device_sms();
-  int P = requested > 0 ? requested : (sms + p.BH - 1) / std::max(p.BH, 1);
+  const int bh = std::max(p.BH, 1);
+  int P;
+  if (requested > 0) {
+    P = requested;
+  } else if (!tensor_path) {
+    P = (sms + bh - 1) / bh;
+  } else {
+    const int cap = std::max(1, 8 * ((sms + bh * cta_per_seg - 1) / (bh * cta_per_seg)));
+    long long best = -1;
+    P = 1;
+    for (int cand = 1; cand <= std::min(units, cap); ++cand) {
+      const int cps = (units + cand - 1) / cand;
+      const int segs = (units + cps - 1) / cps;
+      const long long waves = ((long long)segs * bh * cta_per_seg + sms - 1) / sms;
+      const long long span = waves * cps;
+      if (best < 0 || span < best) {
+        best = span;
+        P = segs;
+      }
+    }
+  }
   P = std::max(1, std::min(P, units));
   p.cps = (units + P - 1) / P;
   p.P = (units + p.cps - 1) / p.cps;
@@ -115,7 +138,9 @@ Plan make_plan(int B, int H, int L, int d, int M, int chunk, bool favor, bool bw
   p.favor = favor ? 1 : 0;
   p.dp = d + 1;
   p.path = path;
-  choose_segments(p, g_opt_segments, path == 2 ? p.tc_tiles : p.nchunks);
+  // the backward of 256 random features runs each segment on a two-CTA cluster
+  const int cta_per_seg = (path == 2 && bwd && M > 128) ? 2 : 1;
+  choose_segments(p, g_opt_segments, path == 2 ? p.tc_tiles : p.nchunks, path == 2, cta_per_seg);
   // master states: fp64 on the CUDA-core path; double-float (hi, lo) fp32
   // pairs on the tensor path, whose reverse states are plain fp32
   const size_t state = (path == 2 ? 1 : 2) * (size_t)p.BH * p.P * p.dp * p.M;

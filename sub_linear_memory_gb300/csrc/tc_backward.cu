@@ -77,6 +77,11 @@ struct Layout {
   }
 };
 
+// fp32 exchange tiles are kept column-chunk-major, 4 floats per chunk:
+// element (r, 4c .. 4c+3) of an R-row tile sits at byte (c * R + r) * 16, so a
+// warp (consecutive rows, one chunk) touches consecutive 16-B words.
+__device__ __forceinline__ uint32_t xoff(int r, int c4, int R) { return (uint32_t)((c4 * R + r) * 16); }
+
 // TMEM columns: R' as a double-float (hi, lo) pair, G, two transients
 constexpr uint32_t kRhi = 0, kRlo = 80, kG = 160, kT = 240, kX = 368;
 
@@ -385,16 +390,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // takes my partial num and den for the rows it owns
         cluster_sync();
         if (!own) {
-          const uint32_t dst = map_peer(s_q + (uint32_t)(((row - 64 * peer) * 64 + 32 * ch) * 4), peer);
+          const uint32_t dst = map_peer(s_q, peer);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) st_peer_v4(dst + 16 * j, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          for (int j = 0; j < 8; ++j)
+            st_peer_v4(dst + xoff(row - 64 * peer, 8 * ch + j, 64), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
           if (ch == 0) st_peer_f32(map_peer(sb + lay.rx_den + (row - 64 * peer) * 4, peer), den);
         }
         cluster_sync();
         if (own) {
           float r[32];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) ld_shared_v4f(s_q + (uint32_t)(((row - 64 * rank) * 64 + 32 * ch + 4 * j) * 4), r + 4 * j);
+          for (int j = 0; j < 8; ++j) ld_shared_v4f(s_q + xoff(row - 64 * rank, 8 * ch + j, 64), r + 4 * j);
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] += r[i];
           den += rx_den[row - 64 * rank];
@@ -470,8 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // park this CTA's dV partial (fp32 [128][64]) in the idle Q/K tiles
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          st_shared_v4(s_q + (uint32_t)((row * 64 + 32 * ch + 4 * j) * 4), __float_as_uint(v[4 * j]),
-                       __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+          st_shared_v4(s_q + xoff(row, 8 * ch + j, 128), __float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                       __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
       } else if (live) {
         uint4 *dst = reinterpret_cast<uint4 *>(p.dv + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch);
 #pragma unroll
@@ -590,16 +596,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dN (dQ) and R-copy (dK) tiles, fp32 [64][64] each
         float c3[32];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) ld_shared_v4f(s_q + (uint32_t)((row * 64 + 32 * ch + 4 * j) * 4), c3 + 4 * j);
+        for (int j = 0; j < 8; ++j) ld_shared_v4f(s_q + xoff(row, 8 * ch + j, 128), c3 + 4 * j);
         if (!own) {
-          const uint32_t o = (uint32_t)(((row - 64 * peer) * 64 + 32 * ch) * 4);
-          const uint32_t dv_dst = map_peer(s_v + o, peer), dq_dst = map_peer(s_dn + o, peer);
-          const uint32_t dk_dst = map_peer(s_rb + o, peer);
+          const uint32_t dv_dst = map_peer(s_v, peer), dq_dst = map_peer(s_dn, peer);
+          const uint32_t dk_dst = map_peer(s_rb, peer);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            st_peer_v4(dv_dst + 16 * j, c3[4 * j], c3[4 * j + 1], c3[4 * j + 2], c3[4 * j + 3]);
-            st_peer_v4(dq_dst + 16 * j, a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]);
-            st_peer_v4(dk_dst + 16 * j, b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]);
+            const uint32_t o = xoff(row - 64 * peer, 8 * ch + j, 64);
+            st_peer_v4(dv_dst + o, c3[4 * j], c3[4 * j + 1], c3[4 * j + 2], c3[4 * j + 3]);
+            st_peer_v4(dq_dst + o, a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]);
+            st_peer_v4(dk_dst + o, b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]);
           }
           if (ch == 0) {
             st_peer_f32(map_peer(sb + lay.rx_usq + (row - 64 * peer) * 4, peer), sq);
@@ -608,18 +614,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         cluster_sync();
         if (own) {
-          const uint32_t o = (uint32_t)(((row - 64 * rank) * 64 + 32 * ch) * 4);
           float r[32];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) ld_shared_v4f(s_v + o + 16 * j, r + 4 * j);
+          for (int j = 0; j < 8; ++j) ld_shared_v4f(s_v + xoff(row - 64 * rank, 8 * ch + j, 64), r + 4 * j);
 #pragma unroll
           for (int i = 0; i < 32; ++i) c3[i] += r[i];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) ld_shared_v4f(s_dn + o + 16 * j, r + 4 * j);
+          for (int j = 0; j < 8; ++j) ld_shared_v4f(s_dn + xoff(row - 64 * rank, 8 * ch + j, 64), r + 4 * j);
 #pragma unroll
           for (int i = 0; i < 32; ++i) a[i] += r[i];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) ld_shared_v4f(s_rb + o + 16 * j, r + 4 * j);
+          for (int j = 0; j < 8; ++j) ld_shared_v4f(s_rb + xoff(row - 64 * rank, 8 * ch + j, 64), r + 4 * j);
 #pragma unroll
           for (int i = 0; i < 32; ++i) b[i] += r[i];
           sq += rx_usq[row - 64 * rank];
@@ -700,6 +705,23 @@ struct FixLayout {
     total = o;
   }
 };
+
+// dst[0:32] = bf16(dst[0:32] + add[0:32]) with 16-B accesses (dst 16-B aligned).
+__device__ __forceinline__ void add_bf16_row32(__nv_bfloat16 *dst, const float *add) {
+  uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 u = d4[j];
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = __uint_as_float(w[i] << 16) + add[8 * j + 2 * i];
+      const float hi = __uint_as_float(w[i] & 0xFFFF0000u) + add[8 * j + 2 * i + 1];
+      w[i] = pack_bf16(lo, hi);
+    }
+    d4[j] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
 
 template <bool FAVOR>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -844,9 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j) st_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), x + 8 * j);
         } else if (live) {
-          __nv_bfloat16 *gk = p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + c0;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) gk[i] = __float2bfloat16_rn(__bfloat162float(gk[i]) + x[i]);
+          add_bf16_row32(p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + c0, x);
         }
       }
       fence_async_smem();
@@ -867,28 +887,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       float v[32];
       tmem_ld32(tmem_addr(tb, 32 * q4, kDV + 32 * ch), v);
-      if (live) {
-        __nv_bfloat16 *gv = p.dv + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) gv[i] = __float2bfloat16_rn(__bfloat162float(gv[i]) + v[i]);
-      }
+      if (live) add_bf16_row32(p.dv + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch, v);
     }
     if (FAVOR) {
       const float sk = usk[row] + usk[kTile + row];
       float b[32];
       tmem_ld32(tmem_addr(tb, 32 * q4, kDK + 32 * ch), b);
       if (live) {
-        __nv_bfloat16 *gk = p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           float xk[8];
           ld_bf16x8(s_k + sw128_offset(row, 32 * ch + 8 * j, kTile), xk);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int e = 8 * j + i;
-            gk[e] = __float2bfloat16_rn(__bfloat162float(gk[e]) + b[e] - xk[i] * sk);
-          }
+          for (int i = 0; i < 8; ++i) b[8 * j + i] = fmaf(-xk[i], sk, b[8 * j + i]);
         }
+        add_bf16_row32(p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch, b);
       }
     }
     cta_sync();

@@ -354,9 +354,15 @@ __device__ __forceinline__ float favor_row_const(float sqnorm, int M) {
   return fmaf(-0.5f * kLog2eF, sqnorm, -0.5f * log2f((float)M));
 }
 
-__device__ __forceinline__ float favor_feature(float s, float c) {
-  return exp2f(fmaf(s, kLog2eF, c));
+// 2^x on the MUFU unit (results below the fp32 normal range flush to zero;
+// such features are far below bf16 resolution of any sum they enter).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
+
+__device__ __forceinline__ float favor_feature(float s, float c) { return ex2_ftz(fmaf(s, kLog2eF, c)); }
 
 __device__ __forceinline__ float elu1_feature(float x) { return x > 0.f ? x + 1.f : __expf(x); }
 

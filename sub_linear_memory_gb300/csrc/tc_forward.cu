@@ -8,18 +8,22 @@
 //   F      = X W_h                     (MMA; X = Q or K, K-major operands)
 //   phi    = exp(F - |x|^2/2)/sqrt(M)  (epilogue: TMEM -> bf16 swizzled smem)
 //   A     += phi_q,h phi_k,h^T         (MMA, fp32 in TMEM)
-//   num'  += phi_q,h R'_h^T            (MMA; R' as a bf16 copy in smem)
+//   num'  += phi_q,h [R_h, S_h]^T      (MMA; bf16 copies of R and of S as
+//                                       a high and a low part in smem)
 //   R'_h  += phi_k,h^T [V, 1]          (MMA; fp32 master state in TMEM)
 // then A is masked to its lower triangle (diagonal kept) and rounded to bf16,
 //   num'  += tril(A) [V, 1]
-// and Y = num / den with den = num'[d] + phi_q . S (the S part is summed on
-// the CUDA cores while phi_q is formed).  A tile of 128 rows holds two
-// 64-row slices or half a 256-row slice; the paper's slice recurrence is
-// exact for any slice size (section 3.4), so the tiling only changes
-// rounding.  MODE_STATE runs only the K side and writes the segment's total
-// R' (the rows eq. (3) adds) for the segment scan: each tile's increment is
-// formed by an MMA that restarts at zero and is added to a double-float
-// (hi, lo) total, so the backward can later remove exactly the same values.
+// and Y = num / den with den = num'[d] + num'[d + 1].  A tile of 128 rows
+// holds two 64-row slices or half a 256-row slice; the paper's slice
+// recurrence is exact for any slice size (section 3.4), so the tiling only
+// changes rounding.
+//
+// MODE_STATE runs only the K side and writes the segment's total R' (the
+// rows eq. (3) adds) for the segment scan.  With `exact` set (the backward's
+// pre-pass) each tile's increment is formed by an MMA that restarts at zero
+// and is added to a double-float (hi, lo) total, so the backward can later
+// remove exactly the same values; otherwise (the forward's pre-pass, which
+// never removes anything) the MMA accumulates in place.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -38,7 +42,7 @@ constexpr int kTile = 128;
 enum { MODE_STATE = 0, MODE_FWD = 1 };
 
 struct Params {
-  int L, M, nt, P, tps, favor;
+  int L, M, nt, P, tps, favor, exact;
   __nv_bfloat16 *y;
   const float *w;
   float *states;     // fp32 [BH][P][M][D + 1]: high parts of the segment states
@@ -49,9 +53,9 @@ struct Params {
 template <int D>
 struct Layout {
   // shared memory (bytes from a 1024-aligned base)
-  uint32_t w, q, k, v, phk, phq, rb, ones, sf, den, bars, total;
+  uint32_t w, q, k, v, phk, phq, rb, ones, sb, bars, total;
   // TMEM columns
-  uint32_t t_f, t_a, t_num, t_r;
+  uint32_t t_f, t_f2, t_a, t_num, t_r;
   // TMEM columns of the state pre-pass: increment, (hi, lo) totals
   uint32_t s_delta, s_hi, s_lo;
   __host__ __device__ Layout(int M, bool favor) {
@@ -64,9 +68,8 @@ struct Layout {
     phk = o; o += kTile * 128 * 2;
     phq = o; o += kTile * 128 * 2;  // also the masked A tile
     rb = o; o += (uint32_t)M * D * 2;
-    ones = o; o += 4096;
-    sf = o; o += (uint32_t)M * 4;
-    den = o; o += 2 * kTile * 4;
+    ones = o; o += 4096;            // [128][16] no-swizzle: column 0 = 1
+    sb = o; o += (uint32_t)M * 32u; // [M][16] no-swizzle: columns 0, 1 = S high, S low
     bars = o; o += 64;
     total = o;
     const int nh = (M + 127) / 128;
@@ -74,6 +77,7 @@ struct Layout {
     t_a = nh > 1 ? 128u : 0u;
     t_num = nh > 1 ? 256u : 128u;
     t_r = t_num + D + 16;
+    t_f2 = nh > 1 ? t_f : t_r + (uint32_t)(D + 16);  // a second feature buffer when it fits
     s_delta = 0;
     s_hi = (D + 16 > 128) ? (uint32_t)(D + 16) : 128u;
     s_lo = s_hi + nh * (D + 16);
@@ -94,15 +98,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *mma_bar = qk_bar + 2;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(qk_bar + 3);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(qk_bar + 4);
-  float *sf = reinterpret_cast<float *>(smem + lay.sf);
-  float *den_part = reinterpret_cast<float *>(smem + lay.den);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q4 = warp & 3, ch = warp >> 2, row = 32 * q4 + lane;
   const int seg = blockIdx.x, bh = blockIdx.y;
   const int M = p.M, nh = (M + 127) / 128, DP = D + 1;
   const int t0 = seg * p.tps, t1 = min(t0 + p.tps, p.nt);
-  const float log2_sqrt_m = 0.5f * log2f((float)M);
+  const bool exact = MODE == MODE_STATE && p.exact;
+  // two feature buffers let the Q- and K-side feature MMAs run back to back
+  const bool dual_f = FAVOR && MODE == MODE_FWD && nh == 1;
 
   if (tid == 0) {
     mbar_init(qk_bar, 1);
@@ -127,8 +131,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   for (int idx = tid; idx < kTile * 16; idx += kThreads) {
     const int r = idx >> 4, x = idx & 15;
-    *reinterpret_cast<__nv_bfloat16 *>(smem + lay.ones + n16_offset(r, x)) =
-        __float2bfloat16_rn(x == 0 ? 1.f : 0.f);
+    *reinterpret_cast<__nv_bfloat16 *>(smem + lay.ones + n16_offset(r, x)) = __float2bfloat16_rn(x == 0 ? 1.f : 0.f);
+  }
+  if (MODE == MODE_FWD) {
+    for (int idx = tid; idx < M * 16; idx += kThreads)
+      *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(idx >> 4, idx & 15)) = __float2bfloat16_rn(0.f);
   }
   if (M < 128) {
     for (int idx = tid; idx < kTile * 128; idx += kThreads) {
@@ -142,8 +149,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
-  // incoming state of the segment -> TMEM master, bf16 copy and S
-  // (the pre-pass instead starts its (hi, lo) totals at zero)
+  // S of feature f as the bf16 pair (high, low) in columns 0, 1 of the S block
+  auto put_s = [&](int f, float sv) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(sv);
+    *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(f, 0)) = hi;
+    *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(f, 1)) =
+        __float2bfloat16_rn(sv - __bfloat162float(hi));
+  };
+
+  // incoming state of the segment -> TMEM master, bf16 copies of R and S
+  // (the pre-pass instead starts its totals at zero)
   const int ncols = D + 16, csplit = ((ncols / 16 + 1) / 2) * 16;
   if (MODE == MODE_STATE) {
     for (int b = 0; b < nh; ++b) {
@@ -151,8 +166,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 16; ++i) z[i] = 0.f;
       for (int c = ch ? csplit : 0; c < (ch ? ncols : csplit); c += 16) {
-        tmem_st16(tmem_addr(tbase, 32 * q4, lay.s_hi + b * ncols + c), z);
-        tmem_st16(tmem_addr(tbase, 32 * q4, lay.s_lo + b * ncols + c), z);
+        if (exact) {
+          tmem_st16(tmem_addr(tbase, 32 * q4, lay.s_hi + b * ncols + c), z);
+          tmem_st16(tmem_addr(tbase, 32 * q4, lay.s_lo + b * ncols + c), z);
+        } else {
+          tmem_st16(tmem_addr(tbase, 32 * q4, lay.t_r + b * ncols + c), z);
+        }
       }
     }
     tmem_st_wait();
@@ -160,8 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t off = ((size_t)bh * p.P + seg - 1) * (size_t)M * DP;
     const float *st = seg > 0 ? p.states + off : nullptr;
     const float *st_lo = seg > 0 ? p.states_lo + off : nullptr;
-    const int blocks = nh;
-    for (int b = 0; b < blocks; ++b) {
+    for (int b = 0; b < nh; ++b) {
       // warps 4b..4b+3 own block b when nh == 2; all warps split columns when nh == 1
       if (nh == 2 && ch != b) continue;
       const int f = 128 * b + row;
@@ -174,16 +192,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int e = c + i;
           v[i] = (st && f < M && e <= D) ? st[(size_t)f * DP + e] + st_lo[(size_t)f * DP + e] : 0.f;
         }
-        tmem_st16(tmem_addr(tbase, 32 * q4, lay.t_r + b * (D + 16) + c), v);
+        tmem_st16(tmem_addr(tbase, 32 * q4, lay.t_r + b * ncols + c), v);
         if (f < M) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int e = c + i;
             if (e < D)
-              *reinterpret_cast<__nv_bfloat16 *>(smem + lay.rb + sw128_offset(f, e, M)) =
-                  __float2bfloat16_rn(v[i]);
+              *reinterpret_cast<__nv_bfloat16 *>(smem + lay.rb + sw128_offset(f, e, M)) = __float2bfloat16_rn(v[i]);
             else if (e == D)
-              sf[f] = v[i];
+              put_s(f, v[i]);
           }
         }
       }
@@ -210,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < D; c += 64) tma_load_3d(smem + lay.v + c * kTile * 2, &tmV, v_bar, c, t * kTile, bh);
   };
   auto mma_sync_all = [&]() {
+    __syncwarp();
     mbar_wait(mma_bar, mma_phase, p.status, abort_flag);
     mma_phase ^= 1;
     tc_fence_after();
@@ -227,11 +245,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t s_q = sbase + lay.q, s_k = sbase + lay.k, s_v = sbase + lay.v;
   const uint32_t s_phk = sbase + lay.phk, s_phq = sbase + lay.phq, s_rb = sbase + lay.rb;
-  const uint32_t s_ones = sbase + lay.ones, s_w = sbase + lay.w;
+  const uint32_t s_ones = sbase + lay.ones, s_w = sbase + lay.w, s_sb = sbase + lay.sb;
+
+  // feature MMA: F = X W_h^T for feature block h (nu features)
+  auto issue_features = [&](uint32_t s_x, uint32_t t_out, int h, int nu) {
+    const uint32_t idesc = make_idesc(128, nu, false, false);
+    for (int s = 0; s < D / 16; ++s)
+      mma_bf16(tbase + t_out, desc_kmajor(s_x, kTile, 0, s), desc_kmajor(s_w, M, 128 * h, s), idesc, s > 0);
+  };
+  // phi = exp2(F log2 e + c) from TMEM into the swizzled bf16 tile
+  auto favor_epilogue = [&](uint32_t t_in, uint32_t s_out, int cols, float c_row, bool zero_row) {
+    for (int c0 = ch * cols; c0 < (ch + 1) * cols; c0 += 32) {
+      float v[32];
+      tmem_ld32(tmem_addr(tbase, 32 * q4, t_in + c0), v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = favor_feature(v[i], c_row);
+      if (zero_row) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) st_bf16x8(s_out + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
+    }
+  };
+  auto elu_epilogue = [&](uint32_t s_x, uint32_t s_out, int cols, bool zero_row) {
+    for (int c0 = ch * cols; c0 < (ch + 1) * cols; c0 += 8) {
+      float v[8];
+      ld_bf16x8(s_x + sw128_offset(row, c0, kTile), v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = zero_row ? 0.f : elu1_feature(v[i]);
+      st_bf16x8(s_out + sw128_offset(row, c0, kTile), v);
+    }
+  };
 
   for (int t = t0; t < t1; ++t) {
     const int valid = min(kTile, p.L - t * kTile);
-    const bool live = row < valid;
+    const bool dead = row >= valid;  // padding rows past L: features forced to zero
     mbar_wait(qk_bar, qk_phase, p.status, abort_flag);
     qk_phase ^= 1;
     float ck = 0.f, cq = 0.f;  // per-row exp2 offsets
@@ -239,51 +288,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       ck = favor_row_const(tile_row_sqnorm(s_k, row, D), M);
       if (MODE == MODE_FWD) cq = favor_row_const(tile_row_sqnorm(s_q, row, D), M);
     }
-    float den_inter = 0.f;
+    if (FAVOR && tid == 0) {
+      issue_features(s_k, lay.t_f, 0, min(128, M));
+      if (dual_f) issue_features(s_q, lay.t_f2, 0, M);
+      mma_commit(mma_bar);
+    }
     for (int h = 0; h < nh; ++h) {
       const int nu = min(128, M - 128 * h);  // features in this block
       const int cols = nu / 2;               // per thread (two threads per row)
-      for (int side = 0; side < (MODE == MODE_FWD ? 2 : 1); ++side) {
-        // side 0: K -> phi_k ; side 1: Q -> phi_q
-        const uint32_t s_x = side ? s_q : s_k;
-        const uint32_t s_out = side ? s_phq : s_phk;
-        if (FAVOR) {
-          if (tid == 0) {
-            const uint32_t idesc = make_idesc(128, nu, false, false);
-            for (int s = 0; s < D / 16; ++s)
-              mma_bf16(tbase + lay.t_f, desc_kmajor(s_x, kTile, 0, s), desc_kmajor(s_w, M, 128 * h, s),
-                       idesc, s > 0);
-            mma_commit(mma_bar);
-          }
-          __syncwarp();
-          mma_sync_all();
-          const float c_row = side ? cq : ck;
-          for (int c0 = ch * cols; c0 < (ch + 1) * cols; c0 += 32) {
-            float v[32];
-            tmem_ld32(tmem_addr(tbase, 32 * q4, lay.t_f + c0), v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = live ? favor_feature(v[i], c_row) : 0.f;
-            if (side) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) den_inter = fmaf(v[i], sf[128 * h + c0 + i], den_inter);
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) st_bf16x8(s_out + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
-          }
-        } else {
-          // elu + 1, elementwise from the bf16 tile (M == D, a single block)
-          for (int c0 = ch * cols; c0 < (ch + 1) * cols; c0 += 8) {
-            float v[8];
-            ld_bf16x8(s_x + sw128_offset(row, c0, kTile), v);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = live ? elu1_feature(v[i]) : 0.f;
-            if (side) {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) den_inter = fmaf(v[i], sf[c0 + i], den_inter);
-            }
-            st_bf16x8(s_out + sw128_offset(row, c0, kTile), v);
-          }
+      // K side (its feature MMA was issued already)
+      if (FAVOR) {
+        mma_sync_all();
+        favor_epilogue(lay.t_f, s_phk, cols, ck, dead);
+        if (dual_f) favor_epilogue(lay.t_f2, s_phq, cols, cq, dead);
+      } else {
+        elu_epilogue(s_k, s_phk, cols, dead);
+        if (MODE == MODE_FWD) elu_epilogue(s_q, s_phq, cols, dead);
+      }
+      fence_async_smem();
+      cta_sync();
+      if (MODE == MODE_FWD && FAVOR && !dual_f) {
+        if (tid == 0) {
+          issue_features(s_q, lay.t_f, h, nu);
+          mma_commit(mma_bar);
         }
+        mma_sync_all();
+        favor_epilogue(lay.t_f, s_phq, cols, cq, dead);
         fence_async_smem();
         cta_sync();
       }
@@ -293,42 +323,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (MODE == MODE_FWD) {
           const uint32_t id_a = make_idesc(128, 128, false, false);
           const uint32_t id_n = make_idesc(128, D, false, true);
+          const uint32_t id_s = make_idesc(128, 16, false, true);
           for (int s = 0; s < nu / 16; ++s)
-            mma_bf16(tbase + lay.t_a, desc_kmajor(s_phq, kTile, 0, s), desc_kmajor(s_phk, kTile, 0, s),
-                     id_a, (h > 0 || s > 0));
-          for (int s = 0; s < nu / 16; ++s)
-            mma_bf16(tbase + lay.t_num, desc_kmajor(s_phq, kTile, 0, s),
-                     desc_mnmajor(s_rb, M, 0, 8 * h + s), id_n, (h > 0 || s > 0));
+            mma_bf16(tbase + lay.t_a, desc_kmajor(s_phq, kTile, 0, s), desc_kmajor(s_phk, kTile, 0, s), id_a,
+                     (h > 0 || s > 0));
+          for (int s = 0; s < nu / 16; ++s) {
+            mma_bf16(tbase + lay.t_num, desc_kmajor(s_phq, kTile, 0, s), desc_mnmajor(s_rb, M, 0, 8 * h + s), id_n,
+                     (h > 0 || s > 0));
+            mma_bf16(tbase + lay.t_num + D, desc_kmajor(s_phq, kTile, 0, s), desc_n16(s_sb, 8 * h + s), id_s,
+                     (h > 0 || s > 0));
+          }
         }
         if (h == 0) {
           mbar_wait(v_bar, v_phase, p.status, abort_flag);
           v_phase ^= 1;
         }
-        if (MODE == MODE_FWD) {
+        if (exact) {
+          issue_state_delta(tbase + lay.s_delta, s_phk, s_v, s_ones, D);
+        } else {
           // the running state only moves forward here: accumulate in place
           const uint32_t id_r = make_idesc(128, D, true, true);
           const uint32_t id_r1 = make_idesc(128, 16, true, true);
-          const uint32_t t_r = tbase + lay.t_r + h * (D + 16);
+          const uint32_t t_r = tbase + lay.t_r + h * ncols;
           for (int s = 0; s < kTile / 16; ++s) {
             mma_bf16(t_r, desc_mnmajor(s_phk, kTile, 0, s), desc_mnmajor(s_v, kTile, 0, s), id_r, 1);
             mma_bf16(t_r + D, desc_mnmajor(s_phk, kTile, 0, s), desc_n16(s_ones, s), id_r1, 1);
           }
-        } else {
-          issue_state_delta(tbase + lay.s_delta, s_phk, s_v, s_ones, D);
         }
+        // the next feature block's K side shares this commit (F is free)
+        if (FAVOR && h + 1 < nh && !exact) issue_features(s_k, lay.t_f, h + 1, min(128, M - 128 * (h + 1)));
         mma_commit(mma_bar);
       }
-      __syncwarp();
-      mma_sync_all();
-      if (MODE == MODE_STATE) {
+      if (exact) {
+        mma_sync_all();
         // (hi, lo) total of block h += this tile's increment
         df_update_tmem(tbase, 32 * q4, lay.s_delta, lay.s_hi + h * ncols, lay.s_lo + h * ncols,
                        ch ? csplit : 0, ch ? ncols : csplit, 1.f);
         cta_sync();
+        if (FAVOR && h + 1 < nh && tid == 0) {
+          issue_features(s_k, lay.t_f, h + 1, min(128, M - 128 * (h + 1)));
+          mma_commit(mma_bar);
+        }
+      } else if (h + 1 == nh || !FAVOR) {
+        mma_sync_all();
       }
     }
     if (MODE == MODE_FWD) {
-      den_part[ch * kTile + row] = den_inter;
       // masked A (diagonal kept) -> bf16 into the phi_q buffer
       for (int c0 = ch * 64; c0 < ch * 64 + 64; c0 += 32) {
         float v[32];
@@ -346,38 +386,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t id_n1 = make_idesc(128, 16, false, true);
         for (int s = 0; s < kTile / 16; ++s) {
           mma_bf16(tbase + lay.t_num, desc_kmajor(s_phq, kTile, 0, s), desc_mnmajor(s_v, kTile, 0, s), id_n, 1);
-          mma_bf16(tbase + lay.t_num + D, desc_kmajor(s_phq, kTile, 0, s), desc_n16(s_ones, s), id_n1, s > 0);
+          mma_bf16(tbase + lay.t_num + D, desc_kmajor(s_phq, kTile, 0, s), desc_n16(s_ones, s), id_n1, 1);
         }
         mma_commit(mma_bar);
       }
-      __syncwarp();
       mma_sync_all();
       if (tid == 0 && t + 1 < t1) issue_v(t + 1);
       // Y = num / den
       {
         float dv[16];
         tmem_ld16(tmem_addr(tbase, 32 * q4, lay.t_num + D), dv);
-        const float den = dv[0] + den_part[row] + den_part[kTile + row];
-        const float inv = 1.0f / den;
+        const float inv = 1.0f / (dv[0] + dv[1]);
         __nv_bfloat16 *yrow = p.y + ((size_t)bh * p.L + (size_t)t * kTile + row) * D;
         for (int c0 = ch * (D / 2); c0 < (ch + 1) * (D / 2); c0 += 32) {
           float v[32];
           tmem_ld32(tmem_addr(tbase, 32 * q4, lay.t_num + c0), v);
-          if (live) {
+          if (!dead) {
             uint4 *dst = reinterpret_cast<uint4 *>(yrow + c0);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint4 u;
-              u.x = pack_bf16(v[8 * j] * inv, v[8 * j + 1] * inv);
-              u.y = pack_bf16(v[8 * j + 2] * inv, v[8 * j + 3] * inv);
-              u.z = pack_bf16(v[8 * j + 4] * inv, v[8 * j + 5] * inv);
-              u.w = pack_bf16(v[8 * j + 6] * inv, v[8 * j + 7] * inv);
-              dst[j] = u;
-            }
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_uint4(pack_bf16(v[8 * j] * inv, v[8 * j + 1] * inv),
+                                  pack_bf16(v[8 * j + 2] * inv, v[8 * j + 3] * inv),
+                                  pack_bf16(v[8 * j + 4] * inv, v[8 * j + 5] * inv),
+                                  pack_bf16(v[8 * j + 6] * inv, v[8 * j + 7] * inv));
           }
         }
       }
-      // refresh the bf16 copy of R' and S for the next tile
+      // refresh the bf16 copies of R' and S for the next tile
       for (int b = 0; b < nh; ++b) {
         if (nh == 2 && ch != b) continue;
         const int f = 128 * b + row;
@@ -386,12 +421,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c_hi = (nh == 2) ? ncols : (ch == 0 ? (ncols / 32) * 16 : ncols);
         for (int c = c_lo; c < c_hi; c += 16) {
           float v[16];
-          tmem_ld16(tmem_addr(tbase, 32 * q4, lay.t_r + b * (D + 16) + c), v);
+          tmem_ld16(tmem_addr(tbase, 32 * q4, lay.t_r + b * ncols + c), v);
 #pragma unroll
           for (int i = 0; i < 16; i += 8) {
             if (c + i + 8 <= D) st_bf16x8(s_rb + sw128_offset(f, c + i, M), v + i);
           }
-          if (c <= D && D < c + 16) sf[f] = v[D - c];
+          if (c <= D && D < c + 16) put_s(f, v[D - c]);
         }
       }
       fence_async_smem();
@@ -408,8 +443,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int f = 128 * b + row;
       for (int c = ch ? csplit : 0; c < (ch ? ncols : csplit); c += 16) {
         float h[16], l[16];
-        tmem_ld16(tmem_addr(tbase, 32 * q4, lay.s_hi + b * ncols + c), h);
-        tmem_ld16(tmem_addr(tbase, 32 * q4, lay.s_lo + b * ncols + c), l);
+        if (exact) {
+          tmem_ld16(tmem_addr(tbase, 32 * q4, lay.s_hi + b * ncols + c), h);
+          tmem_ld16(tmem_addr(tbase, 32 * q4, lay.s_lo + b * ncols + c), l);
+        } else {
+          tmem_ld16(tmem_addr(tbase, 32 * q4, lay.t_r + b * ncols + c), h);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) l[i] = 0.f;
+        }
         if (f < M) {
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -427,9 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool FAVOR, int MODE>
 cudaError_t launch(const Plan &pl, const Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
-                   const CUtensorMap &mv, int nseg, cudaStream_t st) {
+                   const CUtensorMap &mv, int nseg, bool exact, cudaStream_t st) {
   Params p{};
   p.L = pl.L; p.M = pl.M; p.nt = pl.tc_tiles; p.P = pl.P; p.tps = pl.cps; p.favor = FAVOR;
+  p.exact = exact ? 1 : 0;
   p.y = static_cast<__nv_bfloat16 *>(a.y);
   p.w = a.w;
   p.states = a.ws + pl.states_off;
@@ -448,11 +490,12 @@ cudaError_t launch(const Plan &pl, const Args &a, const CUtensorMap &mq, const C
 // states[s] = R' at the end of segment s.
 template <int D, bool FAVOR>
 cudaError_t segment_states(const Plan &pl, const Args &a, const CUtensorMap &mq,
-                           const CUtensorMap &mk, const CUtensorMap &mv, int nseg, cudaStream_t st) {
+                           const CUtensorMap &mk, const CUtensorMap &mv, int nseg, bool exact,
+                           cudaStream_t st) {
   cudaError_t e;
   {
     ProfScope ps("tc_segment_state", st);
-    e = launch<D, FAVOR, MODE_STATE>(pl, a, mq, mk, mv, nseg, st);
+    e = launch<D, FAVOR, MODE_STATE>(pl, a, mq, mk, mv, nseg, exact, st);
     if (e != cudaSuccess) return e;
   }
   if (nseg > 1) {
@@ -470,11 +513,11 @@ cudaError_t forward_family(const Plan &pl, const Args &a, cudaStream_t st) {
     return cudaErrorInvalidValue;
   cudaError_t e;
   if (pl.P > 1) {
-    e = segment_states<D, FAVOR>(pl, a, mq, mk, mv, pl.P - 1, st);
+    e = segment_states<D, FAVOR>(pl, a, mq, mk, mv, pl.P - 1, false, st);
     if (e != cudaSuccess) return e;
   }
   ProfScope ps("tc_forward", st);
-  return launch<D, FAVOR, MODE_FWD>(pl, a, mq, mk, mv, pl.P, st);
+  return launch<D, FAVOR, MODE_FWD>(pl, a, mq, mk, mv, pl.P, false, st);
 }
 
 }  // namespace tcf
@@ -496,9 +539,9 @@ cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, cudaStream
   const int d = p.d;
   if (!make_map_bf16_3d(&mk, a.k, p.BH, p.L, d, tcf::kTile) || !make_map_bf16_3d(&mv, a.v, p.BH, p.L, d, tcf::kTile))
     return cudaErrorInvalidValue;
-  if (d == 64 && p.favor) return tcf::segment_states<64, true>(p, a, mk, mk, mv, nseg, st);
-  if (d == 64) return tcf::segment_states<64, false>(p, a, mk, mk, mv, nseg, st);
-  if (d == 128 && !p.favor) return tcf::segment_states<128, false>(p, a, mk, mk, mv, nseg, st);
+  if (d == 64 && p.favor) return tcf::segment_states<64, true>(p, a, mk, mk, mv, nseg, true, st);
+  if (d == 64) return tcf::segment_states<64, false>(p, a, mk, mk, mv, nseg, true, st);
+  if (d == 128 && !p.favor) return tcf::segment_states<128, false>(p, a, mk, mk, mv, nseg, true, st);
   return cudaErrorInvalidValue;
 }
 
