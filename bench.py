@@ -402,6 +402,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="l32k")
+    ap.add_argument("--heads", default=None,
+                    help="BxH: run the workload's recipe with another batch and head count "
+                         "(a reduced case for profiling); the default is the workload's own")
     ap.add_argument("--no-memory", dest="memory", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-row-frac", type=float, default=0.5,
@@ -414,6 +417,9 @@ def main(argv=None):
     from sub_linear_memory_gb300 import inputs
 
     wl = inputs.WORKLOADS[args.workload]
+    if args.heads:
+        b, h = (int(x) for x in args.heads.lower().split("x"))
+        wl = wl.with_(B=b, H=h)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_native(args, wl)

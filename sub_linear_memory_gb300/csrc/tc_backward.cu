@@ -34,7 +34,7 @@ constexpr int kTile = 128;
 constexpr int D = 64;
 
 struct Params {
-  int L, M, nt, P, tps, favor;
+  int L, M, nt, P, tps, favor, BH;
   __nv_bfloat16 *dq, *dk, *dv;
   const float *w;
   const float *states;     // fp32 [BH][P][M][D + 1]: inclusive segment-end R', high parts
@@ -45,7 +45,7 @@ struct Params {
 
 struct Layout {
   uint32_t w, q, k, v, dy, phq, phk, at, dn, rb, ones, ddb;
-  uint32_t s_f, gs_f, den_a, den_b, dd, usq, usk, dot, rx_den, rx_usq, rx_usk, bars, total;
+  uint32_t sb, s_f, gs_f, dd, usq, usk, dot, rx_den, rx_usq, rx_usk, bars, total;
   __host__ __device__ explicit Layout(int MC) {
     uint32_t o = 0;
     const uint32_t tile = kTile * D * 2;
@@ -61,15 +61,14 @@ struct Layout {
     rb = o; o += (uint32_t)MC * 128u;
     ones = o; o += 4096;
     ddb = o; o += 4096;
+    sb = o; o += (uint32_t)MC * 32u;  // [MC][16] no-swizzle: S high, S low
     s_f = o; o += 128 * 4;
     gs_f = o; o += 128 * 4;
-    den_a = o; o += 2 * kTile * 4;
-    den_b = o; o += 2 * kTile * 4;
     dd = o; o += kTile * 4;
     usq = o; o += 2 * kTile * 4;
     usk = o; o += 2 * kTile * 4;
     dot = o; o += 2 * kTile * 4;
-    rx_den = o; o += 64 * 4;  // cluster exchange: partner's partials for my rows
+    rx_den = o; o += 128 * 4;  // cluster exchange: the peer's den partials
     rx_usq = o; o += 64 * 4;
     rx_usk = o; o += 64 * 4;
     bars = o; o += 64;
@@ -147,8 +146,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *rx_usk = reinterpret_cast<float *>(smem + lay.rx_usk);
   float *s_f = reinterpret_cast<float *>(smem + lay.s_f);
   float *gs_f = reinterpret_cast<float *>(smem + lay.gs_f);
-  float *den_a = reinterpret_cast<float *>(smem + lay.den_a);
-  float *den_b = reinterpret_cast<float *>(smem + lay.den_b);
   float *dd = reinterpret_cast<float *>(smem + lay.dd);
   float *usq = reinterpret_cast<float *>(smem + lay.usq);
   float *usk = reinterpret_cast<float *>(smem + lay.usk);
@@ -183,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = idx >> 4, x = idx & 15;
     st_bf16_scalar(smem, lay.ones + n16_offset(r, x), x == 0 ? 1.f : 0.f);
     st_bf16_scalar(smem, lay.ddb + n16_offset(r, x), 0.f);
+    if (r < MC) st_bf16_scalar(smem, lay.sb + n16_offset(r, x), 0.f);
   }
   if (MC < 128) {  // features beyond MC stay zero in phi_q / phi_k
     for (int idx = tid; idx < kTile * 128; idx += kThreads) {
@@ -227,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_w = sb + lay.w, s_q = sb + lay.q, s_k = sb + lay.k, s_v = sb + lay.v;
   const uint32_t s_dy = sb + lay.dy, s_phq = sb + lay.phq, s_phk = sb + lay.phk;
   const uint32_t s_at = sb + lay.at, s_dn = sb + lay.dn, s_rb = sb + lay.rb;
-  const uint32_t s_ones = sb + lay.ones, s_ddb = sb + lay.ddb;
+  const uint32_t s_ones = sb + lay.ones, s_ddb = sb + lay.ddb, s_sb = sb + lay.sb;
   const uint32_t tile_bytes = kTile * D * 2;
   uint32_t in_phase = 0, mma_phase = 0, rl_phase = 0;
 
@@ -266,181 +264,145 @@ __global__ void __launch_bounds__(kThreads, 1)
       cq = favor_row_const(tile_row_sqnorm(s_q, row, D), M);
     }
 
-    // (b) phi_k
+    // (b) features of both sides: F_k -> T, F_q -> X, one commit
     if (FAVOR) {
       if (tid == 0) {
         const uint32_t id = make_idesc(128, MC, false, false);
         for (int s = 0; s < D / 16; ++s)
           mma_bf16(tb + kT, desc_kmajor(s_k, kTile, 0, s), desc_kmajor(s_w, MC, 0, s), id, s > 0);
+        for (int s = 0; s < D / 16; ++s)
+          mma_bf16(tb + kX, desc_kmajor(s_q, kTile, 0, s), desc_kmajor(s_w, MC, 0, s), id, s > 0);
         mma_done();
       }
       wait_mma();
-      for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 32) {
-        float v[32];
-        tmem_ld32(tmem_addr(tb, 32 * q4, kT + c0), v);
+      for (int side = 0; side < 2; ++side) {
+        const uint32_t t_in = side ? kX : kT, s_out = side ? s_phq : s_phk;
+        const float c_row = side ? cq : ck;
+        for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 32) {
+          float v[32];
+          tmem_ld32(tmem_addr(tb, 32 * q4, t_in + c0), v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = live ? favor_feature(v[i], ck) : 0.f;
+          for (int i = 0; i < 32; ++i) v[i] = favor_feature(v[i], c_row);
+          if (!live) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) st_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) st_bf16x8(s_out + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
+        }
       }
     } else {
-      for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 8) {
-        float v[8];
-        ld_bf16x8(s_k + sw128_offset(row, c0, kTile), v);
+      for (int side = 0; side < 2; ++side) {
+        const uint32_t s_x = side ? s_q : s_k, s_out = side ? s_phq : s_phk;
+        for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 8) {
+          float v[8];
+          ld_bf16x8(s_x + sw128_offset(row, c0, kTile), v);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = live ? elu1_feature(v[i]) : 0.f;
-        st_bf16x8(s_phk + sw128_offset(row, c0, kTile), v);
+          for (int i = 0; i < 8; ++i) v[i] = live ? elu1_feature(v[i]) : 0.f;
+          st_bf16x8(s_out + sw128_offset(row, c0, kTile), v);
+        }
       }
     }
     fence_async_smem();
     cta_sync();
 
     // (c) eq. (19): R' -= phi_k^T [V, 1], removing exactly the increment the
-    // segment pre-pass added for this tile; then the bf16 copy of R and S
+    // segment pre-pass added for this tile (increment -> T), and
+    // A = phi_q phi_k^T -> X, one commit
     if (tid == 0) {
-      issue_state_delta(tb + kX, s_phk, s_v, s_ones, D);
-      mma_done();
-    }
-    wait_mma();
-    df_update_tmem(tb, 32 * q4, kX, kRhi, kRlo, ch ? 48 : 0, ch ? 80 : 48, -1.f);
-    cta_sync();
-    state_to_smem(tb, kRhi, kRlo, q4, ch, row, MC, s_rb, s_f);
-    fence_async_smem();
-    cta_sync();
-
-    // (d) phi_q and phi_q . S
-    float den_inter = 0.f;
-    if (FAVOR) {
-      if (tid == 0) {
-        const uint32_t id = make_idesc(128, MC, false, false);
-        for (int s = 0; s < D / 16; ++s)
-          mma_bf16(tb + kT, desc_kmajor(s_q, kTile, 0, s), desc_kmajor(s_w, MC, 0, s), id, s > 0);
-        mma_done();
-      }
-      wait_mma();
-      for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 32) {
-        float v[32];
-        tmem_ld32(tmem_addr(tb, 32 * q4, kT + c0), v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          v[i] = live ? favor_feature(v[i], cq) : 0.f;
-          den_inter = fmaf(v[i], s_f[c0 + i], den_inter);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) st_bf16x8(s_phq + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
-      }
-    } else {
-      for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 8) {
-        float v[8];
-        ld_bf16x8(s_q + sw128_offset(row, c0, kTile), v);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          v[i] = live ? elu1_feature(v[i]) : 0.f;
-          den_inter = fmaf(v[i], s_f[c0 + i], den_inter);
-        }
-        st_bf16x8(s_phq + sw128_offset(row, c0, kTile), v);
-      }
-    }
-    den_a[ch * kTile + row] = den_inter;
-    fence_async_smem();
-    cta_sync();
-
-    // (e) A = tril(phi_q phi_k^T) -> bf16 tile, row sums
-    if (tid == 0) {
+      issue_state_delta(tb + kT, s_phk, s_v, s_ones, D);
       const uint32_t id = make_idesc(128, 128, false, false);
       for (int s = 0; s < MC / 16; ++s)
-        mma_bf16(tb + kT, desc_kmajor(s_phq, kTile, 0, s), desc_kmajor(s_phk, kTile, 0, s), id, s > 0);
+        mma_bf16(tb + kX, desc_kmajor(s_phq, kTile, 0, s), desc_kmajor(s_phk, kTile, 0, s), id, s > 0);
       mma_done();
     }
     wait_mma();
+    df_update_tmem(tb, 32 * q4, kT, kRhi, kRlo, ch ? 48 : 0, ch ? 80 : 48, -1.f);
+    // tril(A) (diagonal kept) -> bf16 tile
     {
-      float rs = 0.f;
-      for (int c0 = ch * 64; c0 < ch * 64 + 64; c0 += 32) {
-        float v[32];
-        tmem_ld32(tmem_addr(tb, 32 * q4, kT + c0), v);
+      float v[64];
+      tmem_ld32x2(tmem_addr(tb, 32 * q4, kX + 64 * ch), tmem_addr(tb, 32 * q4, kX + 64 * ch + 32), v, v + 32);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          if (c0 + i > row) v[i] = 0.f;
-          rs += v[i];
-        }
+      for (int i = 0; i < 64; ++i)
+        if (64 * ch + i > row) v[i] = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
-      }
-      den_b[ch * kTile + row] = rs;
+      for (int j = 0; j < 8; ++j) st_bf16x8(s_at + sw128_offset(row, 64 * ch + 8 * j, kTile), v + 8 * j);
+    }
+    cta_sync();
+    // bf16 copies of R and of S (high, low) for the MMAs, fp32 S for the epilogues
+    state_to_smem(tb, kRhi, kRlo, q4, ch, row, MC, s_rb, s_f);
+    if (ch == 1 && row < MC) {
+      const float sv = s_f[row];
+      const __nv_bfloat16 hi = __float2bfloat16_rn(sv);
+      *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(row, 0)) = hi;
+      *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(row, 1)) =
+          __float2bfloat16_rn(sv - __bfloat162float(hi));
     }
     fence_async_smem();
     cta_sync();
 
-    // (f) num = A V + phi_q R^T; Y, dN, dD
+    // (f) num' = A [V, 1] + phi_q [R, S]^T -> T (den = columns d, d + 1); Y, dN, dD
     if (tid == 0) {
       const uint32_t id = make_idesc(128, D, false, true);
-      for (int s = 0; s < kTile / 16; ++s)
+      const uint32_t id1 = make_idesc(128, 16, false, true);
+      for (int s = 0; s < kTile / 16; ++s) {
         mma_bf16(tb + kT, desc_kmajor(s_at, kTile, 0, s), desc_mnmajor(s_v, kTile, 0, s), id, s > 0);
-      for (int s = 0; s < MC / 16; ++s)
+        mma_bf16(tb + kT + D, desc_kmajor(s_at, kTile, 0, s), desc_n16(s_ones, s), id1, s > 0);
+      }
+      for (int s = 0; s < MC / 16; ++s) {
         mma_bf16(tb + kT, desc_kmajor(s_phq, kTile, 0, s), desc_mnmajor(s_rb, MC, 0, s), id, 1);
+        mma_bf16(tb + kT + D, desc_kmajor(s_phq, kTile, 0, s), desc_n16(s_sb, s), id1, 1);
+      }
       mma_done();
     }
     wait_mma();
     {
-      float den = den_a[row] + den_a[kTile + row] + den_b[row] + den_b[kTile + row];
+      float den;
+      {
+        float dv[16];
+        tmem_ld16(tmem_addr(tb, 32 * q4, kT + D), dv);
+        den = dv[0] + dv[1];
+      }
       float v[32], g[32];
       tmem_ld32(tmem_addr(tb, 32 * q4, kT + 32 * ch), v);
       if (CS == 2) {
-        // both CTAs are past their features: the peer's Q tile is idle and
-        // takes my partial num and den for the rows it owns
+        // both CTAs are past their features: the peer's Q and K tiles are idle
+        // and take my partial num (all 128 rows) and den; each CTA then forms
+        // dN' for every row itself
         cluster_sync();
-        if (!own) {
-          const uint32_t dst = map_peer(s_q, peer);
+        const uint32_t dst = map_peer(s_q, peer);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            st_peer_v4(dst + xoff(row - 64 * peer, 8 * ch + j, 64), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          if (ch == 0) st_peer_f32(map_peer(sb + lay.rx_den + (row - 64 * peer) * 4, peer), den);
-        }
+        for (int j = 0; j < 8; ++j)
+          st_peer_v4(dst + xoff(row, 8 * ch + j, 128), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        if (ch == 0) st_peer_f32(map_peer(sb + lay.rx_den + row * 4, peer), den);
         cluster_sync();
-        if (own) {
-          float r[32];
+        float r[32];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) ld_shared_v4f(s_q + xoff(row - 64 * rank, 8 * ch + j, 64), r + 4 * j);
+        for (int j = 0; j < 8; ++j) ld_shared_v4f(s_q + xoff(row, 8 * ch + j, 128), r + 4 * j);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] += r[i];
-          den += rx_den[row - 64 * rank];
-        }
+        for (int i = 0; i < 32; ++i) v[i] += r[i];
+        den += rx_den[row];
       }
       const float inv = 1.0f / den;
       float dyy = 0.f;
-      if (own) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) ld_bf16x8(s_dy + sw128_offset(row, 32 * ch + 8 * j, kTile), g + 8 * j);
+      for (int j = 0; j < 4; ++j) ld_bf16x8(s_dy + sw128_offset(row, 32 * ch + 8 * j, kTile), g + 8 * j);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float y = v[i] * inv;
-          dyy = fmaf(g[i], y, dyy);
-          g[i] = live ? g[i] * inv : 0.f;
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t off = sw128_offset(row, 32 * ch + 8 * j, kTile);
-          st_bf16x8(s_dn + off, g + 8 * j);
-          if (CS == 2)
-            st_peer_v4u(map_peer(s_dn + off, peer), pack_bf16(g[8 * j], g[8 * j + 1]),
-                        pack_bf16(g[8 * j + 2], g[8 * j + 3]), pack_bf16(g[8 * j + 4], g[8 * j + 5]),
-                        pack_bf16(g[8 * j + 6], g[8 * j + 7]));
-        }
-        dot[ch * kTile + row] = dyy;
+      for (int i = 0; i < 32; ++i) {
+        const float y = v[i] * inv;
+        dyy = fmaf(g[i], y, dyy);
+        g[i] = live ? g[i] * inv : 0.f;
       }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) st_bf16x8(s_dn + sw128_offset(row, 32 * ch + 8 * j, kTile), g + 8 * j);
+      dot[ch * kTile + row] = dyy;
       __syncthreads();
-      if (own && ch == 0) {
+      if (ch == 0) {
         const float dval = live ? -(dot[row] + dot[kTile + row]) * inv : 0.f;
         dd[row] = dval;
         st_bf16_scalar(smem, lay.ddb + n16_offset(row, 0), dval);
-        if (CS == 2) {
-          st_peer_f32(map_peer(sb + lay.dd + row * 4, peer), dval);
-          const __nv_bfloat16 hb = __float2bfloat16_rn(dval);
-          st_peer_b16(map_peer(s_ddb + n16_offset(row, 0), peer), *reinterpret_cast<const uint16_t *>(&hb));
-        }
       }
     }
-    if (CS == 2) cluster_sync();  // dN', dD of all 128 rows present in both CTAs
     cta_sync();  // dY consumed: its buffer now takes the bf16 copy of G_V
     state_to_smem(tb, kG, kG, q4, ch, row, MC, s_dy, gs_f);
     fence_async_smem();
@@ -462,13 +424,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     wait_mma();
     {
       const float dval = dd[row];
-      for (int c0 = ch * 64; c0 < ch * 64 + 64; c0 += 32) {
-        float v[32];
-        tmem_ld32(tmem_addr(tb, 32 * q4, kT + c0), v);
+      {
+        float v[64];
+        tmem_ld32x2(tmem_addr(tb, 32 * q4, kT + 64 * ch), tmem_addr(tb, 32 * q4, kT + 64 * ch + 32), v, v + 32);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = (c0 + i > row) ? 0.f : v[i] + dval;
+        for (int i = 0; i < 64; ++i) v[i] = (64 * ch + i > row) ? 0.f : v[i] + dval;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
+        for (int j = 0; j < 8; ++j) st_bf16x8(s_at + sw128_offset(row, 64 * ch + 8 * j, kTile), v + 8 * j);
       }
       float v[32];
       tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * ch), v);
@@ -528,8 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float uq = 0.f, uk = 0.f;
       for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 32) {
         float a[32], b[32];
-        tmem_ld32(tmem_addr(tb, 32 * q4, kT + c0), a);
-        tmem_ld32(tmem_addr(tb, 32 * q4, kX + c0), b);
+        tmem_ld32x2(tmem_addr(tb, 32 * q4, kT + c0), tmem_addr(tb, 32 * q4, kX + c0), a, b);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           float fq[8], fk[8];
@@ -588,8 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_mma();
       float sq = usq[row] + usq[kTile + row], sk = usk[row] + usk[kTile + row];
       float a[32], b[32];
-      tmem_ld32(tmem_addr(tb, 32 * q4, kT + 32 * ch), a);
-      tmem_ld32(tmem_addr(tb, 32 * q4, kT + 64 + 32 * ch), b);
+      tmem_ld32x2(tmem_addr(tb, 32 * q4, kT + 32 * ch), tmem_addr(tb, 32 * q4, kT + 64 + 32 * ch), a, b);
       uint32_t s_xq = s_q, s_xk = s_k;
       if (CS == 2) {
         // exchange 2: my partials of the peer's rows go to its idle V (dV),
@@ -689,14 +649,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Correction: add G_end(s) (the G of every later segment) to dK and dV of
 // segment s:  dphi_k += V G_V^T + 1 G_S^T,  dV += phi_k G_V^T, one 128-feature
 // block at a time (every term is a sum over features).
+// The tiles of segments 0 .. P-2 are independent here, so they are dealt out
+// evenly to one CTA per SM (flat over (b, h) and tiles), K and V of the next
+// tile stream in while the current one is processed.
 struct FixLayout {
   uint32_t w, k, v, phk, gb, gs, usk, bars, total;
   __host__ __device__ explicit FixLayout(int M) {
     uint32_t o = 0;
     const uint32_t tile = kTile * D * 2;
     w = o; o += (uint32_t)M * 128u;   // W^T as [M][64]
-    k = o; o += tile;
-    v = o; o += tile;
+    k = o; o += 2 * tile;              // two stages
+    v = o; o += 2 * tile;
     phk = o; o += kTile * 256;
     gb = o; o += (uint32_t)M * 128u;  // G_end(s)[0:d] as bf16 [M][64]
     gs = o; o += (uint32_t)M * 4u;    // G_end(s)[d] (fp32)
@@ -734,21 +697,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nb = (M + 127) / 128, MB = M < 128 ? M : 128;  // feature blocks and their width
   const FixLayout lay(M);
   const uint32_t sb = smem_u32(smem);
-  uint64_t *in_bar = reinterpret_cast<uint64_t *>(smem + lay.bars);
+  uint64_t *in_bar = reinterpret_cast<uint64_t *>(smem + lay.bars);  // stages at [0], [2]
   uint64_t *mma_bar = in_bar + 1;
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(in_bar + 2);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(in_bar + 3);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(in_bar + 3);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(in_bar + 4);
   float *gs_f = reinterpret_cast<float *>(smem + lay.gs);
   float *usk = reinterpret_cast<float *>(smem + lay.usk);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q4 = warp & 3, ch = warp >> 2, row = 32 * q4 + lane;
-  const int seg = blockIdx.x, bh = blockIdx.y;
-  const int t0 = seg * p.tps, t1 = min(t0 + p.tps, p.nt);
   const int half = MB / 2;
+  // flat work: unit u = (bh, tile) over the first (P - 1) * tps tiles of each head
+  const long long per_head = (long long)(p.P - 1) * p.tps;
+  const long long units = per_head * p.BH;
+  const long long u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
 
   if (tid == 0) {
     mbar_init(in_bar, 1);
+    mbar_init(in_bar + 2, 1);
     mbar_init(mma_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -759,14 +725,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i = idx / M, m = idx - i * M;
       st_bf16_scalar(smem, lay.w + sw128_offset(m, i, M), p.w[idx]);
     }
-  }
-  {
-    const float *g = p.gstates + ((size_t)bh * p.P + seg + 1) * (size_t)M * DP;
-    for (int idx = tid; idx < M * D; idx += kThreads) {
-      const int f = idx / D, e = idx - f * D;
-      st_bf16_scalar(smem, lay.gb + sw128_offset(f, e, M), g[(size_t)f * DP + e]);
-    }
-    for (int f = tid; f < M; f += kThreads) gs_f[f] = g[(size_t)f * DP + D];
   }
   if (MB < 128) {
     for (int idx = tid; idx < kTile * 128; idx += kThreads) {
@@ -779,11 +737,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = *tslot;
-  const uint32_t s_w = sb + lay.w, s_k = sb + lay.k, s_v = sb + lay.v, s_phk = sb + lay.phk;
+  const uint32_t s_w = sb + lay.w, s_phk = sb + lay.phk;
   const uint32_t s_gb = sb + lay.gb;
   const uint32_t tile_bytes = kTile * D * 2;
   constexpr uint32_t kF = 0, kDV = 128, kDK = 192;  // TMEM columns
-  uint32_t in_phase = 0, mma_phase = 0;
+  uint32_t in_phase0 = 0, in_phase1 = 0, mma_phase = 0;
+  auto unit_of = [&](long long u, int &bh, int &t, int &seg) {
+    bh = (int)(u / per_head);
+    t = (int)(u - (long long)bh * per_head);
+    seg = t / p.tps;
+  };
+  auto issue_in = [&](long long u, int stage) {
+    int bh, t, seg;
+    unit_of(u, bh, t, seg);
+    mbar_arrive_expect_tx(in_bar + 2 * stage, 2 * tile_bytes);
+    tma_load_3d(smem + lay.k + stage * tile_bytes, &tmK, in_bar + 2 * stage, 0, t * kTile, bh);
+    tma_load_3d(smem + lay.v + stage * tile_bytes, &tmV, in_bar + 2 * stage, 0, t * kTile, bh);
+  };
   auto wait_mma = [&]() {
     __syncwarp();
     mbar_wait(mma_bar, mma_phase, p.status, abort_flag);
@@ -796,16 +766,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
   };
 
-  for (int t = t0; t < t1; ++t) {
+  if (tid == 0 && u0 < u1) issue_in(u0, 0);
+  int cur_key = -1;  // (bh, seg) whose G_end is loaded
+  for (long long u = u0; u < u1; ++u) {
+    const int stage = (int)((u - u0) & 1);
+    int bh, t, seg;
+    unit_of(u, bh, t, seg);
+    const int key = bh * p.P + seg;
+    if (key != cur_key) {
+      // G_end(s) = gstates[s + 1] after the reverse scan -> bf16 [M][64] + G_S
+      __syncthreads();
+      const float *g = p.gstates + ((size_t)bh * p.P + seg + 1) * (size_t)M * DP;
+      for (int idx = tid; idx < M * D; idx += kThreads) {
+        const int f = idx / D, e = idx - f * D;
+        st_bf16_scalar(smem, lay.gb + sw128_offset(f, e, M), g[(size_t)f * DP + e]);
+      }
+      for (int f = tid; f < M; f += kThreads) gs_f[f] = g[(size_t)f * DP + D];
+      fence_async_smem();
+      cta_sync();
+      cur_key = key;
+    }
+    const uint32_t s_k = sb + lay.k + stage * tile_bytes, s_v = sb + lay.v + stage * tile_bytes;
     const int valid = min(kTile, p.L - t * kTile);
     const bool live = row < valid;
-    if (tid == 0) {
-      mbar_arrive_expect_tx(in_bar, 2 * tile_bytes);
-      tma_load_3d(smem + lay.k, &tmK, in_bar, 0, t * kTile, bh);
-      tma_load_3d(smem + lay.v, &tmV, in_bar, 0, t * kTile, bh);
-    }
-    mbar_wait(in_bar, in_phase, p.status, abort_flag);
-    in_phase ^= 1;
+    mbar_wait(in_bar + 2 * stage, stage ? in_phase1 : in_phase0, p.status, abort_flag);
+    if (stage) in_phase1 ^= 1; else in_phase0 ^= 1;
+    if (tid == 0 && u + 1 < u1) issue_in(u + 1, stage ^ 1);
     const float ck = FAVOR ? favor_row_const(tile_row_sqnorm(s_k, row, D), M) : 0.f;
     float uk = 0.f;
     for (int b = 0; b < nb; ++b) {
@@ -920,6 +906,7 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   Params p{};
   p.L = pl.L; p.M = pl.M; p.nt = pl.tc_tiles; p.P = pl.P; p.tps = pl.cps; p.favor = FAVOR;
+  p.BH = pl.BH;
   p.dq = static_cast<__nv_bfloat16 *>(a.dq);
   p.dk = static_cast<__nv_bfloat16 *>(a.dk);
   p.dv = static_cast<__nv_bfloat16 *>(a.dv);
@@ -966,8 +953,13 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
     auto kern = tc_bwd_fix_kernel<FAVOR>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long units = (long long)(pl.P - 1) * pl.cps * pl.BH;
+    const int grid = (int)std::min<long long>(sms, units);
     ProfScope ps("tc_backward_fix", st);
-    kern<<<dim3(pl.P - 1, pl.BH), kThreads, smem, st>>>(mk, mv, p);
+    kern<<<grid, kThreads, smem, st>>>(mk, mv, p);
     e = cudaGetLastError();
   }
   return e;

@@ -54,20 +54,24 @@ __device__ __forceinline__ uint64_t make_desc(uint32_t saddr, uint32_t lbo, uint
 
 constexpr uint32_t kSwizzle128 = 2;
 
+// The start address is the low field of a descriptor, in 16-byte units, and
+// no operand crosses the 256 KB it can address, so stepping along K is an
+// integer add to a loop-invariant base descriptor.
+
 // K-major operand: rows [row0, row0 + extent) of a `rows`-row tile, K step s
 // (16 elements).
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, uint32_t rows, uint32_t row0,
                                                 uint32_t s) {
-  const uint32_t addr = base + (s >> 2) * rows * 128u + (row0 >> 3) * 1024u + (s & 3u) * 32u;
-  return make_desc(addr, 16u, 1024u, kSwizzle128);
+  return make_desc(base + (row0 >> 3) * 1024u, 16u, 1024u, kSwizzle128) +
+         (uint64_t)((s >> 2) * rows * 8u + (s & 3u) * 2u);
 }
 
 // MN-major operand: MN columns [mn0, ...) (mn0 a multiple of 64) of a tile with
 // `rows` K rows, K step s (16 rows).
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, uint32_t rows, uint32_t mn0,
                                                  uint32_t s) {
-  const uint32_t addr = base + (mn0 >> 6) * rows * 128u + s * 2048u;
-  return make_desc(addr, rows * 128u, 1024u, kSwizzle128);
+  return make_desc(base + (mn0 >> 6) * rows * 128u, rows * 128u, 1024u, kSwizzle128) +
+         (uint64_t)(s * 128u);
 }
 
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
@@ -373,7 +377,7 @@ __host__ __device__ __forceinline__ uint32_t n16_offset(uint32_t k, uint32_t n) 
 }
 
 __device__ __forceinline__ uint64_t desc_n16(uint32_t base, uint32_t s) {
-  return make_desc(base + s * 512u, 256u, 128u, 0u);
+  return make_desc(base, 256u, 128u, 0u) + (uint64_t)(s * 32u);
 }
 
 // Increment of one 128-feature block of R'^T over one tile:
@@ -474,6 +478,44 @@ __device__ __forceinline__ void ld_shared_v4f(uint32_t addr, float *v) {
                : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
                : "r"(addr)
                : "memory");
+}
+
+}  // namespace tc
+}  // namespace slim
+
+namespace slim {
+namespace tc {
+
+// Two 32-column TMEM loads (any two addresses of this warp's lanes) with a
+// single wait, so their latencies overlap.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t a0, uint32_t a1, float *v0, float *v1) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, "
+      "%42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, "
+      "%60, %61, %62, %63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]),
+        "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]),
+        "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),
+        "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]),
+        "=r"(r[62]), "=r"(r[63])
+      : "r"(a0), "r"(a1)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v0[i] = __uint_as_float(r[i]);
+    v1[i] = __uint_as_float(r[32 + i]);
+  }
 }
 
 }  // namespace tc

@@ -255,6 +255,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   // phi = exp2(F log2 e + c) from TMEM into the swizzled bf16 tile
   auto favor_epilogue = [&](uint32_t t_in, uint32_t s_out, int cols, float c_row, bool zero_row) {
+    if (cols == 64) {
+      float v[64];
+      tmem_ld32x2(tmem_addr(tbase, 32 * q4, t_in + 64 * ch), tmem_addr(tbase, 32 * q4, t_in + 64 * ch + 32), v,
+                  v + 32);
+#pragma unroll
+      for (int i = 0; i < 64; ++i) v[i] = zero_row ? 0.f : favor_feature(v[i], c_row);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) st_bf16x8(s_out + sw128_offset(row, 64 * ch + 8 * j, kTile), v + 8 * j);
+      return;
+    }
     for (int c0 = ch * cols; c0 < (ch + 1) * cols; c0 += 32) {
       float v[32];
       tmem_ld32(tmem_addr(tbase, 32 * q4, t_in + c0), v);
@@ -370,14 +380,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (MODE == MODE_FWD) {
       // masked A (diagonal kept) -> bf16 into the phi_q buffer
-      for (int c0 = ch * 64; c0 < ch * 64 + 64; c0 += 32) {
-        float v[32];
-        tmem_ld32(tmem_addr(tbase, 32 * q4, lay.t_a + c0), v);
+      {
+        float v[64];
+        tmem_ld32x2(tmem_addr(tbase, 32 * q4, lay.t_a + 64 * ch), tmem_addr(tbase, 32 * q4, lay.t_a + 64 * ch + 32),
+                    v, v + 32);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (c0 + i > row) v[i] = 0.f;
+        for (int i = 0; i < 64; ++i)
+          if (64 * ch + i > row) v[i] = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) st_bf16x8(s_phq + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
+        for (int j = 0; j < 8; ++j) st_bf16x8(s_phq + sw128_offset(row, 64 * ch + 8 * j, kTile), v + 8 * j);
       }
       fence_async_smem();
       cta_sync();
