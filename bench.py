@@ -57,6 +57,47 @@ def work_per_token_head(wl):
     return {"fwd_flops": fwd, "bwd_flops": bwd, "fwd_bytes": 4 * d * s, "bwd_bytes": 7 * d * s}
 
 
+# sources whose digest tags a recorded DRAM-traffic figure (profiles/*.md lines
+# "traffic: <workload> <token-heads> <kernel> <bytes> sources=<digest>")
+KERNEL_SOURCES = {
+    "tc_backward": ("tc_backward.cu", "tc_common.cuh", "common.cuh"),
+    "tc_forward": ("tc_forward.cu", "tc_common.cuh", "common.cuh"),
+}
+
+
+def source_digest(kernel):
+    import hashlib
+    files = KERNEL_SOURCES.get(kernel)
+    if files is None:
+        return None
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "sub_linear_memory_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, wl_name, token_heads):
+    """DRAM bytes per launch from an ncu capture recorded under profiles/,
+    scaled to this launch's token-heads (the kernels stream each token-head's
+    rows once, so traffic grows in proportion); None when no capture of this
+    workload exists or the kernel's sources changed since it was taken."""
+    digest = source_digest(kernel)
+    pdir = os.path.join(ROOT, "profiles")
+    if digest is None or not os.path.isdir(pdir):
+        return None
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith(".md"):
+            continue
+        with open(os.path.join(pdir, fn)) as fh:
+            for ln in fh:
+                f = ln.split()
+                if len(f) == 6 and f[0] == "traffic:" and f[1] == wl_name and f[3] == kernel \
+                        and f[5] == "sources=" + digest:
+                    return float(f[4]) * token_heads / float(f[2])
+    return None
+
+
 KERNEL_WORK = {
     # kernel name -> which algorithmic unit one launch of it processes in full
     "gen_forward": "fwd", "tc_forward": "fwd",
@@ -347,7 +388,7 @@ def run_native(args, wl):
                 roofline = {"bound": "hbm", "achieved": nb / avg_s / 1e9,
                             "peak": peaks["hbm_gbs"], "unit": "GB/s"}
             roofline["frac"] = roofline["achieved"] / roofline["peak"]
-            roofline["traffic"] = None
+            roofline["traffic"] = recorded_traffic(name, wl.name, th)
             roofline["kernel"] = name
             roofline["avg_launch_ms"] = total_ms / launches
             roofline["peak_source"] = peaks["source"] + " (sustained bf16 / copy bandwidth)"
@@ -398,8 +439,8 @@ def run_native(args, wl):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="l32k")
     ap.add_argument("--heads", default=None,

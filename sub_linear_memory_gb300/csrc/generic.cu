@@ -486,11 +486,24 @@ __global__ void scan_states_df_kernel(Plan p, float *hi, float *lo, int nseg) {
     const size_t bh = i / per, e = i - bh * per;
     float *h = hi + bh * p.P * per + e, *l = lo + bh * p.P * per + e;
     double acc = 0.0;
-    for (int s = 0; s < nseg; ++s) {
-      acc += (double)h[s * per] + (double)l[s * per];
-      const float fh = (float)acc;
-      h[s * per] = fh;
-      l[s * per] = (float)(acc - (double)fh);
+    // loads of a group are independent of the running sum, so they overlap
+    for (int s0 = 0; s0 < nseg; s0 += 8) {
+      float xh[8], xl[8];
+      const int n = min(8, nseg - s0);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < n) {
+          xh[j] = h[(size_t)(s0 + j) * per];
+          xl[j] = l[(size_t)(s0 + j) * per];
+        }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < n) {
+          acc += (double)xh[j] + (double)xl[j];
+          const float fh = (float)acc;
+          h[(size_t)(s0 + j) * per] = fh;
+          l[(size_t)(s0 + j) * per] = (float)(acc - (double)fh);
+        }
     }
   }
 }
