@@ -39,6 +39,8 @@ struct Plan {
                        // CUDA-core path, fp32 [BH][P][M][dp] on the tensor path
   size_t scratch_off;  // [BH * P][scratch_stride]
   size_t dwpart_off;   // [BH * P][d][M] (backward with dW only)
+  size_t wimg_off;     // tensor path, FAVOR+: W^T as the bf16 [M][64] swizzled
+                       // shared-memory image the kernels bulk-copy
   size_t scratch_stride;
   size_t total_floats;
 };

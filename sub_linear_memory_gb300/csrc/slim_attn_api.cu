@@ -151,6 +151,7 @@ Plan make_plan(int B, int H, int L, int d, int M, int chunk, bool favor, bool bw
   p.scratch_stride = path == 2 ? 0 : align_floats(generic_scratch_floats(p, bwd));
   p.scratch_off = off; off += p.scratch_stride * p.BH * p.P;
   p.dwpart_off = off; if (bwd && want_dw) off += align_floats((size_t)p.BH * p.P * d * M);
+  p.wimg_off = off; if (path == 2 && favor) off += align_floats((size_t)M * 32);
   p.total_floats = off;
   return p;
 }

@@ -3,14 +3,14 @@
 // "Sub-Linear Memory: How to Make Performers SLiM", sections 2.1 and 3.2.
 // One CTA owns one segment of consecutive 128-row tiles of one (b, h)
 // problem and carries the stacked prefix-sum state R' = [R ; S^T] across
-// tiles (the slice recurrence of eq. (16)-(18)).  Per tile (rows l of the
-// tile, feature block h of at most 128 features):
-//   F      = X W_h                     (MMA; X = Q or K, K-major operands)
+// tiles (the slice recurrence of eq. (16)-(18)).  Per tile, for each block h
+// of at most 128 features:
+//   F      = X W_h                     (MMA; X = K, then Q)
 //   phi    = exp(F - |x|^2/2)/sqrt(M)  (epilogue: TMEM -> bf16 swizzled smem)
-//   A     += phi_q,h phi_k,h^T         (MMA, fp32 in TMEM)
-//   num'  += phi_q,h [R_h, S_h]^T      (MMA; bf16 copies of R and of S as
-//                                       a high and a low part in smem)
 //   R'_h  += phi_k,h^T [V, 1]          (MMA; fp32 master state in TMEM)
+//   A     += phi_q,h phi_k,h^T         (MMA)
+//   num'  += phi_q,h [R_h, S_h]^T      (MMA; bf16 copies of R(t-1) and of S
+//                                       as a high and a low part in smem)
 // then A is masked to its lower triangle (diagonal kept) and rounded to bf16,
 //   num'  += tril(A) [V, 1]
 // and Y = num / den with den = num'[d] + num'[d + 1].  A tile of 128 rows
@@ -18,12 +18,22 @@
 // recurrence is exact for any slice size (section 3.4), so the tiling only
 // changes rounding.
 //
+// The kernel is warp-specialised so that the tensor pipe, the exponentials
+// and the loads overlap across tiles:
+//   warp 0      TMA producer: K, Q, V tiles into a ring of shared slots;
+//   warp 1      MMA issuer (one thread);
+//   warps 2-9   epilogue: two threads per row, each half of the columns.
+// Features and scores go through two TMEM buffers used in turn, so the next
+// feature MMA runs while the epilogue turns the previous one into phi.  Every
+// hand-off is an mbarrier; every wait is bounded.
+//
 // MODE_STATE runs only the K side and writes the segment's total R' (the
-// rows eq. (3) adds) for the segment scan.  With `exact` set (the backward's
-// pre-pass) each tile's increment is formed by an MMA that restarts at zero
-// and is added to a double-float (hi, lo) total, so the backward can later
-// remove exactly the same values; otherwise (the forward's pre-pass, which
-// never removes anything) the MMA accumulates in place.
+// rows eq. (3) adds) for the segment scan.  Each tile's increment is an MMA
+// that restarts at zero -- the same sequence the backward issues to remove
+// it again -- and the epilogue adds it into an fp32 master with CUDA-core
+// (round-to-nearest) adds.  Accumulating many tiles in place on the tensor
+// pipe loses low bits of the small addends; the backward recovers the first
+// tiles' small states by subtraction from this total and would expose that.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -36,99 +46,136 @@ namespace tcf {
 
 using namespace slim::tc;
 
-constexpr int kThreads = 256;
 constexpr int kTile = 128;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
 
 enum { MODE_STATE = 0, MODE_FWD = 1 };
 
 struct Params {
-  int L, M, nt, P, tps, favor, exact;
+  int L, M, nt, P, tps;
   __nv_bfloat16 *y;
-  const float *w;
+  const __nv_bfloat16 *wimg;  // W^T shared-memory image (FAVOR+)
   float *states;     // fp32 [BH][P][M][D + 1]: high parts of the segment states
   float *states_lo;  // same layout: low parts
   int *status;
 };
 
-template <int D>
-struct Layout {
-  // shared memory (bytes from a 1024-aligned base)
-  uint32_t w, q, k, v, phk, phq, rb, ones, sb, bars, total;
-  // TMEM columns
-  uint32_t t_f, t_f2, t_a, t_num, t_r;
-  // TMEM columns of the state pre-pass: increment, (hi, lo) totals
-  uint32_t s_delta, s_hi, s_lo;
-  __host__ __device__ Layout(int M, bool favor) {
-    const uint32_t tile = kTile * D * 2;  // one [128][D] bf16 tile
-    uint32_t o = 0;
-    w = o; o += favor ? (uint32_t)M * 128u : 0u;  // W^T as [M][64] bf16 (D == 64)
-    q = o; o += tile;
-    k = o; o += tile;
-    v = o; o += tile;
-    phk = o; o += kTile * 128 * 2;
-    phq = o; o += kTile * 128 * 2;  // also the masked A tile
-    rb = o; o += (uint32_t)M * D * 2;
-    ones = o; o += 4096;            // [128][16] no-swizzle: column 0 = 1
-    sb = o; o += (uint32_t)M * 32u; // [M][16] no-swizzle: columns 0, 1 = S high, S low
-    bars = o; o += 64;
-    total = o;
-    const int nh = (M + 127) / 128;
-    t_f = 0;
-    t_a = nh > 1 ? 128u : 0u;
-    t_num = nh > 1 ? 256u : 128u;
-    t_r = t_num + D + 16;
-    t_f2 = nh > 1 ? t_f : t_r + (uint32_t)(D + 16);  // a second feature buffer when it fits
-    s_delta = 0;
-    s_hi = (D + 16 > 128) ? (uint32_t)(D + 16) : 128u;
-    s_lo = s_hi + nh * (D + 16);
-  }
+template <int D, bool FAVOR, int MODE>
+struct Cfg {
+  static constexpr int kSlots = D == 128 ? 3 : 4;         // ring of [128][D] bf16 tiles
+  static constexpr int kLoads = MODE == MODE_FWD ? 3 : 2;  // per tile: K, (Q), V
+  static constexpr int kNbuf = FAVOR && MODE == MODE_FWD ? 2 : 1;  // TMEM buffers for F and A
+  static constexpr int kGroup = 1;                         // state pass: tiles per partial
+  static constexpr uint32_t kTileBytes = kTile * D * 2;
+  static constexpr int kCols = D + 16;                     // TMEM columns of num' or one R' block
+};
+
+// mbarrier indices
+enum {
+  B_FULL = 0,       // [slots] TMA -> consumers
+  B_EMPTY = 4,      // [slots] consumers -> TMA (1 MMA arrival + 8 epilogue warps)
+  B_FFULL = 8,      // [2] F or A ready in TMEM buffer
+  B_FEMPTY = 10,    // [2] TMEM buffer read out by the epilogue
+  B_PHK = 12,       // phi_k block stored
+  B_PHQ = 13,       // phi_q block stored
+  B_PHFREE = 14,    // MMAs reading the previous feature block done
+  B_AFULL = 15,     // A and the tile's state update complete (state pass: group partial ready)
+  B_ATFULL = 16,    // masked A stored
+  B_NUMFULL = 17,   // num' complete
+  B_NUMEMPTY = 18,  // num' read out
+  B_RBFULL = 19,    // R(t) read out of TMEM, bf16 copies refreshed (state pass: partial free)
+  B_DONE = 20,      // MMA drain
+  B_SETUP = 21,     // set-up copies (W image, incoming state)
+  B_COUNT = 22
 };
 
 template <int D, bool FAVOR, int MODE>
+struct Layout {
+  using C = Cfg<D, FAVOR, MODE>;
+  // shared memory (bytes from a 1024-aligned base)
+  uint32_t w, slots, phk, phq, rb, sb, ones, bars, total;
+  // TMEM columns
+  uint32_t t_buf0, t_buf1, t_num, t_r, t_m;
+  __host__ __device__ explicit Layout(int M) {
+    uint32_t o = 0;
+    w = o; o += FAVOR ? (uint32_t)M * 128u : 0u;  // W^T as [M][64] bf16 (D == 64)
+    slots = o; o += C::kSlots * C::kTileBytes;
+    phk = o; o += kTile * 128 * 2;                 // one feature block of phi_k
+    phq = o; o += MODE == MODE_FWD ? kTile * 128 * 2 : 0u;  // phi_q block, then masked A
+    rb = o; o += MODE == MODE_FWD ? (uint32_t)M * D * 2 : 0u;
+    sb = o; o += MODE == MODE_FWD ? (uint32_t)M * 32u : 0u;  // [M][16]: S high, S low
+    ones = o; o += 4096;                            // [128][16] no-swizzle: column 0 = 1
+    bars = o; o += 8 * B_COUNT + 16;
+    total = o;
+    t_buf0 = 0;
+    t_buf1 = C::kNbuf > 1 ? 128u : 0u;
+    const uint32_t used = (FAVOR || MODE == MODE_FWD) ? 128u * C::kNbuf : 0u;
+    t_num = used;
+    t_r = MODE == MODE_FWD ? t_num + C::kCols : used;  // R' (state pass: group partial)
+    t_m = t_r + (M > 128 ? 2u : 1u) * C::kCols;        // state pass: fp32 master total
+  }
+};
+
+template <int D, bool FAVOR, int MODE, int M>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, Params p) {
+  using C = Cfg<D, FAVOR, MODE>;
+  constexpr int NC = C::kCols;
+  constexpr int nb = (M + 127) / 128, FB = M < 128 ? M : 128, DP = D + 1;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem =
       reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const Layout<D> lay(p.M, FAVOR);
+  const Layout<D, FAVOR, MODE> lay(M);
   const uint32_t sbase = smem_u32(smem);
-  uint64_t *qk_bar = reinterpret_cast<uint64_t *>(smem + lay.bars);
-  uint64_t *v_bar = qk_bar + 1;
-  uint64_t *mma_bar = qk_bar + 2;
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(qk_bar + 3);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(qk_bar + 4);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + lay.bars);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + B_COUNT);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar + B_COUNT) + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q4 = warp & 3, ch = warp >> 2, row = 32 * q4 + lane;
   const int seg = blockIdx.x, bh = blockIdx.y;
-  const int M = p.M, nh = (M + 127) / 128, DP = D + 1;
-  const int t0 = seg * p.tps, t1 = min(t0 + p.tps, p.nt);
-  const bool exact = MODE == MODE_STATE && p.exact;
-  // two feature buffers let the Q- and K-side feature MMAs run back to back
-  const bool dual_f = FAVOR && MODE == MODE_FWD && nh == 1;
+  const int t0 = seg * p.tps, t1 = min(t0 + p.tps, p.nt), ntl = max(t1 - t0, 0);
 
   if (tid == 0) {
-    mbar_init(qk_bar, 1);
-    mbar_init(v_bar, 1);
-    mbar_init(mma_bar, 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(bar + B_FULL + s, 1);
+      mbar_init(bar + B_EMPTY + s, 1 + kEpiWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar + B_FFULL + b, 1);
+      mbar_init(bar + B_FEMPTY + b, kEpiWarps);
+    }
+    mbar_init(bar + B_PHK, kEpiWarps);
+    mbar_init(bar + B_PHQ, kEpiWarps);
+    mbar_init(bar + B_PHFREE, 1);
+    mbar_init(bar + B_AFULL, 1);
+    mbar_init(bar + B_ATFULL, kEpiWarps);
+    mbar_init(bar + B_NUMFULL, 1);
+    mbar_init(bar + B_NUMEMPTY, kEpiWarps);
+    mbar_init(bar + B_RBFULL, kEpiWarps);
+    mbar_init(bar + B_DONE, 1);
+    mbar_init(bar + B_SETUP, 1);
     *abort_flag = 0;
     fence_barrier_init();
+    // W^T image and the incoming state (high parts: the forward's master is
+    // fp32, below which the low parts do not register) by bulk copy
+    const uint32_t wbytes = FAVOR ? (uint32_t)M * 128u : 0u;
+    const uint32_t sbytes = (MODE == MODE_FWD && seg > 0) ? (uint32_t)(M * DP * 4) : 0u;
+    if (wbytes + sbytes > 0) {
+      mbar_arrive_expect_tx(bar + B_SETUP, wbytes + sbytes);
+      if (wbytes) bulk_load(smem + lay.w, p.wimg, wbytes, bar + B_SETUP);
+      if (sbytes)
+        bulk_load(smem + lay.slots, p.states + ((size_t)bh * p.P + seg - 1) * (size_t)M * DP, sbytes, bar + B_SETUP);
+    }
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
     if (MODE == MODE_FWD) prefetch_tmap(&tmQ);
   }
   if (warp == 0) tmem_alloc(tslot, 512);
 
-  // constant operands: W^T (bf16, K-major rows = features), the ones block,
-  // zero padding of phi_k beyond M (the state MMA always reads 128 features)
-  if (FAVOR) {
-    for (int idx = tid; idx < M * D; idx += kThreads) {
-      const int i = idx / M, m = idx - i * M;
-      *reinterpret_cast<__nv_bfloat16 *>(smem + lay.w + sw128_offset(m, i, M)) =
-          __float2bfloat16_rn(p.w[idx]);
-    }
-  }
+  // constant operands: the ones block, zero padding of phi_k beyond M (the
+  // state MMA always reads 128 features)
   for (int idx = tid; idx < kTile * 16; idx += kThreads) {
     const int r = idx >> 4, x = idx & 15;
     *reinterpret_cast<__nv_bfloat16 *>(smem + lay.ones + n16_offset(r, x)) = __float2bfloat16_rn(x == 0 ? 1.f : 0.f);
@@ -140,360 +187,481 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (M < 128) {
     for (int idx = tid; idx < kTile * 128; idx += kThreads) {
       const int r = idx >> 7, x = idx & 127;
-      if (x >= M) *reinterpret_cast<__nv_bfloat16 *>(smem + lay.phk + sw128_offset(r, x, kTile)) =
-          __float2bfloat16_rn(0.f);
+      if (x >= M)
+        *reinterpret_cast<__nv_bfloat16 *>(smem + lay.phk + sw128_offset(r, x, kTile)) = __float2bfloat16_rn(0.f);
     }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = *tslot;
-
-  // S of feature f as the bf16 pair (high, low) in columns 0, 1 of the S block
-  auto put_s = [&](int f, float sv) {
-    const __nv_bfloat16 hi = __float2bfloat16_rn(sv);
-    *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(f, 0)) = hi;
-    *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(f, 1)) =
-        __float2bfloat16_rn(sv - __bfloat162float(hi));
-  };
-
-  // incoming state of the segment -> TMEM master, bf16 copies of R and S
-  // (the pre-pass instead starts its totals at zero)
-  const int ncols = D + 16, csplit = ((ncols / 16 + 1) / 2) * 16;
-  if (MODE == MODE_STATE) {
-    for (int b = 0; b < nh; ++b) {
-      float z[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) z[i] = 0.f;
-      for (int c = ch ? csplit : 0; c < (ch ? ncols : csplit); c += 16) {
-        if (exact) {
-          tmem_st16(tmem_addr(tbase, 32 * q4, lay.s_hi + b * ncols + c), z);
-          tmem_st16(tmem_addr(tbase, 32 * q4, lay.s_lo + b * ncols + c), z);
-        } else {
-          tmem_st16(tmem_addr(tbase, 32 * q4, lay.t_r + b * ncols + c), z);
-        }
-      }
-    }
-    tmem_st_wait();
-  } else {
-    const size_t off = ((size_t)bh * p.P + seg - 1) * (size_t)M * DP;
-    const float *st = seg > 0 ? p.states + off : nullptr;
-    const float *st_lo = seg > 0 ? p.states_lo + off : nullptr;
-    for (int b = 0; b < nh; ++b) {
-      // warps 4b..4b+3 own block b when nh == 2; all warps split columns when nh == 1
-      if (nh == 2 && ch != b) continue;
-      const int f = 128 * b + row;
-      const int c_lo = (nh == 2) ? 0 : (ch == 0 ? 0 : (ncols / 32) * 16);
-      const int c_hi = (nh == 2) ? ncols : (ch == 0 ? (ncols / 32) * 16 : ncols);
-      for (int c = c_lo; c < c_hi; c += 16) {
-        float v[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int e = c + i;
-          v[i] = (st && f < M && e <= D) ? st[(size_t)f * DP + e] + st_lo[(size_t)f * DP + e] : 0.f;
-        }
-        tmem_st16(tmem_addr(tbase, 32 * q4, lay.t_r + b * ncols + c), v);
-        if (f < M) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int e = c + i;
-            if (e < D)
-              *reinterpret_cast<__nv_bfloat16 *>(smem + lay.rb + sw128_offset(f, e, M)) = __float2bfloat16_rn(v[i]);
-            else if (e == D)
-              put_s(f, v[i]);
-          }
-        }
-      }
-    }
-    tmem_st_wait();
   }
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  const uint32_t tbase = *tslot;
 
-  const uint32_t tile_bytes = kTile * D * 2;
-  uint32_t qk_phase = 0, v_phase = 0, mma_phase = 0;
-  auto issue_qk = [&](int t) {
-    const uint32_t bytes = (MODE == MODE_FWD ? 2u : 1u) * tile_bytes;
-    mbar_arrive_expect_tx(qk_bar, bytes);
-    for (int c = 0; c < D; c += 64) {
-      tma_load_3d(smem + lay.k + c * kTile * 2, &tmK, qk_bar, c, t * kTile, bh);
-      if (MODE == MODE_FWD) tma_load_3d(smem + lay.q + c * kTile * 2, &tmQ, qk_bar, c, t * kTile, bh);
+  // incoming state of the segment -> TMEM master (and, in the forward, its
+  // bf16 copies); the state pass starts its master at zero.  The fp32
+  // [M][D + 1] state arrived in the (still unused) load slots.
+  {
+    const bool in = MODE == MODE_FWD && seg > 0;
+    if ((FAVOR || in) && !mbar_wait(bar + B_SETUP, 0, p.status, abort_flag)) {
+      // nothing usable arrived: the tiles below are skipped by the abort flag
     }
-  };
-  auto issue_v = [&](int t) {
-    mbar_arrive_expect_tx(v_bar, tile_bytes);
-    for (int c = 0; c < D; c += 64) tma_load_3d(smem + lay.v + c * kTile * 2, &tmV, v_bar, c, t * kTile, bh);
-  };
-  auto mma_sync_all = [&]() {
-    __syncwarp();
-    mbar_wait(mma_bar, mma_phase, p.status, abort_flag);
-    mma_phase ^= 1;
-    tc_fence_after();
-  };
-  auto cta_sync = [&]() {
+    const float *stage = reinterpret_cast<const float *>(smem + lay.slots);  // [M][D + 1] fp32
+    const int q4 = warp & 3, half = (warp - 2) >> 2, row = 32 * q4 + lane;
+    const uint32_t t_dst = MODE == MODE_FWD ? lay.t_r : lay.t_m;
+    constexpr int csplit = ((NC / 16 + 1) / 2) * 16;
+    for (int b = 0; b < nb; ++b) {
+      if (warp >= 2) {
+        const int c_lo = nb == 2 ? 0 : (half ? csplit : 0);
+        const int c_hi = nb == 2 ? (b == half ? NC : 0) : (half ? NC : csplit);
+        const int f = 128 * b + row;
+        for (int c = c_lo; c < c_hi; c += 16) {
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = (in && f < M && c + i <= D) ? stage[f * DP + c + i] : 0.f;
+          tmem_st16(tmem_addr(tbase, 32u * q4, t_dst + b * NC + c), v);
+          if (MODE == MODE_FWD && f < M) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 8)
+              if (c + i + 8 <= D) st_bf16x8(sbase + lay.rb + sw128_offset(f, c + i, M), v + i);
+            if (c <= D && D < c + 16) {
+              const __nv_bfloat16 hi = __float2bfloat16_rn(v[D - c]);
+              *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(f, 0)) = hi;
+              *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(f, 1)) =
+                  __float2bfloat16_rn(v[D - c] - __bfloat162float(hi));
+            }
+          }
+        }
+        tmem_st_wait();
+      }
+    }
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-  };
-
-  if (tid == 0 && t0 < t1) {
-    issue_qk(t0);
-    issue_v(t0);
   }
 
-  const uint32_t s_q = sbase + lay.q, s_k = sbase + lay.k, s_v = sbase + lay.v;
-  const uint32_t s_phk = sbase + lay.phk, s_phq = sbase + lay.phq, s_rb = sbase + lay.rb;
-  const uint32_t s_ones = sbase + lay.ones, s_w = sbase + lay.w, s_sb = sbase + lay.sb;
+  const uint32_t s_w = sbase + lay.w, s_phk = sbase + lay.phk, s_phq = sbase + lay.phq;
+  const uint32_t s_rb = sbase + lay.rb, s_sb = sbase + lay.sb, s_ones = sbase + lay.ones;
+  auto t_buf = [&](int b) { return b ? lay.t_buf1 : lay.t_buf0; };
+  auto slot_addr = [&](int n) { return sbase + lay.slots + (uint32_t)(n % C::kSlots) * C::kTileBytes; };
+  auto slot_par = [&](int n) { return (uint32_t)((n / C::kSlots) & 1); };
+  // the TMEM buffer of job j (features, then the tile's A, in issue order)
+  // and the index of that use of the buffer
+  auto job_buf = [&](int j) { return C::kNbuf > 1 ? (j & 1) : 0; };
+  auto job_use = [&](int j) { return C::kNbuf > 1 ? (j >> 1) : j; };
 
-  // feature MMA: F = X W_h^T for feature block h (nu features)
-  auto issue_features = [&](uint32_t s_x, uint32_t t_out, int h, int nu) {
-    const uint32_t idesc = make_idesc(128, nu, false, false);
-    for (int s = 0; s < D / 16; ++s)
-      mma_bf16(tbase + t_out, desc_kmajor(s_x, kTile, 0, s), desc_kmajor(s_w, M, 128 * h, s), idesc, s > 0);
-  };
-  // phi = exp2(F log2 e + c) from TMEM into the swizzled bf16 tile
-  auto favor_epilogue = [&](uint32_t t_in, uint32_t s_out, int cols, float c_row, bool zero_row) {
-    if (cols == 64) {
-      float v[64];
-      tmem_ld32x2(tmem_addr(tbase, 32 * q4, t_in + 64 * ch), tmem_addr(tbase, 32 * q4, t_in + 64 * ch + 32), v,
-                  v + 32);
-#pragma unroll
-      for (int i = 0; i < 64; ++i) v[i] = zero_row ? 0.f : favor_feature(v[i], c_row);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) st_bf16x8(s_out + sw128_offset(row, 64 * ch + 8 * j, kTile), v + 8 * j);
-      return;
-    }
-    for (int c0 = ch * cols; c0 < (ch + 1) * cols; c0 += 32) {
-      float v[32];
-      tmem_ld32(tmem_addr(tbase, 32 * q4, t_in + c0), v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = favor_feature(v[i], c_row);
-      if (zero_row) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int n = 0;
+      bool ok = true;
+      auto load = [&](const CUtensorMap *m, int t) {
+        const int s = n % C::kSlots, u = n / C::kSlots;
+        if (u > 0 && !mbar_wait(bar + B_EMPTY + s, (u - 1) & 1, p.status, abort_flag)) return false;
+        mbar_arrive_expect_tx(bar + B_FULL + s, C::kTileBytes);
+        for (int c = 0; c < D; c += 64)
+          tma_load_3d(smem + lay.slots + s * C::kTileBytes + c * kTile * 2, m, bar + B_FULL + s, c, t * kTile, bh);
+        ++n;
+        return true;
+      };
+      for (int t = t0; t < t1 && ok; ++t) {
+        ok = load(&tmK, t);
+        if (ok && MODE == MODE_FWD) ok = load(&tmQ, t);
+        if (ok) ok = load(&tmV, t);
       }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) st_bf16x8(s_out + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
+      // copies still in flight land before the CTA can leave
+      for (int m = max(0, n - C::kSlots); m < n; ++m) mbar_drain(bar + B_FULL + m % C::kSlots, slot_par(m));
+      if (FAVOR || (MODE == MODE_FWD && seg > 0)) mbar_drain(bar + B_SETUP, 0);
     }
-  };
-  auto elu_epilogue = [&](uint32_t s_x, uint32_t s_out, int cols, bool zero_row) {
-    for (int c0 = ch * cols; c0 < (ch + 1) * cols; c0 += 8) {
-      float v[8];
-      ld_bf16x8(s_x + sw128_offset(row, c0, kTile), v);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = zero_row ? 0.f : elu1_feature(v[i]);
-      st_bf16x8(s_out + sw128_offset(row, c0, kTile), v);
-    }
-  };
-
-  for (int t = t0; t < t1; ++t) {
-    const int valid = min(kTile, p.L - t * kTile);
-    const bool dead = row >= valid;  // padding rows past L: features forced to zero
-    mbar_wait(qk_bar, qk_phase, p.status, abort_flag);
-    qk_phase ^= 1;
-    float ck = 0.f, cq = 0.f;  // per-row exp2 offsets
-    if (FAVOR) {
-      ck = favor_row_const(tile_row_sqnorm(s_k, row, D), M);
-      if (MODE == MODE_FWD) cq = favor_row_const(tile_row_sqnorm(s_q, row, D), M);
-    }
-    if (FAVOR && tid == 0) {
-      issue_features(s_k, lay.t_f, 0, min(128, M));
-      if (dual_f) issue_features(s_q, lay.t_f2, 0, M);
-      mma_commit(mma_bar);
-    }
-    for (int h = 0; h < nh; ++h) {
-      const int nu = min(128, M - 128 * h);  // features in this block
-      const int cols = nu / 2;               // per thread (two threads per row)
-      // K side (its feature MMA was issued already)
-      if (FAVOR) {
-        mma_sync_all();
-        favor_epilogue(lay.t_f, s_phk, cols, ck, dead);
-        if (dual_f) favor_epilogue(lay.t_f2, s_phq, cols, cq, dead);
-      } else {
-        elu_epilogue(s_k, s_phk, cols, dead);
-        if (MODE == MODE_FWD) elu_epilogue(s_q, s_phq, cols, dead);
-      }
-      fence_async_smem();
-      cta_sync();
-      if (MODE == MODE_FWD && FAVOR && !dual_f) {
-        if (tid == 0) {
-          issue_features(s_q, lay.t_f, h, nu);
-          mma_commit(mma_bar);
-        }
-        mma_sync_all();
-        favor_epilogue(lay.t_f, s_phq, cols, cq, dead);
-        fence_async_smem();
-        cta_sync();
-      }
-      // next tile's Q/K can stream in once the last feature block is formed
-      if (h == nh - 1 && tid == 0 && t + 1 < t1) issue_qk(t + 1);
-      if (tid == 0) {
-        if (MODE == MODE_FWD) {
-          const uint32_t id_a = make_idesc(128, 128, false, false);
-          const uint32_t id_n = make_idesc(128, D, false, true);
-          const uint32_t id_s = make_idesc(128, 16, false, true);
-          for (int s = 0; s < nu / 16; ++s)
-            mma_bf16(tbase + lay.t_a, desc_kmajor(s_phq, kTile, 0, s), desc_kmajor(s_phk, kTile, 0, s), id_a,
-                     (h > 0 || s > 0));
-          for (int s = 0; s < nu / 16; ++s) {
-            mma_bf16(tbase + lay.t_num, desc_kmajor(s_phq, kTile, 0, s), desc_mnmajor(s_rb, M, 0, 8 * h + s), id_n,
-                     (h > 0 || s > 0));
-            mma_bf16(tbase + lay.t_num + D, desc_kmajor(s_phq, kTile, 0, s), desc_n16(s_sb, 8 * h + s), id_s,
-                     (h > 0 || s > 0));
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      auto wait = [&](int b, uint32_t par) {
+        if (ok) ok = mbar_wait(bar + b, par, p.status, abort_flag);
+        return ok;
+      };
+      const uint32_t id_a = make_idesc(128, 128, false, false);
+      const uint32_t id_n = make_idesc(128, D, false, true);
+      const uint32_t id_s = make_idesc(128, 16, false, true);
+      const uint32_t id_r = make_idesc(128, D, true, true);
+      const uint32_t id_r1 = make_idesc(128, 16, true, true);
+      int job = 0, n = 0;
+      // feature MMA into the next TMEM buffer: F = X W_h^T
+      auto f_job = [&](uint32_t s_x, int h) {
+        const int b = job_buf(job), u = job_use(job);
+        if (u > 0 && !wait(B_FEMPTY + b, (u - 1) & 1)) return;
+        tc_fence_after();
+        const uint32_t idesc = make_idesc(128, min(128, M - 128 * h), false, false);
+        for (int s = 0; s < D / 16; ++s)
+          mma_bf16(tbase + t_buf(b), desc_kmajor(s_x, kTile, 0, s), desc_kmajor(s_w, M, 128 * h, s), idesc, s > 0);
+        mma_commit(bar + B_FFULL + b);
+        ++job;
+      };
+      // the epilogue's initial state (or zero totals) is in TMEM
+      wait(B_RBFULL, 0);
+      for (int i = 0; i < ntl && ok; ++i) {
+        const int nK = n, nQ = n + 1, nV = n + C::kLoads - 1;
+        n += C::kLoads;
+        const uint32_t s_k = slot_addr(nK), s_q = slot_addr(nQ), s_v = slot_addr(nV);
+        if (FAVOR) {
+          if (!wait(B_FULL + nK % C::kSlots, slot_par(nK))) break;
+          if (MODE == MODE_FWD && !wait(B_FULL + nQ % C::kSlots, slot_par(nQ))) break;
+          tc_fence_after();
+          for (int h = 0; h < nb && ok; ++h) {
+            f_job(s_k, h);
+            if (MODE == MODE_FWD) f_job(s_q, h);
           }
-        }
-        if (h == 0) {
-          mbar_wait(v_bar, v_phase, p.status, abort_flag);
-          v_phase ^= 1;
-        }
-        if (exact) {
-          issue_state_delta(tbase + lay.s_delta, s_phk, s_v, s_ones, D);
+          if (!ok) break;
+          mma_commit(bar + B_EMPTY + nK % C::kSlots);
+          if (MODE == MODE_FWD) mma_commit(bar + B_EMPTY + nQ % C::kSlots);
         } else {
-          // the running state only moves forward here: accumulate in place
-          const uint32_t id_r = make_idesc(128, D, true, true);
-          const uint32_t id_r1 = make_idesc(128, 16, true, true);
-          const uint32_t t_r = tbase + lay.t_r + h * ncols;
-          for (int s = 0; s < kTile / 16; ++s) {
-            mma_bf16(t_r, desc_mnmajor(s_phk, kTile, 0, s), desc_mnmajor(s_v, kTile, 0, s), id_r, 1);
-            mma_bf16(t_r + D, desc_mnmajor(s_phk, kTile, 0, s), desc_n16(s_ones, s), id_r1, 1);
+          // elu+1 features are formed from K and Q by the epilogue alone
+          mbar_arrive(bar + B_EMPTY + nK % C::kSlots);
+          if (MODE == MODE_FWD) mbar_arrive(bar + B_EMPTY + nQ % C::kSlots);
+        }
+        const int ja = job;  // the tile's A job
+        const int gi = i % C::kGroup;  // state pass: position in the group
+        for (int h = 0; h < nb && ok; ++h) {
+          const uint32_t c = (uint32_t)(i * nb + h);
+          if (!wait(B_PHK, c & 1)) break;
+          if (h == 0) {
+            if (!wait(B_FULL + nV % C::kSlots, slot_par(nV))) break;
+            if (MODE == MODE_FWD && !wait(B_RBFULL, i & 1)) break;
+            // the group partial restarts at zero once the epilogue has added it
+            if (MODE == MODE_STATE && gi == 0 && i > 0 && !wait(B_RBFULL, (i / C::kGroup) & 1)) break;
           }
+          tc_fence_after();
+          // R'_h += phi_k,h^T [V, 1] (in place; the state pass restarts each group)
+          const uint32_t t_r = tbase + lay.t_r + h * NC;
+          for (int s = 0; s < kTile / 16; ++s) {
+            const uint32_t acc = (MODE == MODE_FWD || gi > 0 || s > 0) ? 1u : 0u;
+            mma_bf16(t_r, desc_mnmajor(s_phk, kTile, 0, s), desc_mnmajor(s_v, kTile, 0, s), id_r, acc);
+            mma_bf16(t_r + D, desc_mnmajor(s_phk, kTile, 0, s), desc_n16(s_ones, s), id_r1, acc);
+          }
+          if (MODE == MODE_FWD) {
+            if (!wait(B_PHQ, c & 1)) break;
+            if (h == 0) {
+              const int u = job_use(ja);
+              if (u > 0 && !wait(B_FEMPTY + job_buf(ja), (u - 1) & 1)) break;
+              if (i > 0 && !wait(B_NUMEMPTY, (i - 1) & 1)) break;
+            }
+            tc_fence_after();
+            const uint32_t t_a = tbase + t_buf(job_buf(ja));
+            const int nu = min(128, M - 128 * h);
+            for (int s = 0; s < nu / 16; ++s) {
+              const uint32_t acc = (h > 0 || s > 0) ? 1u : 0u;
+              const uint64_t aq = desc_kmajor(s_phq, kTile, 0, s);
+              mma_bf16(t_a, aq, desc_kmajor(s_phk, kTile, 0, s), id_a, acc);
+              mma_bf16(tbase + lay.t_num, aq, desc_mnmajor(s_rb, M, 0, 8 * h + s), id_n, acc);
+              mma_bf16(tbase + lay.t_num + D, aq, desc_n16(s_sb, 8 * h + s), id_s, acc);
+            }
+          }
+          mma_commit(bar + B_PHFREE);
         }
-        // the next feature block's K side shares this commit (F is free)
-        if (FAVOR && h + 1 < nh && !exact) issue_features(s_k, lay.t_f, h + 1, min(128, M - 128 * (h + 1)));
-        mma_commit(mma_bar);
-      }
-      if (exact) {
-        mma_sync_all();
-        // (hi, lo) total of block h += this tile's increment
-        df_update_tmem(tbase, 32 * q4, lay.s_delta, lay.s_hi + h * ncols, lay.s_lo + h * ncols,
-                       ch ? csplit : 0, ch ? ncols : csplit, 1.f);
-        cta_sync();
-        if (FAVOR && h + 1 < nh && tid == 0) {
-          issue_features(s_k, lay.t_f, h + 1, min(128, M - 128 * (h + 1)));
-          mma_commit(mma_bar);
+        if (!ok) break;
+        if (MODE == MODE_FWD) {
+          // A fills its buffer like an F job: one phase of that buffer's barrier
+          mma_commit(bar + B_FFULL + job_buf(ja));
+          ++job;
+          mma_commit(bar + B_AFULL);
+          if (!wait(B_ATFULL, i & 1)) break;
+          tc_fence_after();
+          // num' += tril(A) [V, 1]
+          for (int s = 0; s < kTile / 16; ++s) {
+            const uint64_t aa = desc_kmajor(s_phq, kTile, 0, s);
+            mma_bf16(tbase + lay.t_num, aa, desc_mnmajor(s_v, kTile, 0, s), id_n, 1);
+            mma_bf16(tbase + lay.t_num + D, aa, desc_n16(s_ones, s), id_s, 1);
+          }
+          mma_commit(bar + B_NUMFULL);
         }
-      } else if (h + 1 == nh || !FAVOR) {
-        mma_sync_all();
+        if (MODE == MODE_STATE && (gi == C::kGroup - 1 || i == ntl - 1)) mma_commit(bar + B_AFULL);
+        mma_commit(bar + B_EMPTY + nV % C::kSlots);
       }
+      mma_commit(bar + B_DONE);
+      mbar_drain(bar + B_DONE, 0);
     }
-    if (MODE == MODE_FWD) {
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int q4 = warp & 3, half = (warp - 2) >> 2, row = 32 * q4 + lane;
+    const uint32_t lane_base = 32u * q4;
+    bool ok = true;
+    auto wait = [&](int b, uint32_t par) {
+      if (ok) ok = mbar_wait(bar + b, par, p.status, abort_flag);
+      return ok;
+    };
+    auto arrive = [&](int b) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar + b);
+    };
+    // S of feature f as the bf16 pair (high, low) in columns 0, 1 of the S block
+    auto put_s = [&](int f, float sv) {
+      const __nv_bfloat16 hi = __float2bfloat16_rn(sv);
+      *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(f, 0)) = hi;
+      *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(f, 1)) =
+          __float2bfloat16_rn(sv - __bfloat162float(hi));
+    };
+    // columns [c_lo, c_hi) of R' block b handled by this thread: with two
+    // blocks each half of the warps owns one, with one they split its columns
+    const int csplit = ((NC / 16 + 1) / 2) * 16;
+    auto r_cols = [&](int b, int &c_lo, int &c_hi) {
+      if (nb == 2) {
+        c_lo = 0;
+        c_hi = b == half ? NC : 0;
+      } else {
+        c_lo = half ? csplit : 0;
+        c_hi = half ? NC : csplit;
+      }
+    };
+    auto put_rb = [&](int f, int c, const float *v) {
+      if (f >= M) return;
+#pragma unroll
+      for (int i = 0; i < 16; i += 8)
+        if (c + i + 8 <= D) st_bf16x8(s_rb + sw128_offset(f, c + i, M), v + i);
+      if (c <= D && D < c + 16) put_s(f, v[D - c]);
+    };
+
+    // the incoming state was placed in TMEM during set-up
+    arrive(B_RBFULL);
+
+    constexpr int FC = FAVOR ? 64 : D / 2;  // register columns of one phi half-row
+    const int fcols = FAVOR ? FB / 2 : D / 2;
+    auto store_phi = [&](uint32_t s_out, const float *v) {
+#pragma unroll
+      for (int j = 0; j < FC / 8; ++j)
+        if (8 * j < fcols) st_bf16x8(s_out + sw128_offset(row, fcols * half + 8 * j, kTile), v + 8 * j);
+    };
+    int job = 0, n = 0;
+    // the next F job from TMEM into registers; frees its buffer
+    auto load_f = [&](float *v) {
+      const int b = job_buf(job), u = job_use(job);
+      if (!wait(B_FFULL + b, u & 1)) return;
+      tc_fence_after();
+      const uint32_t a = tmem_addr(tbase, lane_base, t_buf(b) + fcols * half);
+      if (fcols == 64)
+        tmem_ld32x2(a, a + 32, v, v + 32);
+      else
+        tmem_ld32(a, v);
+      tc_fence_before();
+      arrive(B_FEMPTY + b);
+      ++job;
+    };
+    // phi of one half-row: FAVOR+ from the F job, elu+1 from the X tile
+    auto make_phi = [&](uint32_t s_x, float c_row, bool dead, float *v) {
+      if (FAVOR) {
+        load_f(v);
+#pragma unroll
+        for (int x = 0; x < FC; ++x)
+          if (x < fcols) v[x] = dead ? 0.f : favor_feature(v[x], c_row);
+      } else {
+#pragma unroll
+        for (int j = 0; j < FC / 8; ++j) {
+          ld_bf16x8(s_x + sw128_offset(row, FC * half + 8 * j, kTile), v + 8 * j);
+#pragma unroll
+          for (int x = 0; x < 8; ++x) v[8 * j + x] = dead ? 0.f : elu1_feature(v[8 * j + x]);
+        }
+      }
+    };
+
+    for (int i = 0; i < ntl && ok; ++i) {
+      const int t = t0 + i;
+      const int valid = min(kTile, p.L - t * kTile);
+      const bool dead = row >= valid;  // padding rows past L: features forced to zero
+      const int nK = n, nQ = n + 1, nV = n + C::kLoads - 1;
+      n += C::kLoads;
+      const uint32_t s_k = slot_addr(nK), s_q = slot_addr(nQ);
+      if (!wait(B_FULL + nK % C::kSlots, slot_par(nK))) break;
+      if (MODE == MODE_FWD && !wait(B_FULL + nQ % C::kSlots, slot_par(nQ))) break;
+      float ck = 0.f, cq = 0.f;  // per-row exp2 offsets
+      if (FAVOR) {
+        ck = favor_row_const(tile_row_sqnorm(s_k, row, D), M);
+        if (MODE == MODE_FWD) cq = favor_row_const(tile_row_sqnorm(s_q, row, D), M);
+        arrive(B_EMPTY + nK % C::kSlots);
+        if (MODE == MODE_FWD) arrive(B_EMPTY + nQ % C::kSlots);
+      }
+      for (int h = 0; h < nb && ok; ++h) {
+        const uint32_t c = (uint32_t)(i * nb + h);
+        float v[FC];
+        make_phi(s_k, ck, dead, v);
+        if (c > 0 && !wait(B_PHFREE, (c - 1) & 1)) break;
+        if (!ok) break;
+        store_phi(s_phk, v);
+        fence_async_smem();
+        arrive(B_PHK);
+        if (MODE == MODE_FWD) {
+          make_phi(s_q, cq, dead, v);
+          if (!ok) break;
+          store_phi(s_phq, v);
+          fence_async_smem();
+          arrive(B_PHQ);
+        }
+      }
+      if (!ok) break;
+      if (!FAVOR) {
+        arrive(B_EMPTY + nK % C::kSlots);
+        if (MODE == MODE_FWD) arrive(B_EMPTY + nQ % C::kSlots);
+      }
+      if (MODE == MODE_STATE) {
+        arrive(B_EMPTY + nV % C::kSlots);
+        if (i % C::kGroup == C::kGroup - 1 || i == ntl - 1) {
+          // master += group partial (round-to-nearest fp32 adds)
+          if (!wait(B_AFULL, (i / C::kGroup) & 1)) break;
+          tc_fence_after();
+          for (int b = 0; b < nb; ++b) {
+            int c_lo, c_hi;
+            r_cols(b, c_lo, c_hi);
+            for (int c = c_lo; c < c_hi; c += 16) {
+              float x[16], m[16];
+              tmem_ld16(tmem_addr(tbase, lane_base, lay.t_r + b * NC + c), x);
+              tmem_ld16(tmem_addr(tbase, lane_base, lay.t_m + b * NC + c), m);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) m[e] += x[e];
+              tmem_st16(tmem_addr(tbase, lane_base, lay.t_m + b * NC + c), m);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          arrive(B_RBFULL);
+        }
+        continue;
+      }
       // masked A (diagonal kept) -> bf16 into the phi_q buffer
       {
+        if (!wait(B_AFULL, i & 1)) break;
+        tc_fence_after();
+        const int b = job_buf(job);
         float v[64];
-        tmem_ld32x2(tmem_addr(tbase, 32 * q4, lay.t_a + 64 * ch), tmem_addr(tbase, 32 * q4, lay.t_a + 64 * ch + 32),
-                    v, v + 32);
+        const uint32_t a = tmem_addr(tbase, lane_base, t_buf(b) + 64 * half);
+        tmem_ld32x2(a, a + 32, v, v + 32);
+        tc_fence_before();
+        arrive(B_FEMPTY + b);
+        ++job;
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (64 * ch + i > row) v[i] = 0.f;
+        for (int x = 0; x < 64; ++x)
+          if (64 * half + x > row) v[x] = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) st_bf16x8(s_phq + sw128_offset(row, 64 * ch + 8 * j, kTile), v + 8 * j);
+        for (int j = 0; j < 8; ++j) st_bf16x8(s_phq + sw128_offset(row, 64 * half + 8 * j, kTile), v + 8 * j);
+        fence_async_smem();
+        arrive(B_ATFULL);
       }
-      fence_async_smem();
-      cta_sync();
-      if (tid == 0) {
-        const uint32_t id_n = make_idesc(128, D, false, true);
-        const uint32_t id_n1 = make_idesc(128, 16, false, true);
-        for (int s = 0; s < kTile / 16; ++s) {
-          mma_bf16(tbase + lay.t_num, desc_kmajor(s_phq, kTile, 0, s), desc_mnmajor(s_v, kTile, 0, s), id_n, 1);
-          mma_bf16(tbase + lay.t_num + D, desc_kmajor(s_phq, kTile, 0, s), desc_n16(s_ones, s), id_n1, 1);
-        }
-        mma_commit(mma_bar);
-      }
-      mma_sync_all();
-      if (tid == 0 && t + 1 < t1) issue_v(t + 1);
-      // Y = num / den
-      {
-        float dv[16];
-        tmem_ld16(tmem_addr(tbase, 32 * q4, lay.t_num + D), dv);
-        const float inv = 1.0f / (dv[0] + dv[1]);
-        __nv_bfloat16 *yrow = p.y + ((size_t)bh * p.L + (size_t)t * kTile + row) * D;
-        for (int c0 = ch * (D / 2); c0 < (ch + 1) * (D / 2); c0 += 32) {
-          float v[32];
-          tmem_ld32(tmem_addr(tbase, 32 * q4, lay.t_num + c0), v);
-          if (!dead) {
-            uint4 *dst = reinterpret_cast<uint4 *>(yrow + c0);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              dst[j] = make_uint4(pack_bf16(v[8 * j] * inv, v[8 * j + 1] * inv),
-                                  pack_bf16(v[8 * j + 2] * inv, v[8 * j + 3] * inv),
-                                  pack_bf16(v[8 * j + 4] * inv, v[8 * j + 5] * inv),
-                                  pack_bf16(v[8 * j + 6] * inv, v[8 * j + 7] * inv));
-          }
-        }
-      }
-      // refresh the bf16 copies of R' and S for the next tile
-      for (int b = 0; b < nh; ++b) {
-        if (nh == 2 && ch != b) continue;
+      // bf16 copies of R(t) for the next tile
+      for (int b = 0; b < nb; ++b) {
+        int c_lo, c_hi;
+        r_cols(b, c_lo, c_hi);
         const int f = 128 * b + row;
-        if (f >= M) continue;
-        const int c_lo = (nh == 2) ? 0 : (ch == 0 ? 0 : (ncols / 32) * 16);
-        const int c_hi = (nh == 2) ? ncols : (ch == 0 ? (ncols / 32) * 16 : ncols);
         for (int c = c_lo; c < c_hi; c += 16) {
           float v[16];
-          tmem_ld16(tmem_addr(tbase, 32 * q4, lay.t_r + b * ncols + c), v);
-#pragma unroll
-          for (int i = 0; i < 16; i += 8) {
-            if (c + i + 8 <= D) st_bf16x8(s_rb + sw128_offset(f, c + i, M), v + i);
-          }
-          if (c <= D && D < c + 16) put_s(f, v[D - c]);
+          tmem_ld16(tmem_addr(tbase, lane_base, lay.t_r + b * NC + c), v);
+          put_rb(f, c, v);
         }
       }
       fence_async_smem();
-      cta_sync();
-    } else {
-      if (tid == 0 && t + 1 < t1) issue_v(t + 1);
+      tc_fence_before();
+      arrive(B_RBFULL);
+      // Y = num / den
+      {
+        if (!wait(B_NUMFULL, i & 1)) break;
+        tc_fence_after();
+        constexpr int YC = D / 2;  // value columns per thread
+        float dv[16], v[YC];
+        tmem_ld16(tmem_addr(tbase, lane_base, lay.t_num + D), dv);
+        const uint32_t a = tmem_addr(tbase, lane_base, lay.t_num + YC * half);
+        if constexpr (YC == 64)
+          tmem_ld32x2(a, a + 32, v, v + 32);
+        else
+          tmem_ld32(a, v);
+        tc_fence_before();
+        arrive(B_NUMEMPTY);
+        if (!dead) {
+          const float inv = 1.0f / (dv[0] + dv[1]);
+          uint4 *dst = reinterpret_cast<uint4 *>(p.y + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + YC * half);
+#pragma unroll
+          for (int j = 0; j < YC / 8; ++j)
+            dst[j] = make_uint4(pack_bf16(v[8 * j] * inv, v[8 * j + 1] * inv),
+                                pack_bf16(v[8 * j + 2] * inv, v[8 * j + 3] * inv),
+                                pack_bf16(v[8 * j + 4] * inv, v[8 * j + 5] * inv),
+                                pack_bf16(v[8 * j + 6] * inv, v[8 * j + 7] * inv));
+        }
+        arrive(B_EMPTY + nV % C::kSlots);
+      }
+    }
+
+    if (MODE == MODE_STATE && ok) {
+      // segment total of R' -> fp32 [M][D + 1] (high part; the low part is zero)
+      const size_t off = ((size_t)bh * p.P + seg) * (size_t)M * DP;
+      for (int b = 0; b < nb; ++b) {
+        int c_lo, c_hi;
+        r_cols(b, c_lo, c_hi);
+        const int f = 128 * b + row;
+        for (int c = c_lo; c < c_hi; c += 16) {
+          float v[16];
+          tmem_ld16(tmem_addr(tbase, lane_base, lay.t_m + b * NC + c), v);
+          if (f < M) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (c + i <= D) {
+                p.states[off + (size_t)f * DP + c + i] = v[i];
+                p.states_lo[off + (size_t)f * DP + c + i] = 0.f;
+              }
+          }
+        }
+      }
     }
   }
 
-  if (MODE == MODE_STATE) {
-    // segment total of R' -> fp32 [M][D + 1], high and low parts
-    const size_t off = ((size_t)bh * p.P + seg) * (size_t)M * DP;
-    for (int b = 0; b < nh; ++b) {
-      const int f = 128 * b + row;
-      for (int c = ch ? csplit : 0; c < (ch ? ncols : csplit); c += 16) {
-        float h[16], l[16];
-        if (exact) {
-          tmem_ld16(tmem_addr(tbase, 32 * q4, lay.s_hi + b * ncols + c), h);
-          tmem_ld16(tmem_addr(tbase, 32 * q4, lay.s_lo + b * ncols + c), l);
-        } else {
-          tmem_ld16(tmem_addr(tbase, 32 * q4, lay.t_r + b * ncols + c), h);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) l[i] = 0.f;
-        }
-        if (f < M) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (c + i <= D) {
-              p.states[off + (size_t)f * DP + c + i] = h[i];
-              p.states_lo[off + (size_t)f * DP + c + i] = l[i];
-            }
-        }
-      }
-    }
-  }
-  cta_sync();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
-template <int D, bool FAVOR, int MODE>
-cudaError_t launch(const Plan &pl, const Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
-                   const CUtensorMap &mv, int nseg, bool exact, cudaStream_t st) {
+template <int D, bool FAVOR, int MODE, int M>
+cudaError_t launch_m(const Plan &pl, const Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
+                     const CUtensorMap &mv, int nseg, cudaStream_t st) {
   Params p{};
-  p.L = pl.L; p.M = pl.M; p.nt = pl.tc_tiles; p.P = pl.P; p.tps = pl.cps; p.favor = FAVOR;
-  p.exact = exact ? 1 : 0;
+  p.L = pl.L; p.M = pl.M; p.nt = pl.tc_tiles; p.P = pl.P; p.tps = pl.cps;
   p.y = static_cast<__nv_bfloat16 *>(a.y);
-  p.w = a.w;
+  p.wimg = reinterpret_cast<const __nv_bfloat16 *>(a.ws + pl.wimg_off);
   p.states = a.ws + pl.states_off;
   p.states_lo = a.ws + pl.states_lo_off;
   p.status = a.status;
-  const Layout<D> lay(pl.M, FAVOR);
+  const Layout<D, FAVOR, MODE> lay(M);
   const int smem = (int)lay.total + 1024;
-  auto kern = tc_fwd_kernel<D, FAVOR, MODE>;
+  auto kern = tc_fwd_kernel<D, FAVOR, MODE, M>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<dim3(nseg, pl.BH), kThreads, smem, st>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+// M is a compile-time constant of the kernel: FAVOR+ with 64, 128 or 256
+// features, elu+1 with M = d.
+template <int D, bool FAVOR, int MODE>
+cudaError_t launch(const Plan &pl, const Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
+                   const CUtensorMap &mv, int nseg, cudaStream_t st) {
+  if constexpr (!FAVOR) {
+    return pl.M == D ? launch_m<D, FAVOR, MODE, D>(pl, a, mq, mk, mv, nseg, st) : cudaErrorInvalidValue;
+  } else {
+    if (pl.M == 64) return launch_m<D, FAVOR, MODE, 64>(pl, a, mq, mk, mv, nseg, st);
+    if (pl.M == 128) return launch_m<D, FAVOR, MODE, 128>(pl, a, mq, mk, mv, nseg, st);
+    if (pl.M == 256) return launch_m<D, FAVOR, MODE, 256>(pl, a, mq, mk, mv, nseg, st);
+    return cudaErrorInvalidValue;
+  }
+}
+
+// W (fp32 [64][M]) -> the bf16 [M][64] swizzled image of W^T that the
+// kernels copy into shared memory as the K-major B operand of F = X W.
+__global__ void prep_w_kernel(const float *__restrict__ w, __nv_bfloat16 *__restrict__ img, int M) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= M * 64) return;
+  const int i = idx / M, m = idx - i * M;
+  img[sw128_offset(m, i, M) / 2] = __float2bfloat16_rn(w[idx]);
+}
+
+cudaError_t prep_w(const Plan &pl, const Args &a, cudaStream_t st) {
+  if (!pl.favor) return cudaSuccess;
+  const int n = pl.M * 64;
+  prep_w_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.w, reinterpret_cast<__nv_bfloat16 *>(a.ws + pl.wimg_off), pl.M);
   return cudaGetLastError();
 }
 
@@ -501,12 +669,11 @@ cudaError_t launch(const Plan &pl, const Args &a, const CUtensorMap &mq, const C
 // states[s] = R' at the end of segment s.
 template <int D, bool FAVOR>
 cudaError_t segment_states(const Plan &pl, const Args &a, const CUtensorMap &mq,
-                           const CUtensorMap &mk, const CUtensorMap &mv, int nseg, bool exact,
-                           cudaStream_t st) {
+                           const CUtensorMap &mk, const CUtensorMap &mv, int nseg, cudaStream_t st) {
   cudaError_t e;
   {
     ProfScope ps("tc_segment_state", st);
-    e = launch<D, FAVOR, MODE_STATE>(pl, a, mq, mk, mv, nseg, exact, st);
+    e = launch<D, FAVOR, MODE_STATE>(pl, a, mq, mk, mv, nseg, st);
     if (e != cudaSuccess) return e;
   }
   if (nseg > 1) {
@@ -524,18 +691,19 @@ cudaError_t forward_family(const Plan &pl, const Args &a, cudaStream_t st) {
     return cudaErrorInvalidValue;
   cudaError_t e;
   if (pl.P > 1) {
-    e = segment_states<D, FAVOR>(pl, a, mq, mk, mv, pl.P - 1, false, st);
+    e = segment_states<D, FAVOR>(pl, a, mq, mk, mv, pl.P - 1, st);
     if (e != cudaSuccess) return e;
   }
   ProfScope ps("tc_forward", st);
-  return launch<D, FAVOR, MODE_FWD>(pl, a, mq, mk, mv, pl.P, false, st);
+  return launch<D, FAVOR, MODE_FWD>(pl, a, mq, mk, mv, pl.P, st);
 }
 
 }  // namespace tcf
 
 size_t tc_smem_bytes(int d, int M, bool favor) {
-  if (d == 64) return tcf::Layout<64>(M, favor).total + 1024;
-  return tcf::Layout<128>(M, favor).total + 1024;
+  if (d == 64 && favor) return tcf::Layout<64, true, tcf::MODE_FWD>(M).total + 1024;
+  if (d == 64) return tcf::Layout<64, false, tcf::MODE_FWD>(M).total + 1024;
+  return tcf::Layout<128, false, tcf::MODE_FWD>(M).total + 1024;
 }
 
 bool tc_forward_supported(int d, int M, int chunk, bool favor) {
@@ -548,15 +716,19 @@ bool tc_forward_supported(int d, int M, int chunk, bool favor) {
 cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, cudaStream_t st) {
   CUtensorMap mk, mv;
   const int d = p.d;
+  cudaError_t e = tcf::prep_w(p, a, st);
+  if (e != cudaSuccess) return e;
   if (!make_map_bf16_3d(&mk, a.k, p.BH, p.L, d, tcf::kTile) || !make_map_bf16_3d(&mv, a.v, p.BH, p.L, d, tcf::kTile))
     return cudaErrorInvalidValue;
-  if (d == 64 && p.favor) return tcf::segment_states<64, true>(p, a, mk, mk, mv, nseg, true, st);
-  if (d == 64) return tcf::segment_states<64, false>(p, a, mk, mk, mv, nseg, true, st);
-  if (d == 128 && !p.favor) return tcf::segment_states<128, false>(p, a, mk, mk, mv, nseg, true, st);
+  if (d == 64 && p.favor) return tcf::segment_states<64, true>(p, a, mk, mk, mv, nseg, st);
+  if (d == 64) return tcf::segment_states<64, false>(p, a, mk, mk, mv, nseg, st);
+  if (d == 128 && !p.favor) return tcf::segment_states<128, false>(p, a, mk, mk, mv, nseg, st);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t tc_forward(const Plan &p, const Args &a, cudaStream_t st) {
+  cudaError_t e = tcf::prep_w(p, a, st);
+  if (e != cudaSuccess) return e;
   if (p.d == 64 && p.favor) return tcf::forward_family<64, true>(p, a, st);
   if (p.d == 64) return tcf::forward_family<64, false>(p, a, st);
   if (p.d == 128 && !p.favor) return tcf::forward_family<128, false>(p, a, st);
