@@ -37,6 +37,7 @@ struct Params {
   int L, M, nt, P, tps, favor, BH;
   __nv_bfloat16 *dq, *dk, *dv;
   const float *w;
+  const __nv_bfloat16 *wimg;  // W^T as the bf16 [M][64] swizzled shared-memory image
   const float *states;     // fp32 [BH][P][M][D + 1]: inclusive segment-end R', high parts
   const float *states_lo;  // low parts
   float *gstates;          // fp32 [BH][P][M][D + 1]: segment totals of G (out) / G_end (in)
@@ -141,6 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *rl_bar = in_bar + 2;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(in_bar + 3);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(in_bar + 4);
+  uint64_t *setup_bar = in_bar + 5;
   float *rx_den = reinterpret_cast<float *>(smem + lay.rx_den);
   float *rx_usq = reinterpret_cast<float *>(smem + lay.rx_usq);
   float *rx_usk = reinterpret_cast<float *>(smem + lay.rx_usk);
@@ -161,35 +163,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int half = MC / 2;  // feature columns per thread (two threads per row)
   const bool own = CS == 1 || (row >> 6) == rank;  // rows this CTA finalises
 
+  // this CTA's rows of the W^T image (its features are contiguous rows of
+  // it, with the same swizzle phase) and its features' segment-end state
+  // (high and low parts, staged in the phi / A tiles) by bulk copy
+  const uint32_t st_bytes = (uint32_t)(MC * DP * 4);
+  const uint32_t lo_stage = lay.phq + ((st_bytes + 1023u) & ~1023u);
   if (tid == 0) {
     mbar_init(in_bar, 1);
     mbar_init(mma_bar, 1);
     mbar_init(rl_bar, 1);
+    mbar_init(setup_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
+    const size_t soff = ((size_t)bh * p.P + seg) * (size_t)M * DP + (size_t)fbase * DP;
+    mbar_arrive_expect_tx(setup_bar, (FAVOR ? (uint32_t)MC * 128u : 0u) + 2 * st_bytes);
+    if (FAVOR)
+      bulk_load(smem + lay.w, reinterpret_cast<const unsigned char *>(p.wimg) + (size_t)fbase * 128, MC * 128u,
+                setup_bar);
+    bulk_load(smem + lay.phq, p.states + soff, st_bytes, setup_bar);
+    bulk_load(smem + lo_stage, p.states_lo + soff, st_bytes, setup_bar);
   }
   if (warp == 0) tmem_alloc(tslot, 512);
 
-  if (FAVOR) {
-    for (int idx = tid; idx < MC * D; idx += kThreads) {
-      const int i = idx / MC, m = idx - i * MC;
-      st_bf16_scalar(smem, lay.w + sw128_offset(m, i, MC), p.w[(size_t)i * M + fbase + m]);
-    }
-  }
   for (int idx = tid; idx < kTile * 16; idx += kThreads) {
     const int r = idx >> 4, x = idx & 15;
     st_bf16_scalar(smem, lay.ones + n16_offset(r, x), x == 0 ? 1.f : 0.f);
     st_bf16_scalar(smem, lay.ddb + n16_offset(r, x), 0.f);
     if (r < MC) st_bf16_scalar(smem, lay.sb + n16_offset(r, x), 0.f);
-  }
-  if (MC < 128) {  // features beyond MC stay zero in phi_q / phi_k
-    for (int idx = tid; idx < kTile * 128; idx += kThreads) {
-      const int r = idx >> 7, x = idx & 127;
-      if (x >= MC) {
-        st_bf16_scalar(smem, lay.phq + sw128_offset(r, x, kTile), 0.f);
-        st_bf16_scalar(smem, lay.phk + sw128_offset(r, x, kTile), 0.f);
-      }
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -199,7 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // R' <- inclusive state at the segment end (hi, lo); G <- 0
   {
-    const size_t off = ((size_t)bh * p.P + seg) * (size_t)M * DP;
+    mbar_wait(setup_bar, 0, p.status, abort_flag);
+    const float *sh = reinterpret_cast<const float *>(smem + lay.phq);
+    const float *sl = reinterpret_cast<const float *>(smem + lo_stage);
     const int f = row;
     for (int c = ch * 48; c < (ch ? 80 : 48); c += 16) {
       float h[16], l[16], z[16];
@@ -207,8 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 16; ++i) {
         const int e = c + i;
         const bool in = f < MC && e <= D;
-        h[i] = in ? p.states[off + (size_t)(fbase + f) * DP + e] : 0.f;
-        l[i] = in ? p.states_lo[off + (size_t)(fbase + f) * DP + e] : 0.f;
+        h[i] = in ? sh[f * DP + e] : 0.f;
+        l[i] = in ? sl[f * DP + e] : 0.f;
         z[i] = 0.f;
       }
       tmem_st16(tmem_addr(tb, 32 * q4, kRhi + c), h);
@@ -216,6 +218,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st16(tmem_addr(tb, 32 * q4, kG + c), z);
     }
     tmem_st_wait();
+  }
+  __syncthreads();  // the staging area is read before the zero padding goes in
+  if (MC < 128) {  // features beyond MC stay zero in phi_q / phi_k
+    for (int idx = tid; idx < kTile * 128; idx += kThreads) {
+      const int r = idx >> 7, x = idx & 127;
+      if (x >= MC) {
+        st_bf16_scalar(smem, lay.phq + sw128_offset(r, x, kTile), 0.f);
+        st_bf16_scalar(smem, lay.phk + sw128_offset(r, x, kTile), 0.f);
+      }
+    }
   }
   fence_async_smem();
   tc_fence_before();
@@ -701,6 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *mma_bar = in_bar + 1;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(in_bar + 3);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(in_bar + 4);
+  uint64_t *setup_bar = in_bar + 5;
   float *gs_f = reinterpret_cast<float *>(smem + lay.gs);
   float *usk = reinterpret_cast<float *>(smem + lay.usk);
 
@@ -716,16 +729,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(in_bar, 1);
     mbar_init(in_bar + 2, 1);
     mbar_init(mma_bar, 1);
+    mbar_init(setup_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
-  }
-  if (warp == 0) tmem_alloc(tslot, 512);
-  if (FAVOR) {
-    for (int idx = tid; idx < M * D; idx += kThreads) {
-      const int i = idx / M, m = idx - i * M;
-      st_bf16_scalar(smem, lay.w + sw128_offset(m, i, M), p.w[idx]);
+    if (FAVOR) {
+      mbar_arrive_expect_tx(setup_bar, (uint32_t)M * 128u);
+      bulk_load(smem + lay.w, p.wimg, (uint32_t)M * 128u, setup_bar);
     }
   }
+  if (warp == 0) tmem_alloc(tslot, 512);
   if (MB < 128) {
     for (int idx = tid; idx < kTile * 128; idx += kThreads) {
       const int r = idx >> 7, x = idx & 127;
@@ -737,6 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = *tslot;
+  if (FAVOR) mbar_wait(setup_bar, 0, p.status, abort_flag);
   const uint32_t s_w = sb + lay.w, s_phk = sb + lay.phk;
   const uint32_t s_gb = sb + lay.gb;
   const uint32_t tile_bytes = kTile * D * 2;
@@ -776,10 +789,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (key != cur_key) {
       // G_end(s) = gstates[s + 1] after the reverse scan -> bf16 [M][64] + G_S
       __syncthreads();
-      const float *g = p.gstates + ((size_t)bh * p.P + seg + 1) * (size_t)M * DP;
-      for (int idx = tid; idx < M * D; idx += kThreads) {
-        const int f = idx / D, e = idx - f * D;
-        st_bf16_scalar(smem, lay.gb + sw128_offset(f, e, M), g[(size_t)f * DP + e]);
+      const float *__restrict__ g = p.gstates + ((size_t)bh * p.P + seg + 1) * (size_t)M * DP;
+      // loads in batches of 16 so their latencies overlap
+      for (int base = tid; base < M * D; base += 16 * kThreads) {
+        float x[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int idx = base + j * kThreads;
+          x[j] = idx < M * D ? __ldg(g + (size_t)(idx / D) * DP + idx % D) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int idx = base + j * kThreads;
+          if (idx < M * D) st_bf16_scalar(smem, lay.gb + sw128_offset(idx / D, idx % D, M), x[j]);
+        }
       }
       for (int f = tid; f < M; f += kThreads) gs_f[f] = g[(size_t)f * DP + D];
       fence_async_smem();
@@ -911,6 +934,7 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
   p.dk = static_cast<__nv_bfloat16 *>(a.dk);
   p.dv = static_cast<__nv_bfloat16 *>(a.dv);
   p.w = a.w;
+  p.wimg = reinterpret_cast<const __nv_bfloat16 *>(a.ws + pl.wimg_off);
   p.states = a.ws + pl.states_off;
   p.states_lo = a.ws + pl.states_lo_off;
   p.gstates = a.ws + pl.gstates_off;
