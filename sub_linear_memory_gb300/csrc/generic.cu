@@ -478,6 +478,9 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(Plan p, Args a) {
 
 // Inclusive scan over segments of double-float states: acc = sum in fp64,
 // written back as (hi, lo) = (fl(acc), fl(acc - hi)).
+// Inclusive scan of double-float (hi, lo) segment states over segments, in
+// fp32 double-float arithmetic (two-sum): GB300's fp64 rate would make fp64
+// the bottleneck of this memory-bound pass.  Relative error ~2^-47.
 __global__ void scan_states_df_kernel(Plan p, float *hi, float *lo, int nseg) {
   const size_t per = (size_t)p.dp * p.M;
   const size_t n = (size_t)p.BH * per;
@@ -485,25 +488,60 @@ __global__ void scan_states_df_kernel(Plan p, float *hi, float *lo, int nseg) {
        i += (size_t)gridDim.x * blockDim.x) {
     const size_t bh = i / per, e = i - bh * per;
     float *h = hi + bh * p.P * per + e, *l = lo + bh * p.P * per + e;
-    double acc = 0.0;
-    // loads of a group are independent of the running sum, so they overlap
-    for (int s0 = 0; s0 < nseg; s0 += 8) {
-      float xh[8], xl[8];
-      const int n = min(8, nseg - s0);
+    float sh = 0.f, sl = 0.f;
+    // loads of a group do not depend on the running sum, so they overlap
+    for (int s0 = 0; s0 < nseg; s0 += 16) {
+      float xh[16], xl[16];
+      const int cnt = min(16, nseg - s0);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < n) {
+      for (int j = 0; j < 16; ++j)
+        if (j < cnt) {
           xh[j] = h[(size_t)(s0 + j) * per];
           xl[j] = l[(size_t)(s0 + j) * per];
         }
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < n) {
-          acc += (double)xh[j] + (double)xl[j];
-          const float fh = (float)acc;
-          h[(size_t)(s0 + j) * per] = fh;
-          l[(size_t)(s0 + j) * per] = (float)(acc - (double)fh);
+      for (int j = 0; j < 16; ++j)
+        if (j < cnt) {
+          // (sh, sl) += (xh, xl): two-sum of the high parts, then renormalise
+          const float t = sh + xh[j];
+          const float bp = t - sh;
+          float err = (sh - (t - bp)) + (xh[j] - bp);
+          err += sl + xl[j];
+          sh = t + err;
+          sl = err - (sh - t);
+          h[(size_t)(s0 + j) * per] = sh;
+          l[(size_t)(s0 + j) * per] = sl;
         }
+    }
+  }
+}
+
+// Inclusive fp32 scan over segments (reverse: from the last segment down),
+// loads batched as above.
+__global__ void scan_states_f32_kernel(Plan p, float *st, int nseg, int reverse) {
+  const size_t per = (size_t)p.dp * p.M;
+  const size_t n = (size_t)p.BH * per;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t bh = i / per, e = i - bh * per;
+    float *b = st + bh * p.P * per + e;
+    float acc = 0.f;
+    for (int s0 = 0; s0 < nseg; s0 += 16) {
+      float x[16];
+      const int cnt = min(16, nseg - s0);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int s = reverse ? nseg - 1 - (s0 + j) : s0 + j;
+        if (j < cnt) x[j] = b[(size_t)s * per];
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int s = reverse ? nseg - 1 - (s0 + j) : s0 + j;
+        if (j < cnt) {
+          acc += x[j];
+          b[(size_t)s * per] = acc;
+        }
+      }
     }
   }
 }
@@ -585,7 +623,7 @@ cudaError_t generic_backward(const Plan &p, const Args &a, cudaStream_t st) {
 }
 
 cudaError_t scan_states_f32(const Plan &p, float *states, int nseg, cudaStream_t st) {
-  gen::scan_states_kernel<float><<<scan_blocks(p), 256, 0, st>>>(p, states, nseg, 0);
+  gen::scan_states_f32_kernel<<<scan_blocks(p), 256, 0, st>>>(p, states, nseg, 0);
   return cudaGetLastError();
 }
 
@@ -595,7 +633,7 @@ cudaError_t scan_states_df(const Plan &p, float *hi, float *lo, int nseg, cudaSt
 }
 
 cudaError_t scan_states_f32_rev(const Plan &p, float *states, int nseg, cudaStream_t st) {
-  gen::scan_states_kernel<float><<<scan_blocks(p), 256, 0, st>>>(p, states, nseg, 1);
+  gen::scan_states_f32_kernel<<<scan_blocks(p), 256, 0, st>>>(p, states, nseg, 1);
   return cudaGetLastError();
 }
 

@@ -72,7 +72,7 @@ struct Layout {
     rx_den = o; o += 128 * 4;  // cluster exchange: the peer's den partials
     rx_usq = o; o += 64 * 4;
     rx_usk = o; o += 64 * 4;
-    bars = o; o += 64;
+    bars = o; o += 128;
     total = o;
   }
 };
@@ -143,6 +143,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t *tslot = reinterpret_cast<uint32_t *>(in_bar + 3);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(in_bar + 4);
   uint64_t *setup_bar = in_bar + 5;
+  // cluster exchanges: data received (st.async bytes) and receive buffers
+  // released by the peer (remote arrive), one phase each per tile
+  uint64_t *x1_full = in_bar + 6, *x2_full = in_bar + 7, *x1_free = in_bar + 8, *x2_free = in_bar + 9;
   float *rx_den = reinterpret_cast<float *>(smem + lay.rx_den);
   float *rx_usq = reinterpret_cast<float *>(smem + lay.rx_usq);
   float *rx_usk = reinterpret_cast<float *>(smem + lay.rx_usk);
@@ -173,6 +176,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(mma_bar, 1);
     mbar_init(rl_bar, 1);
     mbar_init(setup_bar, 1);
+    mbar_init(x1_full, 1);
+    mbar_init(x2_full, 1);
+    mbar_init(x1_free, 1);
+    mbar_init(x2_free, 1);
     *abort_flag = 0;
     fence_barrier_init();
     const size_t soff = ((size_t)bh * p.P + seg) * (size_t)M * DP + (size_t)fbase * DP;
@@ -239,7 +246,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_at = sb + lay.at, s_dn = sb + lay.dn, s_rb = sb + lay.rb;
   const uint32_t s_ones = sb + lay.ones, s_ddb = sb + lay.ddb, s_sb = sb + lay.sb;
   const uint32_t tile_bytes = kTile * D * 2;
-  uint32_t in_phase = 0, mma_phase = 0, rl_phase = 0;
+  uint32_t in_phase = 0, mma_phase = 0, rl_phase = 0, x_phase = 0;
+  // exchange 1: num partials of all 128 rows (fp32 [128][64]) + den;
+  // exchange 2: dV, dQ, dK partials of the peer's 64 rows (fp32 [64][64]
+  // each) + two row sums
+  constexpr uint32_t kX1Bytes = 128 * 64 * 4 + 128 * 4, kX2Bytes = 3 * 64 * 64 * 4 + 2 * 64 * 4;
+  const uint32_t peer_x1_full = CS == 2 ? map_peer(smem_u32(x1_full), peer) : 0u;
+  const uint32_t peer_x2_full = CS == 2 ? map_peer(smem_u32(x2_full), peer) : 0u;
+  const uint32_t peer_x1_free = CS == 2 ? map_peer(smem_u32(x1_free), peer) : 0u;
+  const uint32_t peer_x2_free = CS == 2 ? map_peer(smem_u32(x2_free), peer) : 0u;
 
   auto issue_in = [&](int t) {
     mbar_arrive_expect_tx(in_bar, 4 * tile_bytes);
@@ -270,6 +285,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool live = row < valid;
     mbar_wait(in_bar, in_phase, p.status, abort_flag);
     in_phase ^= 1;
+    if (CS == 2 && tid == 0) {
+      mbar_arrive_expect_tx(x1_full, kX1Bytes);
+      mbar_arrive_expect_tx(x2_full, kX2Bytes);
+    }
+    if (tid == 0 && t > t0) {
+      // the next tile's inputs head for L2 now; its TMA loads issue at the
+      // end of this tile, when their buffers are free again
+      tma_prefetch_3d(&tmQ, 0, (t - 1) * kTile, bh);
+      tma_prefetch_3d(&tmK, 0, (t - 1) * kTile, bh);
+      tma_prefetch_3d(&tmV, 0, (t - 1) * kTile, bh);
+      tma_prefetch_3d(&tmDY, 0, (t - 1) * kTile, bh);
+    }
     float ck = 0.f, cq = 0.f;
     if (FAVOR) {
       ck = favor_row_const(tile_row_sqnorm(s_k, row, D), M);
@@ -317,6 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_async_smem();
     cta_sync();
+    // my Q and K tiles are idle until the next tile's loads: the peer may
+    // send its num partials there (signalled off the MMA-issuing thread: the
+    // cluster-scope release waits for this thread's earlier stores)
+    if (CS == 2 && tid == 32) mbar_arrive_remote(peer_x1_free);
 
     // (c) eq. (19): R' -= phi_k^T [V, 1], removing exactly the increment the
     // segment pre-pass added for this tile (increment -> T), and
@@ -378,16 +409,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       float v[32], g[32];
       tmem_ld32(tmem_addr(tb, 32 * q4, kT + 32 * ch), v);
       if (CS == 2) {
-        // both CTAs are past their features: the peer's Q and K tiles are idle
-        // and take my partial num (all 128 rows) and den; each CTA then forms
-        // dN' for every row itself
-        cluster_sync();
+        // once the peer is past its features its Q and K tiles take my
+        // partial num (all 128 rows) and den; each CTA then forms dN' for
+        // every row itself
+        mbar_wait(x1_free, x_phase, p.status, abort_flag);
         const uint32_t dst = map_peer(s_q, peer);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          st_peer_v4(dst + xoff(row, 8 * ch + j, 128), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        if (ch == 0) st_peer_f32(map_peer(sb + lay.rx_den + row * 4, peer), den);
-        cluster_sync();
+          st_async_v4(dst + xoff(row, 8 * ch + j, 128), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3],
+                      peer_x1_full);
+        if (ch == 0) st_async_f32(map_peer(sb + lay.rx_den + row * 4, peer), den, peer_x1_full);
+        mbar_wait(x1_full, x_phase, p.status, abort_flag);
         float r[32];
 #pragma unroll
         for (int j = 0; j < 8; ++j) ld_shared_v4f(s_q + xoff(row, 8 * ch + j, 128), r + 4 * j);
@@ -486,9 +518,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     wait_mma();
     if (CS == 2) {
-      // V, dN, R and G copies and the dA tile are idle in both CTAs from here:
-      // bring Q and K back (into the dA tile) for the dQ, dK epilogue
-      cluster_sync();
+      // my V, dN, R and G copies and the dA tile are idle from here: the
+      // peer may send its exchange-2 partials; Q and K come back (into the
+      // dA tile) for the dQ, dK epilogue
+      if (tid == 32) mbar_arrive_remote(peer_x2_free);
       if (tid == 0) {
         mbar_arrive_expect_tx(rl_bar, 2 * tile_bytes);
         tma_load_3d(smem + lay.at, &tmQ, rl_bar, 0, t * kTile, bh);
@@ -570,21 +603,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 8; ++j) ld_shared_v4f(s_q + xoff(row, 8 * ch + j, 128), c3 + 4 * j);
         if (!own) {
+          mbar_wait(x2_free, x_phase, p.status, abort_flag);
           const uint32_t dv_dst = map_peer(s_v, peer), dq_dst = map_peer(s_dn, peer);
           const uint32_t dk_dst = map_peer(s_rb, peer);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint32_t o = xoff(row - 64 * peer, 8 * ch + j, 64);
-            st_peer_v4(dv_dst + o, c3[4 * j], c3[4 * j + 1], c3[4 * j + 2], c3[4 * j + 3]);
-            st_peer_v4(dq_dst + o, a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]);
-            st_peer_v4(dk_dst + o, b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]);
+            st_async_v4(dv_dst + o, c3[4 * j], c3[4 * j + 1], c3[4 * j + 2], c3[4 * j + 3], peer_x2_full);
+            st_async_v4(dq_dst + o, a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3], peer_x2_full);
+            st_async_v4(dk_dst + o, b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3], peer_x2_full);
           }
           if (ch == 0) {
-            st_peer_f32(map_peer(sb + lay.rx_usq + (row - 64 * peer) * 4, peer), sq);
-            st_peer_f32(map_peer(sb + lay.rx_usk + (row - 64 * peer) * 4, peer), sk);
+            st_async_f32(map_peer(sb + lay.rx_usq + (row - 64 * peer) * 4, peer), sq, peer_x2_full);
+            st_async_f32(map_peer(sb + lay.rx_usk + (row - 64 * peer) * 4, peer), sk, peer_x2_full);
           }
+        } else {
+          mbar_wait(x2_full, x_phase, p.status, abort_flag);
         }
-        cluster_sync();
         if (own) {
           float r[32];
 #pragma unroll
@@ -636,6 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       cta_sync();
     }
+    x_phase ^= 1;
     if (tid == 0 && t > t0) issue_in(t - 1);
   }
 

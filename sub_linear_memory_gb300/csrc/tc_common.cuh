@@ -176,6 +176,14 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
       : "memory");
 }
 
+// Pull a tile of a 3-D tensor map into L2 ahead of a later TMA load.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int c0,
                                              int c1, int c2) {
   asm volatile(
@@ -486,6 +494,27 @@ __device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
 
 __device__ __forceinline__ void st_peer_b16(uint32_t addr, uint16_t v) {
   asm volatile("st.shared::cluster.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+// Store to a peer CTA's shared memory (cluster address) that completes
+// its bytes as transactions on the peer's mbarrier `rbar` (cluster address).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d,
+                                            uint32_t rbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
+      : "memory");
+}
+
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(addr), "f"(v),
+               "r"(rbar)
+               : "memory");
+}
+
+// Arrive (release, cluster scope) on an mbarrier of a peer CTA.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t rbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
 }
 
 // All threads of every CTA in the cluster; orders shared (incl. remote) and
