@@ -478,10 +478,11 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(Plan p, Args a) {
 
 // Inclusive scan over segments of double-float states: acc = sum in fp64,
 // written back as (hi, lo) = (fl(acc), fl(acc - hi)).
-// Inclusive scan of double-float (hi, lo) segment states over segments, in
+// Inclusive scan of double-float (hi, lo) segment states over segments (the
+// input low parts are read only when lo_in is set, else taken as zero), in
 // fp32 double-float arithmetic (two-sum): GB300's fp64 rate would make fp64
 // the bottleneck of this memory-bound pass.  Relative error ~2^-47.
-__global__ void scan_states_df_kernel(Plan p, float *hi, float *lo, int nseg) {
+__global__ void scan_states_df_kernel(Plan p, float *hi, float *lo, int nseg, int lo_in) {
   const size_t per = (size_t)p.dp * p.M;
   const size_t n = (size_t)p.BH * per;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -497,7 +498,7 @@ __global__ void scan_states_df_kernel(Plan p, float *hi, float *lo, int nseg) {
       for (int j = 0; j < 16; ++j)
         if (j < cnt) {
           xh[j] = h[(size_t)(s0 + j) * per];
-          xl[j] = l[(size_t)(s0 + j) * per];
+          xl[j] = lo_in ? l[(size_t)(s0 + j) * per] : 0.f;
         }
 #pragma unroll
       for (int j = 0; j < 16; ++j)
@@ -627,8 +628,8 @@ cudaError_t scan_states_f32(const Plan &p, float *states, int nseg, cudaStream_t
   return cudaGetLastError();
 }
 
-cudaError_t scan_states_df(const Plan &p, float *hi, float *lo, int nseg, cudaStream_t st) {
-  gen::scan_states_df_kernel<<<scan_blocks(p), 256, 0, st>>>(p, hi, lo, nseg);
+cudaError_t scan_states_df(const Plan &p, float *hi, float *lo, int nseg, int lo_in, cudaStream_t st) {
+  gen::scan_states_df_kernel<<<scan_blocks(p), 256, 0, st>>>(p, hi, lo, nseg, lo_in);
   return cudaGetLastError();
 }
 

@@ -35,7 +35,7 @@ template <typename T> cudaError_t generic_backward(const Plan &p, const Args &a,
 cudaError_t scan_states_f32(const Plan &p, float *states, int nseg, cudaStream_t st);
 cudaError_t scan_states_f32_rev(const Plan &p, float *states, int nseg, cudaStream_t st);
 // The same forward scan for double-float (hi, lo) states, summed in fp64.
-cudaError_t scan_states_df(const Plan &p, float *hi, float *lo, int nseg, cudaStream_t st);
+cudaError_t scan_states_df(const Plan &p, float *hi, float *lo, int nseg, int lo_in, cudaStream_t st);
 
 // Tensor-core family (tc_forward.cu): bf16 I/O, 128-row tiles.
 bool tc_forward_supported(int d, int M, int chunk, bool favor);

@@ -675,9 +675,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0 && t > t0) issue_in(t - 1);
   }
 
-  // segment total of G -> gstates
+  // segment total of G -> gstates, staged in the idle phi / A tiles for one
+  // coalesced bulk store of this CTA's rows
   {
-    float *out = p.gstates + ((size_t)bh * p.P + seg) * (size_t)M * DP;
+    float *stage = reinterpret_cast<float *>(smem + lay.phq);
     const int f = row;
     for (int c = ch * 48; c < (ch ? 80 : 48); c += 16) {
       float v[16];
@@ -685,11 +686,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (f < MC) {
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          if (c + i <= D) out[(size_t)(fbase + f) * DP + c + i] = v[i];
+          if (c + i <= D) stage[f * DP + c + i] = v[i];
       }
     }
   }
+  fence_async_smem();
   cta_sync();
+  if (tid == 0) {
+    bulk_store(p.gstates + ((size_t)bh * p.P + seg) * (size_t)M * DP + (size_t)fbase * DP, sb + lay.phq,
+               (uint32_t)(MC * DP * 4));
+    tma_store_commit();
+    tma_store_wait_read();
+  }
   if (CS == 2) cluster_sync();  // no remote store may target an exited CTA
   if (warp == 0) tmem_dealloc(tb, 512);
 }

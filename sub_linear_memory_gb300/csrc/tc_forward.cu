@@ -587,8 +587,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (MODE == MODE_STATE && ok) {
-      // segment total of R' -> fp32 [M][D + 1] (high part; the low part is zero)
-      const size_t off = ((size_t)bh * p.P + seg) * (size_t)M * DP;
+      // segment total of R' -> fp32 [M][D + 1] staged in the idle load slots
+      // (and phi_k tile) for one coalesced bulk store after the final barrier
+      float *stage = reinterpret_cast<float *>(smem + lay.slots);
       for (int b = 0; b < nb; ++b) {
         int c_lo, c_hi;
         r_cols(b, c_lo, c_hi);
@@ -599,19 +600,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (f < M) {
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              if (c + i <= D) {
-                p.states[off + (size_t)f * DP + c + i] = v[i];
-                p.states_lo[off + (size_t)f * DP + c + i] = 0.f;
-              }
+              if (c + i <= D) stage[f * DP + c + i] = v[i];
           }
         }
       }
+      fence_async_smem();
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (MODE == MODE_STATE && tid == 0 && !*abort_flag) {
+    // high parts only: the scan takes the low parts of these totals as zero
+    bulk_store(p.states + ((size_t)bh * p.P + seg) * (size_t)M * DP, sbase + lay.slots, (uint32_t)(M * DP * 4));
+    tma_store_commit();
+    tma_store_wait_read();
+  }
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
@@ -676,9 +681,10 @@ cudaError_t segment_states(const Plan &pl, const Args &a, const CUtensorMap &mq,
     e = launch<D, FAVOR, MODE_STATE>(pl, a, mq, mk, mv, nseg, st);
     if (e != cudaSuccess) return e;
   }
-  if (nseg > 1) {
+  {
+    // also for one segment: it writes the low parts the state pass leaves out
     ProfScope ps("scan_states", st);
-    e = scan_states_df(pl, a.ws + pl.states_off, a.ws + pl.states_lo_off, nseg, st);
+    e = scan_states_df(pl, a.ws + pl.states_off, a.ws + pl.states_lo_off, nseg, 0, st);
   }
   return e;
 }
