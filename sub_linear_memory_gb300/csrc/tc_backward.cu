@@ -360,7 +360,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_done();
     }
     wait_mma();
-    df_update_tmem(tb, 32 * q4, kT, kRhi, kRlo, ch ? 48 : 0, ch ? 80 : 48, -1.f);
+    // eq. (19) on the double-float master, and from the updated values the
+    // bf16 copies of R and of S (high, low) for the MMAs, fp32 S for the
+    // epilogues
+    for (int c = ch ? 48 : 0; c < (ch ? 80 : 48); c += 16) {
+      float x[16], h[16], l[16];
+      tmem_ld16(tmem_addr(tb, 32 * q4, kT + c), x);
+      tmem_ld16(tmem_addr(tb, 32 * q4, kRhi + c), h);
+      tmem_ld16(tmem_addr(tb, 32 * q4, kRlo + c), l);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) df_add(h[i], l[i], -x[i]);
+      tmem_st16(tmem_addr(tb, 32 * q4, kRhi + c), h);
+      tmem_st16(tmem_addr(tb, 32 * q4, kRlo + c), l);
+      if (row < MC) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = h[i] + l[i];
+#pragma unroll
+        for (int i = 0; i < 16; i += 8)
+          if (c + i + 8 <= D) st_bf16x8(s_rb + sw128_offset(row, c + i, MC), x + i);
+        if (c <= D && D < c + 16) {
+          const float sv = x[D - c];
+          s_f[row] = sv;
+          const __nv_bfloat16 hi = __float2bfloat16_rn(sv);
+          *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(row, 0)) = hi;
+          *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(row, 1)) =
+              __float2bfloat16_rn(sv - __bfloat162float(hi));
+        }
+      }
+    }
+    tmem_st_wait();
     // tril(A) (diagonal kept) -> bf16 tile
     {
       float v[64];
@@ -370,16 +398,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (64 * ch + i > row) v[i] = 0.f;
 #pragma unroll
       for (int j = 0; j < 8; ++j) st_bf16x8(s_at + sw128_offset(row, 64 * ch + 8 * j, kTile), v + 8 * j);
-    }
-    cta_sync();
-    // bf16 copies of R and of S (high, low) for the MMAs, fp32 S for the epilogues
-    state_to_smem(tb, kRhi, kRlo, q4, ch, row, MC, s_rb, s_f);
-    if (ch == 1 && row < MC) {
-      const float sv = s_f[row];
-      const __nv_bfloat16 hi = __float2bfloat16_rn(sv);
-      *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(row, 0)) = hi;
-      *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(row, 1)) =
-          __float2bfloat16_rn(sv - __bfloat162float(hi));
     }
     fence_async_smem();
     cta_sync();
@@ -517,6 +535,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_done();
     }
     wait_mma();
+    // the next tile's inputs stream in as their tiles fall idle: dY (and V
+    // with one CTA per segment) from here, Q and K / V later in this tile
+    if (tid == 0 && t > t0) {
+      mbar_arrive_expect_tx(in_bar, 4 * tile_bytes);
+      tma_load_3d(smem + lay.dy, &tmDY, in_bar, 0, (t - 1) * kTile, bh);
+      if (CS == 1) tma_load_3d(smem + lay.v, &tmV, in_bar, 0, (t - 1) * kTile, bh);
+    }
     if (CS == 2) {
       // my V, dN, R and G copies and the dA tile are idle from here: the
       // peer may send its exchange-2 partials; Q and K come back (into the
@@ -602,6 +627,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         float c3[32];
 #pragma unroll
         for (int j = 0; j < 8; ++j) ld_shared_v4f(s_q + xoff(row, 8 * ch + j, 128), c3 + 4 * j);
+        // the parked dV has been read: the next tile's Q and K take its place
+        cta_sync();
+        if (tid == 0 && t > t0) {
+          tma_load_3d(smem + lay.q, &tmQ, in_bar, 0, (t - 1) * kTile, bh);
+          tma_load_3d(smem + lay.k, &tmK, in_bar, 0, (t - 1) * kTile, bh);
+        }
         if (!own) {
           mbar_wait(x2_free, x_phase, p.status, abort_flag);
           const uint32_t dv_dst = map_peer(s_v, peer), dq_dst = map_peer(s_dn, peer);
@@ -672,7 +703,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       cta_sync();
     }
     x_phase ^= 1;
-    if (tid == 0 && t > t0) issue_in(t - 1);
+    if (tid == 0 && t > t0) {
+      if (CS == 1) {
+        tma_load_3d(smem + lay.q, &tmQ, in_bar, 0, (t - 1) * kTile, bh);
+        tma_load_3d(smem + lay.k, &tmK, in_bar, 0, (t - 1) * kTile, bh);
+      } else {
+        tma_load_3d(smem + lay.v, &tmV, in_bar, 0, (t - 1) * kTile, bh);
+      }
+    }
   }
 
   // segment total of G -> gstates, staged in the idle phi / A tiles for one
