@@ -9,11 +9,14 @@
 //   phi    = exp(F - |x|^2/2)/sqrt(M)  (epilogue: TMEM -> bf16 swizzled smem)
 //   R'_h  += phi_k,h^T [V, 1]          (MMA; fp32 master state in TMEM)
 //   A     += phi_q,h phi_k,h^T         (MMA)
-//   num'  += phi_q,h [R_h, S_h]^T      (MMA; bf16 copies of R(t-1) and of S
-//                                       as a high and a low part in smem)
+//   num   += phi_q,h R_h^T             (MMA; bf16 copy of R(t-1) in smem)
+//   den   += phi_q,h . S_h             (epilogue, fp32 S(t-1))
 // then A is masked to its lower triangle (diagonal kept) and rounded to bf16,
-//   num'  += tril(A) [V, 1]
-// and Y = num / den with den = num'[d] + num'[d + 1].  A tile of 128 rows
+//   [num, rowsum(A)] += tril(A) [V, 1]
+// and Y = num / (den + rowsum(A)).  With d = 64 the ones column rides along
+// V as a second 64-column operand block (one N = 80 MMA): every tcgen05.mma
+// holds the tensor pipe for at least ~50 cycles, so N = 16 side MMAs for the
+// normaliser would cost as much as the products themselves.  A tile of 128 rows
 // holds two 64-row slices or half a 256-row slice; the paper's slice
 // recurrence is exact for any slice size (section 3.4), so the tiling only
 // changes rounding.
@@ -87,14 +90,15 @@ enum {
   B_RBFULL = 19,    // R(t) read out of TMEM, bf16 copies refreshed (state pass: partial free)
   B_DONE = 20,      // MMA drain
   B_SETUP = 21,     // set-up copies (W image, incoming state)
-  B_COUNT = 22
+  B_EPI = 22,       // epilogue warps' S and den partials written
+  B_COUNT = 23
 };
 
 template <int D, bool FAVOR, int MODE>
 struct Layout {
   using C = Cfg<D, FAVOR, MODE>;
   // shared memory (bytes from a 1024-aligned base)
-  uint32_t w, slots, phk, phq, rb, sb, ones, bars, total;
+  uint32_t w, slots, phk, phq, rb, ones, ss, denp, bars, total;
   // TMEM columns
   uint32_t t_buf0, t_buf1, t_num, t_r, t_m;
   __host__ __device__ explicit Layout(int M) {
@@ -104,8 +108,11 @@ struct Layout {
     phk = o; o += kTile * 128 * 2;                 // one feature block of phi_k
     phq = o; o += MODE == MODE_FWD ? kTile * 128 * 2 : 0u;  // phi_q block, then masked A
     rb = o; o += MODE == MODE_FWD ? (uint32_t)M * D * 2 : 0u;
-    sb = o; o += MODE == MODE_FWD ? (uint32_t)M * 32u : 0u;  // [M][16]: S high, S low
-    ones = o; o += 4096;                            // [128][16] no-swizzle: column 0 = 1
+    // column 0 = 1: a [128][64] 128-B-swizzled block placed after every V
+    // slot (d = 64), else a [128][16] no-swizzle operand
+    ones = o; o += D == 64 ? 16384u : 4096u;
+    ss = o; o += MODE == MODE_FWD ? (uint32_t)M * 4u : 0u;        // fp32 S(t-1)
+    denp = o; o += MODE == MODE_FWD ? 2u * 2u * kTile * 4u : 0u;  // [tile parity][half][row]
     bars = o; o += 8 * B_COUNT + 16;
     total = o;
     t_buf0 = 0;
@@ -156,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar + B_RBFULL, kEpiWarps);
     mbar_init(bar + B_DONE, 1);
     mbar_init(bar + B_SETUP, 1);
+    mbar_init(bar + B_EPI, kEpiWarps);
     *abort_flag = 0;
     fence_barrier_init();
     // W^T image and the incoming state (high parts: the forward's master is
@@ -176,13 +184,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // constant operands: the ones block, zero padding of phi_k beyond M (the
   // state MMA always reads 128 features)
-  for (int idx = tid; idx < kTile * 16; idx += kThreads) {
-    const int r = idx >> 4, x = idx & 15;
-    *reinterpret_cast<__nv_bfloat16 *>(smem + lay.ones + n16_offset(r, x)) = __float2bfloat16_rn(x == 0 ? 1.f : 0.f);
-  }
-  if (MODE == MODE_FWD) {
-    for (int idx = tid; idx < M * 16; idx += kThreads)
-      *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(idx >> 4, idx & 15)) = __float2bfloat16_rn(0.f);
+  for (int idx = tid; idx < kTile * (D == 64 ? 64 : 16); idx += kThreads) {
+    const int r = D == 64 ? idx >> 6 : idx >> 4, x = D == 64 ? idx & 63 : idx & 15;
+    *reinterpret_cast<__nv_bfloat16 *>(smem + lay.ones + (D == 64 ? sw128_offset(r, x, kTile) : n16_offset(r, x))) =
+        __float2bfloat16_rn(x == 0 ? 1.f : 0.f);
   }
   if (M < 128) {
     for (int idx = tid; idx < kTile * 128; idx += kThreads) {
@@ -223,16 +228,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; i += 8)
               if (c + i + 8 <= D) st_bf16x8(sbase + lay.rb + sw128_offset(f, c + i, M), v + i);
-            if (c <= D && D < c + 16) {
-              const __nv_bfloat16 hi = __float2bfloat16_rn(v[D - c]);
-              *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(f, 0)) = hi;
-              *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(f, 1)) =
-                  __float2bfloat16_rn(v[D - c] - __bfloat162float(hi));
-            }
+            if (c <= D && D < c + 16) reinterpret_cast<float *>(smem + lay.ss)[f] = v[D - c];
           }
         }
         tmem_st_wait();
       }
+    }
+    // num' columns d .. d+15 start at zero (only the ones product adds there)
+    if (MODE == MODE_FWD && warp >= 2 && half == 0) {
+      float z[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) z[i] = 0.f;
+      tmem_st16(tmem_addr(tbase, 32u * q4, lay.t_num + D), z);
+      tmem_st_wait();
     }
     fence_async_smem();
     tc_fence_before();
@@ -241,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   const uint32_t s_w = sbase + lay.w, s_phk = sbase + lay.phk, s_phq = sbase + lay.phq;
-  const uint32_t s_rb = sbase + lay.rb, s_sb = sbase + lay.sb, s_ones = sbase + lay.ones;
+  const uint32_t s_rb = sbase + lay.rb, s_ones = sbase + lay.ones;
   auto t_buf = [&](int b) { return b ? lay.t_buf1 : lay.t_buf0; };
   auto slot_addr = [&](int n) { return sbase + lay.slots + (uint32_t)(n % C::kSlots) * C::kTileBytes; };
   auto slot_par = [&](int n) { return (uint32_t)((n / C::kSlots) & 1); };
@@ -281,11 +289,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = mbar_wait(bar + b, par, p.status, abort_flag);
         return ok;
       };
+      constexpr uint32_t NV = D == 64 ? D + 16 : D;  // [V, 1] in one MMA when d = 64
       const uint32_t id_a = make_idesc(128, 128, false, false);
       const uint32_t id_n = make_idesc(128, D, false, true);
+      const uint32_t id_nv = make_idesc(128, NV, false, true);
       const uint32_t id_s = make_idesc(128, 16, false, true);
-      const uint32_t id_r = make_idesc(128, D, true, true);
+      const uint32_t id_r = make_idesc(128, NV, true, true);
       const uint32_t id_r1 = make_idesc(128, 16, true, true);
+      // [V, 1] as an MN-major operand: V's slot, then the ones block LBO bytes on
+      auto desc_v1 = [&](uint32_t s_v, int s) {
+        return make_desc(s_v, s_ones - s_v, 1024u, kSwizzle128) + (uint64_t)(s * 128u);
+      };
       int job = 0, n = 0;
       // feature MMA into the next TMEM buffer: F = X W_h^T
       auto f_job = [&](uint32_t s_x, int h) {
@@ -336,8 +350,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t t_r = tbase + lay.t_r + h * NC;
           for (int s = 0; s < kTile / 16; ++s) {
             const uint32_t acc = (MODE == MODE_FWD || gi > 0 || s > 0) ? 1u : 0u;
-            mma_bf16(t_r, desc_mnmajor(s_phk, kTile, 0, s), desc_mnmajor(s_v, kTile, 0, s), id_r, acc);
-            mma_bf16(t_r + D, desc_mnmajor(s_phk, kTile, 0, s), desc_n16(s_ones, s), id_r1, acc);
+            if (D == 64) {
+              mma_bf16(t_r, desc_mnmajor(s_phk, kTile, 0, s), desc_v1(s_v, s), id_r, acc);
+            } else {
+              mma_bf16(t_r, desc_mnmajor(s_phk, kTile, 0, s), desc_mnmajor(s_v, kTile, 0, s), id_r, acc);
+              mma_bf16(t_r + D, desc_mnmajor(s_phk, kTile, 0, s), desc_n16(s_ones, s), id_r1, acc);
+            }
           }
           if (MODE == MODE_FWD) {
             if (!wait(B_PHQ, c & 1)) break;
@@ -354,7 +372,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t aq = desc_kmajor(s_phq, kTile, 0, s);
               mma_bf16(t_a, aq, desc_kmajor(s_phk, kTile, 0, s), id_a, acc);
               mma_bf16(tbase + lay.t_num, aq, desc_mnmajor(s_rb, M, 0, 8 * h + s), id_n, acc);
-              mma_bf16(tbase + lay.t_num + D, aq, desc_n16(s_sb, 8 * h + s), id_s, acc);
             }
           }
           mma_commit(bar + B_PHFREE);
@@ -370,8 +387,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // num' += tril(A) [V, 1]
           for (int s = 0; s < kTile / 16; ++s) {
             const uint64_t aa = desc_kmajor(s_phq, kTile, 0, s);
-            mma_bf16(tbase + lay.t_num, aa, desc_mnmajor(s_v, kTile, 0, s), id_n, 1);
-            mma_bf16(tbase + lay.t_num + D, aa, desc_n16(s_ones, s), id_s, 1);
+            if (D == 64) {
+              mma_bf16(tbase + lay.t_num, aa, desc_v1(s_v, s), id_nv, 1);
+            } else {
+              mma_bf16(tbase + lay.t_num, aa, desc_mnmajor(s_v, kTile, 0, s), id_n, 1);
+              mma_bf16(tbase + lay.t_num + D, aa, desc_n16(s_ones, s), id_s, 1);
+            }
           }
           mma_commit(bar + B_NUMFULL);
         }
@@ -394,13 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar + b);
     };
-    // S of feature f as the bf16 pair (high, low) in columns 0, 1 of the S block
-    auto put_s = [&](int f, float sv) {
-      const __nv_bfloat16 hi = __float2bfloat16_rn(sv);
-      *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(f, 0)) = hi;
-      *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(f, 1)) =
-          __float2bfloat16_rn(sv - __bfloat162float(hi));
-    };
+    float *ss = reinterpret_cast<float *>(smem + lay.ss);
+    float *denp = reinterpret_cast<float *>(smem + lay.denp);
     // columns [c_lo, c_hi) of R' block b handled by this thread: with two
     // blocks each half of the warps owns one, with one they split its columns
     const int csplit = ((NC / 16 + 1) / 2) * 16;
@@ -418,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 16; i += 8)
         if (c + i + 8 <= D) st_bf16x8(s_rb + sw128_offset(f, c + i, M), v + i);
-      if (c <= D && D < c + 16) put_s(f, v[D - c]);
+      if (c <= D && D < c + 16) ss[f] = v[D - c];
     };
 
     // the incoming state was placed in TMEM during set-up
@@ -479,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         arrive(B_EMPTY + nK % C::kSlots);
         if (MODE == MODE_FWD) arrive(B_EMPTY + nQ % C::kSlots);
       }
+      float dpart = 0.f;  // phi_q . S(t-1) over this thread's features
       for (int h = 0; h < nb && ok; ++h) {
         const uint32_t c = (uint32_t)(i * nb + h);
         float v[FC];
@@ -491,12 +508,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (MODE == MODE_FWD) {
           make_phi(s_q, cq, dead, v);
           if (!ok) break;
+#pragma unroll
+          for (int x = 0; x < FC; ++x)
+            if (x < fcols) dpart = fmaf(v[x], ss[128 * h + fcols * half + x], dpart);
           store_phi(s_phq, v);
           fence_async_smem();
           arrive(B_PHQ);
         }
       }
       if (!ok) break;
+      if (MODE == MODE_FWD) denp[((i & 1) * 2 + half) * kTile + row] = dpart;
       if (!FAVOR) {
         arrive(B_EMPTY + nK % C::kSlots);
         if (MODE == MODE_FWD) arrive(B_EMPTY + nQ % C::kSlots);
@@ -541,6 +562,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (64 * half + x > row) v[x] = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) st_bf16x8(s_phq + sw128_offset(row, 64 * half + 8 * j, kTile), v + 8 * j);
+        if (half == 0) {
+          // num' columns d .. d+15 restart at zero: both halves read them
+          // last tile, before either could get here
+          float z[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) z[x] = 0.f;
+          tmem_st16(tmem_addr(tbase, lane_base, lay.t_num + D), z);
+          tmem_st_wait();
+          tc_fence_before();
+        }
         fence_async_smem();
         arrive(B_ATFULL);
       }
@@ -558,6 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_async_smem();
       tc_fence_before();
       arrive(B_RBFULL);
+      arrive(B_EPI);  // this warp's S(t) and den partials are in shared memory
       // Y = num / den
       {
         if (!wait(B_NUMFULL, i & 1)) break;
@@ -572,8 +604,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(a, v);
         tc_fence_before();
         arrive(B_NUMEMPTY);
+        if (!wait(B_EPI, i & 1)) break;
         if (!dead) {
-          const float inv = 1.0f / (dv[0] + dv[1]);
+          const float inv =
+              1.0f / (dv[0] + denp[((i & 1) * 2) * kTile + row] + denp[((i & 1) * 2 + 1) * kTile + row]);
           uint4 *dst = reinterpret_cast<uint4 *>(p.y + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + YC * half);
 #pragma unroll
           for (int j = 0; j < YC / 8; ++j)
