@@ -41,6 +41,8 @@ struct Plan {
   size_t dwpart_off;   // [BH * P][d][M] (backward with dW only)
   size_t wimg_off;     // tensor path, FAVOR+: W^T as the bf16 [M][64] swizzled
                        // shared-memory image the kernels bulk-copy
+  size_t gimg_off;     // tensor-path backward: per (head, segment) G_end record,
+                       // bf16 [M][64] swizzled image + fp32 [M] (M * 132 bytes)
   size_t scratch_stride;
   size_t total_floats;
 };

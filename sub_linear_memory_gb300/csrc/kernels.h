@@ -43,6 +43,9 @@ size_t tc_smem_bytes(int d, int M, bool favor);
 cudaError_t tc_forward(const Plan &p, const Args &a, cudaStream_t st);
 // K-side totals of R' for the first nseg segments, scanned (tensor path).
 cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, cudaStream_t st);
+// dK, dV += the terms of the later segments' reverse state (after the backward
+// kernel and the reverse scan of the segment G totals).
+cudaError_t tc_correction(const Plan &p, const Args &a, cudaStream_t st);
 
 // Tensor-core SLiM backward (tc_backward.cu): bf16 I/O, d = 64, M <= 128.
 bool tc_backward_supported(int d, int M, int chunk, bool favor);

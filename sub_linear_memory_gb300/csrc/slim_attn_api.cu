@@ -152,6 +152,7 @@ Plan make_plan(int B, int H, int L, int d, int M, int chunk, bool favor, bool bw
   p.scratch_off = off; off += p.scratch_stride * p.BH * p.P;
   p.dwpart_off = off; if (bwd && want_dw) off += align_floats((size_t)p.BH * p.P * d * M);
   p.wimg_off = off; if (path == 2 && favor) off += align_floats((size_t)M * 32);
+  p.gimg_off = off; if (path == 2 && bwd) off += align_floats((size_t)p.BH * p.P * M * 33);
   p.total_floats = off;
   return p;
 }

@@ -740,267 +740,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_dealloc(tb, 512);
 }
 
-// Correction: add G_end(s) (the G of every later segment) to dK and dV of
-// segment s:  dphi_k += V G_V^T + 1 G_S^T,  dV += phi_k G_V^T, one 128-feature
-// block at a time (every term is a sum over features).
-// The tiles of segments 0 .. P-2 are independent here, so they are dealt out
-// evenly to one CTA per SM (flat over (b, h) and tiles), K and V of the next
-// tile stream in while the current one is processed.
-struct FixLayout {
-  uint32_t w, k, v, phk, gb, gs, usk, bars, total;
-  __host__ __device__ explicit FixLayout(int M) {
-    uint32_t o = 0;
-    const uint32_t tile = kTile * D * 2;
-    w = o; o += (uint32_t)M * 128u;   // W^T as [M][64]
-    k = o; o += 2 * tile;              // two stages
-    v = o; o += 2 * tile;
-    phk = o; o += kTile * 256;
-    gb = o; o += (uint32_t)M * 128u;  // G_end(s)[0:d] as bf16 [M][64]
-    gs = o; o += (uint32_t)M * 4u;    // G_end(s)[d] (fp32)
-    usk = o; o += 2 * kTile * 4;
-    bars = o; o += 64;
-    total = o;
-  }
-};
-
-// dst[0:32] = bf16(dst[0:32] + add[0:32]) with 16-B accesses (dst 16-B aligned).
-__device__ __forceinline__ void add_bf16_row32(__nv_bfloat16 *dst, const float *add) {
-  uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint4 u = d4[j];
-    uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float lo = __uint_as_float(w[i] << 16) + add[8 * j + 2 * i];
-      const float hi = __uint_as_float(w[i] & 0xFFFF0000u) + add[8 * j + 2 * i + 1];
-      w[i] = pack_bf16(lo, hi);
-    }
-    d4[j] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
-template <bool FAVOR>
-__global__ void __launch_bounds__(kThreads, 1)
-    tc_bwd_fix_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                      Params p) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char *smem =
-      reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int M = p.M, DP = D + 1;
-  const int nb = (M + 127) / 128, MB = M < 128 ? M : 128;  // feature blocks and their width
-  const FixLayout lay(M);
-  const uint32_t sb = smem_u32(smem);
-  uint64_t *in_bar = reinterpret_cast<uint64_t *>(smem + lay.bars);  // stages at [0], [2]
-  uint64_t *mma_bar = in_bar + 1;
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(in_bar + 3);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(in_bar + 4);
-  uint64_t *setup_bar = in_bar + 5;
-  float *gs_f = reinterpret_cast<float *>(smem + lay.gs);
-  float *usk = reinterpret_cast<float *>(smem + lay.usk);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q4 = warp & 3, ch = warp >> 2, row = 32 * q4 + lane;
-  const int half = MB / 2;
-  // flat work: unit u = (bh, tile) over the first (P - 1) * tps tiles of each head
-  const long long per_head = (long long)(p.P - 1) * p.tps;
-  const long long units = per_head * p.BH;
-  const long long u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
-
-  if (tid == 0) {
-    mbar_init(in_bar, 1);
-    mbar_init(in_bar + 2, 1);
-    mbar_init(mma_bar, 1);
-    mbar_init(setup_bar, 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-    if (FAVOR) {
-      mbar_arrive_expect_tx(setup_bar, (uint32_t)M * 128u);
-      bulk_load(smem + lay.w, p.wimg, (uint32_t)M * 128u, setup_bar);
-    }
-  }
-  if (warp == 0) tmem_alloc(tslot, 512);
-  if (MB < 128) {
-    for (int idx = tid; idx < kTile * 128; idx += kThreads) {
-      const int r = idx >> 7, x = idx & 127;
-      if (x >= MB) st_bf16_scalar(smem, lay.phk + sw128_offset(r, x, kTile), 0.f);
-    }
-  }
-  fence_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tb = *tslot;
-  if (FAVOR) mbar_wait(setup_bar, 0, p.status, abort_flag);
-  const uint32_t s_w = sb + lay.w, s_phk = sb + lay.phk;
-  const uint32_t s_gb = sb + lay.gb;
-  const uint32_t tile_bytes = kTile * D * 2;
-  constexpr uint32_t kF = 0, kDV = 128, kDK = 192;  // TMEM columns
-  uint32_t in_phase0 = 0, in_phase1 = 0, mma_phase = 0;
-  auto unit_of = [&](long long u, int &bh, int &t, int &seg) {
-    bh = (int)(u / per_head);
-    t = (int)(u - (long long)bh * per_head);
-    seg = t / p.tps;
-  };
-  auto issue_in = [&](long long u, int stage) {
-    int bh, t, seg;
-    unit_of(u, bh, t, seg);
-    mbar_arrive_expect_tx(in_bar + 2 * stage, 2 * tile_bytes);
-    tma_load_3d(smem + lay.k + stage * tile_bytes, &tmK, in_bar + 2 * stage, 0, t * kTile, bh);
-    tma_load_3d(smem + lay.v + stage * tile_bytes, &tmV, in_bar + 2 * stage, 0, t * kTile, bh);
-  };
-  auto wait_mma = [&]() {
-    __syncwarp();
-    mbar_wait(mma_bar, mma_phase, p.status, abort_flag);
-    mma_phase ^= 1;
-    tc_fence_after();
-  };
-  auto cta_sync = [&]() {
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-  };
-
-  if (tid == 0 && u0 < u1) issue_in(u0, 0);
-  int cur_key = -1;  // (bh, seg) whose G_end is loaded
-  for (long long u = u0; u < u1; ++u) {
-    const int stage = (int)((u - u0) & 1);
-    int bh, t, seg;
-    unit_of(u, bh, t, seg);
-    const int key = bh * p.P + seg;
-    if (key != cur_key) {
-      // G_end(s) = gstates[s + 1] after the reverse scan -> bf16 [M][64] + G_S
-      __syncthreads();
-      const float *__restrict__ g = p.gstates + ((size_t)bh * p.P + seg + 1) * (size_t)M * DP;
-      // loads in batches of 16 so their latencies overlap
-      for (int base = tid; base < M * D; base += 16 * kThreads) {
-        float x[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int idx = base + j * kThreads;
-          x[j] = idx < M * D ? __ldg(g + (size_t)(idx / D) * DP + idx % D) : 0.f;
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int idx = base + j * kThreads;
-          if (idx < M * D) st_bf16_scalar(smem, lay.gb + sw128_offset(idx / D, idx % D, M), x[j]);
-        }
-      }
-      for (int f = tid; f < M; f += kThreads) gs_f[f] = g[(size_t)f * DP + D];
-      fence_async_smem();
-      cta_sync();
-      cur_key = key;
-    }
-    const uint32_t s_k = sb + lay.k + stage * tile_bytes, s_v = sb + lay.v + stage * tile_bytes;
-    const int valid = min(kTile, p.L - t * kTile);
-    const bool live = row < valid;
-    mbar_wait(in_bar + 2 * stage, stage ? in_phase1 : in_phase0, p.status, abort_flag);
-    if (stage) in_phase1 ^= 1; else in_phase0 ^= 1;
-    if (tid == 0 && u + 1 < u1) issue_in(u + 1, stage ^ 1);
-    const float ck = FAVOR ? favor_row_const(tile_row_sqnorm(s_k, row, D), M) : 0.f;
-    float uk = 0.f;
-    for (int b = 0; b < nb; ++b) {
-      if (FAVOR) {
-        if (tid == 0) {
-          const uint32_t id = make_idesc(128, MB, false, false);
-          for (int s = 0; s < D / 16; ++s)
-            mma_bf16(tb + kF, desc_kmajor(s_k, kTile, 0, s), desc_kmajor(s_w, M, 128 * b, s), id, s > 0);
-          mma_commit(mma_bar);
-        }
-        wait_mma();
-        for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 32) {
-          float v[32];
-          tmem_ld32(tmem_addr(tb, 32 * q4, kF + c0), v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = live ? favor_feature(v[i], ck) : 0.f;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) st_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
-        }
-      } else {
-        for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 8) {
-          float v[8];
-          ld_bf16x8(s_k + sw128_offset(row, c0, kTile), v);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = live ? elu1_feature(v[i]) : 0.f;
-          st_bf16x8(s_phk + sw128_offset(row, c0, kTile), v);
-        }
-      }
-      fence_async_smem();
-      cta_sync();
-      // dphi_k' = V G_V^T -> F ; dV' += phi_k G_V^T -> DV
-      if (tid == 0) {
-        const uint32_t id1 = make_idesc(128, MB, false, false);
-        for (int s = 0; s < D / 16; ++s)
-          mma_bf16(tb + kF, desc_kmajor(s_v, kTile, 0, s), desc_kmajor(s_gb, M, 128 * b, s), id1, s > 0);
-        const uint32_t id2 = make_idesc(128, D, false, true);
-        for (int s = 0; s < MB / 16; ++s)
-          mma_bf16(tb + kDV, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_gb, M, 0, 8 * b + s), id2,
-                   (b > 0 || s > 0));
-        mma_commit(mma_bar);
-      }
-      wait_mma();
-      for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 32) {
-        float x[32];
-        tmem_ld32(tmem_addr(tb, 32 * q4, kF + c0), x);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float fk[8];
-          ld_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), fk);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float dk = x[8 * j + i] + gs_f[128 * b + c0 + 8 * j + i];
-            x[8 * j + i] = FAVOR ? fk[i] * dk : dk * fminf(fk[i], 1.f);
-            uk += x[8 * j + i];
-          }
-        }
-        if (FAVOR) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) st_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), x + 8 * j);
-        } else if (live) {
-          add_bf16_row32(p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + c0, x);
-        }
-      }
-      fence_async_smem();
-      cta_sync();
-      if (FAVOR) {
-        if (tid == 0) {
-          const uint32_t id = make_idesc(128, D, false, true);
-          for (int s = 0; s < MB / 16; ++s)
-            mma_bf16(tb + kDK, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_w, M, 0, 8 * b + s), id,
-                     (b > 0 || s > 0));
-          mma_commit(mma_bar);
-        }
-        wait_mma();  // phi_k is overwritten by the next block's features
-      }
-    }
-    usk[ch * kTile + row] = uk;
-    __syncthreads();
-    {
-      float v[32];
-      tmem_ld32(tmem_addr(tb, 32 * q4, kDV + 32 * ch), v);
-      if (live) add_bf16_row32(p.dv + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch, v);
-    }
-    if (FAVOR) {
-      const float sk = usk[row] + usk[kTile + row];
-      float b[32];
-      tmem_ld32(tmem_addr(tb, 32 * q4, kDK + 32 * ch), b);
-      if (live) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float xk[8];
-          ld_bf16x8(s_k + sw128_offset(row, 32 * ch + 8 * j, kTile), xk);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) b[8 * j + i] = fmaf(-xk[i], sk, b[8 * j + i]);
-        }
-        add_bf16_row32(p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch, b);
-      }
-    }
-    cta_sync();
-  }
-  cta_sync();
-  if (warp == 0) tmem_dealloc(tb, 512);
-}
-
 template <bool FAVOR, int CS>
 cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mdy;
@@ -1054,19 +793,7 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
       e = scan_states_f32_rev(pl, a.ws + pl.gstates_off + (size_t)pl.M * (D + 1), pl.P - 1, st);
       if (e != cudaSuccess) return e;
     }
-    const FixLayout fl(pl.M);
-    const int smem = (int)fl.total + 1024;
-    auto kern = tc_bwd_fix_kernel<FAVOR>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long long units = (long long)(pl.P - 1) * pl.cps * pl.BH;
-    const int grid = (int)std::min<long long>(sms, units);
-    ProfScope ps("tc_backward_fix", st);
-    kern<<<grid, kThreads, smem, st>>>(mk, mv, p);
-    e = cudaGetLastError();
+    e = tc_correction(pl, a, st);
   }
   return e;
 }
