@@ -120,12 +120,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long units = p.per_head * p.BH;
   const long long u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
   const int nun = (int)(u1 - u0);
-  auto unit_bh = [&](long long u) { return (int)(u / p.per_head); };
-  auto unit_t = [&](long long u) { return (int)(u - (long long)unit_bh(u) * p.per_head); };
-  auto unit_key = [&](long long u) { return unit_bh(u) * p.P + unit_t(u) / p.tps; };
-  // a new G_end image is needed at unit i when its (head, segment) differs
-  auto new_key = [&](int i) { return i == 0 || unit_key(u0 + i) != unit_key(u0 + i - 1); };
-  auto last_of_key = [&](int i) { return i == nun - 1 || unit_key(u0 + i) != unit_key(u0 + i + 1); };
+  // every role walks the same units with counters (no divisions per unit):
+  // head bh, tile t, segment seg and position pos of the tile in it; the
+  // segment's G_end changes when pos wraps
+  struct Cursor {
+    int bh, t, seg, pos;
+  };
+  const int per_head = (int)p.per_head;  // a multiple of tps
+  Cursor first;
+  first.bh = (int)(u0 / p.per_head);
+  first.t = (int)(u0 - (long long)first.bh * p.per_head);
+  first.seg = first.t / p.tps;
+  first.pos = first.t - first.seg * p.tps;
+  auto advance = [&](Cursor &c) {
+    ++c.t;
+    if (++c.pos == p.tps) {
+      c.pos = 0;
+      ++c.seg;
+    }
+    if (c.t == per_head) {
+      c.t = 0;
+      c.seg = 0;
+      ++c.bh;
+    }
+  };
+  auto new_key = [&](int i, const Cursor &c) { return i == 0 || c.pos == 0; };
+  auto last_of_key = [&](int i, const Cursor &c) { return i == nun - 1 || c.pos == p.tps - 1; };
   const uint32_t grec_bytes = (uint32_t)M * 132u;
 
   if (tid == 0) {
@@ -184,30 +204,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       // unit j's staged increments -> dK, dV; returns once its slots are read
-      auto flush = [&](int j) {
+      auto flush = [&](int j, const Cursor &c) {
         if (!mbar_wait(bar + B_STG + (j & 1), (j >> 1) & 1, p.status, abort_flag)) return false;
-        const long long u = u0 + j;
-        const int bh = unit_bh(u), t = unit_t(u);
-        tma_reduce_add_3d(&tmDV, slot_addr(2 * j + 1), 0, t * kTile, bh);
-        tma_reduce_add_3d(&tmDK, slot_addr(2 * j), 0, t * kTile, bh);
+        tma_reduce_add_3d(&tmDV, slot_addr(2 * j + 1), 0, c.t * kTile, c.bh);
+        tma_reduce_add_3d(&tmDK, slot_addr(2 * j), 0, c.t * kTile, c.bh);
         tma_store_commit();
         tma_store_wait_read();
         return true;
       };
+      Cursor cur = first, prev1 = first, prev2 = first;  // units i, i-1, i-2
       for (int i = 0; i < nun && ok; ++i) {
-        const long long u = u0 + i;
-        const int bh = unit_bh(u), t = unit_t(u);
-        if (new_key(i)) {
+        if (new_key(i, cur)) {
           // the previous G_end is no longer read once its last unit is done
           if (keys > 0 && !mbar_wait(bar + B_GEMPTY, (keys - 1) & 1, p.status, abort_flag)) break;
           mbar_arrive_expect_tx(bar + B_GFULL, grec_bytes);
-          bulk_load(smem + lay.g, p.grec + (size_t)(bh * p.P + t / p.tps) * grec_bytes, grec_bytes, bar + B_GFULL);
+          bulk_load(smem + lay.g, p.grec + (size_t)(cur.bh * p.P + cur.seg) * grec_bytes, grec_bytes, bar + B_GFULL);
           ++keys;
         }
-        if (i >= 2 && !flush(i - 2)) break;  // unit i takes unit i-2's slots
-        ok = load(&tmK, t, bh) && load(&tmV, t, bh);
+        if (i >= 2 && !flush(i - 2, prev2)) break;  // unit i takes unit i-2's slots
+        ok = load(&tmK, cur.t, cur.bh) && load(&tmV, cur.t, cur.bh);
+        prev2 = prev1;
+        prev1 = cur;
+        advance(cur);
       }
-      for (int j = max(0, nun - 2); j < nun && ok; ++j) ok = flush(j);
+      // the last two units (prev2 = unit nun-2, prev1 = unit nun-1)
+      if (ok && nun >= 2) ok = flush(nun - 2, prev2);
+      if (ok && nun >= 1) ok = flush(nun - 1, prev1);
       tma_store_wait_all();
       for (int m = max(0, n - kSlots); m < n; ++m) mbar_drain(bar + B_FULL + m % kSlots, slot_par(m));
       if (keys > 0) mbar_drain(bar + B_GFULL, (keys - 1) & 1);
@@ -225,10 +247,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_o = make_idesc(128, D, false, true);
       if (FAVOR) wait(B_WFULL, 0);
       int fj = 0, dj = 0, keys = 0;
-      for (int i = 0; i < nun && ok; ++i) {
+      Cursor cur = first;
+      for (int i = 0; i < nun && ok; ++i, advance(cur)) {
         const int nK = 2 * i, nV = 2 * i + 1;
         const uint32_t s_k = slot_addr(nK), s_v = slot_addr(nV);
-        if (new_key(i)) {
+        if (new_key(i, cur)) {
           if (!wait(B_GFULL, keys & 1)) break;
           ++keys;
         }
@@ -280,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         mma_commit(bar + B_OUTFULL);
-        if (last_of_key(i)) mma_commit(bar + B_GEMPTY);
+        if (last_of_key(i, cur)) mma_commit(bar + B_GEMPTY);
       }
       mma_commit(bar + B_DONE);
       mbar_drain(bar + B_DONE, 0);
@@ -301,14 +324,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float *gs = reinterpret_cast<const float *>(smem + lay.gs);
     float *usum = reinterpret_cast<float *>(smem + lay.usum);
     int fj = 0, dj = 0, keys = 0;
-    for (int i = 0; i < nun && ok; ++i) {
-      const long long u = u0 + i;
-      const int bh = unit_bh(u), t = unit_t(u);
+    Cursor cur = first;
+    for (int i = 0; i < nun && ok; ++i, advance(cur)) {
+      const int t = cur.t;
       const int nK = 2 * i, nV = 2 * i + 1;
       const uint32_t s_k = slot_addr(nK);
       const int valid = min(kTile, p.L - t * kTile);
       const bool dead = row >= valid;
-      if (new_key(i)) {
+      if (new_key(i, cur)) {
         if (!wait(B_GFULL, keys & 1)) break;
         ++keys;
       }
@@ -389,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (FAVOR) usum[((i & 1) * 2 + half) * kTile + row] = uk;
       arrive(B_EPI);
-      if (last_of_key(i)) arrive(B_GEMPTY);  // G_S read for the last time
+      if (last_of_key(i, cur)) arrive(B_GEMPTY);  // G_S read for the last time
       // dV += dV', dK += dK' - k rowsum(u)
       if (!wait(B_OUTFULL, i & 1)) break;
       tc_fence_after();
