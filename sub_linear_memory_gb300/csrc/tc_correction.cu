@@ -214,15 +214,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       Cursor cur = first, prev1 = first, prev2 = first;  // units i, i-1, i-2
       for (int i = 0; i < nun && ok; ++i) {
-        if (new_key(i, cur)) {
+        if (i >= 2 && !flush(i - 2, prev2)) break;  // unit i takes unit i-2's slots
+        // K and V first: the MMA warp issues this unit's F early, before it
+        // releases the previous G_end
+        ok = load(&tmK, cur.t, cur.bh) && load(&tmV, cur.t, cur.bh);
+        if (ok && new_key(i, cur)) {
           // the previous G_end is no longer read once its last unit is done
           if (keys > 0 && !mbar_wait(bar + B_GEMPTY, (keys - 1) & 1, p.status, abort_flag)) break;
           mbar_arrive_expect_tx(bar + B_GFULL, grec_bytes);
           bulk_load(smem + lay.g, p.grec + (size_t)(cur.bh * p.P + cur.seg) * grec_bytes, grec_bytes, bar + B_GFULL);
           ++keys;
         }
-        if (i >= 2 && !flush(i - 2, prev2)) break;  // unit i takes unit i-2's slots
-        ok = load(&tmK, cur.t, cur.bh) && load(&tmV, cur.t, cur.bh);
         prev2 = prev1;
         prev1 = cur;
         advance(cur);
@@ -247,10 +249,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_o = make_idesc(128, D, false, true);
       if (FAVOR) wait(B_WFULL, 0);
       int fj = 0, dj = 0, keys = 0;
+      // F = K W_h of unit j: issued one unit ahead, while unit j-1's later
+      // MMAs run, so the epilogue finds it ready when it starts unit j
+      auto f_job = [&](int j, int h) {
+        const int nK = 2 * j;
+        if (h == 0 && !wait(B_FULL + nK % kSlots, slot_par(nK))) return;
+        const int b = fj & 1, use = fj >> 1;
+        if (use > 0 && !wait(B_FEMPTY + b, (use - 1) & 1)) return;
+        tc_fence_after();
+        for (int s = 0; s < D / 16; ++s)
+          mma_bf16(tbase + (b ? kF1 : kF0), desc_kmajor(slot_addr(nK), kTile, 0, s), desc_kmajor(s_w, M, 128 * h, s),
+                   id_f, s > 0);
+        mma_commit(bar + B_FFULL + b);
+        ++fj;
+      };
+      if (FAVOR && nun > 0)
+        for (int h = 0; h < nb && ok; ++h) f_job(0, h);
       Cursor cur = first;
       for (int i = 0; i < nun && ok; ++i, advance(cur)) {
         const int nK = 2 * i, nV = 2 * i + 1;
-        const uint32_t s_k = slot_addr(nK), s_v = slot_addr(nV);
+        const uint32_t s_v = slot_addr(nV);
         if (new_key(i, cur)) {
           if (!wait(B_GFULL, keys & 1)) break;
           ++keys;
@@ -259,17 +277,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait(B_FULL + nV % kSlots, slot_par(nV))) break;
         tc_fence_after();
         for (int h = 0; h < nb && ok; ++h) {
-          if (FAVOR) {
-            // F = K W_h
-            const int b = fj & 1, use = fj >> 1;
-            if (use > 0 && !wait(B_FEMPTY + b, (use - 1) & 1)) break;
-            tc_fence_after();
-            for (int s = 0; s < D / 16; ++s)
-              mma_bf16(tbase + (b ? kF1 : kF0), desc_kmajor(s_k, kTile, 0, s), desc_kmajor(s_w, M, 128 * h, s), id_f,
-                       s > 0);
-            mma_commit(bar + B_FFULL + b);
-            ++fj;
-          }
           // V G_V,h^T
           if (dj > 0 && !wait(B_DEMPTY, (dj - 1) & 1)) break;
           tc_fence_after();
@@ -279,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++dj;
         }
         if (!ok) break;
-        mma_commit(bar + B_EMPTY + nK % kSlots);
+        mma_commit(bar + B_EMPTY + nK % kSlots);  // K's last reader (F of this unit) was issued earlier
         mma_commit(bar + B_EMPTY + nV % kSlots);
         for (int h = 0; h < nb && ok; ++h) {
           const uint32_t c = (uint32_t)(i * nb + h);
@@ -291,6 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16(tbase + kDV, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_g, M, 0, 8 * h + s), id_o,
                      (h > 0 || s > 0) ? 1u : 0u);
           mma_commit(bar + B_PHFREE);
+          // this block's F buffer has been read: the next unit's F_h may go in
+          if (FAVOR && i + 1 < nun) f_job(i + 1, h);
           if (FAVOR) {
             if (!wait(B_U, c & 1)) break;
             tc_fence_after();
