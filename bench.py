@@ -62,6 +62,7 @@ def work_per_token_head(wl):
 KERNEL_SOURCES = {
     "tc_backward": ("tc_backward.cu", "tc_common.cuh", "common.cuh"),
     "tc_forward": ("tc_forward.cu", "tc_common.cuh", "common.cuh"),
+    "tc_backward_fix": ("tc_correction.cu", "tc_common.cuh", "common.cuh"),
 }
 
 
