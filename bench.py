@@ -194,14 +194,15 @@ def max_over_ranks(x, dist):
 
 
 def cpu_oracle_sample(wl, row_frac=1.0, threads=0):
-    """Time the oracle (fwd + bwd) on min(cores, B*H) heads of the workload,
-    optionally on the first ``row_frac`` of the rows; returns (seconds,
-    heads, rows, cores).  Inputs follow the workload recipe on the CPU."""
+    """Time the oracle (fwd + bwd) on min(2 * cores, B*H) heads of the
+    workload, optionally on the first ``row_frac`` of the rows; returns
+    (seconds, heads, rows, cores).  Inputs follow the workload recipe on the
+    CPU."""
     import oracle
     from sub_linear_memory_gb300 import inputs
 
     cores = threads or len(os.sched_getaffinity(0))
-    heads = min(cores, wl.B * wl.H)
+    heads = min(2 * cores, wl.B * wl.H)
     rows = max(1, int(wl.L * row_frac))
     small = wl.with_(L=rows)
     q, k, v, dy, w = inputs.make_inputs(small, heads=(1, heads))
@@ -345,25 +346,52 @@ def run_native(args, wl):
     # end to end through the public API with pinned host buffers
     hq, hk, hv, hdy = (t.cpu().pin_memory() for t in (q, k, v, dy))
     hy, hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(4))
-    dev_in = [torch.empty_like(q) for _ in range(4)]
-    e2e_steps = max(1, min(args.steps, 10))
+    e2e_steps = max(2, min(args.steps, 10))
+    # End to end: every step copies its inputs from pinned host memory and
+    # reads its outputs back. Device buffers are double-buffered by step
+    # parity so that the host-to-device copies of step i+1 and the
+    # device-to-host copies of step i-1 run on their own streams while step i
+    # computes.
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    ins = [[torch.empty_like(q) for _ in range(4)] for _ in range(2)]
+    outs = [[torch.empty_like(q) for _ in range(4)] for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_read = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for dst, src in zip(dev_in, (hq, hk, hv, hdy)):
-            dst.copy_(src, non_blocking=True)
-        yy = binding.slim_attn_fwd(dev_in[0], dev_in[1], dev_in[2], w, wl.chunk, y=y)
-        binding.slim_attn_bwd(dev_in[0], dev_in[1], dev_in[2], w, dev_in[3], wl.chunk, out=out)
-        for dst, src in zip((hy, hdq, hdk, hdv), (yy, dq, dk, dv)):
-            dst.copy_(src, non_blocking=True)
+    def e2e_run(nsteps, e_start=None, e_stop=None):
+        if e_start is not None:
+            e_start.record(stream)
+        h2d_s.wait_stream(stream)
+        for i in range(nsteps):
+            b = i % 2
+            if i >= 2:
+                h2d_s.wait_event(ev_done[b])  # step i-2 no longer reads ins[b]
+            with torch.cuda.stream(h2d_s):
+                for dst, src in zip(ins[b], (hq, hk, hv, hdy)):
+                    dst.copy_(src, non_blocking=True)
+                ev_in[b].record(h2d_s)
+            stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_read[b])  # step i-2's outputs have left outs[b]
+            o = outs[b]
+            binding.slim_attn_fwd(ins[b][0], ins[b][1], ins[b][2], w, wl.chunk, y=o[0])
+            binding.slim_attn_bwd(ins[b][0], ins[b][1], ins[b][2], w, ins[b][3], wl.chunk, out=(o[1], o[2], o[3], None))
+            ev_done[b].record(stream)
+            d2h_s.wait_event(ev_done[b])
+            with torch.cuda.stream(d2h_s):
+                for dst, src in zip((hy, hdq, hdk, hdv), o):
+                    dst.copy_(src, non_blocking=True)
+                ev_read[b].record(d2h_s)
+        stream.wait_stream(d2h_s)
+        if e_stop is not None:
+            e_stop.record(stream)
 
-    e2e_step()
+    e2e_run(2)
     torch.cuda.synchronize()
     barrier(dist)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e2e_run(e2e_steps, e0, e1)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist) / e2e_steps
     nbytes = q.numel() * q.element_size()
@@ -421,7 +449,7 @@ def run_native(args, wl):
                     for n, (c, t) in sorted(kernels.items(), key=lambda kv: -kv[1][1])},
     }
     if args.memory and rank == 0:
-        del hq, hk, hv, hdy, hy, hdq, hdk, hdv, dev_in
+        del hq, hk, hv, hdy, hy, hdq, hdk, hdv, ins, outs
         line["memory"] = memory_sweep(binding, inputs)
     if rank == 0 and world == 1 and args.cpu_baseline:
         secs, heads, rows, cores = cpu_oracle_sample(wl, args.cpu_row_frac)
@@ -449,7 +477,7 @@ def main(argv=None):
                          "(a reduced case for profiling); the default is the workload's own")
     ap.add_argument("--no-memory", dest="memory", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
-    ap.add_argument("--cpu-row-frac", type=float, default=0.5,
+    ap.add_argument("--cpu-row-frac", type=float, default=1.0,
                     help="fraction of the rows the CPU-baseline sample covers")
     ap.add_argument("--ref-row-frac", type=float, default=0.125,
                     help="fraction of the rows each reference-arm step covers")

@@ -517,6 +517,7 @@ cudaError_t tc_correction(const Plan &pl, const Args &a, cudaStream_t st) {
       !make_map_bf16_3d(&mdv, a.dv, pl.BH, pl.L, tcc::D, tcc::kTile))
     return cudaErrorInvalidValue;
   {
+    ProfScope ps("prep_g", st);
     const long long n = (long long)pl.BH * (pl.P - 1) * pl.M * (tcc::D + 1);
     const int blocks = (int)std::min<long long>((n + 255) / 256, 4096);
     tcc::prep_g_kernel<<<blocks, 256, 0, st>>>(a.ws + pl.gstates_off,

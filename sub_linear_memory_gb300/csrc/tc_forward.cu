@@ -699,6 +699,7 @@ __global__ void prep_w_kernel(const float *__restrict__ w, __nv_bfloat16 *__rest
 
 cudaError_t prep_w(const Plan &pl, const Args &a, cudaStream_t st) {
   if (!pl.favor) return cudaSuccess;
+  ProfScope ps("prep_w", st);
   const int n = pl.M * 64;
   prep_w_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.w, reinterpret_cast<__nv_bfloat16 *>(a.ws + pl.wimg_off), pl.M);
   return cudaGetLastError();
