@@ -42,7 +42,9 @@ bool tc_forward_supported(int d, int M, int chunk, bool favor);
 size_t tc_smem_bytes(int d, int M, bool favor);
 cudaError_t tc_forward(const Plan &p, const Args &a, cudaStream_t st);
 // K-side totals of R' for the first nseg segments, scanned (tensor path).
-cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, cudaStream_t st);
+// zero_grads: also set dQ, dK, dV to zero tile by tile (the two-CTA backward
+// then adds each CTA's partials into them).
+cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, bool zero_grads, cudaStream_t st);
 // dK, dV += the terms of the later segments' reverse state (after the backward
 // kernel and the reverse scan of the segment G totals).
 cudaError_t tc_correction(const Plan &p, const Args &a, cudaStream_t st);

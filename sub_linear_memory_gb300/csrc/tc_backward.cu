@@ -17,6 +17,14 @@
 // G starts at zero at the end of each segment, so dK and dV here miss the
 // later segments' G; the correction kernel adds G_end(s) (the reverse scan of
 // the segments' G totals) afterwards: both terms are linear in G.
+//
+// With 256 features a segment runs on a two-CTA cluster, each CTA owning 128
+// features.  num' and den need all features for dN', so the CTAs exchange
+// their partials (distributed shared memory).  dV, dQ and dK are sums over
+// features too, but nothing downstream needs them inside the kernel: each
+// CTA rounds its partial to bf16 and adds it into the (zeroed) outputs with
+// a TMA reduce-add.  The order of the two adds is not fixed, so those
+// outputs may differ from run to run in the last bf16 bit.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -46,7 +54,7 @@ struct Params {
 
 struct Layout {
   uint32_t w, q, k, v, dy, phq, phk, at, dn, rb, ones, ddb;
-  uint32_t sb, s_f, gs_f, dd, usq, usk, dot, rx_den, rx_usq, rx_usk, bars, total;
+  uint32_t sb, s_f, gs_f, dd, usq, usk, dot, rx_den, bars, total;
   __host__ __device__ explicit Layout(int MC) {
     uint32_t o = 0;
     const uint32_t tile = kTile * D * 2;
@@ -70,8 +78,6 @@ struct Layout {
     usk = o; o += 2 * kTile * 4;
     dot = o; o += 2 * kTile * 4;
     rx_den = o; o += 128 * 4;  // cluster exchange: the peer's den partials
-    rx_usq = o; o += 64 * 4;
-    rx_usk = o; o += 64 * 4;
     bars = o; o += 128;
     total = o;
   }
@@ -130,7 +136,8 @@ template <bool FAVOR, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDY,
-                  Params p) {
+                  const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmDK,
+                  const __grid_constant__ CUtensorMap tmDV, Params p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem =
       reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -143,12 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t *tslot = reinterpret_cast<uint32_t *>(in_bar + 3);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(in_bar + 4);
   uint64_t *setup_bar = in_bar + 5;
-  // cluster exchanges: data received (st.async bytes) and receive buffers
-  // released by the peer (remote arrive), one phase each per tile
-  uint64_t *x1_full = in_bar + 6, *x2_full = in_bar + 7, *x1_free = in_bar + 8, *x2_free = in_bar + 9;
+  // cluster exchange of num' and den: data received (st.async bytes) and
+  // receive tiles released by the peer (remote arrive), one phase per tile
+  uint64_t *x1_full = in_bar + 6, *x1_free = in_bar + 8;
   float *rx_den = reinterpret_cast<float *>(smem + lay.rx_den);
-  float *rx_usq = reinterpret_cast<float *>(smem + lay.rx_usq);
-  float *rx_usk = reinterpret_cast<float *>(smem + lay.rx_usk);
   float *s_f = reinterpret_cast<float *>(smem + lay.s_f);
   float *gs_f = reinterpret_cast<float *>(smem + lay.gs_f);
   float *dd = reinterpret_cast<float *>(smem + lay.dd);
@@ -164,7 +169,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int fbase = rank * MC;  // first feature of this CTA
   const int t0 = seg * p.tps, t1 = min(t0 + p.tps, p.nt);
   const int half = MC / 2;  // feature columns per thread (two threads per row)
-  const bool own = CS == 1 || (row >> 6) == rank;  // rows this CTA finalises
 
   // this CTA's rows of the W^T image (its features are contiguous rows of
   // it, with the same swizzle phase) and its features' segment-end state
@@ -177,9 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(rl_bar, 1);
     mbar_init(setup_bar, 1);
     mbar_init(x1_full, 1);
-    mbar_init(x2_full, 1);
     mbar_init(x1_free, 1);
-    mbar_init(x2_free, 1);
     *abort_flag = 0;
     fence_barrier_init();
     const size_t soff = ((size_t)bh * p.P + seg) * (size_t)M * DP + (size_t)fbase * DP;
@@ -247,14 +249,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_ones = sb + lay.ones, s_ddb = sb + lay.ddb, s_sb = sb + lay.sb;
   const uint32_t tile_bytes = kTile * D * 2;
   uint32_t in_phase = 0, mma_phase = 0, rl_phase = 0, x_phase = 0;
-  // exchange 1: num partials of all 128 rows (fp32 [128][64]) + den;
-  // exchange 2: dV, dQ, dK partials of the peer's 64 rows (fp32 [64][64]
-  // each) + two row sums
-  constexpr uint32_t kX1Bytes = 128 * 64 * 4 + 128 * 4, kX2Bytes = 3 * 64 * 64 * 4 + 2 * 64 * 4;
+  // the exchange: num partials of all 128 rows (fp32 [128][64]) + den
+  constexpr uint32_t kX1Bytes = 128 * 64 * 4 + 128 * 4;
   const uint32_t peer_x1_full = CS == 2 ? map_peer(smem_u32(x1_full), peer) : 0u;
-  const uint32_t peer_x2_full = CS == 2 ? map_peer(smem_u32(x2_full), peer) : 0u;
   const uint32_t peer_x1_free = CS == 2 ? map_peer(smem_u32(x1_free), peer) : 0u;
-  const uint32_t peer_x2_free = CS == 2 ? map_peer(smem_u32(x2_free), peer) : 0u;
 
   auto issue_in = [&](int t) {
     mbar_arrive_expect_tx(in_bar, 4 * tile_bytes);
@@ -285,10 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool live = row < valid;
     mbar_wait(in_bar, in_phase, p.status, abort_flag);
     in_phase ^= 1;
-    if (CS == 2 && tid == 0) {
-      mbar_arrive_expect_tx(x1_full, kX1Bytes);
-      mbar_arrive_expect_tx(x2_full, kX2Bytes);
-    }
+    if (CS == 2 && tid == 0) mbar_arrive_expect_tx(x1_full, kX1Bytes);
     if (tid == 0 && t > t0) {
       // the next tile's inputs head for L2 now; its TMA loads issue at the
       // end of this tile, when their buffers are free again
@@ -353,6 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // segment pre-pass added for this tile (increment -> T), and
     // A = phi_q phi_k^T -> X, one commit
     if (tid == 0) {
+      // last tile's dQ, dK partials (staged in the dN and R-copy tiles) have
+      // been read by their reduce-adds before this phase's epilogue reuses them
+      if (CS == 2) tma_store_wait_read();
       issue_state_delta(tb + kT, s_phk, s_v, s_ones, D);
       const uint32_t id = make_idesc(128, 128, false, false);
       for (int s = 0; s < MC / 16; ++s)
@@ -497,11 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float v[32];
       tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * ch), v);
       if (CS == 2) {
-        // park this CTA's dV partial (fp32 [128][64]) in the idle Q/K tiles
+        // this CTA's dV partial -> bf16 in the idle Q tile, for a reduce-add
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          st_shared_v4(s_q + xoff(row, 8 * ch + j, 128), __float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
-                       __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+        for (int j = 0; j < 4; ++j) st_bf16x8(s_q + sw128_offset(row, 32 * ch + 8 * j, kTile), v + 8 * j);
       } else if (live) {
         uint4 *dst = reinterpret_cast<uint4 *>(p.dv + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch);
 #pragma unroll
@@ -512,6 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_async_smem();
     cta_sync();
+    if (CS == 2 && tid == 0) {
+      tma_reduce_add_3d(&tmDV, s_q, 0, t * kTile, bh);
+      tma_store_commit();
+    }
 
     // (h) dphi_q, dphi_k, G update
     if (tid == 0) {
@@ -540,13 +540,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0 && t > t0) {
       mbar_arrive_expect_tx(in_bar, 4 * tile_bytes);
       tma_load_3d(smem + lay.dy, &tmDY, in_bar, 0, (t - 1) * kTile, bh);
-      if (CS == 1) tma_load_3d(smem + lay.v, &tmV, in_bar, 0, (t - 1) * kTile, bh);
+      tma_load_3d(smem + lay.v, &tmV, in_bar, 0, (t - 1) * kTile, bh);
     }
     if (CS == 2) {
-      // my V, dN, R and G copies and the dA tile are idle from here: the
-      // peer may send its exchange-2 partials; Q and K come back (into the
-      // dA tile) for the dQ, dK epilogue
-      if (tid == 32) mbar_arrive_remote(peer_x2_free);
+      // the dA tile is idle from here: Q and K come back into it for the
+      // dQ, dK epilogue (the Q tile holds the dV partial, K took num')
       if (tid == 0) {
         mbar_arrive_expect_tx(rl_bar, 2 * tile_bytes);
         tma_load_3d(smem + lay.at, &tmQ, rl_bar, 0, t * kTile, bh);
@@ -622,97 +620,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32x2(tmem_addr(tb, 32 * q4, kT + 32 * ch), tmem_addr(tb, 32 * q4, kT + 64 + 32 * ch), a, b);
       uint32_t s_xq = s_q, s_xk = s_k;
       if (CS == 2) {
-        // exchange 2: my partials of the peer's rows go to its idle V (dV),
-        // dN (dQ) and R-copy (dK) tiles, fp32 [64][64] each
-        float c3[32];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) ld_shared_v4f(s_q + xoff(row, 8 * ch + j, 128), c3 + 4 * j);
-        // the parked dV has been read: the next tile's Q and K take its place
-        cta_sync();
-        if (tid == 0 && t > t0) {
-          tma_load_3d(smem + lay.q, &tmQ, in_bar, 0, (t - 1) * kTile, bh);
-          tma_load_3d(smem + lay.k, &tmK, in_bar, 0, (t - 1) * kTile, bh);
-        }
-        if (!own) {
-          mbar_wait(x2_free, x_phase, p.status, abort_flag);
-          const uint32_t dv_dst = map_peer(s_v, peer), dq_dst = map_peer(s_dn, peer);
-          const uint32_t dk_dst = map_peer(s_rb, peer);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t o = xoff(row - 64 * peer, 8 * ch + j, 64);
-            st_async_v4(dv_dst + o, c3[4 * j], c3[4 * j + 1], c3[4 * j + 2], c3[4 * j + 3], peer_x2_full);
-            st_async_v4(dq_dst + o, a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3], peer_x2_full);
-            st_async_v4(dk_dst + o, b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3], peer_x2_full);
-          }
-          if (ch == 0) {
-            st_async_f32(map_peer(sb + lay.rx_usq + (row - 64 * peer) * 4, peer), sq, peer_x2_full);
-            st_async_f32(map_peer(sb + lay.rx_usk + (row - 64 * peer) * 4, peer), sk, peer_x2_full);
-          }
-        } else {
-          mbar_wait(x2_full, x_phase, p.status, abort_flag);
-        }
-        if (own) {
-          float r[32];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) ld_shared_v4f(s_v + xoff(row - 64 * rank, 8 * ch + j, 64), r + 4 * j);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) c3[i] += r[i];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) ld_shared_v4f(s_dn + xoff(row - 64 * rank, 8 * ch + j, 64), r + 4 * j);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) a[i] += r[i];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) ld_shared_v4f(s_rb + xoff(row - 64 * rank, 8 * ch + j, 64), r + 4 * j);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) b[i] += r[i];
-          sq += rx_usq[row - 64 * rank];
-          sk += rx_usk[row - 64 * rank];
-          if (live) {
-            uint4 *dst = reinterpret_cast<uint4 *>(p.dv + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              dst[j] = make_uint4(pack_bf16(c3[8 * j], c3[8 * j + 1]), pack_bf16(c3[8 * j + 2], c3[8 * j + 3]),
-                                  pack_bf16(c3[8 * j + 4], c3[8 * j + 5]), pack_bf16(c3[8 * j + 6], c3[8 * j + 7]));
-          }
-        }
         mbar_wait(rl_bar, rl_phase, p.status, abort_flag);
         rl_phase ^= 1;
         s_xq = sb + lay.at;
         s_xk = sb + lay.at + tile_bytes;
       }
-      if (live && own) {
+      // dQ = u_q W^T - q rowsum(u_q), dK likewise (this CTA's features)
+      float oq[32], ok[32];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float xq[8], xk[8];
+        ld_bf16x8(s_xq + sw128_offset(row, 32 * ch + 8 * j, kTile), xq);
+        ld_bf16x8(s_xk + sw128_offset(row, 32 * ch + 8 * j, kTile), xk);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          oq[8 * j + i] = a[8 * j + i] - xq[i] * sq;
+          ok[8 * j + i] = b[8 * j + i] - xk[i] * sk;
+        }
+      }
+      if (CS == 2) {
+        // partials -> bf16 in the idle dN and R-copy tiles for reduce-adds
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          st_bf16x8(s_dn + sw128_offset(row, 32 * ch + 8 * j, kTile), oq + 8 * j);
+          st_bf16x8(s_rb + sw128_offset(row, 32 * ch + 8 * j, kTile), ok + 8 * j);
+        }
+        fence_async_smem();
+        cta_sync();
+        if (tid == 0) {
+          tma_reduce_add_3d(&tmDQ, s_dn, 0, t * kTile, bh);
+          tma_reduce_add_3d(&tmDK, s_rb, 0, t * kTile, bh);
+          tma_store_commit();
+          if (t > t0) {
+            // the dV partial has left the Q tile: the next tile's Q, K go in
+            tma_store_wait_read_1();
+            tma_load_3d(smem + lay.q, &tmQ, in_bar, 0, (t - 1) * kTile, bh);
+            tma_load_3d(smem + lay.k, &tmK, in_bar, 0, (t - 1) * kTile, bh);
+          }
+        }
+      } else if (live) {
         uint4 *gq = reinterpret_cast<uint4 *>(p.dq + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch);
         uint4 *gk = reinterpret_cast<uint4 *>(p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          float xq[8], xk[8];
-          ld_bf16x8(s_xq + sw128_offset(row, 32 * ch + 8 * j, kTile), xq);
-          ld_bf16x8(s_xk + sw128_offset(row, 32 * ch + 8 * j, kTile), xk);
-          float oq[8], ok[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            oq[i] = a[8 * j + i] - xq[i] * sq;
-            ok[i] = b[8 * j + i] - xk[i] * sk;
-          }
-          gq[j] = make_uint4(pack_bf16(oq[0], oq[1]), pack_bf16(oq[2], oq[3]), pack_bf16(oq[4], oq[5]),
-                             pack_bf16(oq[6], oq[7]));
-          gk[j] = make_uint4(pack_bf16(ok[0], ok[1]), pack_bf16(ok[2], ok[3]), pack_bf16(ok[4], ok[5]),
-                             pack_bf16(ok[6], ok[7]));
+          gq[j] = make_uint4(pack_bf16(oq[8 * j], oq[8 * j + 1]), pack_bf16(oq[8 * j + 2], oq[8 * j + 3]),
+                             pack_bf16(oq[8 * j + 4], oq[8 * j + 5]), pack_bf16(oq[8 * j + 6], oq[8 * j + 7]));
+          gk[j] = make_uint4(pack_bf16(ok[8 * j], ok[8 * j + 1]), pack_bf16(ok[8 * j + 2], ok[8 * j + 3]),
+                             pack_bf16(ok[8 * j + 4], ok[8 * j + 5]), pack_bf16(ok[8 * j + 6], ok[8 * j + 7]));
         }
       }
       cta_sync();
     }
     x_phase ^= 1;
-    if (tid == 0 && t > t0) {
-      if (CS == 1) {
-        tma_load_3d(smem + lay.q, &tmQ, in_bar, 0, (t - 1) * kTile, bh);
-        tma_load_3d(smem + lay.k, &tmK, in_bar, 0, (t - 1) * kTile, bh);
-      } else {
-        tma_load_3d(smem + lay.v, &tmV, in_bar, 0, (t - 1) * kTile, bh);
-      }
+    if (CS == 1 && tid == 0 && t > t0) {
+      tma_load_3d(smem + lay.q, &tmQ, in_bar, 0, (t - 1) * kTile, bh);
+      tma_load_3d(smem + lay.k, &tmK, in_bar, 0, (t - 1) * kTile, bh);
     }
   }
 
+  if (CS == 2 && tid == 0) tma_store_wait_all();  // the last tile's reduce-adds
   // segment total of G -> gstates, staged in the idle phi / A tiles for one
   // coalesced bulk store of this CTA's rows
   {
@@ -746,7 +712,15 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
   if (!make_map_bf16_3d(&mq, a.q, pl.BH, pl.L, D, kTile) || !make_map_bf16_3d(&mk, a.k, pl.BH, pl.L, D, kTile) ||
       !make_map_bf16_3d(&mv, a.v, pl.BH, pl.L, D, kTile) || !make_map_bf16_3d(&mdy, a.dy, pl.BH, pl.L, D, kTile))
     return cudaErrorInvalidValue;
-  cudaError_t e = tc_segment_states(pl, a, pl.P, st);  // R' totals of every segment, scanned
+  CUtensorMap mdq, mdk, mdv;
+  if (CS == 2 && (!make_map_bf16_3d(&mdq, a.dq, pl.BH, pl.L, D, kTile) ||
+                  !make_map_bf16_3d(&mdk, a.dk, pl.BH, pl.L, D, kTile) ||
+                  !make_map_bf16_3d(&mdv, a.dv, pl.BH, pl.L, D, kTile)))
+    return cudaErrorInvalidValue;
+  if (CS == 1) mdq = mdk = mdv = mq;  // unused
+  // R' totals of every segment, scanned; with two CTAs per segment the
+  // outputs start at zero for the per-CTA reduce-adds
+  cudaError_t e = tc_segment_states(pl, a, pl.P, CS == 2, st);
   if (e != cudaSuccess) return e;
   Params p{};
   p.L = pl.L; p.M = pl.M; p.nt = pl.tc_tiles; p.P = pl.P; p.tps = pl.cps; p.favor = FAVOR;
@@ -783,7 +757,7 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     ProfScope ps("tc_backward", st);
-    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mdy, p);
+    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mdy, mdq, mdk, mdv, p);
     if (e != cudaSuccess) return e;
   }
   if (pl.P > 1) {

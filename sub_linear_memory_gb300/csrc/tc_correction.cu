@@ -93,14 +93,6 @@ struct Layout {
 // TMEM columns
 constexpr uint32_t kF0 = 0, kF1 = 128, kDc = 256, kDV = 384, kDK = 448;
 
-// dst tile += the staged bf16 tile at shared address src (TMA reduce-add)
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2) {
-  asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(src), "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-
 template <bool FAVOR, int M>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_corr_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,

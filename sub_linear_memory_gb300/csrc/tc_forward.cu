@@ -32,11 +32,14 @@
 //
 // MODE_STATE runs only the K side and writes the segment's total R' (the
 // rows eq. (3) adds) for the segment scan.  Each tile's increment is an MMA
-// that restarts at zero -- the same sequence the backward issues to remove
-// it again -- and the epilogue adds it into an fp32 master with CUDA-core
-// (round-to-nearest) adds.  Accumulating many tiles in place on the tensor
-// pipe loses low bits of the small addends; the backward recovers the first
-// tiles' small states by subtraction from this total and would expose that.
+// that restarts at zero, and the epilogue adds it into an fp32 master in
+// TMEM, as a double-float (low part in shared memory) for the normaliser
+// column S.  The backward recovers the first tiles' small states by
+// subtracting increments from this total, so rounding in the total shows
+// up there: accumulating in place on the tensor pipe cost dQ of the first
+// tiles of a long segment a factor of two hundred, and plain fp32 still a
+// factor of 2.6 through S, whose positive terms make its rounding errors
+// add up; the signed R columns' errors do not.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -57,6 +60,7 @@ enum { MODE_STATE = 0, MODE_FWD = 1 };
 
 struct Params {
   int L, M, nt, P, tps;
+  int zero_grads;  // state pass of a two-CTA backward: zero dQ, dK, dV tile by tile
   __nv_bfloat16 *y;
   const __nv_bfloat16 *wimg;  // W^T shared-memory image (FAVOR+)
   float *states;     // fp32 [BH][P][M][D + 1]: high parts of the segment states
@@ -98,7 +102,7 @@ template <int D, bool FAVOR, int MODE>
 struct Layout {
   using C = Cfg<D, FAVOR, MODE>;
   // shared memory (bytes from a 1024-aligned base)
-  uint32_t w, slots, phk, phq, rb, ones, ss, denp, bars, total;
+  uint32_t w, slots, phk, phq, rb, ones, ss, zero, lo, denp, bars, total;
   // TMEM columns
   uint32_t t_buf0, t_buf1, t_num, t_r, t_m;
   __host__ __device__ explicit Layout(int M) {
@@ -112,6 +116,9 @@ struct Layout {
     // slot (d = 64), else a [128][16] no-swizzle operand
     ones = o; o += D == 64 ? 16384u : 4096u;
     ss = o; o += MODE == MODE_FWD ? (uint32_t)M * 4u : 0u;        // fp32 S(t-1)
+    // a zero tile (state pass of the two-CTA backward, d = 64 only)
+    zero = o; o += (MODE == MODE_STATE && D == 64) ? C::kTileBytes : 0u;
+    lo = o; o += MODE == MODE_STATE ? (uint32_t)M * (D + 1) * 4u : 0u;  // low parts [M][D + 1] (state pass)
     denp = o; o += MODE == MODE_FWD ? 2u * 2u * kTile * 4u : 0u;  // [tile parity][half][row]
     bars = o; o += 8 * B_COUNT + 16;
     total = o;
@@ -127,7 +134,8 @@ struct Layout {
 template <int D, bool FAVOR, int MODE, int M>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, Params p) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDQ,
+                  const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV, Params p) {
   using C = Cfg<D, FAVOR, MODE>;
   constexpr int NC = C::kCols;
   constexpr int nb = (M + 127) / 128, FB = M < 128 ? M : 128, DP = D + 1;
@@ -184,6 +192,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // constant operands: the ones block, zero padding of phi_k beyond M (the
   // state MMA always reads 128 features)
+  if (MODE == MODE_STATE) {
+    if (D == 64)
+      for (int idx = tid; idx < (int)(C::kTileBytes / 16); idx += kThreads)
+        reinterpret_cast<uint4 *>(smem + lay.zero)[idx] = make_uint4(0u, 0u, 0u, 0u);
+    for (int idx = tid; idx < M * (D + 1); idx += kThreads) reinterpret_cast<float *>(smem + lay.lo)[idx] = 0.f;
+  }
   for (int idx = tid; idx < kTile * (D == 64 ? 64 : 16); idx += kThreads) {
     const int r = D == 64 ? idx >> 6 : idx >> 4, x = D == 64 ? idx & 63 : idx & 15;
     *reinterpret_cast<__nv_bfloat16 *>(smem + lay.ones + (D == 64 ? sw128_offset(r, x, kTile) : n16_offset(r, x))) =
@@ -276,7 +290,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = load(&tmK, t);
         if (ok && MODE == MODE_FWD) ok = load(&tmQ, t);
         if (ok) ok = load(&tmV, t);
+        if (MODE == MODE_STATE && D == 64 && p.zero_grads) {
+          // the two-CTA backward adds its per-CTA partials of dQ, dK, dV
+          for (int c = 0; c < D; c += 64) {
+            tma_store_3d(&tmDQ, smem + lay.zero + c * kTile * 2, c, t * kTile, bh);
+            tma_store_3d(&tmDK, smem + lay.zero + c * kTile * 2, c, t * kTile, bh);
+            tma_store_3d(&tmDV, smem + lay.zero + c * kTile * 2, c, t * kTile, bh);
+          }
+          tma_store_commit();
+        }
       }
+      if (MODE == MODE_STATE && D == 64 && p.zero_grads) tma_store_wait_all();
       // copies still in flight land before the CTA can leave
       for (int m = max(0, n - C::kSlots); m < n; ++m) mbar_drain(bar + B_FULL + m % C::kSlots, slot_par(m));
       if (FAVOR || (MODE == MODE_FWD && seg > 0)) mbar_drain(bar + B_SETUP, 0);
@@ -525,18 +549,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (MODE == MODE_STATE) {
         arrive(B_EMPTY + nV % C::kSlots);
         if (i % C::kGroup == C::kGroup - 1 || i == ntl - 1) {
-          // master += group partial (round-to-nearest fp32 adds)
+          // master += this tile's increment (fp32; double-float for S)
           if (!wait(B_AFULL, (i / C::kGroup) & 1)) break;
           tc_fence_after();
+          float *lo = reinterpret_cast<float *>(smem + lay.lo);
           for (int b = 0; b < nb; ++b) {
             int c_lo, c_hi;
             r_cols(b, c_lo, c_hi);
+            const int f = 128 * b + row;
             for (int c = c_lo; c < c_hi; c += 16) {
               float x[16], m[16];
               tmem_ld16(tmem_addr(tbase, lane_base, lay.t_r + b * NC + c), x);
               tmem_ld16(tmem_addr(tbase, lane_base, lay.t_m + b * NC + c), m);
+              const bool has_s = c <= D && D < c + 16;
+              const float ms = has_s ? m[D - c] : 0.f, xs = has_s ? x[D - c] : 0.f;
 #pragma unroll
               for (int e = 0; e < 16; ++e) m[e] += x[e];
+              if (has_s && f < M) {
+                float h = ms, l = lo[f * (D + 1) + D];
+                df_add(h, l, xs);
+                lo[f * (D + 1) + D] = l;
+                m[D - c] = h;
+              }
               tmem_st16(tmem_addr(tbase, lane_base, lay.t_m + b * NC + c), m);
             }
           }
@@ -646,8 +680,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (MODE == MODE_STATE && tid == 0 && !*abort_flag) {
-    // high parts only: the scan takes the low parts of these totals as zero
-    bulk_store(p.states + ((size_t)bh * p.P + seg) * (size_t)M * DP, sbase + lay.slots, (uint32_t)(M * DP * 4));
+    const size_t off = ((size_t)bh * p.P + seg) * (size_t)M * DP;
+    bulk_store(p.states + off, sbase + lay.slots, (uint32_t)(M * DP * 4));
+    bulk_store(p.states_lo + off, sbase + lay.lo, (uint32_t)(M * DP * 4));
     tma_store_commit();
     tma_store_wait_read();
   }
@@ -656,9 +691,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool FAVOR, int MODE, int M>
 cudaError_t launch_m(const Plan &pl, const Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
-                     const CUtensorMap &mv, int nseg, cudaStream_t st) {
+                     const CUtensorMap &mv, const CUtensorMap *mz, int nseg, cudaStream_t st) {
   Params p{};
   p.L = pl.L; p.M = pl.M; p.nt = pl.tc_tiles; p.P = pl.P; p.tps = pl.cps;
+  p.zero_grads = mz != nullptr;
   p.y = static_cast<__nv_bfloat16 *>(a.y);
   p.wimg = reinterpret_cast<const __nv_bfloat16 *>(a.ws + pl.wimg_off);
   p.states = a.ws + pl.states_off;
@@ -669,7 +705,7 @@ cudaError_t launch_m(const Plan &pl, const Args &a, const CUtensorMap &mq, const
   auto kern = tc_fwd_kernel<D, FAVOR, MODE, M>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(nseg, pl.BH), kThreads, smem, st>>>(mq, mk, mv, p);
+  kern<<<dim3(nseg, pl.BH), kThreads, smem, st>>>(mq, mk, mv, mz ? mz[0] : mk, mz ? mz[1] : mk, mz ? mz[2] : mk, p);
   return cudaGetLastError();
 }
 
@@ -677,13 +713,13 @@ cudaError_t launch_m(const Plan &pl, const Args &a, const CUtensorMap &mq, const
 // features, elu+1 with M = d.
 template <int D, bool FAVOR, int MODE>
 cudaError_t launch(const Plan &pl, const Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
-                   const CUtensorMap &mv, int nseg, cudaStream_t st) {
+                   const CUtensorMap &mv, const CUtensorMap *mz, int nseg, cudaStream_t st) {
   if constexpr (!FAVOR) {
-    return pl.M == D ? launch_m<D, FAVOR, MODE, D>(pl, a, mq, mk, mv, nseg, st) : cudaErrorInvalidValue;
+    return pl.M == D ? launch_m<D, FAVOR, MODE, D>(pl, a, mq, mk, mv, mz, nseg, st) : cudaErrorInvalidValue;
   } else {
-    if (pl.M == 64) return launch_m<D, FAVOR, MODE, 64>(pl, a, mq, mk, mv, nseg, st);
-    if (pl.M == 128) return launch_m<D, FAVOR, MODE, 128>(pl, a, mq, mk, mv, nseg, st);
-    if (pl.M == 256) return launch_m<D, FAVOR, MODE, 256>(pl, a, mq, mk, mv, nseg, st);
+    if (pl.M == 64) return launch_m<D, FAVOR, MODE, 64>(pl, a, mq, mk, mv, mz, nseg, st);
+    if (pl.M == 128) return launch_m<D, FAVOR, MODE, 128>(pl, a, mq, mk, mv, mz, nseg, st);
+    if (pl.M == 256) return launch_m<D, FAVOR, MODE, 256>(pl, a, mq, mk, mv, mz, nseg, st);
     return cudaErrorInvalidValue;
   }
 }
@@ -709,17 +745,17 @@ cudaError_t prep_w(const Plan &pl, const Args &a, cudaStream_t st) {
 // states[s] = R' at the end of segment s.
 template <int D, bool FAVOR>
 cudaError_t segment_states(const Plan &pl, const Args &a, const CUtensorMap &mq,
-                           const CUtensorMap &mk, const CUtensorMap &mv, int nseg, cudaStream_t st) {
+                           const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap *mz, int nseg,
+                           cudaStream_t st) {
   cudaError_t e;
   {
     ProfScope ps("tc_segment_state", st);
-    e = launch<D, FAVOR, MODE_STATE>(pl, a, mq, mk, mv, nseg, st);
+    e = launch<D, FAVOR, MODE_STATE>(pl, a, mq, mk, mv, mz, nseg, st);
     if (e != cudaSuccess) return e;
   }
-  {
-    // also for one segment: it writes the low parts the state pass leaves out
+  if (nseg > 1) {
     ProfScope ps("scan_states", st);
-    e = scan_states_df(pl, a.ws + pl.states_off, a.ws + pl.states_lo_off, nseg, 0, st);
+    e = scan_states_df(pl, a.ws + pl.states_off, a.ws + pl.states_lo_off, nseg, 1, st);
   }
   return e;
 }
@@ -732,11 +768,11 @@ cudaError_t forward_family(const Plan &pl, const Args &a, cudaStream_t st) {
     return cudaErrorInvalidValue;
   cudaError_t e;
   if (pl.P > 1) {
-    e = segment_states<D, FAVOR>(pl, a, mq, mk, mv, pl.P - 1, st);
+    e = segment_states<D, FAVOR>(pl, a, mq, mk, mv, nullptr, pl.P - 1, st);
     if (e != cudaSuccess) return e;
   }
   ProfScope ps("tc_forward", st);
-  return launch<D, FAVOR, MODE_FWD>(pl, a, mq, mk, mv, pl.P, st);
+  return launch<D, FAVOR, MODE_FWD>(pl, a, mq, mk, mv, nullptr, pl.P, st);
 }
 
 }  // namespace tcf
@@ -754,16 +790,22 @@ bool tc_forward_supported(int d, int M, int chunk, bool favor) {
   return false;
 }
 
-cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, cudaStream_t st) {
-  CUtensorMap mk, mv;
+cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, bool zero_grads, cudaStream_t st) {
+  CUtensorMap mk, mv, mz[3];
   const int d = p.d;
   cudaError_t e = tcf::prep_w(p, a, st);
   if (e != cudaSuccess) return e;
   if (!make_map_bf16_3d(&mk, a.k, p.BH, p.L, d, tcf::kTile) || !make_map_bf16_3d(&mv, a.v, p.BH, p.L, d, tcf::kTile))
     return cudaErrorInvalidValue;
-  if (d == 64 && p.favor) return tcf::segment_states<64, true>(p, a, mk, mk, mv, nseg, st);
-  if (d == 64) return tcf::segment_states<64, false>(p, a, mk, mk, mv, nseg, st);
-  if (d == 128 && !p.favor) return tcf::segment_states<128, false>(p, a, mk, mk, mv, nseg, st);
+  if (zero_grads &&
+      (!make_map_bf16_3d(&mz[0], a.dq, p.BH, p.L, d, tcf::kTile) ||
+       !make_map_bf16_3d(&mz[1], a.dk, p.BH, p.L, d, tcf::kTile) ||
+       !make_map_bf16_3d(&mz[2], a.dv, p.BH, p.L, d, tcf::kTile)))
+    return cudaErrorInvalidValue;
+  const CUtensorMap *z = zero_grads ? mz : nullptr;
+  if (d == 64 && p.favor) return tcf::segment_states<64, true>(p, a, mk, mk, mv, z, nseg, st);
+  if (d == 64) return tcf::segment_states<64, false>(p, a, mk, mk, mv, z, nseg, st);
+  if (d == 128 && !p.favor) return tcf::segment_states<128, false>(p, a, mk, mk, mv, z, nseg, st);
   return cudaErrorInvalidValue;
 }
 
