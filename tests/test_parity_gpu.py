@@ -220,9 +220,12 @@ def test_tensor_core_backward_long_reversal(_lib):
     ref = oracle.recurrence_backward(_np(q), _np(k), _np(v), _wnp(w), _np(dy), want_dw=False)
     for name, got, exp in (("dQ", dq, ref[0]), ("dK", dk, ref[1]), ("dV", dv, ref[2])):
         check(name, _np(got), exp, TOL[torch.bfloat16])
-    # the first tile, where the recovered state is smallest relative to the total
+    # the first tile, where the recovered state is smallest relative to the
+    # total: exact reversal keeps it at the level of bf16 rounding (about
+    # 6e-3 here), well inside the contract bar; rounding in the segment total
+    # would show up first in this tile
     for name, got, exp in (("dQ[:128]", dq, ref[0]), ("dK[:128]", dk, ref[1])):
-        check(name, _np(got)[..., :128, :], exp[..., :128, :], TOL[torch.bfloat16])
+        check(name, _np(got)[..., :128, :], exp[..., :128, :], 1e-2)
 
 
 @pytest.mark.parametrize("segments", [1, 2, 3, 5])
