@@ -533,12 +533,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_bf16(tb + kG + D, desc_mnmajor(s_phq, kTile, 0, s), desc_n16(s_ddb, s), id_g1, 1);
       }
       mma_done();
+      if (CS == 2 && t > t0) {
+        // the Q tile's dV partial has been read by its reduce-add and the K
+        // tile's num' partial by the exchange epilogue: the next tile's Q and
+        // K stream in while this one finishes
+        tma_store_wait_read();
+        mbar_arrive_expect_tx(in_bar, 4 * tile_bytes);
+        tma_load_3d(smem + lay.q, &tmQ, in_bar, 0, (t - 1) * kTile, bh);
+        tma_load_3d(smem + lay.k, &tmK, in_bar, 0, (t - 1) * kTile, bh);
+      }
     }
     wait_mma();
     // the next tile's inputs stream in as their tiles fall idle: dY (and V
     // with one CTA per segment) from here, Q and K / V later in this tile
     if (tid == 0 && t > t0) {
-      mbar_arrive_expect_tx(in_bar, 4 * tile_bytes);
+      if (CS == 1) mbar_arrive_expect_tx(in_bar, 4 * tile_bytes);
       tma_load_3d(smem + lay.dy, &tmDY, in_bar, 0, (t - 1) * kTile, bh);
       tma_load_3d(smem + lay.v, &tmV, in_bar, 0, (t - 1) * kTile, bh);
     }
@@ -651,12 +660,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_reduce_add_3d(&tmDQ, s_dn, 0, t * kTile, bh);
           tma_reduce_add_3d(&tmDK, s_rb, 0, t * kTile, bh);
           tma_store_commit();
-          if (t > t0) {
-            // the dV partial has left the Q tile: the next tile's Q, K go in
-            tma_store_wait_read_1();
-            tma_load_3d(smem + lay.q, &tmQ, in_bar, 0, (t - 1) * kTile, bh);
-            tma_load_3d(smem + lay.k, &tmK, in_bar, 0, (t - 1) * kTile, bh);
-          }
         }
       } else if (live) {
         uint4 *gq = reinterpret_cast<uint4 *>(p.dq + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch);
