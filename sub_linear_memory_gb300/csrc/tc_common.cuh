@@ -117,6 +117,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test for the completion of phase `parity` of `bar`.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Arrive on `bar` with `count` arrivals at once.
+__device__ __forceinline__ void mbar_arrive_n(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -268,6 +286,19 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// D (+)= A B with A (M = 128 rows, one per TMEM lane) in TMEM: 32-bit column
+// c of a row holds the bf16 pair (k = 2c, 2c + 1), low half first, so K step
+// s (16 elements) starts 8 columns on; B from shared memory.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 op issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile(
@@ -307,6 +338,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// One fp32 TMEM column of this thread's lane.
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  return __uint_as_float(r);
 }
 
 // TMEM address of (lane, column) for a base returned by tmem_alloc.
@@ -389,14 +428,17 @@ namespace tc {
 
 // |x_row|^2 from a swizzled bf16 [128][D] tile.
 __device__ __forceinline__ float tile_row_sqnorm(uint32_t tile_base, int row, int D) {
-  float s = 0.f;
+  // eight independent partial sums: one chain of d dependent FMAs would
+  // cost d FMA latencies per row
+  float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
   for (int c = 0; c < D / 8; ++c) {
     float v[8];
     ld_bf16x8(tile_base + sw128_offset(row, c * 8, 128), v);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) s = fmaf(v[i], v[i], s);
+    for (int i = 0; i < 8; ++i) s[i] = fmaf(v[i], v[i], s[i]);
   }
-  return s;
+  return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
 }
 
 constexpr float kLog2eF = 1.4426950408889634f;
