@@ -55,23 +55,6 @@ namespace tcf {
 using namespace slim::tc;
 
 constexpr int kTile = 128;
-constexpr int kEpiWarps = 8;
-constexpr int kParts = kEpiWarps / 4;  // epilogue threads per row
-constexpr int kThreads = 32 * (2 + kEpiWarps);
-
-// n consecutive fp32 TMEM columns of this thread's lane (n = 16, 32 or 64)
-template <int N>
-__device__ __forceinline__ void tmem_ldn(uint32_t a, float *v) {
-  if constexpr (N == 16) {
-    tmem_ld16(a, v);
-  } else if constexpr (N == 32) {
-    tmem_ld32(a, v);
-  } else {
-    static_assert(N == 64, "16, 32 or 64 columns");
-    tmem_ld32x2(a, a + 32, v, v + 32);
-  }
-}
-
 enum { MODE_STATE = 0, MODE_FWD = 1 };
 
 struct Params {
@@ -83,693 +66,6 @@ struct Params {
   float *states_lo;  // same layout: low parts
   int *status;
 };
-
-template <int D, bool FAVOR, int MODE>
-struct Cfg {
-  static constexpr int kSlots = D == 128 ? 3 : 4;         // ring of [128][D] bf16 tiles
-  static constexpr int kLoads = MODE == MODE_FWD ? 3 : 2;  // per tile: K, (Q), V
-  static constexpr int kNbuf = FAVOR && MODE == MODE_FWD ? 2 : 1;  // TMEM buffers for F and A
-  static constexpr uint32_t kTileBytes = kTile * D * 2;
-  static constexpr int kCols = D + 16;                     // TMEM columns of num' or one R' block
-};
-
-// mbarrier indices
-enum {
-  B_FULL = 0,       // [slots] TMA -> consumers
-  B_EMPTY = 4,      // [slots] consumers -> TMA (1 MMA arrival + 8 epilogue warps)
-  B_FFULL = 8,      // [2] F or A ready in TMEM buffer
-  B_FEMPTY = 10,    // [2] TMEM buffer read out by the epilogue
-  B_PHK = 12,       // phi_k block stored
-  B_PHQ = 13,       // phi_q block stored
-  B_PHFREE = 14,    // MMAs reading the previous feature block done
-  B_AFULL = 15,     // A and the tile's state update complete (state pass: group partial ready)
-  B_ATFULL = 16,    // masked A stored
-  B_NUMFULL = 17,   // num' complete
-  B_NUMEMPTY = 18,  // num' read out
-  B_RBFULL = 19,    // R(t) read out of TMEM, bf16 copies refreshed (state pass: partial free)
-  B_DONE = 20,      // MMA drain
-  B_SETUP = 21,     // set-up copies (W image, incoming state)
-  B_EPI = 22,       // epilogue warps' S and den partials written
-  B_COUNT = 23
-};
-
-template <int D, bool FAVOR, int MODE>
-struct Layout {
-  using C = Cfg<D, FAVOR, MODE>;
-  // shared memory (bytes from a 1024-aligned base)
-  uint32_t w, slots, phk, phq, rb, ones, ss, zero, lo, denp, bars, total;
-  // TMEM columns
-  uint32_t t_buf0, t_buf1, t_num, t_r, t_m;
-  __host__ __device__ explicit Layout(int M) {
-    uint32_t o = 0;
-    w = o; o += FAVOR ? (uint32_t)M * 128u : 0u;  // W^T as [M][64] bf16 (D == 64)
-    slots = o; o += C::kSlots * C::kTileBytes;
-    phk = o; o += kTile * 128 * 2;                 // one feature block of phi_k
-    phq = o; o += MODE == MODE_FWD ? kTile * 128 * 2 : 0u;  // phi_q block, then masked A
-    rb = o; o += MODE == MODE_FWD ? (uint32_t)M * D * 2 : 0u;
-    // column 0 = 1: a [128][64] 128-B-swizzled block placed after every V
-    // slot (d = 64), else a [128][16] no-swizzle operand
-    ones = o; o += D == 64 ? 16384u : 4096u;
-    ss = o; o += MODE == MODE_FWD ? (uint32_t)M * 4u : 0u;        // fp32 S(t-1)
-    // a zero tile (state pass of the two-CTA backward, d = 64 only)
-    zero = o; o += (MODE == MODE_STATE && D == 64) ? C::kTileBytes : 0u;
-    lo = o; o += MODE == MODE_STATE ? (uint32_t)M * (D + 1) * 4u : 0u;  // low parts [M][D + 1] (state pass)
-    denp = o; o += MODE == MODE_FWD ? 2u * kParts * kTile * 4u : 0u;  // [tile parity][part][row]
-    bars = o; o += 8 * B_COUNT + 16;
-    total = o;
-    t_buf0 = 0;
-    t_buf1 = C::kNbuf > 1 ? 128u : 0u;
-    const uint32_t used = (FAVOR || MODE == MODE_FWD) ? 128u * C::kNbuf : 0u;
-    t_num = used;
-    t_r = MODE == MODE_FWD ? t_num + C::kCols : used;  // R' (state pass: group partial)
-    t_m = t_r + (M > 128 ? 2u : 1u) * C::kCols;        // state pass: fp32 master total
-  }
-};
-
-template <int D, bool FAVOR, int MODE, int M>
-__global__ void __launch_bounds__(kThreads, 1)
-    tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDQ,
-                  const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV, Params p) {
-  using C = Cfg<D, FAVOR, MODE>;
-  constexpr int NC = C::kCols;
-  constexpr int nb = (M + 127) / 128, FB = M < 128 ? M : 128, DP = D + 1;
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char *smem =
-      reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const Layout<D, FAVOR, MODE> lay(M);
-  const uint32_t sbase = smem_u32(smem);
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + lay.bars);
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + B_COUNT);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar + B_COUNT) + 1;
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int seg = blockIdx.x, bh = blockIdx.y;
-  const int t0 = seg * p.tps, t1 = min(t0 + p.tps, p.nt), ntl = max(t1 - t0, 0);
-
-  if (tid == 0) {
-    for (int s = 0; s < C::kSlots; ++s) {
-      mbar_init(bar + B_FULL + s, 1);
-      mbar_init(bar + B_EMPTY + s, 1 + kEpiWarps);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar + B_FFULL + b, 1);
-      mbar_init(bar + B_FEMPTY + b, kEpiWarps);
-    }
-    mbar_init(bar + B_PHK, kEpiWarps);
-    mbar_init(bar + B_PHQ, kEpiWarps);
-    mbar_init(bar + B_PHFREE, 1);
-    mbar_init(bar + B_AFULL, 1);
-    mbar_init(bar + B_ATFULL, kEpiWarps);
-    mbar_init(bar + B_NUMFULL, 1);
-    mbar_init(bar + B_NUMEMPTY, kEpiWarps);
-    mbar_init(bar + B_RBFULL, kEpiWarps);
-    mbar_init(bar + B_DONE, 1);
-    mbar_init(bar + B_SETUP, 1);
-    mbar_init(bar + B_EPI, kEpiWarps);
-    *abort_flag = 0;
-    fence_barrier_init();
-    // W^T image and the incoming state (high parts: the forward's master is
-    // fp32, below which the low parts do not register) by bulk copy
-    const uint32_t wbytes = FAVOR ? (uint32_t)M * 128u : 0u;
-    const uint32_t sbytes = (MODE == MODE_FWD && seg > 0) ? (uint32_t)(M * DP * 4) : 0u;
-    if (wbytes + sbytes > 0) {
-      mbar_arrive_expect_tx(bar + B_SETUP, wbytes + sbytes);
-      if (wbytes) bulk_load(smem + lay.w, p.wimg, wbytes, bar + B_SETUP);
-      if (sbytes)
-        bulk_load(smem + lay.slots, p.states + ((size_t)bh * p.P + seg - 1) * (size_t)M * DP, sbytes, bar + B_SETUP);
-    }
-    prefetch_tmap(&tmK);
-    prefetch_tmap(&tmV);
-    if (MODE == MODE_FWD) prefetch_tmap(&tmQ);
-  }
-  if (warp == 0) tmem_alloc(tslot, 512);
-
-  // constant operands: the ones block, zero padding of phi_k beyond M (the
-  // state MMA always reads 128 features)
-  if (MODE == MODE_STATE) {
-    if (D == 64)
-      for (int idx = tid; idx < (int)(C::kTileBytes / 16); idx += kThreads)
-        reinterpret_cast<uint4 *>(smem + lay.zero)[idx] = make_uint4(0u, 0u, 0u, 0u);
-    for (int idx = tid; idx < M * (D + 1); idx += kThreads) reinterpret_cast<float *>(smem + lay.lo)[idx] = 0.f;
-  }
-  for (int idx = tid; idx < kTile * (D == 64 ? 64 : 16); idx += kThreads) {
-    const int r = D == 64 ? idx >> 6 : idx >> 4, x = D == 64 ? idx & 63 : idx & 15;
-    *reinterpret_cast<__nv_bfloat16 *>(smem + lay.ones + (D == 64 ? sw128_offset(r, x, kTile) : n16_offset(r, x))) =
-        __float2bfloat16_rn(x == 0 ? 1.f : 0.f);
-  }
-  if (M < 128) {
-    for (int idx = tid; idx < kTile * 128; idx += kThreads) {
-      const int r = idx >> 7, x = idx & 127;
-      if (x >= M)
-        *reinterpret_cast<__nv_bfloat16 *>(smem + lay.phk + sw128_offset(r, x, kTile)) = __float2bfloat16_rn(0.f);
-    }
-  }
-  fence_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = *tslot;
-
-  // incoming state of the segment -> TMEM master (and, in the forward, its
-  // bf16 copies); the state pass starts its master at zero.  The fp32
-  // [M][D + 1] state arrived in the (still unused) load slots.
-  {
-    const bool in = MODE == MODE_FWD && seg > 0;
-    if ((FAVOR || in) && !mbar_wait(bar + B_SETUP, 0, p.status, abort_flag)) {
-      // nothing usable arrived: the tiles below are skipped by the abort flag
-    }
-    const float *stage = reinterpret_cast<const float *>(smem + lay.slots);  // [M][D + 1] fp32
-    const int q4 = warp & 3, part = (warp - 2) >> 2, row = 32 * q4 + lane;
-    const uint32_t t_dst = MODE == MODE_FWD ? lay.t_r : lay.t_m;
-    if (warp >= 2) {
-      // 16-column chunks of the nb state blocks, dealt out over the parts
-      constexpr int NCH = NC / 16;
-      for (int k = part; k < nb * NCH; k += kParts) {
-        const int b = k / NCH, c = (k - b * NCH) * 16, f = 128 * b + row;
-        float v[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = (in && f < M && c + i <= D) ? stage[f * DP + c + i] : 0.f;
-        tmem_st16(tmem_addr(tbase, 32u * q4, t_dst + b * NC + c), v);
-        if (MODE == MODE_FWD && f < M) {
-#pragma unroll
-          for (int i = 0; i < 16; i += 8)
-            if (c + i + 8 <= D) st_bf16x8(sbase + lay.rb + sw128_offset(f, c + i, M), v + i);
-          if (c == D) reinterpret_cast<float *>(smem + lay.ss)[f] = v[0];  // S opens chunk c = d
-        }
-      }
-      tmem_st_wait();
-    }
-    // num' columns d .. d+15 start at zero (only the ones product adds there)
-    if (MODE == MODE_FWD && warp >= 2 && part == 0) {
-      float z[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) z[i] = 0.f;
-      tmem_st16(tmem_addr(tbase, 32u * q4, lay.t_num + D), z);
-      tmem_st_wait();
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-  }
-
-  const uint32_t s_w = sbase + lay.w, s_phk = sbase + lay.phk, s_phq = sbase + lay.phq;
-  const uint32_t s_rb = sbase + lay.rb, s_ones = sbase + lay.ones;
-  auto t_buf = [&](int b) { return b ? lay.t_buf1 : lay.t_buf0; };
-  auto slot_addr = [&](int n) { return sbase + lay.slots + (uint32_t)(n % C::kSlots) * C::kTileBytes; };
-  auto slot_par = [&](int n) { return (uint32_t)((n / C::kSlots) & 1); };
-
-  if (warp == 0) {
-    // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      int n = 0;
-      bool ok = true;
-      auto load = [&](const CUtensorMap *m, int t) {
-        const int s = n % C::kSlots, u = n / C::kSlots;
-        if (u > 0 && !mbar_wait(bar + B_EMPTY + s, (u - 1) & 1, p.status, abort_flag)) return false;
-        mbar_arrive_expect_tx(bar + B_FULL + s, C::kTileBytes);
-        for (int c = 0; c < D; c += 64)
-          tma_load_3d(smem + lay.slots + s * C::kTileBytes + c * kTile * 2, m, bar + B_FULL + s, c, t * kTile, bh);
-        ++n;
-        return true;
-      };
-      for (int t = t0; t < t1 && ok; ++t) {
-        ok = load(&tmK, t);
-        if (ok && MODE == MODE_FWD) ok = load(&tmQ, t);
-        if (ok) ok = load(&tmV, t);
-        if (MODE == MODE_STATE && D == 64 && p.zero_grads) {
-          // the two-CTA backward adds its per-CTA partials of dQ, dK, dV
-          for (int c = 0; c < D; c += 64) {
-            tma_store_3d(&tmDQ, smem + lay.zero + c * kTile * 2, c, t * kTile, bh);
-            tma_store_3d(&tmDK, smem + lay.zero + c * kTile * 2, c, t * kTile, bh);
-            tma_store_3d(&tmDV, smem + lay.zero + c * kTile * 2, c, t * kTile, bh);
-          }
-          tma_store_commit();
-        }
-      }
-      if (MODE == MODE_STATE && D == 64 && p.zero_grads) tma_store_wait_all();
-      // copies still in flight land before the CTA can leave
-      for (int m = max(0, n - C::kSlots); m < n; ++m) mbar_drain(bar + B_FULL + m % C::kSlots, slot_par(m));
-      if (FAVOR || (MODE == MODE_FWD && seg > 0)) mbar_drain(bar + B_SETUP, 0);
-    }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      bool ok = true;
-      auto wait = [&](int b, uint32_t par) {
-        if (ok) ok = mbar_wait(bar + b, par, p.status, abort_flag);
-        return ok;
-      };
-      constexpr uint32_t NV = D == 64 ? D + 16 : D;  // [V, 1] in one MMA when d = 64
-      const uint32_t id_a = make_idesc(128, 128, false, false);
-      const uint32_t id_n = make_idesc(128, D, false, true);
-      const uint32_t id_nv = make_idesc(128, NV, false, true);
-      const uint32_t id_s = make_idesc(128, 16, false, true);
-      const uint32_t id_r = make_idesc(128, NV, true, true);
-      const uint32_t id_r1 = make_idesc(128, 16, true, true);
-      // [V, 1] as an MN-major operand: V's slot, then the ones block LBO bytes on
-      auto desc_v1 = [&](uint32_t s_v, int s) {
-        return make_desc(s_v, s_ones - s_v, 1024u, kSwizzle128) + (uint64_t)(s * 128u);
-      };
-      // R'_h += phi_k,h^T [V, 1]; the forward accumulates in place, the state
-      // pass restarts each tile's increment at zero
-      auto issue_r = [&](int h, uint32_t s_v, bool fresh) {
-        const uint32_t t_r = tbase + lay.t_r + h * NC;
-        for (int s = 0; s < kTile / 16; ++s) {
-          const uint32_t acc = (fresh && s == 0) ? 0u : 1u;
-          if (D == 64) {
-            mma_bf16(t_r, desc_mnmajor(s_phk, kTile, 0, s), desc_v1(s_v, s), id_r, acc);
-          } else {
-            mma_bf16(t_r, desc_mnmajor(s_phk, kTile, 0, s), desc_mnmajor(s_v, kTile, 0, s), id_r, acc);
-            mma_bf16(t_r + D, desc_mnmajor(s_phk, kTile, 0, s), desc_n16(s_ones, s), id_r1, acc);
-          }
-        }
-      };
-      // feature MMA F = X W_h^T into TMEM buffer b; `uses` counts the jobs
-      // issued on each buffer, whose previous job must have been read out
-      int uses0 = 0, uses1 = 0;
-      auto f_job = [&](uint32_t s_x, int h, int b) {
-        int &u = b ? uses1 : uses0;
-        if (u > 0 && !wait(B_FEMPTY + b, (u - 1) & 1)) return false;
-        tc_fence_after();
-        const uint32_t idesc = make_idesc(128, min(128, M - 128 * h), false, false);
-        for (int s = 0; s < D / 16; ++s)
-          mma_bf16(tbase + t_buf(b), desc_kmajor(s_x, kTile, 0, s), desc_kmajor(s_w, M, 128 * h, s), idesc, s > 0);
-        mma_commit(bar + B_FFULL + b);
-        ++u;
-        return true;
-      };
-      // the epilogue's initial state (or zero totals) is in TMEM
-      wait(B_RBFULL, 0);
-      if constexpr (MODE == MODE_FWD) {
-        // Buffer plan (FAVOR+): buffer 0 carries phi_k,0(t), phi_k,1(t),
-        // phi_q,1(t), phi_k,0(t+1), ...; buffer 1 carries phi_q,0(t) and then
-        // the tile's A, which therefore never waits for a feature job.  The
-        // epilogue finishes tile t-1 (mask, R copy, Y) between phi_k,0(t) and
-        // phi_q,0(t), so the issue order below follows that.
-        static_assert(nb <= 2, "at most 256 features");
-        constexpr int bA = C::kNbuf > 1 ? 1 : 0;  // A's TMEM buffer
-        auto slot_wait = [&](int n) { return wait(B_FULL + n % C::kSlots, slot_par(n)); };
-        auto empty = [&](int n) { mma_commit(bar + B_EMPTY + n % C::kSlots); };
-        // num' += tril(A) [V, 1] for the tile whose masked A is in phi_q's buffer
-        auto issue_av = [&](uint32_t s_v) {
-          for (int s = 0; s < kTile / 16; ++s) {
-            const uint64_t aa = desc_kmajor(s_phq, kTile, 0, s);
-            if (D == 64) {
-              mma_bf16(tbase + lay.t_num, aa, desc_v1(s_v, s), id_nv, 1);
-            } else {
-              mma_bf16(tbase + lay.t_num, aa, desc_mnmajor(s_v, kTile, 0, s), id_n, 1);
-              mma_bf16(tbase + lay.t_num + D, aa, desc_n16(s_ones, s), id_s, 1);
-            }
-          }
-        };
-        // A += phi_q,h phi_k,h^T and num += phi_q,h R_h^T
-        auto issue_anum = [&](int h) {
-          const uint32_t t_a = tbase + t_buf(bA);
-          const int nu = min(128, M - 128 * h);
-          for (int s = 0; s < nu / 16; ++s) {
-            const uint32_t acc = (h > 0 || s > 0) ? 1u : 0u;
-            const uint64_t aq = desc_kmajor(s_phq, kTile, 0, s);
-            mma_bf16(t_a, aq, desc_kmajor(s_phk, kTile, 0, s), id_a, acc);
-            mma_bf16(tbase + lay.t_num, aq, desc_mnmajor(s_rb, M, 0, 8 * h + s), id_n, acc);
-          }
-        };
-        if (FAVOR && ntl > 0 && slot_wait(0) && slot_wait(1)) {
-          f_job(slot_addr(0), 0, 0);
-          if (nb == 1) empty(0);
-          f_job(slot_addr(1), 0, 1);
-          if (nb == 1) empty(1);
-        }
-        for (int i = 0; i < ntl && ok; ++i) {
-          const int nK = 3 * i, nQ = nK + 1, nV = nK + 2;
-          const uint32_t s_k = slot_addr(nK), s_q = slot_addr(nQ), s_v = slot_addr(nV);
-          const uint32_t c = (uint32_t)(i * nb);
-          if (FAVOR && nb > 1) {
-            if (!f_job(s_k, 1, 0)) break;  // phi_k,1(t)
-            empty(nK);
-          }
-          if (!FAVOR) {
-            // elu+1 features are formed from K and Q by the epilogue alone
-            mbar_arrive(bar + B_EMPTY + nK % C::kSlots);
-            mbar_arrive(bar + B_EMPTY + nQ % C::kSlots);
-          }
-          if (i > 0) {
-            // phi_q,0(t) once the mask of tile t-1 has read A out of buffer 1
-            if (FAVOR) {
-              if (!slot_wait(nQ) || !f_job(s_q, 0, 1)) break;
-              if (nb == 1) empty(nQ);
-            }
-            // num'(t-1) += tril(A(t-1)) [V(t-1), 1]
-            if (!wait(B_ATFULL, (i - 1) & 1)) break;
-            tc_fence_after();
-            issue_av(slot_addr(nV - 3));
-            mma_commit(bar + B_NUMFULL);
-            empty(nV - 3);
-          }
-          // block 0: R'_0 += ..., once R(t-1) has been copied out of TMEM
-          if (!wait(B_PHK, c & 1) || !slot_wait(nV) || !wait(B_RBFULL, i & 1)) break;
-          tc_fence_after();
-          issue_r(0, s_v, false);
-          if (FAVOR && nb == 1 && i + 1 < ntl) {
-            // phi_k,0(t+1) ahead of A: buffer 0 is free once phi_k,0(t) is read
-            if (!slot_wait(nK + 3) || !f_job(slot_addr(nK + 3), 0, 0)) break;
-            empty(nK + 3);
-          }
-          if (!wait(B_PHQ, c & 1) || (i > 0 && !wait(B_NUMEMPTY, (i - 1) & 1))) break;
-          {
-            int &u = bA ? uses1 : uses0;
-            if (u > 0 && !wait(B_FEMPTY + bA, (u - 1) & 1)) break;
-          }
-          tc_fence_after();
-          issue_anum(0);
-          mma_commit(bar + B_PHFREE);
-          for (int h = 1; h < nb && ok; ++h) {
-            if (!f_job(s_q, h, 0)) break;  // phi_q,1(t)
-            empty(nQ);
-            if (!wait(B_PHK, (c + h) & 1)) break;
-            tc_fence_after();
-            issue_r(h, s_v, false);
-            if (i + 1 < ntl) {
-              // phi_k,0(t+1) ahead of the last A block
-              if (!slot_wait(nK + 3) || !f_job(slot_addr(nK + 3), 0, 0)) break;
-            }
-            if (!wait(B_PHQ, (c + h) & 1)) break;
-            tc_fence_after();
-            issue_anum(h);
-            mma_commit(bar + B_PHFREE);
-          }
-          if (!ok) break;
-          // A(t) complete: one phase of its buffer, like a feature job
-          mma_commit(bar + B_FFULL + bA);
-          ++(bA ? uses1 : uses0);
-        }
-        if (ok && ntl > 0 && wait(B_ATFULL, (ntl - 1) & 1)) {
-          tc_fence_after();
-          issue_av(slot_addr(3 * (ntl - 1) + 2));
-          mma_commit(bar + B_NUMFULL);
-          empty(3 * (ntl - 1) + 2);
-        }
-      } else {
-        int n = 0;
-        for (int i = 0; i < ntl && ok; ++i) {
-          const int nK = n, nV = n + 1;
-          n += C::kLoads;
-          const uint32_t s_k = slot_addr(nK), s_v = slot_addr(nV);
-          if (FAVOR) {
-            if (!wait(B_FULL + nK % C::kSlots, slot_par(nK))) break;
-            tc_fence_after();
-            for (int h = 0; h < nb && ok; ++h) f_job(s_k, h, 0);
-            if (!ok) break;
-            mma_commit(bar + B_EMPTY + nK % C::kSlots);
-          } else {
-            mbar_arrive(bar + B_EMPTY + nK % C::kSlots);
-          }
-          for (int h = 0; h < nb && ok; ++h) {
-            const uint32_t c = (uint32_t)(i * nb + h);
-            if (!wait(B_PHK, c & 1)) break;
-            if (h == 0) {
-              if (!wait(B_FULL + nV % C::kSlots, slot_par(nV))) break;
-              // the tile's increment restarts at zero once the epilogue has added the last
-              if (i > 0 && !wait(B_RBFULL, i & 1)) break;
-            }
-            tc_fence_after();
-            issue_r(h, s_v, true);
-            mma_commit(bar + B_PHFREE);
-          }
-          if (!ok) break;
-          mma_commit(bar + B_AFULL);
-          mma_commit(bar + B_EMPTY + nV % C::kSlots);
-        }
-      }
-      mma_commit(bar + B_DONE);
-      mbar_drain(bar + B_DONE, 0);
-    }
-  } else {
-    // ---------------------------------------------------------------- epilogue
-    const int q4 = warp & 3, part = (warp - 2) >> 2, row = 32 * q4 + lane;
-    const uint32_t lane_base = 32u * q4;
-    bool ok = true;
-    auto wait = [&](int b, uint32_t par) {
-      if (ok) ok = mbar_wait(bar + b, par, p.status, abort_flag);
-      return ok;
-    };
-    auto arrive = [&](int b) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar + b);
-    };
-    float *ss = reinterpret_cast<float *>(smem + lay.ss);
-    float *denp = reinterpret_cast<float *>(smem + lay.denp);
-    // R' state chunks (16 columns of one block) handled by this thread:
-    // chunk k = part, part + kParts, ... of the nb * NC / 16
-    constexpr int NCH = NC / 16;
-    auto put_rb = [&](int f, int c, const float *v) {
-      if (f >= M) return;
-#pragma unroll
-      for (int i = 0; i < 16; i += 8)
-        if (c + i + 8 <= D) st_bf16x8(s_rb + sw128_offset(f, c + i, M), v + i);
-      if (c == D) ss[f] = v[0];
-    };
-
-    // the incoming state was placed in TMEM during set-up
-    arrive(B_RBFULL);
-
-    constexpr int FC = (FAVOR ? FB : D) / kParts;  // phi columns of this thread
-    auto store_phi = [&](uint32_t s_out, const float *v) {
-#pragma unroll
-      for (int j = 0; j < FC / 8; ++j) st_bf16x8(s_out + sw128_offset(row, FC * part + 8 * j, kTile), v + 8 * j);
-    };
-    // per-buffer counts of the TMEM jobs read out so far
-    int got0 = 0, got1 = 0;
-    // the next job of TMEM buffer b (FC columns of this thread) into registers; frees the buffer
-    auto load_f = [&](int b, float *v) {
-      int &u = b ? got1 : got0;
-      if (!wait(B_FFULL + b, u & 1)) return;
-      tc_fence_after();
-      tmem_ldn<FC>(tmem_addr(tbase, lane_base, t_buf(b) + FC * part), v);
-      tc_fence_before();
-      arrive(B_FEMPTY + b);
-      ++u;
-    };
-    // phi of this thread's columns: FAVOR+ from the F job in buffer b, elu+1 from the X tile
-    auto make_phi = [&](int b, uint32_t s_x, float c_row, bool dead, float *v) {
-      if (FAVOR) {
-        load_f(b, v);
-#pragma unroll
-        for (int x = 0; x < FC; ++x) v[x] = dead ? 0.f : favor_feature(v[x], c_row);
-      } else {
-#pragma unroll
-        for (int j = 0; j < FC / 8; ++j) {
-          ld_bf16x8(s_x + sw128_offset(row, FC * part + 8 * j, kTile), v + 8 * j);
-#pragma unroll
-          for (int x = 0; x < 8; ++x) v[8 * j + x] = dead ? 0.f : elu1_feature(v[8 * j + x]);
-        }
-      }
-    };
-
-    if constexpr (MODE == MODE_FWD) {
-      constexpr int bA = C::kNbuf > 1 ? 1 : 0;  // A's TMEM buffer (see the MMA issuer)
-      // Finish tile j: masked A to bf16 (A's operand buffer), the bf16 copy of
-      // R(j) for the next tile's num MMAs, then Y(j) = num / den.  Runs after
-      // phi_k,0 of tile j + 1, once the MMAs that read tile j's last feature
-      // block (hence A(j) and R(j)) are done.
-      auto finish = [&](int j, bool refresh) {
-        // masked A (diagonal kept) -> bf16 into the phi_q buffer
-        {
-          int &u = bA ? got1 : got0;
-          if (!wait(B_FFULL + bA, u & 1)) return false;
-          tc_fence_after();
-          constexpr int AC = kTile / kParts;  // A columns of this thread, 32 at a time
-#pragma unroll 1
-          for (int c0 = AC * part; c0 < AC * (part + 1); c0 += 32) {
-            float v[32];
-            tmem_ld32(tmem_addr(tbase, lane_base, t_buf(bA) + c0), v);
-#pragma unroll
-            for (int x = 0; x < 32; ++x)
-              if (c0 + x > row) v[x] = 0.f;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) st_bf16x8(s_phq + sw128_offset(row, c0 + 8 * k, kTile), v + 8 * k);
-          }
-          tc_fence_before();
-          arrive(B_FEMPTY + bA);
-          ++u;
-          if (part == 0) {
-            // num' columns d .. d+15 restart at zero; every part read them for
-            // Y(j-1) before the num MMAs of tile j, hence before this point
-            float z[16];
-#pragma unroll
-            for (int x = 0; x < 16; ++x) z[x] = 0.f;
-            tmem_st16(tmem_addr(tbase, lane_base, lay.t_num + D), z);
-            tmem_st_wait();
-            tc_fence_before();
-          }
-          fence_async_smem();
-          arrive(B_ATFULL);
-        }
-        // bf16 copies of R(j) and fp32 S(j) for tile j + 1
-        if (refresh) {
-          for (int k = part; k < nb * NCH; k += kParts) {
-            const int b = k / NCH, c = (k - b * NCH) * 16;
-            float v[16];
-            tmem_ld16(tmem_addr(tbase, lane_base, lay.t_r + b * NC + c), v);
-            put_rb(128 * b + row, c, v);
-          }
-          fence_async_smem();
-          tc_fence_before();
-          arrive(B_RBFULL);
-        }
-        arrive(B_EPI);  // this warp's S(j) and den partials of tile j are in shared memory
-        // Y = num / den
-        if (!wait(B_NUMFULL, j & 1)) return false;
-        tc_fence_after();
-        constexpr int YC = D / kParts;  // value columns per thread
-        float v[YC];
-        const float rowsum_a = tmem_ld1(tmem_addr(tbase, lane_base, lay.t_num + D));
-        tmem_ldn<YC>(tmem_addr(tbase, lane_base, lay.t_num + YC * part), v);
-        tc_fence_before();
-        arrive(B_NUMEMPTY);
-        if (!wait(B_EPI, j & 1)) return false;
-        const int tj = t0 + j;
-        if (row < min(kTile, p.L - tj * kTile)) {
-          float den = rowsum_a;
-#pragma unroll
-          for (int q = 0; q < kParts; ++q) den += denp[((j & 1) * kParts + q) * kTile + row];
-          const float inv = 1.0f / den;
-          uint4 *dst = reinterpret_cast<uint4 *>(p.y + ((size_t)bh * p.L + (size_t)tj * kTile + row) * D + YC * part);
-#pragma unroll
-          for (int k = 0; k < YC / 8; ++k)
-            dst[k] = make_uint4(pack_bf16(v[8 * k] * inv, v[8 * k + 1] * inv),
-                                pack_bf16(v[8 * k + 2] * inv, v[8 * k + 3] * inv),
-                                pack_bf16(v[8 * k + 4] * inv, v[8 * k + 5] * inv),
-                                pack_bf16(v[8 * k + 6] * inv, v[8 * k + 7] * inv));
-        }
-        arrive(B_EMPTY + (3 * j + 2) % C::kSlots);  // V(j)
-        return true;
-      };
-
-      for (int i = 0; i < ntl && ok; ++i) {
-        const int t = t0 + i;
-        const bool dead = row >= min(kTile, p.L - t * kTile);  // padding rows past L: features forced to zero
-        const int nK = 3 * i, nQ = nK + 1;
-        const uint32_t s_k = slot_addr(nK), s_q = slot_addr(nQ);
-        if (!wait(B_FULL + nK % C::kSlots, slot_par(nK))) break;
-        if (!wait(B_FULL + nQ % C::kSlots, slot_par(nQ))) break;
-        float ck = 0.f, cq = 0.f;  // per-row exp2 offsets
-        if (FAVOR) {
-          ck = favor_row_const(tile_row_sqnorm(s_k, row, D), M);
-          cq = favor_row_const(tile_row_sqnorm(s_q, row, D), M);
-          arrive(B_EMPTY + nK % C::kSlots);
-          arrive(B_EMPTY + nQ % C::kSlots);
-        }
-        float dpart[4] = {0.f, 0.f, 0.f, 0.f};  // phi_q . S(t-1) over this thread's features
-#pragma unroll 1
-        for (int h = 0; h < nb && ok; ++h) {
-          const uint32_t c = (uint32_t)(i * nb + h);
-          float v[FC];
-          make_phi(0, s_k, ck, dead, v);
-          if (c > 0 && !wait(B_PHFREE, (c - 1) & 1)) break;
-          store_phi(s_phk, v);
-          fence_async_smem();
-          arrive(B_PHK);
-          if (!FAVOR && h == nb - 1) arrive(B_EMPTY + nK % C::kSlots);
-          if (h == 0 && i > 0 && !finish(i - 1, true)) break;
-          make_phi(h == 0 ? (FAVOR ? 1 : 0) : 0, s_q, cq, dead, v);
-          if (!ok) break;
-#pragma unroll
-          for (int x = 0; x < FC; ++x) dpart[x & 3] = fmaf(v[x], ss[128 * h + FC * part + x], dpart[x & 3]);
-          store_phi(s_phq, v);
-          fence_async_smem();
-          arrive(B_PHQ);
-          if (!FAVOR && h == nb - 1) arrive(B_EMPTY + nQ % C::kSlots);
-        }
-        if (!ok) break;
-        denp[((i & 1) * kParts + part) * kTile + row] = (dpart[0] + dpart[1]) + (dpart[2] + dpart[3]);
-      }
-      if (ok && ntl > 0 && wait(B_PHFREE, (uint32_t)(ntl * nb - 1) & 1)) finish(ntl - 1, false);
-    } else {
-      int n = 0;
-      for (int i = 0; i < ntl && ok; ++i) {
-        const int t = t0 + i;
-        const bool dead = row >= min(kTile, p.L - t * kTile);
-        const int nK = n, nV = n + 1;
-        n += C::kLoads;
-        const uint32_t s_k = slot_addr(nK);
-        if (!wait(B_FULL + nK % C::kSlots, slot_par(nK))) break;
-        float ck = 0.f;
-        if (FAVOR) {
-          ck = favor_row_const(tile_row_sqnorm(s_k, row, D), M);
-          arrive(B_EMPTY + nK % C::kSlots);
-        }
-        for (int h = 0; h < nb && ok; ++h) {
-          const uint32_t c = (uint32_t)(i * nb + h);
-          float v[FC];
-          make_phi(0, s_k, ck, dead, v);
-          if (c > 0 && !wait(B_PHFREE, (c - 1) & 1)) break;
-          if (!ok) break;
-          store_phi(s_phk, v);
-          fence_async_smem();
-          arrive(B_PHK);
-        }
-        if (!ok) break;
-        if (!FAVOR) arrive(B_EMPTY + nK % C::kSlots);
-        arrive(B_EMPTY + nV % C::kSlots);
-        // master += this tile's increment (fp32; double-float for S)
-        if (!wait(B_AFULL, i & 1)) break;
-        tc_fence_after();
-        float *lo = reinterpret_cast<float *>(smem + lay.lo);
-        for (int k = part; k < nb * NCH; k += kParts) {
-          const int b = k / NCH, c = (k - b * NCH) * 16, f = 128 * b + row;
-          float x[16], m[16];
-          tmem_ld16(tmem_addr(tbase, lane_base, lay.t_r + b * NC + c), x);
-          tmem_ld16(tmem_addr(tbase, lane_base, lay.t_m + b * NC + c), m);
-          const bool has_s = c == D;  // S is column 0 of chunk c = d
-          const float ms = m[0], xs = x[0];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) m[e] += x[e];
-          if (has_s && f < M) {
-            float hs = ms, l = lo[f * (D + 1) + D];
-            df_add(hs, l, xs);
-            lo[f * (D + 1) + D] = l;
-            m[0] = hs;
-          }
-          tmem_st16(tmem_addr(tbase, lane_base, lay.t_m + b * NC + c), m);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        arrive(B_RBFULL);
-      }
-    }
-
-    if (MODE == MODE_STATE && ok) {
-      // segment total of R' -> fp32 [M][D + 1] staged in the idle load slots
-      // (and phi_k tile) for one coalesced bulk store after the final barrier
-      float *stage = reinterpret_cast<float *>(smem + lay.slots);
-      for (int k = part; k < nb * NCH; k += kParts) {
-        const int b = k / NCH, c = (k - b * NCH) * 16, f = 128 * b + row;
-        float v[16];
-        tmem_ld16(tmem_addr(tbase, lane_base, lay.t_m + b * NC + c), v);
-        if (f < M) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (c + i <= D) stage[f * DP + c + i] = v[i];
-        }
-      }
-      fence_async_smem();
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (MODE == MODE_STATE && tid == 0 && !*abort_flag) {
-    const size_t off = ((size_t)bh * p.P + seg) * (size_t)M * DP;
-    bulk_store(p.states + off, sbase + lay.slots, (uint32_t)(M * DP * 4));
-    bulk_store(p.states_lo + off, sbase + lay.lo, (uint32_t)(M * DP * 4));
-    tma_store_commit();
-    tma_store_wait_read();
-  }
-  if (warp == 0) tmem_dealloc(tbase, 512);
-}
 
 // ============================================================================
 // Forward with role-specialised epilogue warpgroups.
@@ -1184,7 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait(F_FULL + s, slot_par(n))) break;
       float cr = 0.f;  // exp2 offset of the row
       if (FAVOR) {
-        cr = favor_row_const(tile_row_sqnorm(s_x, row, D), M);
+        // padding rows: F = 0 (zero-filled tile) and 2^-inf = 0, no select
+        cr = dead ? -INFINITY : favor_row_const(tile_row_sqnorm(s_x, row, D), M);
         arrive(F_EMPTY + s);
       }
       // phi_q . S(t-1) needs S(t-1), written with the bf16 copy of R(t-1)
@@ -1202,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             arrive(b_jempty);
             ++jobs;
 #pragma unroll
-            for (int x = 0; x < 64; ++x) v[x] = dead ? 0.f : favor_feature(v[x], cr);
+            for (int x = 0; x < 64; ++x) v[x] = favor_feature(v[x], cr);
           } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -1325,6 +622,381 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace fw
 
+// ============================================================================
+// Segment-state pass (the K side alone): writes each segment's total R' (the
+// rows eq. (3) adds) for the segment scan.  Each tile's increment
+// dR'_h = phi_k,h^T [V, 1] is an MMA that restarts at zero, and the tail
+// warps add it into an fp32 master in TMEM, as a double-float (low part in
+// shared memory) for the normaliser column S.  The backward recovers the
+// first tiles' small states by subtracting increments from this total, so
+// rounding in the total shows up there: accumulating in place on the tensor
+// pipe cost dQ of the first tiles of a long segment a factor of two hundred,
+// and plain fp32 still a factor of 2.6 through S, whose positive terms make
+// its rounding errors add up; the signed R columns' errors do not.
+//   warp 0       TMA producer (K, V ring; zero tiles of dQ, dK, dV when the
+//                two-CTA backward accumulates into them);
+//   warp 1       feature MMAs F = K W, 64 features per job, two TMEM buffers;
+//   warp 2       increment MMAs;
+//   warps 4-11   phi_k: two threads per row, 32 columns of each job each,
+//                into two phi_k buffers used in turn;
+//   warps 12-15  master += increment, then the segment total.
+namespace sw {
+
+constexpr int kWarps = 16;
+constexpr int kThreads = 32 * kWarps;
+
+enum {
+  S_FULL = 0,      // [4] slot loaded
+  S_EMPTY = 4,     // [4] slot free: MMA commit + 8 consumer arrivals
+  S_FFULL = 8,     // [2] feature job in TMEM buffer b
+  S_FEMPTY = 10,   // [2] ... read out (8 warps)
+  S_PHK = 12,      // [2] phi_k block stored in buffer b (8 warps)
+  S_PHFREE = 14,   // [2] increment MMAs reading phi_k buffer b done
+  S_AFULL = 16,    // the tile's increment complete
+  S_INCFREE = 17,  // increment added into the master (4 warps)
+  S_SETUP = 18,    // W image
+  S_DONE = 19,     // [2] MMA drain of each issuing thread
+  S_COUNT = 21
+};
+
+template <int D, bool FAVOR, int M>
+struct StateLayout {
+  static constexpr int kSlots = D == 128 ? 3 : 4;
+  static constexpr uint32_t kTileBytes = kTile * D * 2;
+  static constexpr int NC = D + 16;  // TMEM columns of one R' block
+  uint32_t w, slots, phk, ones, zero, lo, nrm, bars, total;
+  __host__ __device__ StateLayout() {
+    uint32_t o = 0;
+    w = o; o += FAVOR ? (uint32_t)M * 128u : 0u;  // W^T as [M][64] bf16
+    slots = o; o += kSlots * kTileBytes;            // then, at the end, the [M][D + 1] outputs
+    phk = o; o += 2u * kTile * 128 * 2;             // two phi_k blocks
+    ones = o; o += D == 64 ? 16384u : 4096u;
+    zero = o; o += D == 64 ? kTileBytes : 0u;       // zero tile (two-CTA backward, d = 64)
+    lo = o; o += (uint32_t)M * 4u;                  // low parts of S
+    nrm = o; o += 2u * 2u * kTile * 4u;             // [tile parity][half of d][row] partial |k|^2
+    bars = o; o += 8 * S_COUNT + 16;
+    total = o;
+  }
+};
+
+template <int D, bool FAVOR, int M>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_state_ws_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmDK,
+                       const __grid_constant__ CUtensorMap tmDV, Params p) {
+  using LY = StateLayout<D, FAVOR, M>;
+  constexpr int NC = LY::NC, kS = LY::kSlots, DP = D + 1;
+  constexpr int nb = (M + 127) / 128, FB = M < 128 ? M : 128, NCH = NC / 16;
+  constexpr int JT = FAVOR ? M / 64 : 0, JTd = JT > 0 ? JT : 1;  // feature jobs per tile
+  static_assert(LY::kSlots * LY::kTileBytes + 2 * kTile * 128 * 2 >= (uint32_t)M * DP * 4, "output staging fits");
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char *smem =
+      reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const LY lay;
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + lay.bars);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + S_COUNT);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar + S_COUNT) + 1;
+  // TMEM: feature buffers 2 x 64 | increment nb x NC | master nb x NC
+  const uint32_t t_f = 0, t_inc = FAVOR ? 128u : 0u, t_m = t_inc + nb * NC;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int seg = blockIdx.x, bh = blockIdx.y;
+  const int t0 = seg * p.tps, t1 = min(t0 + p.tps, p.nt), ntl = max(t1 - t0, 0);
+
+  if (tid == 0) {
+    for (int s = 0; s < kS; ++s) {
+      mbar_init(bar + S_FULL + s, 1);
+      mbar_init(bar + S_EMPTY + s, 9);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar + S_FFULL + b, 1);
+      mbar_init(bar + S_FEMPTY + b, 8);
+      mbar_init(bar + S_PHK + b, 8);
+      mbar_init(bar + S_PHFREE + b, 1);
+      mbar_init(bar + S_DONE + b, 1);
+    }
+    mbar_init(bar + S_AFULL, 1);
+    mbar_init(bar + S_INCFREE, 4);
+    mbar_init(bar + S_SETUP, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    if (FAVOR) {
+      mbar_arrive_expect_tx(bar + S_SETUP, (uint32_t)M * 128u);
+      bulk_load(smem + lay.w, p.wimg, (uint32_t)M * 128u, bar + S_SETUP);
+    }
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  if (warp == 0) tmem_alloc(tslot, 512);
+  if (D == 64)
+    for (int idx = tid; idx < (int)(LY::kTileBytes / 16); idx += kThreads)
+      reinterpret_cast<uint4 *>(smem + lay.zero)[idx] = make_uint4(0u, 0u, 0u, 0u);
+  for (int idx = tid; idx < M; idx += kThreads) reinterpret_cast<float *>(smem + lay.lo)[idx] = 0.f;
+  for (int idx = tid; idx < kTile * (D == 64 ? 64 : 16); idx += kThreads) {
+    const int r = D == 64 ? idx >> 6 : idx >> 4, x = D == 64 ? idx & 63 : idx & 15;
+    *reinterpret_cast<__nv_bfloat16 *>(smem + lay.ones + (D == 64 ? sw128_offset(r, x, kTile) : n16_offset(r, x))) =
+        __float2bfloat16_rn(x == 0 ? 1.f : 0.f);
+  }
+  if (M < 128) {
+    // features beyond M stay zero: the increment MMA reads 128
+    for (int idx = tid; idx < 2 * kTile * 128; idx += kThreads) {
+      const int b = idx >> 14, r = (idx >> 7) & 127, x = idx & 127;
+      if (x >= M)
+        *reinterpret_cast<__nv_bfloat16 *>(smem + lay.phk + b * kTile * 256 + sw128_offset(r, x, kTile)) =
+            __float2bfloat16_rn(0.f);
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  const int q4 = warp & 3, row = 32 * q4 + lane;
+  const uint32_t lane_base = 32u * q4;
+  if (warp >= 12) {
+    // the master starts at zero
+    float z[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) z[i] = 0.f;
+    for (int k = 0; k < nb * NCH; ++k) tmem_st16(tmem_addr(tbase, lane_base, t_m + (k / NCH) * NC + (k % NCH) * 16), z);
+    tmem_st_wait();
+  }
+  if (FAVOR && warp == 1 && lane == 0) mbar_wait(bar + S_SETUP, 0, p.status, abort_flag);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t s_w = sbase + lay.w, s_phk = sbase + lay.phk, s_ones = sbase + lay.ones;
+  auto slot_addr = [&](int n) { return sbase + lay.slots + (uint32_t)(n % kS) * LY::kTileBytes; };
+  auto slot_par = [&](int n) { return (uint32_t)((n / kS) & 1); };
+  bool ok = true;
+  auto wait = [&](int b, uint32_t par) {
+    if (ok) ok = mbar_wait(bar + b, par, p.status, abort_flag);
+    return ok;
+  };
+  auto arrive = [&](int b) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar + b);
+  };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int n = 0;
+      for (int t = t0; t < t1 && ok; ++t) {
+        for (int r = 0; r < 2 && ok; ++r, ++n) {
+          const int s = n % kS, u = n / kS;
+          if (u > 0 && !wait(S_EMPTY + s, (u - 1) & 1)) break;
+          mbar_arrive_expect_tx(bar + S_FULL + s, LY::kTileBytes);
+          for (int c = 0; c < D; c += 64)
+            tma_load_3d(smem + lay.slots + s * LY::kTileBytes + c * kTile * 2, r ? &tmV : &tmK, bar + S_FULL + s, c,
+                        t * kTile, bh);
+        }
+        if (D == 64 && p.zero_grads) {
+          // the two-CTA backward adds its per-CTA partials of dQ, dK, dV
+          tma_store_3d(&tmDQ, smem + lay.zero, 0, t * kTile, bh);
+          tma_store_3d(&tmDK, smem + lay.zero, 0, t * kTile, bh);
+          tma_store_3d(&tmDV, smem + lay.zero, 0, t * kTile, bh);
+          tma_store_commit();
+        }
+      }
+      if (D == 64 && p.zero_grads) tma_store_wait_all();
+      for (int m = max(0, n - kS); m < n; ++m) mbar_drain(bar + S_FULL + m % kS, slot_par(m));
+      if (FAVOR) mbar_drain(bar + S_SETUP, 0);
+    }
+  } else if (warp == 1 || warp == 2) {
+    // ---------------------------------------------------------------- MMA issuers
+    if (lane == 0 && (FAVOR || warp == 2)) {
+      if (warp == 1) {
+        // feature jobs: job j = features [64 (j % JT), +64) of tile j / JT into buffer j & 1
+        const uint32_t id_f = make_idesc(128, 64, false, false);
+        const uint64_t d_w0 = desc_kmajor(s_w, M, 0, 0);
+        for (int j = 0; j < ntl * JT && ok; ++j) {
+          const int i = j / JTd, n = 2 * i, b = j & 1, u = j >> 1;
+          if (u > 0 && !wait(S_FEMPTY + b, (u - 1) & 1)) break;
+          if (j % JTd == 0 && !wait(S_FULL + n % kS, slot_par(n))) break;
+          tc_fence_after();
+          const uint64_t dx = desc_kmajor(slot_addr(n), kTile, 0, 0);
+          const uint64_t dw = d_w0 + (uint64_t)((j % JTd) * 512);  // 64 rows = 8 atoms of 1024 B
+#pragma unroll
+          for (int s = 0; s < D / 16; ++s)
+            mma_bf16(tbase + t_f + 64 * b, dx + (uint64_t)((s & 3) * 2), dw + (uint64_t)((s & 3) * 2), id_f, s > 0);
+          mma_commit(bar + S_FFULL + b);
+          if (j % JTd == JT - 1) mma_commit(bar + S_EMPTY + n % kS);
+        }
+      } else {
+        constexpr uint32_t NV = D == 64 ? D + 16 : D;  // [V, 1] in one MMA when d = 64
+        const uint32_t id_r = make_idesc(128, NV, true, true);
+        const uint32_t id_r1 = make_idesc(128, 16, true, true);
+        for (int i = 0; i < ntl && ok; ++i) {
+          const int nV = 2 * i + 1;
+          const uint32_t s_v = slot_addr(nV);
+          const uint64_t dv = D == 64 ? make_desc(s_v, s_ones - s_v, 1024u, kSwizzle128) : desc_mnmajor(s_v, kTile, 0, 0);
+          for (int h = 0; h < nb && ok; ++h) {
+            const int c = i * nb + h, b = c & 1;
+            if (!wait(S_PHK + b, (c >> 1) & 1)) break;
+            if (h == 0) {
+              if (!FAVOR) mbar_arrive(bar + S_EMPTY + (2 * i) % kS);  // the MMA's share of the K slot
+              if (!wait(S_FULL + nV % kS, slot_par(nV))) break;
+              if (i > 0 && !wait(S_INCFREE, (i - 1) & 1)) break;  // the last increment is added
+            }
+            tc_fence_after();
+            const uint32_t t_r = tbase + t_inc + h * NC;
+            const uint64_t da = desc_mnmajor(s_phk + b * kTile * 256, kTile, 0, 0);
+#pragma unroll
+            for (int s = 0; s < kTile / 16; ++s) {
+              const uint64_t a = da + (uint64_t)(s * 128);
+              mma_bf16(t_r, a, dv + (uint64_t)(s * 128), id_r, s > 0);
+              if (D != 64) mma_bf16(t_r + D, a, desc_n16(s_ones, s), id_r1, s > 0);
+            }
+            mma_commit(bar + S_PHFREE + b);
+          }
+          if (!ok) break;
+          mma_commit(bar + S_AFULL);
+          mma_commit(bar + S_EMPTY + nV % kS);
+        }
+      }
+      mma_commit(bar + S_DONE + (warp - 1));
+      mbar_drain(bar + S_DONE + (warp - 1), 0);
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ---------------------------------------------------------------- phi_k
+    const int part = (warp - 4) >> 2;  // columns [32 part, +32) of every 64-feature job
+    int jobs = 0;
+    for (int i = 0; i < ntl && ok; ++i) {
+      const int t = t0 + i, n = 2 * i;
+      const bool dead = row >= min(kTile, p.L - t * kTile);  // padding rows past L: features forced to zero
+      const uint32_t s_k = slot_addr(n);
+      if (!wait(S_FULL + n % kS, slot_par(n))) break;
+      float ck = 0.f;
+      if (FAVOR) {
+        // |k|^2 of the row: each of its two threads sums half of d
+        float *nr = reinterpret_cast<float *>(smem + lay.nrm) + (i & 1) * 2 * kTile;
+        nr[part * kTile + row] = tile_row_sqnorm_part(s_k, row, 32 * part, 32);
+        named_barrier_sync(1, 256);
+        // padding rows: F = 0 (zero-filled tile) and 2^-inf = 0, no select
+        ck = dead ? -INFINITY : favor_row_const(nr[row] + nr[kTile + row], M);
+      }
+      for (int h = 0; h < nb && ok; ++h) {
+        const int c = i * nb + h, b = c & 1;
+        const uint32_t s_out = s_phk + b * kTile * 256;
+        for (int half = 0; half < FB / 64; ++half) {
+          float v[32];
+          const int f0 = 64 * half + 32 * part;  // feature offset within the block
+          if (FAVOR) {
+            const int fb = jobs & 1;
+            if (!wait(S_FFULL + fb, (jobs >> 1) & 1)) break;
+            tc_fence_after();
+            tmem_ld32(tmem_addr(tbase, lane_base, t_f + 64 * fb + 32 * part), v);
+            tc_fence_before();
+            arrive(S_FEMPTY + fb);
+            ++jobs;
+#pragma unroll
+            for (int x = 0; x < 32; ++x) v[x] = favor_feature(v[x], ck);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              ld_bf16x8(s_k + sw128_offset(row, 128 * h + f0 + 8 * j, kTile), v + 8 * j);
+#pragma unroll
+              for (int x = 0; x < 8; ++x) v[8 * j + x] = dead ? 0.f : elu1_feature(v[8 * j + x]);
+            }
+          }
+          // the buffer's last block has been read by its increment MMAs
+          if (half == 0 && c >= 2 && !wait(S_PHFREE + b, ((c >> 1) - 1) & 1)) break;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) st_bf16x8(s_out + sw128_offset(row, f0 + 8 * j, kTile), v + 8 * j);
+        }
+        if (!ok) break;
+        fence_async_smem();
+        arrive(S_PHK + b);
+      }
+      if (!ok) break;
+      arrive(S_EMPTY + n % kS);
+    }
+  } else if (warp >= 12) {
+    // ---------------------------------------------------------------- master += increment
+    float *lo = reinterpret_cast<float *>(smem + lay.lo);
+    for (int i = 0; i < ntl && ok; ++i) {
+      if (!wait(S_AFULL, i & 1)) break;
+      tc_fence_after();
+      // per block: the R columns in 32-column steps, then the chunk holding S
+      for (int b = 0; b < nb; ++b) {
+        const int f = 128 * b + row;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          float x[32], m[32];
+          tmem_ld32x2(tmem_addr(tbase, lane_base, t_inc + b * NC + c), tmem_addr(tbase, lane_base, t_m + b * NC + c), x, m);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) m[e] += x[e];
+          tmem_st16(tmem_addr(tbase, lane_base, t_m + b * NC + c), m);
+          tmem_st16(tmem_addr(tbase, lane_base, t_m + b * NC + c + 16), m + 16);
+        }
+        float x[16], m[16];
+        tmem_ld16x2(tmem_addr(tbase, lane_base, t_inc + b * NC + D), tmem_addr(tbase, lane_base, t_m + b * NC + D), x, m);
+        const float ms = m[0], xs = x[0];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) m[e] += x[e];
+        if (f < M) {  // S is column 0 of the chunk at d: double-float
+          float hs = ms, l = lo[f];
+          df_add(hs, l, xs);
+          lo[f] = l;
+          m[0] = hs;
+        }
+        tmem_st16(tmem_addr(tbase, lane_base, t_m + b * NC + D), m);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      arrive(S_INCFREE);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_n(bar + S_EMPTY + (2 * i + 1) % kS, 2);  // V(t): 4 warps x 2
+    }
+  }
+
+  // segment total of R' -> fp32 [M][D + 1] in the idle load slots (and phi_k
+  // buffers), one coalesced bulk store each for the high and the low parts
+  float *stage = reinterpret_cast<float *>(smem + lay.slots);
+  const bool out = ok && !*abort_flag;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp >= 12 && out) {
+    for (int k = 0; k < nb * NCH; ++k) {
+      const int b = k / NCH, c = (k - b * NCH) * 16, f = 128 * b + row;
+      float v[16];
+      tmem_ld16(tmem_addr(tbase, lane_base, t_m + b * NC + c), v);
+      if (f < M) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (c + i <= D) stage[f * DP + c + i] = v[i];
+      }
+    }
+  }
+  fence_async_smem();
+  __syncthreads();
+  const size_t off = ((size_t)bh * p.P + seg) * (size_t)M * DP;
+  if (tid == 0 && !*abort_flag) {
+    bulk_store(p.states + off, sbase + lay.slots, (uint32_t)(M * DP * 4));
+    tma_store_commit();
+    tma_store_wait_read();
+  }
+  __syncthreads();
+  if (!*abort_flag) {
+    const float *lo = reinterpret_cast<const float *>(smem + lay.lo);
+    for (int idx = tid; idx < M * DP; idx += kThreads) stage[idx] = (idx % DP == D) ? lo[idx / DP] : 0.f;
+  }
+  fence_async_smem();
+  __syncthreads();
+  if (tid == 0 && !*abort_flag) {
+    bulk_store(p.states_lo + off, sbase + lay.slots, (uint32_t)(M * DP * 4));
+    tma_store_commit();
+    tma_store_wait_read();
+  }
+  if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
+}  // namespace sw
+
 template <int D, bool FAVOR, int MODE, int M>
 cudaError_t launch_m(const Plan &pl, const Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
                      const CUtensorMap &mv, const CUtensorMap *mz, int nseg, cudaStream_t st) {
@@ -1343,12 +1015,11 @@ cudaError_t launch_m(const Plan &pl, const Args &a, const CUtensorMap &mq, const
     if (e != cudaSuccess) return e;
     kern<<<dim3(nseg, pl.BH), fw::kThreads, smem, st>>>(mq, mk, mv, p);
   } else {
-    const Layout<D, FAVOR, MODE> lay(M);
-    const int smem = (int)lay.total + 1024;
-    auto kern = tc_fwd_kernel<D, FAVOR, MODE, M>;
+    const int smem = (int)sw::StateLayout<D, FAVOR, M>().total + 1024;
+    auto kern = sw::tc_state_ws_kernel<D, FAVOR, M>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(nseg, pl.BH), kThreads, smem, st>>>(mq, mk, mv, mz ? mz[0] : mk, mz ? mz[1] : mk, mz ? mz[2] : mk, p);
+    kern<<<dim3(nseg, pl.BH), sw::kThreads, smem, st>>>(mk, mv, mz ? mz[0] : mk, mz ? mz[1] : mk, mz ? mz[2] : mk, p);
   }
   return cudaGetLastError();
 }
