@@ -37,7 +37,8 @@ namespace tcb {
 
 using namespace slim::tc;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+constexpr int kParts = 4;  // threads per row (TMEM lane): warps w, w + 4, w + 8, w + 12
 constexpr int kTile = 128;
 constexpr int D = 64;
 
@@ -74,10 +75,14 @@ struct Layout {
     s_f = o; o += 128 * 4;
     gs_f = o; o += 128 * 4;
     dd = o; o += kTile * 4;
-    usq = o; o += 2 * kTile * 4;
-    usk = o; o += 2 * kTile * 4;
-    dot = o; o += 2 * kTile * 4;
-    rx_den = o; o += 128 * 4;  // cluster exchange: the peer's den partials
+    usq = o; o += kParts * kTile * 4;  // [part][row] partial row sums of u_q
+    usk = o; o += kParts * kTile * 4;
+    // dY . Y partials: dead before u's row sums are written
+    dot = usq;
+    // cluster exchange, the peer's den partials: read before this tile's
+    // G_S copy is written, and the peer writes them only after this CTA has
+    // passed its next tile's features (hence read G_S)
+    rx_den = gs_f;
     bars = o; o += 128;
     total = o;
   }
@@ -97,31 +102,18 @@ __device__ __forceinline__ void st_bf16_scalar(unsigned char *smem, uint32_t off
 
 // Copy columns [0, 64) of a TMEM state (features on lanes) into a bf16
 // [MC][64] tile and column 64 into an fp32 vector.  Threads: feature
-// f = 32 * (warp % 4) + lane, column half = warp / 4.
-// (col_lo != col: the state is the double-float pair (col, col_lo).)
-__device__ __forceinline__ void state_to_smem(uint32_t tbase, uint32_t col, uint32_t col_lo, int q4,
-                                              int ch, int f, int MC, uint32_t s_tile, float *vec) {
-  float v[32];
-  tmem_ld32(tmem_addr(tbase, 32 * q4, col + 32 * ch), v);
-  if (col_lo != col) {
-    float l[32];
-    tmem_ld32(tmem_addr(tbase, 32 * q4, col_lo + 32 * ch), l);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] += l[i];
-  }
+// f = 32 * (warp % 4) + lane, columns [16 part, +16); part 3 also column 64.
+__device__ __forceinline__ void state_to_smem(uint32_t tbase, uint32_t col, int q4, int part, int f, int MC,
+                                              uint32_t s_tile, float *vec) {
+  float v[16];
+  tmem_ld16(tmem_addr(tbase, 32 * q4, col + 16 * part), v);
   if (f < MC) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) st_bf16x8(s_tile + sw128_offset(f, 32 * ch + 8 * j, MC), v + 8 * j);
+    for (int j = 0; j < 2; ++j) st_bf16x8(s_tile + sw128_offset(f, 16 * part + 8 * j, MC), v + 8 * j);
   }
-  if (ch == 1) {
-    float s[16];
-    tmem_ld16(tmem_addr(tbase, 32 * q4, col + 64), s);
-    if (col_lo != col) {
-      float l[16];
-      tmem_ld16(tmem_addr(tbase, 32 * q4, col_lo + 64), l);
-      s[0] += l[0];
-    }
-    if (f < MC) vec[f] = s[0];
+  if (part == kParts - 1) {
+    const float s0 = tmem_ld1(tmem_addr(tbase, 32 * q4, col + 64));
+    if (f < MC) vec[f] = s0;
   }
 }
 
@@ -132,7 +124,7 @@ __device__ __forceinline__ void state_to_smem(uint32_t tbase, uint32_t col, uint
 // cross-feature sums (num, den; dV, dQ, dK, rowsum(u)) for the 64 rows each
 // owns, plus dN' so both hold it.  Exchange buffers reuse tiles that are
 // provably idle at that point (cluster barriers mark those points).
-template <bool FAVOR, int CS>
+template <bool FAVOR, int CS, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDY,
@@ -141,7 +133,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem =
       reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int MC = p.M / CS;  // features per CTA (<= 128)
+  // MC: features per CTA (<= 128)
+  constexpr int QF = MC / kParts;  // feature columns per thread
+  constexpr int QD = D / kParts;   // value columns per thread
   const Layout lay(MC);
   const uint32_t sb = smem_u32(smem);
   uint64_t *in_bar = reinterpret_cast<uint64_t *>(smem + lay.bars);
@@ -162,13 +156,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *dot = reinterpret_cast<float *>(smem + lay.dot);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q4 = warp & 3, ch = warp >> 2, row = 32 * q4 + lane;
+  const int q4 = warp & 3, part = warp >> 2, row = 32 * q4 + lane;
   const int rank = CS == 2 ? (int)cluster_rank() : 0, peer = 1 - rank;
   const int seg = blockIdx.x / CS, bh = blockIdx.y;
   const int M = p.M, DP = D + 1;
   const int fbase = rank * MC;  // first feature of this CTA
   const int t0 = seg * p.tps, t1 = min(t0 + p.tps, p.nt);
-  const int half = MC / 2;  // feature columns per thread (two threads per row)
 
   // this CTA's rows of the W^T image (its features are contiguous rows of
   // it, with the same swizzle phase) and its features' segment-end state
@@ -212,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float *sh = reinterpret_cast<const float *>(smem + lay.phq);
     const float *sl = reinterpret_cast<const float *>(smem + lo_stage);
     const int f = row;
-    for (int c = ch * 48; c < (ch ? 80 : 48); c += 16) {
+    for (int c = 16 * part; c < 80; c += 16 * kParts) {
       float h[16], l[16], z[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -294,8 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     float ck = 0.f, cq = 0.f;
     if (FAVOR) {
-      ck = favor_row_const(tile_row_sqnorm(s_k, row, D), M);
-      cq = favor_row_const(tile_row_sqnorm(s_q, row, D), M);
+      ck = live ? favor_row_const(tile_row_sqnorm(s_k, row, D), M) : -INFINITY;
+      cq = live ? favor_row_const(tile_row_sqnorm(s_q, row, D), M) : -INFINITY;
     }
 
     // (b) features of both sides: F_k -> T, F_q -> X, one commit
@@ -312,23 +305,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int side = 0; side < 2; ++side) {
         const uint32_t t_in = side ? kX : kT, s_out = side ? s_phq : s_phk;
         const float c_row = side ? cq : ck;
-        for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 32) {
-          float v[32];
+        const int c0 = QF * part;
+        float v[QF];
+        if constexpr (QF == 32) {
           tmem_ld32(tmem_addr(tb, 32 * q4, t_in + c0), v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = favor_feature(v[i], c_row);
-          if (!live) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.f;
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) st_bf16x8(s_out + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
+        } else {
+          tmem_ld16(tmem_addr(tb, 32 * q4, t_in + c0), v);
         }
+        // padding rows: F = 0 (zero-filled tile) and 2^-inf = 0
+#pragma unroll
+        for (int i = 0; i < QF; ++i) v[i] = favor_feature(v[i], c_row);
+#pragma unroll
+        for (int j = 0; j < QF / 8; ++j) st_bf16x8(s_out + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
       }
     } else {
       for (int side = 0; side < 2; ++side) {
         const uint32_t s_x = side ? s_q : s_k, s_out = side ? s_phq : s_phk;
-        for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 8) {
+        for (int c0 = QF * part; c0 < QF * (part + 1); c0 += 8) {
           float v[8];
           ld_bf16x8(s_x + sw128_offset(row, c0, kTile), v);
 #pragma unroll
@@ -361,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // eq. (19) on the double-float master, and from the updated values the
     // bf16 copies of R and of S (high, low) for the MMAs, fp32 S for the
     // epilogues
-    for (int c = ch ? 48 : 0; c < (ch ? 80 : 48); c += 16) {
+    for (int c = 16 * part; c < 80; c += 16 * kParts) {
       float x[16], h[16], l[16];
       tmem_ld16(tmem_addr(tb, 32 * q4, kT + c), x);
       tmem_ld16(tmem_addr(tb, 32 * q4, kRhi + c), h);
@@ -389,13 +382,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_st_wait();
     // tril(A) (diagonal kept) -> bf16 tile
     {
-      float v[64];
-      tmem_ld32x2(tmem_addr(tb, 32 * q4, kX + 64 * ch), tmem_addr(tb, 32 * q4, kX + 64 * ch + 32), v, v + 32);
+      float v[32];
+      tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * part), v);
 #pragma unroll
-      for (int i = 0; i < 64; ++i)
-        if (64 * ch + i > row) v[i] = 0.f;
+      for (int i = 0; i < 32; ++i)
+        if (32 * part + i > row) v[i] = 0.f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) st_bf16x8(s_at + sw128_offset(row, 64 * ch + 8 * j, kTile), v + 8 * j);
+      for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, 32 * part + 8 * j, kTile), v + 8 * j);
     }
     fence_async_smem();
     cta_sync();
@@ -422,8 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(tmem_addr(tb, 32 * q4, kT + D), dv);
         den = dv[0] + dv[1];
       }
-      float v[32], g[32];
-      tmem_ld32(tmem_addr(tb, 32 * q4, kT + 32 * ch), v);
+      float v[QD], g[QD];
+      tmem_ld16(tmem_addr(tb, 32 * q4, kT + QD * part), v);
       if (CS == 2) {
         // once the peer is past its features its Q and K tiles take my
         // partial num (all 128 rows) and den; each CTA then forms dN' for
@@ -431,40 +424,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(x1_free, x_phase, p.status, abort_flag);
         const uint32_t dst = map_peer(s_q, peer);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          st_async_v4(dst + xoff(row, 8 * ch + j, 128), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3],
+        for (int j = 0; j < QD / 4; ++j)
+          st_async_v4(dst + xoff(row, (QD / 4) * part + j, 128), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3],
                       peer_x1_full);
-        if (ch == 0) st_async_f32(map_peer(sb + lay.rx_den + row * 4, peer), den, peer_x1_full);
+        if (part == 0) st_async_f32(map_peer(sb + lay.rx_den + row * 4, peer), den, peer_x1_full);
         mbar_wait(x1_full, x_phase, p.status, abort_flag);
-        float r[32];
+        float r[QD];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) ld_shared_v4f(s_q + xoff(row, 8 * ch + j, 128), r + 4 * j);
+        for (int j = 0; j < QD / 4; ++j) ld_shared_v4f(s_q + xoff(row, (QD / 4) * part + j, 128), r + 4 * j);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] += r[i];
+        for (int i = 0; i < QD; ++i) v[i] += r[i];
         den += rx_den[row];
       }
       const float inv = 1.0f / den;
       float dyy = 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) ld_bf16x8(s_dy + sw128_offset(row, 32 * ch + 8 * j, kTile), g + 8 * j);
+      for (int j = 0; j < QD / 8; ++j) ld_bf16x8(s_dy + sw128_offset(row, QD * part + 8 * j, kTile), g + 8 * j);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < QD; ++i) {
         const float y = v[i] * inv;
         dyy = fmaf(g[i], y, dyy);
         g[i] = live ? g[i] * inv : 0.f;
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) st_bf16x8(s_dn + sw128_offset(row, 32 * ch + 8 * j, kTile), g + 8 * j);
-      dot[ch * kTile + row] = dyy;
+      for (int j = 0; j < QD / 8; ++j) st_bf16x8(s_dn + sw128_offset(row, QD * part + 8 * j, kTile), g + 8 * j);
+      dot[part * kTile + row] = dyy;
       __syncthreads();
-      if (ch == 0) {
-        const float dval = live ? -(dot[row] + dot[kTile + row]) * inv : 0.f;
+      if (part == 0) {
+        const float dval = live ? -((dot[row] + dot[kTile + row]) + (dot[2 * kTile + row] + dot[3 * kTile + row])) * inv : 0.f;
         dd[row] = dval;
         st_bf16_scalar(smem, lay.ddb + n16_offset(row, 0), dval);
       }
     }
     cta_sync();  // dY consumed: its buffer now takes the bf16 copy of G_V
-    state_to_smem(tb, kG, kG, q4, ch, row, MC, s_dy, gs_f);
+    state_to_smem(tb, kG, q4, part, row, MC, s_dy, gs_f);
     fence_async_smem();
     cta_sync();
 
@@ -485,23 +478,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       const float dval = dd[row];
       {
-        float v[64];
-        tmem_ld32x2(tmem_addr(tb, 32 * q4, kT + 64 * ch), tmem_addr(tb, 32 * q4, kT + 64 * ch + 32), v, v + 32);
+        float v[32];
+        tmem_ld32(tmem_addr(tb, 32 * q4, kT + 32 * part), v);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) v[i] = (64 * ch + i > row) ? 0.f : v[i] + dval;
+        for (int i = 0; i < 32; ++i) v[i] = (32 * part + i > row) ? 0.f : v[i] + dval;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) st_bf16x8(s_at + sw128_offset(row, 64 * ch + 8 * j, kTile), v + 8 * j);
+        for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, 32 * part + 8 * j, kTile), v + 8 * j);
       }
-      float v[32];
-      tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * ch), v);
+      float v[QD];
+      tmem_ld16(tmem_addr(tb, 32 * q4, kX + QD * part), v);
       if (CS == 2) {
         // this CTA's dV partial -> bf16 in the idle Q tile, for a reduce-add
 #pragma unroll
-        for (int j = 0; j < 4; ++j) st_bf16x8(s_q + sw128_offset(row, 32 * ch + 8 * j, kTile), v + 8 * j);
+        for (int j = 0; j < QD / 8; ++j) st_bf16x8(s_q + sw128_offset(row, QD * part + 8 * j, kTile), v + 8 * j);
       } else if (live) {
-        uint4 *dst = reinterpret_cast<uint4 *>(p.dv + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch);
+        uint4 *dst = reinterpret_cast<uint4 *>(p.dv + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + QD * part);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < QD / 8; ++j)
           dst[j] = make_uint4(pack_bf16(v[8 * j], v[8 * j + 1]), pack_bf16(v[8 * j + 2], v[8 * j + 3]),
                               pack_bf16(v[8 * j + 4], v[8 * j + 5]), pack_bf16(v[8 * j + 6], v[8 * j + 7]));
       }
@@ -565,11 +558,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       const float dval = dd[row];
       float uq = 0.f, uk = 0.f;
-      for (int c0 = ch * half; c0 < (ch + 1) * half; c0 += 32) {
-        float a[32], b[32];
-        tmem_ld32x2(tmem_addr(tb, 32 * q4, kT + c0), tmem_addr(tb, 32 * q4, kX + c0), a, b);
+      {
+        const int c0 = QF * part;
+        float a[QF], b[QF];
+        if constexpr (QF == 32) {
+          tmem_ld32x2(tmem_addr(tb, 32 * q4, kT + c0), tmem_addr(tb, 32 * q4, kX + c0), a, b);
+        } else {
+          tmem_ld16x2(tmem_addr(tb, 32 * q4, kT + c0), tmem_addr(tb, 32 * q4, kX + c0), a, b);
+        }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < QF / 8; ++j) {
           float fq[8], fk[8];
           ld_bf16x8(s_phq + sw128_offset(row, c0 + 8 * j, kTile), fq);
           ld_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), fk);
@@ -591,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (FAVOR) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < QF / 8; ++j) {
             st_bf16x8(s_phq + sw128_offset(row, c0 + 8 * j, kTile), a + 8 * j);
             st_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), b + 8 * j);
           }
@@ -599,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint4 *gq = reinterpret_cast<uint4 *>(p.dq + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + c0);
           uint4 *gk = reinterpret_cast<uint4 *>(p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + c0);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < QF / 8; ++j) {
             gq[j] = make_uint4(pack_bf16(a[8 * j], a[8 * j + 1]), pack_bf16(a[8 * j + 2], a[8 * j + 3]),
                                pack_bf16(a[8 * j + 4], a[8 * j + 5]), pack_bf16(a[8 * j + 6], a[8 * j + 7]));
             gk[j] = make_uint4(pack_bf16(b[8 * j], b[8 * j + 1]), pack_bf16(b[8 * j + 2], b[8 * j + 3]),
@@ -607,8 +605,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      usq[ch * kTile + row] = uq;
-      usk[ch * kTile + row] = uk;
+      usq[part * kTile + row] = uq;
+      usk[part * kTile + row] = uk;
     }
     fence_async_smem();
     cta_sync();
@@ -624,9 +622,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_done();
       }
       wait_mma();
-      float sq = usq[row] + usq[kTile + row], sk = usk[row] + usk[kTile + row];
-      float a[32], b[32];
-      tmem_ld32x2(tmem_addr(tb, 32 * q4, kT + 32 * ch), tmem_addr(tb, 32 * q4, kT + 64 + 32 * ch), a, b);
+      const float sq = (usq[row] + usq[kTile + row]) + (usq[2 * kTile + row] + usq[3 * kTile + row]);
+      const float sk = (usk[row] + usk[kTile + row]) + (usk[2 * kTile + row] + usk[3 * kTile + row]);
+      float a[QD], b[QD];
+      tmem_ld16x2(tmem_addr(tb, 32 * q4, kT + QD * part), tmem_addr(tb, 32 * q4, kT + 64 + QD * part), a, b);
       uint32_t s_xq = s_q, s_xk = s_k;
       if (CS == 2) {
         mbar_wait(rl_bar, rl_phase, p.status, abort_flag);
@@ -635,12 +634,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_xk = sb + lay.at + tile_bytes;
       }
       // dQ = u_q W^T - q rowsum(u_q), dK likewise (this CTA's features)
-      float oq[32], ok[32];
+      float oq[QD], ok[QD];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < QD / 8; ++j) {
         float xq[8], xk[8];
-        ld_bf16x8(s_xq + sw128_offset(row, 32 * ch + 8 * j, kTile), xq);
-        ld_bf16x8(s_xk + sw128_offset(row, 32 * ch + 8 * j, kTile), xk);
+        ld_bf16x8(s_xq + sw128_offset(row, QD * part + 8 * j, kTile), xq);
+        ld_bf16x8(s_xk + sw128_offset(row, QD * part + 8 * j, kTile), xk);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           oq[8 * j + i] = a[8 * j + i] - xq[i] * sq;
@@ -650,9 +649,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (CS == 2) {
         // partials -> bf16 in the idle dN and R-copy tiles for reduce-adds
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          st_bf16x8(s_dn + sw128_offset(row, 32 * ch + 8 * j, kTile), oq + 8 * j);
-          st_bf16x8(s_rb + sw128_offset(row, 32 * ch + 8 * j, kTile), ok + 8 * j);
+        for (int j = 0; j < QD / 8; ++j) {
+          st_bf16x8(s_dn + sw128_offset(row, QD * part + 8 * j, kTile), oq + 8 * j);
+          st_bf16x8(s_rb + sw128_offset(row, QD * part + 8 * j, kTile), ok + 8 * j);
         }
         fence_async_smem();
         cta_sync();
@@ -662,10 +661,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_store_commit();
         }
       } else if (live) {
-        uint4 *gq = reinterpret_cast<uint4 *>(p.dq + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch);
-        uint4 *gk = reinterpret_cast<uint4 *>(p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * ch);
+        uint4 *gq = reinterpret_cast<uint4 *>(p.dq + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + QD * part);
+        uint4 *gk = reinterpret_cast<uint4 *>(p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + QD * part);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < QD / 8; ++j) {
           gq[j] = make_uint4(pack_bf16(oq[8 * j], oq[8 * j + 1]), pack_bf16(oq[8 * j + 2], oq[8 * j + 3]),
                              pack_bf16(oq[8 * j + 4], oq[8 * j + 5]), pack_bf16(oq[8 * j + 6], oq[8 * j + 7]));
           gk[j] = make_uint4(pack_bf16(ok[8 * j], ok[8 * j + 1]), pack_bf16(ok[8 * j + 2], ok[8 * j + 3]),
@@ -687,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   {
     float *stage = reinterpret_cast<float *>(smem + lay.phq);
     const int f = row;
-    for (int c = ch * 48; c < (ch ? 80 : 48); c += 16) {
+    for (int c = 16 * part; c < 80; c += 16 * kParts) {
       float v[16];
       tmem_ld16(tmem_addr(tb, 32 * q4, kG + c), v);
       if (f < MC) {
@@ -709,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_dealloc(tb, 512);
 }
 
-template <bool FAVOR, int CS>
+template <bool FAVOR, int CS, int MC>
 cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mdy;
   if (!make_map_bf16_3d(&mq, a.q, pl.BH, pl.L, D, kTile) || !make_map_bf16_3d(&mk, a.k, pl.BH, pl.L, D, kTile) ||
@@ -740,7 +739,7 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
   {
     const Layout lay(pl.M / CS);
     const int smem = (int)lay.total + 1024;
-    auto kern = tc_bwd_kernel<FAVOR, CS>;
+    auto kern = tc_bwd_kernel<FAVOR, CS, MC>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (CS > 1) {
@@ -784,9 +783,11 @@ bool tc_backward_supported(int d, int M, int chunk, bool favor) {
 
 cudaError_t tc_backward(const Plan &p, const Args &a, cudaStream_t st) {
   if (p.d != 64) return cudaErrorInvalidValue;
-  if (!p.favor) return tcb::backward_family<false, 1>(p, a, st);
-  if (p.M == 256) return tcb::backward_family<true, 2>(p, a, st);
-  return tcb::backward_family<true, 1>(p, a, st);
+  if (!p.favor) return p.M == 64 ? tcb::backward_family<false, 1, 64>(p, a, st) : cudaErrorInvalidValue;
+  if (p.M == 256) return tcb::backward_family<true, 2, 128>(p, a, st);
+  if (p.M == 128) return tcb::backward_family<true, 1, 128>(p, a, st);
+  if (p.M == 64) return tcb::backward_family<true, 1, 64>(p, a, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace slim
