@@ -12,7 +12,9 @@ SLiM", section 2.1:
   * ``quadratic.forward`` / ``quadratic.backward``: the explicit quadratic form
     of eq. (2), numpy fp64;
   * ``quadratic.softmax_forward``: eq. (1), the exponential attention that the
-    randomized feature map approximates.
+    randomized feature map approximates;
+  * ``prefill_state`` / ``decode_step``: the same recurrence in its serving
+    form, one new row at a time against a carried state (C).
 """
 import ctypes
 import os
@@ -53,7 +55,10 @@ def _load():
             lib.oracle_forward.argtypes = [dp] * 5 + [ctypes.c_long] * 3 + [ctypes.c_int] * 4
             lib.oracle_backward.argtypes = [dp] * 10 + [ctypes.c_long] * 3 + [ctypes.c_int] * 4
             lib.oracle_feature_map.argtypes = [dp] * 3 + [ctypes.c_long] + [ctypes.c_int] * 3
-            for fn in (lib.oracle_forward, lib.oracle_backward, lib.oracle_feature_map):
+            lib.oracle_state.argtypes = [dp] * 4 + [ctypes.c_long] * 3 + [ctypes.c_int] * 4
+            lib.oracle_decode.argtypes = [dp] * 6 + [ctypes.c_long] * 2 + [ctypes.c_int] * 3
+            for fn in (lib.oracle_forward, lib.oracle_backward, lib.oracle_feature_map, lib.oracle_state,
+                       lib.oracle_decode):
                 fn.restype = ctypes.c_int
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -141,6 +146,44 @@ def recurrence_backward(q, k, v, w, dy, threads=0, want_dw=True, want_y=False):
     if want_y:
         out = out + (y.reshape(shape),)
     return out
+
+
+def prefill_state(k, v, w, threads=0):
+    """Serving form of eq. (3)-(4): the stacked state R' = [R ; S^T] after all
+    L rows of k, v ([B, H, L, d]), e-major: [B, H, d + 1, M] with
+    state[e, m] = sum_j v_j[e] g(k_j)[m] for e < d and state[d, m] = sum_j g(k_j)[m]."""
+    k, v = _as4d(k), _as4d(v)
+    b, h, length, d = k.shape
+    _check_w(w, d)
+    m = d if w is None else int(np.shape(w)[1])
+    wf = None if w is None else _f64(w)
+    st = np.empty((b, h, d + 1, m), dtype=np.float64)
+    rc = _load().oracle_state(_ptr(k), _ptr(v), _ptr(wf), _ptr(st), b, h, length, d, m,
+                              MAP_ELU if w is None else MAP_FAVOR, int(threads))
+    if rc:
+        raise ValueError("oracle_state failed (%d)" % rc)
+    return st
+
+
+def decode_step(q, k, v, w, state):
+    """One new row per head: q, k, v [B, H, d]; state [B, H, d + 1, M] is
+    updated in place with the row's term (diagonal included), then
+    y = (g(q) . R) / (g(q) . S) is returned as [B, H, d]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if q.ndim != 3:
+        raise ValueError("q, k, v must be [B, H, d]")
+    b, h, d = q.shape
+    _check_w(w, d)
+    m = d if w is None else int(np.shape(w)[1])
+    if state.dtype != np.float64 or not state.flags.c_contiguous or state.shape != (b, h, d + 1, m):
+        raise ValueError("state must be a contiguous float64 [B, H, d + 1, M] array")
+    wf = None if w is None else _f64(w)
+    y = np.empty((b, h, d), dtype=np.float64)
+    rc = _load().oracle_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(wf), _ptr(state), _ptr(y), b, h, d, m,
+                               MAP_ELU if w is None else MAP_FAVOR)
+    if rc:
+        raise ValueError("oracle_decode failed (%d)" % rc)
+    return y
 
 
 def rel_l2(x, ref):

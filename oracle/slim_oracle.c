@@ -277,3 +277,75 @@ int oracle_max_threads(void) {
   return 1;
 #endif
 }
+
+/* Serving (autoregressive) form of the same recurrence, eq. (3)-(4) taken one
+ * row at a time.  A head's state is the stacked prefix sum R' = [R ; S^T]
+ * kept e-major: state[e][m] for e < d holds R[e][m] = sum_j v_j[e] g(k_j)[m],
+ * and state[d][m] holds S[m] = sum_j g(k_j)[m]; (d + 1) x M numbers per head,
+ * heads [B][H] contiguous.
+ *
+ * oracle_state: the state after the first L rows of k, v ([B][H][L][d]).
+ * Returns 0, or 1 on bad arguments, 2 on allocation failure. */
+int oracle_state(const double *k, const double *v, const double *W, double *state,
+                 long B, long H, long L, int d, int M, int map, int nthreads) {
+  if (check_args(B, H, L, d, M, map)) return 1;
+  set_threads(nthreads);
+  const long heads = B * H;
+  const size_t per = (size_t)(d + 1) * M;
+  int fail = 0;
+#pragma omp parallel for schedule(dynamic) reduction(| : fail)
+  for (long bh = 0; bh < heads; ++bh) {
+    double *st = state + (size_t)bh * per;
+    double *phi = (double *)malloc(sizeof(double) * (size_t)M);
+    if (!phi) {
+      fail |= 1;
+      continue;
+    }
+    memset(st, 0, sizeof(double) * per);
+    for (long j = 0; j < L; ++j) {
+      const double *kj = k + ((size_t)bh * L + j) * d, *vj = v + ((size_t)bh * L + j) * d;
+      feature_map(kj, d, W, M, map, phi);
+      for (int e = 0; e < d; ++e)
+        for (int m = 0; m < M; ++m) st[(size_t)e * M + m] += vj[e] * phi[m];
+      for (int m = 0; m < M; ++m) st[(size_t)d * M + m] += phi[m];
+    }
+    free(phi);
+  }
+  return fail ? 2 : 0;
+}
+
+/* oracle_decode: one new row per head (q, k, v, y are [B][H][d]): the state
+ * takes the row's term first (the diagonal j = l is included), then
+ * y = (g(q) . R) / (g(q) . S).  The state is updated in place. */
+int oracle_decode(const double *q, const double *k, const double *v, const double *W,
+                  double *state, double *y, long B, long H, int d, int M, int map) {
+  if (check_args(B, H, 1, d, M, map)) return 1;
+  const long heads = B * H;
+  const size_t per = (size_t)(d + 1) * M;
+  double *phq = (double *)malloc(sizeof(double) * (size_t)M);
+  double *phk = (double *)malloc(sizeof(double) * (size_t)M);
+  if (!phq || !phk) {
+    free(phq);
+    free(phk);
+    return 2;
+  }
+  for (long bh = 0; bh < heads; ++bh) {
+    double *st = state + (size_t)bh * per;
+    const double *qh = q + (size_t)bh * d, *kh = k + (size_t)bh * d, *vh = v + (size_t)bh * d;
+    feature_map(kh, d, W, M, map, phk);
+    feature_map(qh, d, W, M, map, phq);
+    for (int e = 0; e < d; ++e)
+      for (int m = 0; m < M; ++m) st[(size_t)e * M + m] += vh[e] * phk[m];
+    for (int m = 0; m < M; ++m) st[(size_t)d * M + m] += phk[m];
+    double den = 0.0;
+    for (int m = 0; m < M; ++m) den += phq[m] * st[(size_t)d * M + m];
+    for (int e = 0; e < d; ++e) {
+      double num = 0.0;
+      for (int m = 0; m < M; ++m) num += phq[m] * st[(size_t)e * M + m];
+      y[(size_t)bh * d + e] = num / den;
+    }
+  }
+  free(phq);
+  free(phk);
+  return 0;
+}

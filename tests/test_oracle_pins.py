@@ -249,3 +249,48 @@ def test_oracle_rejects_bad_arguments():
     q, k, v, _, _ = _rand(rng, 1, 1, 4, 4, 4, favor=False)
     with pytest.raises(ValueError):
         oracle.recurrence_forward(q[..., :3], k[..., :3], v[..., :3], np.zeros((4, 4)))
+
+
+# ---- serving form: a carried state, one new row at a time ------------------
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("favor", [True, False])
+def test_decode_chain_equals_quadratic_form(shape, favor):
+    """P-d1: decoding rows one by one from the zero state (eq. (3)-(4) per
+    step, diagonal included) reproduces every row of the eq. (2) quadratic form."""
+    b, h, length, d, m = shape
+    rng = np.random.default_rng(7 + hash((shape, favor)) % 2**32)
+    q, k, v, _, w = _rand(rng, b, h, length, d, m if favor else d, favor)
+    st = np.zeros((b, h, d + 1, m if favor else d))
+    ys = np.stack([oracle.decode_step(q[:, :, l], k[:, :, l], v[:, :, l], w, st) for l in range(length)], axis=2)
+    assert oracle.rel_l2(ys, quadratic.forward(q, k, v, w)) < 1e-12
+
+
+@pytest.mark.parametrize("favor", [True, False])
+def test_prefill_state_closed_form(favor):
+    """P-d2: the state after L rows is [V^T g(K) ; 1^T g(K)], computed here
+    with the numpy feature map and a matmul, independently of the C loops."""
+    rng = np.random.default_rng(11)
+    b, h, length, d, m = 2, 2, 13, 6, 10
+    _, k, v, _, w = _rand(rng, b, h, length, d, m if favor else d, favor)
+    st = oracle.prefill_state(k, v, w)
+    phk = quadratic.feature_map(k, w)
+    ref_r = np.einsum("bhle,bhlm->bhem", v, phk)
+    ref_s = phk.sum(axis=2)
+    assert np.allclose(st[:, :, :d], ref_r, rtol=1e-13, atol=1e-13)
+    assert np.allclose(st[:, :, d], ref_s, rtol=1e-13, atol=1e-13)
+    assert np.all(oracle.prefill_state(k[:, :, :0], v[:, :, :0], w) == 0.0)
+
+
+@pytest.mark.parametrize("favor", [True, False])
+def test_prefill_then_decode_is_the_next_row(favor):
+    """P-d3: prefill over rows < l, then one decode step with row l, gives
+    Y_l of the quadratic form (the state carries exactly the rows before l)."""
+    rng = np.random.default_rng(12)
+    b, h, length, d, m = 1, 3, 20, 8, 16
+    q, k, v, _, w = _rand(rng, b, h, length, d, m if favor else d, favor)
+    y_quad = quadratic.forward(q, k, v, w)
+    for l in (0, 1, 19):
+        st = oracle.prefill_state(k[:, :, :l], v[:, :, :l], w)
+        y = oracle.decode_step(q[:, :, l], k[:, :, l], v[:, :, l], w, st)
+        assert np.allclose(y, y_quad[:, :, l], rtol=1e-12, atol=1e-12)
