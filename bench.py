@@ -465,6 +465,64 @@ def run_native(args, wl):
     return 0
 
 
+def run_decode(args, wl):
+    """Serving step: one new row for every (sequence, head), against a state
+    carried in HBM (fp32 [B][H][d + 1][M]); B sequences of H heads decode one
+    token each per step.  The state (2 x 136 MB read and written per step at
+    128 x 16 heads, d = 64, M = 256) is larger than L2, so no flush is needed."""
+    import torch
+    from sub_linear_memory_gb300 import binding, inputs
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    b, h, d, m = wl.B, wl.H, wl.d, wl.M
+    dtype = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    g = torch.Generator(device="cpu").manual_seed(4321)
+    nsteps = args.warmup + args.steps
+    scale = 1.0 if wl.feature == "elu" else d ** -0.25
+    qkv = (torch.randn((3, nsteps, b, h, d), generator=g) * torch.tensor([scale, scale, 1.0]).view(3, 1, 1, 1, 1))
+    qkv = qkv.to(dev, dtype).contiguous()
+    _, _, _, _, w = inputs.make_inputs(wl.with_(B=1, H=1, L=1))
+    w = None if w is None else w.to(dev)
+    # prompt: a short prefill, so the state holds realistic magnitudes
+    kp = (torch.randn((b, h, 256, d), generator=g) * scale).to(dev, dtype)
+    vp = torch.randn((b, h, 256, d), generator=g).to(dev, dtype)
+    state = binding.slim_attn_state(kp, vp, w, wl.chunk)
+    y = torch.empty((b, h, d), dtype=dtype, device=dev)
+    del kp, vp
+    for i in range(args.warmup):
+        binding.slim_attn_decode(qkv[0, i], qkv[1, i], qkv[2, i], w, state, y)
+    binding.sync_status()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        e0.record()
+        for i in range(args.warmup, nsteps):
+            binding.slim_attn_decode(qkv[0, i], qkv[1, i], qkv[2, i], w, state, y)
+        e1.record()
+        torch.cuda.synchronize()
+    binding.sync_status()
+    ms = e0.elapsed_time(e1) / args.steps
+    s_io = 2 if dtype == torch.bfloat16 else 4
+    nbytes = 2 * b * h * (d + 1) * m * 4 + 4 * b * h * d * s_io + (0 if w is None else d * m * 4)
+    peaks = load_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out = {
+        "metric": "decode tokens/s (one new row for each of B sequences, all heads)",
+        "value": b * 1e3 / ms, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp32 state, %s I/O" % wl.dtype, "data": "synthetic (seeded Gaussian rows, prefill of 256 rows)",
+        "config": {"workload": "decode (%s head shape)" % wl.name, "B": b, "H": h, "d": d, "M": m,
+                   "feature": wl.feature, "l2": "state larger than L2, no flush"},
+        "clocks": clk.summary(), "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": "decode",
+                     "bytes_per_step": nbytes},
+    }
+    print(json.dumps(out))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -479,6 +537,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-row-frac", type=float, default=1.0,
                     help="fraction of the rows the CPU-baseline sample covers")
+    ap.add_argument("--decode", action="store_true",
+                    help="time the serving decode step instead (B defaults to 128 sequences)")
     ap.add_argument("--ref-row-frac", type=float, default=0.125,
                     help="fraction of the rows each reference-arm step covers")
     args = ap.parse_args(argv)
@@ -490,6 +550,10 @@ def main(argv=None):
     if args.heads:
         b, h = (int(x) for x in args.heads.lower().split("x"))
         wl = wl.with_(B=b, H=h)
+    if args.decode:
+        if not args.heads:
+            wl = wl.with_(B=128)
+        return run_decode(args, wl)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_native(args, wl)

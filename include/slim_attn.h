@@ -128,6 +128,35 @@ slim_status slim_attn_fwd_noalloc(const void *q, const void *k, const void *v, c
                                   void *y, int B, int H, int L, int d, int M, int chunk,
                                   slim_stream_t stream);
 
+/* Serving form (section 2.1: eq. (3)-(4) run one row at a time; row l needs
+ * only the state of the rows before it).  A head's state is the stacked
+ * prefix sum R' = [R ; S^T] after some rows j, fp32, e-major, heads
+ * contiguous: state is [B][H][d + 1][M] with
+ *     state[b][h][e][m] = sum_j v_j[e] g(k_j)[m]   (e < d),
+ *     state[b][h][d][m] = sum_j g(k_j)[m].
+ * The caller owns it; nothing else is kept between calls.
+ *
+ * slim_attn_state: the state after all L rows of k, v ([B][H][L][d], bf16
+ * or, for _f32, fp32); overwrites `state` (zero for L = 0).  Takes the
+ * forward's workspace (slim_attn_workspace_bytes(..., 0)) and chunk.
+ * Summed in fp32 per 128-row tile (tensor path) or per slice, segment
+ * totals combined in double-float (tensor) or fp64 (CUDA-core path). */
+slim_status slim_attn_state(const void *k, const void *v, const float *w, float *state, int B, int H, int L,
+                            int d, int M, int chunk, slim_stream_t stream);
+slim_status slim_attn_state_f32(const float *k, const float *v, const float *w, float *state, int B, int H,
+                                int L, int d, int M, int chunk, slim_stream_t stream);
+
+/* slim_attn_decode: one new row per head.  q, k, v: [B][H][d] (bf16, or fp32
+ * for _f32); w as for the forward.  The state takes the new row's term first
+ * (the diagonal is included), then y = (g(q) . R) / (g(q) . S) is written to
+ * y ([B][H][d]).  Starting from slim_attn_state over rows 0 .. l-1, the
+ * decode of row l gives row l of slim_attn_fwd (to rounding).  No workspace;
+ * one CTA per head, fp32 arithmetic. */
+slim_status slim_attn_decode(const void *q, const void *k, const void *v, const float *w, float *state, void *y,
+                             int B, int H, int d, int M, slim_stream_t stream);
+slim_status slim_attn_decode_f32(const float *q, const float *k, const float *v, const float *w, float *state,
+                                 float *y, int B, int H, int d, int M, slim_stream_t stream);
+
 /* Bytes of workspace slim_attn_fwd (is_bwd = 0) or slim_attn_bwd (is_bwd = 1)
  * need for this shape on the current device (either I/O type).  0 for an
  * unsupported shape or an empty problem. */

@@ -27,7 +27,12 @@ _lib.slim_attn_fwd.argtypes = [_vp] * 5 + [_i] * 6 + [_vp]
 _lib.slim_attn_fwd_f32.argtypes = _lib.slim_attn_fwd.argtypes
 _lib.slim_attn_bwd.argtypes = [_vp] * 9 + [_i] * 6 + [_vp]
 _lib.slim_attn_bwd_f32.argtypes = _lib.slim_attn_bwd.argtypes
-for _f in (_lib.slim_attn_fwd, _lib.slim_attn_fwd_f32, _lib.slim_attn_bwd, _lib.slim_attn_bwd_f32):
+_lib.slim_attn_state.argtypes = [_vp] * 4 + [_i] * 6 + [_vp]
+_lib.slim_attn_state_f32.argtypes = _lib.slim_attn_state.argtypes
+_lib.slim_attn_decode.argtypes = [_vp] * 6 + [_i] * 4 + [_vp]
+_lib.slim_attn_decode_f32.argtypes = _lib.slim_attn_decode.argtypes
+for _f in (_lib.slim_attn_fwd, _lib.slim_attn_fwd_f32, _lib.slim_attn_bwd, _lib.slim_attn_bwd_f32,
+           _lib.slim_attn_state, _lib.slim_attn_state_f32, _lib.slim_attn_decode, _lib.slim_attn_decode_f32):
     _f.restype = _i
 _lib.slim_attn_workspace_bytes.argtypes = [_i] * 7
 _lib.slim_attn_workspace_bytes.restype = _sz
@@ -54,6 +59,7 @@ OPT_PATH = 2
 OPT_PROFILE = 3
 EXPORTED = (
     "slim_attn_fwd", "slim_attn_bwd", "slim_attn_fwd_f32", "slim_attn_bwd_f32",
+    "slim_attn_state", "slim_attn_state_f32", "slim_attn_decode", "slim_attn_decode_f32",
     "slim_attn_workspace_bytes", "slim_attn_set_workspace", "slim_attn_set_option",
     "slim_attn_segments", "slim_attn_sync_status", "slim_status_string",
     "slim_attn_profile_count", "slim_attn_profile_get", "slim_attn_profile_reset",
@@ -186,6 +192,40 @@ def slim_attn_bwd(q, k, v, w, dy, chunk, want_dw=False, out=None):
     _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(dy), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dw),
               b, h, length, d, m, chunk, _vp(stream)), "slim_attn_bwd")
     return dq, dk, dv, dw
+
+
+def slim_attn_state(k, v, w, chunk, state=None):
+    """The serving state after all L rows of k, v ([B, H, L, d]): fp32
+    [B, H, d + 1, M], rows e < d = sum_j v_j[e] g(k_j), row d = sum_j g(k_j)."""
+    b, h, length, d, m = _validate(k, v, v, w)
+    if state is None:
+        state = torch.empty((b, h, d + 1, m), dtype=torch.float32, device=k.device)
+    if state.shape != (b, h, d + 1, m) or state.dtype != torch.float32 or not state.is_contiguous():
+        raise ValueError("state must be a contiguous fp32 [B, H, d + 1, M] tensor")
+    _prepare((b, h, max(length, 1), d, m, chunk), False, k.device)
+    fn = _lib.slim_attn_state if k.dtype == torch.bfloat16 else _lib.slim_attn_state_f32
+    stream = torch.cuda.current_stream(k.device).cuda_stream
+    _check(fn(_ptr(k), _ptr(v), _ptr(w), _ptr(state), b, h, length, d, m, chunk, _vp(stream)), "slim_attn_state")
+    return state
+
+
+def slim_attn_decode(q, k, v, w, state, y=None):
+    """One new row per head: q, k, v [B, H, d]; ``state`` (fp32 [B, H, d + 1, M])
+    takes the row's term in place; returns y [B, H, d] in q's dtype."""
+    if q.dim() != 3:
+        raise ValueError("q, k, v must be [B, H, d]")
+    b, h, d = q.shape
+    b2, h2, l2, d2, m = _validate(q.unsqueeze(2), k.unsqueeze(2), v.unsqueeze(2), w)
+    if state.shape != (b, h, d + 1, m) or state.dtype != torch.float32 or not state.is_contiguous() \
+            or state.device != q.device:
+        raise ValueError("state must be a contiguous fp32 [B, H, d + 1, M] tensor on q's device")
+    if y is None:
+        y = torch.empty_like(q)
+    fn = _lib.slim_attn_decode if q.dtype == torch.bfloat16 else _lib.slim_attn_decode_f32
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(state), _ptr(y), b, h, d, m, _vp(stream)),
+           "slim_attn_decode")
+    return y
 
 
 def raw():

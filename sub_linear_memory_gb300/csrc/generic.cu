@@ -638,6 +638,36 @@ cudaError_t scan_states_f32_rev(const Plan &p, float *states, int nseg, cudaStre
   return cudaGetLastError();
 }
 
+namespace gen {
+// The last segment's inclusive state (fp64 e-major [dp][M]) -> fp32 [BH][dp][M].
+__global__ void last_state_f32_kernel(Plan p, const double *states, float *out) {
+  const size_t per = (size_t)p.dp * p.M, n = (size_t)p.BH * per;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t bh = i / per, r = i - bh * per;
+    out[i] = (float)states[(bh * p.P + (p.P - 1)) * per + r];
+  }
+}
+}  // namespace gen
+
+template <typename T>
+cudaError_t generic_prefill_state(const Plan &p, const Args &a, float *state, cudaStream_t st) {
+  {
+    ProfScope ps("gen_segment_state", st);
+    gen::segment_state_kernel<T><<<dim3(p.P, p.BH), gen::kThreads, 0, st>>>(p, a);
+  }
+  if (p.P > 1) {
+    ProfScope ps("gen_scan_states", st);
+    gen::scan_states_kernel<<<scan_blocks(p), 256, 0, st>>>(p, reinterpret_cast<double *>(a.ws + p.states_off), p.P,
+                                                            0);
+  }
+  const size_t n = (size_t)p.BH * p.dp * p.M;
+  gen::last_state_f32_kernel<<<(int)std::min<size_t>((n + 255) / 256, 4096), 256, 0, st>>>(
+      p, reinterpret_cast<const double *>(a.ws + p.states_off), state);
+  return cudaGetLastError();
+}
+
+template cudaError_t generic_prefill_state<float>(const Plan &, const Args &, float *, cudaStream_t);
+template cudaError_t generic_prefill_state<__nv_bfloat16>(const Plan &, const Args &, float *, cudaStream_t);
 template cudaError_t generic_forward<float>(const Plan &, const Args &, cudaStream_t);
 template cudaError_t generic_forward<__nv_bfloat16>(const Plan &, const Args &, cudaStream_t);
 template cudaError_t generic_backward<float>(const Plan &, const Args &, cudaStream_t);

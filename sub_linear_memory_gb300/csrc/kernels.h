@@ -49,6 +49,14 @@ cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, bool zero_
 // kernel and the reverse scan of the segment G totals).
 cudaError_t tc_correction(const Plan &p, const Args &a, cudaStream_t st);
 
+// Serving form (decode.cu, generic.cu): the state after L rows, fp32
+// e-major [BH][d + 1][M], and one decode step for every head.
+template <typename T> cudaError_t generic_prefill_state(const Plan &p, const Args &a, float *state, cudaStream_t st);
+cudaError_t tc_prefill_state(const Plan &p, const Args &a, float *state, cudaStream_t st);
+template <typename T>
+cudaError_t decode_step(const void *q, const void *k, const void *v, const float *w, float *state, void *y, int BH,
+                        int d, int M, cudaStream_t st);
+
 // Tensor-core SLiM backward (tc_backward.cu): bf16 I/O, d = 64, M <= 128.
 bool tc_backward_supported(int d, int M, int chunk, bool favor);
 cudaError_t tc_backward(const Plan &p, const Args &a, cudaStream_t st);

@@ -191,6 +191,49 @@ slim_status run(bool bwd, const void *q, const void *k, const void *v, const flo
   return err == cudaSuccess ? SLIM_OK : SLIM_ERR_CUDA;
 }
 
+// State after all L rows of k, v (serving prefill), into the caller's fp32
+// [B][H][d + 1][M] e-major buffer.
+template <typename T>
+slim_status run_state(const void *k, const void *v, const float *w, float *state, int B, int H, int L, int d,
+                      int M, int chunk, cudaStream_t stream) {
+  const bool favor = w != nullptr;
+  slim_status st = check_shape(B, H, L, d, M, chunk, favor);
+  if (st != SLIM_OK) return st;
+  if ((long long)B * H == 0) return SLIM_OK;
+  if (!state) return SLIM_ERR_INVALID_ARG;
+  if (L == 0) {
+    const size_t bytes = sizeof(float) * (size_t)B * H * (d + 1) * M;
+    return cudaMemsetAsync(state, 0, bytes, stream) == cudaSuccess ? SLIM_OK : SLIM_ERR_CUDA;
+  }
+  if (!k || !v) return SLIM_ERR_INVALID_ARG;
+  const bool tc = sizeof(T) == 2 && g_opt_path != 1 && aligned16(k) && aligned16(v) &&
+                  tc_forward_supported(d, M, chunk, favor);
+  Plan p = make_plan(B, H, L, d, M, chunk, favor, false, false, tc ? 2 : 1);
+  Args a{};
+  a.k = k; a.v = v; a.w = w;
+  if (cudaGetSymbolAddress((void **)&a.status, g_device_status) != cudaSuccess) return SLIM_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_ws || g_ws_bytes < p.total_floats * sizeof(float)) return SLIM_ERR_WORKSPACE;
+    a.ws = static_cast<float *>(g_ws);
+  }
+  cudaError_t err = tc ? tc_prefill_state(p, a, state, stream) : generic_prefill_state<T>(p, a, state, stream);
+  return err == cudaSuccess ? SLIM_OK : SLIM_ERR_CUDA;
+}
+
+// One new row per head against the carried state.
+template <typename T>
+slim_status run_decode(const void *q, const void *k, const void *v, const float *w, float *state, void *y, int B,
+                       int H, int d, int M, cudaStream_t stream) {
+  const bool favor = w != nullptr;
+  slim_status st = check_shape(B, H, 1, d, M, 64, favor);
+  if (st != SLIM_OK) return st;
+  if ((long long)B * H == 0) return SLIM_OK;
+  if (!q || !k || !v || !state || !y) return SLIM_ERR_INVALID_ARG;
+  const cudaError_t err = decode_step<T>(q, k, v, w, state, y, B * H, d, M, stream);
+  return err == cudaSuccess ? SLIM_OK : SLIM_ERR_CUDA;
+}
+
 }  // namespace
 
 // Accessors for entry points that live in other translation units.
@@ -231,6 +274,8 @@ ProfScope::~ProfScope() {
 }  // namespace slim
 
 using slim::run;
+using slim::run_decode;
+using slim::run_state;
 
 extern "C" {
 
@@ -259,6 +304,26 @@ slim_status slim_attn_bwd_f32(const float *q, const float *k, const float *v, co
                               int H, int L, int d, int M, int chunk, slim_stream_t stream) {
   return run<float>(true, q, k, v, w, dy, nullptr, dq, dk, dv, dw, B, H, L, d, M, chunk,
                     (cudaStream_t)stream);
+}
+
+slim_status slim_attn_state(const void *k, const void *v, const float *w, float *state, int B, int H, int L,
+                            int d, int M, int chunk, slim_stream_t stream) {
+  return run_state<__nv_bfloat16>(k, v, w, state, B, H, L, d, M, chunk, (cudaStream_t)stream);
+}
+
+slim_status slim_attn_state_f32(const float *k, const float *v, const float *w, float *state, int B, int H,
+                                int L, int d, int M, int chunk, slim_stream_t stream) {
+  return run_state<float>(k, v, w, state, B, H, L, d, M, chunk, (cudaStream_t)stream);
+}
+
+slim_status slim_attn_decode(const void *q, const void *k, const void *v, const float *w, float *state, void *y,
+                             int B, int H, int d, int M, slim_stream_t stream) {
+  return run_decode<__nv_bfloat16>(q, k, v, w, state, y, B, H, d, M, (cudaStream_t)stream);
+}
+
+slim_status slim_attn_decode_f32(const float *q, const float *k, const float *v, const float *w, float *state,
+                                 float *y, int B, int H, int d, int M, slim_stream_t stream) {
+  return run_decode<float>(q, k, v, w, state, y, B, H, d, M, (cudaStream_t)stream);
 }
 
 size_t slim_attn_workspace_bytes(int B, int H, int L, int d, int M, int chunk, int is_bwd) {

@@ -88,3 +88,22 @@ def test_workspace_does_not_grow_with_sequence_length(lib):
     assert sizes[0] > 0 and sizes[0] == sizes[1] == sizes[2]
     # an L x d x M prefix-sum tensor at L = 2^20 would be 8 GiB per head-group
     assert sizes[2] < (1 << 30)
+
+
+def test_state_and_decode_reject_bad_arguments_before_any_launch(lib):
+    vp = ctypes.c_void_p
+    dummy = vp(256)
+    # decode: d, M outside the supported set; elu+1 needs M == d; NULL buffers
+    assert lib.slim_attn_decode(dummy, dummy, dummy, dummy, dummy, dummy, 1, 1, 48, 64, None) == 2
+    assert lib.slim_attn_decode(dummy, dummy, dummy, dummy, dummy, dummy, 1, 1, 64, 40, None) == 2
+    assert lib.slim_attn_decode(dummy, dummy, dummy, None, dummy, dummy, 1, 1, 64, 128, None) == 1
+    assert lib.slim_attn_decode(None, dummy, dummy, dummy, dummy, dummy, 1, 1, 64, 64, None) == 1
+    assert lib.slim_attn_decode(dummy, dummy, dummy, dummy, None, dummy, 1, 1, 64, 64, None) == 1
+    assert lib.slim_attn_decode_f32(dummy, dummy, dummy, dummy, dummy, dummy, -1, 1, 64, 64, None) == 1
+    # no heads: nothing to do
+    assert lib.slim_attn_decode(dummy, dummy, dummy, dummy, dummy, dummy, 0, 4, 64, 64, None) == 0
+    # state: shape checks as for the forward; NULL state
+    assert lib.slim_attn_state(dummy, dummy, dummy, dummy, 1, 1, 64, 48, 64, 32, None) == 2
+    assert lib.slim_attn_state(dummy, dummy, dummy, dummy, 1, 1, 64, 64, 64, 48, None) == 2
+    assert lib.slim_attn_state(dummy, dummy, dummy, None, 1, 1, 64, 64, 64, 32, None) == 1
+    assert lib.slim_attn_state_f32(dummy, dummy, None, dummy, 1, 1, 64, 64, 128, 32, None) == 1
