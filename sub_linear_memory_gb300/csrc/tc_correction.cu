@@ -12,12 +12,15 @@
 // independent here, so they are dealt out as flat (head, tile) units to one
 // CTA per SM.
 //
-// Warp roles, as in the forward: warp 0 streams K and V (and the bf16 image
-// of G_end when the unit's segment changes) into shared memory, warp 1 issues
-// the MMAs, warps 2-9 run the epilogues, two threads per row.  The epilogue
-// stages each unit's bf16 increments of dK and dV in that unit's K and V
-// slots, and warp 0 adds them to dK and dV with TMA reduce-add copies before
-// it reuses the slots, so no global read sits in the epilogue.  Every
+// Roles (16 warps): warp 0 streams K and V (and the bf16 image of G_end when
+// the unit's segment changes) into shared memory and adds each unit's staged
+// increments to dK and dV with TMA reduce-adds before it reuses the slots;
+// warps 1, 2 and 3 issue the MMAs (F = K W and D = V G_V^T in 64-feature jobs
+// through two TMEM buffers each; dV' and dK' per 128-feature block); warps
+// 4-11 turn each job into phi_k and u (two threads per row, 32 columns each);
+// warps 12-15 finish the unit: dK = dK' - k rowsum(u), both increments to
+// bf16 in the unit's own K and V slots.  (Reading the backward's rows, adding
+// and writing them back from the tail warps instead measured slower.)  Every
 // hand-off is an mbarrier with a bounded wait.
 #include <cuda.h>
 
@@ -35,9 +38,9 @@ using namespace slim::tc;
 
 constexpr int kTile = 128;
 constexpr int D = 64;
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
-constexpr int kSlots = 4;  // K, V of two units in flight
+constexpr int kWarps = 16;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kSlots = 4;  // K, V of two units in flight (K in even slots, V in odd)
 constexpr uint32_t kTileBytes = kTile * D * 2;
 
 struct Params {
@@ -52,28 +55,27 @@ struct Params {
 enum {
   B_FULL = 0,       // [4] TMA -> consumers
   B_EMPTY = 4,      // [4] MMAs done with the slot
-  B_FFULL = 8,      // [2] F ready
-  B_FEMPTY = 10,    // [2] F read out
-  B_DFULL = 12,     // V G_V^T ready
-  B_DEMPTY = 13,    // V G_V^T read out
-  B_PHK = 14,       // phi_k block stored
-  B_PHFREE = 15,    // dV' MMA done with the phi_k block
-  B_U = 16,         // u block stored
-  B_UFREE = 17,     // dK' MMA done with the u block
-  B_OUTFULL = 18,   // dV', dK' complete
-  B_OUTEMPTY = 19,  // dV', dK' read out
-  B_GFULL = 20,     // G_end image landed
-  B_GEMPTY = 21,    // G_end image no longer read (1 MMA commit + 8 epilogue warps)
-  B_WFULL = 22,     // W image landed
-  B_EPI = 23,       // epilogue warps' row-sum halves written
-  B_DONE = 24,
-  B_STG = 25,       // [2] a unit's dK, dV increments staged in its slots (by unit parity)
-  B_COUNT = 27
+  B_FFULL = 8,      // [2] feature job in TMEM buffer b
+  B_FEMPTY = 10,    // [2] ... read out (8 warps)
+  B_DFULL = 12,     // [2] V G_V^T job in TMEM buffer b
+  B_DEMPTY = 14,    // [2] ... read out (8 warps)
+  B_PHK = 16,       // phi_k block stored (8 warps)
+  B_PHFREE = 17,    // dV' MMAs done with the phi_k block
+  B_U = 18,         // u block stored (8 warps)
+  B_UFREE = 19,     // dK' MMAs done with the u block
+  B_OUTFULL = 20,   // dV', dK' complete
+  B_OUTEMPTY = 21,  // dV', dK' read out (4 warps)
+  B_GFULL = 22,     // G_end image landed
+  B_GEMPTY = 23,    // G_end image no longer read (2 MMA commits + 8 warps)
+  B_WFULL = 24,     // W image landed
+  B_EPI = 25,       // [2] row sums of u written (8 warps), by unit parity
+  B_STG = 27,       // [2] a unit's dK, dV increments staged in its slots (4 + 8 warps)
+  B_DONE = 29,      // [3] MMA drain of each issuing thread
+  B_COUNT = 32
 };
 
 template <int M>
 struct Layout {
-  static constexpr bool kFavor = true;
   uint32_t w, slots, g, gs, phk, ub, usum, bars, total;
   __host__ __device__ Layout() {
     uint32_t o = 0;
@@ -84,20 +86,21 @@ struct Layout {
     o = (o + 1023u) & ~1023u;
     phk = o; o += kTile * 128 * 2;
     ub = o; o += kTile * 128 * 2;
-    usum = o; o += 2 * 2 * kTile * 4;  // [unit parity][half][row]
+    usum = o; o += 2 * 2 * kTile * 4;  // [unit parity][part][row]
     bars = o; o += 8 * B_COUNT + 16;
     total = o;
   }
 };
 
-// TMEM columns
-constexpr uint32_t kF0 = 0, kF1 = 128, kDc = 256, kDV = 384, kDK = 448;
+// TMEM columns: F jobs 2 x 64 | D jobs 2 x 64 | dV' 64 | dK' 64
+constexpr uint32_t kF = 0, kDc = 128, kDV = 256, kDK = 320;
 
 template <bool FAVOR, int M>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_corr_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV, Params p) {
-  constexpr int nb = (M + 127) / 128, FB = M < 128 ? M : 128, FC = FB / 2;
+  constexpr int nb = (M + 127) / 128, FB = M < 128 ? M : 128;
+  constexpr int JT = M / 64;  // 64-feature jobs per unit (F and D alike)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem =
       reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -147,23 +150,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar + B_FFULL + b, 1);
-      mbar_init(bar + B_FEMPTY + b, kEpiWarps);
+      mbar_init(bar + B_FEMPTY + b, 8);
+      mbar_init(bar + B_DFULL + b, 1);
+      mbar_init(bar + B_DEMPTY + b, 8);
+      mbar_init(bar + B_EPI + b, 8);
+      mbar_init(bar + B_STG + b, 12);
     }
-    mbar_init(bar + B_DFULL, 1);
-    mbar_init(bar + B_DEMPTY, kEpiWarps);
-    mbar_init(bar + B_PHK, kEpiWarps);
+    mbar_init(bar + B_PHK, 8);
     mbar_init(bar + B_PHFREE, 1);
-    mbar_init(bar + B_U, kEpiWarps);
+    mbar_init(bar + B_U, 8);
     mbar_init(bar + B_UFREE, 1);
     mbar_init(bar + B_OUTFULL, 1);
-    mbar_init(bar + B_OUTEMPTY, kEpiWarps);
+    mbar_init(bar + B_OUTEMPTY, 4);
     mbar_init(bar + B_GFULL, 1);
-    mbar_init(bar + B_GEMPTY, 1 + kEpiWarps);
+    mbar_init(bar + B_GEMPTY, 10);
     mbar_init(bar + B_WFULL, 1);
-    mbar_init(bar + B_EPI, kEpiWarps);
-    mbar_init(bar + B_DONE, 1);
-    mbar_init(bar + B_STG, kEpiWarps);
-    mbar_init(bar + B_STG + 1, kEpiWarps);
+    for (int k = 0; k < 3; ++k) mbar_init(bar + B_DONE + k, 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tmK);
@@ -181,15 +183,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_w = sbase + lay.w, s_g = sbase + lay.g, s_phk = sbase + lay.phk, s_ub = sbase + lay.ub;
   auto slot_addr = [&](int n) { return sbase + lay.slots + (uint32_t)(n % kSlots) * kTileBytes; };
   auto slot_par = [&](int n) { return (uint32_t)((n / kSlots) & 1); };
+  bool ok = true;
+  auto wait = [&](int b, uint32_t par) {
+    if (ok) ok = mbar_wait(bar + b, par, p.status, abort_flag);
+    return ok;
+  };
+  auto arrive = [&](int b) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar + b);
+  };
+  const int q4 = warp & 3, row = 32 * q4 + lane;
+  const uint32_t lane_base = 32u * q4;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       int n = 0, keys = 0;
-      bool ok = true;
       auto load = [&](const CUtensorMap *m, int t, int bh) {
         const int s = n % kSlots, u = n / kSlots;
-        if (u > 0 && !mbar_wait(bar + B_EMPTY + s, (u - 1) & 1, p.status, abort_flag)) return false;
+        if (u > 0 && !wait(B_EMPTY + s, (u - 1) & 1)) return false;
         mbar_arrive_expect_tx(bar + B_FULL + s, kTileBytes);
         tma_load_3d(smem + lay.slots + s * kTileBytes, m, bar + B_FULL + s, 0, t * kTile, bh);
         ++n;
@@ -197,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // unit j's staged increments -> dK, dV; returns once its slots are read
       auto flush = [&](int j, const Cursor &c) {
-        if (!mbar_wait(bar + B_STG + (j & 1), (j >> 1) & 1, p.status, abort_flag)) return false;
+        if (!wait(B_STG + (j & 1), (j >> 1) & 1)) return false;
         tma_reduce_add_3d(&tmDV, slot_addr(2 * j + 1), 0, c.t * kTile, c.bh);
         tma_reduce_add_3d(&tmDK, slot_addr(2 * j), 0, c.t * kTile, c.bh);
         tma_store_commit();
@@ -207,12 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       Cursor cur = first, prev1 = first, prev2 = first;  // units i, i-1, i-2
       for (int i = 0; i < nun && ok; ++i) {
         if (i >= 2 && !flush(i - 2, prev2)) break;  // unit i takes unit i-2's slots
-        // K and V first: the MMA warp issues this unit's F early, before it
-        // releases the previous G_end
-        ok = load(&tmK, cur.t, cur.bh) && load(&tmV, cur.t, cur.bh);
-        if (ok && new_key(i, cur)) {
+        if (!load(&tmK, cur.t, cur.bh) || !load(&tmV, cur.t, cur.bh)) break;
+        if (new_key(i, cur)) {
           // the previous G_end is no longer read once its last unit is done
-          if (keys > 0 && !mbar_wait(bar + B_GEMPTY, (keys - 1) & 1, p.status, abort_flag)) break;
+          if (keys > 0 && !wait(B_GEMPTY, (keys - 1) & 1)) break;
           mbar_arrive_expect_tx(bar + B_GFULL, grec_bytes);
           bulk_load(smem + lay.g, p.grec + (size_t)(cur.bh * p.P + cur.seg) * grec_bytes, grec_bytes, bar + B_GFULL);
           ++keys;
@@ -222,222 +232,216 @@ __global__ void __launch_bounds__(kThreads, 1)
         advance(cur);
       }
       // the last two units (prev2 = unit nun-2, prev1 = unit nun-1)
-      if (ok && nun >= 2) ok = flush(nun - 2, prev2);
-      if (ok && nun >= 1) ok = flush(nun - 1, prev1);
+      if (ok && nun >= 2) flush(nun - 2, prev2);
+      if (ok && nun >= 1) flush(nun - 1, prev1);
       tma_store_wait_all();
       for (int m = max(0, n - kSlots); m < n; ++m) mbar_drain(bar + B_FULL + m % kSlots, slot_par(m));
       if (keys > 0) mbar_drain(bar + B_GFULL, (keys - 1) & 1);
       if (FAVOR) mbar_drain(bar + B_WFULL, 0);
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      bool ok = true;
-      auto wait = [&](int b, uint32_t par) {
-        if (ok) ok = mbar_wait(bar + b, par, p.status, abort_flag);
-        return ok;
-      };
-      const uint32_t id_f = make_idesc(128, FB, false, false);
+  } else if (warp < 4) {
+    // ---------------------------------------------------------------- MMA issuers
+    if (lane == 0 && (FAVOR || warp != 1)) {
+      const uint32_t id64 = make_idesc(128, 64, false, false);
       const uint32_t id_o = make_idesc(128, D, false, true);
-      if (FAVOR) wait(B_WFULL, 0);
-      int fj = 0, dj = 0, keys = 0;
-      // F = K W_h of unit j: issued one unit ahead, while unit j-1's later
-      // MMAs run, so the epilogue finds it ready when it starts unit j
-      auto f_job = [&](int j, int h) {
-        const int nK = 2 * j;
-        if (h == 0 && !wait(B_FULL + nK % kSlots, slot_par(nK))) return;
-        const int b = fj & 1, use = fj >> 1;
-        if (use > 0 && !wait(B_FEMPTY + b, (use - 1) & 1)) return;
-        tc_fence_after();
-        for (int s = 0; s < D / 16; ++s)
-          mma_bf16(tbase + (b ? kF1 : kF0), desc_kmajor(slot_addr(nK), kTile, 0, s), desc_kmajor(s_w, M, 128 * h, s),
-                   id_f, s > 0);
-        mma_commit(bar + B_FFULL + b);
-        ++fj;
-      };
-      if (FAVOR && nun > 0)
-        for (int h = 0; h < nb && ok; ++h) f_job(0, h);
-      Cursor cur = first;
-      for (int i = 0; i < nun && ok; ++i, advance(cur)) {
-        const int nK = 2 * i, nV = 2 * i + 1;
-        const uint32_t s_v = slot_addr(nV);
-        if (new_key(i, cur)) {
-          if (!wait(B_GFULL, keys & 1)) break;
-          ++keys;
-        }
-        if (!wait(B_FULL + nK % kSlots, slot_par(nK))) break;
-        if (!wait(B_FULL + nV % kSlots, slot_par(nV))) break;
-        tc_fence_after();
-        for (int h = 0; h < nb && ok; ++h) {
-          // V G_V,h^T
-          if (dj > 0 && !wait(B_DEMPTY, (dj - 1) & 1)) break;
+      auto ks = [](int s, uint32_t rows) { return (uint64_t)((s >> 2) * rows * 8u + (s & 3) * 2u); };
+      if (warp == 1) {
+        // F = K W: job j = features [64 (j % JT), +64) of unit j / JT into buffer j & 1
+        wait(B_WFULL, 0);
+        const uint64_t d_w0 = desc_kmajor(s_w, M, 0, 0);
+        for (int j = 0; j < nun * JT && ok; ++j) {
+          const int i = j / JT, jj = j - i * JT, nK = 2 * i;
+          if (j >= 2 && !wait(B_FEMPTY + (j & 1), ((j >> 1) - 1) & 1)) break;
+          if (jj == 0 && !wait(B_FULL + nK % kSlots, slot_par(nK))) break;
           tc_fence_after();
+          const uint64_t dx = desc_kmajor(slot_addr(nK), kTile, 0, 0), dw = d_w0 + (uint64_t)(jj * 512);
+#pragma unroll
           for (int s = 0; s < D / 16; ++s)
-            mma_bf16(tbase + kDc, desc_kmajor(s_v, kTile, 0, s), desc_kmajor(s_g, M, 128 * h, s), id_f, s > 0);
-          mma_commit(bar + B_DFULL);
-          ++dj;
+            mma_bf16(tbase + kF + 64 * (j & 1), dx + ks(s, kTile), dw + ks(s, M), id64, s > 0);
+          mma_commit(bar + B_FFULL + (j & 1));
+          if (jj == JT - 1) mma_commit(bar + B_EMPTY + nK % kSlots);
         }
-        if (!ok) break;
-        mma_commit(bar + B_EMPTY + nK % kSlots);  // K's last reader (F of this unit) was issued earlier
-        mma_commit(bar + B_EMPTY + nV % kSlots);
-        for (int h = 0; h < nb && ok; ++h) {
-          const uint32_t c = (uint32_t)(i * nb + h);
-          if (!wait(B_PHK, c & 1)) break;
-          if (h == 0 && i > 0 && !wait(B_OUTEMPTY, (i - 1) & 1)) break;
-          tc_fence_after();
-          // dV' += phi_k,h G_V,h
-          for (int s = 0; s < FB / 16; ++s)
-            mma_bf16(tbase + kDV, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_g, M, 0, 8 * h + s), id_o,
-                     (h > 0 || s > 0) ? 1u : 0u);
-          mma_commit(bar + B_PHFREE);
-          // this block's F buffer has been read: the next unit's F_h may go in
-          if (FAVOR && i + 1 < nun) f_job(i + 1, h);
-          if (FAVOR) {
-            if (!wait(B_U, c & 1)) break;
+      } else if (warp == 2) {
+        // D = V G_V^T, the same jobs
+        int keys = 0;
+        Cursor cur = first;
+        for (int i = 0; i < nun && ok; ++i, advance(cur)) {
+          const int nK = 2 * i, nV = 2 * i + 1;
+          if (new_key(i, cur) && !wait(B_GFULL, keys++ & 1)) break;
+          if (!wait(B_FULL + nV % kSlots, slot_par(nV))) break;
+          const uint64_t dv = desc_kmajor(slot_addr(nV), kTile, 0, 0);
+          for (int jj = 0; jj < JT && ok; ++jj) {
+            const int j = i * JT + jj;
+            if (j >= 2 && !wait(B_DEMPTY + (j & 1), ((j >> 1) - 1) & 1)) break;
             tc_fence_after();
-            // dK' += u_h W_h^T
-            for (int s = 0; s < FB / 16; ++s)
-              mma_bf16(tbase + kDK, desc_kmajor(s_ub, kTile, 0, s), desc_mnmajor(s_w, M, 0, 8 * h + s), id_o,
-                       (h > 0 || s > 0) ? 1u : 0u);
-            mma_commit(bar + B_UFREE);
+            const uint64_t dg = desc_kmajor(s_g, M, 64 * jj, 0);
+#pragma unroll
+            for (int s = 0; s < D / 16; ++s)
+              mma_bf16(tbase + kDc + 64 * (j & 1), dv + ks(s, kTile), dg + ks(s, M), id64, s > 0);
+            mma_commit(bar + B_DFULL + (j & 1));
           }
+          if (!ok) break;
+          mma_commit(bar + B_EMPTY + nV % kSlots);
+          if (!FAVOR) mma_commit(bar + B_EMPTY + nK % kSlots);  // K is read by the epilogue alone
+          if (last_of_key(i, cur)) mma_commit(bar + B_GEMPTY);
         }
-        if (!ok) break;
-        mma_commit(bar + B_OUTFULL);
-        if (last_of_key(i, cur)) mma_commit(bar + B_GEMPTY);
+      } else {
+        // dV' = phi_k G_V and dK' = u W^T, per 128-feature block
+        if (FAVOR) wait(B_WFULL, 0);
+        int keys = 0;
+        Cursor cur = first;
+        for (int i = 0; i < nun && ok; ++i, advance(cur)) {
+          if (new_key(i, cur) && !wait(B_GFULL, keys++ & 1)) break;
+          for (int h = 0; h < nb && ok; ++h) {
+            const uint32_t c = (uint32_t)(i * nb + h);
+            if (!wait(B_PHK, c & 1)) break;
+            if (h == 0 && i > 0 && !wait(B_OUTEMPTY, (i - 1) & 1)) break;
+            tc_fence_after();
+#pragma unroll
+            for (int s = 0; s < FB / 16; ++s)
+              mma_bf16(tbase + kDV, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_g, M, 0, 8 * h + s), id_o,
+                       (h > 0 || s > 0) ? 1u : 0u);
+            mma_commit(bar + B_PHFREE);
+            if (FAVOR) {
+              if (!wait(B_U, c & 1)) break;
+              tc_fence_after();
+#pragma unroll
+              for (int s = 0; s < FB / 16; ++s)
+                mma_bf16(tbase + kDK, desc_kmajor(s_ub, kTile, 0, s), desc_mnmajor(s_w, M, 0, 8 * h + s), id_o,
+                         (h > 0 || s > 0) ? 1u : 0u);
+              mma_commit(bar + B_UFREE);
+            }
+          }
+          if (!ok) break;
+          mma_commit(bar + B_OUTFULL);
+          if (last_of_key(i, cur)) mma_commit(bar + B_GEMPTY);
+        }
       }
-      mma_commit(bar + B_DONE);
-      mbar_drain(bar + B_DONE, 0);
+      mma_commit(bar + B_DONE + (warp - 1));
+      mbar_drain(bar + B_DONE + (warp - 1), 0);
     }
-  } else {
-    // ---------------------------------------------------------------- epilogue
-    const int q4 = warp & 3, half = (warp - 2) >> 2, row = 32 * q4 + lane;
-    const uint32_t lane_base = 32u * q4;
-    bool ok = true;
-    auto wait = [&](int b, uint32_t par) {
-      if (ok) ok = mbar_wait(bar + b, par, p.status, abort_flag);
-      return ok;
-    };
-    auto arrive = [&](int b) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar + b);
-    };
+  } else if (warp < 12) {
+    // ---------------------------------------------------------------- phi_k, u
+    const int part = (warp - 4) >> 2;  // columns [32 part, +32) of every 64-feature job
     const float *gs = reinterpret_cast<const float *>(smem + lay.gs);
     float *usum = reinterpret_cast<float *>(smem + lay.usum);
-    int fj = 0, dj = 0, keys = 0;
+    int keys = 0;
     Cursor cur = first;
     for (int i = 0; i < nun && ok; ++i, advance(cur)) {
-      const int t = cur.t;
-      const int nK = 2 * i, nV = 2 * i + 1;
+      const int nK = 2 * i;
       const uint32_t s_k = slot_addr(nK);
-      const int valid = min(kTile, p.L - t * kTile);
-      const bool dead = row >= valid;
-      if (new_key(i, cur)) {
-        if (!wait(B_GFULL, keys & 1)) break;
-        ++keys;
-      }
+      const bool dead = row >= min(kTile, p.L - cur.t * kTile);
+      if (new_key(i, cur) && !wait(B_GFULL, keys++ & 1)) break;
       if (!wait(B_FULL + nK % kSlots, slot_par(nK))) break;
-      const float ck = FAVOR ? favor_row_const(tile_row_sqnorm(s_k, row, D), M) : 0.f;
+      // padding rows: F = 0 (zero-filled tile) and 2^-inf = 0, no select
+      const float ck = FAVOR ? (dead ? -INFINITY : favor_row_const(tile_row_sqnorm(s_k, row, D), M)) : 0.f;
       float uk = 0.f;
       for (int h = 0; h < nb && ok; ++h) {
         const uint32_t c = (uint32_t)(i * nb + h);
-        const int f0 = 128 * h + FC * half;  // first feature of this thread
-        float v[64];
-        if (FAVOR) {
-          const int b = fj & 1, use = fj >> 1;
-          if (!wait(B_FFULL + b, use & 1)) break;
+        for (int half = 0; half < FB / 64 && ok; ++half) {
+          const int j = (i * nb + h) * (FB / 64) + half;  // the job (F and D alike)
+          const int col = 64 * half + 32 * part;          // column within the block
+          float v[32];
+          if (FAVOR) {
+            if (!wait(B_FFULL + (j & 1), (j >> 1) & 1)) break;
+            tc_fence_after();
+            tmem_ld32(tmem_addr(tbase, lane_base, kF + 64 * (j & 1) + 32 * part), v);
+            tc_fence_before();
+            arrive(B_FEMPTY + (j & 1));
+#pragma unroll
+            for (int x = 0; x < 32; ++x) v[x] = favor_feature(v[x], ck);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              ld_bf16x8(s_k + sw128_offset(row, col + 8 * q, kTile), v + 8 * q);
+#pragma unroll
+              for (int x = 0; x < 8; ++x) v[8 * q + x] = dead ? 0.f : elu1_feature(v[8 * q + x]);
+            }
+          }
+          // phi_k as the MMAs see it (bf16), and u from the same values
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            pk[x] = pack_bf16(v[2 * x], v[2 * x + 1]);
+            v[2 * x] = __uint_as_float(pk[x] << 16);
+            v[2 * x + 1] = __uint_as_float(pk[x] & 0xFFFF0000u);
+          }
+          if (half == 0 && c > 0 && !wait(B_PHFREE, (c - 1) & 1)) break;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            st_shared_v4(s_phk + sw128_offset(row, col + 8 * q, kTile), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                         pk[4 * q + 3]);
+          // u = phi_k * (V G_V^T + G_S)   (elu+1: dphi_k' * min(phi_k, 1))
+          float dd[32];
+          if (!wait(B_DFULL + (j & 1), (j >> 1) & 1)) break;
           tc_fence_after();
-          const uint32_t a = tmem_addr(tbase, lane_base, (b ? kF1 : kF0) + FC * half);
-          if (FC == 64)
-            tmem_ld32x2(a, a + 32, v, v + 32);
-          else
-            tmem_ld32(a, v);
+          tmem_ld32(tmem_addr(tbase, lane_base, kDc + 64 * (j & 1) + 32 * part), dd);
           tc_fence_before();
-          arrive(B_FEMPTY + b);
-          ++fj;
+          arrive(B_DEMPTY + (j & 1));
+          const float *g = gs + 128 * h + col;
 #pragma unroll
-          for (int x = 0; x < 64; ++x)
-            if (x < FC) v[x] = dead ? 0.f : favor_feature(v[x], ck);
-        } else {
+          for (int x = 0; x < 32; ++x) {
+            const float dk = dd[x] + g[x];
+            dd[x] = FAVOR ? v[x] * dk : dk * fminf(v[x], 1.f);
+            uk += dd[x];
+          }
+          if (FAVOR) {
+            if (half == 0 && c > 0 && !wait(B_UFREE, (c - 1) & 1)) break;
 #pragma unroll
-          for (int j = 0; j < FC / 8; ++j) {
-            ld_bf16x8(s_k + sw128_offset(row, FC * half + 8 * j, kTile), v + 8 * j);
+            for (int q = 0; q < 4; ++q) st_bf16x8(s_ub + sw128_offset(row, col + 8 * q, kTile), dd + 8 * q);
+          } else {
+            // elu+1 (M = d): u is dK's increment (feature m = column m); it
+            // takes the place of this thread's K values in the K slot
 #pragma unroll
-            for (int x = 0; x < 8; ++x) v[8 * j + x] = dead ? 0.f : elu1_feature(v[8 * j + x]);
+            for (int q = 0; q < 4; ++q) st_bf16x8(s_k + sw128_offset(row, 128 * h + col + 8 * q, kTile), dd + 8 * q);
           }
         }
-        // phi_k block -> smem for dV' (after the previous block's dV' read it)
-        if (c > 0 && !wait(B_PHFREE, (c - 1) & 1)) break;
-#pragma unroll
-        for (int j = 0; j < FC / 8; ++j) st_bf16x8(s_phk + sw128_offset(row, FC * half + 8 * j, kTile), v + 8 * j);
+        if (!ok) break;
         fence_async_smem();
         arrive(B_PHK);
-        // u = phi_k * (V G_V^T + G_S) with phi_k as stored (bf16)
-        if (!wait(B_DFULL, dj & 1)) break;
-        tc_fence_after();
-        float d[64];
-        {
-          const uint32_t a = tmem_addr(tbase, lane_base, kDc + FC * half);
-          if (FC == 64)
-            tmem_ld32x2(a, a + 32, d, d + 32);
-          else
-            tmem_ld32(a, d);
-        }
-        tc_fence_before();
-        arrive(B_DEMPTY);
-        ++dj;
-#pragma unroll
-        for (int j = 0; j < FC / 8; ++j) {
-          float fk[8];
-          ld_bf16x8(s_phk + sw128_offset(row, FC * half + 8 * j, kTile), fk);
-#pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            const float dk = d[8 * j + x] + gs[f0 + 8 * j + x];
-            d[8 * j + x] = FAVOR ? fk[x] * dk : dk * fminf(fk[x], 1.f);
-            uk += d[8 * j + x];
-          }
-        }
-        if (FAVOR) {
-          if (c > 0 && !wait(B_UFREE, (c - 1) & 1)) break;
-#pragma unroll
-          for (int j = 0; j < FC / 8; ++j) st_bf16x8(s_ub + sw128_offset(row, FC * half + 8 * j, kTile), d + 8 * j);
-          fence_async_smem();
-          arrive(B_U);
-        } else {
-          // elu+1 (M = d): u is dK's increment (feature m = column m); it takes
-          // the place of this thread's K values in the K slot
-#pragma unroll
-          for (int j = 0; j < FC / 8; ++j) st_bf16x8(s_k + sw128_offset(row, f0 + 8 * j, kTile), d + 8 * j);
-        }
+        if (FAVOR) arrive(B_U);
       }
       if (!ok) break;
-      if (FAVOR) usum[((i & 1) * 2 + half) * kTile + row] = uk;
-      arrive(B_EPI);
+      usum[((i & 1) * 2 + part) * kTile + row] = uk;
+      arrive(B_EPI + (i & 1));
       if (last_of_key(i, cur)) arrive(B_GEMPTY);  // G_S read for the last time
-      // dV += dV', dK += dK' - k rowsum(u)
+      fence_async_smem();
+      arrive(B_STG + (i & 1));
+    }
+  } else {
+    // ---------------------------------------------------------------- dK, dV increments
+    const float *usum = reinterpret_cast<const float *>(smem + lay.usum);
+    for (int i = 0; i < nun && ok; ++i) {
+      const int nK = 2 * i, nV = 2 * i + 1;
+      const uint32_t s_k = slot_addr(nK), s_v = slot_addr(nV);
       if (!wait(B_OUTFULL, i & 1)) break;
       tc_fence_after();
-      float dv[32], dkk[32];
-      tmem_ld32x2(tmem_addr(tbase, lane_base, kDV + 32 * half), tmem_addr(tbase, lane_base, kDK + 32 * half), dv,
-                  dkk);
-      tc_fence_before();
-      arrive(B_OUTEMPTY);
-      if (!wait(B_EPI, i & 1)) break;
-      // increments -> bf16 in this unit's slots (dV over V; dK over K, whose
-      // values this thread reads first); rows past L are clipped by the TMA
-      const uint32_t s_v = slot_addr(nV);
+      {
+        // dV' -> bf16 over V (the D MMAs are done with it)
+        float dv[64];
+        tmem_ld32x2(tmem_addr(tbase, lane_base, kDV), tmem_addr(tbase, lane_base, kDV + 32), dv, dv + 32);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) st_bf16x8(s_v + sw128_offset(row, 32 * half + 8 * j, kTile), dv + 8 * j);
+        for (int q = 0; q < 8; ++q) st_bf16x8(s_v + sw128_offset(row, 8 * q, kTile), dv + 8 * q);
+      }
       if (FAVOR) {
+        // dK' - k rowsum(u) -> bf16 over K (whose values are read first)
+        float dk[64];
+        tmem_ld32x2(tmem_addr(tbase, lane_base, kDK), tmem_addr(tbase, lane_base, kDK + 32), dk, dk + 32);
+        tc_fence_before();
+        arrive(B_OUTEMPTY);
+        if (!wait(B_EPI + (i & 1), (i >> 1) & 1)) break;
         const float sk = usum[((i & 1) * 2) * kTile + row] + usum[((i & 1) * 2 + 1) * kTile + row];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int q = 0; q < 8; ++q) {
           float xk[8];
-          ld_bf16x8(s_k + sw128_offset(row, 32 * half + 8 * j, kTile), xk);
+          ld_bf16x8(s_k + sw128_offset(row, 8 * q, kTile), xk);
 #pragma unroll
-          for (int x = 0; x < 8; ++x) dkk[8 * j + x] = fmaf(-xk[x], sk, dkk[8 * j + x]);
-          st_bf16x8(s_k + sw128_offset(row, 32 * half + 8 * j, kTile), dkk + 8 * j);
+          for (int x = 0; x < 8; ++x) dk[8 * q + x] = fmaf(-xk[x], sk, dk[8 * q + x]);
+          st_bf16x8(s_k + sw128_offset(row, 8 * q, kTile), dk + 8 * q);
         }
+      } else {
+        tc_fence_before();
+        arrive(B_OUTEMPTY);
       }
       fence_async_smem();
       arrive(B_STG + (i & 1));
