@@ -60,23 +60,23 @@ enum {
   B_DFULL = 12,     // [2] V G_V^T job in TMEM buffer b
   B_DEMPTY = 14,    // [2] ... read out (8 warps)
   B_PHK = 16,       // phi_k block stored (8 warps)
-  B_PHFREE = 17,    // dV' MMAs done with the phi_k block
-  B_U = 18,         // u block stored (8 warps)
-  B_UFREE = 19,     // dK' MMAs done with the u block
-  B_OUTFULL = 20,   // dV', dK' complete
-  B_OUTEMPTY = 21,  // dV', dK' read out (4 warps)
-  B_GFULL = 22,     // G_end image landed
-  B_GEMPTY = 23,    // G_end image no longer read (2 MMA commits + 8 warps)
-  B_WFULL = 24,     // W image landed
-  B_EPI = 25,       // [2] row sums of u written (8 warps), by unit parity
-  B_STG = 27,       // [2] a unit's dK, dV increments staged in its slots (4 + 8 warps)
-  B_DONE = 29,      // [3] MMA drain of each issuing thread
-  B_COUNT = 32
+  B_U = 17,         // u block packed in TMEM (8 warps)
+  B_PHFREE = 18,    // [2] dV' MMAs done with phi_k buffer b
+  B_UFREE = 20,     // [2] dK' MMAs done with u buffer b
+  B_OUTFULL = 22,   // dV', dK' complete
+  B_OUTEMPTY = 23,  // dV', dK' read out (4 warps)
+  B_GFULL = 24,     // G_end image landed
+  B_GEMPTY = 25,    // G_end image no longer read (2 MMA commits + 8 warps)
+  B_WFULL = 26,     // W image landed
+  B_EPI = 27,       // [2] row sums of u written (8 warps), by unit parity
+  B_STG = 29,       // [2] a unit's dK, dV increments staged in its slots (4 + 8 warps)
+  B_DONE = 31,      // [3] MMA drain of each issuing thread
+  B_COUNT = 34
 };
 
 template <int M>
 struct Layout {
-  uint32_t w, slots, g, gs, phk, ub, usum, bars, total;
+  uint32_t w, slots, g, gs, phk, usum, bars, total;
   __host__ __device__ Layout() {
     uint32_t o = 0;
     w = o; o += M * 128u;
@@ -84,16 +84,16 @@ struct Layout {
     g = o; o += M * 128u;   // G_end[:, 0:64] as bf16 [M][64], swizzled
     gs = o; o += M * 4u;    // G_end[:, 64] fp32 (directly after g: one bulk copy)
     o = (o + 1023u) & ~1023u;
-    phk = o; o += kTile * 128 * 2;
-    ub = o; o += kTile * 128 * 2;
+    phk = o; o += 2 * kTile * 128 * 2;  // two phi_k blocks, used in turn
     usum = o; o += 2 * 2 * kTile * 4;  // [unit parity][part][row]
     bars = o; o += 8 * B_COUNT + 16;
     total = o;
   }
 };
 
-// TMEM columns: F jobs 2 x 64 | D jobs 2 x 64 | dV' 64 | dK' 64
-constexpr uint32_t kF = 0, kDc = 128, kDV = 256, kDK = 320;
+// TMEM columns: F jobs 2 x 64 | D jobs 2 x 64 | dV' 64 | dK' 64 | u, two
+// 128-feature blocks of bf16 pairs (the A operand of dK' = u W^T) 2 x 64
+constexpr uint32_t kF = 0, kDc = 128, kDV = 256, kDK = 320, kU = 384;
 
 template <bool FAVOR, int M>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -155,11 +155,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar + B_DEMPTY + b, 8);
       mbar_init(bar + B_EPI + b, 8);
       mbar_init(bar + B_STG + b, 12);
+      mbar_init(bar + B_PHFREE + b, 1);
+      mbar_init(bar + B_UFREE + b, 1);
     }
     mbar_init(bar + B_PHK, 8);
-    mbar_init(bar + B_PHFREE, 1);
     mbar_init(bar + B_U, 8);
-    mbar_init(bar + B_UFREE, 1);
     mbar_init(bar + B_OUTFULL, 1);
     mbar_init(bar + B_OUTEMPTY, 4);
     mbar_init(bar + B_GFULL, 1);
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  const uint32_t s_w = sbase + lay.w, s_g = sbase + lay.g, s_phk = sbase + lay.phk, s_ub = sbase + lay.ub;
+  const uint32_t s_w = sbase + lay.w, s_g = sbase + lay.g, s_phk = sbase + lay.phk;
   auto slot_addr = [&](int n) { return sbase + lay.slots + (uint32_t)(n % kSlots) * kTileBytes; };
   auto slot_par = [&](int n) { return (uint32_t)((n / kSlots) & 1); };
   bool ok = true;
@@ -293,23 +293,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < nun && ok; ++i, advance(cur)) {
           if (new_key(i, cur) && !wait(B_GFULL, keys++ & 1)) break;
           for (int h = 0; h < nb && ok; ++h) {
-            const uint32_t c = (uint32_t)(i * nb + h);
+            const uint32_t c = (uint32_t)(i * nb + h), b = c & 1;
             if (!wait(B_PHK, c & 1)) break;
             if (h == 0 && i > 0 && !wait(B_OUTEMPTY, (i - 1) & 1)) break;
             tc_fence_after();
+            const uint32_t s_ph = s_phk + b * kTile * 256;
 #pragma unroll
             for (int s = 0; s < FB / 16; ++s)
-              mma_bf16(tbase + kDV, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_g, M, 0, 8 * h + s), id_o,
+              mma_bf16(tbase + kDV, desc_kmajor(s_ph, kTile, 0, s), desc_mnmajor(s_g, M, 0, 8 * h + s), id_o,
                        (h > 0 || s > 0) ? 1u : 0u);
-            mma_commit(bar + B_PHFREE);
+            mma_commit(bar + B_PHFREE + b);
             if (FAVOR) {
               if (!wait(B_U, c & 1)) break;
               tc_fence_after();
 #pragma unroll
               for (int s = 0; s < FB / 16; ++s)
-                mma_bf16(tbase + kDK, desc_kmajor(s_ub, kTile, 0, s), desc_mnmajor(s_w, M, 0, 8 * h + s), id_o,
-                         (h > 0 || s > 0) ? 1u : 0u);
-              mma_commit(bar + B_UFREE);
+                mma_bf16_ta(tbase + kDK, tbase + kU + 64 * b + 8 * s, desc_mnmajor(s_w, M, 0, 8 * h + s), id_o,
+                            (h > 0 || s > 0) ? 1u : 0u);
+              mma_commit(bar + B_UFREE + b);
             }
           }
           if (!ok) break;
@@ -337,7 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float ck = FAVOR ? (dead ? -INFINITY : favor_row_const(tile_row_sqnorm(s_k, row, D), M)) : 0.f;
       float uk = 0.f;
       for (int h = 0; h < nb && ok; ++h) {
-        const uint32_t c = (uint32_t)(i * nb + h);
+        const uint32_t c = (uint32_t)(i * nb + h), b = c & 1;
+        const uint32_t s_ph = s_phk + b * kTile * 256;
         for (int half = 0; half < FB / 64 && ok; ++half) {
           const int j = (i * nb + h) * (FB / 64) + half;  // the job (F and D alike)
           const int col = 64 * half + 32 * part;          // column within the block
@@ -366,10 +368,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[2 * x] = __uint_as_float(pk[x] << 16);
             v[2 * x + 1] = __uint_as_float(pk[x] & 0xFFFF0000u);
           }
-          if (half == 0 && c > 0 && !wait(B_PHFREE, (c - 1) & 1)) break;
+          // the buffer's last block has been read by its dV' MMAs
+          if (half == 0 && c >= 2 && !wait(B_PHFREE + b, ((c >> 1) - 1) & 1)) break;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            st_shared_v4(s_phk + sw128_offset(row, col + 8 * q, kTile), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+            st_shared_v4(s_ph + sw128_offset(row, col + 8 * q, kTile), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
                          pk[4 * q + 3]);
           // u = phi_k * (V G_V^T + G_S)   (elu+1: dphi_k' * min(phi_k, 1))
           float dd[32];
@@ -386,9 +389,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uk += dd[x];
           }
           if (FAVOR) {
-            if (half == 0 && c > 0 && !wait(B_UFREE, (c - 1) & 1)) break;
+            // u as bf16 pairs into TMEM: feature f of the block -> column f / 2
+            if (half == 0 && c >= 2 && !wait(B_UFREE + b, ((c >> 1) - 1) & 1)) break;
+            float pu[16];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) st_bf16x8(s_ub + sw128_offset(row, col + 8 * q, kTile), dd + 8 * q);
+            for (int x = 0; x < 16; ++x) pu[x] = __uint_as_float(pack_bf16(dd[2 * x], dd[2 * x + 1]));
+            tmem_st16(tmem_addr(tbase, lane_base, kU + 64 * b + col / 2), pu);
           } else {
             // elu+1 (M = d): u is dK's increment (feature m = column m); it
             // takes the place of this thread's K values in the K slot
@@ -399,7 +405,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         fence_async_smem();
         arrive(B_PHK);
-        if (FAVOR) arrive(B_U);
+        if (FAVOR) {
+          tmem_st_wait();
+          tc_fence_before();
+          arrive(B_U);
+        }
       }
       if (!ok) break;
       usum[((i & 1) * 2 + part) * kTile + row] = uk;
