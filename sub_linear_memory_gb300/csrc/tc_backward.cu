@@ -147,6 +147,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // cluster exchange of num' and den: data received (st.async bytes) and
   // receive tiles released by the peer (remote arrive), one phase per tile
   uint64_t *x1_full = in_bar + 6, *x1_free = in_bar + 8;
+  // inputs: Q, K on in_bar (needed first, by the features); V, dY on in2_bar
+  // (needed from the state increment on), so a tile starts before they land
+  uint64_t *in2_bar = in_bar + 10;
   float *rx_den = reinterpret_cast<float *>(smem + lay.rx_den);
   float *s_f = reinterpret_cast<float *>(smem + lay.s_f);
   float *gs_f = reinterpret_cast<float *>(smem + lay.gs_f);
@@ -170,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t lo_stage = lay.phq + ((st_bytes + 1023u) & ~1023u);
   if (tid == 0) {
     mbar_init(in_bar, 1);
+    mbar_init(in2_bar, 1);
     mbar_init(mma_bar, 1);
     mbar_init(rl_bar, 1);
     mbar_init(setup_bar, 1);
@@ -241,18 +245,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_at = sb + lay.at, s_dn = sb + lay.dn, s_rb = sb + lay.rb;
   const uint32_t s_ones = sb + lay.ones, s_ddb = sb + lay.ddb, s_sb = sb + lay.sb;
   const uint32_t tile_bytes = kTile * D * 2;
-  uint32_t in_phase = 0, mma_phase = 0, rl_phase = 0, x_phase = 0;
+  uint32_t in_phase = 0, in2_phase = 0, mma_phase = 0, rl_phase = 0, x_phase = 0;
   // the exchange: num partials of all 128 rows (fp32 [128][64]) + den
   constexpr uint32_t kX1Bytes = 128 * 64 * 4 + 128 * 4;
   const uint32_t peer_x1_full = CS == 2 ? map_peer(smem_u32(x1_full), peer) : 0u;
   const uint32_t peer_x1_free = CS == 2 ? map_peer(smem_u32(x1_free), peer) : 0u;
 
   auto issue_in = [&](int t) {
-    mbar_arrive_expect_tx(in_bar, 4 * tile_bytes);
+    mbar_arrive_expect_tx(in_bar, 2 * tile_bytes);
     tma_load_3d(smem + lay.q, &tmQ, in_bar, 0, t * kTile, bh);
     tma_load_3d(smem + lay.k, &tmK, in_bar, 0, t * kTile, bh);
-    tma_load_3d(smem + lay.v, &tmV, in_bar, 0, t * kTile, bh);
-    tma_load_3d(smem + lay.dy, &tmDY, in_bar, 0, t * kTile, bh);
+    mbar_arrive_expect_tx(in2_bar, 2 * tile_bytes);
+    tma_load_3d(smem + lay.v, &tmV, in2_bar, 0, t * kTile, bh);
+    tma_load_3d(smem + lay.dy, &tmDY, in2_bar, 0, t * kTile, bh);
   };
   auto mma_done = [&]() {
     mma_commit(mma_bar);
@@ -285,11 +290,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_3d(&tmV, 0, (t - 1) * kTile, bh);
       tma_prefetch_3d(&tmDY, 0, (t - 1) * kTile, bh);
     }
-    float ck = 0.f, cq = 0.f;
-    if (FAVOR) {
-      ck = live ? favor_row_const(tile_row_sqnorm(s_k, row, D), M) : -INFINITY;
-      cq = live ? favor_row_const(tile_row_sqnorm(s_q, row, D), M) : -INFINITY;
-    }
 
     // (b) features of both sides: F_k -> T, F_q -> X, one commit
     if (FAVOR) {
@@ -301,6 +301,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16(tb + kX, desc_kmajor(s_q, kTile, 0, s), desc_kmajor(s_w, MC, 0, s), id, s > 0);
         mma_done();
       }
+      // |k|^2, |q|^2 of the row while the MMAs run, each part summing a
+      // quarter of the columns (the u row-sum arrays are idle until (i))
+      usq[part * kTile + row] = tile_row_sqnorm_part(s_k, row, QD * part, QD);
+      usk[part * kTile + row] = tile_row_sqnorm_part(s_q, row, QD * part, QD);
+      __syncthreads();
+      const float nk = (usq[row] + usq[kTile + row]) + (usq[2 * kTile + row] + usq[3 * kTile + row]);
+      const float nq = (usk[row] + usk[kTile + row]) + (usk[2 * kTile + row] + usk[3 * kTile + row]);
+      const float ck = live ? favor_row_const(nk, M) : -INFINITY;
+      const float cq = live ? favor_row_const(nq, M) : -INFINITY;
       wait_mma();
       for (int side = 0; side < 2; ++side) {
         const uint32_t t_in = side ? kX : kT, s_out = side ? s_phq : s_phk;
@@ -340,6 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (c) eq. (19): R' -= phi_k^T [V, 1], removing exactly the increment the
     // segment pre-pass added for this tile (increment -> T), and
     // A = phi_q phi_k^T -> X, one commit
+    mbar_wait(in2_bar, in2_phase, p.status, abort_flag);  // V (and dY, read in (f))
+    in2_phase ^= 1;
     if (tid == 0) {
       // last tile's dQ, dK partials (staged in the dN and R-copy tiles) have
       // been read by their reduce-adds before this phase's epilogue reuses them
@@ -527,22 +538,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_done();
       if (CS == 2 && t > t0) {
-        // the Q tile's dV partial has been read by its reduce-add and the K
-        // tile's num' partial by the exchange epilogue: the next tile's Q and
-        // K stream in while this one finishes
-        tma_store_wait_read();
-        mbar_arrive_expect_tx(in_bar, 4 * tile_bytes);
-        tma_load_3d(smem + lay.q, &tmQ, in_bar, 0, (t - 1) * kTile, bh);
+        // the K tile's num' partial has been read by the exchange epilogue:
+        // the next tile's K streams in while this one finishes (Q follows
+        // once the reduce-add has read the dV partial out of the Q tile)
+        mbar_arrive_expect_tx(in_bar, 2 * tile_bytes);
         tma_load_3d(smem + lay.k, &tmK, in_bar, 0, (t - 1) * kTile, bh);
       }
     }
     wait_mma();
-    // the next tile's inputs stream in as their tiles fall idle: dY (and V
-    // with one CTA per segment) from here, Q and K / V later in this tile
+    // the next tile's inputs stream in as their tiles fall idle: dY and V
+    // from here; Q and K at (h) with a CTA pair, at the end of the tile alone
     if (tid == 0 && t > t0) {
-      if (CS == 1) mbar_arrive_expect_tx(in_bar, 4 * tile_bytes);
-      tma_load_3d(smem + lay.dy, &tmDY, in_bar, 0, (t - 1) * kTile, bh);
-      tma_load_3d(smem + lay.v, &tmV, in_bar, 0, (t - 1) * kTile, bh);
+      if (CS == 2) {
+        tma_store_wait_read();
+        tma_load_3d(smem + lay.q, &tmQ, in_bar, 0, (t - 1) * kTile, bh);
+      }
+      mbar_arrive_expect_tx(in2_bar, 2 * tile_bytes);
+      tma_load_3d(smem + lay.dy, &tmDY, in2_bar, 0, (t - 1) * kTile, bh);
+      tma_load_3d(smem + lay.v, &tmV, in2_bar, 0, (t - 1) * kTile, bh);
     }
     if (CS == 2) {
       // the dA tile is idle from here: Q and K come back into it for the
@@ -675,6 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     x_phase ^= 1;
     if (CS == 1 && tid == 0 && t > t0) {
+      mbar_arrive_expect_tx(in_bar, 2 * tile_bytes);
       tma_load_3d(smem + lay.q, &tmQ, in_bar, 0, (t - 1) * kTile, bh);
       tma_load_3d(smem + lay.k, &tmK, in_bar, 0, (t - 1) * kTile, bh);
     }
