@@ -54,7 +54,7 @@ struct Params {
 };
 
 struct Layout {
-  uint32_t w, q, k, v, dy, phq, phk, at, dn, rb, ones, ddb;
+  uint32_t w, q, k, v, dy, phq, phk, at, gv, rb, ones, ddb;
   uint32_t sb, s_f, gs_f, dd, usq, usk, dot, rx_den, bars, total;
   __host__ __device__ explicit Layout(int MC) {
     uint32_t o = 0;
@@ -63,11 +63,11 @@ struct Layout {
     q = o; o += tile;
     k = o; o += tile;
     v = o; o += tile;
-    dy = o; o += tile;  // dY, then the bf16 copy of G_V
+    dy = o; o += tile;  // dY, then dN (in place)
     phq = o; o += kTile * 256;
     phk = o; o += kTile * 256;
     at = o; o += kTile * 256;  // masked A, then masked dA
-    dn = o; o += tile;
+    gv = o; o += tile;  // the bf16 copy of G_V; with a CTA pair, then the dQ partial
     rb = o; o += (uint32_t)MC * 128u;
     ones = o; o += 4096;
     ddb = o; o += 4096;
@@ -79,10 +79,10 @@ struct Layout {
     usk = o; o += kParts * kTile * 4;
     // dY . Y partials: dead before u's row sums are written
     dot = usq;
-    // cluster exchange, the peer's den partials: read before this tile's
-    // G_S copy is written, and the peer writes them only after this CTA has
-    // passed its next tile's features (hence read G_S)
-    rx_den = gs_f;
+    // cluster exchange, the peer's den partials: the peer writes them only
+    // after this CTA is past its features (the last use of usk before (f)),
+    // and they are read before u's row sums are written
+    rx_den = usk;
     bars = o; o += 128;
     total = o;
   }
@@ -150,6 +150,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // inputs: Q, K on in_bar (needed first, by the features); V, dY on in2_bar
   // (needed from the state increment on), so a tile starts before they land
   uint64_t *in2_bar = in_bar + 10;
+  // a second MMA-completion barrier, for a group whose epilogue overlaps the
+  // group issued after it
+  uint64_t *mmb_bar = in_bar + 11;
   float *rx_den = reinterpret_cast<float *>(smem + lay.rx_den);
   float *s_f = reinterpret_cast<float *>(smem + lay.s_f);
   float *gs_f = reinterpret_cast<float *>(smem + lay.gs_f);
@@ -174,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(in_bar, 1);
     mbar_init(in2_bar, 1);
+    mbar_init(mmb_bar, 1);
     mbar_init(mma_bar, 1);
     mbar_init(rl_bar, 1);
     mbar_init(setup_bar, 1);
@@ -242,10 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t s_w = sb + lay.w, s_q = sb + lay.q, s_k = sb + lay.k, s_v = sb + lay.v;
   const uint32_t s_dy = sb + lay.dy, s_phq = sb + lay.phq, s_phk = sb + lay.phk;
-  const uint32_t s_at = sb + lay.at, s_dn = sb + lay.dn, s_rb = sb + lay.rb;
+  const uint32_t s_at = sb + lay.at, s_gv = sb + lay.gv, s_rb = sb + lay.rb;
   const uint32_t s_ones = sb + lay.ones, s_ddb = sb + lay.ddb, s_sb = sb + lay.sb;
   const uint32_t tile_bytes = kTile * D * 2;
-  uint32_t in_phase = 0, in2_phase = 0, mma_phase = 0, rl_phase = 0, x_phase = 0;
+  uint32_t in_phase = 0, in2_phase = 0, mma_phase = 0, mmb_phase = 0, rl_phase = 0, x_phase = 0;
   // the exchange: num partials of all 128 rows (fp32 [128][64]) + den
   constexpr uint32_t kX1Bytes = 128 * 64 * 4 + 128 * 4;
   const uint32_t peer_x1_full = CS == 2 ? map_peer(smem_u32(x1_full), peer) : 0u;
@@ -266,6 +270,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     mbar_wait(mma_bar, mma_phase, p.status, abort_flag);
     mma_phase ^= 1;
+    tc_fence_after();
+  };
+  auto wait_mmb = [&]() {
+    __syncwarp();
+    mbar_wait(mmb_bar, mmb_phase, p.status, abort_flag);
+    mmb_phase ^= 1;
     tc_fence_after();
   };
   auto cta_sync = [&]() {
@@ -346,20 +356,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     // cluster-scope release waits for this thread's earlier stores)
     if (CS == 2 && tid == 32) mbar_arrive_remote(peer_x1_free);
 
-    // (c) eq. (19): R' -= phi_k^T [V, 1], removing exactly the increment the
-    // segment pre-pass added for this tile (increment -> T), and
-    // A = phi_q phi_k^T -> X, one commit
-    mbar_wait(in2_bar, in2_phase, p.status, abort_flag);  // V (and dY, read in (f))
-    in2_phase ^= 1;
+    // (c) A = phi_q phi_k^T -> X (its own commit: the mask below overlaps
+    // the next group), and eq. (19): R' -= phi_k^T [V, 1], removing exactly
+    // the increment the segment pre-pass added for this tile (increment -> T)
     if (tid == 0) {
-      // last tile's dQ, dK partials (staged in the dN and R-copy tiles) have
+      // last tile's dQ, dK partials (staged in the G_V-copy and R-copy tiles) have
       // been read by their reduce-adds before this phase's epilogue reuses them
       if (CS == 2) tma_store_wait_read();
-      issue_state_delta(tb + kT, s_phk, s_v, s_ones, D);
       const uint32_t id = make_idesc(128, 128, false, false);
       for (int s = 0; s < MC / 16; ++s)
         mma_bf16(tb + kX, desc_kmajor(s_phq, kTile, 0, s), desc_kmajor(s_phk, kTile, 0, s), id, s > 0);
+      mma_commit(mmb_bar);
+    }
+    mbar_wait(in2_bar, in2_phase, p.status, abort_flag);  // V (and dY, read in (f))
+    in2_phase ^= 1;
+    if (tid == 0) {
+      issue_state_delta(tb + kT, s_phk, s_v, s_ones, D);
       mma_done();
+    }
+    wait_mmb();
+    // tril(A) (diagonal kept) -> bf16 tile
+    {
+      float v[32];
+      tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * part), v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (32 * part + i > row) v[i] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, 32 * part + 8 * j, kTile), v + 8 * j);
     }
     wait_mma();
     // eq. (19) on the double-float master, and from the updated values the
@@ -391,16 +415,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     tmem_st_wait();
-    // tril(A) (diagonal kept) -> bf16 tile
-    {
-      float v[32];
-      tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * part), v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (32 * part + i > row) v[i] = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, 32 * part + 8 * j, kTile), v + 8 * j);
-    }
     fence_async_smem();
     cta_sync();
 
@@ -418,6 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_done();
     }
+    // while the MMAs run: the bf16 copy of G_V (G as the last tile left it)
+    // into its tile, whose last reader (the previous dQ reduce-add with a
+    // CTA pair) was waited for in (c); G_S as fp32
+    state_to_smem(tb, kG, q4, part, row, MC, s_gv, gs_f);
     wait_mma();
     {
       float den;
@@ -458,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         g[i] = live ? g[i] * inv : 0.f;
       }
 #pragma unroll
-      for (int j = 0; j < QD / 8; ++j) st_bf16x8(s_dn + sw128_offset(row, QD * part + 8 * j, kTile), g + 8 * j);
+      for (int j = 0; j < QD / 8; ++j) st_bf16x8(s_dy + sw128_offset(row, QD * part + 8 * j, kTile), g + 8 * j);
       dot[part * kTile + row] = dyy;
       __syncthreads();
       if (part == 0) {
@@ -467,8 +485,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         st_bf16_scalar(smem, lay.ddb + n16_offset(row, 0), dval);
       }
     }
-    cta_sync();  // dY consumed: its buffer now takes the bf16 copy of G_V
-    state_to_smem(tb, kG, q4, part, row, MC, s_dy, gs_f);
     fence_async_smem();
     cta_sync();
 
@@ -477,12 +493,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_v1 = make_idesc(128, D, true, true);
       const uint32_t id_v2 = make_idesc(128, D, false, true);
       for (int s = 0; s < kTile / 16; ++s)
-        mma_bf16(tb + kX, desc_mnmajor(s_at, kTile, 0, s), desc_mnmajor(s_dn, kTile, 0, s), id_v1, s > 0);
+        mma_bf16(tb + kX, desc_mnmajor(s_at, kTile, 0, s), desc_mnmajor(s_dy, kTile, 0, s), id_v1, s > 0);
       for (int s = 0; s < MC / 16; ++s)
-        mma_bf16(tb + kX, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_dy, MC, 0, s), id_v2, 1);
+        mma_bf16(tb + kX, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_gv, MC, 0, s), id_v2, 1);
       const uint32_t id_a = make_idesc(128, 128, false, false);
       for (int s = 0; s < D / 16; ++s)
-        mma_bf16(tb + kT, desc_kmajor(s_dn, kTile, 0, s), desc_kmajor(s_v, kTile, 0, s), id_a, s > 0);
+        mma_bf16(tb + kT, desc_kmajor(s_dy, kTile, 0, s), desc_kmajor(s_v, kTile, 0, s), id_a, s > 0);
       mma_done();
     }
     wait_mma();
@@ -524,16 +540,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kTile / 16; ++s)
         mma_bf16(tb + kT, desc_kmajor(s_at, kTile, 0, s), desc_mnmajor(s_phk, kTile, 0, s), id_q1, s > 0);
       for (int s = 0; s < D / 16; ++s)
-        mma_bf16(tb + kT, desc_kmajor(s_dn, kTile, 0, s), desc_kmajor(s_rb, MC, 0, s), id_q2, 1);
+        mma_bf16(tb + kT, desc_kmajor(s_dy, kTile, 0, s), desc_kmajor(s_rb, MC, 0, s), id_q2, 1);
       const uint32_t id_k1 = make_idesc(128, MC, true, true);
       for (int s = 0; s < kTile / 16; ++s)
         mma_bf16(tb + kX, desc_mnmajor(s_at, kTile, 0, s), desc_mnmajor(s_phq, kTile, 0, s), id_k1, s > 0);
       for (int s = 0; s < D / 16; ++s)
-        mma_bf16(tb + kX, desc_kmajor(s_v, kTile, 0, s), desc_kmajor(s_dy, MC, 0, s), id_q2, 1);
+        mma_bf16(tb + kX, desc_kmajor(s_v, kTile, 0, s), desc_kmajor(s_gv, MC, 0, s), id_q2, 1);
       const uint32_t id_g = make_idesc(128, D, true, true);
       const uint32_t id_g1 = make_idesc(128, 16, true, true);
       for (int s = 0; s < kTile / 16; ++s) {
-        mma_bf16(tb + kG, desc_mnmajor(s_phq, kTile, 0, s), desc_mnmajor(s_dn, kTile, 0, s), id_g, 1);
+        mma_bf16(tb + kG, desc_mnmajor(s_phq, kTile, 0, s), desc_mnmajor(s_dy, kTile, 0, s), id_g, 1);
         mma_bf16(tb + kG + D, desc_mnmajor(s_phq, kTile, 0, s), desc_n16(s_ddb, s), id_g1, 1);
       }
       mma_done();
@@ -660,16 +676,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (CS == 2) {
-        // partials -> bf16 in the idle dN and R-copy tiles for reduce-adds
+        // partials -> bf16 in the idle G_V-copy and R-copy tiles for reduce-adds
 #pragma unroll
         for (int j = 0; j < QD / 8; ++j) {
-          st_bf16x8(s_dn + sw128_offset(row, QD * part + 8 * j, kTile), oq + 8 * j);
+          st_bf16x8(s_gv + sw128_offset(row, QD * part + 8 * j, kTile), oq + 8 * j);
           st_bf16x8(s_rb + sw128_offset(row, QD * part + 8 * j, kTile), ok + 8 * j);
         }
         fence_async_smem();
         cta_sync();
         if (tid == 0) {
-          tma_reduce_add_3d(&tmDQ, s_dn, 0, t * kTile, bh);
+          tma_reduce_add_3d(&tmDQ, s_gv, 0, t * kTile, bh);
           tma_reduce_add_3d(&tmDK, s_rb, 0, t * kTile, bh);
           tma_store_commit();
         }
