@@ -19,8 +19,9 @@
 // the segments' G totals) afterwards: both terms are linear in G.
 //
 // With 256 features a segment runs on a two-CTA cluster, each CTA owning 128
-// features.  num' and den need all features for dN', so the CTAs exchange
-// their partials (distributed shared memory).  dV, dQ and dK are sums over
+// features.  dN' needs two row sums over all features, den and dY . num
+// (dY . Y = dY . num / den), so the CTAs swap their partials of those two
+// (distributed shared memory, two floats per row).  dV, dQ and dK are sums over
 // features too, but nothing downstream needs them inside the kernel: each
 // CTA rounds its partial to bf16 and adds it into the (zeroed) outputs with
 // a TMA reduce-add.  The order of the two adds is not fixed, so those
@@ -41,6 +42,7 @@ constexpr int kThreads = 512;
 constexpr int kParts = 4;  // threads per row (TMEM lane): warps w, w + 4, w + 8, w + 12
 constexpr int kTile = 128;
 constexpr int D = 64;
+static_assert(16 * kParts == D, "the R update gives each part 16 value columns");
 
 struct Params {
   int L, M, nt, P, tps, favor, BH;
@@ -55,7 +57,7 @@ struct Params {
 
 struct Layout {
   uint32_t w, q, k, v, dy, phq, phk, at, gv, rb, ones, ddb;
-  uint32_t sb, s_f, gs_f, dd, usq, usk, dot, rx_den, bars, total;
+  uint32_t sb, s_f, gs_f, dd, usq, usk, dot, rx, bars, total;
   __host__ __device__ explicit Layout(int MC) {
     uint32_t o = 0;
     const uint32_t tile = kTile * D * 2;
@@ -79,19 +81,15 @@ struct Layout {
     usk = o; o += kParts * kTile * 4;
     // dY . Y partials: dead before u's row sums are written
     dot = usq;
-    // cluster exchange, the peer's den partials: the peer writes them only
-    // after this CTA is past its features (the last use of usk before (f)),
-    // and they are read before u's row sums are written
-    rx_den = usk;
+    // cluster exchange, the peer's row partials of den and dY . num
+    // ([2][128]): the peer writes them only after this CTA is past its
+    // features (the last use of usk before (f)), and they are read before
+    // u's row sums are written
+    rx = usk;
     bars = o; o += 128;
     total = o;
   }
 };
-
-// fp32 exchange tiles are kept column-chunk-major, 4 floats per chunk:
-// element (r, 4c .. 4c+3) of an R-row tile sits at byte (c * R + r) * 16, so a
-// warp (consecutive rows, one chunk) touches consecutive 16-B words.
-__device__ __forceinline__ uint32_t xoff(int r, int c4, int R) { return (uint32_t)((c4 * R + r) * 16); }
 
 // TMEM columns: R' as a double-float (hi, lo) pair, G, two transients
 constexpr uint32_t kRhi = 0, kRlo = 80, kG = 160, kT = 240, kX = 368;
@@ -120,10 +118,9 @@ __device__ __forceinline__ void state_to_smem(uint32_t tbase, uint32_t col, int 
 // CS = 1: one CTA per segment holds all M <= 128 features.
 // CS = 2: a cluster of two CTAs per segment; CTA c owns features
 // [128c, 128c + 128) with their R' and G, computes every per-feature term
-// locally, and the two exchange through distributed shared memory the
-// cross-feature sums (num, den; dV, dQ, dK, rowsum(u)) for the 64 rows each
-// owns, plus dN' so both hold it.  Exchange buffers reuse tiles that are
-// provably idle at that point (cluster barriers mark those points).
+// locally, and the two swap through distributed shared memory the row sums
+// den and dY . num, so both form the same dN' for all 128 rows.  dV, dQ and
+// dK partials go to global memory by TMA reduce-add.
 template <bool FAVOR, int CS, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -144,8 +141,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t *tslot = reinterpret_cast<uint32_t *>(in_bar + 3);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(in_bar + 4);
   uint64_t *setup_bar = in_bar + 5;
-  // cluster exchange of num' and den: data received (st.async bytes) and
-  // receive tiles released by the peer (remote arrive), one phase per tile
+  // cluster exchange of the den and dY . num partials: data received
+  // (st.async bytes) and receive slots released by the peer (remote arrive),
+  // one phase per tile
   uint64_t *x1_full = in_bar + 6, *x1_free = in_bar + 8;
   // inputs: Q, K on in_bar (needed first, by the features); V, dY on in2_bar
   // (needed from the state increment on), so a tile starts before they land
@@ -153,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // a second MMA-completion barrier, for a group whose epilogue overlaps the
   // group issued after it
   uint64_t *mmb_bar = in_bar + 11;
-  float *rx_den = reinterpret_cast<float *>(smem + lay.rx_den);
+  float *rx = reinterpret_cast<float *>(smem + lay.rx);
   float *s_f = reinterpret_cast<float *>(smem + lay.s_f);
   float *gs_f = reinterpret_cast<float *>(smem + lay.gs_f);
   float *dd = reinterpret_cast<float *>(smem + lay.dd);
@@ -250,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_ones = sb + lay.ones, s_ddb = sb + lay.ddb, s_sb = sb + lay.sb;
   const uint32_t tile_bytes = kTile * D * 2;
   uint32_t in_phase = 0, in2_phase = 0, mma_phase = 0, mmb_phase = 0, rl_phase = 0, x_phase = 0;
-  // the exchange: num partials of all 128 rows (fp32 [128][64]) + den
-  constexpr uint32_t kX1Bytes = 128 * 64 * 4 + 128 * 4;
+  // the exchange: two fp32 row sums for each of the 128 rows
+  constexpr uint32_t kX1Bytes = 2 * kTile * 4;
   const uint32_t peer_x1_full = CS == 2 ? map_peer(smem_u32(x1_full), peer) : 0u;
   const uint32_t peer_x1_free = CS == 2 ? map_peer(smem_u32(x1_free), peer) : 0u;
 
@@ -351,8 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_async_smem();
     cta_sync();
-    // my Q and K tiles are idle until the next tile's loads: the peer may
-    // send its num partials there (signalled off the MMA-issuing thread: the
+    // my receive slots (in usk) are idle until (i): the peer may send its
+    // row partials there (signalled off the MMA-issuing thread: the
     // cluster-scope release waits for this thread's earlier stores)
     if (CS == 2 && tid == 32) mbar_arrive_remote(peer_x1_free);
 
@@ -389,11 +387,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // eq. (19) on the double-float master, and from the updated values the
     // bf16 copies of R and of S (high, low) for the MMAs, fp32 S for the
     // epilogues
-    for (int c = 16 * part; c < 80; c += 16 * kParts) {
+    // (R: 16 columns per part; S, column D, on part 3)
+    {
+      const int c = 16 * part;
       float x[16], h[16], l[16];
-      tmem_ld16(tmem_addr(tb, 32 * q4, kT + c), x);
-      tmem_ld16(tmem_addr(tb, 32 * q4, kRhi + c), h);
-      tmem_ld16(tmem_addr(tb, 32 * q4, kRlo + c), l);
+      tmem_ld16x3(tmem_addr(tb, 32 * q4, kT + c), tmem_addr(tb, 32 * q4, kRhi + c),
+                  tmem_addr(tb, 32 * q4, kRlo + c), x, h, l);
 #pragma unroll
       for (int i = 0; i < 16; ++i) df_add(h[i], l[i], -x[i]);
       tmem_st16(tmem_addr(tb, 32 * q4, kRhi + c), h);
@@ -402,10 +401,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) x[i] = h[i] + l[i];
 #pragma unroll
-        for (int i = 0; i < 16; i += 8)
-          if (c + i + 8 <= D) st_bf16x8(s_rb + sw128_offset(row, c + i, MC), x + i);
-        if (c <= D && D < c + 16) {
-          const float sv = x[D - c];
+        for (int i = 0; i < 16; i += 8) st_bf16x8(s_rb + sw128_offset(row, c + i, MC), x + i);
+      }
+      if (part == kParts - 1) {
+        float xs, hs, ls;
+        tmem_ld1x3(tmem_addr(tb, 32 * q4, kT + D), tmem_addr(tb, 32 * q4, kRhi + D),
+                   tmem_addr(tb, 32 * q4, kRlo + D), xs, hs, ls);
+        df_add(hs, ls, -xs);
+        tmem_st1(tmem_addr(tb, 32 * q4, kRhi + D), hs);
+        tmem_st1(tmem_addr(tb, 32 * q4, kRlo + D), ls);
+        if (row < MC) {
+          const float sv = hs + ls;
           s_f[row] = sv;
           const __nv_bfloat16 hi = __float2bfloat16_rn(sv);
           *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(row, 0)) = hi;
@@ -438,49 +444,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     state_to_smem(tb, kG, q4, part, row, MC, s_gv, gs_f);
     wait_mma();
     {
-      float den;
-      {
-        float dv[16];
-        tmem_ld16(tmem_addr(tb, 32 * q4, kT + D), dv);
-        den = dv[0] + dv[1];
-      }
-      float v[QD], g[QD];
-      tmem_ld16(tmem_addr(tb, 32 * q4, kT + QD * part), v);
-      if (CS == 2) {
-        // once the peer is past its features its Q and K tiles take my
-        // partial num (all 128 rows) and den; each CTA then forms dN' for
-        // every row itself
-        mbar_wait(x1_free, x_phase, p.status, abort_flag);
-        const uint32_t dst = map_peer(s_q, peer);
-#pragma unroll
-        for (int j = 0; j < QD / 4; ++j)
-          st_async_v4(dst + xoff(row, (QD / 4) * part + j, 128), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3],
-                      peer_x1_full);
-        if (part == 0) st_async_f32(map_peer(sb + lay.rx_den + row * 4, peer), den, peer_x1_full);
-        mbar_wait(x1_full, x_phase, p.status, abort_flag);
-        float r[QD];
-#pragma unroll
-        for (int j = 0; j < QD / 4; ++j) ld_shared_v4f(s_q + xoff(row, (QD / 4) * part + j, 128), r + 4 * j);
-#pragma unroll
-        for (int i = 0; i < QD; ++i) v[i] += r[i];
-        den += rx_den[row];
-      }
-      const float inv = 1.0f / den;
-      float dyy = 0.f;
+      // dN = dY / den and dD = -(dY . Y) / den with Y = num / den: only the
+      // row sums den and dY . num are needed, both linear in the features,
+      // so with a CTA pair each CTA forms its partials and the two swap two
+      // floats per row
+      float v[QD], g[QD], dv[16];
+      tmem_ld16x2(tmem_addr(tb, 32 * q4, kT + QD * part), tmem_addr(tb, 32 * q4, kT + D), v, dv);
+      float den = dv[0] + dv[1];
 #pragma unroll
       for (int j = 0; j < QD / 8; ++j) ld_bf16x8(s_dy + sw128_offset(row, QD * part + 8 * j, kTile), g + 8 * j);
+      float dyy = 0.f;
 #pragma unroll
-      for (int i = 0; i < QD; ++i) {
-        const float y = v[i] * inv;
-        dyy = fmaf(g[i], y, dyy);
-        g[i] = live ? g[i] * inv : 0.f;
-      }
-#pragma unroll
-      for (int j = 0; j < QD / 8; ++j) st_bf16x8(s_dy + sw128_offset(row, QD * part + 8 * j, kTile), g + 8 * j);
+      for (int i = 0; i < QD; ++i) dyy = fmaf(g[i], v[i], dyy);
       dot[part * kTile + row] = dyy;
       __syncthreads();
+      float dsum = (dot[row] + dot[kTile + row]) + (dot[2 * kTile + row] + dot[3 * kTile + row]);
+      if (CS == 2) {
+        // the peer's receive slots (in its u row-sum array) are free once it
+        // is past its features
+        if (part == 0) {
+          mbar_wait(x1_free, x_phase, p.status, abort_flag);
+          st_async_f32(map_peer(sb + lay.rx + row * 4, peer), den, peer_x1_full);
+          st_async_f32(map_peer(sb + lay.rx + (kTile + row) * 4, peer), dsum, peer_x1_full);
+        }
+        mbar_wait(x1_full, x_phase, p.status, abort_flag);
+        // a + b == b + a: both CTAs hold the same totals
+        den += rx[row];
+        dsum += rx[kTile + row];
+      }
+      const float inv = 1.0f / den;
+#pragma unroll
+      for (int i = 0; i < QD; ++i) g[i] = live ? g[i] * inv : 0.f;
+#pragma unroll
+      for (int j = 0; j < QD / 8; ++j) st_bf16x8(s_dy + sw128_offset(row, QD * part + 8 * j, kTile), g + 8 * j);
       if (part == 0) {
-        const float dval = live ? -((dot[row] + dot[kTile + row]) + (dot[2 * kTile + row] + dot[3 * kTile + row])) * inv : 0.f;
+        const float dval = live ? -(dsum * inv) * inv : 0.f;
         dd[row] = dval;
         st_bf16_scalar(smem, lay.ddb + n16_offset(row, 0), dval);
       }
@@ -504,16 +502,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     wait_mma();
     {
       const float dval = dd[row];
-      {
-        float v[32];
-        tmem_ld32(tmem_addr(tb, 32 * q4, kT + 32 * part), v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = (32 * part + i > row) ? 0.f : v[i] + dval;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, 32 * part + 8 * j, kTile), v + 8 * j);
-      }
       float v[QD];
-      tmem_ld16(tmem_addr(tb, 32 * q4, kX + QD * part), v);
+      {
+        float a[32];
+        tmem_ld32p16(tmem_addr(tb, 32 * q4, kT + 32 * part), tmem_addr(tb, 32 * q4, kX + QD * part), a, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) a[i] = (32 * part + i > row) ? 0.f : a[i] + dval;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, 32 * part + 8 * j, kTile), a + 8 * j);
+      }
       if (CS == 2) {
         // this CTA's dV partial -> bf16 in the idle Q tile, for a reduce-add
 #pragma unroll
@@ -554,9 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_done();
       if (CS == 2 && t > t0) {
-        // the K tile's num' partial has been read by the exchange epilogue:
-        // the next tile's K streams in while this one finishes (Q follows
-        // once the reduce-add has read the dV partial out of the Q tile)
+        // the K tile is idle since the features: the next tile's K streams
+        // in while this one finishes (Q follows once the reduce-add has read
+        // the dV partial out of the Q tile)
         mbar_arrive_expect_tx(in_bar, 2 * tile_bytes);
         tma_load_3d(smem + lay.k, &tmK, in_bar, 0, (t - 1) * kTile, bh);
       }
@@ -575,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (CS == 2) {
       // the dA tile is idle from here: Q and K come back into it for the
-      // dQ, dK epilogue (the Q tile holds the dV partial, K took num')
+      // dQ, dK epilogue (the Q tile holds the dV partial, K the next K)
       if (tid == 0) {
         mbar_arrive_expect_tx(rl_bar, 2 * tile_bytes);
         tma_load_3d(smem + lay.at, &tmQ, rl_bar, 0, t * kTile, bh);
@@ -597,14 +594,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int j = 0; j < QF / 8; ++j) {
-          float fq[8], fk[8];
+          float fq[8], fk[8], sv[8], gv[8];
           ld_bf16x8(s_phq + sw128_offset(row, c0 + 8 * j, kTile), fq);
           ld_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), fk);
+          // S and G_S of these 8 features (the same for every row): 128-bit loads
+          *reinterpret_cast<float4 *>(sv) = *reinterpret_cast<const float4 *>(s_f + c0 + 8 * j);
+          *reinterpret_cast<float4 *>(sv + 4) = *reinterpret_cast<const float4 *>(s_f + c0 + 8 * j + 4);
+          *reinterpret_cast<float4 *>(gv) = *reinterpret_cast<const float4 *>(gs_f + c0 + 8 * j);
+          *reinterpret_cast<float4 *>(gv + 4) = *reinterpret_cast<const float4 *>(gs_f + c0 + 8 * j + 4);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const int m = c0 + 8 * j + i;
-            const float dq = fmaf(dval, s_f[m], a[8 * j + i]);
-            const float dk = b[8 * j + i] + gs_f[m];
+            const float dq = fmaf(dval, sv[i], a[8 * j + i]);
+            const float dk = b[8 * j + i] + gv[i];
             if (FAVOR) {
               a[8 * j + i] = fq[i] * dq;
               b[8 * j + i] = fk[i] * dk;
