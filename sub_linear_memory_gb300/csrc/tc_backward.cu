@@ -530,7 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_store_commit();
     }
 
-    // (h) dphi_q, dphi_k, G update
+    // (h) dphi_q -> T, dphi_k -> X (one commit: u needs only these), then
+    // the G update (its own commit: it runs under u, which leaves phi_q, dN
+    // and dD, the update's operands, in place)
     if (tid == 0) {
       const uint32_t id_q1 = make_idesc(128, MC, false, true);
       const uint32_t id_q2 = make_idesc(128, MC, false, false);
@@ -543,6 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_bf16(tb + kX, desc_mnmajor(s_at, kTile, 0, s), desc_mnmajor(s_phq, kTile, 0, s), id_k1, s > 0);
       for (int s = 0; s < D / 16; ++s)
         mma_bf16(tb + kX, desc_kmajor(s_v, kTile, 0, s), desc_kmajor(s_gv, MC, 0, s), id_q2, 1);
+      mma_commit(mmb_bar);
       const uint32_t id_g = make_idesc(128, D, true, true);
       const uint32_t id_g1 = make_idesc(128, 16, true, true);
       for (int s = 0; s < kTile / 16; ++s) {
@@ -558,16 +561,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(smem + lay.k, &tmK, in_bar, 0, (t - 1) * kTile, bh);
       }
     }
-    wait_mma();
-    // the next tile's inputs stream in as their tiles fall idle: dY and V
-    // from here; Q and K at (h) with a CTA pair, at the end of the tile alone
+    wait_mmb();
+    // the next tile's inputs stream in as their tiles fall idle: V from
+    // here, dY once the G update has read dN; Q and K at (h) with a CTA
+    // pair, at the end of the tile alone
     if (tid == 0 && t > t0) {
       if (CS == 2) {
         tma_store_wait_read();
         tma_load_3d(smem + lay.q, &tmQ, in_bar, 0, (t - 1) * kTile, bh);
       }
       mbar_arrive_expect_tx(in2_bar, 2 * tile_bytes);
-      tma_load_3d(smem + lay.dy, &tmDY, in2_bar, 0, (t - 1) * kTile, bh);
       tma_load_3d(smem + lay.v, &tmV, in2_bar, 0, (t - 1) * kTile, bh);
     }
     if (CS == 2) {
@@ -580,7 +583,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
 
-    // (i) u = phi * dphi (in place over phi), row sums; elu+1 writes dQ, dK here
+    // (i) u = phi * dphi, row sums; FAVOR+: u as bf16 pairs into TMEM over
+    // dphi (the A operand of (j)); elu+1 writes dQ, dK here
     {
       const float dval = dd[row];
       float uq = 0.f, uk = 0.f;
@@ -618,10 +622,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (FAVOR) {
+          // feature m of u -> column m / 2 (low half of the pair first); the
+          // four parts of a row share its TMEM lane, so every part's dphi
+          // loads complete before any part stores
+          float pq[QF / 2], pk[QF / 2];
 #pragma unroll
-          for (int j = 0; j < QF / 8; ++j) {
-            st_bf16x8(s_phq + sw128_offset(row, c0 + 8 * j, kTile), a + 8 * j);
-            st_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), b + 8 * j);
+          for (int x = 0; x < QF / 2; ++x) {
+            pq[x] = __uint_as_float(pack_bf16(a[2 * x], a[2 * x + 1]));
+            pk[x] = __uint_as_float(pack_bf16(b[2 * x], b[2 * x + 1]));
+          }
+          named_barrier_sync(1 + q4, kParts * 32);
+          if constexpr (QF == 32) {
+            tmem_st16(tmem_addr(tb, 32 * q4, kT + c0 / 2), pq);
+            tmem_st16(tmem_addr(tb, 32 * q4, kX + c0 / 2), pk);
+          } else {
+            tmem_st8(tmem_addr(tb, 32 * q4, kT + c0 / 2), pq);
+            tmem_st8(tmem_addr(tb, 32 * q4, kX + c0 / 2), pk);
           }
         } else if (live) {
           uint4 *gq = reinterpret_cast<uint4 *>(p.dq + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + c0);
@@ -638,16 +654,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       usq[part * kTile + row] = uq;
       usk[part * kTile + row] = uk;
     }
-    fence_async_smem();
+    if (FAVOR) tmem_st_wait();
     cta_sync();
+    wait_mma();  // the G update: dN's tile takes the next dY
+    if (tid == 0 && t > t0) tma_load_3d(smem + lay.dy, &tmDY, in2_bar, 0, (t - 1) * kTile, bh);
 
     if (FAVOR) {
-      // (j) dQ = u_q W^T - q rowsum(u_q), dK likewise
+      // (j) dQ = u_q W^T - q rowsum(u_q) -> T + 64, dK likewise -> X + 64
       if (tid == 0) {
         const uint32_t id = make_idesc(128, D, false, true);
         for (int s = 0; s < MC / 16; ++s) {
-          mma_bf16(tb + kT, desc_kmajor(s_phq, kTile, 0, s), desc_mnmajor(s_w, MC, 0, s), id, s > 0);
-          mma_bf16(tb + kT + 64, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_w, MC, 0, s), id, s > 0);
+          mma_bf16_ta(tb + kT + 64, tb + kT + 8 * s, desc_mnmajor(s_w, MC, 0, s), id, s > 0);
+          mma_bf16_ta(tb + kX + 64, tb + kX + 8 * s, desc_mnmajor(s_w, MC, 0, s), id, s > 0);
         }
         mma_done();
       }
@@ -655,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sq = (usq[row] + usq[kTile + row]) + (usq[2 * kTile + row] + usq[3 * kTile + row]);
       const float sk = (usk[row] + usk[kTile + row]) + (usk[2 * kTile + row] + usk[3 * kTile + row]);
       float a[QD], b[QD];
-      tmem_ld16x2(tmem_addr(tb, 32 * q4, kT + QD * part), tmem_addr(tb, 32 * q4, kT + 64 + QD * part), a, b);
+      tmem_ld16x2(tmem_addr(tb, 32 * q4, kT + 64 + QD * part), tmem_addr(tb, 32 * q4, kX + 64 + QD * part), a, b);
       uint32_t s_xq = s_q, s_xk = s_k;
       if (CS == 2) {
         mbar_wait(rl_bar, rl_phase, p.status, abort_flag);

@@ -732,5 +732,14 @@ __device__ __forceinline__ void tmem_ld32p16(uint32_t a0, uint32_t a1, float *v0
   for (int i = 0; i < 16; ++i) v1[i] = __uint_as_float(r[32 + i]);
 }
 
+// 8 consecutive fp32 columns into this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float *v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+               "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+               "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+               : "memory");
+}
+
 }  // namespace tc
 }  // namespace slim
