@@ -57,7 +57,7 @@ struct Params {
 
 struct Layout {
   uint32_t w, q, k, v, dy, phq, phk, at, gv, rb, ones, ddb;
-  uint32_t sb, s_f, gs_f, dd, usq, usk, dot, rx, bars, total;
+  uint32_t asum, s_f, gs_f, dd, usq, usk, dot, rx, bars, total;
   __host__ __device__ explicit Layout(int MC) {
     uint32_t o = 0;
     const uint32_t tile = kTile * D * 2;
@@ -73,7 +73,7 @@ struct Layout {
     rb = o; o += (uint32_t)MC * 128u;
     ones = o; o += 4096;
     ddb = o; o += 4096;
-    sb = o; o += (uint32_t)MC * 32u;  // [MC][16] no-swizzle: S high, S low
+    asum = o; o += kParts * kTile * 4;  // [part][row]: row sums of tril(A), then den partials
     s_f = o; o += 128 * 4;
     gs_f = o; o += 128 * 4;
     dd = o; o += kTile * 4;
@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *usq = reinterpret_cast<float *>(smem + lay.usq);
   float *usk = reinterpret_cast<float *>(smem + lay.usk);
   float *dot = reinterpret_cast<float *>(smem + lay.dot);
+  float *asum = reinterpret_cast<float *>(smem + lay.asum);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q4 = warp & 3, part = warp >> 2, row = 32 * q4 + lane;
@@ -197,7 +198,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = idx >> 4, x = idx & 15;
     st_bf16_scalar(smem, lay.ones + n16_offset(r, x), x == 0 ? 1.f : 0.f);
     st_bf16_scalar(smem, lay.ddb + n16_offset(r, x), 0.f);
-    if (r < MC) st_bf16_scalar(smem, lay.sb + n16_offset(r, x), 0.f);
   }
   tc_fence_before();
   __syncthreads();
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_w = sb + lay.w, s_q = sb + lay.q, s_k = sb + lay.k, s_v = sb + lay.v;
   const uint32_t s_dy = sb + lay.dy, s_phq = sb + lay.phq, s_phk = sb + lay.phk;
   const uint32_t s_at = sb + lay.at, s_gv = sb + lay.gv, s_rb = sb + lay.rb;
-  const uint32_t s_ones = sb + lay.ones, s_ddb = sb + lay.ddb, s_sb = sb + lay.sb;
+  const uint32_t s_ones = sb + lay.ones, s_ddb = sb + lay.ddb;
   const uint32_t tile_bytes = kTile * D * 2;
   uint32_t in_phase = 0, in2_phase = 0, mma_phase = 0, mmb_phase = 0, rl_phase = 0, x_phase = 0;
   // the exchange: two fp32 row sums for each of the 128 rows
@@ -373,21 +373,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_done();
     }
     wait_mmb();
-    // tril(A) (diagonal kept) -> bf16 tile
+    // tril(A) (diagonal kept) -> bf16 tile, and this part's row sum of it
     {
       float v[32];
       tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * part), v);
+      float r4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
+      for (int i = 0; i < 32; ++i) {
         if (32 * part + i > row) v[i] = 0.f;
+        r4[i & 3] += v[i];
+      }
+      asum[part * kTile + row] = (r4[0] + r4[1]) + (r4[2] + r4[3]);
 #pragma unroll
       for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, 32 * part + 8 * j, kTile), v + 8 * j);
     }
     wait_mma();
     // eq. (19) on the double-float master, and from the updated values the
-    // bf16 copies of R and of S (high, low) for the MMAs, fp32 S for the
-    // epilogues
-    // (R: 16 columns per part; S, column D, on part 3)
+    // bf16 copy of R for the MMAs and fp32 S for the epilogues (R: 16
+    // columns per part; S, column D, on part 3)
     {
       const int c = 16 * part;
       float x[16], h[16], l[16];
@@ -410,37 +413,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         df_add(hs, ls, -xs);
         tmem_st1(tmem_addr(tb, 32 * q4, kRhi + D), hs);
         tmem_st1(tmem_addr(tb, 32 * q4, kRlo + D), ls);
-        if (row < MC) {
-          const float sv = hs + ls;
-          s_f[row] = sv;
-          const __nv_bfloat16 hi = __float2bfloat16_rn(sv);
-          *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(row, 0)) = hi;
-          *reinterpret_cast<__nv_bfloat16 *>(smem + lay.sb + n16_offset(row, 1)) =
-              __float2bfloat16_rn(sv - __bfloat162float(hi));
-        }
+        if (row < MC) s_f[row] = hs + ls;
       }
     }
     tmem_st_wait();
     fence_async_smem();
     cta_sync();
 
-    // (f) num' = A [V, 1] + phi_q [R, S]^T -> T (den = columns d, d + 1); Y, dN, dD
+    // (f) num = A V + phi_q R^T -> T; Y, dN, dD.  den = rowsum(tril A) +
+    // phi_q . S comes from the CUDA cores while the MMAs run
     if (tid == 0) {
       const uint32_t id = make_idesc(128, D, false, true);
-      const uint32_t id1 = make_idesc(128, 16, false, true);
-      for (int s = 0; s < kTile / 16; ++s) {
+      for (int s = 0; s < kTile / 16; ++s)
         mma_bf16(tb + kT, desc_kmajor(s_at, kTile, 0, s), desc_mnmajor(s_v, kTile, 0, s), id, s > 0);
-        mma_bf16(tb + kT + D, desc_kmajor(s_at, kTile, 0, s), desc_n16(s_ones, s), id1, s > 0);
-      }
-      for (int s = 0; s < MC / 16; ++s) {
+      for (int s = 0; s < MC / 16; ++s)
         mma_bf16(tb + kT, desc_kmajor(s_phq, kTile, 0, s), desc_mnmajor(s_rb, MC, 0, s), id, 1);
-        mma_bf16(tb + kT + D, desc_kmajor(s_phq, kTile, 0, s), desc_n16(s_sb, s), id1, 1);
-      }
       mma_done();
     }
-    // while the MMAs run: the bf16 copy of G_V (G as the last tile left it)
-    // into its tile, whose last reader (the previous dQ reduce-add with a
-    // CTA pair) was waited for in (c); G_S as fp32
+    {
+      // this thread's features of phi_q . S (S after eq. (19), fp32), added
+      // to its part of rowsum(tril A) in its own slot
+      const int c0 = QF * part;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < QF / 8; ++j) {
+        float fq[8], sv[8];
+        ld_bf16x8(s_phq + sw128_offset(row, c0 + 8 * j, kTile), fq);
+        *reinterpret_cast<float4 *>(sv) = *reinterpret_cast<const float4 *>(s_f + c0 + 8 * j);
+        *reinterpret_cast<float4 *>(sv + 4) = *reinterpret_cast<const float4 *>(s_f + c0 + 8 * j + 4);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i & 3] = fmaf(fq[i], sv[i], acc[i & 3]);
+      }
+      asum[part * kTile + row] += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    }
+    // also while the MMAs run: the bf16 copy of G_V (G as the last tile
+    // left it) into its tile, whose last reader (the previous dQ reduce-add
+    // with a CTA pair) was waited for in (c); G_S as fp32
     state_to_smem(tb, kG, q4, part, row, MC, s_gv, gs_f);
     wait_mma();
     {
@@ -448,9 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // row sums den and dY . num are needed, both linear in the features,
       // so with a CTA pair each CTA forms its partials and the two swap two
       // floats per row
-      float v[QD], g[QD], dv[16];
-      tmem_ld16x2(tmem_addr(tb, 32 * q4, kT + QD * part), tmem_addr(tb, 32 * q4, kT + D), v, dv);
-      float den = dv[0] + dv[1];
+      float v[QD], g[QD];
+      tmem_ld16(tmem_addr(tb, 32 * q4, kT + QD * part), v);
 #pragma unroll
       for (int j = 0; j < QD / 8; ++j) ld_bf16x8(s_dy + sw128_offset(row, QD * part + 8 * j, kTile), g + 8 * j);
       float dyy = 0.f;
@@ -459,6 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       dot[part * kTile + row] = dyy;
       __syncthreads();
       float dsum = (dot[row] + dot[kTile + row]) + (dot[2 * kTile + row] + dot[3 * kTile + row]);
+      float den = (asum[row] + asum[kTile + row]) + (asum[2 * kTile + row] + asum[3 * kTile + row]);
       if (CS == 2) {
         // the peer's receive slots (in its u row-sum array) are free once it
         // is past its features
