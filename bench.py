@@ -300,7 +300,9 @@ def run_native(args, wl):
     q, k, v, dy, w = inputs.make_inputs(wl, device="cuda")
     y = torch.empty_like(q)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    out = (dq, dk, dv, None)
+    # learnable W: the backward also returns dW (fp32 [d, M])
+    dw = torch.empty((wl.d, wl.M), dtype=torch.float32, device=q.device) if (args.dw and w is not None) else None
+    out = (dq, dk, dv, dw)
 
     def step():
         binding.slim_attn_fwd(q, k, v, w, wl.chunk, y=y)
@@ -376,7 +378,7 @@ def run_native(args, wl):
                 stream.wait_event(ev_read[b])  # step i-2's outputs have left outs[b]
             o = outs[b]
             binding.slim_attn_fwd(ins[b][0], ins[b][1], ins[b][2], w, wl.chunk, y=o[0])
-            binding.slim_attn_bwd(ins[b][0], ins[b][1], ins[b][2], w, ins[b][3], wl.chunk, out=(o[1], o[2], o[3], None))
+            binding.slim_attn_bwd(ins[b][0], ins[b][1], ins[b][2], w, ins[b][3], wl.chunk, out=(o[1], o[2], o[3], dw))
             ev_done[b].record(stream)
             d2h_s.wait_event(ev_done[b])
             with torch.cuda.stream(d2h_s):
@@ -434,7 +436,7 @@ def run_native(args, wl):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Gaussian Q, K, V, dY; block-orthogonal random W)",
-        "config": config_of(wl, world),
+        "config": dict(config_of(wl, world), **({"learnable_w": "dW computed by the backward"} if dw is not None else {})),
         "clocks": clocks.summary(),
         "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": 4 * nbytes, "d2h_bytes_per_step": 4 * nbytes,
@@ -533,6 +535,8 @@ def main(argv=None):
     ap.add_argument("--heads", default=None,
                     help="BxH: run the workload's recipe with another batch and head count "
                          "(a reduced case for profiling); the default is the workload's own")
+    ap.add_argument("--dw", action="store_true",
+                    help="learnable W: the backward also computes dW")
     ap.add_argument("--no-memory", dest="memory", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-row-frac", type=float, default=1.0,

@@ -633,6 +633,13 @@ cudaError_t scan_states_df(const Plan &p, float *hi, float *lo, int nseg, int lo
   return cudaGetLastError();
 }
 
+cudaError_t reduce_dw(const Plan &p, const float *parts, float *dw, cudaStream_t st) {
+  const int n = p.d * p.M;
+  ProfScope ps("reduce_dw", st);
+  gen::reduce_dw_kernel<<<(n + 255) / 256, 256, 0, st>>>(p, parts, dw);
+  return cudaGetLastError();
+}
+
 cudaError_t scan_states_f32_rev(const Plan &p, float *states, int nseg, cudaStream_t st) {
   gen::scan_states_f32_kernel<<<scan_blocks(p), 256, 0, st>>>(p, states, nseg, 1);
   return cudaGetLastError();

@@ -36,6 +36,8 @@ cudaError_t scan_states_f32(const Plan &p, float *states, int nseg, cudaStream_t
 cudaError_t scan_states_f32_rev(const Plan &p, float *states, int nseg, cudaStream_t st);
 // The same forward scan for double-float (hi, lo) states, summed in fp64.
 cudaError_t scan_states_df(const Plan &p, float *hi, float *lo, int nseg, int lo_in, cudaStream_t st);
+// dW [d][M] = the sum, in a fixed order, of the BH x P per-segment partials.
+cudaError_t reduce_dw(const Plan &p, const float *parts, float *dw, cudaStream_t st);
 
 // Tensor-core family (tc_forward.cu): bf16 I/O, 128-row tiles.
 bool tc_forward_supported(int d, int M, int chunk, bool favor);
@@ -48,6 +50,10 @@ cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, bool zero_
 // dK, dV += the terms of the later segments' reverse state (after the backward
 // kernel and the reverse scan of the segment G totals).
 cudaError_t tc_correction(const Plan &p, const Args &a, cudaStream_t st);
+// Learnable W (FAVOR+): the later segments' reverse-state terms of dW, added
+// to the per-segment partials (after tc_correction, which builds the G_end
+// images it reads).
+cudaError_t tc_dw_correction(const Plan &p, const Args &a, cudaStream_t st);
 
 // Serving form (decode.cu, generic.cu): the state after L rows, fp32
 // e-major [BH][d + 1][M], and one decode step for every head.

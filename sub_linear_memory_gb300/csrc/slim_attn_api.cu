@@ -180,7 +180,7 @@ slim_status run(bool bwd, const void *q, const void *k, const void *v, const flo
   if (!bwd && !y) return SLIM_ERR_INVALID_ARG;
   if (bwd && (!dy || !dq || !dk || !dv)) return SLIM_ERR_INVALID_ARG;
   const bool io_ok = sizeof(T) == 2 && g_opt_path != 1 && aligned16(q) && aligned16(k) && aligned16(v);
-  const bool tc = io_ok && (bwd ? (dw == nullptr && tc_backward_supported(d, M, chunk, favor) &&
+  const bool tc = io_ok && (bwd ? (tc_backward_supported(d, M, chunk, favor) &&
                                    aligned16(dy) && aligned16(dq) && aligned16(dk) && aligned16(dv))
                                 : (tc_forward_supported(d, M, chunk, favor) && aligned16(y)));
   Plan p = make_plan(B, H, L, d, M, chunk, favor, bwd, dw != nullptr, tc ? 2 : 1);

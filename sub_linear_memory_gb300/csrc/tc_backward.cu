@@ -52,6 +52,7 @@ struct Params {
   const float *states;     // fp32 [BH][P][M][D + 1]: inclusive segment-end R', high parts
   const float *states_lo;  // low parts
   float *gstates;          // fp32 [BH][P][M][D + 1]: segment totals of G (out) / G_end (in)
+  float *dwpart;           // learnable W: fp32 [BH][P][D][M] dW partial of each segment (added to)
   int *status;
 };
 
@@ -121,7 +122,10 @@ __device__ __forceinline__ void state_to_smem(uint32_t tbase, uint32_t col, int 
 // locally, and the two swap through distributed shared memory the row sums
 // den and dY . num, so both form the same dN' for all 128 rows.  dV, dQ and
 // dK partials go to global memory by TMA reduce-add.
-template <bool FAVOR, int CS, int MC>
+// DW (learnable W, FAVOR+): each tile also forms dW^T = u_q^T Q + u_k^T K for
+// this CTA's features on the tensor cores (u in the phi tiles, the result in
+// the TMEM columns u leaves free) and adds it to the segment's dW partial.
+template <bool FAVOR, int CS, int MC, bool DW>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDY,
@@ -592,7 +596,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // (i) u = phi * dphi, row sums; FAVOR+: u as bf16 pairs into TMEM over
-    // dphi (the A operand of (j)); elu+1 writes dQ, dK here
+    // dphi (the A operand of (j)); elu+1 writes dQ, dK here.  With DW, u_k
+    // also goes over phi_k (no MMA reads it any more) and u_q over phi_q
+    // once the G update has read phi_q
+    uint32_t uq_pairs[QF / 2];
     {
       const float dval = dd[row];
       float uq = 0.f, uk = 0.f;
@@ -647,6 +654,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st8(tmem_addr(tb, 32 * q4, kT + c0 / 2), pq);
             tmem_st8(tmem_addr(tb, 32 * q4, kX + c0 / 2), pk);
           }
+          if (DW) {
+#pragma unroll
+            for (int j = 0; j < QF / 8; ++j)
+              st_shared_v4(s_phk + sw128_offset(row, c0 + 8 * j, kTile), __float_as_uint(pk[4 * j]),
+                           __float_as_uint(pk[4 * j + 1]), __float_as_uint(pk[4 * j + 2]),
+                           __float_as_uint(pk[4 * j + 3]));
+#pragma unroll
+            for (int x = 0; x < QF / 2; ++x) uq_pairs[x] = __float_as_uint(pq[x]);
+          }
         } else if (live) {
           uint4 *gq = reinterpret_cast<uint4 *>(p.dq + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + c0);
           uint4 *gk = reinterpret_cast<uint4 *>(p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + c0);
@@ -666,6 +682,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     cta_sync();
     wait_mma();  // the G update: dN's tile takes the next dY
     if (tid == 0 && t > t0) tma_load_3d(smem + lay.dy, &tmDY, in2_bar, 0, (t - 1) * kTile, bh);
+    if (DW) {
+      // phi_q has been read by the G update: u_q over it, for the dW MMAs
+      const int c0 = QF * part;
+#pragma unroll
+      for (int j = 0; j < QF / 8; ++j)
+        st_shared_v4(s_phq + sw128_offset(row, c0 + 8 * j, kTile), uq_pairs[4 * j], uq_pairs[4 * j + 1],
+                     uq_pairs[4 * j + 2], uq_pairs[4 * j + 3]);
+      fence_async_smem();
+      cta_sync();
+    }
 
     if (FAVOR) {
       // (j) dQ = u_q W^T - q rowsum(u_q) -> T + 64, dK likewise -> X + 64
@@ -688,6 +714,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         rl_phase ^= 1;
         s_xq = sb + lay.at;
         s_xk = sb + lay.at + tile_bytes;
+      }
+      if (DW && tid == 0) {
+        // dW^T = u_q^T Q + u_k^T K (features on the lanes) -> T: the dQ, dK
+        // MMAs have read u's TMEM pairs there
+        const uint32_t id_w = make_idesc(128, D, true, true);
+        for (int s = 0; s < kTile / 16; ++s)
+          mma_bf16(tb + kT, desc_mnmajor(s_phq, kTile, 0, s), desc_mnmajor(s_xq, kTile, 0, s), id_w, s > 0);
+        for (int s = 0; s < kTile / 16; ++s)
+          mma_bf16(tb + kT, desc_mnmajor(s_phk, kTile, 0, s), desc_mnmajor(s_xk, kTile, 0, s), id_w, 1);
+        mma_commit(mmb_bar);
       }
       // dQ = u_q W^T - q rowsum(u_q), dK likewise (this CTA's features)
       float oq[QD], ok[QD];
@@ -725,6 +761,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                              pack_bf16(oq[8 * j + 4], oq[8 * j + 5]), pack_bf16(oq[8 * j + 6], oq[8 * j + 7]));
           gk[j] = make_uint4(pack_bf16(ok[8 * j], ok[8 * j + 1]), pack_bf16(ok[8 * j + 2], ok[8 * j + 3]),
                              pack_bf16(ok[8 * j + 4], ok[8 * j + 5]), pack_bf16(ok[8 * j + 6], ok[8 * j + 7]));
+        }
+      }
+      if (DW) {
+        // this tile's dW^T rows (features fbase + row, 16 value columns per
+        // part) into the segment's partial dW [D][M]: one thread owns each
+        // element, so a plain read-add-write
+        wait_mmb();
+        float wv[16];
+        tmem_ld16(tmem_addr(tb, 32 * q4, kT + 16 * part), wv);
+        if (row < MC) {
+          float *dst = p.dwpart + (((size_t)bh * p.P + seg) * D + 16 * part) * (size_t)M + fbase + row;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) dst[(size_t)i * M] += wv[i];
         }
       }
       cta_sync();
@@ -777,6 +826,12 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
                   !make_map_bf16_3d(&mdv, a.dv, pl.BH, pl.L, D, kTile)))
     return cudaErrorInvalidValue;
   if (CS == 1) mdq = mdk = mdv = mq;  // unused
+  const bool want_dw = FAVOR && a.dw != nullptr;
+  float *dwpart = a.ws + pl.dwpart_off;
+  if (want_dw) {
+    cudaError_t e = cudaMemsetAsync(dwpart, 0, sizeof(float) * (size_t)pl.BH * pl.P * D * pl.M, st);
+    if (e != cudaSuccess) return e;
+  }
   // R' totals of every segment, scanned; with two CTAs per segment the
   // outputs start at zero for the per-CTA reduce-adds
   cudaError_t e = tc_segment_states(pl, a, pl.P, CS == 2, st);
@@ -792,11 +847,12 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
   p.states = a.ws + pl.states_off;
   p.states_lo = a.ws + pl.states_lo_off;
   p.gstates = a.ws + pl.gstates_off;
+  p.dwpart = dwpart;
   p.status = a.status;
   {
     const Layout lay(pl.M / CS);
     const int smem = (int)lay.total + 1024;
-    auto kern = tc_bwd_kernel<FAVOR, CS, MC>;
+    auto kern = want_dw ? tc_bwd_kernel<FAVOR, CS, MC, FAVOR> : tc_bwd_kernel<FAVOR, CS, MC, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (CS > 1) {
@@ -827,7 +883,12 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
       if (e != cudaSuccess) return e;
     }
     e = tc_correction(pl, a, st);
+    if (e != cudaSuccess) return e;
+    // dW's share of the later segments' reverse state
+    if (want_dw) e = tc_dw_correction(pl, a, st);
+    if (e != cudaSuccess) return e;
   }
+  if (want_dw) e = reduce_dw(pl, dwpart, a.dw, st);
   return e;
 }
 

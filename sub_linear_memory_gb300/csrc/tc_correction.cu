@@ -487,6 +487,224 @@ __global__ void prep_g_kernel(const float *__restrict__ gstates, unsigned char *
   }
 }
 
+// ---------------------------------------------------------------------------
+// dW's share of the later segments' reverse state (FAVOR+, learnable W).
+// For a row k of segment s, with G = G_end(s):
+//   dphi_k' = V G_V^T + G_S,  u' = phi_k * dphi_k',  dW += k^T u'
+// (the same u' whose u' W^T the correction kernel adds to dK).  One CTA per
+// (segment < P - 1, head) walks the segment's tiles in order, 512 threads,
+// four per row (TMEM lane quadrant w % 4, a quarter of the features each):
+//   F = K W -> TMEM; phi_k -> shared tile; D = V G_V^T -> the same TMEM
+//   columns; u' = phi_k * (D + G_S) over phi_k in place; dW^T += u'^T K on
+//   the tensor cores (features on the lanes, accumulated over the segment)
+// K and V are double-buffered: tile t + 1 loads while tile t computes.  The
+// segment's dW^T is added to its partial [D][M] at the end.
+struct DwParams {
+  int L, P, tps, nt, BH, M;
+  const __nv_bfloat16 *wimg;  // W^T image [M][64]
+  const unsigned char *grec;  // per (head, segment): G_end image [M][64] bf16, then G_S fp32 [M]
+  float *dwpart;              // fp32 [BH][P][D][M]
+  int *status;
+};
+
+template <int M>
+struct DwLayout {
+  static constexpr uint32_t kPhCols = M < 128 ? 128 : M;
+  uint32_t w, g, gs, kv, ph, nrm, bars, total;
+  __host__ __device__ DwLayout() {
+    uint32_t o = 0;
+    w = o; o += M * 128u;
+    g = o; o += M * 128u;
+    gs = o; o += M * 4u;  // directly after g: one bulk copy of the record
+    o = (o + 1023u) & ~1023u;
+    kv = o; o += 2 * 2 * kTileBytes;      // [buffer][K, V]
+    ph = o; o += kTile * kPhCols * 2u;    // phi_k, then u', [row][feature] swizzled
+    nrm = o; o += 4 * kTile * 4u;         // [part][row] partial |k|^2
+    bars = o; o += 64;
+    total = o;
+  }
+};
+
+template <int M>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_dw_corr_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, DwParams p) {
+  constexpr int nb = (M + 127) / 128;       // 128-feature blocks (dW MMAs)
+  constexpr int QF = M / 4;                 // features per thread
+  constexpr uint32_t kFD = 0, kW = M;       // TMEM: F, then D | dW^T, nb x 64 columns
+  constexpr uint32_t kCols = M == 256 ? 512u : (M == 128 ? 256u : 128u);
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char *smem =
+      reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const DwLayout<M> lay;
+  const uint32_t sb = smem_u32(smem);
+  uint64_t *ld_bar = reinterpret_cast<uint64_t *>(smem + lay.bars);  // [2]
+  uint64_t *setup_bar = ld_bar + 2;
+  uint64_t *mma_bar = ld_bar + 3;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(ld_bar + 4);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(ld_bar + 5);
+  float *nrm = reinterpret_cast<float *>(smem + lay.nrm);
+  const float *gs = reinterpret_cast<const float *>(smem + lay.gs);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q4 = warp & 3, part = warp >> 2, row = 32 * q4 + lane;
+  const int seg = blockIdx.x, bh = blockIdx.y;
+  const int t0 = seg * p.tps, t1 = min(t0 + p.tps, p.nt);
+  const uint32_t s_w = sb + lay.w, s_g = sb + lay.g, s_ph = sb + lay.ph;
+
+  if (tid == 0) {
+    mbar_init(ld_bar, 1);
+    mbar_init(ld_bar + 1, 1);
+    mbar_init(setup_bar, 1);
+    mbar_init(mma_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    mbar_arrive_expect_tx(setup_bar, (uint32_t)M * 256u + (uint32_t)M * 4u);
+    bulk_load(smem + lay.w, p.wimg, (uint32_t)M * 128u, setup_bar);
+    bulk_load(smem + lay.g, p.grec + ((size_t)bh * p.P + seg) * (size_t)M * 132u, (uint32_t)M * 132u, setup_bar);
+    if (t0 < t1) {
+      mbar_arrive_expect_tx(ld_bar, 2 * kTileBytes);
+      tma_load_3d(smem + lay.kv, &tmK, ld_bar, 0, t0 * kTile, bh);
+      tma_load_3d(smem + lay.kv + kTileBytes, &tmV, ld_bar, 0, t0 * kTile, bh);
+    }
+  }
+  if (warp == 0) tmem_alloc(tslot, kCols);
+  if (M < 128) {  // features beyond M stay zero: the dW MMA reads 128
+    for (int idx = tid; idx < kTile * 128; idx += kThreads) {
+      const int r = idx >> 7, x = idx & 127;
+      if (x >= M) *reinterpret_cast<__nv_bfloat16 *>(smem + lay.ph + sw128_offset(r, x, kTile)) = __float2bfloat16_rn(0.f);
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = *tslot;
+  mbar_wait(setup_bar, 0, p.status, abort_flag);
+
+  uint32_t mphase = 0;
+  auto wait_mma = [&]() {
+    __syncwarp();
+    mbar_wait(mma_bar, mphase, p.status, abort_flag);
+    mphase ^= 1;
+    tc_fence_after();
+  };
+  auto cta_sync = [&]() {
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  };
+  const uint32_t id_f = make_idesc(128, M, false, false);
+  const uint32_t id_w = make_idesc(128, 64, true, true);
+
+  for (int i = 0; t0 + i < t1; ++i) {
+    const int t = t0 + i, b = i & 1;
+    const uint32_t s_k = sb + lay.kv + (uint32_t)b * 2u * kTileBytes, s_v = s_k + kTileBytes;
+    const bool live = row < min(kTile, p.L - t * kTile);
+    mbar_wait(ld_bar + b, (uint32_t)(i >> 1) & 1u, p.status, abort_flag);
+    // F = K W
+    if (tid == 0) {
+      for (int s = 0; s < D / 16; ++s)
+        mma_bf16(tb + kFD, desc_kmajor(s_k, kTile, 0, s), desc_kmajor(s_w, M, 0, s), id_f, s > 0);
+      mma_commit(mma_bar);
+    }
+    nrm[part * kTile + row] = tile_row_sqnorm_part(s_k, row, 16 * part, 16);
+    __syncthreads();
+    const float ck = live ? favor_row_const((nrm[row] + nrm[kTile + row]) + (nrm[2 * kTile + row] + nrm[3 * kTile + row]), M)
+                          : -INFINITY;
+    wait_mma();
+    // every MMA of the previous tile is complete (in order, one commit):
+    // its K, V buffer takes tile t + 1
+    if (tid == 0 && t + 1 < t1) {
+      uint64_t *nb_bar = ld_bar + (b ^ 1);
+      const uint32_t nk = sb + lay.kv + (uint32_t)(b ^ 1) * 2u * kTileBytes;
+      mbar_arrive_expect_tx(nb_bar, 2 * kTileBytes);
+      tma_load_3d(smem + (nk - sb), &tmK, nb_bar, 0, (t + 1) * kTile, bh);
+      tma_load_3d(smem + (nk - sb) + kTileBytes, &tmV, nb_bar, 0, (t + 1) * kTile, bh);
+    }
+    // phi_k (padding rows: F = 0 and 2^-inf = 0)
+#pragma unroll
+    for (int c = 0; c < QF; c += 16) {
+      float v[16];
+      tmem_ld16(tmem_addr(tb, 32 * q4, kFD + QF * part + c), v);
+#pragma unroll
+      for (int x = 0; x < 16; ++x) v[x] = favor_feature(v[x], ck);
+      st_bf16x8(s_ph + sw128_offset(row, QF * part + c, kTile), v);
+      st_bf16x8(s_ph + sw128_offset(row, QF * part + c + 8, kTile), v + 8);
+    }
+    cta_sync();  // F is read out: D may overwrite it
+    // D = V G_V^T
+    if (tid == 0) {
+      for (int s = 0; s < D / 16; ++s)
+        mma_bf16(tb + kFD, desc_kmajor(s_v, kTile, 0, s), desc_kmajor(s_g, M, 0, s), id_f, s > 0);
+      mma_commit(mma_bar);
+    }
+    wait_mma();
+    // u' = phi_k * (D + G_S), over phi_k
+#pragma unroll
+    for (int c = 0; c < QF; c += 16) {
+      const int f0 = QF * part + c;
+      float dv[16], ph[16], g[16];
+      tmem_ld16(tmem_addr(tb, 32 * q4, kFD + f0), dv);
+      ld_bf16x8(s_ph + sw128_offset(row, f0, kTile), ph);
+      ld_bf16x8(s_ph + sw128_offset(row, f0 + 8, kTile), ph + 8);
+#pragma unroll
+      for (int x = 0; x < 16; x += 4) *reinterpret_cast<float4 *>(g + x) = *reinterpret_cast<const float4 *>(gs + f0 + x);
+#pragma unroll
+      for (int x = 0; x < 16; ++x) ph[x] *= dv[x] + g[x];
+      st_bf16x8(s_ph + sw128_offset(row, f0, kTile), ph);
+      st_bf16x8(s_ph + sw128_offset(row, f0 + 8, kTile), ph + 8);
+    }
+    fence_async_smem();
+    cta_sync();
+    // dW^T += u'^T K, per 128-feature block; no commit of its own: the next
+    // tile's F commit covers it (MMAs complete in order), the last one is
+    // committed after the loop
+    if (tid == 0) {
+      for (int h = 0; h < nb; ++h)
+        for (int s = 0; s < kTile / 16; ++s)
+          mma_bf16(tb + kW + 64 * h, desc_mnmajor(s_ph, kTile, 128 * h, s), desc_mnmajor(s_k, kTile, 0, s), id_w,
+                   i > 0 || s > 0);
+    }
+  }
+  if (t0 < t1) {
+    if (tid == 0) mma_commit(mma_bar);
+    wait_mma();
+    if (!*abort_flag) {
+      float *base = p.dwpart + ((size_t)bh * p.P + seg) * (size_t)D * M;
+#pragma unroll
+      for (int h = 0; h < nb; ++h) {
+        float v[16];
+        tmem_ld16(tmem_addr(tb, 32 * q4, kW + 64 * h + 16 * part), v);
+        const int f = 128 * h + row;
+        if (f < M) {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) base[(size_t)(16 * part + x) * M + f] += v[x];
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, kCols);
+}
+
+template <int M>
+cudaError_t launch_dw(const Plan &pl, const Args &a, const CUtensorMap &mk, const CUtensorMap &mv, cudaStream_t st) {
+  DwParams p{};
+  p.L = pl.L; p.P = pl.P; p.tps = pl.cps; p.nt = pl.tc_tiles; p.BH = pl.BH; p.M = M;
+  p.wimg = reinterpret_cast<const __nv_bfloat16 *>(a.ws + pl.wimg_off);
+  p.grec = reinterpret_cast<const unsigned char *>(a.ws + pl.gimg_off);
+  p.dwpart = a.ws + pl.dwpart_off;
+  p.status = a.status;
+  const DwLayout<M> lay;
+  const int smem = (int)lay.total + 1024;
+  auto kern = tc_dw_corr_kernel<M>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(pl.P - 1, pl.BH), kThreads, smem, st>>>(mk, mv, p);
+  return cudaGetLastError();
+}
+
 template <bool FAVOR, int M>
 cudaError_t launch(const Plan &pl, const Args &a, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mdk,
                    const CUtensorMap &mdv, cudaStream_t st) {
@@ -537,6 +755,19 @@ cudaError_t tc_correction(const Plan &pl, const Args &a, cudaStream_t st) {
   if (pl.M == 64) return tcc::launch<true, 64>(pl, a, mk, mv, mdk, mdv, st);
   if (pl.M == 128) return tcc::launch<true, 128>(pl, a, mk, mv, mdk, mdv, st);
   if (pl.M == 256) return tcc::launch<true, 256>(pl, a, mk, mv, mdk, mdv, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t tc_dw_correction(const Plan &pl, const Args &a, cudaStream_t st) {
+  if (pl.P < 2 || !pl.favor || !a.dw) return cudaSuccess;
+  CUtensorMap mk, mv;
+  if (!make_map_bf16_3d(&mk, a.k, pl.BH, pl.L, tcc::D, tcc::kTile) ||
+      !make_map_bf16_3d(&mv, a.v, pl.BH, pl.L, tcc::D, tcc::kTile))
+    return cudaErrorInvalidValue;
+  ProfScope ps("tc_dw_fix", st);
+  if (pl.M == 64) return tcc::launch_dw<64>(pl, a, mk, mv, st);
+  if (pl.M == 128) return tcc::launch_dw<128>(pl, a, mk, mv, st);
+  if (pl.M == 256) return tcc::launch_dw<256>(pl, a, mk, mv, st);
   return cudaErrorInvalidValue;
 }
 

@@ -206,6 +206,26 @@ def test_tensor_core_backward_segments(segments, M, _lib):
         check(name, _np(got), exp, TOL[torch.bfloat16])
 
 
+@pytest.mark.parametrize("M", [64, 128, 256])
+@pytest.mark.parametrize("segments", [1, 3])
+def test_tensor_core_dw(segments, M, _lib):
+    """Learnable W on the tensor path: each tile's X^T u from the backward
+    kernel, plus (segments > 1) the later segments' reverse-state share."""
+    q, k, v, dy, w = small_case(1, 2, 1300, 64, M, 128, torch.bfloat16, "favor", seed=12)
+    _lib.set_option(_lib.OPT_SEGMENTS, segments)
+    try:
+        (dq, dk, dv, dw), names = _run_profiled(
+            _lib, lambda: _lib.slim_attn_bwd(q, k, v, w, dy, 128, want_dw=True))
+    finally:
+        _lib.set_option(_lib.OPT_SEGMENTS, 0)
+    assert "tc_backward" in names and "reduce_dw" in names, names
+    if segments > 1:
+        assert "tc_dw_fix" in names, names
+    ref = oracle.recurrence_backward(_np(q), _np(k), _np(v), _wnp(w), _np(dy), want_dw=True)
+    for name, got, exp in zip(("dQ", "dK", "dV", "dW"), (dq, dk, dv, dw), ref):
+        check(name, _np(got), exp, TOL[torch.bfloat16])
+
+
 def test_tensor_core_backward_long_reversal(_lib):
     """One segment of 160 tiles: the backward removes each tile's state
     increment in turn (eq. (19)); the double-float state keeps the early
