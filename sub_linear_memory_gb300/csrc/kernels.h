@@ -66,5 +66,9 @@ cudaError_t decode_step(const void *q, const void *k, const void *v, const float
 // Tensor-core SLiM backward (tc_backward.cu): bf16 I/O, d = 64, M <= 128.
 bool tc_backward_supported(int d, int M, int chunk, bool favor);
 cudaError_t tc_backward(const Plan &p, const Args &a, cudaStream_t st);
+// elu+1 at d = M = 128 (tc_backward_elu.cu): two-CTA clusters that split the
+// value columns, plus their correction of dK, dV.
+bool tc_backward_elu128_supported(int d, int M, int chunk, bool favor);
+cudaError_t tc_backward_elu128(const Plan &p, const Args &a, cudaStream_t st);
 
 }  // namespace slim

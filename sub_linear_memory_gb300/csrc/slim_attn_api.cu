@@ -142,8 +142,9 @@ Plan make_plan(int B, int H, int L, int d, int M, int chunk, bool favor, bool bw
   p.favor = favor ? 1 : 0;
   p.dp = d + 1;
   p.path = path;
-  // the backward of 256 random features runs each segment on a two-CTA cluster
-  const int cta_per_seg = (path == 2 && bwd && M > 128) ? 2 : 1;
+  // the backward of 256 random features, and of elu+1 at d = 128, runs each
+  // segment on a two-CTA cluster
+  const int cta_per_seg = (path == 2 && bwd && (M > 128 || d == 128)) ? 2 : 1;
   // the tensor backward's correction pass: measured about a third of a
   // backward tile's time per tile and SM (l32k: 4.5 us against 13.2 us)
   const double tail_w = (path == 2 && bwd) ? 0.35 : 0.0;
@@ -159,7 +160,8 @@ Plan make_plan(int B, int H, int L, int d, int M, int chunk, bool favor, bool bw
   p.scratch_off = off; off += p.scratch_stride * p.BH * p.P;
   p.dwpart_off = off; if (bwd && want_dw) off += align_floats((size_t)p.BH * p.P * d * M);
   p.wimg_off = off; if (path == 2 && favor) off += align_floats((size_t)M * 32);
-  p.gimg_off = off; if (path == 2 && bwd) off += align_floats((size_t)p.BH * p.P * M * 33);
+  // bf16 G_end images [M][d] and fp32 G_S [M] per (head, segment)
+  p.gimg_off = off; if (path == 2 && bwd) off += align_floats((size_t)p.BH * p.P * M * (d / 2 + 1));
   p.total_floats = off;
   return p;
 }

@@ -895,11 +895,13 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
 }  // namespace tcb
 
 bool tc_backward_supported(int d, int M, int chunk, bool favor) {
+  if (tc_backward_elu128_supported(d, M, chunk, favor)) return true;
   if (chunk < 64 || d != 64) return false;
   return favor ? (M == 64 || M == 128 || M == 256) : M == 64;
 }
 
 cudaError_t tc_backward(const Plan &p, const Args &a, cudaStream_t st) {
+  if (tc_backward_elu128_supported(p.d, p.M, p.C, p.favor != 0)) return tc_backward_elu128(p, a, st);
   if (p.d != 64) return cudaErrorInvalidValue;
   if (!p.favor) return p.M == 64 ? tcb::backward_family<false, 1, 64>(p, a, st) : cudaErrorInvalidValue;
   if (p.M == 256) return tcb::backward_family<true, 2, 128>(p, a, st);

@@ -160,6 +160,9 @@ TC_BWD_SHAPES = [
     (1, 2, 129, 64, 64, 128, "favor"),    # one tile + a 1-row tail
     (1, 2, 700, 64, 256, 128, "favor"),   # M = 256: a two-CTA cluster per segment
     (2, 1, 300, 64, 256, 64, "favor"),
+    (1, 2, 300, 128, 128, 64, "elu"),     # elu+1 at d = 128: value columns split over a pair
+    (2, 1, 1000, 128, 128, 128, "elu"),
+    (1, 1, 1, 128, 128, 64, "elu"),       # one row
 ]
 
 
@@ -223,6 +226,23 @@ def test_tensor_core_dw(segments, M, _lib):
         assert "tc_dw_fix" in names, names
     ref = oracle.recurrence_backward(_np(q), _np(k), _np(v), _wnp(w), _np(dy), want_dw=True)
     for name, got, exp in zip(("dQ", "dK", "dV", "dW"), (dq, dk, dv, dw), ref):
+        check(name, _np(got), exp, TOL[torch.bfloat16])
+
+
+@pytest.mark.parametrize("segments", [1, 2, 4])
+def test_tensor_core_backward_elu128_segments(segments, _lib):
+    """elu+1 at d = 128: segments > 1 exercise the correction of dK, dV."""
+    q, k, v, dy, w = small_case(1, 2, 1100, 128, 128, 64, torch.bfloat16, "elu", seed=13)
+    _lib.set_option(_lib.OPT_SEGMENTS, segments)
+    try:
+        (dq, dk, dv, _), names = _run_profiled(_lib, lambda: _lib.slim_attn_bwd(q, k, v, w, dy, 64))
+    finally:
+        _lib.set_option(_lib.OPT_SEGMENTS, 0)
+    assert "tc_backward" in names, names
+    if segments > 1:
+        assert "tc_backward_fix" in names, names
+    ref = oracle.recurrence_backward(_np(q), _np(k), _np(v), None, _np(dy), want_dw=False)
+    for name, got, exp in (("dQ", dq, ref[0]), ("dK", dk, ref[1]), ("dV", dv, ref[2])):
         check(name, _np(got), exp, TOL[torch.bfloat16])
 
 
