@@ -559,6 +559,37 @@ __global__ void reduce_dw_kernel(Plan p, const float *parts, float *dw) {
   }
 }
 
+// The same sum for partials of dW^T ([part][M][d], the tensor path):
+// thread (f, group of 4 value columns) reads 16-byte chunks, 8 partials at a time.
+__global__ void reduce_dw_t_kernel(Plan p, const float *parts, float *dw) {
+  const int d = p.d, M = p.M, nq = d / 4;
+  const size_t per = (size_t)M * d;
+  const int nparts = p.BH * p.P;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < M * nq; i += gridDim.x * blockDim.x) {
+    const int f = i / nq, e0 = 4 * (i - f * nq);
+    const float *src = parts + (size_t)f * d + e0;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    int c = 0;
+    for (; c + 8 <= nparts; c += 8) {
+      float4 x[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = *reinterpret_cast<const float4 *>(src + (size_t)(c + j) * per);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        s.x += x[j].x; s.y += x[j].y; s.z += x[j].z; s.w += x[j].w;
+      }
+    }
+    for (; c < nparts; ++c) {
+      const float4 x = *reinterpret_cast<const float4 *>(src + (size_t)c * per);
+      s.x += x.x; s.y += x.y; s.z += x.z; s.w += x.w;
+    }
+    dw[(size_t)(e0 + 0) * M + f] = s.x;
+    dw[(size_t)(e0 + 1) * M + f] = s.y;
+    dw[(size_t)(e0 + 2) * M + f] = s.z;
+    dw[(size_t)(e0 + 3) * M + f] = s.w;
+  }
+}
+
 }  // namespace gen
 
 size_t generic_scratch_floats(const Plan &p, bool bwd) {
@@ -633,10 +664,10 @@ cudaError_t scan_states_df(const Plan &p, float *hi, float *lo, int nseg, int lo
   return cudaGetLastError();
 }
 
-cudaError_t reduce_dw(const Plan &p, const float *parts, float *dw, cudaStream_t st) {
-  const int n = p.d * p.M;
+cudaError_t reduce_dw_t(const Plan &p, const float *parts, float *dw, cudaStream_t st) {
+  const int n = p.M * (p.d / 4);
   ProfScope ps("reduce_dw", st);
-  gen::reduce_dw_kernel<<<(n + 255) / 256, 256, 0, st>>>(p, parts, dw);
+  gen::reduce_dw_t_kernel<<<(n + 127) / 128, 128, 0, st>>>(p, parts, dw);
   return cudaGetLastError();
 }
 

@@ -36,8 +36,9 @@ cudaError_t scan_states_f32(const Plan &p, float *states, int nseg, cudaStream_t
 cudaError_t scan_states_f32_rev(const Plan &p, float *states, int nseg, cudaStream_t st);
 // The same forward scan for double-float (hi, lo) states, summed in fp64.
 cudaError_t scan_states_df(const Plan &p, float *hi, float *lo, int nseg, int lo_in, cudaStream_t st);
-// dW [d][M] = the sum, in a fixed order, of the BH x P per-segment partials.
-cudaError_t reduce_dw(const Plan &p, const float *parts, float *dw, cudaStream_t st);
+// dW [d][M] = the sum, in a fixed order, of the BH x P per-segment partials
+// of dW^T ([M][d] each).
+cudaError_t reduce_dw_t(const Plan &p, const float *parts, float *dw, cudaStream_t st);
 
 // Tensor-core family (tc_forward.cu): bf16 I/O, 128-row tiles.
 bool tc_forward_supported(int d, int M, int chunk, bool favor);

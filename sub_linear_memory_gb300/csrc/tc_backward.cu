@@ -52,7 +52,7 @@ struct Params {
   const float *states;     // fp32 [BH][P][M][D + 1]: inclusive segment-end R', high parts
   const float *states_lo;  // low parts
   float *gstates;          // fp32 [BH][P][M][D + 1]: segment totals of G (out) / G_end (in)
-  float *dwpart;           // learnable W: fp32 [BH][P][D][M] dW partial of each segment (added to)
+  float *dwpart;           // learnable W: fp32 [BH][P][M][D] dW^T partial of each segment (added to)
   int *status;
 };
 
@@ -765,15 +765,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (DW) {
         // this tile's dW^T rows (features fbase + row, 16 value columns per
-        // part) into the segment's partial dW [D][M]: one thread owns each
-        // element, so a plain read-add-write
+        // part) added to the segment's partial dW^T [M][D] without waiting
         wait_mmb();
         float wv[16];
         tmem_ld16(tmem_addr(tb, 32 * q4, kT + 16 * part), wv);
         if (row < MC) {
-          float *dst = p.dwpart + (((size_t)bh * p.P + seg) * D + 16 * part) * (size_t)M + fbase + row;
+          float *dst = p.dwpart + (((size_t)bh * p.P + seg) * M + fbase + row) * D + 16 * part;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) dst[(size_t)i * M] += wv[i];
+          for (int i = 0; i < 16; i += 4) red_add_v4(dst + i, wv[i], wv[i + 1], wv[i + 2], wv[i + 3]);
         }
       }
       cta_sync();
@@ -888,7 +887,7 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
     if (want_dw) e = tc_dw_correction(pl, a, st);
     if (e != cudaSuccess) return e;
   }
-  if (want_dw) e = reduce_dw(pl, dwpart, a.dw, st);
+  if (want_dw) e = reduce_dw_t(pl, dwpart, a.dw, st);
   return e;
 }
 

@@ -530,12 +530,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 //   dK_j += (V_j G^T + G_S) * min(phi_k,j, 1),   dV_j += phi_k,j G
 // One CTA per (segment, head) walks the segment's tiles: phi_k in place over
 // K, then D = V G^T and dV' = phi_k G on the tensor cores (G_end as a bf16
-// [feature][column] image), and a read-add-write of dK, dV rows.  K and V
-// are double-buffered.
+// [feature][column] image); the increments, in bf16 over the tile's own K
+// and V slots, go into dK, dV by TMA reduce-add.  K and V are
+// double-buffered.
 
 struct CorrParams {
   int L, P, tps, nt, BH;
-  __nv_bfloat16 *dk, *dv;
   const unsigned char *grec;  // per (head, segment): G_end image [128][128] bf16, then G_S fp32 [128]
   int *status;
 };
@@ -577,7 +577,8 @@ struct CorrLayout {
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
-    elu_corr_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, CorrParams p) {
+    elu_corr_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV, CorrParams p) {
   constexpr uint32_t kD = 0, kV = 128;  // TMEM: V G^T | phi_k G
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem =
@@ -657,42 +658,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(mma_bar, mphase, p.status, abort_flag);
     mphase ^= 1;
     tc_fence_after();
-    // every MMA up to this tile's is complete: the other buffer takes tile t + 1
-    if (tid == 0 && t + 1 < t1) load(t + 1, b ^ 1);
-    float dk[32], dv[32];
-    tmem_ld32x2(tmem_addr(tb, 32 * q4, kD + 32 * part), tmem_addr(tb, 32 * q4, kV + 32 * part), dk, dv);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int f0 = 32 * part + 8 * j;
-      float ph[8];
-      ld_bf16x8(s_k + sw128_offset(row, f0, kTile), ph);
-#pragma unroll
-      for (int x = 0; x < 8; ++x) dk[8 * j + x] = (dk[8 * j + x] + gs[f0 + x]) * fminf(ph[x], 1.f);
+    // every MMA up to this tile's is complete, and the last tile's reduce-adds
+    // have read their sources: the other buffer takes tile t + 1
+    if (tid == 0 && t + 1 < t1) {
+      if (i > 0) tma_store_wait_read();
+      load(t + 1, b ^ 1);
     }
-    if (live) {
-      const size_t off = ((size_t)bh * p.L + (size_t)t * kTile + row) * D + 32 * part;
-      uint4 *gk = reinterpret_cast<uint4 *>(p.dk + off);
-      uint4 *gv = reinterpret_cast<uint4 *>(p.dv + off);
+    {
+      float dk[32], dv[32];
+      tmem_ld32x2(tmem_addr(tb, 32 * q4, kD + 32 * part), tmem_addr(tb, 32 * q4, kV + 32 * part), dk, dv);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint4 ok = gk[j], ov = gv[j];
-        const uint32_t wk[4] = {ok.x, ok.y, ok.z, ok.w}, wv[4] = {ov.x, ov.y, ov.z, ov.w};
-        uint32_t nk[4], nv[4];
+        const int f0 = 32 * part + 8 * j;
+        const uint32_t ak = s_k + sw128_offset(row, f0, kTile);
+        float ph[8];
+        ld_bf16x8(ak, ph);
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const __nv_bfloat162 hk = *reinterpret_cast<const __nv_bfloat162 *>(&wk[x]);
-          const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162 *>(&wv[x]);
-          nk[x] = pack_bf16(__low2float(hk) + dk[8 * j + 2 * x], __high2float(hk) + dk[8 * j + 2 * x + 1]);
-          nv[x] = pack_bf16(__low2float(hv) + dv[8 * j + 2 * x], __high2float(hv) + dv[8 * j + 2 * x + 1]);
-        }
-        gk[j] = make_uint4(nk[0], nk[1], nk[2], nk[3]);
-        gv[j] = make_uint4(nv[0], nv[1], nv[2], nv[3]);
+        for (int x = 0; x < 8; ++x) dk[8 * j + x] = (dk[8 * j + x] + gs[f0 + x]) * fminf(ph[x], 1.f);
+        // increments in place of this thread's own phi_k and V elements
+        st_bf16x8(ak, dk + 8 * j);
+        st_bf16x8(s_v + sw128_offset(row, f0, kTile), dv + 8 * j);
       }
     }
+    fence_async_smem();
     tc_fence_before();
-    __syncthreads();  // TMEM and phi_k are read out before the next tile's MMAs
+    __syncthreads();  // TMEM and the increments are complete before the next tile's MMAs
     tc_fence_after();
+    if (tid == 0) {
+      for (int c = 0; c < D; c += 64) {
+        tma_reduce_add_3d(&tmDK, s_k + c * kTile * 2, c, t * kTile, bh);
+        tma_reduce_add_3d(&tmDV, s_v + c * kTile * 2, c, t * kTile, bh);
+      }
+      tma_store_commit();
+    }
   }
+  if (tid == 0) tma_store_wait_all();
+  __syncthreads();
   if (warp == 0) tmem_dealloc(tb, 256);
 }
 
@@ -704,10 +705,11 @@ bool tc_backward_elu128_supported(int d, int M, int chunk, bool favor) {
 
 cudaError_t tc_backward_elu128(const Plan &pl, const Args &a, cudaStream_t st) {
   using namespace tce;
-  CUtensorMap mq, mk, mv, mdy, mdq, mdk;
+  CUtensorMap mq, mk, mv, mdy, mdq, mdk, mdv;
   if (!make_map_bf16_3d(&mq, a.q, pl.BH, pl.L, D, kTile) || !make_map_bf16_3d(&mk, a.k, pl.BH, pl.L, D, kTile) ||
       !make_map_bf16_3d(&mv, a.v, pl.BH, pl.L, D, kTile) || !make_map_bf16_3d(&mdy, a.dy, pl.BH, pl.L, D, kTile) ||
-      !make_map_bf16_3d(&mdq, a.dq, pl.BH, pl.L, D, kTile) || !make_map_bf16_3d(&mdk, a.dk, pl.BH, pl.L, D, kTile))
+      !make_map_bf16_3d(&mdq, a.dq, pl.BH, pl.L, D, kTile) || !make_map_bf16_3d(&mdk, a.dk, pl.BH, pl.L, D, kTile) ||
+      !make_map_bf16_3d(&mdv, a.dv, pl.BH, pl.L, D, kTile))
     return cudaErrorInvalidValue;
   // each CTA of a pair adds its share of dQ and dK
   const size_t io_bytes = sizeof(__nv_bfloat16) * (size_t)pl.BH * pl.L * D;
@@ -751,8 +753,6 @@ cudaError_t tc_backward_elu128(const Plan &pl, const Args &a, cudaStream_t st) {
   }
   CorrParams cp{};
   cp.L = pl.L; cp.P = pl.P; cp.tps = pl.cps; cp.nt = pl.tc_tiles; cp.BH = pl.BH;
-  cp.dk = static_cast<__nv_bfloat16 *>(a.dk);
-  cp.dv = static_cast<__nv_bfloat16 *>(a.dv);
   cp.grec = reinterpret_cast<const unsigned char *>(a.ws + pl.gimg_off);
   cp.status = a.status;
   const CorrLayout lay;
@@ -760,7 +760,7 @@ cudaError_t tc_backward_elu128(const Plan &pl, const Args &a, cudaStream_t st) {
   e = cudaFuncSetAttribute(elu_corr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   ProfScope ps("tc_backward_fix", st);
-  elu_corr_kernel<<<dim3(pl.P - 1, pl.BH), kThreads, smem, st>>>(mk, mv, cp);
+  elu_corr_kernel<<<dim3(pl.P - 1, pl.BH), kThreads, smem, st>>>(mk, mv, mdk, mdv, cp);
   return cudaGetLastError();
 }
 

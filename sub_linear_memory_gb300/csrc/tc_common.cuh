@@ -587,6 +587,12 @@ __device__ __forceinline__ void st_peer_v4u(uint32_t addr, uint32_t a, uint32_t 
                : "memory");
 }
 
+// Fire-and-forget add of four consecutive floats into global memory.
+__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
 __device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }

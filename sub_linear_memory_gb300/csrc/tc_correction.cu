@@ -498,12 +498,12 @@ __global__ void prep_g_kernel(const float *__restrict__ gstates, unsigned char *
 //   columns; u' = phi_k * (D + G_S) over phi_k in place; dW^T += u'^T K on
 //   the tensor cores (features on the lanes, accumulated over the segment)
 // K and V are double-buffered: tile t + 1 loads while tile t computes.  The
-// segment's dW^T is added to its partial [D][M] at the end.
+// segment's dW^T is added to its partial [M][D] at the end.
 struct DwParams {
   int L, P, tps, nt, BH, M;
   const __nv_bfloat16 *wimg;  // W^T image [M][64]
   const unsigned char *grec;  // per (head, segment): G_end image [M][64] bf16, then G_S fp32 [M]
-  float *dwpart;              // fp32 [BH][P][D][M]
+  float *dwpart;              // fp32 [BH][P][M][D]: dW^T partials
   int *status;
 };
 
@@ -670,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) mma_commit(mma_bar);
     wait_mma();
     if (!*abort_flag) {
-      float *base = p.dwpart + ((size_t)bh * p.P + seg) * (size_t)D * M;
+      float *base = p.dwpart + ((size_t)bh * p.P + seg) * (size_t)M * D;
 #pragma unroll
       for (int h = 0; h < nb; ++h) {
         float v[16];
@@ -678,7 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int f = 128 * h + row;
         if (f < M) {
 #pragma unroll
-          for (int x = 0; x < 16; ++x) base[(size_t)(16 * part + x) * M + f] += v[x];
+          for (int x = 0; x < 16; x += 4)
+            red_add_v4(base + (size_t)f * D + 16 * part + x, v[x], v[x + 1], v[x + 2], v[x + 3]);
         }
       }
     }
