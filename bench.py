@@ -60,9 +60,9 @@ def work_per_token_head(wl):
 # sources whose digest tags a recorded DRAM-traffic figure (profiles/*.md lines
 # "traffic: <workload> <token-heads> <kernel> <bytes> sources=<digest>")
 KERNEL_SOURCES = {
-    "tc_backward": ("tc_backward.cu", "tc_common.cuh", "common.cuh"),
+    "tc_backward": ("tc_backward.cu", "tc_backward_elu.cu", "tc_common.cuh", "common.cuh"),
     "tc_forward": ("tc_forward.cu", "tc_common.cuh", "common.cuh"),
-    "tc_backward_fix": ("tc_correction.cu", "tc_common.cuh", "common.cuh"),
+    "tc_backward_fix": ("tc_correction.cu", "tc_backward_elu.cu", "tc_common.cuh", "common.cuh"),
 }
 
 
