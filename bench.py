@@ -44,16 +44,19 @@ def load_peaks():
                 "source": "fallback"}
 
 
-def work_per_token_head(wl):
+def work_per_token_head(wl, dw=False):
     """Algorithmic FLOPs and bytes per (token, head): a multiply-add counts 2,
     the causal C x C block counts its triangle, d' = d + 1 carries the
-    normaliser, recomputation is excluded."""
+    normaliser, recomputation is excluded; dw: the backward also forms
+    dW = sum of x^T u over the q and k rows (4 d M)."""
     d, M, C = wl.d, wl.M, wl.chunk
     dp = d + 1
     s = 4 if wl.dtype == "fp32" else 2
     feat = 4 * d * M if wl.feature == "favor" else 0
     fwd = feat + M * (C + 1) + dp * (C + 1) + 4 * M * dp + d
     bwd = dp * (C + 1) + 2 * M * (C + 1) + d * (C + 1) + 8 * M * dp + 2 * M * d + feat
+    if dw and wl.feature == "favor":
+        bwd += 4 * d * M
     return {"fwd_flops": fwd, "bwd_flops": bwd, "fwd_bytes": 4 * d * s, "bwd_bytes": 7 * d * s}
 
 
@@ -399,7 +402,7 @@ def run_native(args, wl):
     nbytes = q.numel() * q.element_size()
 
     # roofline of the dominant kernel (largest share of the timed region)
-    work = work_per_token_head(wl)
+    work = work_per_token_head(wl, dw is not None)
     th = wl.B * wl.H * wl.L
     dom = max(kernels.items(), key=lambda kv: kv[1][1]) if kernels else None
     roofline = None

@@ -64,7 +64,8 @@ template <typename T>
 cudaError_t decode_step(const void *q, const void *k, const void *v, const float *w, float *state, void *y, int BH,
                         int d, int M, cudaStream_t st);
 
-// Tensor-core SLiM backward (tc_backward.cu): bf16 I/O, d = 64, M <= 128.
+// Tensor-core SLiM backward (tc_backward.cu): bf16 I/O, d = 64 with M <= 256 (a
+// two-CTA cluster per segment at M = 256), learnable W included.
 bool tc_backward_supported(int d, int M, int chunk, bool favor);
 cudaError_t tc_backward(const Plan &p, const Args &a, cudaStream_t st);
 // elu+1 at d = M = 128 (tc_backward_elu.cu): two-CTA clusters that split the
