@@ -280,6 +280,7 @@ def memory_sweep(binding, inputs, exps=(16, 18, 20)):
         y = binding.slim_attn_fwd(q, k, v, w, wl.chunk)
         dq, dk, dv, _ = binding.slim_attn_bwd(q, k, v, w, dy, wl.chunk)
         torch.cuda.synchronize()
+        binding.sync_status()
         peak = torch.cuda.max_memory_allocated() - before
         io = sum(t.numel() * t.element_size() for t in (q, k, v, dy, y, dq, dk, dv))
         ws = max(binding.workspace_bytes(wl.B, wl.H, wl.L, wl.d, wl.M, wl.chunk, b) for b in (0, 1))
@@ -324,16 +325,25 @@ def run_native(args, wl):
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        h0 = time.perf_counter()
         ev0.record(stream)
         for _ in range(args.steps):
             step()
         ev1.record(stream)
         torch.cuda.synchronize()
+        host_ms = (time.perf_counter() - h0) * 1e3
     barrier(dist)
     binding.profile_enable(False)
     kernels = binding.profile_read()
     binding.sync_status()
-    ms = max_over_ranks(ev0.elapsed_time(ev1), dist)
+    ev_ms = ev0.elapsed_time(ev1)
+    # The events and the host clock bracket the same synchronised region, so
+    # the events can only read longer if the GPU's clock moved while it ran;
+    # then the host's time stands.
+    timer = {"source": "cuda_events", "event_ms": ev_ms, "host_ms": host_ms}
+    if ev_ms > 1.02 * host_ms:
+        timer["source"] = "host (the GPU clock moved during the timed region)"
+    ms = max_over_ranks(host_ms if ev_ms > 1.02 * host_ms else ev_ms, dist)
     ms_per_step = ms / args.steps
     tokens = wl.B * wl.L
     value = world * tokens * args.steps / (ms / 1e3)
@@ -341,12 +351,19 @@ def run_native(args, wl):
     # forward alone (same inputs), for the forward tokens/s figure
     torch.cuda.synchronize()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h0 = time.perf_counter()
     f0.record(stream)
     for _ in range(args.steps):
         binding.slim_attn_fwd(q, k, v, w, wl.chunk, y=y)
     f1.record(stream)
     torch.cuda.synchronize()
-    fwd_ms = f0.elapsed_time(f1) / args.steps
+    fwd_host_ms = (time.perf_counter() - h0) * 1e3
+    fwd_ms = f0.elapsed_time(f1)
+    if fwd_ms > 1.02 * fwd_host_ms:
+        timer["forward_alone"] = "host (the GPU clock moved during the loop)"
+        fwd_ms = fwd_host_ms
+    fwd_ms /= args.steps
+    binding.sync_status()  # a device-side error in these launches fails the run
 
     # end to end through the public API with pinned host buffers
     hq, hk, hv, hdy = (t.cpu().pin_memory() for t in (q, k, v, dy))
@@ -399,6 +416,7 @@ def run_native(args, wl):
     e2e_run(e2e_steps, e0, e1)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist) / e2e_steps
+    binding.sync_status()
     nbytes = q.numel() * q.element_size()
 
     # roofline of the dominant kernel (largest share of the timed region)
@@ -445,6 +463,7 @@ def run_native(args, wl):
                 "h2d_bytes_per_step": 4 * nbytes, "d2h_bytes_per_step": 4 * nbytes,
                 "ms_per_step": e2e_ms},
         "gpu_launches": launches,
+        "timer": timer,
         "roofline": roofline,
         "step_roofline": {"roofline_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_per_step,
                           "fwd_roofline_ms": fwd_roof * 1e3, "fwd_ms": fwd_ms,

@@ -155,6 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // a second MMA-completion barrier, for a group whose epilogue overlaps the
   // group issued after it
   uint64_t *mmb_bar = in_bar + 11;
+  // used once, after a timed-out wait: completes when every MMA issued so far has
+  uint64_t *drain_bar = in_bar + 12;
   float *rx = reinterpret_cast<float *>(smem + lay.rx);
   float *s_f = reinterpret_cast<float *>(smem + lay.s_f);
   float *gs_f = reinterpret_cast<float *>(smem + lay.gs_f);
@@ -186,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(setup_bar, 1);
     mbar_init(x1_full, 1);
     mbar_init(x1_free, 1);
+    mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
     const size_t soff = ((size_t)bh * p.P + seg) * (size_t)M * DP + (size_t)fbase * DP;
@@ -208,10 +211,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (CS == 2) cluster_sync();  // the peer is running before any remote store
   tc_fence_after();
   const uint32_t tb = *tslot;
+  // false once a wait of this thread has given up (or seen another give
+  // up): thread 0 then issues nothing more.  A wait that returns true saw
+  // its phase complete, so while thread 0's waits succeed the barriers it
+  // arms are in step, whatever another thread's wait did.
+  bool go = true;
 
   // R' <- inclusive state at the segment end (hi, lo); G <- 0
   {
-    mbar_wait(setup_bar, 0, p.status, abort_flag);
+    go &= mbar_wait(setup_bar, 0, p.status, abort_flag);
     const float *sh = reinterpret_cast<const float *>(smem + lay.phq);
     const float *sl = reinterpret_cast<const float *>(smem + lo_stage);
     const int f = row;
@@ -270,13 +278,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto wait_mma = [&]() {
     __syncwarp();
-    mbar_wait(mma_bar, mma_phase, p.status, abort_flag);
+    go &= mbar_wait(mma_bar, mma_phase, p.status, abort_flag);
     mma_phase ^= 1;
     tc_fence_after();
   };
   auto wait_mmb = [&]() {
     __syncwarp();
-    mbar_wait(mmb_bar, mmb_phase, p.status, abort_flag);
+    go &= mbar_wait(mmb_bar, mmb_phase, p.status, abort_flag);
     mmb_phase ^= 1;
     tc_fence_after();
   };
@@ -285,16 +293,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
   };
+  // thread 0 issues every MMA, copy and barrier arm; once a wait of this CTA
+  // has given up it issues nothing more (the other waits return at once),
+  // so the drain after the loop covers everything in flight
+  auto issue0 = [&]() { return tid == 0 && go; };
 
   if (tid == 0 && t0 < t1) issue_in(t1 - 1);
 
   for (int t = t1 - 1; t >= t0; --t) {
     const int valid = min(kTile, p.L - t * kTile);
     const bool live = row < valid;
-    mbar_wait(in_bar, in_phase, p.status, abort_flag);
+    go &= mbar_wait(in_bar, in_phase, p.status, abort_flag);
     in_phase ^= 1;
-    if (CS == 2 && tid == 0) mbar_arrive_expect_tx(x1_full, kX1Bytes);
-    if (tid == 0 && t > t0) {
+    if (CS == 2 && issue0()) mbar_arrive_expect_tx(x1_full, kX1Bytes);
+    if (issue0() && t > t0) {
       // the next tile's inputs head for L2 now; its TMA loads issue at the
       // end of this tile, when their buffers are free again
       tma_prefetch_3d(&tmQ, 0, (t - 1) * kTile, bh);
@@ -305,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // (b) features of both sides: F_k -> T, F_q -> X, one commit
     if (FAVOR) {
-      if (tid == 0) {
+      if (issue0()) {
         const uint32_t id = make_idesc(128, MC, false, false);
         for (int s = 0; s < D / 16; ++s)
           mma_bf16(tb + kT, desc_kmajor(s_k, kTile, 0, s), desc_kmajor(s_w, MC, 0, s), id, s > 0);
@@ -356,12 +368,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // my receive slots (in usk) are idle until (i): the peer may send its
     // row partials there (signalled off the MMA-issuing thread: the
     // cluster-scope release waits for this thread's earlier stores)
-    if (CS == 2 && tid == 32) mbar_arrive_remote(peer_x1_free);
+    if (CS == 2 && tid == 32 && go) mbar_arrive_remote(peer_x1_free);
 
     // (c) A = phi_q phi_k^T -> X (its own commit: the mask below overlaps
     // the next group), and eq. (19): R' -= phi_k^T [V, 1], removing exactly
     // the increment the segment pre-pass added for this tile (increment -> T)
-    if (tid == 0) {
+    if (issue0()) {
       // last tile's dQ, dK partials (staged in the G_V-copy and R-copy tiles) have
       // been read by their reduce-adds before this phase's epilogue reuses them
       if (CS == 2) tma_store_wait_read();
@@ -370,9 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_bf16(tb + kX, desc_kmajor(s_phq, kTile, 0, s), desc_kmajor(s_phk, kTile, 0, s), id, s > 0);
       mma_commit(mmb_bar);
     }
-    mbar_wait(in2_bar, in2_phase, p.status, abort_flag);  // V (and dY, read in (f))
+    go &= mbar_wait(in2_bar, in2_phase, p.status, abort_flag);  // V (and dY, read in (f))
     in2_phase ^= 1;
-    if (tid == 0) {
+    if (issue0()) {
       issue_state_delta(tb + kT, s_phk, s_v, s_ones, D);
       mma_done();
     }
@@ -426,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // (f) num = A V + phi_q R^T -> T; Y, dN, dD.  den = rowsum(tril A) +
     // phi_q . S comes from the CUDA cores while the MMAs run
-    if (tid == 0) {
+    if (issue0()) {
       const uint32_t id = make_idesc(128, D, false, true);
       for (int s = 0; s < kTile / 16; ++s)
         mma_bf16(tb + kT, desc_kmajor(s_at, kTile, 0, s), desc_mnmajor(s_v, kTile, 0, s), id, s > 0);
@@ -474,12 +486,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (CS == 2) {
         // the peer's receive slots (in its u row-sum array) are free once it
         // is past its features
-        if (part == 0) {
-          mbar_wait(x1_free, x_phase, p.status, abort_flag);
+        if (part == 0 && go) {
+          go &= mbar_wait(x1_free, x_phase, p.status, abort_flag);
           st_async_f32(map_peer(sb + lay.rx + row * 4, peer), den, peer_x1_full);
           st_async_f32(map_peer(sb + lay.rx + (kTile + row) * 4, peer), dsum, peer_x1_full);
         }
-        mbar_wait(x1_full, x_phase, p.status, abort_flag);
+        go &= mbar_wait(x1_full, x_phase, p.status, abort_flag);
         // a + b == b + a: both CTAs hold the same totals
         den += rx[row];
         dsum += rx[kTile + row];
@@ -499,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cta_sync();
 
     // (g) dV = A^T dN + phi_k G_V^T ; raw dA = dN V^T
-    if (tid == 0) {
+    if (issue0()) {
       const uint32_t id_v1 = make_idesc(128, D, true, true);
       const uint32_t id_v2 = make_idesc(128, D, false, true);
       for (int s = 0; s < kTile / 16; ++s)
@@ -537,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_async_smem();
     cta_sync();
-    if (CS == 2 && tid == 0) {
+    if (CS == 2 && issue0()) {
       tma_reduce_add_3d(&tmDV, s_q, 0, t * kTile, bh);
       tma_store_commit();
     }
@@ -545,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (h) dphi_q -> T, dphi_k -> X (one commit: u needs only these), then
     // the G update (its own commit: it runs under u, which leaves phi_q, dN
     // and dD, the update's operands, in place)
-    if (tid == 0) {
+    if (issue0()) {
       const uint32_t id_q1 = make_idesc(128, MC, false, true);
       const uint32_t id_q2 = make_idesc(128, MC, false, false);
       for (int s = 0; s < kTile / 16; ++s)
@@ -577,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the next tile's inputs stream in as their tiles fall idle: V from
     // here, dY once the G update has read dN; Q and K at (h) with a CTA
     // pair, at the end of the tile alone
-    if (tid == 0 && t > t0) {
+    if (issue0() && t > t0) {
       if (CS == 2) {
         tma_store_wait_read();
         tma_load_3d(smem + lay.q, &tmQ, in_bar, 0, (t - 1) * kTile, bh);
@@ -588,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (CS == 2) {
       // the dA tile is idle from here: Q and K come back into it for the
       // dQ, dK epilogue (the Q tile holds the dV partial, K the next K)
-      if (tid == 0) {
+      if (issue0()) {
         mbar_arrive_expect_tx(rl_bar, 2 * tile_bytes);
         tma_load_3d(smem + lay.at, &tmQ, rl_bar, 0, t * kTile, bh);
         tma_load_3d(smem + lay.at + tile_bytes, &tmK, rl_bar, 0, t * kTile, bh);
@@ -681,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (FAVOR) tmem_st_wait();
     cta_sync();
     wait_mma();  // the G update: dN's tile takes the next dY
-    if (tid == 0 && t > t0) tma_load_3d(smem + lay.dy, &tmDY, in2_bar, 0, (t - 1) * kTile, bh);
+    if (issue0() && t > t0) tma_load_3d(smem + lay.dy, &tmDY, in2_bar, 0, (t - 1) * kTile, bh);
     if (DW) {
       // phi_q has been read by the G update: u_q over it, for the dW MMAs
       const int c0 = QF * part;
@@ -695,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (FAVOR) {
       // (j) dQ = u_q W^T - q rowsum(u_q) -> T + 64, dK likewise -> X + 64
-      if (tid == 0) {
+      if (issue0()) {
         const uint32_t id = make_idesc(128, D, false, true);
         for (int s = 0; s < MC / 16; ++s) {
           mma_bf16_ta(tb + kT + 64, tb + kT + 8 * s, desc_mnmajor(s_w, MC, 0, s), id, s > 0);
@@ -710,12 +722,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld16x2(tmem_addr(tb, 32 * q4, kT + 64 + QD * part), tmem_addr(tb, 32 * q4, kX + 64 + QD * part), a, b);
       uint32_t s_xq = s_q, s_xk = s_k;
       if (CS == 2) {
-        mbar_wait(rl_bar, rl_phase, p.status, abort_flag);
+        go &= mbar_wait(rl_bar, rl_phase, p.status, abort_flag);
         rl_phase ^= 1;
         s_xq = sb + lay.at;
         s_xk = sb + lay.at + tile_bytes;
       }
-      if (DW && tid == 0) {
+      if (DW && issue0()) {
         // dW^T = u_q^T Q + u_k^T K (features on the lanes) -> T: the dQ, dK
         // MMAs have read u's TMEM pairs there
         const uint32_t id_w = make_idesc(128, D, true, true);
@@ -747,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_async_smem();
         cta_sync();
-        if (tid == 0) {
+        if (issue0()) {
           tma_reduce_add_3d(&tmDQ, s_gv, 0, t * kTile, bh);
           tma_reduce_add_3d(&tmDK, s_rb, 0, t * kTile, bh);
           tma_store_commit();
@@ -778,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       cta_sync();
     }
     x_phase ^= 1;
-    if (CS == 1 && tid == 0 && t > t0) {
+    if (CS == 1 && issue0() && t > t0) {
       mbar_arrive_expect_tx(in_bar, 2 * tile_bytes);
       tma_load_3d(smem + lay.q, &tmQ, in_bar, 0, (t - 1) * kTile, bh);
       tma_load_3d(smem + lay.k, &tmK, in_bar, 0, (t - 1) * kTile, bh);
@@ -786,6 +798,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (CS == 2 && tid == 0) tma_store_wait_all();  // the last tile's reduce-adds
+  if (tid == 0 && *abort_flag) {
+    // a wait gave up: this CTA's MMAs and the loads armed before that land
+    // before TMEM is freed and the CTA leaves.  An input barrier whose phase
+    // is armed completes it when its bytes land (one of the two parities
+    // passes at once); one with nothing armed gives up after 20 ms.
+    mma_commit(drain_bar);
+    mbar_drain(drain_bar, 0);
+    uint64_t *const armed[4] = {in_bar, in2_bar, rl_bar, setup_bar};
+    for (int i = 0; i < 4; ++i)
+      for (uint32_t par = 0; par < 2; ++par) mbar_drain(armed[i], par, 20000000ull);
+  }
   // segment total of G -> gstates, staged in the idle phi / A tiles for one
   // coalesced bulk store of this CTA's rows
   {

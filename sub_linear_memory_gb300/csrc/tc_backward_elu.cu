@@ -99,6 +99,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t *x1_free = in_bar + 5;  // the peer may send them
   uint32_t *tslot = reinterpret_cast<uint32_t *>(in_bar + 6);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(in_bar + 7);
+  // used once, after a timed-out wait: completes when every MMA issued so far has
+  uint64_t *drain_bar = in_bar + 8;
   float *s_hi = reinterpret_cast<float *>(smem + lay.s_hi);
   float *s_lo = reinterpret_cast<float *>(smem + lay.s_lo);
   float *gs = reinterpret_cast<float *>(smem + lay.gs);
@@ -123,6 +125,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(mmb_bar, 1);
     mbar_init(x1_full, 1);
     mbar_init(x1_free, 1);
+    mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tmQ);
@@ -136,6 +139,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // the peer is running before any remote store
   tc_fence_after();
   const uint32_t tb = *tslot;
+  // false once a wait of this thread has given up (or seen another give
+  // up): thread 0 then issues nothing more.  A wait that returns true saw
+  // its phase complete, so while thread 0's waits succeed the barriers it
+  // arms are in step, whatever another thread's wait did.
+  bool go = true;
 
   auto load_qk = [&](int t) {
     mbar_arrive_expect_tx(in_bar, 2 * kTileBytes);
@@ -189,13 +197,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t peer_x1_free = map_peer(smem_u32(x1_free), peer);
   auto wait_mma = [&]() {
     __syncwarp();
-    mbar_wait(mma_bar, mma_phase, p.status, abort_flag);
+    go &= mbar_wait(mma_bar, mma_phase, p.status, abort_flag);
     mma_phase ^= 1;
     tc_fence_after();
   };
   auto wait_mmb = [&]() {
     __syncwarp();
-    mbar_wait(mmb_bar, mmb_phase, p.status, abort_flag);
+    go &= mbar_wait(mmb_bar, mmb_phase, p.status, abort_flag);
     mmb_phase ^= 1;
     tc_fence_after();
   };
@@ -204,13 +212,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
   };
+  // thread 0 issues every MMA, copy and barrier arm; once a wait of this CTA
+  // has given up it issues nothing more, so the drain after the loop covers
+  // everything in flight
+  auto issue0 = [&]() { return tid == 0 && go; };
 
   for (int t = t1 - 1; t >= t0; --t) {
     const int valid = min(kTile, p.L - t * kTile);
     const bool live = row < valid;
-    mbar_wait(in_bar, in_phase, p.status, abort_flag);
+    go &= mbar_wait(in_bar, in_phase, p.status, abort_flag);
     in_phase ^= 1;
-    if (tid == 0) {
+    if (issue0()) {
       mbar_arrive_expect_tx(x1_full, kTile * 4);
       if (t > t0) {
         tma_prefetch_3d(&tmQ, 0, (t - 1) * kTile, bh);
@@ -237,19 +249,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_async_smem();
     cta_sync();
     // my receive slot is free (read in the last tile's (f)): the peer may send
-    if (tid == 32) mbar_arrive_remote(peer_x1_free);
+    if (tid == 32 && go) mbar_arrive_remote(peer_x1_free);
 
     // (c) A = phi_q phi_k^T -> X (its own commit), and eq. (19): this CTA's
     // increment phi_k^T V[:, own] -> T
-    if (tid == 0) {
+    if (issue0()) {
       const uint32_t id = make_idesc(128, 128, false, false);
       for (int s = 0; s < kTile / 16; ++s)
         mma_bf16(tb + kX, desc_kmajor(s_q, kTile, 0, s), desc_kmajor(s_k, kTile, 0, s), id, s > 0);
       mma_commit(mmb_bar);
     }
-    mbar_wait(in2_bar, in2_phase, p.status, abort_flag);  // V (and dY, read in (f))
+    go &= mbar_wait(in2_bar, in2_phase, p.status, abort_flag);  // V (and dY, read in (f))
     in2_phase ^= 1;
-    if (tid == 0) {
+    if (issue0()) {
       const uint32_t id = make_idesc(128, DH, true, true);
       for (int s = 0; s < kTile / 16; ++s)
         mma_bf16(tb + kT, desc_mnmajor(s_k, kTile, 0, s), desc_mnmajor(s_v, kTile, cv, s), id, s > 0);
@@ -311,7 +323,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     // (f) num = A V[:, own] + phi_q R[own]^T -> T; den = rowsum(tril A) +
     // phi_q . S on the CUDA cores while the MMAs run, and the bf16 copy of G
-    if (tid == 0) {
+    if (issue0()) {
       const uint32_t id = make_idesc(128, DH, false, true);
       for (int s = 0; s < kTile / 16; ++s)
         mma_bf16(tb + kT, desc_kmajor(s_at, kTile, 0, s), desc_mnmajor(s_v, kTile, cv, s), id, s > 0);
@@ -351,11 +363,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     {
       float dsum = (dot[row] + dot[kTile + row]) + (dot[2 * kTile + row] + dot[3 * kTile + row]);
       const float den = (asum[row] + asum[kTile + row]) + (asum[2 * kTile + row] + asum[3 * kTile + row]);
-      if (part == 0) {
-        mbar_wait(x1_free, x_phase, p.status, abort_flag);
+      if (part == 0 && go) {
+        go &= mbar_wait(x1_free, x_phase, p.status, abort_flag);
         st_async_f32(map_peer(sb + lay.rx + row * 4, peer), dsum, peer_x1_full);
       }
-      mbar_wait(x1_full, x_phase, p.status, abort_flag);
+      go &= mbar_wait(x1_full, x_phase, p.status, abort_flag);
       // CTA 0 adds (own + peer), CTA 1 (peer + own): the same sum, a + b == b + a
       dsum = rank == 0 ? dsum + rx[row] : rx[row] + dsum;
       const float inv = 1.0f / den;
@@ -375,7 +387,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cta_sync();
 
     // (g) dV[:, own] = A^T dN[:, own] + phi_k G[own]^T -> X; raw dA = dN V^T -> T
-    if (tid == 0) {
+    if (issue0()) {
       const uint32_t id_v1 = make_idesc(128, DH, true, true);
       const uint32_t id_v2 = make_idesc(128, DH, false, true);
       for (int s = 0; s < kTile / 16; ++s)
@@ -413,7 +425,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     //   CTA 0: dA phi_k + dN[:, 0:64] R[0:64]^T,  dA^T phi_q + V[:, 0:64] G[0:64]^T
     //   CTA 1:            dN[:, 64:] R[64:]^T,                V[:, 64:] G[64:]^T
     // then G[own] += phi_q^T dN[:, own] (its own commit, under the epilogue)
-    if (tid == 0) {
+    if (issue0()) {
       if (rank == 0) {
         const uint32_t id1 = make_idesc(128, 128, false, true);
         for (int s = 0; s < kTile / 16; ++s)
@@ -449,7 +461,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       dot[g * kTile + f] = cs;
     }
     wait_mmb();
-    if (tid == 0 && t > t0) load_v(t - 1);  // V is read by no later MMA of this tile
+    if (issue0() && t > t0) load_v(t - 1);  // V is read by no later MMA of this tile
     // (i) dQ, dK shares = dphi * g'(x), g' = min(phi, 1); CTA 0 adds the dD S^T
     // and G_S terms.  dK goes over phi_k now, dQ over phi_q once the G
     // update has read phi_q
@@ -481,7 +493,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     cta_sync();  // every thread has read phi_q, phi_k and G_S
     wait_mma();  // the G update has read phi_q and dN
-    if (tid == 0 && t > t0) load_dy(t - 1);
+    if (issue0() && t > t0) load_dy(t - 1);
     if (rank == 0 && tid < D)
       gs[tid] += (dot[tid] + dot[kTile + tid]) + (dot[2 * kTile + tid] + dot[3 * kTile + tid]);
 #pragma unroll
@@ -490,7 +502,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                    qpk[4 * j + 3]);
     fence_async_smem();
     cta_sync();
-    if (tid == 0) {
+    if (issue0()) {
       for (int c = 0; c < D; c += 64) {
         tma_reduce_add_3d(&tmDQ, s_q + c * kTile * 2, c, t * kTile, bh);
         tma_reduce_add_3d(&tmDK, s_k + c * kTile * 2, c, t * kTile, bh);
@@ -506,6 +518,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 
   if (tid == 0) tma_store_wait_all();
+  if (tid == 0 && *abort_flag) {
+    // a wait gave up: this CTA's MMAs and the loads armed before that land
+    // before TMEM is freed and the CTA leaves (an armed phase completes when
+    // its bytes land; one with nothing armed gives up after 20 ms)
+    mma_commit(drain_bar);
+    mbar_drain(drain_bar, 0);
+    uint64_t *const armed[2] = {in_bar, in2_bar};
+    for (int i = 0; i < 2; ++i)
+      for (uint32_t par = 0; par < 2; ++par) mbar_drain(armed[i], par, 20000000ull);
+  }
   // segment total of G (this CTA's columns; CTA 0 also G_S) -> gstates
   {
     const size_t base = ((size_t)bh * p.P + seg) * (size_t)D * (D + 1);
@@ -590,6 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *mma_bar = ld_bar + 3;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(ld_bar + 4);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(ld_bar + 5);
+  uint64_t *drain_bar = ld_bar + 6;  // used once, after a timed-out wait
   const float *gs = reinterpret_cast<const float *>(smem + lay.gs);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -612,6 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(ld_bar + 1, 1);
     mbar_init(setup_bar, 1);
     mbar_init(mma_bar, 1);
+    mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
     mbar_arrive_expect_tx(setup_bar, kRecBytes);
@@ -623,7 +647,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = *tslot;
-  mbar_wait(setup_bar, 0, p.status, abort_flag);
+  // false once a wait of this thread has given up (or seen another give
+  // up): thread 0 then issues nothing more.  A wait that returns true saw
+  // its phase complete, so while thread 0's waits succeed the barriers it
+  // arms are in step, whatever another thread's wait did.
+  bool go = true;
+  go &= mbar_wait(setup_bar, 0, p.status, abort_flag);
 
   uint32_t mphase = 0;
   const uint32_t id_d = make_idesc(128, 128, false, false);
@@ -632,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = t0 + i, b = i & 1;
     const uint32_t s_k = sb + lay.kv + (uint32_t)b * 2u * kTileBytes, s_v = s_k + kTileBytes;
     const bool live = row < min(kTile, p.L - t * kTile);
-    mbar_wait(ld_bar + b, (uint32_t)(i >> 1) & 1u, p.status, abort_flag);
+    go &= mbar_wait(ld_bar + b, (uint32_t)(i >> 1) & 1u, p.status, abort_flag);
     // phi_k in place over K (padding rows: 0)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -647,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0) {
+    if (tid == 0 && go) {
       for (int s = 0; s < D / 16; ++s)
         mma_bf16(tb + kD, desc_kmajor(s_v, kTile, 0, s), desc_kmajor(s_g, D, 0, s), id_d, s > 0);
       for (int s = 0; s < D / 16; ++s)
@@ -655,12 +684,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(mma_bar);
     }
     __syncwarp();
-    mbar_wait(mma_bar, mphase, p.status, abort_flag);
+    go &= mbar_wait(mma_bar, mphase, p.status, abort_flag);
     mphase ^= 1;
     tc_fence_after();
     // every MMA up to this tile's is complete, and the last tile's reduce-adds
     // have read their sources: the other buffer takes tile t + 1
-    if (tid == 0 && t + 1 < t1) {
+    if (tid == 0 && go && t + 1 < t1) {
       if (i > 0) tma_store_wait_read();
       load(t + 1, b ^ 1);
     }
@@ -684,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();  // TMEM and the increments are complete before the next tile's MMAs
     tc_fence_after();
-    if (tid == 0) {
+    if (tid == 0 && go) {
       for (int c = 0; c < D; c += 64) {
         tma_reduce_add_3d(&tmDK, s_k + c * kTile * 2, c, t * kTile, bh);
         tma_reduce_add_3d(&tmDV, s_v + c * kTile * 2, c, t * kTile, bh);
@@ -693,6 +722,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (tid == 0) tma_store_wait_all();
+  if (tid == 0 && *abort_flag) {
+    // a wait gave up (nothing was issued after it): this CTA's MMAs and the
+    // loads armed before that land before TMEM is freed and the CTA leaves
+    // (an armed phase completes when its bytes land; one with nothing armed
+    // gives up after 20 ms)
+    mma_commit(drain_bar);
+    mbar_drain(drain_bar, 0);
+    uint64_t *const armed[3] = {ld_bar, ld_bar + 1, setup_bar};
+    for (int i = 0; i < 3; ++i)
+      for (uint32_t par = 0; par < 2; ++par) mbar_drain(armed[i], par, 20000000ull);
+  }
   __syncthreads();
   if (warp == 0) tmem_dealloc(tb, 256);
 }

@@ -59,19 +59,24 @@ enum {
   B_FEMPTY = 10,    // [2] ... read out (8 warps)
   B_DFULL = 12,     // [2] V G_V^T job in TMEM buffer b
   B_DEMPTY = 14,    // [2] ... read out (8 warps)
-  B_PHK = 16,       // phi_k block stored (8 warps)
-  B_U = 17,         // u block packed in TMEM (8 warps)
-  B_PHFREE = 18,    // [2] dV' MMAs done with phi_k buffer b
-  B_UFREE = 20,     // [2] dK' MMAs done with u buffer b
-  B_OUTFULL = 22,   // dV', dK' complete
-  B_OUTEMPTY = 23,  // dV', dK' read out (4 warps)
-  B_GFULL = 24,     // G_end image landed
-  B_GEMPTY = 25,    // G_end image no longer read (2 MMA commits + 8 warps)
-  B_WFULL = 26,     // W image landed
-  B_EPI = 27,       // [2] row sums of u written (8 warps), by unit parity
-  B_STG = 29,       // [2] a unit's dK, dV increments staged in its slots (4 + 8 warps)
-  B_DONE = 31,      // [3] MMA drain of each issuing thread
-  B_COUNT = 34
+  // phi_k and u are double-buffered, so each buffer has its own "stored"
+  // barrier: the phi_k warps may run two blocks ahead of the dV', dK'
+  // issuer (it can stall on B_OUTEMPTY), and one barrier for both buffers
+  // would then be two phases ahead of the issuer's wait, whose parity test
+  // cannot tell phase c from c + 2
+  B_PHK = 16,       // [2] phi_k block stored in buffer b (8 warps)
+  B_U = 18,         // [2] u block packed in TMEM buffer b (8 warps)
+  B_PHFREE = 20,    // [2] dV' MMAs done with phi_k buffer b
+  B_UFREE = 22,     // [2] dK' MMAs done with u buffer b
+  B_OUTFULL = 24,   // dV', dK' complete
+  B_OUTEMPTY = 25,  // dV', dK' read out (4 warps)
+  B_GFULL = 26,     // G_end image landed
+  B_GEMPTY = 27,    // G_end image no longer read (2 MMA commits + 8 warps)
+  B_WFULL = 28,     // W image landed
+  B_EPI = 29,       // [2] row sums of u written (8 warps), by unit parity
+  B_STG = 31,       // [2] a unit's dK, dV increments staged in its slots (4 + 8 warps)
+  B_DONE = 33,      // [3] MMA drain of each issuing thread
+  B_COUNT = 36
 };
 
 template <int M>
@@ -157,9 +162,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar + B_STG + b, 12);
       mbar_init(bar + B_PHFREE + b, 1);
       mbar_init(bar + B_UFREE + b, 1);
+      mbar_init(bar + B_PHK + b, 8);
+      mbar_init(bar + B_U + b, 8);
     }
-    mbar_init(bar + B_PHK, 8);
-    mbar_init(bar + B_U, 8);
     mbar_init(bar + B_OUTFULL, 1);
     mbar_init(bar + B_OUTEMPTY, 4);
     mbar_init(bar + B_GFULL, 1);
@@ -294,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (new_key(i, cur) && !wait(B_GFULL, keys++ & 1)) break;
           for (int h = 0; h < nb && ok; ++h) {
             const uint32_t c = (uint32_t)(i * nb + h), b = c & 1;
-            if (!wait(B_PHK, c & 1)) break;
+            if (!wait(B_PHK + b, (c >> 1) & 1)) break;
             if (h == 0 && i > 0 && !wait(B_OUTEMPTY, (i - 1) & 1)) break;
             tc_fence_after();
             const uint32_t s_ph = s_phk + b * kTile * 256;
@@ -304,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        (h > 0 || s > 0) ? 1u : 0u);
             mma_commit(bar + B_PHFREE + b);
             if (FAVOR) {
-              if (!wait(B_U, c & 1)) break;
+              if (!wait(B_U + b, (c >> 1) & 1)) break;
               tc_fence_after();
 #pragma unroll
               for (int s = 0; s < FB / 16; ++s)
@@ -404,11 +409,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         fence_async_smem();
-        arrive(B_PHK);
+        arrive(B_PHK + b);
         if (FAVOR) {
           tmem_st_wait();
           tc_fence_before();
-          arrive(B_U);
+          arrive(B_U + b);
         }
       }
       if (!ok) break;
@@ -418,6 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_async_smem();
       arrive(B_STG + (i & 1));
     }
+    // a wait that gave up between a block's two halves leaves u's store of
+    // the first half unwaited: TMEM is freed after this
+    if (FAVOR) tmem_st_wait();
   } else {
     // ---------------------------------------------------------------- dK, dV increments
     const float *usum = reinterpret_cast<const float *>(smem + lay.usum);
@@ -542,6 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *mma_bar = ld_bar + 3;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(ld_bar + 4);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(ld_bar + 5);
+  uint64_t *drain_bar = ld_bar + 6;  // used once, after a timed-out wait
   float *nrm = reinterpret_cast<float *>(smem + lay.nrm);
   const float *gs = reinterpret_cast<const float *>(smem + lay.gs);
 
@@ -556,6 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(ld_bar + 1, 1);
     mbar_init(setup_bar, 1);
     mbar_init(mma_bar, 1);
+    mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
     mbar_arrive_expect_tx(setup_bar, (uint32_t)M * 256u + (uint32_t)M * 4u);
@@ -579,12 +589,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = *tslot;
-  mbar_wait(setup_bar, 0, p.status, abort_flag);
+  // false once a wait of this thread has given up (or seen another give
+  // up): thread 0 then issues nothing more.  A wait that returns true saw
+  // its phase complete, so while thread 0's waits succeed the barriers it
+  // arms are in step, whatever another thread's wait did.
+  bool go = true;
+  go &= mbar_wait(setup_bar, 0, p.status, abort_flag);
 
   uint32_t mphase = 0;
   auto wait_mma = [&]() {
     __syncwarp();
-    mbar_wait(mma_bar, mphase, p.status, abort_flag);
+    go &= mbar_wait(mma_bar, mphase, p.status, abort_flag);
     mphase ^= 1;
     tc_fence_after();
   };
@@ -600,9 +615,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = t0 + i, b = i & 1;
     const uint32_t s_k = sb + lay.kv + (uint32_t)b * 2u * kTileBytes, s_v = s_k + kTileBytes;
     const bool live = row < min(kTile, p.L - t * kTile);
-    mbar_wait(ld_bar + b, (uint32_t)(i >> 1) & 1u, p.status, abort_flag);
+    go &= mbar_wait(ld_bar + b, (uint32_t)(i >> 1) & 1u, p.status, abort_flag);
     // F = K W
-    if (tid == 0) {
+    if (tid == 0 && go) {
       for (int s = 0; s < D / 16; ++s)
         mma_bf16(tb + kFD, desc_kmajor(s_k, kTile, 0, s), desc_kmajor(s_w, M, 0, s), id_f, s > 0);
       mma_commit(mma_bar);
@@ -614,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     wait_mma();
     // every MMA of the previous tile is complete (in order, one commit):
     // its K, V buffer takes tile t + 1
-    if (tid == 0 && t + 1 < t1) {
+    if (tid == 0 && go && t + 1 < t1) {
       uint64_t *nb_bar = ld_bar + (b ^ 1);
       const uint32_t nk = sb + lay.kv + (uint32_t)(b ^ 1) * 2u * kTileBytes;
       mbar_arrive_expect_tx(nb_bar, 2 * kTileBytes);
@@ -633,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     cta_sync();  // F is read out: D may overwrite it
     // D = V G_V^T
-    if (tid == 0) {
+    if (tid == 0 && go) {
       for (int s = 0; s < D / 16; ++s)
         mma_bf16(tb + kFD, desc_kmajor(s_v, kTile, 0, s), desc_kmajor(s_g, M, 0, s), id_f, s > 0);
       mma_commit(mma_bar);
@@ -659,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // dW^T += u'^T K, per 128-feature block; no commit of its own: the next
     // tile's F commit covers it (MMAs complete in order), the last one is
     // committed after the loop
-    if (tid == 0) {
+    if (tid == 0 && go) {
       for (int h = 0; h < nb; ++h)
         for (int s = 0; s < kTile / 16; ++s)
           mma_bf16(tb + kW + 64 * h, desc_mnmajor(s_ph, kTile, 128 * h, s), desc_mnmajor(s_k, kTile, 0, s), id_w,
@@ -683,6 +698,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+  }
+  if (tid == 0 && *abort_flag) {
+    // a wait gave up (nothing was issued after it): this CTA's MMAs and the
+    // loads armed before that land before TMEM is freed and the CTA leaves
+    // (an armed phase completes when its bytes land; one with nothing armed
+    // gives up after 20 ms)
+    mma_commit(drain_bar);
+    mbar_drain(drain_bar, 0);
+    uint64_t *const armed[3] = {ld_bar, ld_bar + 1, setup_bar};
+    for (int i = 0; i < 3; ++i)
+      for (uint32_t par = 0; par < 2; ++par) mbar_drain(armed[i], par, 20000000ull);
   }
   tc_fence_before();
   __syncthreads();

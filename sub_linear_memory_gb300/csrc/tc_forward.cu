@@ -222,8 +222,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_rb = sbase + lay.rb, s_ones = sbase + lay.ones;
   float *ss = reinterpret_cast<float *>(smem + lay.ss);
   float *den = reinterpret_cast<float *>(smem + lay.den);
-  auto slot_addr = [&](int n) { return sbase + lay.slots + (uint32_t)(n % kS) * LY::kTileBytes; };
-  auto slot_par = [&](int n) { return (uint32_t)((n / kS) & 1); };
+  // Load n = 3 i + r is K (r = 0), Q (1) or V (2) of tile i.  Every slot holds
+  // one kind only (K in 0, Q in 1, V in 2 and, with four slots, 3 for odd
+  // tiles), so each consumer waits on every phase of the slots it reads.  A
+  // slot that rotated through the kinds would make a consumer wait on a phase
+  // whose predecessor (another kind's load, never waited on by it) may still
+  // be in flight, and a parity wait then passes on that predecessor's
+  // predecessor: the consumer reads the slot before its load lands.
+  auto slot_idx = [&](int n) {
+    const int i = n / 3, r = n - 3 * i;
+    return r < 2 ? r : (kS == 4 ? 2 + (i & 1) : 2);
+  };
+  auto slot_use = [&](int n) {  // loads into this slot before load n
+    const int i = n / 3, r = n - 3 * i;
+    return (r == 2 && kS == 4) ? i >> 1 : i;
+  };
+  auto slot_addr = [&](int n) { return sbase + lay.slots + (uint32_t)slot_idx(n) * LY::kTileBytes; };
+  auto slot_par = [&](int n) { return (uint32_t)(slot_use(n) & 1); };
   const int q4 = warp & 3, row = 32 * q4 + lane;
   const uint32_t lane_base = 32u * q4;
 
@@ -288,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = t0; t < t1 && ok; ++t) {
         const CUtensorMap *maps[3] = {&tmK, &tmQ, &tmV};
         for (int r = 0; r < 3 && ok; ++r, ++n) {
-          const int s = n % kS, u = n / kS;
+          const int s = slot_idx(n), u = slot_use(n);
           if (u > 0 && !wait(F_EMPTY + s, (u - 1) & 1)) break;
           mbar_arrive_expect_tx(bar + F_FULL + s, LY::kTileBytes);
           for (int c = 0; c < D; c += 64)
@@ -296,7 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         t * kTile, bh);
         }
       }
-      for (int m = max(0, n - kS); m < n; ++m) mbar_drain(bar + F_FULL + m % kS, slot_par(m));
+      // the last load of every slot (the last tile's K, Q, V and, with four
+      // slots, the V before it)
+      for (int m = max(0, n - kS); m < n; ++m) mbar_drain(bar + F_FULL + slot_idx(m), slot_par(m));
       if (FAVOR || seg > 0) mbar_drain(bar + F_SETUP, 0);
     }
   } else if (warp < 4) {
@@ -321,14 +338,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < ntl * JT && ok; ++j) {
           const int i = j / JTd, n = 3 * i + side;
           if (j > 0 && !wait(b_empty, (j - 1) & 1)) break;
-          if (j % JTd == 0 && !wait(F_FULL + n % kS, slot_par(n))) break;
+          if (j % JTd == 0 && !wait(F_FULL + slot_idx(n), slot_par(n))) break;
           tc_fence_after();
-          const uint64_t dx = d_x0 + (uint64_t)(n % kS) * kSlotStep;
+          const uint64_t dx = d_x0 + (uint64_t)slot_idx(n) * kSlotStep;
           const uint64_t dw = d_w0 + (uint64_t)((j % JTd) * 512);  // 64 rows = 8 atoms of 1024 B
 #pragma unroll
           for (int s = 0; s < D / 16; ++s) mma_bf16(t_d, dx + ks(s, kTile), dw + ks(s, M), id_f, s > 0);
           commit(b_full);
-          if (j % JTd == JT - 1) commit(F_EMPTY + n % kS);
+          if (j % JTd == JT - 1) commit(F_EMPTY + slot_idx(n));
         }
       } else {
         const uint32_t id_a = make_idesc(128, 128, false, false);
@@ -345,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t d_ones = desc_n16(s_ones, 0);
         // [V, 1] of load n: the slot moves the start address up and the ones block's LBO down
         auto slot_v = [&](int n) {
-          const uint64_t q = (uint64_t)(n % kS) * kSlotStep;
+          const uint64_t q = (uint64_t)slot_idx(n) * kSlotStep;
           return D == 64 ? d_v0 + q - (q << 16) : d_v0 + q;
         };
         auto test = [&](int b, uint32_t par) { return mbar_test(bar + b, par); };
@@ -395,14 +412,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             issue_av(nav);
             commit(F_NUMFULL);
-            commit(F_EMPTY + (3 * nav + 2) % kS);
+            commit(F_EMPTY + slot_idx(3 * nav + 2));
             ++nav;
             did = true;
           }
           if (!did && nr < NB) {
             const int i = nr / nb, h = nr % nb;
             if (r_got == 0 && test(F_PHK, nr & 1)) r_got = h > 0 ? 3 : 1;
-            if (r_got == 1 && test(F_FULL + (3 * i + 2) % kS, slot_par(3 * i + 2))) r_got = 2;
+            if (r_got == 1 && test(F_FULL + slot_idx(3 * i + 2), slot_par(3 * i + 2))) r_got = 2;
             if (r_got == 2 && test(F_RBFULL, i & 1)) r_got = 3;
             if (r_got == 3) {
               tc_fence_after();
@@ -432,8 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               a_got = 0;
               if (!FAVOR && h == 0) {
                 // elu+1 features are formed by the epilogue alone: the MMA's share of the K and Q slots
-                mbar_arrive(bar + F_EMPTY + (3 * i) % kS);
-                mbar_arrive(bar + F_EMPTY + (3 * i + 1) % kS);
+                mbar_arrive(bar + F_EMPTY + slot_idx(3 * i));
+                mbar_arrive(bar + F_EMPTY + slot_idx(3 * i + 1));
               }
               if (nr > i * nb + h) {
                 commit(F_KFREE);
@@ -475,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < ntl && ok; ++i) {
       const int t = t0 + i;
       const bool dead = row >= min(kTile, p.L - t * kTile);  // padding rows past L: features forced to zero
-      const int n = 3 * i + side, s = n % kS;
+      const int n = 3 * i + side, s = slot_idx(n);
       const uint32_t s_x = slot_addr(n);
       if (!wait(F_FULL + s, slot_par(n))) break;
       float cr = 0.f;  // exp2 offset of the row
@@ -610,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         arrive(F_NUMEMPTY);
       }
-      arrive(F_EMPTY + (3 * i + 2) % kS);
+      arrive(F_EMPTY + slot_idx(3 * i + 2));
     }
   }
 
@@ -768,8 +785,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
 
   const uint32_t s_w = sbase + lay.w, s_phk = sbase + lay.phk, s_ones = sbase + lay.ones;
-  auto slot_addr = [&](int n) { return sbase + lay.slots + (uint32_t)(n % kS) * LY::kTileBytes; };
-  auto slot_par = [&](int n) { return (uint32_t)((n / kS) & 1); };
+  // Load n = 2 i + r is K (r = 0) or V (1) of tile i.  Every slot holds one
+  // kind only, so each consumer waits on every phase of its slots (see the
+  // forward): with four slots K takes 0 and 2, V 1 and 3, by tile parity;
+  // with three, K takes 0 and V takes 1 and 2 by tile parity.
+  auto slot_idx = [&](int n) {
+    const int i = n >> 1, r = n & 1;
+    return kS == 4 ? n & 3 : (r == 0 ? 0 : 1 + (i & 1));
+  };
+  auto slot_use = [&](int n) {  // loads into this slot before load n
+    const int i = n >> 1, r = n & 1;
+    return kS == 4 ? n >> 2 : (r == 0 ? i : i >> 1);
+  };
+  auto slot_addr = [&](int n) { return sbase + lay.slots + (uint32_t)slot_idx(n) * LY::kTileBytes; };
+  auto slot_par = [&](int n) { return (uint32_t)(slot_use(n) & 1); };
   bool ok = true;
   auto wait = [&](int b, uint32_t par) {
     if (ok) ok = mbar_wait(bar + b, par, p.status, abort_flag);
@@ -786,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int n = 0;
       for (int t = t0; t < t1 && ok; ++t) {
         for (int r = 0; r < 2 && ok; ++r, ++n) {
-          const int s = n % kS, u = n / kS;
+          const int s = slot_idx(n), u = slot_use(n);
           if (u > 0 && !wait(S_EMPTY + s, (u - 1) & 1)) break;
           mbar_arrive_expect_tx(bar + S_FULL + s, LY::kTileBytes);
           for (int c = 0; c < D; c += 64)
@@ -802,7 +831,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (D == 64 && p.zero_grads) tma_store_wait_all();
-      for (int m = max(0, n - kS); m < n; ++m) mbar_drain(bar + S_FULL + m % kS, slot_par(m));
+      // the last load of every slot
+      for (int m = max(0, n - kS); m < n; ++m) mbar_drain(bar + S_FULL + slot_idx(m), slot_par(m));
       if (FAVOR) mbar_drain(bar + S_SETUP, 0);
     }
   } else if (warp == 1 || warp == 2) {
@@ -815,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < ntl * JT && ok; ++j) {
           const int i = j / JTd, n = 2 * i, b = j & 1, u = j >> 1;
           if (u > 0 && !wait(S_FEMPTY + b, (u - 1) & 1)) break;
-          if (j % JTd == 0 && !wait(S_FULL + n % kS, slot_par(n))) break;
+          if (j % JTd == 0 && !wait(S_FULL + slot_idx(n), slot_par(n))) break;
           tc_fence_after();
           const uint64_t dx = desc_kmajor(slot_addr(n), kTile, 0, 0);
           const uint64_t dw = d_w0 + (uint64_t)((j % JTd) * 512);  // 64 rows = 8 atoms of 1024 B
@@ -823,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int s = 0; s < D / 16; ++s)
             mma_bf16(tbase + t_f + 64 * b, dx + (uint64_t)((s & 3) * 2), dw + (uint64_t)((s & 3) * 2), id_f, s > 0);
           mma_commit(bar + S_FFULL + b);
-          if (j % JTd == JT - 1) mma_commit(bar + S_EMPTY + n % kS);
+          if (j % JTd == JT - 1) mma_commit(bar + S_EMPTY + slot_idx(n));
         }
       } else {
         constexpr uint32_t NV = D == 64 ? D + 16 : D;  // [V, 1] in one MMA when d = 64
@@ -837,8 +867,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int c = i * nb + h, b = c & 1;
             if (!wait(S_PHK + b, (c >> 1) & 1)) break;
             if (h == 0) {
-              if (!FAVOR) mbar_arrive(bar + S_EMPTY + (2 * i) % kS);  // the MMA's share of the K slot
-              if (!wait(S_FULL + nV % kS, slot_par(nV))) break;
+              if (!FAVOR) mbar_arrive(bar + S_EMPTY + slot_idx(2 * i));  // the MMA's share of the K slot
+              if (!wait(S_FULL + slot_idx(nV), slot_par(nV))) break;
               if (i > 0 && !wait(S_INCFREE, (i - 1) & 1)) break;  // the last increment is added
             }
             tc_fence_after();
@@ -854,7 +884,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!ok) break;
           mma_commit(bar + S_AFULL);
-          mma_commit(bar + S_EMPTY + nV % kS);
+          mma_commit(bar + S_EMPTY + slot_idx(nV));
         }
       }
       mma_commit(bar + S_DONE + (warp - 1));
@@ -868,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = t0 + i, n = 2 * i;
       const bool dead = row >= min(kTile, p.L - t * kTile);  // padding rows past L: features forced to zero
       const uint32_t s_k = slot_addr(n);
-      if (!wait(S_FULL + n % kS, slot_par(n))) break;
+      if (!wait(S_FULL + slot_idx(n), slot_par(n))) break;
       float ck = 0.f;
       if (FAVOR) {
         // |k|^2 of the row: each of its two threads sums half of d
@@ -912,7 +942,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         arrive(S_PHK + b);
       }
       if (!ok) break;
-      arrive(S_EMPTY + n % kS);
+      arrive(S_EMPTY + slot_idx(n));
     }
   } else if (warp >= 12) {
     // ---------------------------------------------------------------- master += increment
@@ -949,7 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       arrive(S_INCFREE);
       __syncwarp();
-      if (lane == 0) mbar_arrive_n(bar + S_EMPTY + (2 * i + 1) % kS, 2);  // V(t): 4 warps x 2
+      if (lane == 0) mbar_arrive_n(bar + S_EMPTY + slot_idx(2 * i + 1), 2);  // V(t): 4 warps x 2
     }
   }
 

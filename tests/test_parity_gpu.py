@@ -324,6 +324,32 @@ def test_outputs_do_not_depend_on_stale_workspace(_lib):
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("M", [64, 256])
+def test_long_segments_repeat_cleanly(M, _lib):
+    """Many tiles per CTA and every SM busy: the 1M-row workload's head shape
+    at 2^18 rows (and the same with 256 features), thirty fwd + bwd runs in a
+    row.  Each must end with a clean device status (a barrier wait that gives
+    up raises here) and, with 64 features, give bit-identical outputs: with
+    one CTA per segment every output element is stored once and corrected at
+    most once.  A forward whose load slots rotated through K, Q and V tiles
+    let a consumer read a slot before its load landed about once in three
+    such runs, one 128-row tile of Y wrong: far too little for the
+    whole-head relative L2 bar to see."""
+    wl = inputs.WORKLOADS["l1m"].with_(L=1 << 18, M=M, index=300 + M)
+    q, k, v, dy, w = inputs.make_inputs(wl, device="cuda")
+    first = run_library(q, k, v, w, dy, wl.chunk, want_dw=False)
+    deterministic = M <= 128  # 256 features: a CTA pair adds its two partials in either order
+    for _ in range(29):
+        again = run_library(q, k, v, w, dy, wl.chunk, want_dw=False)
+        if deterministic:
+            for a, b in zip(first[:4], again[:4]):
+                assert torch.equal(a, b)
+    if not deterministic:
+        for a, b in zip(first[:4], again[:4]):
+            d = (a.float() - b.float()).norm() / b.float().norm()
+            assert d <= 1e-2, float(d)
+
+
 # ---- full-size workloads: sampled heads ----------------------------------
 
 FULL = {
