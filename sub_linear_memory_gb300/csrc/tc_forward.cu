@@ -1087,11 +1087,15 @@ cudaError_t prep_w(const Plan &pl, const Args &a, cudaStream_t st) {
 }
 
 // Totals of R' over the first nseg segments, then their inclusive scan:
-// states[s] = R' at the end of segment s.
+// states[s] = R' at the end of segment s.  `exact`: the scan keeps the high
+// and low parts (double-float), as the backward's reversal needs; the
+// forward reads only the high parts of its incoming state, for which a
+// plain fp32 scan of the high parts (a relative error of about 2^-24 per
+// segment added) is enough and moves half the bytes.
 template <int D, bool FAVOR>
 cudaError_t segment_states(const Plan &pl, const Args &a, const CUtensorMap &mq,
                            const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap *mz, int nseg,
-                           cudaStream_t st) {
+                           bool exact, cudaStream_t st) {
   cudaError_t e;
   {
     ProfScope ps("tc_segment_state", st);
@@ -1100,7 +1104,8 @@ cudaError_t segment_states(const Plan &pl, const Args &a, const CUtensorMap &mq,
   }
   if (nseg > 1) {
     ProfScope ps("scan_states", st);
-    e = scan_states_df(pl, a.ws + pl.states_off, a.ws + pl.states_lo_off, nseg, 1, st);
+    e = exact ? scan_states_df(pl, a.ws + pl.states_off, a.ws + pl.states_lo_off, nseg, 1, st)
+              : scan_states_f32(pl, a.ws + pl.states_off, nseg, st);
   }
   return e;
 }
@@ -1113,7 +1118,7 @@ cudaError_t forward_family(const Plan &pl, const Args &a, cudaStream_t st) {
     return cudaErrorInvalidValue;
   cudaError_t e;
   if (pl.P > 1) {
-    e = segment_states<D, FAVOR>(pl, a, mq, mk, mv, nullptr, pl.P - 1, st);
+    e = segment_states<D, FAVOR>(pl, a, mq, mk, mv, nullptr, pl.P - 1, false, st);
     if (e != cudaSuccess) return e;
   }
   ProfScope ps("tc_forward", st);
@@ -1152,9 +1157,9 @@ cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, bool zero_
        !make_map_bf16_3d(&mz[2], a.dv, p.BH, p.L, d, tcf::kTile)))
     return cudaErrorInvalidValue;
   const CUtensorMap *z = zero_grads ? mz : nullptr;
-  if (d == 64 && p.favor) return tcf::segment_states<64, true>(p, a, mk, mk, mv, z, nseg, st);
-  if (d == 64) return tcf::segment_states<64, false>(p, a, mk, mk, mv, z, nseg, st);
-  if (d == 128 && !p.favor) return tcf::segment_states<128, false>(p, a, mk, mk, mv, z, nseg, st);
+  if (d == 64 && p.favor) return tcf::segment_states<64, true>(p, a, mk, mk, mv, z, nseg, true, st);
+  if (d == 64) return tcf::segment_states<64, false>(p, a, mk, mk, mv, z, nseg, true, st);
+  if (d == 128 && !p.favor) return tcf::segment_states<128, false>(p, a, mk, mk, mv, z, nseg, true, st);
   return cudaErrorInvalidValue;
 }
 

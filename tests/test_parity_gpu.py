@@ -101,6 +101,29 @@ SMALL = [
 ]
 
 
+def check_tiles(name, got, ref, tol):
+    """Error of every 128-row tile of every head on its own, over the RMS tile
+    norm of the reference: a whole tensor's norm cannot see one wrong tile
+    among thousands.  (Over the tile's own norm it would flag rows whose
+    exact dK is a small difference of large bf16-rounded terms; at l32k
+    head 0, tile 66, that reads 0.27 for correct code.)"""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    B, H, L, d = ref.shape
+    nt, full = (L + 127) // 128, L // 128
+    parts = [(got[:, :, :full * 128].reshape(B, H, full, 128 * d), ref[:, :, :full * 128].reshape(B, H, full, 128 * d))]
+    if full < nt:
+        parts.append((got[:, :, full * 128:].reshape(B, H, 1, -1), ref[:, :, full * 128:].reshape(B, H, 1, -1)))
+    num = np.concatenate([np.linalg.norm(g - r, axis=3) for g, r in parts], axis=2)
+    den = np.concatenate([np.linalg.norm(r, axis=3) for _, r in parts], axis=2)
+    err = num / np.sqrt(np.mean(den ** 2))
+    worst = float(err.max())
+    at = np.unravel_index(int(err.argmax()), err.shape)
+    print("%s worst tile error / RMS tile norm %.3e at (b, h, tile) %s (tol %.2f)"
+          % (name, worst, tuple(int(x) for x in at), tol))
+    assert np.isfinite(worst) and worst <= tol, "%s: tile %s error %.3e of the RMS tile norm > %.2f" % (name, at, worst, tol)
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
 @pytest.mark.parametrize("case", SMALL, ids=lambda c: "x".join(map(str, c)))
 def test_small_against_oracle(case, dtype):
@@ -376,12 +399,17 @@ def test_full_size_workload(name):
         idx_h = torch.tensor([h for _, h in heads])
         sel = lambda t: _np(t[idx_b, idx_h].unsqueeze(0))
     qn, kn, vn, dyn, wn = sel(q), sel(k), sel(v), sel(dy), _wnp(w)
+    # every tile on its own too: a tile read before its load landed is off
+    # by about its own norm; correct bf16 tiles stay below 0.14 of the RMS
+    # tile norm on these workloads
+    tile_tol = 0.25 if wl.torch_dtype == torch.bfloat16 else 1e-3
     y_ref = oracle.recurrence_forward(qn, kn, vn, wn)
     check("Y", sel(y), y_ref, tol)
+    check_tiles("Y", sel(y), y_ref, tile_tol)
     del y_ref
     dq_ref, dk_ref, dv_ref, dw_ref = oracle.recurrence_backward(qn, kn, vn, wn, dyn, want_dw=want_dw)
-    check("dQ", sel(dq), dq_ref, tol)
-    check("dK", sel(dk), dk_ref, tol)
-    check("dV", sel(dv), dv_ref, tol)
+    for name, got, ref in (("dQ", dq, dq_ref), ("dK", dk, dk_ref), ("dV", dv, dv_ref)):
+        check(name, sel(got), ref, tol)
+        check_tiles(name, sel(got), ref, tile_tol)
     if want_dw:
         check("dW", _np(dw), dw_ref, tol)
