@@ -29,6 +29,30 @@ __device__ __forceinline__ float warp_sum32(float x) {
   return x;
 }
 
+// One step of a transposed warp reduction: the lane keeps the half of its
+// n values that bit `o` of its lane index selects and adds the partner's
+// copy of that half (the partner sends the half it does not keep).
+template <int n, int o>
+__device__ __forceinline__ void halve(float *v, int lane) {
+  const bool up = (lane & o) != 0;
+#pragma unroll
+  for (int i = 0; i < n / 2; ++i) {
+    const float keep = up ? v[i + n / 2] : v[i], send = up ? v[i] : v[i + n / 2];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+  }
+}
+
+// Sums of v[0..15] over the warp's 32 lanes by recursive halving: lanes 2r
+// and 2r + 1 end with the sum of v[r].  16 shuffles for the 16 sums, where
+// 16 separate butterflies take 80.
+__device__ __forceinline__ float warp_sum16_transposed(float *v, int lane) {
+  halve<16, 16>(v, lane);
+  halve<8, 8>(v, lane);
+  halve<4, 4>(v, lane);
+  halve<2, 2>(v, lane);
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
 // One CTA per head; thread m < M owns feature m.
 template <typename T>
 __global__ void __launch_bounds__(256) decode_kernel(const T *__restrict__ q, const T *__restrict__ k,
@@ -65,6 +89,7 @@ __global__ void __launch_bounds__(256) decode_kernel(const T *__restrict__ q, co
     if (favor) {
       // g(x)_m = exp(x . w_m - |x|^2 / 2) / sqrt(M), w_m = column m of W [d][M]
       float fq = 0.f, fk = 0.f;
+#pragma unroll 8
       for (int i = 0; i < d; ++i) {
         const float wi = w[(size_t)i * M + t];
         fq = fmaf(xs[0][i], wi, fq);
@@ -83,7 +108,7 @@ __global__ void __launch_bounds__(256) decode_kernel(const T *__restrict__ q, co
   // before its stores (a store ahead of the next row's load would make each
   // row wait a memory round trip), then the row's term is added and the
   // per-warp partials of g(q) . state[e] formed
-  constexpr int kRows = 16;
+  constexpr int kRows = 16;  // warp_sum16_transposed reduces 16 rows
   float *st = state + (size_t)bh * (d + 1) * M;
   float nxt[kRows];  // the next block, loaded before this block's stores
 #pragma unroll
@@ -103,12 +128,9 @@ __global__ void __launch_bounds__(256) decode_kernel(const T *__restrict__ q, co
       if (act && e <= d) st[(size_t)e * M + t] = cur[j];
     }
 #pragma unroll
-    for (int j = 0; j < kRows; ++j) cur[j] = warp_sum32(phq * cur[j]);
-    if (lane == 0) {
-#pragma unroll
-      for (int j = 0; j < kRows; ++j)
-        if (e0 + j <= d) part[warp][e0 + j] = cur[j];
-    }
+    for (int j = 0; j < kRows; ++j) cur[j] *= phq;
+    const float sum = warp_sum16_transposed(cur, lane);  // row e0 + lane / 2
+    if ((lane & 1) == 0 && e0 + (lane >> 1) <= d) part[warp][e0 + (lane >> 1)] = sum;
   }
   __syncthreads();
   for (int e = t; e < d; e += blockDim.x) {
