@@ -104,33 +104,41 @@ __global__ void __launch_bounds__(256) decode_kernel(const T *__restrict__ q, co
       phk = xk > 0.f ? xk + 1.f : expf(xk);
     }
   }
-  // state rows e = 0 .. d, kRows at a time: every load of a block is issued
-  // before its stores (a store ahead of the next row's load would make each
-  // row wait a memory round trip), then the row's term is added and the
-  // per-warp partials of g(q) . state[e] formed
+  // value rows e = 0 .. d - 1, kRows at a time (d is a multiple of 16):
+  // every load of a block is issued before its stores (a store ahead of the
+  // next row's load would make each row wait a memory round trip), then the
+  // row's term is added and the per-warp partials of g(q) . state[e] formed;
+  // the S row (e = d) is loaded with the last block and handled after it
   constexpr int kRows = 16;  // warp_sum16_transposed reduces 16 rows
   float *st = state + (size_t)bh * (d + 1) * M;
   float nxt[kRows];  // the next block, loaded before this block's stores
 #pragma unroll
-  for (int j = 0; j < kRows; ++j) nxt[j] = (act && j <= d) ? st[(size_t)j * M + t] : 0.f;
-  for (int e0 = 0; e0 <= d; e0 += kRows) {
+  for (int j = 0; j < kRows; ++j) nxt[j] = act ? st[(size_t)j * M + t] : 0.f;
+  float srow = 0.f;
+  for (int e0 = 0; e0 < d; e0 += kRows) {
     float cur[kRows];
+    const bool more = e0 + kRows < d;
 #pragma unroll
     for (int j = 0; j < kRows; ++j) {
       cur[j] = nxt[j];
-      const int e = e0 + kRows + j;
-      nxt[j] = (act && e <= d) ? st[(size_t)e * M + t] : 0.f;
+      nxt[j] = (act && more) ? st[(size_t)(e0 + kRows + j) * M + t] : 0.f;
     }
+    if (!more) srow = act ? st[(size_t)d * M + t] : 0.f;
 #pragma unroll
     for (int j = 0; j < kRows; ++j) {
-      const int e = e0 + j;
-      cur[j] = fmaf(e < d ? xs[2][e < d ? e : 0] : 1.f, phk, cur[j]);
-      if (act && e <= d) st[(size_t)e * M + t] = cur[j];
+      cur[j] = fmaf(xs[2][e0 + j], phk, cur[j]);
+      if (act) st[(size_t)(e0 + j) * M + t] = cur[j];
     }
 #pragma unroll
     for (int j = 0; j < kRows; ++j) cur[j] *= phq;
     const float sum = warp_sum16_transposed(cur, lane);  // row e0 + lane / 2
-    if ((lane & 1) == 0 && e0 + (lane >> 1) <= d) part[warp][e0 + (lane >> 1)] = sum;
+    if ((lane & 1) == 0) part[warp][e0 + (lane >> 1)] = sum;
+  }
+  srow += phk;  // S gains g(k)
+  if (act) st[(size_t)d * M + t] = srow;
+  {
+    const float sum = warp_sum32(phq * srow);
+    if (lane == 0) part[warp][d] = sum;
   }
   __syncthreads();
   for (int e = t; e < d; e += blockDim.x) {
