@@ -566,17 +566,14 @@ constexpr uint32_t kRecBytes = kTileBytes + D * 4;
 
 // G_end(s) = the scanned G total at index s + 1 -> image + G_S record of (bh, s)
 __global__ void prep_g128_kernel(const float *__restrict__ gstates, unsigned char *__restrict__ grec, int P, int BH) {
+  // x: the (feature, column) pairs of one record; y: its (head, segment)
   const int DP = D + 1;
-  const long long n = (long long)BH * (P - 1) * D * DP;
-  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const int e = (int)(idx % DP);
-    const long long r = idx / DP;
-    const int f = (int)(r % D);
-    const long long hs = r / D;
-    const int s = (int)(hs % (P - 1));
-    const int bh = (int)(hs / (P - 1));
-    const float g = gstates[(((size_t)bh * P + s + 1) * D + f) * DP + e];
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= D * DP) return;
+  const int f = r / DP, e = r - f * DP;
+  for (int hs = blockIdx.y; hs < BH * (P - 1); hs += gridDim.y) {
+    const int bh = hs / (P - 1), s = hs - bh * (P - 1);
+    const float g = gstates[((size_t)bh * P + s + 1) * (size_t)D * DP + r];
     unsigned char *rec = grec + ((size_t)bh * P + s) * (size_t)kRecBytes;
     if (e < D)
       *reinterpret_cast<__nv_bfloat16 *>(rec + sw128_offset(f, e, D)) = __float2bfloat16_rn(g);
@@ -784,9 +781,8 @@ cudaError_t tc_backward_elu128(const Plan &pl, const Args &a, cudaStream_t st) {
   }
   {
     ProfScope ps("prep_g", st);
-    const long long n = (long long)pl.BH * (pl.P - 1) * D * (D + 1);
-    const int blocks = (int)std::min<long long>((n + 255) / 256, 4096);
-    prep_g128_kernel<<<blocks, 256, 0, st>>>(a.ws + pl.gstates_off, reinterpret_cast<unsigned char *>(a.ws + pl.gimg_off),
+    const dim3 grid((D * (D + 1) + 255) / 256, (unsigned)std::min(pl.BH * (pl.P - 1), 65535));
+    prep_g128_kernel<<<grid, 256, 0, st>>>(a.ws + pl.gstates_off, reinterpret_cast<unsigned char *>(a.ws + pl.gimg_off),
                                              pl.P, pl.BH);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -476,17 +476,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // record: bf16 [M][64] swizzled image of columns 0..63, then fp32 column 64.
 __global__ void prep_g_kernel(const float *__restrict__ gstates, unsigned char *__restrict__ grec, int M, int P,
                               int BH) {
+  // x: the (feature, column) pairs of one record; y: its (head, segment),
+  // so every division is by a constant or once per thread
   const int DP = D + 1;
-  const long long n = (long long)BH * (P - 1) * M * DP;
-  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const int e = (int)(idx % DP);
-    const long long r = idx / DP;
-    const int f = (int)(r % M);
-    const long long hs = r / M;  // bh * (P - 1) + s
-    const int s = (int)(hs % (P - 1));
-    const int bh = (int)(hs / (P - 1));
-    const float g = gstates[(((size_t)bh * P + s + 1) * M + f) * DP + e];
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= M * DP) return;
+  const int f = r / DP, e = r - f * DP;
+  for (int hs = blockIdx.y; hs < BH * (P - 1); hs += gridDim.y) {
+    const int bh = hs / (P - 1), s = hs - bh * (P - 1);
+    const float g = gstates[((size_t)bh * P + s + 1) * (size_t)M * DP + r];
     unsigned char *rec = grec + ((size_t)bh * P + s) * (size_t)M * 132u;
     if (e < D)
       *reinterpret_cast<__nv_bfloat16 *>(rec + sw128_offset(f, e, M)) = __float2bfloat16_rn(g);
@@ -769,9 +767,9 @@ cudaError_t tc_correction(const Plan &pl, const Args &a, cudaStream_t st) {
     return cudaErrorInvalidValue;
   {
     ProfScope ps("prep_g", st);
-    const long long n = (long long)pl.BH * (pl.P - 1) * pl.M * (tcc::D + 1);
-    const int blocks = (int)std::min<long long>((n + 255) / 256, 4096);
-    tcc::prep_g_kernel<<<blocks, 256, 0, st>>>(a.ws + pl.gstates_off,
+    const int rec = pl.M * (tcc::D + 1);
+    const dim3 grid((rec + 255) / 256, (unsigned)std::min(pl.BH * (pl.P - 1), 65535));
+    tcc::prep_g_kernel<<<grid, 256, 0, st>>>(a.ws + pl.gstates_off,
                                                reinterpret_cast<unsigned char *>(a.ws + pl.gimg_off), pl.M, pl.P,
                                                pl.BH);
     cudaError_t e = cudaGetLastError();
