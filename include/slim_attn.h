@@ -46,8 +46,11 @@
  * Errors: no exception or abort crosses this ABI.  Argument problems are
  * detected on the host and returned before anything is enqueued.  Launch
  * failures return SLIM_ERR_CUDA.  Kernels that wait on on-chip barriers give
- * up after a bounded number of polls and record SLIM_ERR_TIMEOUT in a device
- * status word, which slim_attn_sync_status() reads back (and clears).
+ * up after about a second of polling and record SLIM_ERR_TIMEOUT in a device
+ * status word, which slim_attn_sync_status() reads back (and clears); such a
+ * kernel issues no further copies or tensor-core work, lets what it already
+ * issued land, frees its tensor memory and returns, so the context stays
+ * usable (the outputs of that call are then undefined).
  */
 #ifndef SLIM_ATTN_H
 #define SLIM_ATTN_H
