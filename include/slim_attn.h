@@ -119,17 +119,27 @@ slim_status slim_attn_bwd_f32(const float *q, const float *k, const float *v,
  * and result as slim_attn_fwd, but no workspace is registered or used: the
  * scratch is a 64 MiB array compiled into the library, resident on every GPU
  * that loads the library until the process exits.  The paper has no
- * counterpart; this is a deployment convenience.
- *   - Problems whose slim_attn_workspace_bytes(..., 0) exceeds
- *     SLIM_NOALLOC_SCRATCH_BYTES return SLIM_ERR_WORKSPACE before any launch.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make it before any
- *     stream capture.  It calls no allocator itself.
+ * counterpart; this is a deployment convenience.  It always runs the
+ * CUDA-core forward kernels.
+ *   - Problems whose CUDA-core forward workspace (slice-boundary states and
+ *     per-CTA scratch of that kernel family) exceeds
+ *     SLIM_NOALLOC_SCRATCH_BYTES return SLIM_ERR_WORKSPACE before any launch;
+ *     slim_attn_noalloc_bytes() gives that size.
+ *   - Every call looks up the array's device address (cudaGetSymbolAddress)
+ *     with the caller's device current; the first call on a device loads the
+ *     library's device code there if nothing else has, so make it before any
+ *     stream capture.  After a device reset the next call finds the array anew.  It calls
+ *     no allocator itself.
  *   - Every call shares the one array: calls that overlap on the GPU race.
  *     No value is carried from one call to the next. */
 slim_status slim_attn_fwd_noalloc(const void *q, const void *k, const void *v, const float *w,
                                   void *y, int B, int H, int L, int d, int M, int chunk,
                                   slim_stream_t stream);
+
+/* Bytes of the fixed array slim_attn_fwd_noalloc would use for this shape
+ * (0 for an unsupported shape or an empty problem); the call is refused when
+ * this exceeds SLIM_NOALLOC_SCRATCH_BYTES. */
+size_t slim_attn_noalloc_bytes(int B, int H, int L, int d, int M, int chunk);
 
 /* Serving form (section 2.1: eq. (3)-(4) run one row at a time; row l needs
  * only the state of the rows before it).  A head's state is the stacked
@@ -192,6 +202,18 @@ void slim_attn_profile_reset(void);
 
 /* Wait for `stream`, then read and clear the device status word. */
 slim_status slim_attn_sync_status(slim_stream_t stream);
+
+/* Self-test of the failure path (not part of the method): launches one warp
+ * that waits, with the same bounded wait the tensor-core kernels use, on an
+ * on-chip barrier that nothing ever completes.  The wait gives up after
+ * limit_ns nanoseconds (1e3 <= limit_ns <= 1e8, else SLIM_ERR_INVALID_ARG)
+ * and records SLIM_ERR_TIMEOUT in the device status word, so the next
+ * slim_attn_sync_status(stream) returns SLIM_ERR_TIMEOUT (and clears it).
+ * waited_ns: NULL, or a device pointer to one unsigned 64-bit word that
+ * receives how long the wait ran (1 if it wrongly saw the barrier complete).
+ * Nothing else is in flight in that kernel: no copy, no tensor-core work and
+ * no tensor memory, so giving up leaves nothing behind. */
+slim_status slim_attn_selftest_timeout(long long limit_ns, unsigned long long *waited_ns, slim_stream_t stream);
 
 /* Human-readable name of a status code (static storage). */
 const char *slim_status_string(slim_status status);

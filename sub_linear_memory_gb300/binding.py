@@ -51,6 +51,12 @@ _lib.slim_attn_profile_get.argtypes = [_i, ctypes.POINTER(ctypes.c_char_p),
 _lib.slim_attn_profile_get.restype = _i
 _lib.slim_attn_profile_reset.argtypes = []
 _lib.slim_attn_profile_reset.restype = None
+_lib.slim_attn_noalloc_bytes.argtypes = [_i] * 6
+_lib.slim_attn_noalloc_bytes.restype = _sz
+_lib.slim_attn_fwd_noalloc.argtypes = _lib.slim_attn_fwd.argtypes
+_lib.slim_attn_fwd_noalloc.restype = _i
+_lib.slim_attn_selftest_timeout.argtypes = [ctypes.c_longlong, _vp, _vp]
+_lib.slim_attn_selftest_timeout.restype = _i
 _lib.slim_status_string.argtypes = [_i]
 _lib.slim_status_string.restype = ctypes.c_char_p
 
@@ -63,6 +69,7 @@ EXPORTED = (
     "slim_attn_workspace_bytes", "slim_attn_set_workspace", "slim_attn_set_option",
     "slim_attn_segments", "slim_attn_sync_status", "slim_status_string",
     "slim_attn_profile_count", "slim_attn_profile_get", "slim_attn_profile_reset",
+    "slim_attn_fwd_noalloc", "slim_attn_noalloc_bytes", "slim_attn_selftest_timeout",
 )
 
 
@@ -109,6 +116,19 @@ def segments(B, H, L, d, M, chunk):
 
 def workspace_bytes(B, H, L, d, M, chunk, is_bwd):
     return _lib.slim_attn_workspace_bytes(B, H, L, d, M, chunk, int(is_bwd))
+
+
+def noalloc_bytes(B, H, L, d, M, chunk):
+    return _lib.slim_attn_noalloc_bytes(B, H, L, d, M, chunk)
+
+
+def selftest_timeout(limit_ns, waited=None, stream=None):
+    """Launch the bounded-wait self-test (a wait on a barrier nothing arms);
+    ``waited`` is an optional int64 CUDA tensor of one element that receives
+    the nanoseconds the wait ran."""
+    s = torch.cuda.current_stream() if stream is None else stream
+    _check(_lib.slim_attn_selftest_timeout(int(limit_ns), _ptr(waited), _vp(s.cuda_stream)),
+           "slim_attn_selftest_timeout")
 
 
 def sync_status(stream=None):

@@ -12,16 +12,17 @@
 // The array below is allocated when the library's device code is loaded on a
 // GPU and stays resident on every GPU that loads the library until the
 // process exits.  Host code may not pass its name to a kernel (on the host it
-// is only a stand-in symbol, not a device address), so the first call on each
-// device looks up the real device address with cudaGetSymbolAddress while
-// that device is current and caches it.  Make that first call before any
-// stream capture begins.  All calls share the one array: calls that overlap on
-// the GPU (several streams, or several host threads) race on it.  Every value
-// the forward kernels read from it is written earlier in the same call, so
-// nothing needs clearing between calls.
+// is only a stand-in symbol, not a device address), so every call looks up
+// the real device address with cudaGetSymbolAddress while the caller's device
+// is current.  The lookup is not cached: a device reset, or another driver
+// context made current on the same device, reloads the module and may move
+// the array, and a cached address would then point at freed memory.  The
+// first call on a device loads the module if nothing else has; make it before
+// any stream capture begins.  All calls share the one array: calls that
+// overlap on the GPU (several streams, or several host threads) race on it.
+// Every value the forward kernels read from it is written earlier in the same
+// call, so nothing needs clearing between calls.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -31,22 +32,11 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SLIM_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[kMaxDevices] = {};
-
-// Device address of g_noalloc_scratch on the current device (looked up once).
+// Device address of g_noalloc_scratch in the current device's context.
 slim_status noalloc_scratch(void **out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SLIM_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return SLIM_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void *ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return SLIM_ERR_CUDA;
-    g_noalloc_ptr[dev] = ptr;
-  }
-  *out = g_noalloc_ptr[dev];
+  void *ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return SLIM_ERR_CUDA;
+  *out = ptr;
   return SLIM_OK;
 }
 
@@ -74,4 +64,12 @@ extern "C" slim_status slim_attn_fwd_noalloc(const void *q, const void *k, const
   if (!a.status) return SLIM_ERR_CUDA;
   return generic_forward<__nv_bfloat16>(p, a, (cudaStream_t)stream) == cudaSuccess ? SLIM_OK
                                                                                    : SLIM_ERR_CUDA;
+}
+
+extern "C" size_t slim_attn_noalloc_bytes(int B, int H, int L, int d, int M, int chunk) {
+  using namespace slim;
+  // the plan does not depend on the feature map: check the shape as FAVOR+
+  if (shape_status(B, H, L, d, M, chunk, true) != SLIM_OK) return 0;
+  if ((long long)B * H * L == 0) return 0;
+  return plan_for(B, H, L, d, M, chunk, true, false, false).total_floats * sizeof(float);
 }

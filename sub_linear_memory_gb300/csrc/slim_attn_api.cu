@@ -336,8 +336,9 @@ slim_status slim_attn_decode_f32(const float *q, const float *k, const float *v,
 }
 
 size_t slim_attn_workspace_bytes(int B, int H, int L, int d, int M, int chunk, int is_bwd) {
-  // elu+1 has M == d; the plan does not depend on the feature map otherwise
-  if (slim::check_shape(B, H, L, d, M, chunk, M != d || true) != SLIM_OK) return 0;
+  // the plan does not depend on the feature map: check the shape as FAVOR+
+  // (which accepts every M that elu+1 does)
+  if (slim::check_shape(B, H, L, d, M, chunk, true) != SLIM_OK) return 0;
   if ((long long)B * H * L == 0) return 0;
   size_t floats = 0;
   for (int path = 1; path <= 2; ++path) {

@@ -918,7 +918,7 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
 
 bool tc_backward_supported(int d, int M, int chunk, bool favor) {
   if (tc_backward_elu128_supported(d, M, chunk, favor)) return true;
-  if (chunk < 64 || d != 64) return false;
+  if (d != 64) return false;  // 128-row tiles for every slice size
   return favor ? (M == 64 || M == 128 || M == 256) : M == 64;
 }
 

@@ -737,7 +737,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace tce
 
 bool tc_backward_elu128_supported(int d, int M, int chunk, bool favor) {
-  return !favor && d == tce::D && M == tce::D && chunk >= 64;
+  (void)chunk;  // 128-row tiles for every slice size
+  return !favor && d == tce::D && M == tce::D;
 }
 
 cudaError_t tc_backward_elu128(const Plan &pl, const Args &a, cudaStream_t st) {

@@ -107,3 +107,20 @@ def test_state_and_decode_reject_bad_arguments_before_any_launch(lib):
     assert lib.slim_attn_state(dummy, dummy, dummy, dummy, 1, 1, 64, 64, 64, 48, None) == 2
     assert lib.slim_attn_state(dummy, dummy, dummy, None, 1, 1, 64, 64, 64, 32, None) == 1
     assert lib.slim_attn_state_f32(dummy, dummy, None, dummy, 1, 1, 64, 64, 128, 32, None) == 1
+
+
+def test_selftest_rejects_bad_limits_on_the_host(lib):
+    # limits outside [1 us, 100 ms] return SLIM_ERR_INVALID_ARG before any launch
+    for bad in (0, 999, 100_000_001, -5):
+        assert lib.slim_attn_selftest_timeout(bad, None, None) == 1
+
+
+def test_noalloc_size_query(lib):
+    """slim_attn_noalloc_bytes is the CUDA-core forward plan's size: never more
+    than the registered-workspace size for the same shape, 0 when empty."""
+    assert lib.slim_attn_noalloc_bytes(0, 4, 128, 64, 64, 64) == 0
+    assert lib.slim_attn_noalloc_bytes(1, 1, 64, 48, 64, 32) == 0  # d unsupported
+    for shape in ((2, 4, 2048, 64, 128, 64), (1, 3, 777, 32, 64, 32), (2, 16, 32768, 64, 256, 128)):
+        n = lib.slim_attn_noalloc_bytes(*shape)
+        assert 0 < n <= lib.slim_attn_workspace_bytes(*shape, 0)
+    assert lib.slim_attn_noalloc_bytes(2, 16, 32768, 64, 256, 128) > (64 << 20)
