@@ -14,7 +14,12 @@ SLiM", section 2.1:
   * ``quadratic.softmax_forward``: eq. (1), the exponential attention that the
     randomized feature map approximates;
   * ``prefill_state`` / ``decode_step``: the same recurrence in its serving
-    form, one new row at a time against a carried state (C).
+    form, one new row at a time against a carried state (C);
+  * the forward and backward also take the boundary state of rows that came
+    before (``state0``) and the gradient arriving from rows that come after
+    (``g0``), and return the state after the last row and the gradient with
+    respect to ``state0``: a sequence cut into windows is then the same
+    computation, window by window.
 """
 import ctypes
 import os
@@ -54,11 +59,13 @@ def _load():
             dp = ctypes.POINTER(ctypes.c_double)
             lib.oracle_forward.argtypes = [dp] * 5 + [ctypes.c_long] * 3 + [ctypes.c_int] * 4
             lib.oracle_backward.argtypes = [dp] * 10 + [ctypes.c_long] * 3 + [ctypes.c_int] * 4
+            lib.oracle_forward_carry.argtypes = [dp] * 7 + [ctypes.c_long] * 3 + [ctypes.c_int] * 4
+            lib.oracle_backward_carry.argtypes = [dp] * 13 + [ctypes.c_long] * 3 + [ctypes.c_int] * 4
             lib.oracle_feature_map.argtypes = [dp] * 3 + [ctypes.c_long] + [ctypes.c_int] * 3
             lib.oracle_state.argtypes = [dp] * 4 + [ctypes.c_long] * 3 + [ctypes.c_int] * 4
             lib.oracle_decode.argtypes = [dp] * 6 + [ctypes.c_long] * 2 + [ctypes.c_int] * 3
             for fn in (lib.oracle_forward, lib.oracle_backward, lib.oracle_feature_map, lib.oracle_state,
-                       lib.oracle_decode):
+                       lib.oracle_decode, lib.oracle_forward_carry, lib.oracle_backward_carry):
                 fn.restype = ctypes.c_int
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -108,43 +115,70 @@ def feature_map(x, w):
     return out.reshape(x.shape[:-1] + (m,))
 
 
-def recurrence_forward(q, k, v, w, threads=0):
+def _state_arg(st, b, h, d, m, what):
+    if st is None:
+        return None
+    st = _f64(st)
+    if st.shape != (b, h, d + 1, m):
+        raise ValueError("%s must be [B, H, d + 1, M] = %s, got %s" % (what, (b, h, d + 1, m), st.shape))
+    return st
+
+
+def recurrence_forward(q, k, v, w, threads=0, state0=None, return_state=False):
     """Y = Att^lin(Q, K, V) by the per-step recurrence; arrays [B, H, L, d]
-    (or [L, d]).  w None selects elu+1, else W is [d, M]."""
+    (or [L, d]).  w None selects elu+1, else W is [d, M].
+
+    ``state0`` ([B, H, d + 1, M], e-major like the serving state): the stacked
+    prefix sums R' = [R ; S^T] of rows that came before these (default zero).
+    ``return_state``: also return the state after the last row."""
     shape = np.shape(q)
     q, k, v = _as4d(q), _as4d(k), _as4d(v)
     b, h, length, d = q.shape
     _check_w(w, d)
     m = d if w is None else int(np.shape(w)[1])
     wf = None if w is None else _f64(w)
+    s0 = _state_arg(state0, b, h, d, m, "state0")
+    s_out = np.empty((b, h, d + 1, m), dtype=np.float64) if return_state else None
     y = np.empty_like(q)
-    rc = _load().oracle_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(wf), _ptr(y), b, h, length,
-                                d, m, MAP_ELU if w is None else MAP_FAVOR, int(threads))
+    rc = _load().oracle_forward_carry(_ptr(q), _ptr(k), _ptr(v), _ptr(wf), _ptr(y), _ptr(s0), _ptr(s_out),
+                                      b, h, length, d, m, MAP_ELU if w is None else MAP_FAVOR, int(threads))
     if rc:
         raise ValueError("oracle_forward failed (%d)" % rc)
-    return y.reshape(shape)
+    y = y.reshape(shape)
+    return (y, s_out) if return_state else y
 
 
-def recurrence_backward(q, k, v, w, dy, threads=0, want_dw=True, want_y=False):
-    """Gradients of sum(dy * Y): returns (dq, dk, dv, dw[, y]); dw is None for
-    elu+1 or when ``want_dw`` is False."""
+def recurrence_backward(q, k, v, w, dy, threads=0, want_dw=True, want_y=False, state0=None, g0=None,
+                        want_gstate=False):
+    """Gradients of sum(dy * Y) + sum(g0 * R'_L): returns (dq, dk, dv, dw[, y][, g_state]);
+    dw is None for elu+1 or when ``want_dw`` is False.
+
+    ``state0`` ([B, H, d + 1, M]): the state the forward started from (default
+    zero).  ``g0`` (same layout, default zero): the gradient of what follows
+    these rows with respect to the state R'_L after the last row.
+    ``want_gstate``: also return the gradient with respect to state0."""
     shape = np.shape(q)
     q, k, v, dy = _as4d(q), _as4d(k), _as4d(v), _as4d(dy)
     b, h, length, d = q.shape
     _check_w(w, d)
     m = d if w is None else int(np.shape(w)[1])
     wf = None if w is None else _f64(w)
+    s0 = _state_arg(state0, b, h, d, m, "state0")
+    gin = _state_arg(g0, b, h, d, m, "g0")
+    gout = np.empty((b, h, d + 1, m), dtype=np.float64) if want_gstate else None
     dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
     dw = np.empty((d, m), dtype=np.float64) if (w is not None and want_dw) else None
     y = np.empty_like(q) if want_y else None
-    rc = _load().oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(wf), _ptr(dy), _ptr(dq),
-                                 _ptr(dk), _ptr(dv), _ptr(dw), _ptr(y), b, h, length, d, m,
-                                 MAP_ELU if w is None else MAP_FAVOR, int(threads))
+    rc = _load().oracle_backward_carry(_ptr(q), _ptr(k), _ptr(v), _ptr(wf), _ptr(dy), _ptr(dq),
+                                       _ptr(dk), _ptr(dv), _ptr(dw), _ptr(y), _ptr(s0), _ptr(gin), _ptr(gout),
+                                       b, h, length, d, m, MAP_ELU if w is None else MAP_FAVOR, int(threads))
     if rc:
         raise ValueError("oracle_backward failed (%d)" % rc)
     out = (dq.reshape(shape), dk.reshape(shape), dv.reshape(shape), dw)
     if want_y:
         out = out + (y.reshape(shape),)
+    if want_gstate:
+        out = out + (gout,)
     return out
 
 

@@ -103,14 +103,20 @@ static void set_threads(int nthreads) {
 #endif
 }
 
-/* Forward: y = Att^lin(q, k, v) by the per-step recurrence.  Returns 0 on
- * success, 1 on bad arguments, 2 on allocation failure. */
-int oracle_forward(const double *q, const double *k, const double *v,
-                   const double *W, double *y, long B, long H, long L, int d,
-                   int M, int map, int nthreads) {
+/* Forward: y = Att^lin(q, k, v) by the per-step recurrence, starting from
+ * the stacked prefix-sum state R'_0 = [R_0 ; S_0^T] of rows that came before
+ * (state0, [B][H][d + 1][M] e-major like the serving state, or NULL for
+ * zero), and writing the state after the last row to state_out (same layout,
+ * or NULL).  Rows before the first one enter only through that state: the
+ * prefix sums of eq. (3) simply start from it.  Returns 0 on success, 1 on
+ * bad arguments, 2 on allocation failure. */
+int oracle_forward_carry(const double *q, const double *k, const double *v,
+                         const double *W, double *y, const double *state0, double *state_out,
+                         long B, long H, long L, int d, int M, int map, int nthreads) {
   if (check_args(B, H, L, d, M, map)) return 1;
   set_threads(nthreads);
   const long heads = B * H;
+  const size_t per = (size_t)(d + 1) * M;
   int failed = 0;
 #pragma omp parallel for schedule(dynamic, 1)
   for (long bh = 0; bh < heads; ++bh) {
@@ -122,6 +128,10 @@ int oracle_forward(const double *q, const double *k, const double *v,
 #pragma omp atomic write
       failed = 1;
     } else {
+      if (state0) {
+        memcpy(R, state0 + (size_t)bh * per, (size_t)d * M * sizeof(double));
+        memcpy(S, state0 + (size_t)bh * per + (size_t)d * M, (size_t)M * sizeof(double));
+      }
       const size_t base = (size_t)bh * L * d;
       for (long l = 0; l < L; ++l) {
         const double *ql = q + base + (size_t)l * d;
@@ -143,20 +153,38 @@ int oracle_forward(const double *q, const double *k, const double *v,
           yl[e] = num / den;
         }
       }
+      if (state_out) {
+        memcpy(state_out + (size_t)bh * per, R, (size_t)d * M * sizeof(double));
+        memcpy(state_out + (size_t)bh * per + (size_t)d * M, S, (size_t)M * sizeof(double));
+      }
     }
     free(R); free(S); free(phik); free(phiq);
   }
   return failed ? 2 : 0;
 }
 
-/* Backward of the loss sum_l dy_l . y_l.  dq, dk, dv are [B][H][L][d];
- * dW (d x M) is overwritten with the gradient summed over every head and row
- * when it is not NULL (FAVOR+ only).  y, if not NULL, receives the forward
- * output as a by-product. */
-int oracle_backward(const double *q, const double *k, const double *v,
-                    const double *W, const double *dy, double *dq, double *dk,
-                    double *dv, double *dW, double *y, long B, long H, long L,
-                    int d, int M, int map, int nthreads) {
+/* The forward from a zero state (the whole sequence in one call). */
+int oracle_forward(const double *q, const double *k, const double *v,
+                   const double *W, double *y, long B, long H, long L, int d,
+                   int M, int map, int nthreads) {
+  return oracle_forward_carry(q, k, v, W, y, NULL, NULL, B, H, L, d, M, map, nthreads);
+}
+
+/* Backward of the loss sum_l dy_l . y_l + sum g0 * R'_L, where the forward
+ * started from state0 (NULL: zero) and R'_L is the state after the last row
+ * (e-major [d + 1][M] per head, as state0).  g0 (NULL: zero) is the gradient
+ * of whatever comes after these rows with respect to R'_L: the reverse
+ * prefix sum of section 3.3 starts from it instead of from zero.  dq, dk, dv
+ * are [B][H][L][d]; dW (d x M) is overwritten with the gradient summed over
+ * every head and row when it is not NULL (FAVOR+ only).  y, if not NULL,
+ * receives the forward output as a by-product.  g_out (NULL: not written)
+ * receives the gradient with respect to state0, which is the reverse state
+ * G_1 = g0 + sum_l dN'_l (x) g(Q_l) over every row (same layout). */
+int oracle_backward_carry(const double *q, const double *k, const double *v,
+                          const double *W, const double *dy, double *dq, double *dk,
+                          double *dv, double *dW, double *y, const double *state0,
+                          const double *g0, double *g_out, long B, long H, long L,
+                          int d, int M, int map, int nthreads) {
   if (check_args(B, H, L, d, M, map)) return 1;
   set_threads(nthreads);
   const long heads = B * H;
@@ -190,6 +218,9 @@ int oracle_backward(const double *q, const double *k, const double *v,
       failed = 1;
     } else {
       const size_t base = (size_t)bh * L * d;
+      const size_t per = (size_t)dp * M;
+      if (state0) memcpy(Rp, state0 + (size_t)bh * per, per * sizeof(double));
+      if (g0) memcpy(G, g0 + (size_t)bh * per, per * sizeof(double));
       /* forward sweep: Y_l, dN'_l and dg(Q_l) = R'_l^T dN'_l */
       for (long l = 0; l < L; ++l) {
         const double *ql = q + base + (size_t)l * d;
@@ -223,7 +254,7 @@ int oracle_backward(const double *q, const double *k, const double *v,
         feature_map_backward(ql, d, W, M, map, phiq, dphi, dq + base + (size_t)l * d,
                              dWt);
       }
-      /* reverse sweep: G_j = sum_{l>=j} dN'_l (x) g(Q_l) */
+      /* reverse sweep: G_j = g0 + sum_{l>=j} dN'_l (x) g(Q_l) */
       for (long l = L - 1; l >= 0; --l) {
         const double *kl = k + base + (size_t)l * d;
         const double *vl = v + base + (size_t)l * d;
@@ -246,6 +277,7 @@ int oracle_backward(const double *q, const double *k, const double *v,
         feature_map_backward(kl, d, W, M, map, phik, dphi, dk + base + (size_t)l * d,
                              dWt);
       }
+      if (g_out) memcpy(g_out + (size_t)bh * per, G, per * sizeof(double));
     }
     free(Rp); free(G); free(phiq_all); free(dNp_all);
     free(phik); free(dphi); free(yl);
@@ -259,6 +291,15 @@ int oracle_backward(const double *q, const double *k, const double *v,
   }
   free(dW_parts);
   return failed ? 2 : 0;
+}
+
+/* The backward from zero states at both ends (the whole sequence). */
+int oracle_backward(const double *q, const double *k, const double *v,
+                    const double *W, const double *dy, double *dq, double *dk,
+                    double *dv, double *dW, double *y, long B, long H, long L,
+                    int d, int M, int map, int nthreads) {
+  return oracle_backward_carry(q, k, v, W, dy, dq, dk, dv, dW, y, NULL, NULL, NULL, B, H, L, d, M,
+                               map, nthreads);
 }
 
 /* The feature map alone, for every row of x ([rows][d] -> [rows][M]). */

@@ -294,3 +294,75 @@ def test_prefill_then_decode_is_the_next_row(favor):
         st = oracle.prefill_state(k[:, :, :l], v[:, :, :l], w)
         y = oracle.decode_step(q[:, :, l], k[:, :, l], v[:, :, l], w, st)
         assert np.allclose(y, y_quad[:, :, l], rtol=1e-12, atol=1e-12)
+
+
+# ---- carried boundary states (a sequence processed window by window) -------
+
+
+def _carry_case(rng, favor, length=6, prior=4, b=1, h=2):
+    d, m = 3, (5 if favor else 3)
+    q, k, v, dy, w = _rand(rng, b, h, length, d, m, favor)
+    # a realistic incoming state: the prefix sums of a few earlier rows
+    _, kp, vp, _, _ = _rand(rng, b, h, prior, d, m, favor)
+    state0 = oracle.prefill_state(kp, vp, w)
+    g0 = rng.standard_normal((b, h, d + 1, m)) * 0.3
+    return q, k, v, dy, w, state0, g0
+
+
+@pytest.mark.parametrize("favor", [True, False])
+def test_carry_finite_differences(favor):
+    """The backward with carried states is the gradient of
+    sum(dY * Y) + sum(g0 * R'_L), where the forward starts from state0 and
+    R'_L is its final state: central differences in q, k, v, W and state0."""
+    rng = np.random.default_rng(41 if favor else 43)
+    q, k, v, dy, w, state0, g0 = _carry_case(rng, favor)
+
+    def loss():
+        y, s_out = oracle.recurrence_forward(q, k, v, w, state0=state0, return_state=True)
+        return float(np.sum(dy * y) + np.sum(g0 * s_out))
+
+    dq, dk, dv, dw, gs = oracle.recurrence_backward(q, k, v, w, dy, state0=state0, g0=g0, want_gstate=True)
+    pairs = [(q, dq), (k, dk), (v, dv), (state0, gs)] + ([(w, dw)] if favor else [])
+    for x, g in pairs:
+        fd = _fd_grad(loss, x)
+        assert oracle.rel_l2(g, fd) < 1e-6
+
+
+@pytest.mark.parametrize("favor", [True, False])
+def test_carry_final_state_closed_form(favor):
+    """The state after the last row is state0 plus the rows' own prefix sums:
+    R'_L = state0 + sum_j [V_j ; 1] (x) g(K_j), summed here directly from the
+    feature map."""
+    rng = np.random.default_rng(47)
+    q, k, v, _, w, state0, _ = _carry_case(rng, favor, length=9)
+    _, s_out = oracle.recurrence_forward(q, k, v, w, state0=state0, return_state=True)
+    phik = oracle.feature_map(k, w)  # [B, H, L, M]
+    vp = np.concatenate([v, np.ones(v.shape[:-1] + (1,))], axis=-1)  # [B, H, L, d + 1]
+    expect = state0 + np.einsum("bhle,bhlm->bhem", vp, phik)
+    np.testing.assert_allclose(s_out, expect, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("favor", [True, False])
+@pytest.mark.parametrize("cut", [1, 7, 12])
+def test_windows_with_carried_states_equal_one_pass(favor, cut):
+    """A sequence cut at row `cut` into two windows: the forward of the second
+    starts from the first's final state, the backward of the first takes the
+    second's gradient with respect to its incoming state as g0.  Outputs,
+    gradients (dW summed over the windows) and the gradient with respect to
+    the very first state equal one pass over all rows."""
+    rng = np.random.default_rng(53 + cut)
+    q, k, v, dy, w, state0, g0 = _carry_case(rng, favor, length=13)
+    y_all = oracle.recurrence_forward(q, k, v, w, state0=state0)
+    full = oracle.recurrence_backward(q, k, v, w, dy, state0=state0, g0=g0, want_gstate=True)
+    a = lambda t: t[:, :, :cut]
+    b_ = lambda t: t[:, :, cut:]
+    y1, s1 = oracle.recurrence_forward(a(q), a(k), a(v), w, state0=state0, return_state=True)
+    y2 = oracle.recurrence_forward(b_(q), b_(k), b_(v), w, state0=s1)
+    np.testing.assert_allclose(np.concatenate([y1, y2], axis=2), y_all, rtol=1e-12, atol=1e-12)
+    g2 = oracle.recurrence_backward(b_(q), b_(k), b_(v), w, b_(dy), state0=s1, g0=g0, want_gstate=True)
+    g1 = oracle.recurrence_backward(a(q), a(k), a(v), w, a(dy), state0=state0, g0=g2[4], want_gstate=True)
+    for i in range(3):
+        np.testing.assert_allclose(np.concatenate([g1[i], g2[i]], axis=2), full[i], rtol=1e-10, atol=1e-12)
+    if favor:
+        np.testing.assert_allclose(g1[3] + g2[3], full[3], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g1[4], full[4], rtol=1e-10, atol=1e-12)
