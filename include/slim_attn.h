@@ -110,6 +110,52 @@ slim_status slim_attn_bwd_f32(const float *q, const float *k, const float *v,
                               float *dv, float *dw, int B, int H, int L, int d, int M,
                               int chunk, slim_stream_t stream);
 
+/* The same operations for one window of a longer sequence (section 3.2: a
+ * slice is linked to the rows before it only by the prefix-sum state at its
+ * boundary; section 3.3: to the rows after it only by the reverse state).
+ * Every state is fp32, e-major, heads contiguous: [B][H][d + 1][M] with rows
+ * e < d the value part and row d the normaliser part, the layout of the
+ * serving state below.  Each pointer may be NULL: an incoming state is then
+ * zero and an outgoing one is not written.  The caller owns them; they must
+ * not overlap each other or the workspace.
+ *   slim_attn_fwd_carry: the forward of rows that follow earlier rows whose
+ *     state is state_in; writes the state after the last row to state_out.
+ *   slim_attn_bwd_carry: the gradients of sum(dy * y) + sum(g_in * R'_L),
+ *     R'_L the state after the last row, for a forward that started from
+ *     state_in: g_in is the gradient arriving at R'_L from the rows after
+ *     this window.  g_out receives the gradient with respect to state_in,
+ *     which is the g_in of the window before.  dw covers this window only.
+ * Cutting a sequence into windows and chaining these calls (the forward left
+ * to right, passing state_out on; the backward right to left, passing g_out
+ * on and restoring each window's state_in) gives the outputs and gradients
+ * of one call over all rows, to rounding, with device memory for one window.
+ * The elu+1 backward at d = 128 runs on the CUDA-core kernels when it carries
+ * a state. */
+slim_status slim_attn_fwd_carry(const void *q, const void *k, const void *v, const float *w, void *y,
+                                const float *state_in, float *state_out, int B, int H, int L, int d, int M,
+                                int chunk, slim_stream_t stream);
+slim_status slim_attn_bwd_carry(const void *q, const void *k, const void *v, const float *w, const void *dy,
+                                void *dq, void *dk, void *dv, float *dw, const float *state_in, const float *g_in,
+                                float *g_out, int B, int H, int L, int d, int M, int chunk, slim_stream_t stream);
+slim_status slim_attn_fwd_carry_f32(const float *q, const float *k, const float *v, const float *w, float *y,
+                                    const float *state_in, float *state_out, int B, int H, int L, int d, int M,
+                                    int chunk, slim_stream_t stream);
+slim_status slim_attn_bwd_carry_f32(const float *q, const float *k, const float *v, const float *w,
+                                    const float *dy, float *dq, float *dk, float *dv, float *dw,
+                                    const float *state_in, const float *g_in, float *g_out, int B, int H, int L,
+                                    int d, int M, int chunk, slim_stream_t stream);
+
+/* Copy rows [src_row0, src_row0 + rows) of each of `heads` heads of src
+ * (src_rows rows per head, row_bytes bytes per row, heads contiguous) into
+ * rows [dst_row0, ...) of dst (dst_rows rows per head): one strided
+ * asynchronous copy on `stream`, host or device memory on either side (by
+ * unified addressing; pinned host memory for the copy to overlap other work).
+ * Moves a window of [B][H][L][d] tensors between a host-resident sequence and
+ * device buffers.  Bounds are checked on the host. */
+slim_status slim_attn_copy_rows(void *dst, long long dst_rows, long long dst_row0, const void *src,
+                                long long src_rows, long long src_row0, long long rows, long long heads,
+                                long long row_bytes, slim_stream_t stream);
+
 /* Size of the fixed device scratch array behind slim_attn_fwd_noalloc. */
 #define SLIM_NOALLOC_SCRATCH_BYTES (64u << 20)
 

@@ -51,6 +51,16 @@ _lib.slim_attn_profile_get.argtypes = [_i, ctypes.POINTER(ctypes.c_char_p),
 _lib.slim_attn_profile_get.restype = _i
 _lib.slim_attn_profile_reset.argtypes = []
 _lib.slim_attn_profile_reset.restype = None
+_lib.slim_attn_fwd_carry.argtypes = [_vp] * 7 + [_i] * 6 + [_vp]
+_lib.slim_attn_fwd_carry_f32.argtypes = _lib.slim_attn_fwd_carry.argtypes
+_lib.slim_attn_bwd_carry.argtypes = [_vp] * 12 + [_i] * 6 + [_vp]
+_lib.slim_attn_bwd_carry_f32.argtypes = _lib.slim_attn_bwd_carry.argtypes
+for _f in (_lib.slim_attn_fwd_carry, _lib.slim_attn_fwd_carry_f32, _lib.slim_attn_bwd_carry,
+           _lib.slim_attn_bwd_carry_f32):
+    _f.restype = _i
+_ll = ctypes.c_longlong
+_lib.slim_attn_copy_rows.argtypes = [_vp, _ll, _ll, _vp, _ll, _ll, _ll, _ll, _ll, _vp]
+_lib.slim_attn_copy_rows.restype = _i
 _lib.slim_attn_noalloc_bytes.argtypes = [_i] * 6
 _lib.slim_attn_noalloc_bytes.restype = _sz
 _lib.slim_attn_fwd_noalloc.argtypes = _lib.slim_attn_fwd.argtypes
@@ -70,6 +80,8 @@ EXPORTED = (
     "slim_attn_segments", "slim_attn_sync_status", "slim_status_string",
     "slim_attn_profile_count", "slim_attn_profile_get", "slim_attn_profile_reset",
     "slim_attn_fwd_noalloc", "slim_attn_noalloc_bytes", "slim_attn_selftest_timeout",
+    "slim_attn_fwd_carry", "slim_attn_bwd_carry", "slim_attn_fwd_carry_f32", "slim_attn_bwd_carry_f32",
+    "slim_attn_copy_rows",
 )
 
 
@@ -185,33 +197,79 @@ def _prepare(shape, is_bwd, device):
     _check(_lib.slim_attn_set_workspace(_vp(buf.data_ptr()), buf.numel()), "slim_attn_set_workspace")
 
 
-def slim_attn_fwd(q, k, v, w, chunk, y=None):
-    """Y = Att^lin(Q, K, V) through the library (bf16 or fp32 I/O by q's dtype)."""
+def _check_state(st, b, h, d, m, device, what):
+    if st is None:
+        return
+    if st.shape != (b, h, d + 1, m) or st.dtype != torch.float32 or not st.is_contiguous() \
+            or st.device != device:
+        raise ValueError("%s must be a contiguous fp32 [B, H, d + 1, M] tensor on q's device" % what)
+
+
+def slim_attn_fwd(q, k, v, w, chunk, y=None, state_in=None, state_out=None):
+    """Y = Att^lin(Q, K, V) through the library (bf16 or fp32 I/O by q's dtype).
+
+    ``state_in`` / ``state_out`` (fp32 [B, H, d + 1, M], optional): the
+    prefix-sum state of rows before these, and a buffer for the state after
+    the last row (a window of a longer sequence)."""
     b, h, length, d, m = _validate(q, k, v, w)
     if y is None:
         y = torch.empty_like(q)
+    _check_state(state_in, b, h, d, m, q.device, "state_in")
+    _check_state(state_out, b, h, d, m, q.device, "state_out")
     _prepare((b, h, length, d, m, chunk), False, q.device)
-    fn = _lib.slim_attn_fwd if q.dtype == torch.bfloat16 else _lib.slim_attn_fwd_f32
     stream = torch.cuda.current_stream(q.device).cuda_stream
-    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(y), b, h, length, d, m, chunk, _vp(stream)),
-           "slim_attn_fwd")
+    if state_in is None and state_out is None:
+        fn = _lib.slim_attn_fwd if q.dtype == torch.bfloat16 else _lib.slim_attn_fwd_f32
+        _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(y), b, h, length, d, m, chunk, _vp(stream)),
+               "slim_attn_fwd")
+    else:
+        fn = _lib.slim_attn_fwd_carry if q.dtype == torch.bfloat16 else _lib.slim_attn_fwd_carry_f32
+        _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(y), _ptr(state_in), _ptr(state_out),
+                  b, h, length, d, m, chunk, _vp(stream)), "slim_attn_fwd_carry")
     return y
 
 
-def slim_attn_bwd(q, k, v, w, dy, chunk, want_dw=False, out=None):
-    """Gradients of sum(dy * Y): returns (dq, dk, dv, dw or None)."""
+def slim_attn_bwd(q, k, v, w, dy, chunk, want_dw=False, out=None, state_in=None, g_in=None, g_out=None):
+    """Gradients of sum(dy * Y): returns (dq, dk, dv, dw or None).
+
+    For a window of a longer sequence: ``state_in`` is the state the forward
+    started from, ``g_in`` the gradient arriving at the state after the last
+    row (both fp32 [B, H, d + 1, M], optional), and ``g_out`` a buffer for the
+    gradient with respect to ``state_in``."""
     b, h, length, d, m = _validate(q, k, v, w, (dy,))
     if out is None:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
         dw = torch.empty((d, m), dtype=torch.float32, device=q.device) if (want_dw and w is not None) else None
     else:
         dq, dk, dv, dw = out
+    for st, what in ((state_in, "state_in"), (g_in, "g_in"), (g_out, "g_out")):
+        _check_state(st, b, h, d, m, q.device, what)
     _prepare((b, h, length, d, m, chunk), True, q.device)
-    fn = _lib.slim_attn_bwd if q.dtype == torch.bfloat16 else _lib.slim_attn_bwd_f32
     stream = torch.cuda.current_stream(q.device).cuda_stream
-    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(dy), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dw),
-              b, h, length, d, m, chunk, _vp(stream)), "slim_attn_bwd")
+    if state_in is None and g_in is None and g_out is None:
+        fn = _lib.slim_attn_bwd if q.dtype == torch.bfloat16 else _lib.slim_attn_bwd_f32
+        _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(dy), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dw),
+                  b, h, length, d, m, chunk, _vp(stream)), "slim_attn_bwd")
+    else:
+        fn = _lib.slim_attn_bwd_carry if q.dtype == torch.bfloat16 else _lib.slim_attn_bwd_carry_f32
+        _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(dy), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dw),
+                  _ptr(state_in), _ptr(g_in), _ptr(g_out), b, h, length, d, m, chunk, _vp(stream)),
+               "slim_attn_bwd_carry")
     return dq, dk, dv, dw
+
+
+def copy_rows(dst, dst_row0, src, src_row0, rows, stream=None):
+    """Rows [src_row0, +rows) of every head of src ([B, H, L_src, d]) into rows
+    [dst_row0, +rows) of dst ([B, H, L_dst, d]); host (pinned) or device
+    tensors on either side, one strided asynchronous copy on ``stream``."""
+    if src.dim() != 4 or dst.dim() != 4 or src.shape[:2] != dst.shape[:2] or src.shape[3] != dst.shape[3] \
+            or src.dtype != dst.dtype or not src.is_contiguous() or not dst.is_contiguous():
+        raise ValueError("src and dst must be contiguous [B, H, L, d] tensors of one dtype and head shape")
+    s = torch.cuda.current_stream() if stream is None else stream
+    heads = src.shape[0] * src.shape[1]
+    row_bytes = src.shape[3] * src.element_size()
+    _check(_lib.slim_attn_copy_rows(_ptr(dst), dst.shape[2], dst_row0, _ptr(src), src.shape[2], src_row0, rows,
+                                    heads, row_bytes, _vp(s.cuda_stream)), "slim_attn_copy_rows")
 
 
 def slim_attn_state(k, v, w, chunk, state=None):

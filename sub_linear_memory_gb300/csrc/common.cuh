@@ -43,6 +43,8 @@ struct Plan {
                        // shared-memory image the kernels bulk-copy
   size_t gimg_off;     // tensor-path backward: per (head, segment) G_end record,
                        // bf16 [M][64] swizzled image + fp32 [M] (M * 132 bytes)
+  size_t carry_off;    // tensor path: the carried states R'_0 and G_0 turned
+                       // features-major, fp32 [2][BH][M][dp]
   size_t scratch_stride;
   size_t total_floats;
 };
@@ -55,6 +57,13 @@ struct Args {
   float *dw;
   float *ws;       // workspace base
   int *status;     // device status word (SLIM_OK or the first error recorded)
+  // carried boundary states, fp32 e-major [BH][d + 1][M] (NULL: zero / not
+  // wanted): R' of the rows before this call, R' after its last row, the
+  // gradient arriving at that final state, the gradient w.r.t. state_in
+  const float *state_in;
+  float *state_out;
+  const float *g_in;
+  float *g_out;
 };
 
 __host__ __device__ inline size_t align_floats(size_t n) { return (n + 63) & ~size_t(63); }  // 256 B

@@ -270,21 +270,22 @@ __global__ void __launch_bounds__(kThreads) segment_state_kernel(Plan p, Args a)
   }
 }
 
-// In-place inclusive scan of segment states over s (forward: R'; reverse: G).
+// In-place inclusive scan of segment states over s (forward: R'; reverse: G),
+// starting from `init` (fp32 [BH][dp][M], the carried state of rows outside
+// this call) when it is not NULL.
 template <typename S>
-__global__ void scan_states_kernel(Plan p, S *st, int nseg, int reverse) {
+__global__ void scan_states_kernel(Plan p, S *st, int nseg, int reverse, const float *init) {
   const size_t per = (size_t)p.dp * p.M;
   const size_t n = (size_t)p.BH * per;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x) {
     const size_t bh = i / per, e = i - bh * per;
     S *b = st + bh * p.P * per + e;
+    S acc = init ? (S)init[i] : (S)0;
     if (!reverse) {
-      S acc = b[0];
-      for (int s = 1; s < nseg; ++s) { acc += b[s * per]; b[s * per] = acc; }
+      for (int s = 0; s < nseg; ++s) { acc += b[s * per]; b[s * per] = acc; }
     } else {
-      S acc = b[(size_t)(nseg - 1) * per];
-      for (int s = nseg - 2; s >= 0; --s) { acc += b[s * per]; b[s * per] = acc; }
+      for (int s = nseg - 1; s >= 0; --s) { acc += b[s * per]; b[s * per] = acc; }
     }
   }
 }
@@ -296,8 +297,10 @@ __global__ void __launch_bounds__(kThreads) forward_kernel(Plan p, Args a) {
   __shared__ float sq[256], den[256];
   const int s = blockIdx.x, bh = blockIdx.y;
   FwdScratch sc = fwd_scratch(p, cta_scratch(p, a));
+  // segment 0 starts from the carried state (zero when there is none)
   const double *R0 = s > 0 ? state_ptr(p, a, p.states_off, bh, s - 1) : nullptr;
-  for (int i = threadIdx.x; i < p.dp * p.M; i += kThreads) sc.R[i] = R0 ? R0[i] : 0.0;
+  const float *R0c = (s == 0 && a.state_in) ? a.state_in + (size_t)bh * p.dp * p.M : nullptr;
+  for (int i = threadIdx.x; i < p.dp * p.M; i += kThreads) sc.R[i] = R0 ? R0[i] : (R0c ? (double)R0c[i] : 0.0);
   __syncthreads();
   const int c0 = s * p.cps, c1 = min(c0 + p.cps, p.nchunks);
   for (int c = c0; c < c1; ++c) {
@@ -329,12 +332,14 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) segment_dg_kernel(Plan p, Args a) {
   __shared__ float sq[256], den[256];
   const int s = blockIdx.x, bh = blockIdx.y;
-  if (s == 0) return;
+  // segment 0's total is needed only for the gradient w.r.t. the incoming state
+  if (s == 0 && !a.g_out) return;
   double *out = state_ptr(p, a, p.gstates_off, bh, s);
   FwdScratch sc = fwd_scratch(p, cta_scratch(p, a));
-  const double *R0 = state_ptr(p, a, p.states_off, bh, s - 1);
+  const double *R0 = s > 0 ? state_ptr(p, a, p.states_off, bh, s - 1) : nullptr;
+  const float *R0c = (s == 0 && a.state_in) ? a.state_in + (size_t)bh * p.dp * p.M : nullptr;
   for (int i = threadIdx.x; i < p.dp * p.M; i += kThreads) {
-    sc.R[i] = R0[i];
+    sc.R[i] = R0 ? R0[i] : (R0c ? (double)R0c[i] : 0.0);
     out[i] = 0.0;
   }
   __syncthreads();
@@ -402,10 +407,13 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(Plan p, Args a) {
   BwdScratch sc = bwd_scratch(p, cta_scratch(p, a));
   float *dwp = a.dw ? a.ws + p.dwpart_off + ((size_t)bh * p.P + s) * d * M : nullptr;
   const double *Rend = state_ptr(p, a, p.states_off, bh, s);
+  // the last segment's reverse state starts from the gradient arriving at the
+  // final state (zero when there is none); the others from the scan
   const double *Gend = s + 1 < p.P ? state_ptr(p, a, p.gstates_off, bh, s + 1) : nullptr;
+  const float *Gc = (s + 1 == p.P && a.g_in) ? a.g_in + (size_t)bh * dp * M : nullptr;
   for (int i = threadIdx.x; i < dp * M; i += kThreads) {
     sc.R[i] = Rend[i];
-    sc.G[i] = Gend ? Gend[i] : 0.0;
+    sc.G[i] = Gend ? Gend[i] : (Gc ? (double)Gc[i] : 0.0);
   }
   if (dwp)
     for (int i = threadIdx.x; i < d * M; i += kThreads) dwp[i] = 0.f;
@@ -482,14 +490,15 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(Plan p, Args a) {
 // input low parts are read only when lo_in is set, else taken as zero), in
 // fp32 double-float arithmetic (two-sum): GB300's fp64 rate would make fp64
 // the bottleneck of this memory-bound pass.  Relative error ~2^-47.
-__global__ void scan_states_df_kernel(Plan p, float *hi, float *lo, int nseg, int lo_in) {
+__global__ void scan_states_df_kernel(Plan p, float *hi, float *lo, int nseg, int lo_in, const float *init) {
   const size_t per = (size_t)p.dp * p.M;
   const size_t n = (size_t)p.BH * per;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x) {
     const size_t bh = i / per, e = i - bh * per;
     float *h = hi + bh * p.P * per + e, *l = lo + bh * p.P * per + e;
-    float sh = 0.f, sl = 0.f;
+    // the sum starts from the carried state of earlier rows, if any
+    float sh = init ? init[i] : 0.f, sl = 0.f;
     // loads of a group do not depend on the running sum, so they overlap
     for (int s0 = 0; s0 < nseg; s0 += 16) {
       float xh[16], xl[16];
@@ -519,14 +528,14 @@ __global__ void scan_states_df_kernel(Plan p, float *hi, float *lo, int nseg, in
 
 // Inclusive fp32 scan over segments (reverse: from the last segment down),
 // loads batched as above.
-__global__ void scan_states_f32_kernel(Plan p, float *st, int nseg, int reverse) {
+__global__ void scan_states_f32_kernel(Plan p, float *st, int nseg, int reverse, const float *init) {
   const size_t per = (size_t)p.dp * p.M;
   const size_t n = (size_t)p.BH * per;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x) {
     const size_t bh = i / per, e = i - bh * per;
     float *b = st + bh * p.P * per + e;
-    float acc = 0.f;
+    float acc = init ? init[i] : 0.f;
     for (int s0 = 0; s0 < nseg; s0 += 16) {
       float x[16];
       const int cnt = min(16, nseg - s0);
@@ -600,6 +609,18 @@ size_t generic_scratch_floats(const Plan &p, bool bwd) {
   return 2 * st + 4 * cm + 2 * cc + cdp + cd;
 }
 
+namespace gen {
+// Slot s of per-segment fp64 states (e-major [dp][M]), plus `add` (fp32
+// [BH][dp][M]) when it is not NULL -> fp32 [BH][dp][M].
+__global__ void slot_f32_kernel(Plan p, const double *states, int s, const float *add, float *out) {
+  const size_t per = (size_t)p.dp * p.M, n = (size_t)p.BH * per;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t bh = i / per, r = i - bh * per;
+    out[i] = (float)(states[(bh * p.P + s) * per + r] + (add ? (double)add[i] : 0.0));
+  }
+}
+}  // namespace gen
+
 static int scan_blocks(const Plan &p) {
   const size_t n = (size_t)p.BH * p.dp * p.M;
   return (int)std::min<size_t>((n + 255) / 256, 4096);
@@ -607,17 +628,27 @@ static int scan_blocks(const Plan &p) {
 
 template <typename T>
 cudaError_t generic_forward(const Plan &p, const Args &a, cudaStream_t st) {
-  if (p.P > 1) {
+  // segment totals (the last one only for the final state), scanned from the
+  // carried incoming state
+  const int nseg = a.state_out ? p.P : p.P - 1;
+  if (nseg > 0) {
     {
       ProfScope ps("gen_segment_state", st);
-      gen::segment_state_kernel<T><<<dim3(p.P - 1, p.BH), gen::kThreads, 0, st>>>(p, a);
+      gen::segment_state_kernel<T><<<dim3(nseg, p.BH), gen::kThreads, 0, st>>>(p, a);
     }
     ProfScope ps("gen_scan_states", st);
     gen::scan_states_kernel<<<scan_blocks(p), 256, 0, st>>>(
-        p, reinterpret_cast<double *>(a.ws + p.states_off), p.P - 1, 0);
+        p, reinterpret_cast<double *>(a.ws + p.states_off), nseg, 0, a.state_in);
   }
-  ProfScope ps("gen_forward", st);
-  gen::forward_kernel<T><<<dim3(p.P, p.BH), gen::kThreads, 0, st>>>(p, a);
+  {
+    ProfScope ps("gen_forward", st);
+    gen::forward_kernel<T><<<dim3(p.P, p.BH), gen::kThreads, 0, st>>>(p, a);
+  }
+  if (a.state_out) {
+    const size_t n = (size_t)p.BH * p.dp * p.M;
+    gen::slot_f32_kernel<<<(int)std::min<size_t>((n + 255) / 256, 4096), 256, 0, st>>>(
+        p, reinterpret_cast<const double *>(a.ws + p.states_off), p.P - 1, nullptr, a.state_out);
+  }
   return cudaGetLastError();
 }
 
@@ -630,17 +661,20 @@ cudaError_t generic_backward(const Plan &p, const Args &a, cudaStream_t st) {
   {
     ProfScope ps("gen_scan_states", st);
     gen::scan_states_kernel<<<scan_blocks(p), 256, 0, st>>>(
-        p, reinterpret_cast<double *>(a.ws + p.states_off), p.P, 0);
+        p, reinterpret_cast<double *>(a.ws + p.states_off), p.P, 0, a.state_in);
   }
-  if (p.P > 1) {
+  if (p.P > 1 || a.g_out) {
     {
       ProfScope ps("gen_segment_dg", st);
       gen::segment_dg_kernel<T><<<dim3(p.P, p.BH), gen::kThreads, 0, st>>>(p, a);
     }
-    // G_end(s) = sum_{s' > s} dG_s': reverse inclusive scan over s = 1..P-1
+    // G_end(s) = g_in + sum_{s' > s} dG_s': reverse inclusive scan over
+    // s = 1..P-1, or over s = 0..P-1 when the gradient w.r.t. the incoming
+    // state (slot 0 afterwards) is wanted
     ProfScope ps("gen_scan_states", st);
+    const int s0 = a.g_out ? 0 : 1;
     gen::scan_states_kernel<<<scan_blocks(p), 256, 0, st>>>(
-        p, reinterpret_cast<double *>(a.ws + p.gstates_off) + (size_t)p.dp * p.M, p.P - 1, 1);
+        p, reinterpret_cast<double *>(a.ws + p.gstates_off) + (size_t)s0 * p.dp * p.M, p.P - s0, 1, a.g_in);
   }
   {
     ProfScope ps("gen_backward", st);
@@ -651,16 +685,22 @@ cudaError_t generic_backward(const Plan &p, const Args &a, cudaStream_t st) {
     ProfScope ps("gen_reduce_dw", st);
     gen::reduce_dw_kernel<<<(n + 255) / 256, 256, 0, st>>>(p, a.ws + p.dwpart_off, a.dw);
   }
+  if (a.g_out) {
+    const size_t n = (size_t)p.BH * p.dp * p.M;
+    gen::slot_f32_kernel<<<(int)std::min<size_t>((n + 255) / 256, 4096), 256, 0, st>>>(
+        p, reinterpret_cast<const double *>(a.ws + p.gstates_off), 0, nullptr, a.g_out);
+  }
   return cudaGetLastError();
 }
 
-cudaError_t scan_states_f32(const Plan &p, float *states, int nseg, cudaStream_t st) {
-  gen::scan_states_f32_kernel<<<scan_blocks(p), 256, 0, st>>>(p, states, nseg, 0);
+cudaError_t scan_states_f32(const Plan &p, float *states, int nseg, const float *init, cudaStream_t st) {
+  gen::scan_states_f32_kernel<<<scan_blocks(p), 256, 0, st>>>(p, states, nseg, 0, init);
   return cudaGetLastError();
 }
 
-cudaError_t scan_states_df(const Plan &p, float *hi, float *lo, int nseg, int lo_in, cudaStream_t st) {
-  gen::scan_states_df_kernel<<<scan_blocks(p), 256, 0, st>>>(p, hi, lo, nseg, lo_in);
+cudaError_t scan_states_df(const Plan &p, float *hi, float *lo, int nseg, int lo_in, const float *init,
+                           cudaStream_t st) {
+  gen::scan_states_df_kernel<<<scan_blocks(p), 256, 0, st>>>(p, hi, lo, nseg, lo_in, init);
   return cudaGetLastError();
 }
 
@@ -671,21 +711,11 @@ cudaError_t reduce_dw_t(const Plan &p, const float *parts, float *dw, cudaStream
   return cudaGetLastError();
 }
 
-cudaError_t scan_states_f32_rev(const Plan &p, float *states, int nseg, cudaStream_t st) {
-  gen::scan_states_f32_kernel<<<scan_blocks(p), 256, 0, st>>>(p, states, nseg, 1);
+cudaError_t scan_states_f32_rev(const Plan &p, float *states, int nseg, const float *init, cudaStream_t st) {
+  gen::scan_states_f32_kernel<<<scan_blocks(p), 256, 0, st>>>(p, states, nseg, 1, init);
   return cudaGetLastError();
 }
 
-namespace gen {
-// The last segment's inclusive state (fp64 e-major [dp][M]) -> fp32 [BH][dp][M].
-__global__ void last_state_f32_kernel(Plan p, const double *states, float *out) {
-  const size_t per = (size_t)p.dp * p.M, n = (size_t)p.BH * per;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-    const size_t bh = i / per, r = i - bh * per;
-    out[i] = (float)states[(bh * p.P + (p.P - 1)) * per + r];
-  }
-}
-}  // namespace gen
 
 template <typename T>
 cudaError_t generic_prefill_state(const Plan &p, const Args &a, float *state, cudaStream_t st) {
@@ -696,11 +726,11 @@ cudaError_t generic_prefill_state(const Plan &p, const Args &a, float *state, cu
   if (p.P > 1) {
     ProfScope ps("gen_scan_states", st);
     gen::scan_states_kernel<<<scan_blocks(p), 256, 0, st>>>(p, reinterpret_cast<double *>(a.ws + p.states_off), p.P,
-                                                            0);
+                                                            0, nullptr);
   }
   const size_t n = (size_t)p.BH * p.dp * p.M;
-  gen::last_state_f32_kernel<<<(int)std::min<size_t>((n + 255) / 256, 4096), 256, 0, st>>>(
-      p, reinterpret_cast<const double *>(a.ws + p.states_off), state);
+  gen::slot_f32_kernel<<<(int)std::min<size_t>((n + 255) / 256, 4096), 256, 0, st>>>(
+      p, reinterpret_cast<const double *>(a.ws + p.states_off), p.P - 1, nullptr, state);
   return cudaGetLastError();
 }
 

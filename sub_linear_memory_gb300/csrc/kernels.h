@@ -31,11 +31,13 @@ size_t generic_scratch_floats(const Plan &p, bool bwd);
 template <typename T> cudaError_t generic_forward(const Plan &p, const Args &a, cudaStream_t st);
 template <typename T> cudaError_t generic_backward(const Plan &p, const Args &a, cudaStream_t st);
 // In-place inclusive scan over the first nseg segment states (fp32 layout),
-// forward (state s += state s-1) or reverse (state s += state s+1).
-cudaError_t scan_states_f32(const Plan &p, float *states, int nseg, cudaStream_t st);
-cudaError_t scan_states_f32_rev(const Plan &p, float *states, int nseg, cudaStream_t st);
-// The same forward scan for double-float (hi, lo) states, summed in fp64.
-cudaError_t scan_states_df(const Plan &p, float *hi, float *lo, int nseg, int lo_in, cudaStream_t st);
+// forward (state s += state s-1) or reverse (state s += state s+1), starting
+// from `init` (one state per head in the same layout, or NULL for zero).
+cudaError_t scan_states_f32(const Plan &p, float *states, int nseg, const float *init, cudaStream_t st);
+cudaError_t scan_states_f32_rev(const Plan &p, float *states, int nseg, const float *init, cudaStream_t st);
+// The same forward scan for double-float (hi, lo) states, in double-float arithmetic.
+cudaError_t scan_states_df(const Plan &p, float *hi, float *lo, int nseg, int lo_in, const float *init,
+                           cudaStream_t st);
 // dW [d][M] = the sum, in a fixed order, of the BH x P per-segment partials
 // of dW^T ([M][d] each).
 cudaError_t reduce_dw_t(const Plan &p, const float *parts, float *dw, cudaStream_t st);
@@ -44,17 +46,28 @@ cudaError_t reduce_dw_t(const Plan &p, const float *parts, float *dw, cudaStream
 bool tc_forward_supported(int d, int M, int chunk, bool favor);
 size_t tc_smem_bytes(int d, int M, bool favor);
 cudaError_t tc_forward(const Plan &p, const Args &a, cudaStream_t st);
-// K-side totals of R' for the first nseg segments, scanned (tensor path).
-// zero_grads: also set dQ, dK, dV to zero tile by tile (the two-CTA backward
-// then adds each CTA's partials into them).
-cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, bool zero_grads, cudaStream_t st);
+// K-side totals of R' for the first nseg segments, scanned from `init` (the
+// carried incoming state, features-major fp32 [BH][M][d + 1], or NULL) as
+// double-float pairs (tensor path).  zero_grads: also set dQ, dK, dV to zero
+// tile by tile (the two-CTA backward then adds each CTA's partials into them).
+cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, bool zero_grads, const float *init,
+                              cudaStream_t st);
+// Carried states (carry.cu): the caller's e-major [BH][d + 1][M] layout into
+// the tensor path's features-major [BH][M][d + 1], and the sum of one slot of
+// two features-major state arrays ([BH][pa][M][d + 1], b may be NULL) back
+// into e-major.
+cudaError_t emajor_to_fm(const Plan &p, const float *src, float *dst, cudaStream_t st);
+cudaError_t fm_to_emajor(const Plan &p, const float *a, int pa, int sa, const float *b, int pb, int sb, float *out,
+                         cudaStream_t st);
 // dK, dV += the terms of the later segments' reverse state (after the backward
-// kernel and the reverse scan of the segment G totals).
-cudaError_t tc_correction(const Plan &p, const Args &a, cudaStream_t st);
+// kernel and the reverse scan of the segment G totals).  g_last: the reverse
+// state arriving from rows after this call (features-major [BH][M][d + 1]),
+// which is also the last segment's G_end, or NULL.
+cudaError_t tc_correction(const Plan &p, const Args &a, const float *g_last, cudaStream_t st);
 // Learnable W (FAVOR+): the later segments' reverse-state terms of dW, added
 // to the per-segment partials (after tc_correction, which builds the G_end
 // images it reads).
-cudaError_t tc_dw_correction(const Plan &p, const Args &a, cudaStream_t st);
+cudaError_t tc_dw_correction(const Plan &p, const Args &a, const float *g_last, cudaStream_t st);
 
 // Serving form (decode.cu, generic.cu): the state after L rows, fp32
 // e-major [BH][d + 1][M], and one decode step for every head.

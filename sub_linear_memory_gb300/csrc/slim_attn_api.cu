@@ -6,6 +6,7 @@
 #include <map>
 #include <mutex>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "common.cuh"
@@ -162,33 +163,63 @@ Plan make_plan(int B, int H, int L, int d, int M, int chunk, bool favor, bool bw
   p.wimg_off = off; if (path == 2 && favor) off += align_floats((size_t)M * 32);
   // bf16 G_end images [M][d] and fp32 G_S [M] per (head, segment)
   p.gimg_off = off; if (path == 2 && bwd) off += align_floats((size_t)p.BH * p.P * M * (d / 2 + 1));
+  // carried states turned features-major: R'_0 and G (tensor path)
+  p.carry_off = off; if (path == 2) off += align_floats((size_t)2 * p.BH * M * p.dp);
   p.total_floats = off;
   return p;
 }
 
+// Carried boundary states (fp32 e-major [B][H][d + 1][M] each, NULL = zero in
+// / not wanted out): state_in, state_out (forward) and state_in, g_in, g_out
+// (backward).
+struct Carry {
+  const float *state_in = nullptr;
+  float *state_out = nullptr;
+  const float *g_in = nullptr;
+  float *g_out = nullptr;
+  bool any() const { return state_in || state_out || g_in || g_out; }
+};
+
 template <typename T>
 slim_status run(bool bwd, const void *q, const void *k, const void *v, const float *w,
                 const void *dy, void *y, void *dq, void *dk, void *dv, float *dw, int B, int H,
-                int L, int d, int M, int chunk, cudaStream_t stream) {
+                int L, int d, int M, int chunk, cudaStream_t stream, const Carry &c = Carry()) {
   const bool favor = w != nullptr;
   slim_status st = check_shape(B, H, L, d, M, chunk, favor);
   if (st != SLIM_OK) return st;
   if (!favor && dw) return SLIM_ERR_INVALID_ARG;
   if ((long long)B * H * L == 0) {
     if (dw && cudaMemsetAsync(dw, 0, sizeof(float) * d * M, stream) != cudaSuccess) return SLIM_ERR_CUDA;
+    // no rows: the final state is the incoming one, and the gradient w.r.t. the
+    // incoming state is the one arriving at the final state
+    const size_t sbytes = sizeof(float) * (size_t)B * H * (d + 1) * M;
+    const std::pair<float *, const float *> pass[2] = {{c.state_out, c.state_in}, {c.g_out, c.g_in}};
+    for (const auto &pr : pass) {
+      if (!pr.first || sbytes == 0) continue;
+      const cudaError_t e = pr.second ? cudaMemcpyAsync(pr.first, pr.second, sbytes, cudaMemcpyDefault, stream)
+                                      : cudaMemsetAsync(pr.first, 0, sbytes, stream);
+      if (e != cudaSuccess) return SLIM_ERR_CUDA;
+    }
     return SLIM_OK;
   }
   if (!q || !k || !v) return SLIM_ERR_INVALID_ARG;
   if (!bwd && !y) return SLIM_ERR_INVALID_ARG;
   if (bwd && (!dy || !dq || !dk || !dv)) return SLIM_ERR_INVALID_ARG;
   const bool io_ok = sizeof(T) == 2 && g_opt_path != 1 && aligned16(q) && aligned16(k) && aligned16(v);
-  const bool tc = io_ok && (bwd ? (tc_backward_supported(d, M, chunk, favor) &&
-                                   aligned16(dy) && aligned16(dq) && aligned16(dk) && aligned16(dv))
+  // the two-CTA elu+1 backward at d = 128 takes no carried state: such calls
+  // run on the CUDA-core kernels
+  const bool tc_bwd = tc_backward_supported(d, M, chunk, favor) &&
+                      !(c.any() && tc_backward_elu128_supported(d, M, chunk, favor));
+  const bool tc = io_ok && (bwd ? (tc_bwd && aligned16(dy) && aligned16(dq) && aligned16(dk) && aligned16(dv))
                                 : (tc_forward_supported(d, M, chunk, favor) && aligned16(y)));
   Plan p = make_plan(B, H, L, d, M, chunk, favor, bwd, dw != nullptr, tc ? 2 : 1);
   Args a{};
   a.q = q; a.k = k; a.v = v; a.dy = dy; a.y = y; a.dq = dq; a.dk = dk; a.dv = dv;
   a.w = w; a.dw = dw;
+  a.state_in = c.state_in;
+  a.state_out = bwd ? nullptr : c.state_out;
+  a.g_in = bwd ? c.g_in : nullptr;
+  a.g_out = bwd ? c.g_out : nullptr;
   if (cudaGetSymbolAddress((void **)&a.status, g_device_status) != cudaSuccess) return SLIM_ERR_CUDA;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -282,6 +313,7 @@ ProfScope::~ProfScope() {
 
 }  // namespace slim
 
+using slim::Carry;
 using slim::run;
 using slim::run_decode;
 using slim::run_state;
@@ -313,6 +345,48 @@ slim_status slim_attn_bwd_f32(const float *q, const float *k, const float *v, co
                               int H, int L, int d, int M, int chunk, slim_stream_t stream) {
   return run<float>(true, q, k, v, w, dy, nullptr, dq, dk, dv, dw, B, H, L, d, M, chunk,
                     (cudaStream_t)stream);
+}
+
+slim_status slim_attn_fwd_carry(const void *q, const void *k, const void *v, const float *w, void *y,
+                                const float *state_in, float *state_out, int B, int H, int L, int d, int M,
+                                int chunk, slim_stream_t stream) {
+  Carry c;
+  c.state_in = state_in;
+  c.state_out = state_out;
+  return run<__nv_bfloat16>(false, q, k, v, w, nullptr, y, nullptr, nullptr, nullptr, nullptr, B, H, L, d, M,
+                            chunk, (cudaStream_t)stream, c);
+}
+
+slim_status slim_attn_bwd_carry(const void *q, const void *k, const void *v, const float *w, const void *dy,
+                                void *dq, void *dk, void *dv, float *dw, const float *state_in, const float *g_in,
+                                float *g_out, int B, int H, int L, int d, int M, int chunk, slim_stream_t stream) {
+  Carry c;
+  c.state_in = state_in;
+  c.g_in = g_in;
+  c.g_out = g_out;
+  return run<__nv_bfloat16>(true, q, k, v, w, dy, nullptr, dq, dk, dv, dw, B, H, L, d, M, chunk,
+                            (cudaStream_t)stream, c);
+}
+
+slim_status slim_attn_fwd_carry_f32(const float *q, const float *k, const float *v, const float *w, float *y,
+                                    const float *state_in, float *state_out, int B, int H, int L, int d, int M,
+                                    int chunk, slim_stream_t stream) {
+  Carry c;
+  c.state_in = state_in;
+  c.state_out = state_out;
+  return run<float>(false, q, k, v, w, nullptr, y, nullptr, nullptr, nullptr, nullptr, B, H, L, d, M, chunk,
+                    (cudaStream_t)stream, c);
+}
+
+slim_status slim_attn_bwd_carry_f32(const float *q, const float *k, const float *v, const float *w,
+                                    const float *dy, float *dq, float *dk, float *dv, float *dw,
+                                    const float *state_in, const float *g_in, float *g_out, int B, int H, int L,
+                                    int d, int M, int chunk, slim_stream_t stream) {
+  Carry c;
+  c.state_in = state_in;
+  c.g_in = g_in;
+  c.g_out = g_out;
+  return run<float>(true, q, k, v, w, dy, nullptr, dq, dk, dv, dw, B, H, L, d, M, chunk, (cudaStream_t)stream, c);
 }
 
 slim_status slim_attn_state(const void *k, const void *v, const float *w, float *state, int B, int H, int L,

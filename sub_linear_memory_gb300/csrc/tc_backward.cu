@@ -854,9 +854,22 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
     cudaError_t e = cudaMemsetAsync(dwpart, 0, sizeof(float) * (size_t)pl.BH * pl.P * D * pl.M, st);
     if (e != cudaSuccess) return e;
   }
+  // carried states -> features-major: R'_0 of earlier rows (the scan starts
+  // from it) and the reverse state G arriving from later rows
+  float *init = nullptr, *g_last = nullptr;
+  if (a.state_in) {
+    init = a.ws + pl.carry_off;
+    cudaError_t e = emajor_to_fm(pl, a.state_in, init, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.g_in) {
+    g_last = a.ws + pl.carry_off + (size_t)pl.BH * pl.M * (D + 1);
+    cudaError_t e = emajor_to_fm(pl, a.g_in, g_last, st);
+    if (e != cudaSuccess) return e;
+  }
   // R' totals of every segment, scanned; with two CTAs per segment the
   // outputs start at zero for the per-CTA reduce-adds
-  cudaError_t e = tc_segment_states(pl, a, pl.P, CS == 2, st);
+  cudaError_t e = tc_segment_states(pl, a, pl.P, CS == 2, init, st);
   if (e != cudaSuccess) return e;
   Params p{};
   p.L = pl.L; p.M = pl.M; p.nt = pl.tc_tiles; p.P = pl.P; p.tps = pl.cps; p.favor = FAVOR;
@@ -897,20 +910,30 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
     e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mdy, mdq, mdk, mdv, p);
     if (e != cudaSuccess) return e;
   }
-  if (pl.P > 1) {
-    {
+  if (pl.P > 1 || g_last) {
+    if (pl.P > 1) {
       ProfScope ps("scan_states", st);
-      // G_end(s) = sum over s' > s: reverse inclusive scan over segments 1..P-1
-      e = scan_states_f32_rev(pl, a.ws + pl.gstates_off + (size_t)pl.M * (D + 1), pl.P - 1, st);
+      // G_end(s) = G arriving from later rows + sum over s' > s: reverse
+      // inclusive scan over segments 1..P-1
+      e = scan_states_f32_rev(pl, a.ws + pl.gstates_off + (size_t)pl.M * (D + 1), pl.P - 1, g_last, st);
       if (e != cudaSuccess) return e;
     }
-    e = tc_correction(pl, a, st);
+    e = tc_correction(pl, a, g_last, st);
     if (e != cudaSuccess) return e;
     // dW's share of the later segments' reverse state
-    if (want_dw) e = tc_dw_correction(pl, a, st);
+    if (want_dw) e = tc_dw_correction(pl, a, g_last, st);
     if (e != cudaSuccess) return e;
   }
   if (want_dw) e = reduce_dw_t(pl, dwpart, a.dw, st);
+  if (e != cudaSuccess) return e;
+  // gradient w.r.t. the carried incoming state: the reverse state before the
+  // first row, segment 0's own total plus G_end(0)
+  if (a.g_out) {
+    if (pl.P > 1)
+      e = fm_to_emajor(pl, a.ws + pl.gstates_off, pl.P, 0, a.ws + pl.gstates_off, pl.P, 1, a.g_out, st);
+    else
+      e = fm_to_emajor(pl, a.ws + pl.gstates_off, pl.P, 0, g_last, 1, 0, a.g_out, st);
+  }
   return e;
 }
 

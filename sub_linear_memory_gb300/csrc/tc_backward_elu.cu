@@ -754,7 +754,7 @@ cudaError_t tc_backward_elu128(const Plan &pl, const Args &a, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(a.dq, 0, io_bytes, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(a.dk, 0, io_bytes, st);
   if (e != cudaSuccess) return e;
-  e = tc_segment_states(pl, a, pl.P, false, st);
+  e = tc_segment_states(pl, a, pl.P, false, nullptr, st);
   if (e != cudaSuccess) return e;
   {
     Params p{};
@@ -777,7 +777,7 @@ cudaError_t tc_backward_elu128(const Plan &pl, const Args &a, cudaStream_t st) {
   {
     ProfScope ps("scan_states", st);
     // G_end(s) = sum over s' > s: reverse inclusive scan over segments 1..P-1
-    e = scan_states_f32_rev(pl, a.ws + pl.gstates_off + (size_t)D * (D + 1), pl.P - 1, st);
+    e = scan_states_f32_rev(pl, a.ws + pl.gstates_off + (size_t)D * (D + 1), pl.P - 1, nullptr, st);
     if (e != cudaSuccess) return e;
   }
   {

@@ -45,7 +45,8 @@ constexpr uint32_t kTileBytes = kTile * D * 2;
 
 struct Params {
   int L, P, tps, BH;
-  long long per_head;  // units per head: tiles of segments 0 .. P-2
+  long long per_head;  // units per head: tiles of segments 0 .. P-2, or of every
+                       // segment when a reverse state arrives from later rows
   __nv_bfloat16 *dk, *dv;
   const __nv_bfloat16 *wimg;  // W^T image [M][64] (FAVOR+)
   const unsigned char *grec;  // per (head, segment): G_end image [M][64] bf16, then G_S fp32 [M]
@@ -116,7 +117,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(bar + B_COUNT) + 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // this CTA's units [u0, u1): unit u = (head, tile) over the first P-1 segments
+  // this CTA's units [u0, u1): unit u = (head, tile) over the first P-1
+  // segments (every segment, the last one possibly short, when a reverse
+  // state arrives from later rows)
   const long long units = p.per_head * p.BH;
   const long long u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
   const int nun = (int)(u1 - u0);
@@ -126,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   struct Cursor {
     int bh, t, seg, pos;
   };
-  const int per_head = (int)p.per_head;  // a multiple of tps
+  const int per_head = (int)p.per_head;
   Cursor first;
   first.bh = (int)(u0 / p.per_head);
   first.t = (int)(u0 - (long long)first.bh * p.per_head);
@@ -141,11 +144,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (c.t == per_head) {
       c.t = 0;
       c.seg = 0;
+      c.pos = 0;
       ++c.bh;
     }
   };
   auto new_key = [&](int i, const Cursor &c) { return i == 0 || c.pos == 0; };
-  auto last_of_key = [&](int i, const Cursor &c) { return i == nun - 1 || c.pos == p.tps - 1; };
+  auto last_of_key = [&](int i, const Cursor &c) {
+    return i == nun - 1 || c.pos == p.tps - 1 || c.t == per_head - 1;
+  };
   const uint32_t grec_bytes = (uint32_t)M * 132u;
 
   if (tid == 0) {
@@ -474,17 +480,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // G_end(s) = gstates[s + 1] (after the reverse scan) -> per (head, segment)
 // record: bf16 [M][64] swizzled image of columns 0..63, then fp32 column 64.
-__global__ void prep_g_kernel(const float *__restrict__ gstates, unsigned char *__restrict__ grec, int M, int P,
-                              int BH) {
+// nrec records per head: P - 1, or P when a reverse state g_last
+// (features-major [BH][M][D + 1]) arrives from later rows: it is the last
+// segment's G_end.
+__global__ void prep_g_kernel(const float *__restrict__ gstates, const float *__restrict__ g_last,
+                              unsigned char *__restrict__ grec, int M, int P, int nrec, int BH) {
   // x: the (feature, column) pairs of one record; y: its (head, segment),
   // so every division is by a constant or once per thread
   const int DP = D + 1;
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= M * DP) return;
   const int f = r / DP, e = r - f * DP;
-  for (int hs = blockIdx.y; hs < BH * (P - 1); hs += gridDim.y) {
-    const int bh = hs / (P - 1), s = hs - bh * (P - 1);
-    const float g = gstates[((size_t)bh * P + s + 1) * (size_t)M * DP + r];
+  for (int hs = blockIdx.y; hs < BH * nrec; hs += gridDim.y) {
+    const int bh = hs / nrec, s = hs - bh * nrec;
+    const float g = s + 1 < P ? gstates[((size_t)bh * P + s + 1) * (size_t)M * DP + r]
+                              : g_last[(size_t)bh * M * DP + r];
     unsigned char *rec = grec + ((size_t)bh * P + s) * (size_t)M * 132u;
     if (e < D)
       *reinterpret_cast<__nv_bfloat16 *>(rec + sw128_offset(f, e, M)) = __float2bfloat16_rn(g);
@@ -498,7 +508,8 @@ __global__ void prep_g_kernel(const float *__restrict__ gstates, unsigned char *
 // For a row k of segment s, with G = G_end(s):
 //   dphi_k' = V G_V^T + G_S,  u' = phi_k * dphi_k',  dW += k^T u'
 // (the same u' whose u' W^T the correction kernel adds to dK).  One CTA per
-// (segment < P - 1, head) walks the segment's tiles in order, 512 threads,
+// (segment < P - 1, or every segment when a reverse state arrives from later
+// rows; head) walks the segment's tiles in order, 512 threads,
 // four per row (TMEM lane quadrant w % 4, a quarter of the features each):
 //   F = K W -> TMEM; phi_k -> shared tile; D = V G_V^T -> the same TMEM
 //   columns; u' = phi_k * (D + G_S) over phi_k in place; dW^T += u'^T K on
@@ -714,7 +725,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int M>
-cudaError_t launch_dw(const Plan &pl, const Args &a, const CUtensorMap &mk, const CUtensorMap &mv, cudaStream_t st) {
+cudaError_t launch_dw(const Plan &pl, const Args &a, const CUtensorMap &mk, const CUtensorMap &mv, int nrec,
+                      cudaStream_t st) {
   DwParams p{};
   p.L = pl.L; p.P = pl.P; p.tps = pl.cps; p.nt = pl.tc_tiles; p.BH = pl.BH; p.M = M;
   p.wimg = reinterpret_cast<const __nv_bfloat16 *>(a.ws + pl.wimg_off);
@@ -726,16 +738,16 @@ cudaError_t launch_dw(const Plan &pl, const Args &a, const CUtensorMap &mk, cons
   auto kern = tc_dw_corr_kernel<M>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(pl.P - 1, pl.BH), kThreads, smem, st>>>(mk, mv, p);
+  kern<<<dim3(nrec, pl.BH), kThreads, smem, st>>>(mk, mv, p);
   return cudaGetLastError();
 }
 
 template <bool FAVOR, int M>
 cudaError_t launch(const Plan &pl, const Args &a, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mdk,
-                   const CUtensorMap &mdv, cudaStream_t st) {
+                   const CUtensorMap &mdv, bool all_segments, cudaStream_t st) {
   Params p{};
   p.L = pl.L; p.P = pl.P; p.tps = pl.cps; p.BH = pl.BH;
-  p.per_head = (long long)(pl.P - 1) * pl.cps;
+  p.per_head = all_segments ? (long long)pl.tc_tiles : (long long)(pl.P - 1) * pl.cps;
   p.dk = static_cast<__nv_bfloat16 *>(a.dk);
   p.dv = static_cast<__nv_bfloat16 *>(a.dv);
   p.wimg = reinterpret_cast<const __nv_bfloat16 *>(a.ws + pl.wimg_off);
@@ -757,8 +769,9 @@ cudaError_t launch(const Plan &pl, const Args &a, const CUtensorMap &mk, const C
 
 }  // namespace tcc
 
-cudaError_t tc_correction(const Plan &pl, const Args &a, cudaStream_t st) {
-  if (pl.P < 2) return cudaSuccess;
+cudaError_t tc_correction(const Plan &pl, const Args &a, const float *g_last, cudaStream_t st) {
+  const int nrec = g_last ? pl.P : pl.P - 1;
+  if (nrec < 1) return cudaSuccess;
   CUtensorMap mk, mv, mdk, mdv;
   if (!make_map_bf16_3d(&mk, a.k, pl.BH, pl.L, tcc::D, tcc::kTile) ||
       !make_map_bf16_3d(&mv, a.v, pl.BH, pl.L, tcc::D, tcc::kTile) ||
@@ -768,31 +781,34 @@ cudaError_t tc_correction(const Plan &pl, const Args &a, cudaStream_t st) {
   {
     ProfScope ps("prep_g", st);
     const int rec = pl.M * (tcc::D + 1);
-    const dim3 grid((rec + 255) / 256, (unsigned)std::min(pl.BH * (pl.P - 1), 65535));
-    tcc::prep_g_kernel<<<grid, 256, 0, st>>>(a.ws + pl.gstates_off,
+    const dim3 grid((rec + 255) / 256, (unsigned)std::min(pl.BH * nrec, 65535));
+    tcc::prep_g_kernel<<<grid, 256, 0, st>>>(a.ws + pl.gstates_off, g_last,
                                                reinterpret_cast<unsigned char *>(a.ws + pl.gimg_off), pl.M, pl.P,
-                                               pl.BH);
+                                               nrec, pl.BH);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   ProfScope ps("tc_backward_fix", st);
-  if (!pl.favor) return pl.M == 64 ? tcc::launch<false, 64>(pl, a, mk, mv, mdk, mdv, st) : cudaErrorInvalidValue;
-  if (pl.M == 64) return tcc::launch<true, 64>(pl, a, mk, mv, mdk, mdv, st);
-  if (pl.M == 128) return tcc::launch<true, 128>(pl, a, mk, mv, mdk, mdv, st);
-  if (pl.M == 256) return tcc::launch<true, 256>(pl, a, mk, mv, mdk, mdv, st);
+  const bool all = g_last != nullptr;
+  if (!pl.favor)
+    return pl.M == 64 ? tcc::launch<false, 64>(pl, a, mk, mv, mdk, mdv, all, st) : cudaErrorInvalidValue;
+  if (pl.M == 64) return tcc::launch<true, 64>(pl, a, mk, mv, mdk, mdv, all, st);
+  if (pl.M == 128) return tcc::launch<true, 128>(pl, a, mk, mv, mdk, mdv, all, st);
+  if (pl.M == 256) return tcc::launch<true, 256>(pl, a, mk, mv, mdk, mdv, all, st);
   return cudaErrorInvalidValue;
 }
 
-cudaError_t tc_dw_correction(const Plan &pl, const Args &a, cudaStream_t st) {
-  if (pl.P < 2 || !pl.favor || !a.dw) return cudaSuccess;
+cudaError_t tc_dw_correction(const Plan &pl, const Args &a, const float *g_last, cudaStream_t st) {
+  const int nrec = g_last ? pl.P : pl.P - 1;
+  if (nrec < 1 || !pl.favor || !a.dw) return cudaSuccess;
   CUtensorMap mk, mv;
   if (!make_map_bf16_3d(&mk, a.k, pl.BH, pl.L, tcc::D, tcc::kTile) ||
       !make_map_bf16_3d(&mv, a.v, pl.BH, pl.L, tcc::D, tcc::kTile))
     return cudaErrorInvalidValue;
   ProfScope ps("tc_dw_fix", st);
-  if (pl.M == 64) return tcc::launch_dw<64>(pl, a, mk, mv, st);
-  if (pl.M == 128) return tcc::launch_dw<128>(pl, a, mk, mv, st);
-  if (pl.M == 256) return tcc::launch_dw<256>(pl, a, mk, mv, st);
+  if (pl.M == 64) return tcc::launch_dw<64>(pl, a, mk, mv, nrec, st);
+  if (pl.M == 128) return tcc::launch_dw<128>(pl, a, mk, mv, nrec, st);
+  if (pl.M == 256) return tcc::launch_dw<256>(pl, a, mk, mv, nrec, st);
   return cudaErrorInvalidValue;
 }
 

@@ -64,6 +64,7 @@ struct Params {
   const __nv_bfloat16 *wimg;  // W^T shared-memory image (FAVOR+)
   float *states;     // fp32 [BH][P][M][D + 1]: high parts of the segment states
   float *states_lo;  // same layout: low parts
+  const float *state_in;  // carried state of earlier rows, fp32 [BH][M][D + 1], or NULL
   int *status;
 };
 
@@ -195,12 +196,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // W^T image and the incoming state (fp32 [M][D + 1], staged in the load
     // slots and the phi_k buffer behind them) by bulk copy
     const uint32_t wbytes = FAVOR ? (uint32_t)M * 128u : 0u;
-    const uint32_t sbytes = seg > 0 ? (uint32_t)(M * DP * 4) : 0u;
+    // segment 0 starts from the carried state of earlier rows, if any
+    const uint32_t sbytes = (seg > 0 || p.state_in) ? (uint32_t)(M * DP * 4) : 0u;
     if (wbytes + sbytes > 0) {
       mbar_arrive_expect_tx(bar + F_SETUP, wbytes + sbytes);
       if (wbytes) bulk_load(smem + lay.w, p.wimg, wbytes, bar + F_SETUP);
       if (sbytes)
-        bulk_load(smem + lay.slots, p.states + ((size_t)bh * p.P + seg - 1) * (size_t)M * DP, sbytes, bar + F_SETUP);
+        bulk_load(smem + lay.slots,
+                  seg > 0 ? p.states + ((size_t)bh * p.P + seg - 1) * (size_t)M * DP
+                          : p.state_in + (size_t)bh * M * DP,
+                  sbytes, bar + F_SETUP);
     }
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
@@ -255,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // incoming state -> TMEM master R' and its bf16 copies; num' columns d ..
   // d+15 start at zero (the tail warps, which own those copies)
   if (warp >= 12) {
-    const bool in = seg > 0;
+    const bool in = seg > 0 || p.state_in != nullptr;
     if ((FAVOR || in) && !mbar_wait(bar + F_SETUP, 0, p.status, abort_flag)) {
       // nothing usable arrived: the tiles below are skipped by the abort flag
     }
@@ -314,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the last load of every slot (the last tile's K, Q, V and, with four
       // slots, the V before it)
       for (int m = max(0, n - kS); m < n; ++m) mbar_drain(bar + F_FULL + slot_idx(m), slot_par(m));
-      if (FAVOR || seg > 0) mbar_drain(bar + F_SETUP, 0);
+      if (FAVOR || seg > 0 || p.state_in) mbar_drain(bar + F_SETUP, 0);
     }
   } else if (warp < 4) {
     // ---------------------------------------------------------------- MMA issuers
@@ -1029,8 +1034,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool FAVOR, int MODE, int M>
 cudaError_t launch_m(const Plan &pl, const Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
-                     const CUtensorMap &mv, const CUtensorMap *mz, int nseg, cudaStream_t st) {
+                     const CUtensorMap &mv, const CUtensorMap *mz, int nseg, const float *state_in,
+                     cudaStream_t st) {
   Params p{};
+  p.state_in = state_in;
   p.L = pl.L; p.M = pl.M; p.nt = pl.tc_tiles; p.P = pl.P; p.tps = pl.cps;
   p.zero_grads = mz != nullptr;
   p.y = static_cast<__nv_bfloat16 *>(a.y);
@@ -1058,13 +1065,14 @@ cudaError_t launch_m(const Plan &pl, const Args &a, const CUtensorMap &mq, const
 // features, elu+1 with M = d.
 template <int D, bool FAVOR, int MODE>
 cudaError_t launch(const Plan &pl, const Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
-                   const CUtensorMap &mv, const CUtensorMap *mz, int nseg, cudaStream_t st) {
+                   const CUtensorMap &mv, const CUtensorMap *mz, int nseg, const float *state_in, cudaStream_t st) {
   if constexpr (!FAVOR) {
-    return pl.M == D ? launch_m<D, FAVOR, MODE, D>(pl, a, mq, mk, mv, mz, nseg, st) : cudaErrorInvalidValue;
+    return pl.M == D ? launch_m<D, FAVOR, MODE, D>(pl, a, mq, mk, mv, mz, nseg, state_in, st)
+                     : cudaErrorInvalidValue;
   } else {
-    if (pl.M == 64) return launch_m<D, FAVOR, MODE, 64>(pl, a, mq, mk, mv, mz, nseg, st);
-    if (pl.M == 128) return launch_m<D, FAVOR, MODE, 128>(pl, a, mq, mk, mv, mz, nseg, st);
-    if (pl.M == 256) return launch_m<D, FAVOR, MODE, 256>(pl, a, mq, mk, mv, mz, nseg, st);
+    if (pl.M == 64) return launch_m<D, FAVOR, MODE, 64>(pl, a, mq, mk, mv, mz, nseg, state_in, st);
+    if (pl.M == 128) return launch_m<D, FAVOR, MODE, 128>(pl, a, mq, mk, mv, mz, nseg, state_in, st);
+    if (pl.M == 256) return launch_m<D, FAVOR, MODE, 256>(pl, a, mq, mk, mv, mz, nseg, state_in, st);
     return cudaErrorInvalidValue;
   }
 }
@@ -1087,25 +1095,26 @@ cudaError_t prep_w(const Plan &pl, const Args &a, cudaStream_t st) {
 }
 
 // Totals of R' over the first nseg segments, then their inclusive scan:
-// states[s] = R' at the end of segment s.  `exact`: the scan keeps the high
-// and low parts (double-float), as the backward's reversal needs; the
-// forward reads only the high parts of its incoming state, for which a
+// states[s] = R' at the end of segment s, counting from `init` (the carried
+// state of earlier rows, features-major, or NULL).  `exact`: the scan keeps
+// the high and low parts (double-float), as the backward's reversal needs;
+// the forward reads only the high parts of its incoming state, for which a
 // plain fp32 scan of the high parts (a relative error of about 2^-24 per
 // segment added) is enough and moves half the bytes.
 template <int D, bool FAVOR>
 cudaError_t segment_states(const Plan &pl, const Args &a, const CUtensorMap &mq,
                            const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap *mz, int nseg,
-                           bool exact, cudaStream_t st) {
+                           bool exact, const float *init, cudaStream_t st) {
   cudaError_t e;
   {
     ProfScope ps("tc_segment_state", st);
-    e = launch<D, FAVOR, MODE_STATE>(pl, a, mq, mk, mv, mz, nseg, st);
+    e = launch<D, FAVOR, MODE_STATE>(pl, a, mq, mk, mv, mz, nseg, nullptr, st);
     if (e != cudaSuccess) return e;
   }
-  if (nseg > 1) {
+  if (nseg > 1 || (nseg > 0 && init)) {
     ProfScope ps("scan_states", st);
-    e = exact ? scan_states_df(pl, a.ws + pl.states_off, a.ws + pl.states_lo_off, nseg, 1, st)
-              : scan_states_f32(pl, a.ws + pl.states_off, nseg, st);
+    e = exact ? scan_states_df(pl, a.ws + pl.states_off, a.ws + pl.states_lo_off, nseg, 1, init, st)
+              : scan_states_f32(pl, a.ws + pl.states_off, nseg, init, st);
   }
   return e;
 }
@@ -1117,12 +1126,31 @@ cudaError_t forward_family(const Plan &pl, const Args &a, cudaStream_t st) {
       !make_map_bf16_3d(&mv, a.v, pl.BH, pl.L, D, kTile))
     return cudaErrorInvalidValue;
   cudaError_t e;
-  if (pl.P > 1) {
-    e = segment_states<D, FAVOR>(pl, a, mq, mk, mv, nullptr, pl.P - 1, false, st);
+  // carried state of earlier rows -> features-major, read by segment 0 and
+  // the scan
+  const float *init = nullptr;
+  if (a.state_in) {
+    float *fm = a.ws + pl.carry_off;
+    e = emajor_to_fm(pl, a.state_in, fm, st);
+    if (e != cudaSuccess) return e;
+    init = fm;
+  }
+  // every segment's total when the final state is wanted (kept exactly as
+  // double-float pairs then), else all but the last
+  const int nseg = a.state_out ? pl.P : pl.P - 1;
+  if (nseg > 0) {
+    e = segment_states<D, FAVOR>(pl, a, mq, mk, mv, nullptr, nseg, a.state_out != nullptr, init, st);
     if (e != cudaSuccess) return e;
   }
-  ProfScope ps("tc_forward", st);
-  return launch<D, FAVOR, MODE_FWD>(pl, a, mq, mk, mv, nullptr, pl.P, st);
+  {
+    ProfScope ps("tc_forward", st);
+    e = launch<D, FAVOR, MODE_FWD>(pl, a, mq, mk, mv, nullptr, pl.P, init, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.state_out)
+    e = fm_to_emajor(pl, a.ws + pl.states_off, pl.P, pl.P - 1, a.ws + pl.states_lo_off, pl.P, pl.P - 1, a.state_out,
+                     st);
+  return e;
 }
 
 }  // namespace tcf
@@ -1147,7 +1175,8 @@ bool tc_forward_supported(int d, int M, int chunk, bool favor) {
   return false;
 }
 
-cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, bool zero_grads, cudaStream_t st) {
+cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, bool zero_grads, const float *init,
+                              cudaStream_t st) {
   CUtensorMap mk, mv, mz[3];
   const int d = p.d;
   cudaError_t e = tcf::prep_w(p, a, st);
@@ -1160,9 +1189,9 @@ cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, bool zero_
        !make_map_bf16_3d(&mz[2], a.dv, p.BH, p.L, d, tcf::kTile)))
     return cudaErrorInvalidValue;
   const CUtensorMap *z = zero_grads ? mz : nullptr;
-  if (d == 64 && p.favor) return tcf::segment_states<64, true>(p, a, mk, mk, mv, z, nseg, true, st);
-  if (d == 64) return tcf::segment_states<64, false>(p, a, mk, mk, mv, z, nseg, true, st);
-  if (d == 128 && !p.favor) return tcf::segment_states<128, false>(p, a, mk, mk, mv, z, nseg, true, st);
+  if (d == 64 && p.favor) return tcf::segment_states<64, true>(p, a, mk, mk, mv, z, nseg, true, init, st);
+  if (d == 64) return tcf::segment_states<64, false>(p, a, mk, mk, mv, z, nseg, true, init, st);
+  if (d == 128 && !p.favor) return tcf::segment_states<128, false>(p, a, mk, mk, mv, z, nseg, true, init, st);
   return cudaErrorInvalidValue;
 }
 
