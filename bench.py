@@ -342,6 +342,60 @@ def workload_timings(binding, inputs, peaks, names, steps=20, warmup=3):
     return out
 
 
+def streamed_timings(binding, inputs, exps=(20, 22), window=1 << 18, steps=2):
+    """fwd + bwd of the 1M workload's head shape with Q, K, V, dY (and Y, dQ,
+    dK, dV) kept in pinned host memory and run window by window (stream.py):
+    CUDA-event time per step on the current stream (the host<->device copies
+    are part of the work), the bytes copied, and the peak device memory held
+    against L."""
+    from sub_linear_memory_gb300 import stream
+
+    base = inputs.WORKLOADS["l1m"]
+    out = {"workload": "l1m head shape (B=1, H=8, d=64, M=64, chunk 256), inputs and outputs in pinned host memory",
+           "window": window, "L": [], "ms_per_step": [], "tokens_per_s": [], "peak_device_bytes": [],
+           "h2d_bytes_per_step": [], "d2h_bytes_per_step": []}
+    for e in exps:
+        wl = base.with_(L=1 << e)
+        dev_inputs = inputs.make_inputs(wl, device="cuda")
+        q, k, v, dy = (t.cpu().pin_memory() for t in dev_inputs[:4])
+        w = dev_inputs[4]
+        del dev_inputs
+        y, dq, dk, dv = (torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(4))
+        nwin = (wl.L + window - 1) // window
+        ckpt = torch.empty((nwin, wl.B, wl.H, wl.d + 1, wl.M), dtype=torch.float32).pin_memory()
+        binding.release_workspace()
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        torch.cuda.reset_peak_memory_stats()
+        before = torch.cuda.memory_allocated()
+
+        def step():
+            _, ck = stream.streamed_forward(q, k, v, w, wl.chunk, window, y=y, ckpt=ckpt)
+            stream.streamed_backward(q, k, v, dy, w, wl.chunk, ck, out=(dq, dk, dv))
+
+        step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        binding.sync_status()
+        ms = e0.elapsed_time(e1) / steps
+        nbytes = q.numel() * q.element_size()
+        out["L"].append(wl.L)
+        out["ms_per_step"].append(ms)
+        out["tokens_per_s"].append(wl.B * wl.L / (ms / 1e3))
+        out["peak_device_bytes"].append(int(torch.cuda.max_memory_allocated() - before))
+        out["h2d_bytes_per_step"].append(7 * nbytes)  # q, k, v forward; q, k, v, dy backward
+        out["d2h_bytes_per_step"].append(4 * nbytes)  # y; dq, dk, dv
+        del q, k, v, dy, w, y, dq, dk, dv, ckpt
+        binding.release_workspace()
+        torch.cuda.empty_cache()
+    return out
+
+
 def tokens_per_s_from_sample(wl, secs, heads, rows, cores):
     rounds = math.ceil(wl.B * wl.H / heads)
     full_secs = secs * rounds * (wl.L / rows)
@@ -607,6 +661,9 @@ def run_native(args, wl):
     if args.memory and rank == 0:
         del hq, hk, hv, hdy, hy, hdq, hdk, hdv, ins, outs
         line["memory"] = memory_sweep(binding, inputs)
+    if rank == 0 and world == 1 and args.stream:
+        # sequences kept in host memory, window by window: device memory vs L
+        line["stream"] = streamed_timings(binding, inputs)
     if rank == 0 and world == 1 and args.workloads:
         # the other configs, each timed outside the main region
         others = [n for n in ("l4k", "l1m", "elu16k", "l32k") if n != wl.name]
@@ -696,6 +753,8 @@ def main(argv=None):
     ap.add_argument("--no-memory", dest="memory", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false",
                     help="skip the oracle pass (CPU baseline and parity check)")
+    ap.add_argument("--no-stream", dest="stream", action="store_false",
+                    help="skip the host-resident (streamed window) timings")
     ap.add_argument("--no-workloads", dest="workloads", action="store_false",
                     help="skip the timings of the other workloads")
     ap.add_argument("--cpu-row-frac", type=float, default=1.0,

@@ -15,6 +15,8 @@ SLiM", section 2.1:
     randomized feature map approximates;
   * ``prefill_state`` / ``decode_step``: the same recurrence in its serving
     form, one new row at a time against a carried state (C);
+  * W may be one [d, M] matrix shared by every head or one per head
+    ([H, d, M], dW then per head too);
   * the forward and backward also take the boundary state of rows that came
     before (``state0``) and the gradient arriving from rows that come after
     (``g0``), and return the state after the last row and the gradient with
@@ -28,6 +30,7 @@ import threading
 
 import numpy as np
 
+from . import orf  # noqa: F401  (re-exported)
 from . import quadratic  # noqa: F401  (re-exported)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -124,7 +127,38 @@ def _state_arg(st, b, h, d, m, what):
     return st
 
 
+def _per_head(w):
+    return w is not None and np.ndim(w) == 3
+
+
 def recurrence_forward(q, k, v, w, threads=0, state0=None, return_state=False):
+    if _per_head(w):
+        return _forward_per_head(q, k, v, w, threads, state0, return_state)
+    return _recurrence_forward(q, k, v, w, threads, state0, return_state)
+
+
+def _forward_per_head(q, k, v, w, threads, state0, return_state):
+    """W per head ([H, d, M]): head h of every batch entry uses w[h]; each head
+    is the shared-W computation with its own W."""
+    q, k, v = _as4d(q), _as4d(k), _as4d(v)
+    h_count = q.shape[1]
+    if np.shape(w)[0] != h_count:
+        raise ValueError("per-head W must be [H, d, M] with H = %d" % h_count)
+    ys, states = [], []
+    for h in range(h_count):
+        sl = lambda t: np.ascontiguousarray(t[:, h:h + 1])
+        out = _recurrence_forward(sl(q), sl(k), sl(v), w[h], threads, None if state0 is None else sl(state0),
+                                  return_state)
+        if return_state:
+            ys.append(out[0])
+            states.append(out[1])
+        else:
+            ys.append(out)
+    y = np.concatenate(ys, axis=1)
+    return (y, np.concatenate(states, axis=1)) if return_state else y
+
+
+def _recurrence_forward(q, k, v, w, threads=0, state0=None, return_state=False):
     """Y = Att^lin(Q, K, V) by the per-step recurrence; arrays [B, H, L, d]
     (or [L, d]).  w None selects elu+1, else W is [d, M].
 
@@ -150,6 +184,36 @@ def recurrence_forward(q, k, v, w, threads=0, state0=None, return_state=False):
 
 def recurrence_backward(q, k, v, w, dy, threads=0, want_dw=True, want_y=False, state0=None, g0=None,
                         want_gstate=False):
+    if _per_head(w):
+        return _backward_per_head(q, k, v, w, dy, threads, want_dw, want_y, state0, g0, want_gstate)
+    return _recurrence_backward(q, k, v, w, dy, threads, want_dw, want_y, state0, g0, want_gstate)
+
+
+def _backward_per_head(q, k, v, w, dy, threads, want_dw, want_y, state0, g0, want_gstate):
+    """W per head ([H, d, M]): dW is per head too, [H, d, M], summed over the
+    batch entries and rows of that head."""
+    q, k, v, dy = _as4d(q), _as4d(k), _as4d(v), _as4d(dy)
+    h_count = q.shape[1]
+    if np.shape(w)[0] != h_count:
+        raise ValueError("per-head W must be [H, d, M] with H = %d" % h_count)
+    parts = []
+    for h in range(h_count):
+        sl = lambda t: None if t is None else np.ascontiguousarray(t[:, h:h + 1])
+        parts.append(_recurrence_backward(sl(q), sl(k), sl(v), w[h], sl(dy), threads, want_dw, want_y,
+                                          sl(state0), sl(g0), want_gstate))
+    cat = lambda i: np.concatenate([p[i] for p in parts], axis=1)
+    out = (cat(0), cat(1), cat(2), np.stack([p[3] for p in parts]) if want_dw else None)
+    i = 4
+    if want_y:
+        out = out + (cat(i),)
+        i += 1
+    if want_gstate:
+        out = out + (cat(i),)
+    return out
+
+
+def _recurrence_backward(q, k, v, w, dy, threads=0, want_dw=True, want_y=False, state0=None, g0=None,
+                         want_gstate=False):
     """Gradients of sum(dy * Y) + sum(g0 * R'_L): returns (dq, dk, dv, dw[, y][, g_state]);
     dw is None for elu+1 or when ``want_dw`` is False.
 

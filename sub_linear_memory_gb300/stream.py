@@ -67,10 +67,11 @@ def _check_host(*ts):
             raise ValueError("streamed tensors must be contiguous pinned host [B, H, L, d] tensors")
 
 
-def streamed_forward(q, k, v, w, chunk, window, y=None, device=None):
+def streamed_forward(q, k, v, w, chunk, window, y=None, ckpt=None, device=None):
     """Y for host-resident q, k, v (pinned [B, H, L, d]); returns (y, checkpoints)
     with y pinned host.  ``window`` rows per library call (a multiple of 128
-    keeps the calls on whole 128-row tiles)."""
+    keeps the calls on whole 128-row tiles).  ``ckpt``: optional pinned fp32
+    [n_windows, B, H, d + 1, M] buffer for the boundary checkpoints."""
     _check_host(q, k, v)
     b, h, length, d = q.shape
     m = d if w is None else w.shape[1]
@@ -78,7 +79,12 @@ def streamed_forward(q, k, v, w, chunk, window, y=None, device=None):
     if y is None:
         y = torch.empty(q.shape, dtype=q.dtype).pin_memory()
     wins = _windows(length, window)
-    ckpt = torch.zeros((len(wins), b, h, d + 1, m), dtype=torch.float32).pin_memory()
+    if ckpt is None:
+        ckpt = torch.empty((len(wins), b, h, d + 1, m), dtype=torch.float32).pin_memory()
+    if ckpt.shape != (len(wins), b, h, d + 1, m) or not ckpt.is_pinned():
+        raise ValueError("ckpt must be a pinned fp32 [n_windows, B, H, d + 1, M] tensor")
+    if wins:
+        ckpt[0].zero_()  # window 0 starts from the zero state
     if not wins:
         return y, Checkpoints(ckpt, window, length)
     comp = torch.cuda.current_stream(dev)
