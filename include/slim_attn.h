@@ -83,7 +83,13 @@ typedef enum {
   SLIM_OPT_PATH = 2,
   /* Per-kernel timing: 1 = record a CUDA event pair around every kernel
    * launch, on the launch stream (read with slim_attn_profile_get), 0 = off. */
-  SLIM_OPT_PROFILE = 3
+  SLIM_OPT_PROFILE = 3,
+  /* FAVOR+ projections: 0 = one W [d][M] shared by every batch entry and
+   * head (the default); 1 = one W per head, w is fp32 [H][d][M] (head h of
+   * every batch entry uses w[h]) and dw is [H][d][M], each summed over the
+   * batch entries and rows of its head.  Applies to every entry point that
+   * takes w, and to the workspace sizes. */
+  SLIM_OPT_W_PER_HEAD = 4
 } slim_option;
 
 /* Forward, bf16 I/O: y = Att^lin(q, k, v) (section 2.1, eq. (2)-(4); slices
@@ -155,6 +161,21 @@ slim_status slim_attn_bwd_carry_f32(const float *q, const float *k, const float 
 slim_status slim_attn_copy_rows(void *dst, long long dst_rows, long long dst_row0, const void *src,
                                 long long src_rows, long long src_row0, long long rows, long long heads,
                                 long long row_bytes, slim_stream_t stream);
+
+/* Redraw of the FAVOR+ projection on the device (section 2.1: the
+ * randomized feature map of Performers, whose W is redrawn during training).
+ * Writes n independent matrices w [n][d][M] (fp32; n = H for one W per head,
+ * see SLIM_OPT_W_PER_HEAD): in each, the M columns come in blocks of d
+ * orthogonal directions (the Q factor, diag(R) > 0, of a d x d standard
+ * Gaussian matrix), each rescaled to the length of an independent N(0, I_d)
+ * vector; the last block is cut at M.  Gaussians: Philox4x32-10 (Salmon et
+ * al., SC 2011) with key (seed mod 2^32, seed div 2^32) and counter
+ * (j, block, matrix, step mod 2^32), uniforms (x + 1/2) / 2^32 paired by
+ * Box-Muller; the same (seed, step) always gives the same matrices.
+ * 1 <= d <= 128, 1 <= M <= 65536, 0 <= n <= 65535; w is a device pointer the
+ * caller owns. */
+slim_status slim_attn_draw_orf(float *w, int n, int d, int M, unsigned long long seed, unsigned long long step,
+                               slim_stream_t stream);
 
 /* Size of the fixed device scratch array behind slim_attn_fwd_noalloc. */
 #define SLIM_NOALLOC_SCRATCH_BYTES (64u << 20)

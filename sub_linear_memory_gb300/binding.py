@@ -61,6 +61,8 @@ for _f in (_lib.slim_attn_fwd_carry, _lib.slim_attn_fwd_carry_f32, _lib.slim_att
 _ll = ctypes.c_longlong
 _lib.slim_attn_copy_rows.argtypes = [_vp, _ll, _ll, _vp, _ll, _ll, _ll, _ll, _ll, _vp]
 _lib.slim_attn_copy_rows.restype = _i
+_lib.slim_attn_draw_orf.argtypes = [_vp, _i, _i, _i, ctypes.c_ulonglong, ctypes.c_ulonglong, _vp]
+_lib.slim_attn_draw_orf.restype = _i
 _lib.slim_attn_noalloc_bytes.argtypes = [_i] * 6
 _lib.slim_attn_noalloc_bytes.restype = _sz
 _lib.slim_attn_fwd_noalloc.argtypes = _lib.slim_attn_fwd.argtypes
@@ -73,6 +75,7 @@ _lib.slim_status_string.restype = ctypes.c_char_p
 OPT_SEGMENTS = 1
 OPT_PATH = 2
 OPT_PROFILE = 3
+OPT_W_PER_HEAD = 4
 EXPORTED = (
     "slim_attn_fwd", "slim_attn_bwd", "slim_attn_fwd_f32", "slim_attn_bwd_f32",
     "slim_attn_state", "slim_attn_state_f32", "slim_attn_decode", "slim_attn_decode_f32",
@@ -81,7 +84,7 @@ EXPORTED = (
     "slim_attn_profile_count", "slim_attn_profile_get", "slim_attn_profile_reset",
     "slim_attn_fwd_noalloc", "slim_attn_noalloc_bytes", "slim_attn_selftest_timeout",
     "slim_attn_fwd_carry", "slim_attn_bwd_carry", "slim_attn_fwd_carry_f32", "slim_attn_bwd_carry_f32",
-    "slim_attn_copy_rows",
+    "slim_attn_copy_rows", "slim_attn_draw_orf",
 )
 
 
@@ -182,12 +185,13 @@ def _validate(q, k, v, w, extra=()):
     if q.dtype not in (torch.bfloat16, torch.float32) or q.device.type != "cuda":
         raise ValueError("tensors must be CUDA bf16 or fp32")
     if w is not None:
-        if w.dtype != torch.float32 or w.device != q.device or w.dim() != 2 or not w.is_contiguous():
-            raise ValueError("w must be a contiguous fp32 [d, M] tensor on q's device")
-        if w.shape[0] != q.shape[3]:
-            raise ValueError("w must be [d, M]")
+        # [d, M] shared by every head, or [H, d, M] with SLIM_OPT_W_PER_HEAD set
+        if w.dtype != torch.float32 or w.device != q.device or w.dim() not in (2, 3) or not w.is_contiguous():
+            raise ValueError("w must be a contiguous fp32 [d, M] or [H, d, M] tensor on q's device")
+        if w.shape[-2] != q.shape[3] or (w.dim() == 3 and w.shape[0] != q.shape[1]):
+            raise ValueError("w must be [d, M] or [H, d, M]")
     b, h, length, d = q.shape
-    m = d if w is None else w.shape[1]
+    m = d if w is None else w.shape[-1]
     return b, h, length, d, m
 
 
@@ -239,7 +243,7 @@ def slim_attn_bwd(q, k, v, w, dy, chunk, want_dw=False, out=None, state_in=None,
     b, h, length, d, m = _validate(q, k, v, w, (dy,))
     if out is None:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-        dw = torch.empty((d, m), dtype=torch.float32, device=q.device) if (want_dw and w is not None) else None
+        dw = torch.empty(tuple(w.shape), dtype=torch.float32, device=q.device) if (want_dw and w is not None) else None
     else:
         dq, dk, dv, dw = out
     for st, what in ((state_in, "state_in"), (g_in, "g_in"), (g_out, "g_out")):
@@ -256,6 +260,19 @@ def slim_attn_bwd(q, k, v, w, dy, chunk, want_dw=False, out=None, state_in=None,
                   _ptr(state_in), _ptr(g_in), _ptr(g_out), b, h, length, d, m, chunk, _vp(stream)),
                "slim_attn_bwd_carry")
     return dq, dk, dv, dw
+
+
+def draw_orf(n, d, m, seed, step=0, out=None, device=None):
+    """n FAVOR+ projections [n, d, m] (fp32, on the device) drawn by the
+    library's counter-based redraw for (seed, step)."""
+    if out is None:
+        dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        out = torch.empty((n, d, m), dtype=torch.float32, device=dev)
+    if out.shape != (n, d, m) or out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous fp32 [n, d, M] tensor")
+    stream = torch.cuda.current_stream(out.device).cuda_stream
+    _check(_lib.slim_attn_draw_orf(_ptr(out), n, d, m, seed, step, _vp(stream)), "slim_attn_draw_orf")
+    return out
 
 
 def copy_rows(dst, dst_row0, src, src_row0, rows, stream=None):

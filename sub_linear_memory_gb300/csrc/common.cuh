@@ -31,6 +31,7 @@ struct Plan {
   int dp;       // d + 1: rows of the stacked state R' = [R ; S^T]
   int path;     // 1 = CUDA-core kernels, 2 = tensor-core kernels
   int tc_tiles; // 128-row tiles per (b, h) (tensor-core path)
+  int wh;       // FAVOR+ projections: 1 (one W shared by every head) or H (one per head)
   // workspace layout, in floats from the registered base
   size_t states_off;   // inclusive segment-end states R': CUDA-core path fp64
                        // [BH][P][dp][M]; tensor path fp32 [BH][P][M][dp]
@@ -67,5 +68,8 @@ struct Args {
 };
 
 __host__ __device__ inline size_t align_floats(size_t n) { return (n + 63) & ~size_t(63); }  // 256 B
+
+// Index of the W matrix head bh = b * H + h uses: h with one W per head, else 0.
+__host__ __device__ inline int w_head(const Plan &p, int bh) { return p.wh > 1 ? bh % p.H : 0; }
 
 }  // namespace slim

@@ -58,11 +58,12 @@ template <typename T>
 __global__ void __launch_bounds__(256) decode_kernel(const T *__restrict__ q, const T *__restrict__ k,
                                                      const T *__restrict__ v, const float *__restrict__ w,
                                                      float *__restrict__ state, T *__restrict__ y, int d, int M,
-                                                     int favor) {
+                                                     int favor, int wh) {
   __shared__ float xs[3][kMaxD];                 // the head's q, k, v row
   __shared__ float part[kMaxWarps][kMaxD + 1];   // per-warp partial sums of g(q) . state[e]
   __shared__ float nrm[2];
   const int bh = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5, nw = blockDim.x >> 5;
+  if (favor) w += (size_t)(bh % wh) * d * M;  // this head's W (wh = 1: one W for every head)
   for (int i = t; i < 3 * d; i += blockDim.x) {
     const int r = i / d, c = i - r * d;
     const T *src = r == 0 ? q : (r == 1 ? k : v);
@@ -169,13 +170,13 @@ __global__ void state_from_df_kernel(const float *__restrict__ hi, const float *
 
 template <typename T>
 cudaError_t decode_step(const void *q, const void *k, const void *v, const float *w, float *state, void *y, int BH,
-                        int d, int M, cudaStream_t st) {
+                        int d, int M, int wh, cudaStream_t st) {
   if (BH == 0) return cudaSuccess;
   const int threads = ((M + 31) / 32) * 32;
   ProfScope ps("decode", st);
   dec::decode_kernel<T><<<BH, threads, 0, st>>>(static_cast<const T *>(q), static_cast<const T *>(k),
                                                 static_cast<const T *>(v), w, state, static_cast<T *>(y), d, M,
-                                                w != nullptr ? 1 : 0);
+                                                w != nullptr ? 1 : 0, wh);
   return cudaGetLastError();
 }
 
@@ -190,8 +191,8 @@ cudaError_t tc_prefill_state(const Plan &p, const Args &a, float *state, cudaStr
 }
 
 template cudaError_t decode_step<float>(const void *, const void *, const void *, const float *, float *, void *,
-                                        int, int, int, cudaStream_t);
+                                        int, int, int, int, cudaStream_t);
 template cudaError_t decode_step<__nv_bfloat16>(const void *, const void *, const void *, const float *, float *,
-                                                void *, int, int, int, cudaStream_t);
+                                                void *, int, int, int, int, cudaStream_t);
 
 }  // namespace slim

@@ -239,6 +239,11 @@ __device__ __forceinline__ double *state_ptr(const Plan &p, const Args &a, size_
   return reinterpret_cast<double *>(a.ws + off) + ((size_t)bh * p.P + s) * p.dp * p.M;
 }
 
+// The W [d][M] head bh uses (NULL for elu+1).
+__device__ __forceinline__ const float *head_w(const Plan &p, const Args &a, int bh) {
+  return a.w ? a.w + (size_t)w_head(p, bh) * p.d * p.M : nullptr;
+}
+
 template <typename T>
 __device__ __forceinline__ const T *head_ptr(const void *base, const Plan &p, int bh, int row0) {
   return static_cast<const T *>(base) + ((size_t)bh * p.L + row0) * p.d;
@@ -256,6 +261,7 @@ __global__ void __launch_bounds__(kThreads) segment_state_kernel(Plan p, Args a)
   const int s = blockIdx.x, bh = blockIdx.y;
   double *out = state_ptr(p, a, p.states_off, bh, s);
   FwdScratch sc = fwd_scratch(p, cta_scratch(p, a));
+  const float *w = head_w(p, a, bh);
   for (int i = threadIdx.x; i < p.dp * p.M; i += kThreads) out[i] = 0.0;
   const int c0 = s * p.cps, c1 = min(c0 + p.cps, p.nchunks);
   for (int c = c0; c < c1; ++c) {
@@ -263,7 +269,7 @@ __global__ void __launch_bounds__(kThreads) segment_state_kernel(Plan p, Args a)
     const T *k = head_ptr<T>(a.k, p, bh, ch.row0), *v = head_ptr<T>(a.v, p, bh, ch.row0);
     if (p.favor) row_sqnorms(k, ch.rows, p.d, sq);
     __syncthreads();
-    feature_rows(p, k, ch.rows, a.w, sq, sc.phk);
+    feature_rows(p, k, ch.rows, w, sq, sc.phk);
     __syncthreads();
     state_add(p, out, sc.phk, v, ch.rows, 1.f);
     __syncthreads();
@@ -313,8 +319,8 @@ __global__ void __launch_bounds__(kThreads) forward_kernel(Plan p, Args a) {
       row_sqnorms(k, ch.rows, p.d, den);  // den[] doubles as |k|^2 here
     }
     __syncthreads();
-    feature_rows(p, q, ch.rows, a.w, sq, sc.phq);
-    feature_rows(p, k, ch.rows, a.w, den, sc.phk);
+    feature_rows(p, q, ch.rows, head_w(p, a, bh), sq, sc.phq);
+    feature_rows(p, k, ch.rows, head_w(p, a, bh), den, sc.phk);
     __syncthreads();
     causal_scores(p, sc.phq, sc.phk, ch.rows, sc.A);
     __syncthreads();
@@ -353,8 +359,8 @@ __global__ void __launch_bounds__(kThreads) segment_dg_kernel(Plan p, Args a) {
       row_sqnorms(k, ch.rows, p.d, den);
     }
     __syncthreads();
-    feature_rows(p, q, ch.rows, a.w, sq, sc.phq);
-    feature_rows(p, k, ch.rows, a.w, den, sc.phk);
+    feature_rows(p, q, ch.rows, head_w(p, a, bh), sq, sc.phq);
+    feature_rows(p, k, ch.rows, head_w(p, a, bh), den, sc.phk);
     __syncthreads();
     causal_scores(p, sc.phq, sc.phk, ch.rows, sc.A);
     __syncthreads();
@@ -431,8 +437,8 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(Plan p, Args a) {
       row_sqnorms(k, rows, d, sk);
     }
     __syncthreads();
-    feature_rows(p, q, rows, a.w, sq, sc.phq);
-    feature_rows(p, k, rows, a.w, sk, sc.phk);
+    feature_rows(p, q, rows, head_w(p, a, bh), sq, sc.phq);
+    feature_rows(p, k, rows, head_w(p, a, bh), sk, sc.phk);
     __syncthreads();
     state_add(p, sc.R, sc.phk, v, rows, -1.f);  // eq. (19): state before this chunk
     causal_scores(p, sc.phq, sc.phk, rows, sc.A);
@@ -477,9 +483,9 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(Plan p, Args a) {
     }
     __syncthreads();
     reverse_state_add(p, sc.G, sc.dNp, sc.phq, rows);  // eq. (20)
-    feature_backward(p, q, rows, a.w, sc.phq, sc.dphq, sq, dq, dwp);
+    feature_backward(p, q, rows, head_w(p, a, bh), sc.phq, sc.dphq, sq, dq, dwp);
     __syncthreads();
-    feature_backward(p, k, rows, a.w, sc.phk, sc.dphk, sk, dk, dwp);
+    feature_backward(p, k, rows, head_w(p, a, bh), sc.phk, sc.dphk, sk, dk, dwp);
     __syncthreads();
   }
 }
@@ -556,15 +562,19 @@ __global__ void scan_states_f32_kernel(Plan p, float *st, int nseg, int reverse,
   }
 }
 
-// dw[i] = sum over CTAs of the per-CTA partials (fixed order: deterministic).
+// dw[i] = sum over CTAs of the per-CTA partials (fixed order: deterministic);
+// with one W per head, dW of head h (blockIdx.y) sums its batch entries' CTAs.
 __global__ void reduce_dw_kernel(Plan p, const float *parts, float *dw) {
   const size_t n = (size_t)p.d * p.M;
-  const int nparts = p.BH * p.P;
+  const int h = blockIdx.y, nb = p.wh > 1 ? p.B : p.BH, stride = p.wh > 1 ? p.H : 1;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x) {
     float s = 0.f;
-    for (int c = 0; c < nparts; ++c) s += parts[(size_t)c * n + i];
-    dw[i] = s;
+    for (int b = 0; b < nb; ++b) {
+      const int bh = b * stride + h;
+      for (int c = 0; c < p.P; ++c) s += parts[((size_t)bh * p.P + c) * n + i];
+    }
+    dw[(size_t)h * n + i] = s;
   }
 }
 
@@ -573,23 +583,32 @@ __global__ void reduce_dw_kernel(Plan p, const float *parts, float *dw) {
 __global__ void reduce_dw_t_kernel(Plan p, const float *parts, float *dw) {
   const int d = p.d, M = p.M, nq = d / 4;
   const size_t per = (size_t)M * d;
-  const int nparts = p.BH * p.P;
+  // one W per head: head h = blockIdx.y sums the P partials of each of its
+  // batch entries, which are P * H apart
+  const int h = blockIdx.y;
+  const int nparts = p.wh > 1 ? p.B * p.P : p.BH * p.P;
+  dw += (size_t)h * d * M;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < M * nq; i += gridDim.x * blockDim.x) {
     const int f = i / nq, e0 = 4 * (i - f * nq);
     const float *src = parts + (size_t)f * d + e0;
+    auto part = [&](int c) -> const float * {
+      if (p.wh <= 1) return src + (size_t)c * per;
+      const int b = c / p.P, s = c - b * p.P;
+      return src + ((size_t)(b * p.H + h) * p.P + s) * per;
+    };
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     int c = 0;
     for (; c + 8 <= nparts; c += 8) {
       float4 x[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) x[j] = *reinterpret_cast<const float4 *>(src + (size_t)(c + j) * per);
+      for (int j = 0; j < 8; ++j) x[j] = *reinterpret_cast<const float4 *>(part(c + j));
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         s.x += x[j].x; s.y += x[j].y; s.z += x[j].z; s.w += x[j].w;
       }
     }
     for (; c < nparts; ++c) {
-      const float4 x = *reinterpret_cast<const float4 *>(src + (size_t)c * per);
+      const float4 x = *reinterpret_cast<const float4 *>(part(c));
       s.x += x.x; s.y += x.y; s.z += x.z; s.w += x.w;
     }
     dw[(size_t)(e0 + 0) * M + f] = s.x;
@@ -683,7 +702,7 @@ cudaError_t generic_backward(const Plan &p, const Args &a, cudaStream_t st) {
   if (a.dw) {
     const int n = p.d * p.M;
     ProfScope ps("gen_reduce_dw", st);
-    gen::reduce_dw_kernel<<<(n + 255) / 256, 256, 0, st>>>(p, a.ws + p.dwpart_off, a.dw);
+    gen::reduce_dw_kernel<<<dim3((n + 255) / 256, p.wh), 256, 0, st>>>(p, a.ws + p.dwpart_off, a.dw);
   }
   if (a.g_out) {
     const size_t n = (size_t)p.BH * p.dp * p.M;
@@ -707,7 +726,7 @@ cudaError_t scan_states_df(const Plan &p, float *hi, float *lo, int nseg, int lo
 cudaError_t reduce_dw_t(const Plan &p, const float *parts, float *dw, cudaStream_t st) {
   const int n = p.M * (p.d / 4);
   ProfScope ps("reduce_dw", st);
-  gen::reduce_dw_t_kernel<<<(n + 127) / 128, 128, 0, st>>>(p, parts, dw);
+  gen::reduce_dw_t_kernel<<<dim3((n + 127) / 128, p.wh), 128, 0, st>>>(p, parts, dw);
   return cudaGetLastError();
 }
 

@@ -73,9 +73,10 @@ cudaError_t tc_dw_correction(const Plan &p, const Args &a, const float *g_last, 
 // e-major [BH][d + 1][M], and one decode step for every head.
 template <typename T> cudaError_t generic_prefill_state(const Plan &p, const Args &a, float *state, cudaStream_t st);
 cudaError_t tc_prefill_state(const Plan &p, const Args &a, float *state, cudaStream_t st);
+// wh: W matrices (1 shared, or one per head: head bh uses W[bh % wh]).
 template <typename T>
 cudaError_t decode_step(const void *q, const void *k, const void *v, const float *w, float *state, void *y, int BH,
-                        int d, int M, cudaStream_t st);
+                        int d, int M, int wh, cudaStream_t st);
 
 // Tensor-core SLiM backward (tc_backward.cu): bf16 I/O, d = 64 with M <= 256 (a
 // two-CTA cluster per segment at M = 256), learnable W included.

@@ -24,6 +24,7 @@ void *g_ws = nullptr;
 size_t g_ws_bytes = 0;
 int g_opt_segments = 0;
 int g_opt_path = 0;
+int g_opt_w_per_head = 0;
 
 // ---- per-kernel profiling ----
 std::mutex g_prof_mu;
@@ -141,6 +142,7 @@ Plan make_plan(int B, int H, int L, int d, int M, int chunk, bool favor, bool bw
   p.nchunks = (L + chunk - 1) / chunk;
   p.tc_tiles = (L + 127) / 128;
   p.favor = favor ? 1 : 0;
+  p.wh = (favor && g_opt_w_per_head) ? H : 1;
   p.dp = d + 1;
   p.path = path;
   // the backward of 256 random features, and of elu+1 at d = 128, runs each
@@ -160,7 +162,7 @@ Plan make_plan(int B, int H, int L, int d, int M, int chunk, bool favor, bool bw
   p.scratch_stride = path == 2 ? 0 : align_floats(generic_scratch_floats(p, bwd));
   p.scratch_off = off; off += p.scratch_stride * p.BH * p.P;
   p.dwpart_off = off; if (bwd && want_dw) off += align_floats((size_t)p.BH * p.P * d * M);
-  p.wimg_off = off; if (path == 2 && favor) off += align_floats((size_t)M * 32);
+  p.wimg_off = off; if (path == 2 && favor) off += align_floats((size_t)std::max(p.wh, 1) * M * 32);
   // bf16 G_end images [M][d] and fp32 G_S [M] per (head, segment)
   p.gimg_off = off; if (path == 2 && bwd) off += align_floats((size_t)p.BH * p.P * M * (d / 2 + 1));
   // carried states turned features-major: R'_0 and G (tensor path)
@@ -189,7 +191,9 @@ slim_status run(bool bwd, const void *q, const void *k, const void *v, const flo
   if (st != SLIM_OK) return st;
   if (!favor && dw) return SLIM_ERR_INVALID_ARG;
   if ((long long)B * H * L == 0) {
-    if (dw && cudaMemsetAsync(dw, 0, sizeof(float) * d * M, stream) != cudaSuccess) return SLIM_ERR_CUDA;
+    const size_t dw_mats = g_opt_w_per_head ? (size_t)std::max(H, 0) : 1;
+    if (dw && dw_mats && cudaMemsetAsync(dw, 0, sizeof(float) * dw_mats * d * M, stream) != cudaSuccess)
+      return SLIM_ERR_CUDA;
     // no rows: the final state is the incoming one, and the gradient w.r.t. the
     // incoming state is the one arriving at the final state
     const size_t sbytes = sizeof(float) * (size_t)B * H * (d + 1) * M;
@@ -270,7 +274,7 @@ slim_status run_decode(const void *q, const void *k, const void *v, const float 
   if (st != SLIM_OK) return st;
   if ((long long)B * H == 0) return SLIM_OK;
   if (!q || !k || !v || !state || !y) return SLIM_ERR_INVALID_ARG;
-  const cudaError_t err = decode_step<T>(q, k, v, w, state, y, B * H, d, M, stream);
+  const cudaError_t err = decode_step<T>(q, k, v, w, state, y, B * H, d, M, favor && g_opt_w_per_head ? H : 1, stream);
   return err == cudaSuccess ? SLIM_OK : SLIM_ERR_CUDA;
 }
 
@@ -444,6 +448,10 @@ slim_status slim_attn_set_option(int option, int value) {
     case SLIM_OPT_PATH:
       if (value < 0 || value > 2) return SLIM_ERR_INVALID_ARG;
       slim::g_opt_path = value;
+      return SLIM_OK;
+    case SLIM_OPT_W_PER_HEAD:
+      if (value < 0 || value > 1) return SLIM_ERR_INVALID_ARG;
+      slim::g_opt_w_per_head = value;
       return SLIM_OK;
     default:
       return SLIM_ERR_INVALID_ARG;

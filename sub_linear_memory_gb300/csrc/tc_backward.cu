@@ -46,6 +46,7 @@ static_assert(16 * kParts == D, "the R update gives each part 16 value columns")
 
 struct Params {
   int L, M, nt, P, tps, favor, BH;
+  int H, wstride;  // heads; bf16 elements between per-head W^T images (0: one shared W)
   __nv_bfloat16 *dq, *dk, *dv;
   const float *w;
   const __nv_bfloat16 *wimg;  // W^T as the bf16 [M][64] swizzled shared-memory image
@@ -194,7 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t soff = ((size_t)bh * p.P + seg) * (size_t)M * DP + (size_t)fbase * DP;
     mbar_arrive_expect_tx(setup_bar, (FAVOR ? (uint32_t)MC * 128u : 0u) + 2 * st_bytes);
     if (FAVOR)
-      bulk_load(smem + lay.w, reinterpret_cast<const unsigned char *>(p.wimg) + (size_t)fbase * 128, MC * 128u,
+      bulk_load(smem + lay.w,
+                reinterpret_cast<const unsigned char *>(p.wimg + (size_t)(bh % p.H) * p.wstride) + (size_t)fbase * 128,
+                MC * 128u,
                 setup_bar);
     bulk_load(smem + lay.phq, p.states + soff, st_bytes, setup_bar);
     bulk_load(smem + lo_stage, p.states_lo + soff, st_bytes, setup_bar);
@@ -874,6 +877,7 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
   Params p{};
   p.L = pl.L; p.M = pl.M; p.nt = pl.tc_tiles; p.P = pl.P; p.tps = pl.cps; p.favor = FAVOR;
   p.BH = pl.BH;
+  p.H = pl.H; p.wstride = pl.wh > 1 ? pl.M * 64 : 0;
   p.dq = static_cast<__nv_bfloat16 *>(a.dq);
   p.dk = static_cast<__nv_bfloat16 *>(a.dk);
   p.dv = static_cast<__nv_bfloat16 *>(a.dv);

@@ -45,6 +45,7 @@ constexpr uint32_t kTileBytes = kTile * D * 2;
 
 struct Params {
   int L, P, tps, BH;
+  int H, wstride;  // heads; bf16 elements between per-head W^T images (0: one shared W)
   long long per_head;  // units per head: tiles of segments 0 .. P-2, or of every
                        // segment when a reverse state arrives from later rows
   __nv_bfloat16 *dk, *dv;
@@ -120,7 +121,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // this CTA's units [u0, u1): unit u = (head, tile) over the first P-1
   // segments (every segment, the last one possibly short, when a reverse
   // state arrives from later rows)
-  const long long units = p.per_head * p.BH;
+  // with one W per head the grid is [CTAs per head][head]: a CTA's units stay
+  // in head blockIdx.y, whose W it loads once
+  const long long units = p.per_head * (gridDim.y > 1 ? 1 : p.BH);
   const long long u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
   const int nun = (int)(u1 - u0);
   // every role walks the same units with counters (no divisions per unit):
@@ -131,8 +134,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   const int per_head = (int)p.per_head;
   Cursor first;
-  first.bh = (int)(u0 / p.per_head);
-  first.t = (int)(u0 - (long long)first.bh * p.per_head);
+  const long long h0 = u0 / p.per_head;  // heads before this CTA's first unit (0 on a per-head grid)
+  first.bh = (int)blockIdx.y + (int)h0;
+  first.t = (int)(u0 - h0 * p.per_head);
   first.seg = first.t / p.tps;
   first.pos = first.t - first.seg * p.tps;
   auto advance = [&](Cursor &c) {
@@ -183,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmV);
     if (FAVOR) {
       mbar_arrive_expect_tx(bar + B_WFULL, (uint32_t)M * 128u);
-      bulk_load(smem + lay.w, p.wimg, (uint32_t)M * 128u, bar + B_WFULL);
+      bulk_load(smem + lay.w, p.wimg + (size_t)(blockIdx.y % p.H) * p.wstride, (uint32_t)M * 128u, bar + B_WFULL);
     }
   }
   if (warp == 0) tmem_alloc(tslot, 512);
@@ -518,6 +522,7 @@ __global__ void prep_g_kernel(const float *__restrict__ gstates, const float *__
 // segment's dW^T is added to its partial [M][D] at the end.
 struct DwParams {
   int L, P, tps, nt, BH, M;
+  int H, wstride;  // heads; bf16 elements between per-head W^T images (0: one shared W)
   const __nv_bfloat16 *wimg;  // W^T image [M][64]
   const unsigned char *grec;  // per (head, segment): G_end image [M][64] bf16, then G_S fp32 [M]
   float *dwpart;              // fp32 [BH][P][M][D]: dW^T partials
@@ -578,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
     mbar_arrive_expect_tx(setup_bar, (uint32_t)M * 256u + (uint32_t)M * 4u);
-    bulk_load(smem + lay.w, p.wimg, (uint32_t)M * 128u, setup_bar);
+    bulk_load(smem + lay.w, p.wimg + (size_t)(bh % p.H) * p.wstride, (uint32_t)M * 128u, setup_bar);
     bulk_load(smem + lay.g, p.grec + ((size_t)bh * p.P + seg) * (size_t)M * 132u, (uint32_t)M * 132u, setup_bar);
     if (t0 < t1) {
       mbar_arrive_expect_tx(ld_bar, 2 * kTileBytes);
@@ -729,6 +734,7 @@ cudaError_t launch_dw(const Plan &pl, const Args &a, const CUtensorMap &mk, cons
                       cudaStream_t st) {
   DwParams p{};
   p.L = pl.L; p.P = pl.P; p.tps = pl.cps; p.nt = pl.tc_tiles; p.BH = pl.BH; p.M = M;
+  p.H = pl.H; p.wstride = pl.wh > 1 ? M * 64 : 0;
   p.wimg = reinterpret_cast<const __nv_bfloat16 *>(a.ws + pl.wimg_off);
   p.grec = reinterpret_cast<const unsigned char *>(a.ws + pl.gimg_off);
   p.dwpart = a.ws + pl.dwpart_off;
@@ -747,6 +753,7 @@ cudaError_t launch(const Plan &pl, const Args &a, const CUtensorMap &mk, const C
                    const CUtensorMap &mdv, bool all_segments, cudaStream_t st) {
   Params p{};
   p.L = pl.L; p.P = pl.P; p.tps = pl.cps; p.BH = pl.BH;
+  p.H = pl.H; p.wstride = pl.wh > 1 ? M * 64 : 0;
   p.per_head = all_segments ? (long long)pl.tc_tiles : (long long)(pl.P - 1) * pl.cps;
   p.dk = static_cast<__nv_bfloat16 *>(a.dk);
   p.dv = static_cast<__nv_bfloat16 *>(a.dv);
@@ -761,9 +768,15 @@ cudaError_t launch(const Plan &pl, const Args &a, const CUtensorMap &mk, const C
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long units = p.per_head * pl.BH;
-  const int grid = (int)std::min<long long>(sms, units);
-  kern<<<grid, kThreads, smem, st>>>(mk, mv, mdk, mdv, p);
+  if (p.wstride == 0) {
+    const long long units = p.per_head * pl.BH;
+    const int grid = (int)std::min<long long>(sms, units);
+    kern<<<grid, kThreads, smem, st>>>(mk, mv, mdk, mdv, p);
+  } else {
+    // one W per head: each CTA stays in one head (every CTA gets >= 1 unit)
+    const long long per_head_ctas = std::max<long long>(1, std::min<long long>(p.per_head, sms / std::max(pl.BH, 1)));
+    kern<<<dim3((unsigned)per_head_ctas, pl.BH), kThreads, smem, st>>>(mk, mv, mdk, mdv, p);
+  }
   return cudaGetLastError();
 }
 

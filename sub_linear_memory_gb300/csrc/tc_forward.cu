@@ -59,6 +59,7 @@ enum { MODE_STATE = 0, MODE_FWD = 1 };
 
 struct Params {
   int L, M, nt, P, tps;
+  int H, wstride;  // heads; bf16 elements between per-head W^T images (0: one shared W)
   int zero_grads;  // state pass of a two-CTA backward: zero dQ, dK, dV tile by tile
   __nv_bfloat16 *y;
   const __nv_bfloat16 *wimg;  // W^T shared-memory image (FAVOR+)
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbytes = (seg > 0 || p.state_in) ? (uint32_t)(M * DP * 4) : 0u;
     if (wbytes + sbytes > 0) {
       mbar_arrive_expect_tx(bar + F_SETUP, wbytes + sbytes);
-      if (wbytes) bulk_load(smem + lay.w, p.wimg, wbytes, bar + F_SETUP);
+      if (wbytes) bulk_load(smem + lay.w, p.wimg + (size_t)(bh % p.H) * p.wstride, wbytes, bar + F_SETUP);
       if (sbytes)
         bulk_load(smem + lay.slots,
                   seg > 0 ? p.states + ((size_t)bh * p.P + seg - 1) * (size_t)M * DP
@@ -745,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     if (FAVOR) {
       mbar_arrive_expect_tx(bar + S_SETUP, (uint32_t)M * 128u);
-      bulk_load(smem + lay.w, p.wimg, (uint32_t)M * 128u, bar + S_SETUP);
+      bulk_load(smem + lay.w, p.wimg + (size_t)(bh % p.H) * p.wstride, (uint32_t)M * 128u, bar + S_SETUP);
     }
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
@@ -1039,6 +1040,7 @@ cudaError_t launch_m(const Plan &pl, const Args &a, const CUtensorMap &mq, const
   Params p{};
   p.state_in = state_in;
   p.L = pl.L; p.M = pl.M; p.nt = pl.tc_tiles; p.P = pl.P; p.tps = pl.cps;
+  p.H = pl.H; p.wstride = pl.wh > 1 ? pl.M * 64 : 0;
   p.zero_grads = mz != nullptr;
   p.y = static_cast<__nv_bfloat16 *>(a.y);
   p.wimg = reinterpret_cast<const __nv_bfloat16 *>(a.ws + pl.wimg_off);
@@ -1077,11 +1079,14 @@ cudaError_t launch(const Plan &pl, const Args &a, const CUtensorMap &mq, const C
   }
 }
 
-// W (fp32 [64][M]) -> the bf16 [M][64] swizzled image of W^T that the
-// kernels copy into shared memory as the K-major B operand of F = X W.
+// W (fp32 [64][M], one per blockIdx.y) -> the bf16 [M][64] swizzled image
+// of W^T that the kernels copy into shared memory as the K-major B operand of
+// F = X W.
 __global__ void prep_w_kernel(const float *__restrict__ w, __nv_bfloat16 *__restrict__ img, int M) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= M * 64) return;
+  w += (size_t)blockIdx.y * M * 64;
+  img += (size_t)blockIdx.y * M * 64;
   const int i = idx / M, m = idx - i * M;
   img[sw128_offset(m, i, M) / 2] = __float2bfloat16_rn(w[idx]);
 }
@@ -1090,7 +1095,8 @@ cudaError_t prep_w(const Plan &pl, const Args &a, cudaStream_t st) {
   if (!pl.favor) return cudaSuccess;
   ProfScope ps("prep_w", st);
   const int n = pl.M * 64;
-  prep_w_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.w, reinterpret_cast<__nv_bfloat16 *>(a.ws + pl.wimg_off), pl.M);
+  prep_w_kernel<<<dim3((n + 255) / 256, pl.wh), 256, 0, st>>>(
+      a.w, reinterpret_cast<__nv_bfloat16 *>(a.ws + pl.wimg_off), pl.M);
   return cudaGetLastError();
 }
 
