@@ -339,10 +339,55 @@ def workload_timings(binding, inputs, peaks, names, steps=20, warmup=3):
                          peaks["bf16_tflops"], peaks["hbm_gbs"], peaks["source"])}
         del q, k, v, dy, w, y, grads
         torch.cuda.empty_cache()
+    if "l32k" in inputs.WORKLOADS:
+        out["l32k_per_head_w_redraw_dw"] = per_head_redraw_timing(binding, inputs, peaks, steps, warmup)
     return out
 
 
-def streamed_timings(binding, inputs, exps=(20, 22), window=1 << 18, steps=2):
+def per_head_redraw_timing(binding, inputs, peaks, steps=20, warmup=3):
+    """The l32k shape with one FAVOR+ projection per head, redrawn on the device
+    every step (slim_attn_draw_orf), and dW per head from the backward."""
+    wl = inputs.WORKLOADS["l32k"]
+    q, k, v, dy, _ = inputs.make_inputs(wl, device="cuda")
+    y = torch.empty_like(q)
+    w = torch.empty((wl.H, wl.d, wl.M), dtype=torch.float32, device="cuda")
+    dw = torch.empty_like(w)
+    grads = (torch.empty_like(q), torch.empty_like(q), torch.empty_like(q), dw)
+    stream = torch.cuda.current_stream()
+    binding.set_option(binding.OPT_W_PER_HEAD, 1)
+    try:
+        it = [0]
+
+        def step():
+            binding.draw_orf(wl.H, wl.d, wl.M, seed=2024, step=it[0], out=w)
+            it[0] += 1
+            binding.slim_attn_fwd(q, k, v, w, wl.chunk, y=y)
+            binding.slim_attn_bwd(q, k, v, w, dy, wl.chunk, out=grads)
+
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        binding.sync_status()
+    finally:
+        binding.set_option(binding.OPT_W_PER_HEAD, 0)
+    ms = e0.elapsed_time(e1) / steps
+    work = work_per_token_head(wl, dw=True)
+    th = wl.B * wl.H * wl.L
+    roof = max((work["fwd_flops"] + work["bwd_flops"]) * th / (peaks["bf16_tflops"] * 1e12),
+               (work["fwd_bytes"] + work["bwd_bytes"]) * th / (peaks["hbm_gbs"] * 1e9))
+    return {"B": wl.B, "H": wl.H, "L": wl.L, "d": wl.d, "M": wl.M, "chunk": wl.chunk,
+            "feature": "FAVOR+, one block-orthogonal W per head redrawn on the device every step, dW per head",
+            "ms_per_step": ms, "tokens_per_s": wl.B * wl.L / (ms / 1e3), "roofline_ms": roof * 1e3,
+            "frac": roof * 1e3 / ms, "steps": steps}
+
+
+def streamed_timings(binding, inputs, exps=(20, 21, 22), window=1 << 18, steps=3, warmup=2):
     """fwd + bwd of the 1M workload's head shape with Q, K, V, dY (and Y, dQ,
     dK, dV) kept in pinned host memory and run window by window (stream.py):
     CUDA-event time per step on the current stream (the host<->device copies
@@ -373,7 +418,8 @@ def streamed_timings(binding, inputs, exps=(20, 22), window=1 << 18, steps=2):
             _, ck = stream.streamed_forward(q, k, v, w, wl.chunk, window, y=y, ckpt=ckpt)
             stream.streamed_backward(q, k, v, dy, w, wl.chunk, ck, out=(dq, dk, dv))
 
-        step()
+        for _ in range(warmup):
+            step()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
