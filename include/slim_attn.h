@@ -177,6 +177,64 @@ slim_status slim_attn_copy_rows(void *dst, long long dst_rows, long long dst_row
 slim_status slim_attn_draw_orf(float *w, int n, int d, int M, unsigned long long seed, unsigned long long step,
                                slim_stream_t stream);
 
+/* A multi-layer Performer language model (section 2.2, eq. 5-10: the GPT-2
+ * style Transformer with linear attention) and one loss + gradient
+ * evaluation by Algorithm 1 (section 3): slices of `chunk` rows, each
+ * layer's boundary state carried forward, the backward walking the slices in
+ * reverse with each layer's incoming state recovered by subtraction (eq. 19)
+ * and its reverse state carried back (eq. 20).  Device memory: one slice's
+ * activations and 3 x layers boundary states, whatever L is.
+ * Per layer r: Xb = LN1(X), [Q | K | V] = Xb W_qkv (head h: columns
+ * h d .. h d + d - 1 of each third), H = X + [Att(Q_h, K_h, V_h)]_h,
+ * X' = H + GeLU(LN2(H) W1 + b1) W2 + b2 (exact GeLU, LN eps 1e-5 with gain
+ * and bias); X^(0) = E[token] + sinusoidal position (sin on even, cos on odd
+ * coordinates, position l - 1 for row l, wavelengths 10000^(2i / d_model));
+ * logits = X^(s) W_out + b_out; loss = sum over rows l < L of the
+ * cross-entropy against token l + 1.  All fp32 (the attention runs on the
+ * CUDA-core kernels). */
+typedef struct {
+  int vocab;     /* |Sigma| */
+  int d_model;   /* heads * d, d in {16, 32, 64, 128} */
+  int heads;
+  int d_ff;
+  int layers;    /* s */
+  int favor;     /* 1: FAVOR+ attention, one fixed projection per layer shared by its heads; 0: elu+1 */
+  int features;  /* M for FAVOR+ (a multiple of 16, <= 256); ignored for elu+1 (M = d) */
+} slim_lm_config;
+
+/* Floats in the parameter vector: E [vocab][d_model]; per layer ln1_g,
+ * ln1_b [d_model], W_qkv [d_model][3 d_model], ln2_g, ln2_b [d_model],
+ * W1 [d_model][d_ff], b1 [d_ff], W2 [d_ff][d_model], b2 [d_model]; then
+ * W_out [d_model][vocab], b_out [vocab]; row-major, in that order.
+ * 0 for an invalid configuration. */
+size_t slim_lm_param_count(const slim_lm_config *cfg);
+
+/* Device workspace bytes for B sequences and slices of `chunk` rows
+ * (independent of L).  0 for an invalid configuration. */
+size_t slim_lm_workspace_bytes(const slim_lm_config *cfg, int B, int chunk);
+
+/* Loss and gradient: params (device fp32, slim_lm_param_count floats),
+ * feature_w (device fp32 [layers][d][M] FAVOR+ projections, or NULL for
+ * elu+1), tokens (device int32 [B][L], values in [0, vocab)); grads (device
+ * fp32, same layout as params) is overwritten; *loss (device fp64) receives
+ * the summed cross-entropy.  checkpoints: NULL or slim_lm_checkpoint_bytes of
+ * device or pinned host memory (see below).  workspace: 256-byte aligned device memory of
+ * slim_lm_workspace_bytes(cfg, B, chunk) bytes.  Runs on `stream`; returns
+ * SLIM_ERR_UNSUPPORTED while SLIM_OPT_W_PER_HEAD is set. */
+slim_status slim_lm_loss_grad(const slim_lm_config *cfg, const float *params, const float *feature_w,
+                              const int *tokens, int B, int L, int chunk, float *grads, double *loss,
+                              float *checkpoints, void *workspace, size_t workspace_bytes, slim_stream_t stream);
+
+/* Bytes of the optional `checkpoints` buffer of slim_lm_loss_grad: every
+ * slice's incoming boundary states (layers x B x heads x (d + 1) x M floats
+ * per slice).  Given that buffer (device or pinned host memory; host memory
+ * keeps the device footprint independent of L), the backward restores each
+ * slice's states from it exactly; given NULL, it recovers them by
+ * subtracting the slice's increment from the state after it (eq. 19) in
+ * fp32, whose cancellation grows with the spread of the features (the
+ * paper notes the discrepancy growing as C shrinks). */
+size_t slim_lm_checkpoint_bytes(const slim_lm_config *cfg, int B, int L, int chunk);
+
 /* Size of the fixed device scratch array behind slim_attn_fwd_noalloc. */
 #define SLIM_NOALLOC_SCRATCH_BYTES (64u << 20)
 

@@ -63,6 +63,21 @@ _lib.slim_attn_copy_rows.argtypes = [_vp, _ll, _ll, _vp, _ll, _ll, _ll, _ll, _ll
 _lib.slim_attn_copy_rows.restype = _i
 _lib.slim_attn_draw_orf.argtypes = [_vp, _i, _i, _i, ctypes.c_ulonglong, ctypes.c_ulonglong, _vp]
 _lib.slim_attn_draw_orf.restype = _i
+class LMConfig(ctypes.Structure):
+    """slim_lm_config: the multi-layer Performer language model's shape."""
+    _fields_ = [("vocab", _i), ("d_model", _i), ("heads", _i), ("d_ff", _i), ("layers", _i), ("favor", _i),
+                ("features", _i)]
+
+
+_lib.slim_lm_param_count.argtypes = [ctypes.POINTER(LMConfig)]
+_lib.slim_lm_param_count.restype = _sz
+_lib.slim_lm_workspace_bytes.argtypes = [ctypes.POINTER(LMConfig), _i, _i]
+_lib.slim_lm_workspace_bytes.restype = _sz
+_lib.slim_lm_loss_grad.argtypes = [ctypes.POINTER(LMConfig), _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _sz,
+                                   _vp]
+_lib.slim_lm_checkpoint_bytes.argtypes = [ctypes.POINTER(LMConfig), _i, _i, _i]
+_lib.slim_lm_checkpoint_bytes.restype = _sz
+_lib.slim_lm_loss_grad.restype = _i
 _lib.slim_attn_noalloc_bytes.argtypes = [_i] * 6
 _lib.slim_attn_noalloc_bytes.restype = _sz
 _lib.slim_attn_fwd_noalloc.argtypes = _lib.slim_attn_fwd.argtypes
@@ -84,7 +99,8 @@ EXPORTED = (
     "slim_attn_profile_count", "slim_attn_profile_get", "slim_attn_profile_reset",
     "slim_attn_fwd_noalloc", "slim_attn_noalloc_bytes", "slim_attn_selftest_timeout",
     "slim_attn_fwd_carry", "slim_attn_bwd_carry", "slim_attn_fwd_carry_f32", "slim_attn_bwd_carry_f32",
-    "slim_attn_copy_rows", "slim_attn_draw_orf",
+    "slim_attn_copy_rows", "slim_attn_draw_orf", "slim_lm_param_count", "slim_lm_workspace_bytes",
+    "slim_lm_loss_grad", "slim_lm_checkpoint_bytes",
 )
 
 
@@ -326,3 +342,58 @@ def slim_attn_decode(q, k, v, w, state, y=None):
 def raw():
     """The loaded ctypes library (for tests that call the C ABI directly)."""
     return _lib
+
+
+def lm_config(vocab, d_model, heads, d_ff, layers, favor=True, features=64):
+    return LMConfig(vocab, d_model, heads, d_ff, layers, 1 if favor else 0, features)
+
+
+def lm_param_count(cfg):
+    return _lib.slim_lm_param_count(ctypes.byref(cfg))
+
+
+def lm_workspace_bytes(cfg, B, chunk):
+    return _lib.slim_lm_workspace_bytes(ctypes.byref(cfg), B, chunk)
+
+
+_lm_ws = {}
+
+
+def lm_checkpoint_bytes(cfg, B, L, chunk):
+    return _lib.slim_lm_checkpoint_bytes(ctypes.byref(cfg), B, L, chunk)
+
+
+def lm_loss_grad(cfg, params, feature_w, tokens, chunk, grads=None, checkpoints=None):
+    """Loss (fp64 device scalar) and gradient (fp32, params' layout) of the
+    multi-layer Performer on tokens (int32 device [B, L]) by Algorithm 1 with
+    slices of ``chunk`` rows.  ``checkpoints``: None (states recovered by
+    subtraction) or a float32 tensor of lm_checkpoint_bytes (device, or pinned
+    host to keep device memory independent of L).  The workspace is a cached
+    torch allocation."""
+    if tokens.dtype != torch.int32 or tokens.dim() != 2 or not tokens.is_contiguous():
+        raise ValueError("tokens must be a contiguous int32 [B, L] tensor")
+    b, length = tokens.shape
+    n = lm_param_count(cfg)
+    if n == 0 or params.numel() != n or params.dtype != torch.float32 or not params.is_contiguous():
+        raise ValueError("params must be a contiguous fp32 tensor of slim_lm_param_count floats")
+    if grads is None:
+        grads = torch.empty_like(params)
+    nbytes = lm_workspace_bytes(cfg, b, min(chunk, length))
+    key = params.device.index
+    buf = _lm_ws.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=params.device)
+        _lm_ws[key] = buf
+    loss = torch.empty((), dtype=torch.float64, device=params.device)
+    stream = torch.cuda.current_stream(params.device).cuda_stream
+    if checkpoints is not None and checkpoints.numel() * checkpoints.element_size() < lm_checkpoint_bytes(
+            cfg, b, length, chunk):
+        raise ValueError("checkpoints too small")
+    _check(_lib.slim_lm_loss_grad(ctypes.byref(cfg), _ptr(params), _ptr(feature_w), _ptr(tokens), b, length, chunk,
+                                  _ptr(grads), _ptr(loss), _ptr(checkpoints), _vp(buf.data_ptr()), buf.numel(),
+                                  _vp(stream)), "slim_lm_loss_grad")
+    return loss, grads
+
+
+def lm_release_workspace():
+    _lm_ws.clear()

@@ -20,9 +20,24 @@ class ProfScope {
   void *start_;
 };
 
+// fp32 attention on an explicit workspace (slim_attn_api.cu), for the
+// language-model driver: forward with carried states, backward with carried
+// states (no dW), and the state after all rows.
+slim_status attn_fwd_f32_ws(const float *q, const float *k, const float *v, const float *w, float *y,
+                            const float *state_in, float *state_out, int B, int H, int L, int d, int M, int chunk,
+                            float *ws, size_t ws_bytes, cudaStream_t st);
+slim_status attn_bwd_f32_ws(const float *q, const float *k, const float *v, const float *w, const float *dy,
+                            float *dq, float *dk, float *dv, const float *state_in, const float *g_in, float *g_out,
+                            int B, int H, int L, int d, int M, int chunk, float *ws, size_t ws_bytes,
+                            cudaStream_t st);
+slim_status attn_state_f32_ws(const float *k, const float *v, const float *w, float *state, int B, int H, int L,
+                              int d, int M, int chunk, float *ws, size_t ws_bytes, cudaStream_t st);
+
 // Shape validation and the segment plan of slim_attn_api.cu.
 slim_status shape_status(int B, int H, int L, int d, int M, int chunk, bool favor);
 Plan plan_for(int B, int H, int L, int d, int M, int chunk, bool favor, bool bwd, bool want_dw);
+// The current SLIM_OPT_W_PER_HEAD setting.
+int opt_w_per_head();
 // Device address of the status word (nullptr on failure).
 int *device_status_ptr();
 

@@ -179,6 +179,9 @@ struct Carry {
   float *state_out = nullptr;
   const float *g_in = nullptr;
   float *g_out = nullptr;
+  // a workspace for this call instead of the registered one (internal callers)
+  float *ws = nullptr;
+  size_t ws_bytes = 0;
   bool any() const { return state_in || state_out || g_in || g_out; }
 };
 
@@ -225,7 +228,10 @@ slim_status run(bool bwd, const void *q, const void *k, const void *v, const flo
   a.g_in = bwd ? c.g_in : nullptr;
   a.g_out = bwd ? c.g_out : nullptr;
   if (cudaGetSymbolAddress((void **)&a.status, g_device_status) != cudaSuccess) return SLIM_ERR_CUDA;
-  {
+  if (c.ws) {
+    if (c.ws_bytes < p.total_floats * sizeof(float)) return SLIM_ERR_WORKSPACE;
+    a.ws = c.ws;
+  } else {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_ws || g_ws_bytes < p.total_floats * sizeof(float)) return SLIM_ERR_WORKSPACE;
     a.ws = static_cast<float *>(g_ws);
@@ -239,7 +245,7 @@ slim_status run(bool bwd, const void *q, const void *k, const void *v, const flo
 // [B][H][d + 1][M] e-major buffer.
 template <typename T>
 slim_status run_state(const void *k, const void *v, const float *w, float *state, int B, int H, int L, int d,
-                      int M, int chunk, cudaStream_t stream) {
+                      int M, int chunk, cudaStream_t stream, float *ws_override = nullptr, size_t ws_bytes = 0) {
   const bool favor = w != nullptr;
   slim_status st = check_shape(B, H, L, d, M, chunk, favor);
   if (st != SLIM_OK) return st;
@@ -256,7 +262,10 @@ slim_status run_state(const void *k, const void *v, const float *w, float *state
   Args a{};
   a.k = k; a.v = v; a.w = w;
   if (cudaGetSymbolAddress((void **)&a.status, g_device_status) != cudaSuccess) return SLIM_ERR_CUDA;
-  {
+  if (ws_override) {
+    if (ws_bytes < p.total_floats * sizeof(float)) return SLIM_ERR_WORKSPACE;
+    a.ws = ws_override;
+  } else {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_ws || g_ws_bytes < p.total_floats * sizeof(float)) return SLIM_ERR_WORKSPACE;
     a.ws = static_cast<float *>(g_ws);
@@ -280,6 +289,37 @@ slim_status run_decode(const void *q, const void *k, const void *v, const float 
 
 }  // namespace
 
+// The fp32 attention calls of the language-model driver (lm.cu), each on a
+// workspace of its own.
+slim_status attn_fwd_f32_ws(const float *q, const float *k, const float *v, const float *w, float *y,
+                            const float *state_in, float *state_out, int B, int H, int L, int d, int M, int chunk,
+                            float *ws, size_t ws_bytes, cudaStream_t st) {
+  Carry c;
+  c.state_in = state_in;
+  c.state_out = state_out;
+  c.ws = ws;
+  c.ws_bytes = ws_bytes;
+  return run<float>(false, q, k, v, w, nullptr, y, nullptr, nullptr, nullptr, nullptr, B, H, L, d, M, chunk, st, c);
+}
+
+slim_status attn_bwd_f32_ws(const float *q, const float *k, const float *v, const float *w, const float *dy,
+                            float *dq, float *dk, float *dv, const float *state_in, const float *g_in, float *g_out,
+                            int B, int H, int L, int d, int M, int chunk, float *ws, size_t ws_bytes,
+                            cudaStream_t st) {
+  Carry c;
+  c.state_in = state_in;
+  c.g_in = g_in;
+  c.g_out = g_out;
+  c.ws = ws;
+  c.ws_bytes = ws_bytes;
+  return run<float>(true, q, k, v, w, dy, nullptr, dq, dk, dv, nullptr, B, H, L, d, M, chunk, st, c);
+}
+
+slim_status attn_state_f32_ws(const float *k, const float *v, const float *w, float *state, int B, int H, int L,
+                              int d, int M, int chunk, float *ws, size_t ws_bytes, cudaStream_t st) {
+  return run_state<float>(k, v, w, state, B, H, L, d, M, chunk, st, ws, ws_bytes);
+}
+
 // Accessors for entry points that live in other translation units.
 slim_status shape_status(int B, int H, int L, int d, int M, int chunk, bool favor) {
   return check_shape(B, H, L, d, M, chunk, favor);
@@ -287,6 +327,11 @@ slim_status shape_status(int B, int H, int L, int d, int M, int chunk, bool favo
 
 Plan plan_for(int B, int H, int L, int d, int M, int chunk, bool favor, bool bwd, bool want_dw) {
   return make_plan(B, H, L, d, M, chunk, favor, bwd, want_dw);
+}
+
+int opt_w_per_head() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_opt_w_per_head;
 }
 
 int *device_status_ptr() {
