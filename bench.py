@@ -442,6 +442,72 @@ def streamed_timings(binding, inputs, exps=(20, 21, 22), window=1 << 18, steps=3
     return out
 
 
+LM_CONFIG = {"vocab": 256, "d_model": 256, "heads": 4, "d_ff": 1024, "layers": 3, "M": 64}
+
+
+def lm_timings(binding, B=2, L=4096, chunks=(64, 256, 1024, 4096), steps=2, warmup=1):
+    """One loss + gradient evaluation of a 3-layer Performer language model by
+    Algorithm 1 (slim_lm_loss_grad), as the SLiM page measures it (section 4):
+    wall-clock time (CUDA events) and peak device memory of the call
+    (torch.cuda.max_memory_allocated above what was allocated before it: the
+    gradient buffer and the workspace; the 10 MB of parameters come on top)
+    against the slice size C, on random byte strings with a randomly
+    initialised model.  Boundary states are kept as checkpoints in
+    pinned host memory; one line per C also times the recovery by
+    subtraction (eq. 19), which needs no checkpoints."""
+    import numpy as np
+    from sub_linear_memory_gb300 import inputs
+
+    c = LM_CONFIG
+    cfg = binding.lm_config(c["vocab"], c["d_model"], c["heads"], c["d_ff"], c["layers"], True, c["M"])
+    d = c["d_model"] // c["heads"]
+    params = torch.tensor(inputs.lm_init_params(c, 11), dtype=torch.float32, device="cuda")
+    fw = binding.draw_orf(c["layers"], d, c["M"], seed=11)  # one fixed projection per layer
+    tok = torch.tensor(np.random.default_rng(12).integers(0, c["vocab"], size=(B, L)), dtype=torch.int32,
+                       device="cuda")
+    out = {"model": "Performer LM: vocab %d, d_model %d, %d heads (d %d), d_ff %d, %d layers, FAVOR+ M %d"
+                    % (c["vocab"], c["d_model"], c["heads"], d, c["d_ff"], c["layers"], c["M"]),
+           "B": B, "L": L, "data": "random strings over 256 symbols, random initialisation",
+           "C": [], "ms_per_step": [], "tokens_per_s": [], "peak_device_bytes": [], "checkpoint_host_bytes": [],
+           "ms_per_step_recovered_by_subtraction": []}
+    for C in chunks:
+        for mode in ("checkpoints", "subtraction"):
+            ck = None
+            if mode == "checkpoints":
+                ck = torch.empty(binding.lm_checkpoint_bytes(cfg, B, L, C) // 4, dtype=torch.float32).pin_memory()
+            binding.lm_release_workspace()
+            binding.release_workspace()
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+            torch.cuda.reset_peak_memory_stats()
+            before = torch.cuda.memory_allocated()  # parameters, projections, tokens and earlier buffers
+            grads = torch.empty_like(params)
+            for _ in range(warmup):
+                binding.lm_loss_grad(cfg, params, fw, tok, C, grads=grads, checkpoints=ck)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                loss, _ = binding.lm_loss_grad(cfg, params, fw, tok, C, grads=grads, checkpoints=ck)
+            e1.record()
+            torch.cuda.synchronize()
+            binding.sync_status()
+            ms = e0.elapsed_time(e1) / steps
+            if mode == "checkpoints":
+                out["C"].append(C)
+                out["ms_per_step"].append(ms)
+                out["tokens_per_s"].append(B * L / (ms / 1e3))
+                out["peak_device_bytes"].append(int(torch.cuda.max_memory_allocated() - before))
+                out["checkpoint_host_bytes"].append(int(ck.numel() * 4))
+                out["loss_per_token"] = float(loss) / (B * (L - 1))
+            else:
+                out["ms_per_step_recovered_by_subtraction"].append(ms)
+    binding.lm_release_workspace()
+    del params, fw, tok
+    torch.cuda.empty_cache()
+    return out
+
+
 def tokens_per_s_from_sample(wl, secs, heads, rows, cores):
     rounds = math.ceil(wl.B * wl.H / heads)
     full_secs = secs * rounds * (wl.L / rows)
@@ -710,6 +776,9 @@ def run_native(args, wl):
     if rank == 0 and world == 1 and args.stream:
         # sequences kept in host memory, window by window: device memory vs L
         line["stream"] = streamed_timings(binding, inputs)
+    if rank == 0 and world == 1 and args.lm:
+        # NEXT: the multi-layer model of the SLiM page, time and memory against C
+        line["lm"] = lm_timings(binding)
     if rank == 0 and world == 1 and args.workloads:
         # the other configs, each timed outside the main region
         others = [n for n in ("l4k", "l1m", "elu16k", "l32k") if n != wl.name]
@@ -799,6 +868,8 @@ def main(argv=None):
     ap.add_argument("--no-memory", dest="memory", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false",
                     help="skip the oracle pass (CPU baseline and parity check)")
+    ap.add_argument("--no-lm", dest="lm", action="store_false",
+                    help="skip the multi-layer Performer (Algorithm 1) timings")
     ap.add_argument("--no-stream", dest="stream", action="store_false",
                     help="skip the host-resident (streamed window) timings")
     ap.add_argument("--no-workloads", dest="workloads", action="store_false",

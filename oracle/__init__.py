@@ -30,6 +30,7 @@ import threading
 
 import numpy as np
 
+from . import lm  # noqa: F401  (re-exported)
 from . import orf  # noqa: F401  (re-exported)
 from . import quadratic  # noqa: F401  (re-exported)
 

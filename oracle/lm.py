@@ -128,27 +128,3 @@ def loss_only(theta, tokens, cfg, feature_w=None):
         tok = torch.as_tensor(np.asarray(tokens, dtype=np.int64))
         fw = None if feature_w is None else torch.as_tensor(np.asarray(feature_w, dtype=np.float64))
         return float(forward_loss(th, tok, cfg, fw))
-
-
-def init_params(cfg, seed):
-    """Random initialisation (numpy fp64): E ~ N(0, 0.02^2) like GPT-2,
-    projections ~ N(0, 1/fan_in), biases zero, layer-norm gains one.  The
-    query and key thirds of W_qkv carry the Performer's d^(-1/4) normaliser
-    (so that g(q) . g(k) estimates exp(q . k / sqrt(d)), and q, k have the
-    scale of the attention workloads' inputs)."""
-    rng = np.random.default_rng(seed)
-    d = cfg["d_model"] // cfg["heads"]
-    parts = []
-    for name, shp in param_shapes(cfg["vocab"], cfg["d_model"], cfg["d_ff"], cfg["layers"]):
-        if name.startswith("ln") and "_g_" in name:
-            parts.append(np.ones(shp))
-        elif name.startswith(("b", "ln")) or name == "b_out":
-            parts.append(np.zeros(shp))
-        elif name == "E":
-            parts.append(rng.standard_normal(shp) * 0.02)
-        else:
-            w = rng.standard_normal(shp) / math.sqrt(shp[0])
-            if name.startswith("W_qkv"):
-                w[:, :2 * cfg["d_model"]] *= d ** -0.25
-            parts.append(w)
-    return np.concatenate([x.ravel() for x in parts])

@@ -122,3 +122,42 @@ def make_inputs(wl, device="cpu", heads=None, want_dy=True):
     if w is not None:
         w = w.to(device)
     return q, k, v, dy, w
+
+
+# ---- the multi-layer Performer language model: a random initialisation ----
+
+def lm_param_layout(cfg):
+    """Names and shapes of the model's parameters, in the order of its flat
+    parameter vector: E, then per layer ln1_g, ln1_b, W_qkv, ln2_g, ln2_b,
+    W1, b1, W2, b2, then W_out, b_out."""
+    v, dm, ff = cfg["vocab"], cfg["d_model"], cfg["d_ff"]
+    out = [("E", (v, dm))]
+    for r in range(cfg["layers"]):
+        out += [("ln1_g", (dm,)), ("ln1_b", (dm,)), ("W_qkv", (dm, 3 * dm)), ("ln2_g", (dm,)), ("ln2_b", (dm,)),
+                ("W1", (dm, ff)), ("b1", (ff,)), ("W2", (ff, dm)), ("b2", (dm,))]
+    return out + [("W_out", (dm, v)), ("b_out", (v,))]
+
+
+def lm_init_params(cfg, seed):
+    """A random initialisation as a flat float64 numpy vector: E ~ N(0, 0.02^2)
+    (as GPT-2), projections ~ N(0, 1/fan_in) with the query and key thirds of
+    W_qkv times d^(-1/4) (the Performer's normaliser, d = d_model / heads),
+    biases zero, layer-norm gains one."""
+    import numpy as np
+
+    rng = np.random.default_rng(seed)
+    d = cfg["d_model"] // cfg["heads"]
+    parts = []
+    for name, shp in lm_param_layout(cfg):
+        if name.endswith("_g"):
+            parts.append(np.ones(shp))
+        elif name.startswith("b") or name.endswith("_b"):
+            parts.append(np.zeros(shp))
+        elif name == "E":
+            parts.append(rng.standard_normal(shp) * 0.02)
+        else:
+            w = rng.standard_normal(shp) / math.sqrt(shp[0])
+            if name == "W_qkv":
+                w[:, :2 * cfg["d_model"]] *= d ** -0.25
+            parts.append(w)
+    return np.concatenate([x.ravel() for x in parts])

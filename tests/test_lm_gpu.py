@@ -14,6 +14,7 @@ import torch
 
 import oracle
 from oracle import lm, orf
+from sub_linear_memory_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -32,7 +33,7 @@ def lib():
 
 
 def _setup(lib, favor, B, L, seed):
-    theta = lm.init_params(CFG, seed)
+    theta = inputs.lm_init_params(CFG, seed)
     d = CFG["d_model"] // CFG["heads"]
     fw = orf.orf_matrices(CFG["layers"], d, CFG["M"], seed=seed).astype(np.float32) if favor else None
     tok = np.random.default_rng(seed).integers(0, CFG["vocab"], size=(B, L))

@@ -16,12 +16,13 @@ import torch
 
 import oracle
 from oracle import lm, orf
+from sub_linear_memory_gb300 import inputs
 
 CFG = {"vocab": 11, "d_model": 8, "heads": 2, "d_ff": 12, "layers": 2, "M": 8}
 
 
 def _model(seed, favor=True, cfg=CFG):
-    theta = lm.init_params(cfg, seed)
+    theta = inputs.lm_init_params(cfg, seed)
     d = cfg["d_model"] // cfg["heads"]
     fw = orf.orf_matrices(cfg["layers"], d, cfg["M"], seed=seed) if favor else None
     return theta, fw
