@@ -70,7 +70,8 @@ typedef enum {
   SLIM_ERR_UNSUPPORTED = 2,  /* shape outside the supported set, misaligned */
   SLIM_ERR_WORKSPACE = 3,    /* no workspace registered, or too small */
   SLIM_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
-  SLIM_ERR_TIMEOUT = 5       /* a device-side bounded wait gave up */
+  SLIM_ERR_TIMEOUT = 5,      /* a device-side bounded wait gave up */
+  SLIM_ERR_BOUNDS = 6        /* a bounds check of the debug build failed (-DSLIM_DEBUG) */
 } slim_status;
 
 /* Options for slim_attn_set_option(). */

@@ -13,11 +13,14 @@ import threading
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-library_path = os.path.join(_HERE, "libslim_attn.so")
+# SLIM_ATTN_LIBRARY=debug loads the -DSLIM_DEBUG build (bounds checks; every
+# call waits and reports device-side errors itself)
+library_path = os.path.join(_HERE, "libslim_attn_debug.so" if os.environ.get("SLIM_ATTN_LIBRARY") == "debug"
+                            else "libslim_attn.so")
 
 if not os.path.exists(library_path):
     raise ImportError(
-        "libslim_attn.so is not built (run sub_linear_memory_gb300.build.build() "
+        os.path.basename(library_path) + " is not built (run sub_linear_memory_gb300.build.build() "
         "or __graft_entry__.build()); there is no non-CUDA fallback")
 
 _lib = ctypes.CDLL(library_path)

@@ -69,6 +69,15 @@ struct Args {
 
 __host__ __device__ inline size_t align_floats(size_t n) { return (n + 63) & ~size_t(63); }  // 256 B
 
+// Debug builds (-DSLIM_DEBUG): a failed bounds check records SLIM_ERR_BOUNDS in
+// the device status word and evaluates to false, so the caller skips the
+// access (no trap: the context stays usable); release builds compile it away.
+#ifdef SLIM_DEBUG
+#define SLIM_DCHECK(status, cond) ((cond) ? true : (atomicCAS((status), 0, (int)SLIM_ERR_BOUNDS), false))
+#else
+#define SLIM_DCHECK(status, cond) true
+#endif
+
 // Index of the W matrix head bh = b * H + h uses: h with one W per head, else 0.
 __host__ __device__ inline int w_head(const Plan &p, int bh) { return p.wh > 1 ? bh % p.H : 0; }
 

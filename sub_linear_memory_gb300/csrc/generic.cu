@@ -259,6 +259,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) segment_state_kernel(Plan p, Args a) {
   __shared__ float sq[256];
   const int s = blockIdx.x, bh = blockIdx.y;
+  if (!SLIM_DCHECK(a.status, s < p.P && bh < p.BH && (long long)s * p.cps < p.nchunks)) return;
   double *out = state_ptr(p, a, p.states_off, bh, s);
   FwdScratch sc = fwd_scratch(p, cta_scratch(p, a));
   const float *w = head_w(p, a, bh);
@@ -302,6 +303,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) forward_kernel(Plan p, Args a) {
   __shared__ float sq[256], den[256];
   const int s = blockIdx.x, bh = blockIdx.y;
+  if (!SLIM_DCHECK(a.status, s < p.P && bh < p.BH && (long long)s * p.cps < p.nchunks)) return;
   FwdScratch sc = fwd_scratch(p, cta_scratch(p, a));
   // segment 0 starts from the carried state (zero when there is none)
   const double *R0 = s > 0 ? state_ptr(p, a, p.states_off, bh, s - 1) : nullptr;
@@ -338,6 +340,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) segment_dg_kernel(Plan p, Args a) {
   __shared__ float sq[256], den[256];
   const int s = blockIdx.x, bh = blockIdx.y;
+  if (!SLIM_DCHECK(a.status, s < p.P && bh < p.BH && (long long)s * p.cps < p.nchunks)) return;
   // segment 0's total is needed only for the gradient w.r.t. the incoming state
   if (s == 0 && !a.g_out) return;
   double *out = state_ptr(p, a, p.gstates_off, bh, s);
@@ -409,6 +412,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) backward_kernel(Plan p, Args a) {
   __shared__ float sq[256], sk[256], den[256];
   const int s = blockIdx.x, bh = blockIdx.y;
+  if (!SLIM_DCHECK(a.status, s < p.P && bh < p.BH && (long long)s * p.cps < p.nchunks)) return;
   const int d = p.d, M = p.M, C = p.C, dp = p.dp;
   BwdScratch sc = bwd_scratch(p, cta_scratch(p, a));
   float *dwp = a.dw ? a.ws + p.dwpart_off + ((size_t)bh * p.P + s) * d * M : nullptr;

@@ -25,6 +25,8 @@
 // the workspace is caller-owned too.
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <algorithm>
 #include <cmath>
 
@@ -413,6 +415,10 @@ extern "C" slim_status slim_lm_loss_grad(const slim_lm_config *cfg, const float 
                                          slim_stream_t stream) {
   using namespace slim;
   using namespace slim::lm;
+  nvtxRangePushA("slim_lm_loss_grad");
+  struct Pop {
+    ~Pop() { nvtxRangePop(); }
+  } pop;
   Cfg c;
   slim_status stt = check_cfg(cfg, c);
   if (stt != SLIM_OK) return stt;
@@ -574,5 +580,9 @@ extern "C" slim_status slim_lm_loss_grad(const slim_lm_config *cfg, const float 
     std::swap(gcur, gnext);
     cuda_ok();
   }
+#ifdef SLIM_DEBUG
+  // debug builds: wait, and report device-side errors from this call
+  if (err == SLIM_OK) err = slim_attn_sync_status(stream);
+#endif
   return err;
 }

@@ -9,6 +9,8 @@
 #include <utility>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -74,6 +76,19 @@ void fold_pending() {
 }
 
 bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+// The status a call returns once its work is enqueued.  Debug builds
+// (-DSLIM_DEBUG) wait for the work and report device-side errors (a failed
+// bounds check, a timed-out wait) from the call that caused them.
+slim_status finish(cudaError_t err, cudaStream_t st) {
+  if (err != cudaSuccess) return SLIM_ERR_CUDA;
+#ifdef SLIM_DEBUG
+  return slim_attn_sync_status((slim_stream_t)st);
+#else
+  (void)st;
+  return SLIM_OK;
+#endif
+}
 
 bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -185,10 +200,19 @@ struct Carry {
   bool any() const { return state_in || state_out || g_in || g_out; }
 };
 
+// An NVTX range around one entry point (visible in Nsight timelines; free
+// when no tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+
 template <typename T>
 slim_status run(bool bwd, const void *q, const void *k, const void *v, const float *w,
                 const void *dy, void *y, void *dq, void *dk, void *dv, float *dw, int B, int H,
                 int L, int d, int M, int chunk, cudaStream_t stream, const Carry &c = Carry()) {
+  NvtxRange range(bwd ? (sizeof(T) == 2 ? "slim_attn_bwd" : "slim_attn_bwd_f32")
+                      : (sizeof(T) == 2 ? "slim_attn_fwd" : "slim_attn_fwd_f32"));
   const bool favor = w != nullptr;
   slim_status st = check_shape(B, H, L, d, M, chunk, favor);
   if (st != SLIM_OK) return st;
@@ -238,7 +262,7 @@ slim_status run(bool bwd, const void *q, const void *k, const void *v, const flo
   }
   cudaError_t err = tc ? (bwd ? tc_backward(p, a, stream) : tc_forward(p, a, stream))
                       : (bwd ? generic_backward<T>(p, a, stream) : generic_forward<T>(p, a, stream));
-  return err == cudaSuccess ? SLIM_OK : SLIM_ERR_CUDA;
+  return finish(err, stream);
 }
 
 // State after all L rows of k, v (serving prefill), into the caller's fp32
@@ -246,6 +270,7 @@ slim_status run(bool bwd, const void *q, const void *k, const void *v, const flo
 template <typename T>
 slim_status run_state(const void *k, const void *v, const float *w, float *state, int B, int H, int L, int d,
                       int M, int chunk, cudaStream_t stream, float *ws_override = nullptr, size_t ws_bytes = 0) {
+  NvtxRange range("slim_attn_state");
   const bool favor = w != nullptr;
   slim_status st = check_shape(B, H, L, d, M, chunk, favor);
   if (st != SLIM_OK) return st;
@@ -271,20 +296,21 @@ slim_status run_state(const void *k, const void *v, const float *w, float *state
     a.ws = static_cast<float *>(g_ws);
   }
   cudaError_t err = tc ? tc_prefill_state(p, a, state, stream) : generic_prefill_state<T>(p, a, state, stream);
-  return err == cudaSuccess ? SLIM_OK : SLIM_ERR_CUDA;
+  return finish(err, stream);
 }
 
 // One new row per head against the carried state.
 template <typename T>
 slim_status run_decode(const void *q, const void *k, const void *v, const float *w, float *state, void *y, int B,
                        int H, int d, int M, cudaStream_t stream) {
+  NvtxRange range("slim_attn_decode");
   const bool favor = w != nullptr;
   slim_status st = check_shape(B, H, 1, d, M, 64, favor);
   if (st != SLIM_OK) return st;
   if ((long long)B * H == 0) return SLIM_OK;
   if (!q || !k || !v || !state || !y) return SLIM_ERR_INVALID_ARG;
   const cudaError_t err = decode_step<T>(q, k, v, w, state, y, B * H, d, M, favor && g_opt_w_per_head ? H : 1, stream);
-  return err == cudaSuccess ? SLIM_OK : SLIM_ERR_CUDA;
+  return finish(err, stream);
 }
 
 }  // namespace
@@ -549,6 +575,7 @@ const char *slim_status_string(slim_status status) {
     case SLIM_ERR_WORKSPACE: return "SLIM_ERR_WORKSPACE: workspace missing or too small";
     case SLIM_ERR_CUDA: return "SLIM_ERR_CUDA: CUDA runtime error";
     case SLIM_ERR_TIMEOUT: return "SLIM_ERR_TIMEOUT: device-side wait gave up";
+    case SLIM_ERR_BOUNDS: return "SLIM_ERR_BOUNDS: a debug-build bounds check failed";
     default: return "unknown slim_status";
   }
 }

@@ -171,6 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q4 = warp & 3, part = warp >> 2, row = 32 * q4 + lane;
   const int rank = CS == 2 ? (int)cluster_rank() : 0, peer = 1 - rank;
   const int seg = blockIdx.x / CS, bh = blockIdx.y;
+  // debug builds: a segment outside the plan records SLIM_ERR_BOUNDS and the CTA does nothing
+  if (!SLIM_DCHECK(p.status, seg < p.P && bh < p.BH && seg * p.tps < p.nt)) return;
   const int M = p.M, DP = D + 1;
   const int fbase = rank * MC;  // first feature of this CTA
   const int t0 = seg * p.tps, t1 = min(t0 + p.tps, p.nt);

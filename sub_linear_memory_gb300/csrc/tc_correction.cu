@@ -126,6 +126,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long units = p.per_head * (gridDim.y > 1 ? 1 : p.BH);
   const long long u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
   const int nun = (int)(u1 - u0);
+  // debug builds: a unit range outside the heads records SLIM_ERR_BOUNDS and the CTA does nothing
+  if (!SLIM_DCHECK(p.status, nun >= 1 && (long long)blockIdx.y + (u1 - 1) / p.per_head < p.BH)) return;
   // every role walks the same units with counters (no divisions per unit):
   // head bh, tile t, segment seg and position pos of the tile in it; the
   // segment's G_end changes when pos wraps
@@ -571,6 +573,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q4 = warp & 3, part = warp >> 2, row = 32 * q4 + lane;
   const int seg = blockIdx.x, bh = blockIdx.y;
+  // debug builds: a segment outside the plan records SLIM_ERR_BOUNDS and the CTA does nothing
+  if (!SLIM_DCHECK(p.status, seg < p.P && bh < p.BH && seg * p.tps < p.nt)) return;
   const int t0 = seg * p.tps, t1 = min(t0 + p.tps, p.nt);
   const uint32_t s_w = sb + lay.w, s_g = sb + lay.g, s_ph = sb + lay.ph;
 

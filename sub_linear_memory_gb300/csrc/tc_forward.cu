@@ -168,6 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int seg = blockIdx.x, bh = blockIdx.y;
+  // debug builds: a segment outside the plan records SLIM_ERR_BOUNDS and the CTA does nothing
+  if (!SLIM_DCHECK(p.status, seg < p.P && seg * p.tps < p.nt)) return;
   const int t0 = seg * p.tps, t1 = min(t0 + p.tps, p.nt), ntl = max(t1 - t0, 0);
 
   if (tid == 0) {
@@ -725,6 +727,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int seg = blockIdx.x, bh = blockIdx.y;
+  // debug builds: a segment outside the plan records SLIM_ERR_BOUNDS and the CTA does nothing
+  if (!SLIM_DCHECK(p.status, seg < p.P && seg * p.tps < p.nt)) return;
   const int t0 = seg * p.tps, t1 = min(t0 + p.tps, p.nt), ntl = max(t1 - t0, 0);
 
   if (tid == 0) {

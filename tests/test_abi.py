@@ -124,3 +124,15 @@ def test_noalloc_size_query(lib):
         n = lib.slim_attn_noalloc_bytes(*shape)
         assert 0 < n <= lib.slim_attn_workspace_bytes(*shape, 0)
     assert lib.slim_attn_noalloc_bytes(2, 16, 32768, 64, 256, 128) > (64 << 20)
+
+
+def test_debug_build_exports_every_declared_symbol():
+    """The -DSLIM_DEBUG variant (device-side bounds checks that record
+    SLIM_ERR_BOUNDS; every call waits and reports device errors itself)
+    builds and exports the same C ABI."""
+    path = build.build(debug=True)
+    dbg = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(dbg, name), name
+    dbg.slim_status_string.restype = ctypes.c_char_p
+    assert dbg.slim_status_string(6).startswith(b"SLIM_ERR_BOUNDS")
