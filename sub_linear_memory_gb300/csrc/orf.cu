@@ -51,17 +51,21 @@ __device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32
   }
 }
 
-// Gaussian number idx of block b of matrix i (fp64).
-__device__ double gaussian(uint32_t k0, uint32_t k1, uint32_t step, int i, int b, int idx) {
-  uint32_t c[4] = {(uint32_t)(idx >> 2), (uint32_t)b, (uint32_t)i, step};
+// The four Gaussians 4j .. 4j + 3 of block b of matrix i (fp64): one Philox
+// call, two Box-Muller pairs.
+__device__ __forceinline__ void gaussians4(uint32_t k0, uint32_t k1, uint32_t step, int i, int b, int j, double g[4]) {
+  uint32_t c[4] = {(uint32_t)j, (uint32_t)b, (uint32_t)i, step};
   philox4x32_10(c, k0, k1);
-  const int pair = (idx >> 1) & 1;  // (x0, x1) or (x2, x3)
-  const double ua = ((double)c[2 * pair] + 0.5) * (1.0 / 4294967296.0);
-  const double ub = ((double)c[2 * pair + 1] + 0.5) * (1.0 / 4294967296.0);
-  const double rad = sqrt(-2.0 * log(ua));
-  double s, co;
-  sincospi(2.0 * ub, &s, &co);  // angle 2 pi ub
-  return (idx & 1) ? rad * s : rad * co;
+#pragma unroll
+  for (int pair = 0; pair < 2; ++pair) {
+    const double ua = ((double)c[2 * pair] + 0.5) * (1.0 / 4294967296.0);
+    const double ub = ((double)c[2 * pair + 1] + 0.5) * (1.0 / 4294967296.0);
+    const double rad = sqrt(-2.0 * log(ua));
+    double s, co;
+    sincospi(2.0 * ub, &s, &co);  // angle 2 pi ub
+    g[2 * pair] = rad * co;
+    g[2 * pair + 1] = rad * s;
+  }
 }
 
 __device__ __forceinline__ double warp_sum_d(double v) {
@@ -80,18 +84,38 @@ __global__ void __launch_bounds__(kOrfThreads) orf_kernel(float *__restrict__ w,
   double *red = coef + d;   // [1] the column norm
   const int b = blockIdx.x, i = blockIdx.y, t = threadIdx.x;
   const int warp = t >> 5, lane = t & 31, nw = kOrfThreads / 32;
-  for (int idx = t; idx < d * d; idx += kOrfThreads) {
-    const int r = idx / d, c = idx - r * d;
-    Q[c * d + r] = gaussian(k0, k1, step, i, b, idx);
+  const int dd = d * d;
+  // lengths first, through Q's buffer: Gaussians dd .. 2 dd - 1 (one Philox
+  // call per thread and step; a call that straddles dd runs in both phases)
+  for (int j = dd / 4 + t; 4 * j < 2 * dd; j += kOrfThreads) {
+    double g[4];
+    gaussians4(k0, k1, step, i, b, j, g);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int idx = 4 * j + e;
+      if (idx >= dd && idx < 2 * dd) Q[idx - dd] = g[e];
+    }
   }
-  // lengths: column c sums its d squares in a fixed order (deterministic)
+  __syncthreads();
+  // column c sums its d squares in a fixed order (deterministic)
   for (int c = t; c < d; c += kOrfThreads) {
     double s = 0.0;
-    for (int r = 0; r < d; ++r) {
-      const double g = gaussian(k0, k1, step, i, b, d * d + r * d + c);
-      s = fma(g, g, s);
-    }
+    for (int r = 0; r < d; ++r) s = fma(Q[r * d + c], Q[r * d + c], s);
     len[c] = sqrt(s);
+  }
+  __syncthreads();
+  // then G, stored by columns: G[r][c] = Gaussian r d + c
+  for (int j = t; 4 * j < dd; j += kOrfThreads) {
+    double g[4];
+    gaussians4(k0, k1, step, i, b, j, g);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int idx = 4 * j + e;
+      if (idx < dd) {
+        const int r = idx / d, c = idx - r * d;
+        Q[c * d + r] = g[e];
+      }
+    }
   }
   __syncthreads();
   for (int c = 0; c < d; ++c) {
