@@ -592,6 +592,9 @@ def run_native(args, wl):
     from sub_linear_memory_gb300 import binding, inputs
 
     peaks = load_peaks()
+    # the backward reads the boundary states the forward of the same step left
+    # in the workspace (SLIM_OPT_REUSE_STATES) instead of recomputing them
+    binding.set_option(binding.OPT_REUSE_STATES, 1 if args.reuse else 0)
     q, k, v, dy, w = inputs.make_inputs(wl, device="cuda")
     y = torch.empty_like(q)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
@@ -755,7 +758,9 @@ def run_native(args, wl):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Gaussian Q, K, V, dY; block-orthogonal random W)",
-        "config": dict(config_of(wl, world), **({"learnable_w": "dW computed by the backward"} if dw is not None else {})),
+        "config": dict(config_of(wl, world), **({"learnable_w": "dW computed by the backward"} if dw is not None else {}),
+                       state_reuse=("the backward reads the forward's boundary states" if args.reuse
+                                    else "the backward recomputes the boundary states")),
         "clocks": clocks.summary(),
         "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": 4 * nbytes, "d2h_bytes_per_step": 4 * nbytes,
@@ -865,6 +870,8 @@ def main(argv=None):
                          "(a reduced case for profiling); the default is the workload's own")
     ap.add_argument("--dw", action="store_true",
                     help="learnable W: the backward also computes dW")
+    ap.add_argument("--no-reuse", dest="reuse", action="store_false",
+                    help="the backward recomputes the boundary states instead of reading the forward's")
     ap.add_argument("--no-memory", dest="memory", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false",
                     help="skip the oracle pass (CPU baseline and parity check)")

@@ -90,7 +90,21 @@ typedef enum {
    * every batch entry uses w[h]) and dw is [H][d][M], each summed over the
    * batch entries and rows of its head.  Applies to every entry point that
    * takes w, and to the workspace sizes. */
-  SLIM_OPT_W_PER_HEAD = 4
+  SLIM_OPT_W_PER_HEAD = 4,
+  /* Forward-to-backward reuse of the boundary states (section 3.2 keeps only
+   * the states at the slice boundaries; section 3.3 rebuilds the rest from
+   * them): 0 = off (the default), 1 = on.  When on, slim_attn_fwd on the
+   * tensor-core path at d = 64 (bf16 I/O), when its segments are the ones the
+   * backward of the same shape uses, leaves the exact end state of each
+   * segment in the registered workspace and tags it with k, v, w, the shape
+   * and the workspace.  The next slim_attn_bwd with the same k, v, w
+   * pointers, shape and workspace, and no other call on that workspace in
+   * between, reads those states instead of recomputing them; any mismatch
+   * recomputes them, so results never depend on the tag.  The caller
+   * guarantees that the contents of k, v and w do not change between the two
+   * calls (they are not compared).  Carried-state calls (slim_attn_*_carry)
+   * neither leave nor read tagged states. */
+  SLIM_OPT_REUSE_STATES = 5
 } slim_option;
 
 /* Forward, bf16 I/O: y = Att^lin(q, k, v) (section 2.1, eq. (2)-(4); slices

@@ -94,6 +94,7 @@ OPT_SEGMENTS = 1
 OPT_PATH = 2
 OPT_PROFILE = 3
 OPT_W_PER_HEAD = 4
+OPT_REUSE_STATES = 5
 EXPORTED = (
     "slim_attn_fwd", "slim_attn_bwd", "slim_attn_fwd_f32", "slim_attn_bwd_f32",
     "slim_attn_state", "slim_attn_state_f32", "slim_attn_decode", "slim_attn_decode_f32",

@@ -65,6 +65,11 @@ struct Args {
   float *state_out;
   const float *g_in;
   float *g_out;
+  // SLIM_OPT_REUSE_STATES (tensor path): the forward leaves every segment's
+  // exact end state in the workspace; the backward reads those instead of
+  // running its own state pass
+  int keep_states;
+  int reuse_states;
 };
 
 __host__ __device__ inline size_t align_floats(size_t n) { return (n + 63) & ~size_t(63); }  // 256 B

@@ -67,6 +67,8 @@ cudaError_t tc_forward(const Plan &p, const Args &a, cudaStream_t st);
 // tile by tile (the two-CTA backward then adds each CTA's partials into them).
 cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, bool zero_grads, const float *init,
                               cudaStream_t st);
+// FAVOR+: W -> the bf16 W^T image the tensor kernels copy (in the workspace).
+cudaError_t tc_prep_w(const Plan &p, const Args &a, cudaStream_t st);
 // Carried states (carry.cu): the caller's e-major [BH][d + 1][M] layout into
 // the tensor path's features-major [BH][M][d + 1], and the sum of one slot of
 // two features-major state arrays ([BH][pa][M][d + 1], b may be NULL) back

@@ -27,6 +27,21 @@ size_t g_ws_bytes = 0;
 int g_opt_segments = 0;
 int g_opt_path = 0;
 int g_opt_w_per_head = 0;
+int g_opt_reuse_states = 0;
+
+// What the last forward with SLIM_OPT_REUSE_STATES left in the registered
+// workspace: its inputs, shape and workspace, and the workspace generation
+// (bumped by every call that writes the registered workspace's states).
+struct StateTag {
+  bool valid = false;
+  const void *k = nullptr, *v = nullptr;
+  const float *w = nullptr;
+  int B = 0, H = 0, L = 0, d = 0, M = 0, chunk = 0, wh = 0, P = 0;
+  const void *ws = nullptr;
+  unsigned long long gen = 0;
+};
+StateTag g_tag;
+unsigned long long g_ws_gen = 0;
 
 // ---- per-kernel profiling ----
 std::mutex g_prof_mu;
@@ -252,6 +267,16 @@ slim_status run(bool bwd, const void *q, const void *k, const void *v, const flo
   a.g_in = bwd ? c.g_in : nullptr;
   a.g_out = bwd ? c.g_out : nullptr;
   if (cudaGetSymbolAddress((void **)&a.status, g_device_status) != cudaSuccess) return SLIM_ERR_CUDA;
+  // SLIM_OPT_REUSE_STATES: a forward on the registered workspace whose
+  // segments are the ones the backward would choose tags the end states it
+  // leaves there; a backward takes them when the tag matches its k, v, w,
+  // shape, segments and workspace and no call has written the workspace since
+  bool reuse = tc && d == 64 && !c.any() && !c.ws;
+  if (reuse && !bwd) {
+    const Plan pb = make_plan(B, H, L, d, M, chunk, favor, true, false, 2);
+    reuse = pb.P == p.P && pb.cps == p.cps;
+  }
+  bool tag_it = false;
   if (c.ws) {
     if (c.ws_bytes < p.total_floats * sizeof(float)) return SLIM_ERR_WORKSPACE;
     a.ws = c.ws;
@@ -259,9 +284,32 @@ slim_status run(bool bwd, const void *q, const void *k, const void *v, const flo
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_ws || g_ws_bytes < p.total_floats * sizeof(float)) return SLIM_ERR_WORKSPACE;
     a.ws = static_cast<float *>(g_ws);
+    const StateTag &t = g_tag;
+    if (reuse && g_opt_reuse_states && bwd && t.valid && t.gen == g_ws_gen && t.ws == g_ws && t.k == k &&
+        t.v == v && t.w == w && t.B == B && t.H == H && t.L == L && t.d == d && t.M == M && t.chunk == chunk &&
+        t.wh == p.wh && t.P == p.P) {
+      a.reuse_states = 1;  // reads the tagged states, writes none
+    } else {
+      ++g_ws_gen;
+      g_tag.valid = false;
+      if (reuse && g_opt_reuse_states && !bwd) {
+        a.keep_states = 1;
+        tag_it = true;
+      }
+    }
   }
   cudaError_t err = tc ? (bwd ? tc_backward(p, a, stream) : tc_forward(p, a, stream))
                       : (bwd ? generic_backward<T>(p, a, stream) : generic_forward<T>(p, a, stream));
+  if (tag_it && err == cudaSuccess) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    StateTag t;
+    t.valid = true;
+    t.k = k; t.v = v; t.w = w;
+    t.B = B; t.H = H; t.L = L; t.d = d; t.M = M; t.chunk = chunk; t.wh = p.wh; t.P = p.P;
+    t.ws = g_ws;
+    t.gen = g_ws_gen;
+    g_tag = t;
+  }
   return finish(err, stream);
 }
 
@@ -294,6 +342,8 @@ slim_status run_state(const void *k, const void *v, const float *w, float *state
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_ws || g_ws_bytes < p.total_floats * sizeof(float)) return SLIM_ERR_WORKSPACE;
     a.ws = static_cast<float *>(g_ws);
+    ++g_ws_gen;
+    g_tag.valid = false;
   }
   cudaError_t err = tc ? tc_prefill_state(p, a, state, stream) : generic_prefill_state<T>(p, a, state, stream);
   return finish(err, stream);
@@ -501,6 +551,10 @@ slim_status slim_attn_set_workspace(void *ptr, size_t bytes) {
   if ((ptr == nullptr) != (bytes == 0)) return SLIM_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(ptr) % 256 != 0) return SLIM_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(slim::g_mu);
+  if (ptr != slim::g_ws || bytes != slim::g_ws_bytes) {
+    slim::g_tag.valid = false;
+    ++slim::g_ws_gen;
+  }
   slim::g_ws = ptr;
   slim::g_ws_bytes = bytes;
   return SLIM_OK;
@@ -523,6 +577,11 @@ slim_status slim_attn_set_option(int option, int value) {
     case SLIM_OPT_W_PER_HEAD:
       if (value < 0 || value > 1) return SLIM_ERR_INVALID_ARG;
       slim::g_opt_w_per_head = value;
+      return SLIM_OK;
+    case SLIM_OPT_REUSE_STATES:
+      if (value < 0 || value > 1) return SLIM_ERR_INVALID_ARG;
+      slim::g_opt_reuse_states = value;
+      slim::g_tag.valid = false;
       return SLIM_OK;
     default:
       return SLIM_ERR_INVALID_ARG;

@@ -841,6 +841,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_dealloc(tb, 512);
 }
 
+// dQ, dK, dV = 0 before the CTA pairs add their partials (16-byte stores,
+// a grid of whole waves over the SMs)
+__global__ void zero3_kernel(uint4 *__restrict__ a, uint4 *__restrict__ b, uint4 *__restrict__ c, size_t n16) {
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x) {
+    a[i] = z;
+    b[i] = z;
+    c[i] = z;
+  }
+}
+
+cudaError_t zero_outputs(const Plan &pl, const Args &a, cudaStream_t st) {
+  const size_t n16 = (size_t)pl.BH * pl.L * D * sizeof(__nv_bfloat16) / 16;  // d = 64: 8 per row
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int blocks = (int)std::max<size_t>(1, std::min<size_t>((n16 + 255) / 256, (size_t)sms * 8));
+  ProfScope ps("zero_grads", st);
+  zero3_kernel<<<blocks, 256, 0, st>>>(static_cast<uint4 *>(a.dq), static_cast<uint4 *>(a.dk),
+                                       static_cast<uint4 *>(a.dv), n16);
+  return cudaGetLastError();
+}
+
 template <bool FAVOR, int CS, int MC>
 cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mdy;
@@ -873,8 +895,16 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   // R' totals of every segment, scanned; with two CTAs per segment the
-  // outputs start at zero for the per-CTA reduce-adds
-  cudaError_t e = tc_segment_states(pl, a, pl.P, CS == 2, init, st);
+  // outputs start at zero for the per-CTA reduce-adds.  With the end states
+  // the forward left (same segments, same exact scan) only the W image and
+  // the zeroed outputs remain to be made.
+  cudaError_t e;
+  if (a.reuse_states) {
+    e = tc_prep_w(pl, a, st);
+    if (e == cudaSuccess && CS == 2) e = zero_outputs(pl, a, st);
+  } else {
+    e = tc_segment_states(pl, a, pl.P, CS == 2, init, st);
+  }
   if (e != cudaSuccess) return e;
   Params p{};
   p.L = pl.L; p.M = pl.M; p.nt = pl.tc_tiles; p.P = pl.P; p.tps = pl.cps; p.favor = FAVOR;

@@ -1145,11 +1145,13 @@ cudaError_t forward_family(const Plan &pl, const Args &a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     init = fm;
   }
-  // every segment's total when the final state is wanted (kept exactly as
-  // double-float pairs then), else all but the last
-  const int nseg = a.state_out ? pl.P : pl.P - 1;
+  // every segment's total when the final state is wanted, or when the
+  // backward is to read the end states (kept exactly as double-float pairs
+  // then), else all but the last
+  const bool all = a.state_out != nullptr || a.keep_states;
+  const int nseg = all ? pl.P : pl.P - 1;
   if (nseg > 0) {
-    e = segment_states<D, FAVOR>(pl, a, mq, mk, mv, nullptr, nseg, a.state_out != nullptr, init, st);
+    e = segment_states<D, FAVOR>(pl, a, mq, mk, mv, nullptr, nseg, all, init, st);
     if (e != cudaSuccess) return e;
   }
   {
@@ -1204,6 +1206,8 @@ cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, bool zero_
   if (d == 128 && !p.favor) return tcf::segment_states<128, false>(p, a, mk, mk, mv, z, nseg, true, init, st);
   return cudaErrorInvalidValue;
 }
+
+cudaError_t tc_prep_w(const Plan &p, const Args &a, cudaStream_t st) { return tcf::prep_w(p, a, st); }
 
 cudaError_t tc_forward(const Plan &p, const Args &a, cudaStream_t st) {
   cudaError_t e = tcf::prep_w(p, a, st);

@@ -81,6 +81,20 @@ def test_workspace_registration_rules(lib):
     assert lib.slim_attn_set_option(1, -1) == 1
 
 
+def test_reuse_states_option(lib):
+    """SLIM_OPT_REUSE_STATES takes 0 or 1 and changes no plan (no GPU needed)."""
+    assert lib.slim_attn_set_option(5, 2) == 1
+    assert lib.slim_attn_set_option(5, -1) == 1
+    shape = (2, 16, 32768, 64, 256, 128)
+    off = [lib.slim_attn_workspace_bytes(*shape, b) for b in (0, 1)]
+    assert lib.slim_attn_set_option(5, 1) == 0
+    try:
+        on = [lib.slim_attn_workspace_bytes(*shape, b) for b in (0, 1)]
+    finally:
+        assert lib.slim_attn_set_option(5, 0) == 0
+    assert on == off and min(off) > 0
+
+
 def test_workspace_does_not_grow_with_sequence_length(lib):
     """Sub-linear memory: past the point where every SM has a segment, the
     workspace is independent of L (only boundary states and chunk scratch)."""
