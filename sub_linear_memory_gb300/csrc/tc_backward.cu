@@ -340,21 +340,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float ck = live ? favor_row_const(nk, M) : -INFINITY;
       const float cq = live ? favor_row_const(nq, M) : -INFINITY;
       wait_mma();
-      for (int side = 0; side < 2; ++side) {
-        const uint32_t t_in = side ? kX : kT, s_out = side ? s_phq : s_phk;
-        const float c_row = side ? cq : ck;
+      {
+        // both sides' F with one wait, so the two loads' latencies overlap
         const int c0 = QF * part;
-        float v[QF];
+        float fk[QF], fq[QF];
         if constexpr (QF == 32) {
-          tmem_ld32(tmem_addr(tb, 32 * q4, t_in + c0), v);
+          tmem_ld32x2(tmem_addr(tb, 32 * q4, kT + c0), tmem_addr(tb, 32 * q4, kX + c0), fk, fq);
         } else {
-          tmem_ld16(tmem_addr(tb, 32 * q4, t_in + c0), v);
+          tmem_ld16x2(tmem_addr(tb, 32 * q4, kT + c0), tmem_addr(tb, 32 * q4, kX + c0), fk, fq);
         }
         // padding rows: F = 0 (zero-filled tile) and 2^-inf = 0
 #pragma unroll
-        for (int i = 0; i < QF; ++i) v[i] = favor_feature(v[i], c_row);
+        for (int i = 0; i < QF; ++i) {
+          fk[i] = favor_feature(fk[i], ck);
+          fq[i] = favor_feature(fq[i], cq);
+        }
 #pragma unroll
-        for (int j = 0; j < QF / 8; ++j) st_bf16x8(s_out + sw128_offset(row, c0 + 8 * j, kTile), v + 8 * j);
+        for (int j = 0; j < QF / 8; ++j) {
+          st_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), fk + 8 * j);
+          st_bf16x8(s_phq + sw128_offset(row, c0 + 8 * j, kTile), fq + 8 * j);
+        }
       }
     } else {
       for (int side = 0; side < 2; ++side) {
