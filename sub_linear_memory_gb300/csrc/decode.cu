@@ -181,7 +181,7 @@ cudaError_t decode_step(const void *q, const void *k, const void *v, const float
 }
 
 cudaError_t tc_prefill_state(const Plan &p, const Args &a, float *state, cudaStream_t st) {
-  cudaError_t e = tc_segment_states(p, a, p.P, false, nullptr, st);
+  cudaError_t e = tc_segment_states(p, a, p.P, 0, nullptr, st);
   if (e != cudaSuccess) return e;
   const size_t n = (size_t)p.BH * (p.d + 1) * p.M;
   const int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);

@@ -63,9 +63,10 @@ size_t tc_smem_bytes(int d, int M, bool favor);
 cudaError_t tc_forward(const Plan &p, const Args &a, cudaStream_t st);
 // K-side totals of R' for the first nseg segments, scanned from `init` (the
 // carried incoming state, features-major fp32 [BH][M][d + 1], or NULL) as
-// double-float pairs (tensor path).  zero_grads: also set dQ, dK, dV to zero
-// tile by tile (the two-CTA backward then adds each CTA's partials into them).
-cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, bool zero_grads, const float *init,
+// double-float pairs (tensor path).  zero_grads: also set these outputs to
+// zero tile by tile (1 dQ, 2 dK, 4 dV; the two-CTA backwards then add each
+// CTA's partials into them).
+cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, int zero_grads, const float *init,
                               cudaStream_t st);
 // FAVOR+: W -> the bf16 W^T image the tensor kernels copy (in the workspace).
 cudaError_t tc_prep_w(const Plan &p, const Args &a, cudaStream_t st);

@@ -908,7 +908,7 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
     e = tc_prep_w(pl, a, st);
     if (e == cudaSuccess && CS == 2) e = zero_outputs(pl, a, st);
   } else {
-    e = tc_segment_states(pl, a, pl.P, CS == 2, init, st);
+    e = tc_segment_states(pl, a, pl.P, CS == 2 ? 7 : 0, init, st);
   }
   if (e != cudaSuccess) return e;
   Params p{};

@@ -749,12 +749,9 @@ cudaError_t tc_backward_elu128(const Plan &pl, const Args &a, cudaStream_t st) {
       !make_map_bf16_3d(&mdq, a.dq, pl.BH, pl.L, D, kTile) || !make_map_bf16_3d(&mdk, a.dk, pl.BH, pl.L, D, kTile) ||
       !make_map_bf16_3d(&mdv, a.dv, pl.BH, pl.L, D, kTile))
     return cudaErrorInvalidValue;
-  // each CTA of a pair adds its share of dQ and dK
-  const size_t io_bytes = sizeof(__nv_bfloat16) * (size_t)pl.BH * pl.L * D;
-  cudaError_t e = cudaMemsetAsync(a.dq, 0, io_bytes, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(a.dk, 0, io_bytes, st);
-  if (e != cudaSuccess) return e;
-  e = tc_segment_states(pl, a, pl.P, false, nullptr, st);
+  // each CTA of a pair adds its share of dQ and dK: the state pass zeroes
+  // them tile by tile while it runs
+  cudaError_t e = tc_segment_states(pl, a, pl.P, 1 | 2, nullptr, st);
   if (e != cudaSuccess) return e;
   {
     Params p{};

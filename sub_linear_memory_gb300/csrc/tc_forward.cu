@@ -60,7 +60,7 @@ enum { MODE_STATE = 0, MODE_FWD = 1 };
 struct Params {
   int L, M, nt, P, tps;
   int H, wstride;  // heads; bf16 elements between per-head W^T images (0: one shared W)
-  int zero_grads;  // state pass of a two-CTA backward: zero dQ, dK, dV tile by tile
+  int zero_grads;  // state pass of a two-CTA backward: zero these outputs tile by tile (1 dQ, 2 dK, 4 dV)
   __nv_bfloat16 *y;
   const __nv_bfloat16 *wimg;  // W^T shared-memory image (FAVOR+)
   float *states;     // fp32 [BH][P][M][D + 1]: high parts of the segment states
@@ -658,8 +658,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // pipe cost dQ of the first tiles of a long segment a factor of two hundred,
 // and plain fp32 still a factor of 2.6 through S, whose positive terms make
 // its rounding errors add up; the signed R columns' errors do not.
-//   warp 0       TMA producer (K, V ring; zero tiles of dQ, dK, dV when the
-//                two-CTA backward accumulates into them);
+//   warp 0       TMA producer (K, V ring; zero tiles of the outputs a
+//                two-CTA backward accumulates into);
 //   warp 1       feature MMAs F = K W, 64 features per job, two TMEM buffers;
 //   warp 2       increment MMAs;
 //   warps 4-11   phi_k: two threads per row, 32 columns of each job each,
@@ -696,7 +696,7 @@ struct StateLayout {
     slots = o; o += kSlots * kTileBytes;            // then, at the end, the [M][D + 1] outputs
     phk = o; o += 2u * kTile * 128 * 2;             // two phi_k blocks
     ones = o; o += D == 64 ? 16384u : 4096u;
-    zero = o; o += D == 64 ? kTileBytes : 0u;       // zero tile (two-CTA backward, d = 64)
+    zero = o; o += kTile * 64 * 2;                  // zero box of [128][64] (two-CTA backward)
     lo = o; o += (uint32_t)M * 4u;                  // low parts of S
     nrm = o; o += 2u * 2u * kTile * 4u;             // [tile parity][half of d][row] partial |k|^2
     bars = o; o += 8 * S_COUNT + 16;
@@ -756,9 +756,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmV);
   }
   if (warp == 0) tmem_alloc(tslot, 512);
-  if (D == 64)
-    for (int idx = tid; idx < (int)(LY::kTileBytes / 16); idx += kThreads)
-      reinterpret_cast<uint4 *>(smem + lay.zero)[idx] = make_uint4(0u, 0u, 0u, 0u);
+  for (int idx = tid; idx < kTile * 64 * 2 / 16; idx += kThreads)
+    reinterpret_cast<uint4 *>(smem + lay.zero)[idx] = make_uint4(0u, 0u, 0u, 0u);
   for (int idx = tid; idx < M; idx += kThreads) reinterpret_cast<float *>(smem + lay.lo)[idx] = 0.f;
   for (int idx = tid; idx < kTile * (D == 64 ? 64 : 16); idx += kThreads) {
     const int r = D == 64 ? idx >> 6 : idx >> 4, x = D == 64 ? idx & 63 : idx & 15;
@@ -832,15 +831,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(smem + lay.slots + s * LY::kTileBytes + c * kTile * 2, r ? &tmV : &tmK, bar + S_FULL + s, c,
                         t * kTile, bh);
         }
-        if (D == 64 && p.zero_grads) {
-          // the two-CTA backward adds its per-CTA partials of dQ, dK, dV
-          tma_store_3d(&tmDQ, smem + lay.zero, 0, t * kTile, bh);
-          tma_store_3d(&tmDK, smem + lay.zero, 0, t * kTile, bh);
-          tma_store_3d(&tmDV, smem + lay.zero, 0, t * kTile, bh);
+        if (p.zero_grads) {
+          // the two-CTA backward adds its per-CTA partials into these
+          for (int c = 0; c < D; c += 64) {
+            if (p.zero_grads & 1) tma_store_3d(&tmDQ, smem + lay.zero, c, t * kTile, bh);
+            if (p.zero_grads & 2) tma_store_3d(&tmDK, smem + lay.zero, c, t * kTile, bh);
+            if (p.zero_grads & 4) tma_store_3d(&tmDV, smem + lay.zero, c, t * kTile, bh);
+          }
           tma_store_commit();
         }
       }
-      if (D == 64 && p.zero_grads) tma_store_wait_all();
+      if (p.zero_grads) tma_store_wait_all();
       // the last load of every slot
       for (int m = max(0, n - kS); m < n; ++m) mbar_drain(bar + S_FULL + slot_idx(m), slot_par(m));
       if (FAVOR) mbar_drain(bar + S_SETUP, 0);
@@ -1039,13 +1040,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool FAVOR, int MODE, int M>
 cudaError_t launch_m(const Plan &pl, const Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
-                     const CUtensorMap &mv, const CUtensorMap *mz, int nseg, const float *state_in,
+                     const CUtensorMap &mv, const CUtensorMap *mz, int zero_mask, int nseg, const float *state_in,
                      cudaStream_t st) {
   Params p{};
   p.state_in = state_in;
   p.L = pl.L; p.M = pl.M; p.nt = pl.tc_tiles; p.P = pl.P; p.tps = pl.cps;
   p.H = pl.H; p.wstride = pl.wh > 1 ? pl.M * 64 : 0;
-  p.zero_grads = mz != nullptr;
+  p.zero_grads = mz != nullptr ? zero_mask : 0;
   p.y = static_cast<__nv_bfloat16 *>(a.y);
   p.wimg = reinterpret_cast<const __nv_bfloat16 *>(a.ws + pl.wimg_off);
   p.states = a.ws + pl.states_off;
@@ -1071,14 +1072,15 @@ cudaError_t launch_m(const Plan &pl, const Args &a, const CUtensorMap &mq, const
 // features, elu+1 with M = d.
 template <int D, bool FAVOR, int MODE>
 cudaError_t launch(const Plan &pl, const Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
-                   const CUtensorMap &mv, const CUtensorMap *mz, int nseg, const float *state_in, cudaStream_t st) {
+                   const CUtensorMap &mv, const CUtensorMap *mz, int zero_mask, int nseg, const float *state_in,
+                   cudaStream_t st) {
   if constexpr (!FAVOR) {
-    return pl.M == D ? launch_m<D, FAVOR, MODE, D>(pl, a, mq, mk, mv, mz, nseg, state_in, st)
+    return pl.M == D ? launch_m<D, FAVOR, MODE, D>(pl, a, mq, mk, mv, mz, zero_mask, nseg, state_in, st)
                      : cudaErrorInvalidValue;
   } else {
-    if (pl.M == 64) return launch_m<D, FAVOR, MODE, 64>(pl, a, mq, mk, mv, mz, nseg, state_in, st);
-    if (pl.M == 128) return launch_m<D, FAVOR, MODE, 128>(pl, a, mq, mk, mv, mz, nseg, state_in, st);
-    if (pl.M == 256) return launch_m<D, FAVOR, MODE, 256>(pl, a, mq, mk, mv, mz, nseg, state_in, st);
+    if (pl.M == 64) return launch_m<D, FAVOR, MODE, 64>(pl, a, mq, mk, mv, mz, zero_mask, nseg, state_in, st);
+    if (pl.M == 128) return launch_m<D, FAVOR, MODE, 128>(pl, a, mq, mk, mv, mz, zero_mask, nseg, state_in, st);
+    if (pl.M == 256) return launch_m<D, FAVOR, MODE, 256>(pl, a, mq, mk, mv, mz, zero_mask, nseg, state_in, st);
     return cudaErrorInvalidValue;
   }
 }
@@ -1113,12 +1115,12 @@ cudaError_t prep_w(const Plan &pl, const Args &a, cudaStream_t st) {
 // segment added) is enough and moves half the bytes.
 template <int D, bool FAVOR>
 cudaError_t segment_states(const Plan &pl, const Args &a, const CUtensorMap &mq,
-                           const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap *mz, int nseg,
+                           const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap *mz, int zero_mask, int nseg,
                            bool exact, const float *init, cudaStream_t st) {
   cudaError_t e;
   {
     ProfScope ps("tc_segment_state", st);
-    e = launch<D, FAVOR, MODE_STATE>(pl, a, mq, mk, mv, mz, nseg, nullptr, st);
+    e = launch<D, FAVOR, MODE_STATE>(pl, a, mq, mk, mv, mz, zero_mask, nseg, nullptr, st);
     if (e != cudaSuccess) return e;
   }
   if (nseg > 1 || (nseg > 0 && init)) {
@@ -1151,12 +1153,12 @@ cudaError_t forward_family(const Plan &pl, const Args &a, cudaStream_t st) {
   const bool all = a.state_out != nullptr || a.keep_states;
   const int nseg = all ? pl.P : pl.P - 1;
   if (nseg > 0) {
-    e = segment_states<D, FAVOR>(pl, a, mq, mk, mv, nullptr, nseg, all, init, st);
+    e = segment_states<D, FAVOR>(pl, a, mq, mk, mv, nullptr, 0, nseg, all, init, st);
     if (e != cudaSuccess) return e;
   }
   {
     ProfScope ps("tc_forward", st);
-    e = launch<D, FAVOR, MODE_FWD>(pl, a, mq, mk, mv, nullptr, pl.P, init, st);
+    e = launch<D, FAVOR, MODE_FWD>(pl, a, mq, mk, mv, nullptr, 0, pl.P, init, st);
     if (e != cudaSuccess) return e;
   }
   if (a.state_out)
@@ -1187,7 +1189,7 @@ bool tc_forward_supported(int d, int M, int chunk, bool favor) {
   return false;
 }
 
-cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, bool zero_grads, const float *init,
+cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, int zero_grads, const float *init,
                               cudaStream_t st) {
   CUtensorMap mk, mv, mz[3];
   const int d = p.d;
@@ -1195,15 +1197,17 @@ cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, bool zero_
   if (e != cudaSuccess) return e;
   if (!make_map_bf16_3d(&mk, a.k, p.BH, p.L, d, tcf::kTile) || !make_map_bf16_3d(&mv, a.v, p.BH, p.L, d, tcf::kTile))
     return cudaErrorInvalidValue;
-  if (zero_grads &&
-      (!make_map_bf16_3d(&mz[0], a.dq, p.BH, p.L, d, tcf::kTile) ||
-       !make_map_bf16_3d(&mz[1], a.dk, p.BH, p.L, d, tcf::kTile) ||
-       !make_map_bf16_3d(&mz[2], a.dv, p.BH, p.L, d, tcf::kTile)))
-    return cudaErrorInvalidValue;
+  // dummies (never stored to) for the outputs left alone
+  mz[0] = mz[1] = mz[2] = mk;
+  void *const outs[3] = {a.dq, a.dk, a.dv};
+  for (int o = 0; o < 3; ++o)
+    if ((zero_grads >> o & 1) && !make_map_bf16_3d(&mz[o], outs[o], p.BH, p.L, d, tcf::kTile))
+      return cudaErrorInvalidValue;
   const CUtensorMap *z = zero_grads ? mz : nullptr;
-  if (d == 64 && p.favor) return tcf::segment_states<64, true>(p, a, mk, mk, mv, z, nseg, true, init, st);
-  if (d == 64) return tcf::segment_states<64, false>(p, a, mk, mk, mv, z, nseg, true, init, st);
-  if (d == 128 && !p.favor) return tcf::segment_states<128, false>(p, a, mk, mk, mv, z, nseg, true, init, st);
+  if (d == 64 && p.favor) return tcf::segment_states<64, true>(p, a, mk, mk, mv, z, zero_grads, nseg, true, init, st);
+  if (d == 64) return tcf::segment_states<64, false>(p, a, mk, mk, mv, z, zero_grads, nseg, true, init, st);
+  if (d == 128 && !p.favor)
+    return tcf::segment_states<128, false>(p, a, mk, mk, mv, z, zero_grads, nseg, true, init, st);
   return cudaErrorInvalidValue;
 }
 
