@@ -262,9 +262,11 @@ def oracle_baseline_and_parity(wl, binding, want_dw, row_frac=1.0):
     check_dw = want_dw and w is not None and rows == wl.L
     t0 = time.perf_counter()
     y_ref = oracle.recurrence_forward(qn, kn, vn, wn, threads=cores)
+    t_fwd = time.perf_counter() - t0
     grads = oracle.recurrence_backward(qn, kn, vn, wn, dyn, threads=cores, want_dw=check_dw)
     secs = time.perf_counter() - t0
     base = {"value": tokens_per_s_from_sample(wl, secs, heads, rows, cores), "unit": "tokens/s",
+            "fwd_value": tokens_per_s_from_sample(wl, t_fwd, heads, rows, cores),
             "cores": cores, "kind": "oracle",
             "sample": "%d of %d heads x first %d of %d rows, fp64 recurrence fwd+bwd (%.1f s), scaled to the full workload"
                       % (heads, bh, rows, wl.L, secs)}
@@ -586,6 +588,75 @@ def memory_sweep(binding, inputs, exps=(16, 18, 20)):
     return out
 
 
+def recompute_flops_per_token_head(wl, state_passes):
+    """FLOPs the kernels spend beyond the algorithmic count, per token-head:
+    the backward recomputes the forward of every tile (features, A and num')
+    and every segment-state pass recomputes the K-side features and the state
+    increments."""
+    d, M, C, dp = wl.d, wl.M, wl.chunk, wl.d + 1
+    favor = wl.feature == "favor"
+    fwd_again = (4 * d * M if favor else 0) + M * (C + 1) + dp * (C + 1) + 4 * M * dp
+    state_pass = (2 * d * M if favor else 0) + 2 * M * dp
+    return fwd_again + state_passes * state_pass
+
+
+def ex2_ceiling(binding, sm_mhz, wl, ms_per_step, reps=5):
+    """The exponential unit's measured rate (slim_attn_probe_ex2: a kernel of
+    nothing but dependent 2^x chains) and the time the step's algorithmic
+    exponentials (2M per token-head forward, as many backward) would take at
+    that rate: a third ceiling next to the tensor and memory peaks."""
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    blocks, iters = props.multi_processor_count * 8, 8192
+    sink = torch.empty(blocks * 256, dtype=torch.float32, device="cuda")
+    for _ in range(2):
+        binding.probe_ex2(blocks, iters, sink)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        binding.probe_ex2(blocks, iters, sink)
+    e1.record()
+    torch.cuda.synchronize()
+    binding.sync_status()
+    rate = blocks * 256 * iters * 8 * reps / (e0.elapsed_time(e1) / 1e3)
+    exps = (4 * wl.M if wl.feature == "favor" else 0) * wl.B * wl.H * wl.L
+    out = {"ex2_per_s": rate, "exps_per_step": exps, "ceiling_ms": exps / rate * 1e3,
+           "frac": exps / rate * 1e3 / ms_per_step,
+           "note": "informational: algorithmic exponentials (2M per token-head forward, 2M backward) at the "
+                   "measured rate of the exponential unit"}
+    if sm_mhz:
+        out["per_sm_per_clk"] = rate / (props.multi_processor_count * sm_mhz * 1e6)
+    return out
+
+
+def oracle_config_timings(names=("tiny", "l4k", "l1m", "elu16k"), max_rows=4096):
+    """The fp64 oracle on the host cores for the other configs, forward and
+    forward + backward, each on min(2 * cores, B*H) heads and the first
+    min(L, max_rows) rows, scaled to the full workload (heads are independent
+    and the recurrence is linear in L)."""
+    import oracle
+    from sub_linear_memory_gb300 import inputs
+
+    cores = len(os.sched_getaffinity(0))
+    out = {}
+    for name in names:
+        wl = inputs.WORKLOADS[name]
+        heads = min(2 * cores, wl.B * wl.H)
+        rows = min(wl.L, max_rows)
+        q, k, v, dy, w = inputs.make_inputs(wl.with_(L=rows), heads=(1, heads))
+        qn, kn, vn, dyn = (t.to(torch.float64).numpy() for t in (q, k, v, dy))
+        wn = None if w is None else w.to(torch.float64).numpy()
+        t0 = time.perf_counter()
+        oracle.recurrence_forward(qn, kn, vn, wn, threads=cores)
+        t1 = time.perf_counter()
+        oracle.recurrence_backward(qn, kn, vn, wn, dyn, threads=cores, want_dw=False)
+        t2 = time.perf_counter()
+        out[name] = {"fwd_tokens_per_s": tokens_per_s_from_sample(wl, t1 - t0, heads, rows, cores),
+                     "fwd_bwd_tokens_per_s": tokens_per_s_from_sample(wl, t2 - t0, heads, rows, cores),
+                     "cores": cores, "sample": "%d of %d heads x first %d of %d rows" % (heads, wl.B * wl.H, rows, wl.L)}
+    return out
+
+
 def run_native(args, wl):
     rank, world, local, dist = dist_setup(args.gpus)
     torch.cuda.set_device(local)
@@ -775,6 +846,14 @@ def run_native(args, wl):
         "kernels": {n: {"launches": c, "total_ms": t, "share": t / max(sum(x[1] for x in kernels.values()), 1e-12)}
                     for n, (c, t) in sorted(kernels.items(), key=lambda kv: -kv[1][1])},
     }
+    # hardware FLOPs: the algorithmic count plus what the kernels recompute
+    passes = kernels.get("tc_segment_state", (0, 0.0))[0] / max(args.steps, 1)
+    rec = recompute_flops_per_token_head(wl, passes)
+    line["step_roofline"]["hw_flops_per_token_head"] = work["fwd_flops"] + work["bwd_flops"] + rec
+    line["step_roofline"]["recompute_flops_per_token_head"] = rec
+    line["step_roofline"]["hw_tflops"] = (step_flops + rec * th) / (ms_per_step / 1e3) / 1e12
+    if rank == 0:
+        line["mufu"] = ex2_ceiling(binding, line["clocks"].get("sm_mhz"), wl, ms_per_step)
     if args.memory and rank == 0:
         del hq, hk, hv, hdy, hy, hdq, hdk, hdv, ins, outs
         line["memory"] = memory_sweep(binding, inputs)
@@ -791,6 +870,8 @@ def run_native(args, wl):
     if rank == 0 and world == 1 and args.cpu_baseline:
         base, parity = oracle_baseline_and_parity(wl, binding, dw is not None, args.cpu_row_frac)
         line["cpu_baseline"] = base
+        line["cpu_baseline_configs"] = oracle_config_timings(
+            tuple(n for n in ("tiny", "l4k", "l1m", "elu16k", "l32k") if n != wl.name))
         if parity is not None:
             line["parity"] = parity
     if rank == 0:

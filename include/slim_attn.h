@@ -355,6 +355,15 @@ slim_status slim_attn_sync_status(slim_stream_t stream);
  * no tensor memory, so giving up leaves nothing behind. */
 slim_status slim_attn_selftest_timeout(long long limit_ns, unsigned long long *waited_ns, slim_stream_t stream);
 
+/* Measurement helper (not part of the method): `blocks` CTAs of 256 threads,
+ * each thread iters x 8 dependent-in-eight-chains hardware 2^x evaluations
+ * (the exponential the FAVOR+ features use), nothing else of note, so the
+ * kernel runs at the exponential unit's rate.  Timing it gives that rate:
+ * blocks * 256 * iters * 8 evaluations.  sink: device memory for
+ * blocks * 256 floats (written, to keep the work live).  1 <= blocks <= 65535,
+ * 1 <= iters <= 2^20, else SLIM_ERR_INVALID_ARG. */
+slim_status slim_attn_probe_ex2(int blocks, int iters, float *sink, slim_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *slim_status_string(slim_status status);
 

@@ -87,6 +87,8 @@ _lib.slim_attn_fwd_noalloc.argtypes = _lib.slim_attn_fwd.argtypes
 _lib.slim_attn_fwd_noalloc.restype = _i
 _lib.slim_attn_selftest_timeout.argtypes = [ctypes.c_longlong, _vp, _vp]
 _lib.slim_attn_selftest_timeout.restype = _i
+_lib.slim_attn_probe_ex2.argtypes = [_i, _i, _vp, _vp]
+_lib.slim_attn_probe_ex2.restype = _i
 _lib.slim_status_string.argtypes = [_i]
 _lib.slim_status_string.restype = ctypes.c_char_p
 
@@ -104,7 +106,7 @@ EXPORTED = (
     "slim_attn_fwd_noalloc", "slim_attn_noalloc_bytes", "slim_attn_selftest_timeout",
     "slim_attn_fwd_carry", "slim_attn_bwd_carry", "slim_attn_fwd_carry_f32", "slim_attn_bwd_carry_f32",
     "slim_attn_copy_rows", "slim_attn_draw_orf", "slim_lm_param_count", "slim_lm_workspace_bytes",
-    "slim_lm_loss_grad", "slim_lm_checkpoint_bytes",
+    "slim_lm_loss_grad", "slim_lm_checkpoint_bytes", "slim_attn_probe_ex2",
 )
 
 
@@ -164,6 +166,15 @@ def selftest_timeout(limit_ns, waited=None, stream=None):
     s = torch.cuda.current_stream() if stream is None else stream
     _check(_lib.slim_attn_selftest_timeout(int(limit_ns), _ptr(waited), _vp(s.cuda_stream)),
            "slim_attn_selftest_timeout")
+
+
+def probe_ex2(blocks, iters, sink, stream=None):
+    """Launch the exponential-unit probe: blocks * 256 * iters * 8 hardware
+    2^x evaluations; ``sink`` is an fp32 CUDA tensor of blocks * 256 elements."""
+    if sink.dtype != torch.float32 or not sink.is_cuda or sink.numel() < blocks * 256:
+        raise ValueError("sink must be an fp32 CUDA tensor of blocks * 256 elements")
+    s = torch.cuda.current_stream() if stream is None else stream
+    _check(_lib.slim_attn_probe_ex2(int(blocks), int(iters), _ptr(sink), _vp(s.cuda_stream)), "slim_attn_probe_ex2")
 
 
 def sync_status(stream=None):

@@ -81,6 +81,14 @@ def test_workspace_registration_rules(lib):
     assert lib.slim_attn_set_option(1, -1) == 1
 
 
+def test_probe_ex2_rejects_bad_arguments_before_any_launch(lib):
+    vp = ctypes.c_void_p
+    assert lib.slim_attn_probe_ex2(0, 1, vp(256), None) == 1
+    assert lib.slim_attn_probe_ex2(1, 0, vp(256), None) == 1
+    assert lib.slim_attn_probe_ex2(1, 1 << 21, vp(256), None) == 1
+    assert lib.slim_attn_probe_ex2(1, 1, None, None) == 1
+
+
 def test_reuse_states_option(lib):
     """SLIM_OPT_REUSE_STATES takes 0 or 1 and changes no plan (no GPU needed)."""
     assert lib.slim_attn_set_option(5, 2) == 1
