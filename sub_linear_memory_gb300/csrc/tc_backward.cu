@@ -351,9 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // padding rows: F = 0 (zero-filled tile) and 2^-inf = 0
 #pragma unroll
-        for (int i = 0; i < QF; ++i) {
-          fk[i] = favor_feature(fk[i], ck);
-          fq[i] = favor_feature(fq[i], cq);
+        for (int i = 0; i < QF; i += 2) {
+          favor_feature2(fk[i], fk[i + 1], ck);
+          favor_feature2(fq[i], fq[i + 1], cq);
         }
 #pragma unroll
         for (int j = 0; j < QF / 8; ++j) {
@@ -755,9 +755,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ld_bf16x8(s_xq + sw128_offset(row, QD * part + 8 * j, kTile), xq);
         ld_bf16x8(s_xk + sw128_offset(row, QD * part + 8 * j, kTile), xk);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          oq[8 * j + i] = a[8 * j + i] - xq[i] * sq;
-          ok[8 * j + i] = b[8 * j + i] - xk[i] * sk;
+        for (int i = 0; i < 8; i += 2) {
+          const float2 q2 = __ffma2_rn(make_float2(-xq[i], -xq[i + 1]), make_float2(sq, sq),
+                                       make_float2(a[8 * j + i], a[8 * j + i + 1]));
+          const float2 k2 = __ffma2_rn(make_float2(-xk[i], -xk[i + 1]), make_float2(sk, sk),
+                                       make_float2(b[8 * j + i], b[8 * j + i + 1]));
+          oq[8 * j + i] = q2.x;
+          oq[8 * j + i + 1] = q2.y;
+          ok[8 * j + i] = k2.x;
+          ok[8 * j + i + 1] = k2.y;
         }
       }
       if (CS == 2) {

@@ -509,6 +509,13 @@ __device__ __forceinline__ float ex2_ftz(float x) {
 }
 
 __device__ __forceinline__ float favor_feature(float s, float c) { return ex2_ftz(fmaf(s, kLog2eF, c)); }
+// The same for two values: the two arguments in one packed fp32x2 FMA (each
+// rounded as fmaf rounds it), then two exponentials.
+__device__ __forceinline__ void favor_feature2(float &s0, float &s1, float c) {
+  const float2 t = __ffma2_rn(make_float2(s0, s1), make_float2(kLog2eF, kLog2eF), make_float2(c, c));
+  s0 = ex2_ftz(t.x);
+  s1 = ex2_ftz(t.y);
+}
 
 __device__ __forceinline__ float elu1_feature(float x) { return x > 0.f ? x + 1.f : __expf(x); }
 

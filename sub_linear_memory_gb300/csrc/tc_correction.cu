@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             arrive(B_FEMPTY + (j & 1));
 #pragma unroll
-            for (int x = 0; x < 32; ++x) v[x] = favor_feature(v[x], ck);
+            for (int x = 0; x < 32; x += 2) favor_feature2(v[x], v[x + 1], ck);
           } else {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -660,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float v[16];
       tmem_ld16(tmem_addr(tb, 32 * q4, kFD + QF * part + c), v);
 #pragma unroll
-      for (int x = 0; x < 16; ++x) v[x] = favor_feature(v[x], ck);
+      for (int x = 0; x < 16; x += 2) favor_feature2(v[x], v[x + 1], ck);
       st_bf16x8(s_ph + sw128_offset(row, QF * part + c, kTile), v);
       st_bf16x8(s_ph + sw128_offset(row, QF * part + c + 8, kTile), v + 8);
     }

@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             arrive(b_jempty);
             ++jobs;
 #pragma unroll
-            for (int x = 0; x < 64; ++x) v[x] = favor_feature(v[x], cr);
+            for (int x = 0; x < 64; x += 2) favor_feature2(v[x], v[x + 1], cr);
           } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
