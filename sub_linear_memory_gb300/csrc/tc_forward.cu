@@ -511,7 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // phi_q . S(t-1) needs S(t-1), written with the bf16 copy of R(t-1)
       if (side && !wait(F_RBFULL, i & 1)) break;
-      float dp[4] = {0.f, 0.f, 0.f, 0.f};
+      // dp[x & 3] sums of phi_q . S(t-1), as two packed pairs: (0, 1), (2, 3)
+      float2 dp[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       for (int h = 0; h < nb && ok; ++h) {
         const uint32_t c = (uint32_t)(i * nb + h);
         for (int half = 0; half < FB / 64; ++half) {
@@ -534,9 +535,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (side) {
-            const float *sh = ss + 128 * h + 64 * half;
+            const float2 *sh = reinterpret_cast<const float2 *>(ss + 128 * h + 64 * half);
 #pragma unroll
-            for (int x = 0; x < 64; ++x) dp[x & 3] = fmaf(v[x], sh[x], dp[x & 3]);
+            for (int x = 0; x < 64; x += 2)
+              dp[(x >> 1) & 1] = __ffma2_rn(make_float2(v[x], v[x + 1]), sh[x >> 1], dp[(x >> 1) & 1]);
           }
           if (half == 0 && c > 0 && !wait(b_free, (c - 1) & 1)) break;
 #pragma unroll
@@ -549,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (!FAVOR) arrive(F_EMPTY + s);
       if (side) {
-        den[(i & 1) * kTile + row] = (dp[0] + dp[1]) + (dp[2] + dp[3]);
+        den[(i & 1) * kTile + row] = (dp[0].x + dp[0].y) + (dp[1].x + dp[1].y);
         arrive(F_DEN + (i & 1));
       }
     }
