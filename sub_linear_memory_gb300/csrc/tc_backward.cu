@@ -423,7 +423,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld16x3(tmem_addr(tb, 32 * q4, kT + c), tmem_addr(tb, 32 * q4, kRhi + c),
                   tmem_addr(tb, 32 * q4, kRlo + c), x, h, l);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) df_add(h[i], l[i], -x[i]);
+      for (int i = 0; i < 16; i += 2) {
+        float2 h2 = make_float2(h[i], h[i + 1]), l2 = make_float2(l[i], l[i + 1]);
+        df_sub2(h2, l2, make_float2(x[i], x[i + 1]));
+        h[i] = h2.x;
+        h[i + 1] = h2.y;
+        l[i] = l2.x;
+        l[i + 1] = l2.y;
+      }
       tmem_st16(tmem_addr(tb, 32 * q4, kRhi + c), h);
       tmem_st16(tmem_addr(tb, 32 * q4, kRlo + c), l);
       if (row < MC) {
@@ -486,10 +493,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld16(tmem_addr(tb, 32 * q4, kT + QD * part), v);
 #pragma unroll
       for (int j = 0; j < QD / 8; ++j) ld_bf16x8(s_dy + sw128_offset(row, QD * part + 8 * j, kTile), g + 8 * j);
-      float dyy = 0.f;
+      float2 dyy2 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < QD; ++i) dyy = fmaf(g[i], v[i], dyy);
-      dot[part * kTile + row] = dyy;
+      for (int i = 0; i < QD; i += 2) dyy2 = __ffma2_rn(make_float2(g[i], g[i + 1]), make_float2(v[i], v[i + 1]), dyy2);
+      dot[part * kTile + row] = dyy2.x + dyy2.y;
       __syncthreads();
       float dsum = (dot[row] + dot[kTile + row]) + (dot[2 * kTile + row] + dot[3 * kTile + row]);
       float den = (asum[row] + asum[kTile + row]) + (asum[2 * kTile + row] + asum[3 * kTile + row]);
@@ -506,9 +513,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         den += rx[row];
         dsum += rx[kTile + row];
       }
-      const float inv = 1.0f / den;
+      const float inv = live ? 1.0f / den : 0.f;
 #pragma unroll
-      for (int i = 0; i < QD; ++i) g[i] = live ? g[i] * inv : 0.f;
+      for (int i = 0; i < QD; i += 2) {
+        const float2 gi = __fmul2_rn(make_float2(g[i], g[i + 1]), make_float2(inv, inv));
+        g[i] = gi.x;
+        g[i + 1] = gi.y;
+      }
 #pragma unroll
       for (int j = 0; j < QD / 8; ++j) st_bf16x8(s_dy + sw128_offset(row, QD * part + 8 * j, kTile), g + 8 * j);
       if (part == 0) {
@@ -541,7 +552,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         float a[32];
         tmem_ld32p16(tmem_addr(tb, 32 * q4, kT + 32 * part), tmem_addr(tb, 32 * q4, kX + QD * part), a, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) a[i] = (32 * part + i > row) ? 0.f : a[i] + dval;
+        for (int i = 0; i < 32; i += 2) {
+          const float2 ai = __fadd2_rn(make_float2(a[i], a[i + 1]), make_float2(dval, dval));
+          a[i] = (32 * part + i > row) ? 0.f : ai.x;
+          a[i + 1] = (32 * part + i + 1 > row) ? 0.f : ai.y;
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, 32 * part + 8 * j, kTile), a + 8 * j);
       }

@@ -555,6 +555,20 @@ __device__ __forceinline__ void df_add(float &hi, float &lo, float x) {
   lo = t - (hi - s);
 }
 
+// df_add(hi, lo, -x) for two values at once in packed fp32x2 arithmetic,
+// bit for bit: a - b is formed as fma(b, -1, a), which rounds the exact
+// difference once, as the subtraction does.
+__device__ __forceinline__ void df_sub2(float2 &hi, float2 &lo, float2 x) {
+  const float2 m1 = make_float2(-1.f, -1.f);
+  const float2 s = __ffma2_rn(x, m1, hi);                          // hi - x
+  const float2 bp = __ffma2_rn(hi, m1, s);                         // s - hi
+  const float2 e1 = __ffma2_rn(__ffma2_rn(bp, m1, s), m1, hi);     // hi - (s - bp)
+  const float2 e = __ffma2_rn(__fadd2_rn(x, bp), m1, e1);          // e1 + (-x - bp)
+  const float2 t = __fadd2_rn(lo, e);
+  hi = __fadd2_rn(s, t);
+  lo = __ffma2_rn(__ffma2_rn(s, m1, hi), m1, t);                   // t - (hi - s)
+}
+
 // Columns [c_lo, c_hi) (multiples of 16) of this warp's 32 lanes:
 // (hi, lo) += sign * delta, all three in TMEM.
 __device__ __forceinline__ void df_update_tmem(uint32_t tbase, int lane_base, uint32_t t_delta,

@@ -608,10 +608,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16 *yrow = p.y + ((size_t)bh * p.L + (size_t)t * kTile + row) * D;
       auto store_y = [&](int c0, const float *v, float inv) {
         uint4 *dst = reinterpret_cast<uint4 *>(yrow + c0);
+        const float2 inv2 = make_float2(inv, inv);
+        auto y2 = [&](int x) {
+          const float2 r = __fmul2_rn(make_float2(v[x], v[x + 1]), inv2);
+          return pack_bf16(r.x, r.y);
+        };
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          dst[k] = make_uint4(pack_bf16(v[8 * k] * inv, v[8 * k + 1] * inv), pack_bf16(v[8 * k + 2] * inv, v[8 * k + 3] * inv),
-                              pack_bf16(v[8 * k + 4] * inv, v[8 * k + 5] * inv), pack_bf16(v[8 * k + 6] * inv, v[8 * k + 7] * inv));
+        for (int k = 0; k < 4; ++k) dst[k] = make_uint4(y2(8 * k), y2(8 * k + 2), y2(8 * k + 4), y2(8 * k + 6));
       };
       const float rowsum_a = tmem_ld1(tmem_addr(tbase, lane_base, lay.t_num + D));
       if constexpr (D == 64) {
