@@ -403,13 +403,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       float v[32];
       tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * part), v);
-      float r4[4] = {0.f, 0.f, 0.f, 0.f};
+      // r4[i & 3] sums as two packed pairs: (0, 1), (2, 3)
+      float2 r4[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 32; i += 2) {
         if (32 * part + i > row) v[i] = 0.f;
-        r4[i & 3] += v[i];
+        if (32 * part + i + 1 > row) v[i + 1] = 0.f;
+        r4[(i >> 1) & 1] = __fadd2_rn(r4[(i >> 1) & 1], make_float2(v[i], v[i + 1]));
       }
-      asum[part * kTile + row] = (r4[0] + r4[1]) + (r4[2] + r4[3]);
+      asum[part * kTile + row] = (r4[0].x + r4[0].y) + (r4[1].x + r4[1].y);
 #pragma unroll
       for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, 32 * part + 8 * j, kTile), v + 8 * j);
     }
@@ -467,7 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // this thread's features of phi_q . S (S after eq. (19), fp32), added
       // to its part of rowsum(tril A) in its own slot
       const int c0 = QF * part;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      // acc[i & 3] sums as two packed pairs: (0, 1), (2, 3)
+      float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int j = 0; j < QF / 8; ++j) {
         float fq[8], sv[8];
@@ -475,9 +478,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<float4 *>(sv) = *reinterpret_cast<const float4 *>(s_f + c0 + 8 * j);
         *reinterpret_cast<float4 *>(sv + 4) = *reinterpret_cast<const float4 *>(s_f + c0 + 8 * j + 4);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i & 3] = fmaf(fq[i], sv[i], acc[i & 3]);
+        for (int i = 0; i < 8; i += 2)
+          acc[(i >> 1) & 1] = __ffma2_rn(make_float2(fq[i], fq[i + 1]), make_float2(sv[i], sv[i + 1]), acc[(i >> 1) & 1]);
       }
-      asum[part * kTile + row] += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+      asum[part * kTile + row] += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
     }
     // also while the MMAs run: the bf16 copy of G_V (G as the last tile
     // left it) into its tile, whose last reader (the previous dQ reduce-add

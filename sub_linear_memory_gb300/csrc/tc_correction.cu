@@ -399,11 +399,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           arrive(B_DEMPTY + (j & 1));
           const float *g = gs + 128 * h + col;
+          if (FAVOR) {
+            // feature pairs in packed fp32x2 arithmetic
+            const float2 *g2 = reinterpret_cast<const float2 *>(g);
 #pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            const float dk = dd[x] + g[x];
-            dd[x] = FAVOR ? v[x] * dk : dk * fminf(v[x], 1.f);
-            uk += dd[x];
+            for (int x = 0; x < 32; x += 2) {
+              const float2 u2 = __fmul2_rn(make_float2(v[x], v[x + 1]), __fadd2_rn(make_float2(dd[x], dd[x + 1]), g2[x >> 1]));
+              dd[x] = u2.x;
+              dd[x + 1] = u2.y;
+              uk += u2.x;
+              uk += u2.y;
+            }
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+              const float dk = dd[x] + g[x];
+              dd[x] = dk * fminf(v[x], 1.f);
+              uk += dd[x];
+            }
           }
           if (FAVOR) {
             // u as bf16 pairs into TMEM: feature f of the block -> column f / 2

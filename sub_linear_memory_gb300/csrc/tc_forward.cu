@@ -974,7 +974,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           float x[32], m[32];
           tmem_ld32x2(tmem_addr(tbase, lane_base, t_inc + b * NC + c), tmem_addr(tbase, lane_base, t_m + b * NC + c), x, m);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) m[e] += x[e];
+          for (int e = 0; e < 32; e += 2) {
+            const float2 s2 = __fadd2_rn(make_float2(m[e], m[e + 1]), make_float2(x[e], x[e + 1]));
+            m[e] = s2.x;
+            m[e + 1] = s2.y;
+          }
           tmem_st16(tmem_addr(tbase, lane_base, t_m + b * NC + c), m);
           tmem_st16(tmem_addr(tbase, lane_base, t_m + b * NC + c + 16), m + 16);
         }
