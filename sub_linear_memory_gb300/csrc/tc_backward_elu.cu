@@ -282,13 +282,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     {
       float v[32];
       tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * part), v);
-      float r4[4] = {0.f, 0.f, 0.f, 0.f};
+      // r4[i & 3] sums as two packed pairs: (0, 1), (2, 3)
+      float2 r4[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 32; i += 2) {
         if (32 * part + i > row) v[i] = 0.f;
-        r4[i & 3] += v[i];
+        if (32 * part + i + 1 > row) v[i + 1] = 0.f;
+        r4[(i >> 1) & 1] = __fadd2_rn(r4[(i >> 1) & 1], make_float2(v[i], v[i + 1]));
       }
-      asum[part * kTile + row] = (r4[0] + r4[1]) + (r4[2] + r4[3]);
+      asum[part * kTile + row] = (r4[0].x + r4[0].y) + (r4[1].x + r4[1].y);
 #pragma unroll
       for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, 32 * part + 8 * j, kTile), v + 8 * j);
     }
@@ -354,10 +356,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tmem_ld16(tmem_addr(tb, 32 * q4, kT + 16 * part), v);
 #pragma unroll
       for (int j = 0; j < 2; ++j) ld_bf16x8(s_dy + sw128_offset(row, cv + 16 * part + 8 * j, kTile), g + 8 * j);
-      float dyy = 0.f;
+      float2 dyy2 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) dyy = fmaf(g[i], v[i], dyy);
-      dot[part * kTile + row] = dyy;
+      for (int i = 0; i < 16; i += 2) dyy2 = __ffma2_rn(make_float2(g[i], g[i + 1]), make_float2(v[i], v[i + 1]), dyy2);
+      dot[part * kTile + row] = dyy2.x + dyy2.y;
     }
     __syncthreads();
     {
@@ -370,7 +372,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       go &= mbar_wait(x1_full, x_phase, p.status, abort_flag);
       // CTA 0 adds (own + peer), CTA 1 (peer + own): the same sum, a + b == b + a
       dsum = rank == 0 ? dsum + rx[row] : rx[row] + dsum;
-      const float inv = 1.0f / den;
+      const float inv = live ? 1.0f / den : 0.f;
       // dN = dY / den over all 128 columns, in place
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -378,7 +380,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t a = s_dy + sw128_offset(row, 32 * part + 8 * j, kTile);
         ld_bf16x8(a, g);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) g[i] = live ? g[i] * inv : 0.f;
+        for (int i = 0; i < 8; i += 2) {
+          const float2 gi = __fmul2_rn(make_float2(g[i], g[i + 1]), make_float2(inv, inv));
+          g[i] = gi.x;
+          g[i + 1] = gi.y;
+        }
         st_bf16x8(a, g);
       }
       if (part == 0) dd[row] = live ? -(dsum * inv) * inv : 0.f;

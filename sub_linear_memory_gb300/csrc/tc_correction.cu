@@ -479,7 +479,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           float xk[8];
           ld_bf16x8(s_k + sw128_offset(row, 8 * q, kTile), xk);
 #pragma unroll
-          for (int x = 0; x < 8; ++x) dk[8 * q + x] = fmaf(-xk[x], sk, dk[8 * q + x]);
+          for (int x = 0; x < 8; x += 2) {
+            const float2 r = __ffma2_rn(make_float2(-xk[x], -xk[x + 1]), make_float2(sk, sk),
+                                        make_float2(dk[8 * q + x], dk[8 * q + x + 1]));
+            dk[8 * q + x] = r.x;
+            dk[8 * q + x + 1] = r.y;
+          }
           st_bf16x8(s_k + sw128_offset(row, 8 * q, kTile), dk + 8 * q);
         }
       } else {
