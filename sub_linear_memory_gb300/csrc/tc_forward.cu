@@ -566,11 +566,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         uint32_t pk[64];
 #pragma unroll
-        for (int c0 = 0; c0 < kTile; c0 += 32) {
-          float v[32];
-          tmem_ld32(tmem_addr(tbase, lane_base, lay.t_a + c0), v);
+        for (int c0 = 0; c0 < kTile; c0 += 64) {
+          // two 32-column loads under one wait
+          float v[64];
+          tmem_ld32x2(tmem_addr(tbase, lane_base, lay.t_a + c0), tmem_addr(tbase, lane_base, lay.t_a + c0 + 32), v,
+                      v + 32);
 #pragma unroll
-          for (int x = 0; x < 32; x += 2)
+          for (int x = 0; x < 64; x += 2)
             pk[(c0 + x) >> 1] = pack_bf16(c0 + x > row ? 0.f : v[x], c0 + x + 1 > row ? 0.f : v[x + 1]);
         }
 #pragma unroll
