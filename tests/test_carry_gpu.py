@@ -181,3 +181,31 @@ def test_streamed_device_memory_does_not_grow_with_length(lib):
         del q, k, v, dy, qh, kh, vh, dyh, y, ckpt
     print("streamed peak device bytes at L = 2^15, 2^17:", peaks)
     assert peaks[1] <= peaks[0] + (1 << 20), peaks
+
+
+def test_streamed_long_sequence_matches_oracle_on_sampled_heads(lib):
+    """The 1M workload's head shape at L = 2^18 in pinned host memory, run in
+    2^16-row windows (the bench's streamed leg at a quarter of its shortest
+    length): Y, dQ, dK, dV and the last checkpoint of two heads against the
+    oracle's one pass (heads are independent, so a head is an exact unit)."""
+    from sub_linear_memory_gb300 import stream
+
+    wl = inputs.WORKLOADS["l1m"].with_(L=1 << 18, index=960)
+    q, k, v, dy, w = inputs.make_inputs(wl)
+    qh, kh, vh, dyh = (_pinned(t) for t in (q, k, v, dy))
+    wd = w.cuda()
+    window = 1 << 16
+    y, ckpt = stream.streamed_forward(qh, kh, vh, wd, wl.chunk, window)
+    dq, dk, dv, _ = stream.streamed_backward(qh, kh, vh, dyh, wd, wl.chunk, ckpt)
+    torch.cuda.synchronize()
+    lib.sync_status()
+    heads = [1, 6]
+    sel = lambda t: _np(t[:, heads])
+    qn, kn, vn, dyn, wn = sel(q), sel(k), sel(v), sel(dy), _np(w)
+    _check("Y", sel(y), oracle.recurrence_forward(qn, kn, vn, wn), 2e-2)
+    ref = oracle.recurrence_backward(qn, kn, vn, wn, dyn, want_dw=False)
+    for name, got, exp in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        _check(name, sel(got), exp, 2e-2)
+    last = ckpt.states.shape[0] - 1
+    exp = oracle.prefill_state(kn[:, :, :last * window], vn[:, :, :last * window], wn)
+    _check("checkpoint %d" % last, _np(ckpt.states[last][:, heads]), exp, 2e-2)

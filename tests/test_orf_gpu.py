@@ -154,3 +154,30 @@ def test_per_head_w_serving(dtype, lib):
     st_ref = np.concatenate([oracle.prefill_state(kn[:, h:h + 1, :L], vn[:, h:h + 1, :L], wn[h]) for h in range(H)],
                             axis=1)
     assert oracle.rel_l2(_np(prefill), st_ref) <= tol
+
+
+def test_per_head_w_full_size_l32k(lib):
+    """The l32k workload at full size with one W per head redrawn on the
+    device and dW per head, as the bench's per-head leg runs it: every
+    output of two heads (both batch entries of each, so dW per head is
+    complete) against the oracle."""
+    wl = inputs.WORKLOADS["l32k"]
+    q, k, v, dy, _ = (None if t is None else t.cuda() for t in inputs.make_inputs(wl))
+    w = lib.draw_orf(wl.H, wl.d, wl.M, seed=2024, step=5)
+    lib.set_option(lib.OPT_W_PER_HEAD, 1)
+    try:
+        y = lib.slim_attn_fwd(q, k, v, w, wl.chunk)
+        dq, dk, dv, dw = lib.slim_attn_bwd(q, k, v, w, dy, wl.chunk, want_dw=True)
+        lib.sync_status()
+    finally:
+        lib.set_option(lib.OPT_W_PER_HEAD, 0)
+    for h in (3, 12):
+        sel = lambda t: _np(t[:, h:h + 1])
+        qn, kn, vn, dyn, wn = sel(q), sel(k), sel(v), sel(dy), _np(w)[h:h + 1]
+        y_ref = oracle.recurrence_forward(qn, kn, vn, wn)
+        ref = oracle.recurrence_backward(qn, kn, vn, wn, dyn, want_dw=True)
+        for name, got, exp in (("Y", sel(y), y_ref), ("dQ", sel(dq), ref[0]), ("dK", sel(dk), ref[1]),
+                               ("dV", sel(dv), ref[2]), ("dW", _np(dw)[h:h + 1], ref[3])):
+            err = oracle.rel_l2(got, exp)
+            print("head %d %s rel L2 %.3e" % (h, name, err))
+            assert err <= 2e-2, (h, name, err)
