@@ -867,6 +867,14 @@ def run_native(args, wl):
         # the other configs, each timed outside the main region
         others = [n for n in ("l4k", "l1m", "elu16k", "l32k") if n != wl.name]
         line["workloads"] = workload_timings(binding, inputs, peaks, others)
+        # the serving decode step: 128 sequences of the l32k head shape
+        dwl = inputs.WORKLOADS["l32k"].with_(B=128)
+        d_ms, d_bytes, _ = decode_timing(binding, inputs, dwl, 50, 5)
+        d_gbs = d_bytes / (d_ms * 1e-3) / 1e9
+        line["decode"] = {"B": dwl.B, "H": dwl.H, "d": dwl.d, "M": dwl.M, "ms_per_step": d_ms,
+                          "tokens_per_s": dwl.B * 1e3 / d_ms, "bytes_per_step": d_bytes, "achieved_gbs": d_gbs,
+                          "frac": d_gbs / peaks["hbm_gbs"], "steps": 50,
+                          "note": "one new row for each of 128 sequences x 16 heads against the fp32 state in HBM"}
     if rank == 0 and world == 1 and args.cpu_baseline:
         base, parity = oracle_baseline_and_parity(wl, binding, dw is not None, args.cpu_row_frac)
         line["cpu_baseline"] = base
@@ -881,20 +889,17 @@ def run_native(args, wl):
     return 0
 
 
-def run_decode(args, wl):
+def decode_timing(binding, inputs, wl, steps, warmup, clock_gpu=None):
     """Serving step: one new row for every (sequence, head), against a state
     carried in HBM (fp32 [B][H][d + 1][M]); B sequences of H heads decode one
     token each per step.  The state (2 x 136 MB read and written per step at
-    128 x 16 heads, d = 64, M = 256) is larger than L2, so no flush is needed."""
-    import torch
-    from sub_linear_memory_gb300 import binding, inputs
-
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
+    128 x 16 heads, d = 64, M = 256) is larger than L2, so no flush is needed.
+    Returns (ms per step, bytes per step, clock summary or None)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
     b, h, d, m = wl.B, wl.H, wl.d, wl.M
     dtype = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     g = torch.Generator(device="cpu").manual_seed(4321)
-    nsteps = args.warmup + args.steps
+    nsteps = warmup + steps
     scale = 1.0 if wl.feature == "elu" else d ** -0.25
     qkv = (torch.randn((3, nsteps, b, h, d), generator=g) * torch.tensor([scale, scale, 1.0]).view(3, 1, 1, 1, 1))
     qkv = qkv.to(dev, dtype).contiguous()
@@ -906,21 +911,35 @@ def run_decode(args, wl):
     state = binding.slim_attn_state(kp, vp, w, wl.chunk)
     y = torch.empty((b, h, d), dtype=dtype, device=dev)
     del kp, vp
-    for i in range(args.warmup):
+    for i in range(warmup):
         binding.slim_attn_decode(qkv[0, i], qkv[1, i], qkv[2, i], w, state, y)
     binding.sync_status()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(0) as clk:
-        e0.record()
-        for i in range(args.warmup, nsteps):
-            binding.slim_attn_decode(qkv[0, i], qkv[1, i], qkv[2, i], w, state, y)
-        e1.record()
-        torch.cuda.synchronize()
+    clk = ClockSampler(clock_gpu) if clock_gpu is not None else None
+    if clk is not None:
+        clk.__enter__()
+    e0.record()
+    for i in range(warmup, nsteps):
+        binding.slim_attn_decode(qkv[0, i], qkv[1, i], qkv[2, i], w, state, y)
+    e1.record()
+    torch.cuda.synchronize()
+    if clk is not None:
+        clk.__exit__(None, None, None)
     binding.sync_status()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = e0.elapsed_time(e1) / steps
     s_io = 2 if dtype == torch.bfloat16 else 4
     nbytes = 2 * b * h * (d + 1) * m * 4 + 4 * b * h * d * s_io + (0 if w is None else d * m * 4)
+    del qkv, state, y
+    return ms, nbytes, (clk.summary() if clk is not None else None)
+
+
+def run_decode(args, wl):
+    from sub_linear_memory_gb300 import binding, inputs
+
+    torch.cuda.set_device(0)
+    ms, nbytes, clocks = decode_timing(binding, inputs, wl, args.steps, args.warmup, clock_gpu=0)
+    b, h, d, m = wl.B, wl.H, wl.d, wl.M
     peaks = load_peaks()
     gbs = nbytes / (ms * 1e-3) / 1e9
     out = {
@@ -930,7 +949,7 @@ def run_decode(args, wl):
         "dtype": "fp32 state, %s I/O" % wl.dtype, "data": "synthetic (seeded Gaussian rows, prefill of 256 rows)",
         "config": {"workload": "decode (%s head shape)" % wl.name, "B": b, "H": h, "d": d, "M": m,
                    "feature": wl.feature, "l2": "state larger than L2, no flush"},
-        "clocks": clk.summary(), "gpu_launches": args.steps,
+        "clocks": clocks, "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": "decode",
                      "bytes_per_step": nbytes},
