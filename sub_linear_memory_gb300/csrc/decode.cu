@@ -85,6 +85,12 @@ __global__ void __launch_bounds__(256) decode_kernel(const T *__restrict__ q, co
   }
   __syncthreads();
   const bool act = t < M;
+  // the first block of state rows is in flight while the features are formed
+  constexpr int kRows = 16;  // warp_sum16_transposed reduces 16 rows
+  float *st = state + (size_t)bh * (d + 1) * M;
+  float nxt[kRows];  // the next block, loaded before this block's stores
+#pragma unroll
+  for (int j = 0; j < kRows; ++j) nxt[j] = act ? st[(size_t)j * M + t] : 0.f;
   float phq = 0.f, phk = 0.f;
   if (act) {
     if (favor) {
@@ -110,11 +116,6 @@ __global__ void __launch_bounds__(256) decode_kernel(const T *__restrict__ q, co
   // next row's load would make each row wait a memory round trip), then the
   // row's term is added and the per-warp partials of g(q) . state[e] formed;
   // the S row (e = d) is loaded with the last block and handled after it
-  constexpr int kRows = 16;  // warp_sum16_transposed reduces 16 rows
-  float *st = state + (size_t)bh * (d + 1) * M;
-  float nxt[kRows];  // the next block, loaded before this block's stores
-#pragma unroll
-  for (int j = 0; j < kRows; ++j) nxt[j] = act ? st[(size_t)j * M + t] : 0.f;
   float srow = 0.f;
   for (int e0 = 0; e0 < d; e0 += kRows) {
     float cur[kRows];
