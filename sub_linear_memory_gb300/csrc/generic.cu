@@ -92,14 +92,14 @@ __device__ void causal_scores(const Plan &p, const float *phq, const float *phk,
 // den[l] = sum_j A[l][j] + phi_q[l] . S, then Y[l][e] = num[l][e] / den[l]
 // with num = A V + phi_q R^T (R' holds the state before this chunk).
 template <typename T>
-__device__ void chunk_outputs(const Plan &p, const float *A, const float *phq, const double *R,
+__device__ void chunk_outputs(const Plan &p, const float *A, const float *phq, const float *Rf,
                               const T *v, int rows, float *den, float *yc, T *y) {
   const int d = p.d, M = p.M, C = p.C;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   for (int l = warp; l < rows; l += kWarps) {
     float s = 0.f;
     for (int j = lane; j <= l; j += 32) s += A[(size_t)l * C + j];
-    for (int m = lane; m < M; m += 32) s = fmaf(phq[(size_t)l * M + m], (float)R[(size_t)d * M + m], s);
+    for (int m = lane; m < M; m += 32) s = fmaf(phq[(size_t)l * M + m], Rf[(size_t)d * M + m], s);
     s = warp_sum(s);
     if (lane == 0) den[l] = s;
   }
@@ -109,8 +109,8 @@ __device__ void chunk_outputs(const Plan &p, const float *A, const float *phq, c
     float num = 0.f;
     for (int j = 0; j <= l; ++j) num = fmaf(A[(size_t)l * C + j], to_f32(v[(size_t)j * d + e]), num);
     const float *a = phq + (size_t)l * M;
-    const double *r = R + (size_t)e * M;
-    for (int m = 0; m < M; ++m) num = fmaf(a[m], (float)r[m], num);
+    const float *r = Rf + (size_t)e * M;
+    for (int m = 0; m < M; ++m) num = fmaf(a[m], r[m], num);
     const float val = num / den[l];
     if (yc) yc[idx] = val;
     if (y) y[idx] = from_f32<T>(val);
@@ -210,11 +210,21 @@ __device__ void feature_backward(const Plan &p, const T *x, int rows, const floa
   }
 }
 
+// dst[i] = (float)src[i] over this CTA's share of n elements: the element
+// partition of state_add and reverse_state_add, so a thread converts only the
+// values it wrote itself.  The chunk's products read the fp32 copy: the same
+// values they took from the fp64 state before, converted once per element
+// instead of once per use (fp64 conversions are slow on this GPU).
+__device__ __forceinline__ void state_to_f32(const double *src, float *dst, int n) {
+  for (int idx = threadIdx.x; idx < n; idx += kThreads) dst[idx] = (float)src[idx];
+}
+
 // ---- kernels ------------------------------------------------------------
 
 struct FwdScratch {
   double *R;
   float *phq, *phk, *A, *yc, *dNp;
+  float *Rf;  // fp32 copy of R for the chunk's products (one conversion per element)
 };
 
 // Master states are fp64: a state of dp x M numbers takes 2 * dp * M floats.
@@ -226,6 +236,7 @@ __device__ __forceinline__ FwdScratch fwd_scratch(const Plan &p, float *base) {
   s.A = s.phk + align_floats((size_t)p.C * p.M);
   s.yc = s.A + align_floats((size_t)p.C * p.C);
   s.dNp = s.yc + align_floats((size_t)p.C * p.d);
+  s.Rf = s.dNp + align_floats((size_t)p.C * p.dp);
   return s;
 }
 
@@ -325,8 +336,9 @@ __global__ void __launch_bounds__(kThreads) forward_kernel(Plan p, Args a) {
     feature_rows(p, k, ch.rows, head_w(p, a, bh), den, sc.phk);
     __syncthreads();
     causal_scores(p, sc.phq, sc.phk, ch.rows, sc.A);
+    state_to_f32(sc.R, sc.Rf, p.dp * p.M);
     __syncthreads();
-    chunk_outputs(p, sc.A, sc.phq, sc.R, v, ch.rows, den, (float *)nullptr, y);
+    chunk_outputs(p, sc.A, sc.phq, sc.Rf, v, ch.rows, den, (float *)nullptr, y);
     __syncthreads();
     state_add(p, sc.R, sc.phk, v, ch.rows, 1.f);
     __syncthreads();
@@ -366,8 +378,9 @@ __global__ void __launch_bounds__(kThreads) segment_dg_kernel(Plan p, Args a) {
     feature_rows(p, k, ch.rows, head_w(p, a, bh), den, sc.phk);
     __syncthreads();
     causal_scores(p, sc.phq, sc.phk, ch.rows, sc.A);
+    state_to_f32(sc.R, sc.Rf, p.dp * p.M);
     __syncthreads();
-    chunk_outputs(p, sc.A, sc.phq, sc.R, v, ch.rows, den, sc.yc, (T *)nullptr);
+    chunk_outputs(p, sc.A, sc.phq, sc.Rf, v, ch.rows, den, sc.yc, (T *)nullptr);
     __syncthreads();
     output_grads(p, dy, sc.yc, den, ch.rows, sc.dNp);
     __syncthreads();
@@ -380,6 +393,7 @@ __global__ void __launch_bounds__(kThreads) segment_dg_kernel(Plan p, Args a) {
 struct BwdScratch {
   double *R, *G;
   float *phq, *phk, *dphq, *dphk, *A, *dA, *dNp, *yc;
+  float *Rf, *Gf;  // fp32 copies of R and G for the chunk's products
 };
 
 __device__ __forceinline__ BwdScratch bwd_scratch(const Plan &p, float *base) {
@@ -396,6 +410,8 @@ __device__ __forceinline__ BwdScratch bwd_scratch(const Plan &p, float *base) {
   s.dA = s.A + cc;
   s.dNp = s.dA + cc;
   s.yc = s.dNp + align_floats((size_t)p.C * p.dp);
+  s.Rf = s.yc + align_floats((size_t)p.C * p.d);
+  s.Gf = s.Rf + align_floats((size_t)p.dp * p.M);
   return s;
 }
 
@@ -424,6 +440,7 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(Plan p, Args a) {
   for (int i = threadIdx.x; i < dp * M; i += kThreads) {
     sc.R[i] = Rend[i];
     sc.G[i] = Gend ? Gend[i] : (Gc ? (double)Gc[i] : 0.0);
+    sc.Gf[i] = (float)sc.G[i];
   }
   if (dwp)
     for (int i = threadIdx.x; i < d * M; i += kThreads) dwp[i] = 0.f;
@@ -445,9 +462,10 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(Plan p, Args a) {
     feature_rows(p, k, rows, head_w(p, a, bh), sk, sc.phk);
     __syncthreads();
     state_add(p, sc.R, sc.phk, v, rows, -1.f);  // eq. (19): state before this chunk
+    state_to_f32(sc.R, sc.Rf, dp * M);
     causal_scores(p, sc.phq, sc.phk, rows, sc.A);
     __syncthreads();
-    chunk_outputs(p, sc.A, sc.phq, sc.R, v, rows, den, sc.yc, (T *)nullptr);
+    chunk_outputs(p, sc.A, sc.phq, sc.Rf, v, rows, den, sc.yc, (T *)nullptr);
     __syncthreads();
     output_grads(p, dy, sc.yc, den, rows, sc.dNp);
     __syncthreads();
@@ -467,12 +485,12 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(Plan p, Args a) {
       // dg(Q_r)_m = sum_{j<=r} dA[r][j] g(K_j)_m + sum_e dN'[r][e] R'[e][m]
       float t = 0.f;
       for (int j = 0; j <= r; ++j) t = fmaf(sc.dA[(size_t)r * C + j], sc.phk[(size_t)j * M + m], t);
-      for (int e = 0; e < dp; ++e) t = fmaf(sc.dNp[(size_t)r * dp + e], (float)sc.R[(size_t)e * M + m], t);
+      for (int e = 0; e < dp; ++e) t = fmaf(sc.dNp[(size_t)r * dp + e], sc.Rf[(size_t)e * M + m], t);
       sc.dphq[idx] = t;
       // dg(K_r)_m = sum_{l>=r} dA[l][r] g(Q_l)_m + sum_e V'[r][e] G[e][m]
-      float u = (float)sc.G[(size_t)d * M + m];
+      float u = sc.Gf[(size_t)d * M + m];
       for (int l = r; l < rows; ++l) u = fmaf(sc.dA[(size_t)l * C + r], sc.phq[(size_t)l * M + m], u);
-      for (int e = 0; e < d; ++e) u = fmaf(to_f32(v[(size_t)r * d + e]), (float)sc.G[(size_t)e * M + m], u);
+      for (int e = 0; e < d; ++e) u = fmaf(to_f32(v[(size_t)r * d + e]), sc.Gf[(size_t)e * M + m], u);
       sc.dphk[idx] = u;
     }
     // dV[j][e] = sum_{l>=j} A[l][j] dN[l][e] + sum_m G[e][m] g(K_j)_m
@@ -480,13 +498,14 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(Plan p, Args a) {
       const int j = idx / d, e = idx - j * d;
       float t = 0.f;
       for (int l = j; l < rows; ++l) t = fmaf(sc.A[(size_t)l * C + j], sc.dNp[(size_t)l * dp + e], t);
-      const double *g = sc.G + (size_t)e * M;
+      const float *g = sc.Gf + (size_t)e * M;
       const float *f = sc.phk + (size_t)j * M;
-      for (int m = 0; m < M; ++m) t = fmaf((float)g[m], f[m], t);
+      for (int m = 0; m < M; ++m) t = fmaf(g[m], f[m], t);
       dv[idx] = from_f32<T>(t);
     }
     __syncthreads();
     reverse_state_add(p, sc.G, sc.dNp, sc.phq, rows);  // eq. (20)
+    state_to_f32(sc.G, sc.Gf, dp * M);  // for the next chunk (read after the barriers below)
     feature_backward(p, q, rows, head_w(p, a, bh), sc.phq, sc.dphq, sq, dq, dwp);
     __syncthreads();
     feature_backward(p, k, rows, head_w(p, a, bh), sc.phk, sc.dphk, sk, dk, dwp);
@@ -628,8 +647,9 @@ size_t generic_scratch_floats(const Plan &p, bool bwd) {
   const size_t st = align_floats((size_t)2 * p.dp * p.M), cm = align_floats((size_t)p.C * p.M);
   const size_t cc = align_floats((size_t)p.C * p.C);
   const size_t cd = align_floats((size_t)p.C * p.d), cdp = align_floats((size_t)p.C * p.dp);
-  if (!bwd) return st + 2 * cm + cc + cd + cdp;
-  return 2 * st + 4 * cm + 2 * cc + cdp + cd;
+  const size_t sf = align_floats((size_t)p.dp * p.M);  // fp32 copies of the states
+  if (!bwd) return st + 2 * cm + cc + cd + cdp + sf;
+  return 2 * st + 4 * cm + 2 * cc + cdp + cd + 2 * sf;
 }
 
 namespace gen {

@@ -315,6 +315,7 @@ int grid_for(long long n) { return (int)std::min<long long>((n + 255) / 256, 819
 void gemm(cudaStream_t st, int m, int n, int k, const float *A, long long sam, long long sak, const float *B,
           long long sbk, long long sbn, float *C, long long ldc, float beta, const float *bias = nullptr) {
   const dim3 grid((n + 63) / 64, (m + 63) / 64);
+  ProfScope ps("lm_gemm", st);
   sgemm_kernel<<<grid, 256, 0, st>>>(m, n, k, A, sam, sak, B, sbk, sbn, C, ldc, beta, bias);
 }
 
