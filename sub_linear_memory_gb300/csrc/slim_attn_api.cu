@@ -134,7 +134,14 @@ int device_sms() {
 // tail_w: work outside the main kernel that covers the rows of segments
 // 0 .. P-2, in main-kernel tile times per tile and SM (the backward's
 // correction of dK, dV by the later segments' reverse state).
-void choose_segments(Plan &p, int requested, int units, int tensor_path, int cta_per_seg, double tail_w) {
+// fwd_model: the tensor-path forward, whose segments each cost about two
+// tiles' time more than their tiles (prologue, state and W loads, pipeline
+// fill and drain), and whose segment-state pass runs segments 0 .. P-2 at
+// about 0.4 of a forward tile per tile, with the same overhead.  Measured on
+// the GB300: forward l4k 0.114 / 0.127 / 0.163 / 0.248 ms at P = 4 / 8 / 16 /
+// 32 (the model's order and ratios within 5%), l32k best at P = 19.
+void choose_segments(Plan &p, int requested, int units, int tensor_path, int cta_per_seg, double tail_w,
+                     bool fwd_model = false) {
   const int sms = device_sms();
   const int bh = std::max(p.BH, 1);
   int P;
@@ -150,8 +157,12 @@ void choose_segments(Plan &p, int requested, int units, int tensor_path, int cta
       const int cps = (units + cand - 1) / cand;
       const int segs = (units + cps - 1) / cps;
       const long long waves = ((long long)segs * bh * cta_per_seg + sms - 1) / sms;
-      const double span = (double)(waves * cps) +
-                          tail_w * (double)(segs - 1) / segs * (double)units * bh / sms;
+      double span = (double)(waves * cps) + tail_w * (double)(segs - 1) / segs * (double)units * bh / sms;
+      if (fwd_model) {
+        constexpr double kSegOverhead = 2.0, kStateTile = 0.4;
+        const long long waves_s = ((long long)(segs - 1) * bh + sms - 1) / sms;
+        span = (double)waves * (cps + kSegOverhead) + kStateTile * (double)waves_s * (cps + kSegOverhead);
+      }
       if (best < 0.0 || span < best - 1e-9) {
         best = span;
         P = segs;
@@ -181,7 +192,8 @@ Plan make_plan(int B, int H, int L, int d, int M, int chunk, bool favor, bool bw
   // the tensor backward's correction pass: measured about a third of a
   // backward tile's time per tile and SM (l32k: 4.5 us against 13.2 us)
   const double tail_w = (path == 2 && bwd) ? 0.35 : 0.0;
-  choose_segments(p, g_opt_segments, path == 2 ? p.tc_tiles : p.nchunks, path == 2, cta_per_seg, tail_w);
+  choose_segments(p, g_opt_segments, path == 2 ? p.tc_tiles : p.nchunks, path == 2, cta_per_seg, tail_w,
+                  path == 2 && !bwd);
   // master states: fp64 on the CUDA-core path; double-float (hi, lo) fp32
   // pairs on the tensor path, whose reverse states are plain fp32
   const size_t state = (path == 2 ? 1 : 2) * (size_t)p.BH * p.P * p.dp * p.M;
