@@ -93,7 +93,9 @@ typedef enum {
   SLIM_OPT_W_PER_HEAD = 4,
   /* Forward-to-backward reuse of the boundary states (section 3.2 keeps only
    * the states at the slice boundaries; section 3.3 rebuilds the rest from
-   * them): 0 = off (the default), 1 = on.  When on, slim_attn_fwd on the
+   * them): 0 = off (the default), 1 = on.  When on, the tensor-core
+   * backward at d = 64 plans the forward's segments when its own cost model
+   * puts them within 10% of its best plan, and slim_attn_fwd on the
    * tensor-core path at d = 64 (bf16 I/O), when its segments are the ones the
    * backward of the same shape uses, leaves the exact end state of each
    * segment in the registered workspace and tags it with k, v, w, the shape

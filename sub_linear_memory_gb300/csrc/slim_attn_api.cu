@@ -140,6 +140,18 @@ int device_sms() {
 // about 0.4 of a forward tile per tile, with the same overhead.  Measured on
 // the GB300: forward l4k 0.114 / 0.127 / 0.163 / 0.248 ms at P = 4 / 8 / 16 /
 // 32 (the model's order and ratios within 5%), l32k best at P = 19.
+// Makespan, in main-kernel tile times, of the tensor path cut into `segs`
+// segments of `cps` units (the model choose_segments minimises).
+double plan_span(int segs, int cps, int units, int bh, int cta_per_seg, double tail_w, bool fwd_model, int sms) {
+  const long long waves = ((long long)segs * bh * cta_per_seg + sms - 1) / sms;
+  if (fwd_model) {
+    constexpr double kSegOverhead = 2.0, kStateTile = 0.4;
+    const long long waves_s = ((long long)(segs - 1) * bh + sms - 1) / sms;
+    return (double)waves * (cps + kSegOverhead) + kStateTile * (double)waves_s * (cps + kSegOverhead);
+  }
+  return (double)(waves * cps) + tail_w * (double)(segs - 1) / segs * (double)units * bh / sms;
+}
+
 void choose_segments(Plan &p, int requested, int units, int tensor_path, int cta_per_seg, double tail_w,
                      bool fwd_model = false) {
   const int sms = device_sms();
@@ -156,13 +168,7 @@ void choose_segments(Plan &p, int requested, int units, int tensor_path, int cta
     for (int cand = 1; cand <= std::min(units, cap); ++cand) {
       const int cps = (units + cand - 1) / cand;
       const int segs = (units + cps - 1) / cps;
-      const long long waves = ((long long)segs * bh * cta_per_seg + sms - 1) / sms;
-      double span = (double)(waves * cps) + tail_w * (double)(segs - 1) / segs * (double)units * bh / sms;
-      if (fwd_model) {
-        constexpr double kSegOverhead = 2.0, kStateTile = 0.4;
-        const long long waves_s = ((long long)(segs - 1) * bh + sms - 1) / sms;
-        span = (double)waves * (cps + kSegOverhead) + kStateTile * (double)waves_s * (cps + kSegOverhead);
-      }
+      const double span = plan_span(segs, cps, units, bh, cta_per_seg, tail_w, fwd_model, sms);
       if (best < 0.0 || span < best - 1e-9) {
         best = span;
         P = segs;
@@ -174,7 +180,6 @@ void choose_segments(Plan &p, int requested, int units, int tensor_path, int cta
   p.P = (units + p.cps - 1) / p.cps;
 }
 
-// path: 1 = CUDA-core kernels, 2 = tensor-core kernels.
 Plan make_plan(int B, int H, int L, int d, int M, int chunk, bool favor, bool bwd, bool want_dw,
                int path = 1) {
   Plan p{};
@@ -194,6 +199,24 @@ Plan make_plan(int B, int H, int L, int d, int M, int chunk, bool favor, bool bw
   const double tail_w = (path == 2 && bwd) ? 0.35 : 0.0;
   choose_segments(p, g_opt_segments, path == 2 ? p.tc_tiles : p.nchunks, path == 2, cta_per_seg, tail_w,
                   path == 2 && !bwd);
+  // SLIM_OPT_REUSE_STATES: a tensor backward at d = 64 takes the forward's
+  // segments when its own model puts them within 10% of its best, so that it
+  // can read the forward's states (the state pass it skips is about a tenth of
+  // its time; l32k measured 2.026 ms per step that way against 2.061 with
+  // its own 7 segments and the forward's 9)
+  if (path == 2 && bwd && d == 64 && g_opt_reuse_states && g_opt_segments == 0) {
+    Plan f = p;
+    choose_segments(f, 0, p.tc_tiles, 1, 1, 0.0, true);
+    if (f.P != p.P) {
+      const int sms = device_sms(), bh = std::max(p.BH, 1);
+      const double own = plan_span(p.P, p.cps, p.tc_tiles, bh, cta_per_seg, tail_w, false, sms);
+      const double theirs = plan_span(f.P, f.cps, p.tc_tiles, bh, cta_per_seg, tail_w, false, sms);
+      if (theirs <= 1.1 * own) {
+        p.P = f.P;
+        p.cps = f.cps;
+      }
+    }
+  }
   // master states: fp64 on the CUDA-core path; double-float (hi, lo) fp32
   // pairs on the tensor path, whose reverse states are plain fp32
   const size_t state = (path == 2 ? 1 : 2) * (size_t)p.BH * p.P * p.dp * p.M;

@@ -90,7 +90,8 @@ def test_probe_ex2_rejects_bad_arguments_before_any_launch(lib):
 
 
 def test_reuse_states_option(lib):
-    """SLIM_OPT_REUSE_STATES takes 0 or 1 and changes no plan (no GPU needed)."""
+    """SLIM_OPT_REUSE_STATES takes 0 or 1; it leaves the forward's plan alone
+    (the backward may take the forward's segments), no GPU needed."""
     assert lib.slim_attn_set_option(5, 2) == 1
     assert lib.slim_attn_set_option(5, -1) == 1
     shape = (2, 16, 32768, 64, 256, 128)
@@ -100,7 +101,7 @@ def test_reuse_states_option(lib):
         on = [lib.slim_attn_workspace_bytes(*shape, b) for b in (0, 1)]
     finally:
         assert lib.slim_attn_set_option(5, 0) == 0
-    assert on == off and min(off) > 0
+    assert on[0] == off[0] and min(off + on) > 0
 
 
 def test_workspace_does_not_grow_with_sequence_length(lib):
