@@ -326,7 +326,9 @@ slim_status slim_attn_set_workspace(void *ptr, size_t bytes);
 /* Process-wide tuning / testing knobs (see slim_option). */
 slim_status slim_attn_set_option(int option, int value);
 
-/* Segments per (b, h) that a call with this shape uses on the current device. */
+/* Segments per (b, h) that slim_attn_fwd (bf16 I/O, aligned tensors) plans
+ * for this shape on the current device: the tensor-core plan where the shape
+ * has a tensor-core forward, else the CUDA-core plan. */
 int slim_attn_segments(int B, int H, int L, int d, int M, int chunk);
 
 /* Per-kernel profile (SLIM_OPT_PROFILE): waits for every recorded event,

@@ -626,7 +626,9 @@ slim_status slim_attn_set_option(int option, int value) {
 int slim_attn_segments(int B, int H, int L, int d, int M, int chunk) {
   if (slim::check_shape(B, H, L, d, M, chunk, true) != SLIM_OK) return 0;
   if ((long long)B * H * L == 0) return 0;
-  return slim::make_plan(B, H, L, d, M, chunk, true, false, false).P;
+  // the bf16 forward's plan: the tensor path where either feature map has it
+  const bool tc = slim::tc_forward_supported(d, M, chunk, true) || slim::tc_forward_supported(d, M, chunk, false);
+  return slim::make_plan(B, H, L, d, M, chunk, true, false, false, tc ? 2 : 1).P;
 }
 
 int slim_attn_profile_count(void) {
