@@ -25,6 +25,38 @@ __device__ __forceinline__ float warp_sum(float s) {
   return s;
 }
 
+// sum over i < n of a[i sa] b[i sb] (plus init) with four independent
+// accumulators: the dependent FMA chain is a quarter as long, which is what
+// bounds these per-thread loops.  The additions' order is not the plain
+// loop's; the result moves within fp32 rounding.
+template <typename TA, typename TB>
+__device__ __forceinline__ float dot4(const TA *a, long long sa, const TB *b, long long sb, int n, float init = 0.f) {
+  float s0 = init, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+  int i = 0;
+  for (; i + 4 <= n; i += 4) {
+    s0 = fmaf(to_f32(a[(long long)i * sa]), to_f32(b[(long long)i * sb]), s0);
+    s1 = fmaf(to_f32(a[(long long)(i + 1) * sa]), to_f32(b[(long long)(i + 1) * sb]), s1);
+    s2 = fmaf(to_f32(a[(long long)(i + 2) * sa]), to_f32(b[(long long)(i + 2) * sb]), s2);
+    s3 = fmaf(to_f32(a[(long long)(i + 3) * sa]), to_f32(b[(long long)(i + 3) * sb]), s3);
+  }
+  for (; i < n; ++i) s0 = fmaf(to_f32(a[(long long)i * sa]), to_f32(b[(long long)i * sb]), s0);
+  return (s0 + s1) + (s2 + s3);
+}
+
+// sum over i < n of a[i sa], four accumulators likewise.
+__device__ __forceinline__ float sum4(const float *a, long long sa, int n) {
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+  int i = 0;
+  for (; i + 4 <= n; i += 4) {
+    s0 += a[(long long)i * sa];
+    s1 += a[(long long)(i + 1) * sa];
+    s2 += a[(long long)(i + 2) * sa];
+    s3 += a[(long long)(i + 3) * sa];
+  }
+  for (; i < n; ++i) s0 += a[(long long)i * sa];
+  return (s0 + s1) + (s2 + s3);
+}
+
 struct Chunk {
   int row0, rows;
 };
@@ -63,8 +95,7 @@ __device__ void feature_rows(const Plan &p, const T *x, int rows, const float *w
     const T *xr = x + (size_t)r * d;
     float f;
     if (p.favor) {
-      float dot = 0.f;
-      for (int i = 0; i < d; ++i) dot = fmaf(to_f32(xr[i]), w[(size_t)i * M + m], dot);
+      const float dot = dot4(xr, 1, w + m, M, d);
       f = expf(dot - 0.5f * sq[r]) * inv_sqrt_m;
     } else {
       const float t = to_f32(xr[m]);
@@ -80,11 +111,7 @@ __device__ void causal_scores(const Plan &p, const float *phq, const float *phk,
   const int M = p.M, C = p.C;
   for (int idx = threadIdx.x; idx < rows * rows; idx += kThreads) {
     const int l = idx / rows, j = idx - l * rows;
-    float s = 0.f;
-    if (j <= l) {
-      const float *a = phq + (size_t)l * M, *b = phk + (size_t)j * M;
-      for (int m = 0; m < M; ++m) s = fmaf(a[m], b[m], s);
-    }
+    const float s = j <= l ? dot4(phq + (size_t)l * M, 1, phk + (size_t)j * M, 1, M) : 0.f;
     A[(size_t)l * C + j] = s;
   }
 }
@@ -106,11 +133,8 @@ __device__ void chunk_outputs(const Plan &p, const float *A, const float *phq, c
   __syncthreads();
   for (int idx = threadIdx.x; idx < rows * d; idx += kThreads) {
     const int l = idx / d, e = idx - l * d;
-    float num = 0.f;
-    for (int j = 0; j <= l; ++j) num = fmaf(A[(size_t)l * C + j], to_f32(v[(size_t)j * d + e]), num);
-    const float *a = phq + (size_t)l * M;
-    const float *r = Rf + (size_t)e * M;
-    for (int m = 0; m < M; ++m) num = fmaf(a[m], r[m], num);
+    float num = dot4(A + (size_t)l * C, 1, v + e, d, l + 1);
+    num = dot4(phq + (size_t)l * M, 1, Rf + (size_t)e * M, 1, M, num);
     const float val = num / den[l];
     if (yc) yc[idx] = val;
     if (y) y[idx] = from_f32<T>(val);
@@ -128,12 +152,7 @@ __device__ void state_add(const Plan &p, double *R, const float *phk, const T *v
   const int d = p.d, M = p.M, dp = p.dp;
   for (int idx = threadIdx.x; idx < dp * M; idx += kThreads) {
     const int e = idx / M, m = idx - e * M;
-    float s = 0.f;
-    if (e < d) {
-      for (int j = 0; j < rows; ++j) s = fmaf(to_f32(v[(size_t)j * d + e]), phk[(size_t)j * M + m], s);
-    } else {
-      for (int j = 0; j < rows; ++j) s += phk[(size_t)j * M + m];
-    }
+    const float s = e < d ? dot4(v + e, d, phk + m, M, rows) : sum4(phk + m, M, rows);
     R[idx] += (double)(sign * s);
   }
 }
@@ -163,8 +182,7 @@ __device__ void reverse_state_add(const Plan &p, double *G, const float *dNp, co
   const int M = p.M, dp = p.dp;
   for (int idx = threadIdx.x; idx < dp * M; idx += kThreads) {
     const int e = idx / M, m = idx - e * M;
-    float s = 0.f;
-    for (int l = 0; l < rows; ++l) s = fmaf(dNp[(size_t)l * dp + e], phq[(size_t)l * M + m], s);
+    const float s = dot4(dNp + e, dp, phq + m, M, rows);
     G[idx] += (double)s;
   }
 }
@@ -195,17 +213,13 @@ __device__ void feature_backward(const Plan &p, const T *x, int rows, const floa
   __syncthreads();
   for (int idx = threadIdx.x; idx < rows * d; idx += kThreads) {
     const int r = idx / d, i = idx - r * d;
-    const float *u = dphi + (size_t)r * M, *wi = w + (size_t)i * M;
-    float s = 0.f;
-    for (int m = 0; m < M; ++m) s = fmaf(wi[m], u[m], s);
+    const float s = dot4(w + (size_t)i * M, 1, dphi + (size_t)r * M, 1, M);
     dx[idx] = from_f32<T>(s - to_f32(x[idx]) * usum[r]);
   }
   if (dwp) {
     for (int idx = threadIdx.x; idx < d * M; idx += kThreads) {
       const int i = idx / M, m = idx - i * M;
-      float s = 0.f;
-      for (int r = 0; r < rows; ++r) s = fmaf(to_f32(x[(size_t)r * d + i]), dphi[(size_t)r * M + m], s);
-      dwp[idx] += s;
+      dwp[idx] += dot4(x + i, d, dphi + m, M, rows);
     }
   }
 }
@@ -472,35 +486,26 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(Plan p, Args a) {
     // dA[l][j] = dN'_l . V'_j for j <= l
     for (int idx = threadIdx.x; idx < rows * rows; idx += kThreads) {
       const int l = idx / rows, j = idx - l * rows;
-      float t = 0.f;
-      if (j <= l) {
-        t = sc.dNp[(size_t)l * dp + d];
-        for (int e = 0; e < d; ++e) t = fmaf(sc.dNp[(size_t)l * dp + e], to_f32(v[(size_t)j * d + e]), t);
-      }
+      const float t = j <= l ? dot4(sc.dNp + (size_t)l * dp, 1, v + (size_t)j * d, 1, d, sc.dNp[(size_t)l * dp + d]) : 0.f;
       sc.dA[(size_t)l * C + j] = t;
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < rows * M; idx += kThreads) {
       const int r = idx / M, m = idx - r * M;
       // dg(Q_r)_m = sum_{j<=r} dA[r][j] g(K_j)_m + sum_e dN'[r][e] R'[e][m]
-      float t = 0.f;
-      for (int j = 0; j <= r; ++j) t = fmaf(sc.dA[(size_t)r * C + j], sc.phk[(size_t)j * M + m], t);
-      for (int e = 0; e < dp; ++e) t = fmaf(sc.dNp[(size_t)r * dp + e], sc.Rf[(size_t)e * M + m], t);
+      float t = dot4(sc.dA + (size_t)r * C, 1, sc.phk + m, M, r + 1);
+      t = dot4(sc.dNp + (size_t)r * dp, 1, sc.Rf + m, M, dp, t);
       sc.dphq[idx] = t;
       // dg(K_r)_m = sum_{l>=r} dA[l][r] g(Q_l)_m + sum_e V'[r][e] G[e][m]
-      float u = sc.Gf[(size_t)d * M + m];
-      for (int l = r; l < rows; ++l) u = fmaf(sc.dA[(size_t)l * C + r], sc.phq[(size_t)l * M + m], u);
-      for (int e = 0; e < d; ++e) u = fmaf(to_f32(v[(size_t)r * d + e]), sc.Gf[(size_t)e * M + m], u);
+      float u = dot4(sc.dA + (size_t)r * C + r, C, sc.phq + (size_t)r * M + m, M, rows - r, sc.Gf[(size_t)d * M + m]);
+      u = dot4(v + (size_t)r * d, 1, sc.Gf + m, M, d, u);
       sc.dphk[idx] = u;
     }
     // dV[j][e] = sum_{l>=j} A[l][j] dN[l][e] + sum_m G[e][m] g(K_j)_m
     for (int idx = threadIdx.x; idx < rows * d; idx += kThreads) {
       const int j = idx / d, e = idx - j * d;
-      float t = 0.f;
-      for (int l = j; l < rows; ++l) t = fmaf(sc.A[(size_t)l * C + j], sc.dNp[(size_t)l * dp + e], t);
-      const float *g = sc.Gf + (size_t)e * M;
-      const float *f = sc.phk + (size_t)j * M;
-      for (int m = 0; m < M; ++m) t = fmaf(g[m], f[m], t);
+      float t = dot4(sc.A + (size_t)j * C + j, C, sc.dNp + (size_t)j * dp + e, dp, rows - j);
+      t = dot4(sc.Gf + (size_t)e * M, 1, sc.phk + (size_t)j * M, 1, M, t);
       dv[idx] = from_f32<T>(t);
     }
     __syncthreads();
