@@ -138,6 +138,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // MC: features per CTA (<= 128)
   constexpr int QF = MC / kParts;  // feature columns per thread
   constexpr int QD = D / kParts;   // value columns per thread
+  // 128 features: dphi_k and dphi_q complete on barriers of their own, so
+  // u_k and the dK MMAs run under dphi_q's MMAs; with 64 the MMAs are short
+  // and the extra hand-offs cost more than they hide (one commit for both)
+  constexpr bool kSplitU = MC == 128;
   const Layout lay(MC);
   const uint32_t sb = smem_u32(smem);
   uint64_t *in_bar = reinterpret_cast<uint64_t *>(smem + lay.bars);
@@ -158,6 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *mmb_bar = in_bar + 11;
   // used once, after a timed-out wait: completes when every MMA issued so far has
   uint64_t *drain_bar = in_bar + 12;
+  // dphi_q complete (dphi_k's completion is on mmb_bar)
+  uint64_t *mmc_bar = in_bar + 13;
   float *rx = reinterpret_cast<float *>(smem + lay.rx);
   float *s_f = reinterpret_cast<float *>(smem + lay.s_f);
   float *gs_f = reinterpret_cast<float *>(smem + lay.gs_f);
@@ -192,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(x1_full, 1);
     mbar_init(x1_free, 1);
     mbar_init(drain_bar, 1);
+    mbar_init(mmc_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
     const size_t soff = ((size_t)bh * p.P + seg) * (size_t)M * DP + (size_t)fbase * DP;
@@ -264,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_at = sb + lay.at, s_gv = sb + lay.gv, s_rb = sb + lay.rb;
   const uint32_t s_ones = sb + lay.ones, s_ddb = sb + lay.ddb;
   const uint32_t tile_bytes = kTile * D * 2;
-  uint32_t in_phase = 0, in2_phase = 0, mma_phase = 0, mmb_phase = 0, rl_phase = 0, x_phase = 0;
+  uint32_t in_phase = 0, in2_phase = 0, mma_phase = 0, mmb_phase = 0, mmc_phase = 0, rl_phase = 0, x_phase = 0;
   // the exchange: two fp32 row sums for each of the 128 rows
   constexpr uint32_t kX1Bytes = 2 * kTile * 4;
   const uint32_t peer_x1_full = CS == 2 ? map_peer(smem_u32(x1_full), peer) : 0u;
@@ -291,6 +298,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     go &= mbar_wait(mmb_bar, mmb_phase, p.status, abort_flag);
     mmb_phase ^= 1;
+    tc_fence_after();
+  };
+  auto wait_mmc = [&]() {
+    __syncwarp();
+    go &= mbar_wait(mmc_bar, mmc_phase, p.status, abort_flag);
+    mmc_phase ^= 1;
     tc_fence_after();
   };
   auto cta_sync = [&]() {
@@ -583,22 +596,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_store_commit();
     }
 
-    // (h) dphi_q -> T, dphi_k -> X (one commit: u needs only these), then
-    // the G update (its own commit: it runs under u, which leaves phi_q, dN
-    // and dD, the update's operands, in place)
+    // (h) dphi_k -> X (kSplitU: its own commit, u_k starts on it while
+    // dphi_q's MMAs run), dphi_q -> T, then the G update (its own commit:
+    // it runs under u, which leaves phi_q, dN and dD, the update's operands,
+    // in place)
     if (issue0()) {
-      const uint32_t id_q1 = make_idesc(128, MC, false, true);
       const uint32_t id_q2 = make_idesc(128, MC, false, false);
-      for (int s = 0; s < kTile / 16; ++s)
-        mma_bf16(tb + kT, desc_kmajor(s_at, kTile, 0, s), desc_mnmajor(s_phk, kTile, 0, s), id_q1, s > 0);
-      for (int s = 0; s < D / 16; ++s)
-        mma_bf16(tb + kT, desc_kmajor(s_dy, kTile, 0, s), desc_kmajor(s_rb, MC, 0, s), id_q2, 1);
       const uint32_t id_k1 = make_idesc(128, MC, true, true);
       for (int s = 0; s < kTile / 16; ++s)
         mma_bf16(tb + kX, desc_mnmajor(s_at, kTile, 0, s), desc_mnmajor(s_phq, kTile, 0, s), id_k1, s > 0);
       for (int s = 0; s < D / 16; ++s)
         mma_bf16(tb + kX, desc_kmajor(s_v, kTile, 0, s), desc_kmajor(s_gv, MC, 0, s), id_q2, 1);
-      mma_commit(mmb_bar);
+      if (kSplitU) mma_commit(mmb_bar);
+      const uint32_t id_q1 = make_idesc(128, MC, false, true);
+      for (int s = 0; s < kTile / 16; ++s)
+        mma_bf16(tb + kT, desc_kmajor(s_at, kTile, 0, s), desc_mnmajor(s_phk, kTile, 0, s), id_q1, s > 0);
+      for (int s = 0; s < D / 16; ++s)
+        mma_bf16(tb + kT, desc_kmajor(s_dy, kTile, 0, s), desc_kmajor(s_rb, MC, 0, s), id_q2, 1);
+      mma_commit(kSplitU ? mmc_bar : mmb_bar);
       const uint32_t id_g = make_idesc(128, D, true, true);
       const uint32_t id_g1 = make_idesc(128, 16, true, true);
       for (int s = 0; s < kTile / 16; ++s) {
@@ -626,6 +641,86 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(in2_bar, 2 * tile_bytes);
       tma_load_3d(smem + lay.v, &tmV, in2_bar, 0, (t - 1) * kTile, bh);
     }
+
+    // (i) u = phi * dphi and its row sums, one side at a time: u_k (with
+    // kSplitU while dphi_q's MMAs run), then u_q.  FAVOR+: u as bf16 pairs
+    // into TMEM over dphi (the A operand of (j)), with kSplitU the dK MMAs
+    // issued between the two sides; elu+1 writes dQ, dK here.  With DW, u_k also goes over phi_k
+    // once dphi_q has read it, and u_q over phi_q once the G update has
+    // read phi_q.  The dphi terms that are not MMAs are added here:
+    // dphi_q += dD S, dphi_k += G_S (coef * vec, coef = dD or 1).
+    auto u_side = [&](uint32_t col, uint32_t s_phi, const float *vec, float coef, float *usum,
+                      uint32_t (&pairs)[QF / 2], __nv_bfloat16 *gout) {
+      const int c0 = QF * part;
+      float a[QF];
+      if constexpr (QF == 32) {
+        tmem_ld32(tmem_addr(tb, 32 * q4, col + c0), a);
+      } else {
+        tmem_ld16(tmem_addr(tb, 32 * q4, col + c0), a);
+      }
+      const float2 cf = make_float2(coef, coef);
+      float2 ua = make_float2(0.f, 0.f), ub = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < QF / 8; ++j) {
+        float fv[8], sv[8];
+        ld_bf16x8(s_phi + sw128_offset(row, c0 + 8 * j, kTile), fv);
+        // these 8 features' S or G_S (the same for every row): 128-bit loads
+        *reinterpret_cast<float4 *>(sv) = *reinterpret_cast<const float4 *>(vec + c0 + 8 * j);
+        *reinterpret_cast<float4 *>(sv + 4) = *reinterpret_cast<const float4 *>(vec + c0 + 8 * j + 4);
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+          const float2 dphi = __ffma2_rn(cf, make_float2(sv[i], sv[i + 1]), make_float2(a[8 * j + i], a[8 * j + i + 1]));
+          const float2 g = FAVOR ? make_float2(fv[i], fv[i + 1])
+                                 : make_float2(fminf(fv[i], 1.f), fminf(fv[i + 1], 1.f));
+          const float2 u = __fmul2_rn(g, dphi);
+          a[8 * j + i] = u.x;
+          a[8 * j + i + 1] = u.y;
+          if (i & 2) {
+            ub = __fadd2_rn(ub, u);
+          } else {
+            ua = __fadd2_rn(ua, u);
+          }
+        }
+      }
+      usum[part * kTile + row] = (ua.x + ua.y) + (ub.x + ub.y);
+      if (FAVOR) {
+        // feature m of u -> column m / 2 (low half of the pair first); the
+        // four parts of a row share its TMEM lane, so every part's dphi
+        // loads complete before any part stores
+        float pk[QF / 2];
+#pragma unroll
+        for (int x = 0; x < QF / 2; ++x) pk[x] = __uint_as_float(pack_bf16(a[2 * x], a[2 * x + 1]));
+        named_barrier_sync(1 + q4, kParts * 32);
+        if constexpr (QF == 32) {
+          tmem_st16(tmem_addr(tb, 32 * q4, col + c0 / 2), pk);
+        } else {
+          tmem_st8(tmem_addr(tb, 32 * q4, col + c0 / 2), pk);
+        }
+        if (DW) {
+#pragma unroll
+          for (int x = 0; x < QF / 2; ++x) pairs[x] = __float_as_uint(pk[x]);
+        }
+      } else if (live) {
+        uint4 *g = reinterpret_cast<uint4 *>(gout + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + c0);
+#pragma unroll
+        for (int j = 0; j < QF / 8; ++j)
+          g[j] = make_uint4(pack_bf16(a[8 * j], a[8 * j + 1]), pack_bf16(a[8 * j + 2], a[8 * j + 3]),
+                            pack_bf16(a[8 * j + 4], a[8 * j + 5]), pack_bf16(a[8 * j + 6], a[8 * j + 7]));
+      }
+    };
+    uint32_t uq_pairs[QF / 2], uk_pairs[QF / 2];
+    u_side(kX, s_phk, gs_f, 1.f, usk, uk_pairs, p.dk);
+    if (FAVOR && kSplitU) {
+      // dK = u_k W^T (-> X + 64) under u_q
+      tmem_st_wait();
+      cta_sync();
+      if (issue0()) {
+        const uint32_t id = make_idesc(128, D, false, true);
+        for (int s = 0; s < MC / 16; ++s)
+          mma_bf16_ta(tb + kX + 64, tb + kX + 8 * s, desc_mnmajor(s_w, MC, 0, s), id, s > 0);
+      }
+    }
+    if (kSplitU) wait_mmc();
     if (CS == 2) {
       // the dA tile is idle from here: Q and K come back into it for the
       // dQ, dK epilogue (the Q tile holds the dV partial, K the next K)
@@ -635,93 +730,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(smem + lay.at + tile_bytes, &tmK, rl_bar, 0, t * kTile, bh);
       }
     }
-
-    // (i) u = phi * dphi, row sums; FAVOR+: u as bf16 pairs into TMEM over
-    // dphi (the A operand of (j)); elu+1 writes dQ, dK here.  With DW, u_k
-    // also goes over phi_k (no MMA reads it any more) and u_q over phi_q
-    // once the G update has read phi_q
-    uint32_t uq_pairs[QF / 2];
-    {
-      const float dval = dd[row];
-      float uq = 0.f, uk = 0.f;
-      {
-        const int c0 = QF * part;
-        float a[QF], b[QF];
-        if constexpr (QF == 32) {
-          tmem_ld32x2(tmem_addr(tb, 32 * q4, kT + c0), tmem_addr(tb, 32 * q4, kX + c0), a, b);
-        } else {
-          tmem_ld16x2(tmem_addr(tb, 32 * q4, kT + c0), tmem_addr(tb, 32 * q4, kX + c0), a, b);
-        }
+    if (DW) {
+      // phi_k has been read by dphi_q: u_k over it, for the dW MMAs
+      const int c0 = QF * part;
 #pragma unroll
-        for (int j = 0; j < QF / 8; ++j) {
-          float fq[8], fk[8], sv[8], gv[8];
-          ld_bf16x8(s_phq + sw128_offset(row, c0 + 8 * j, kTile), fq);
-          ld_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), fk);
-          // S and G_S of these 8 features (the same for every row): 128-bit loads
-          *reinterpret_cast<float4 *>(sv) = *reinterpret_cast<const float4 *>(s_f + c0 + 8 * j);
-          *reinterpret_cast<float4 *>(sv + 4) = *reinterpret_cast<const float4 *>(s_f + c0 + 8 * j + 4);
-          *reinterpret_cast<float4 *>(gv) = *reinterpret_cast<const float4 *>(gs_f + c0 + 8 * j);
-          *reinterpret_cast<float4 *>(gv + 4) = *reinterpret_cast<const float4 *>(gs_f + c0 + 8 * j + 4);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float dq = fmaf(dval, sv[i], a[8 * j + i]);
-            const float dk = b[8 * j + i] + gv[i];
-            if (FAVOR) {
-              a[8 * j + i] = fq[i] * dq;
-              b[8 * j + i] = fk[i] * dk;
-            } else {
-              a[8 * j + i] = dq * fminf(fq[i], 1.f);
-              b[8 * j + i] = dk * fminf(fk[i], 1.f);
-            }
-            uq += a[8 * j + i];
-            uk += b[8 * j + i];
-          }
-        }
-        if (FAVOR) {
-          // feature m of u -> column m / 2 (low half of the pair first); the
-          // four parts of a row share its TMEM lane, so every part's dphi
-          // loads complete before any part stores
-          float pq[QF / 2], pk[QF / 2];
-#pragma unroll
-          for (int x = 0; x < QF / 2; ++x) {
-            pq[x] = __uint_as_float(pack_bf16(a[2 * x], a[2 * x + 1]));
-            pk[x] = __uint_as_float(pack_bf16(b[2 * x], b[2 * x + 1]));
-          }
-          named_barrier_sync(1 + q4, kParts * 32);
-          if constexpr (QF == 32) {
-            tmem_st16(tmem_addr(tb, 32 * q4, kT + c0 / 2), pq);
-            tmem_st16(tmem_addr(tb, 32 * q4, kX + c0 / 2), pk);
-          } else {
-            tmem_st8(tmem_addr(tb, 32 * q4, kT + c0 / 2), pq);
-            tmem_st8(tmem_addr(tb, 32 * q4, kX + c0 / 2), pk);
-          }
-          if (DW) {
-#pragma unroll
-            for (int j = 0; j < QF / 8; ++j)
-              st_shared_v4(s_phk + sw128_offset(row, c0 + 8 * j, kTile), __float_as_uint(pk[4 * j]),
-                           __float_as_uint(pk[4 * j + 1]), __float_as_uint(pk[4 * j + 2]),
-                           __float_as_uint(pk[4 * j + 3]));
-#pragma unroll
-            for (int x = 0; x < QF / 2; ++x) uq_pairs[x] = __float_as_uint(pq[x]);
-          }
-        } else if (live) {
-          uint4 *gq = reinterpret_cast<uint4 *>(p.dq + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + c0);
-          uint4 *gk = reinterpret_cast<uint4 *>(p.dk + ((size_t)bh * p.L + (size_t)t * kTile + row) * D + c0);
-#pragma unroll
-          for (int j = 0; j < QF / 8; ++j) {
-            gq[j] = make_uint4(pack_bf16(a[8 * j], a[8 * j + 1]), pack_bf16(a[8 * j + 2], a[8 * j + 3]),
-                               pack_bf16(a[8 * j + 4], a[8 * j + 5]), pack_bf16(a[8 * j + 6], a[8 * j + 7]));
-            gk[j] = make_uint4(pack_bf16(b[8 * j], b[8 * j + 1]), pack_bf16(b[8 * j + 2], b[8 * j + 3]),
-                               pack_bf16(b[8 * j + 4], b[8 * j + 5]), pack_bf16(b[8 * j + 6], b[8 * j + 7]));
-          }
-        }
-      }
-      usq[part * kTile + row] = uq;
-      usk[part * kTile + row] = uk;
+      for (int j = 0; j < QF / 8; ++j)
+        st_shared_v4(s_phk + sw128_offset(row, c0 + 8 * j, kTile), uk_pairs[4 * j], uk_pairs[4 * j + 1],
+                     uk_pairs[4 * j + 2], uk_pairs[4 * j + 3]);
     }
+    u_side(kT, s_phq, s_f, dd[row], usq, uq_pairs, p.dq);
     if (FAVOR) tmem_st_wait();
-    cta_sync();
+    // every thread is past the G update's phase before thread 0 can commit
+    // the next group on the same barrier
     wait_mma();  // the G update: dN's tile takes the next dY
+    cta_sync();
     if (issue0() && t > t0) tma_load_3d(smem + lay.dy, &tmDY, in2_bar, 0, (t - 1) * kTile, bh);
     if (DW) {
       // phi_q has been read by the G update: u_q over it, for the dW MMAs
@@ -736,13 +758,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (FAVOR) {
       // (j) dQ = u_q W^T - q rowsum(u_q) -> T + 64, dK likewise -> X + 64
+      // (its MMAs issued under u_q)
       if (issue0()) {
         const uint32_t id = make_idesc(128, D, false, true);
         for (int s = 0; s < MC / 16; ++s) {
           mma_bf16_ta(tb + kT + 64, tb + kT + 8 * s, desc_mnmajor(s_w, MC, 0, s), id, s > 0);
-          mma_bf16_ta(tb + kX + 64, tb + kX + 8 * s, desc_mnmajor(s_w, MC, 0, s), id, s > 0);
+          if (!kSplitU) mma_bf16_ta(tb + kX + 64, tb + kX + 8 * s, desc_mnmajor(s_w, MC, 0, s), id, s > 0);
         }
-        mma_done();
+        mma_done();  // with kSplitU, the dK MMAs issued under u_q too
       }
       wait_mma();
       const float sq = (usq[row] + usq[kTile + row]) + (usq[2 * kTile + row] + usq[3 * kTile + row]);
