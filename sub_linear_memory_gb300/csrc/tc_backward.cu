@@ -8,7 +8,8 @@
 //   A   = tril(phi_q phi_k^T),  num = A V + phi_q R^T,
 //   den = rowsum(A) + phi_q . S,  Y = num / den
 //   dN  = dY / den,  dD = -(dY . Y) / den     (dN' = [dN ; dD])
-//   dA  = tril(dN V^T + dD 1^T)
+//   dA  = tril(dN V^T + dD 1^T)              (as diag(1/den) (dY V^T) + dD 1^T:
+//                                             the MMA needs dY only, not dN)
 //   dV  = A^T dN + phi_k G_V^T
 //   dphi_q = dA phi_k + dN R^T + dD S^T
 //   dphi_k = dA^T phi_q + V G_V^T + 1 G_S^T
@@ -477,6 +478,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < MC / 16; ++s)
         mma_bf16(tb + kT, desc_kmajor(s_phq, kTile, 0, s), desc_mnmajor(s_rb, MC, 0, s), id, 1);
       mma_done();
+      // dY V^T -> X (A is dead there since its mask, its loads complete
+      // before the barrier above): dA before its row scaling by 1 / den,
+      // which (g) applies, so dA needs no MMA after dN
+      const uint32_t id_a = make_idesc(128, 128, false, false);
+      for (int s = 0; s < D / 16; ++s)
+        mma_bf16(tb + kX, desc_kmajor(s_dy, kTile, 0, s), desc_kmajor(s_v, kTile, 0, s), id_a, s > 0);
+      mma_commit(mmb_bar);
     }
     {
       // this thread's features of phi_q . S (S after eq. (19), fp32), added
@@ -501,6 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // with a CTA pair) was waited for in (c); G_S as fp32
     state_to_smem(tb, kG, q4, part, row, MC, s_gv, gs_f);
     wait_mma();
+    float inv;  // 1 / den of this thread's row (0 on padding rows)
     {
       // dN = dY / den and dD = -(dY . Y) / den with Y = num / den: only the
       // row sums den and dY . num are needed, both linear in the features,
@@ -530,13 +539,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         den += rx[row];
         dsum += rx[kTile + row];
       }
-      const float inv = live ? 1.0f / den : 0.f;
+      inv = live ? 1.0f / den : 0.f;
 #pragma unroll
       for (int i = 0; i < QD; i += 2) {
         const float2 gi = __fmul2_rn(make_float2(g[i], g[i + 1]), make_float2(inv, inv));
         g[i] = gi.x;
         g[i + 1] = gi.y;
       }
+      wait_mmb();  // dY V^T has read dY
 #pragma unroll
       for (int j = 0; j < QD / 8; ++j) st_bf16x8(s_dy + sw128_offset(row, QD * part + 8 * j, kTile), g + 8 * j);
       if (part == 0) {
@@ -548,35 +558,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_async_smem();
     cta_sync();
 
-    // (g) dV = A^T dN + phi_k G_V^T ; raw dA = dN V^T
+    // (g) dV = A^T dN + phi_k G_V^T -> T (num has been read there); while
+    // its MMAs run, dA = tril(dN V^T + dD 1^T) = tril(diag(1/den) dY V^T +
+    // dD 1^T) from the product in X, stored once the MMAs have read the
+    // masked A out of its tile
     if (issue0()) {
       const uint32_t id_v1 = make_idesc(128, D, true, true);
       const uint32_t id_v2 = make_idesc(128, D, false, true);
       for (int s = 0; s < kTile / 16; ++s)
-        mma_bf16(tb + kX, desc_mnmajor(s_at, kTile, 0, s), desc_mnmajor(s_dy, kTile, 0, s), id_v1, s > 0);
+        mma_bf16(tb + kT, desc_mnmajor(s_at, kTile, 0, s), desc_mnmajor(s_dy, kTile, 0, s), id_v1, s > 0);
       for (int s = 0; s < MC / 16; ++s)
-        mma_bf16(tb + kX, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_gv, MC, 0, s), id_v2, 1);
-      const uint32_t id_a = make_idesc(128, 128, false, false);
-      for (int s = 0; s < D / 16; ++s)
-        mma_bf16(tb + kT, desc_kmajor(s_dy, kTile, 0, s), desc_kmajor(s_v, kTile, 0, s), id_a, s > 0);
+        mma_bf16(tb + kT, desc_kmajor(s_phk, kTile, 0, s), desc_mnmajor(s_gv, MC, 0, s), id_v2, 1);
       mma_done();
     }
-    wait_mma();
     {
       const float dval = dd[row];
-      float v[QD];
+      uint32_t pa[16];
       {
         float a[32];
-        tmem_ld32p16(tmem_addr(tb, 32 * q4, kT + 32 * part), tmem_addr(tb, 32 * q4, kX + QD * part), a, v);
+        tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * part), a);
+        const float2 inv2 = make_float2(inv, inv), dv2 = make_float2(dval, dval);
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float2 ai = __fadd2_rn(make_float2(a[i], a[i + 1]), make_float2(dval, dval));
-          a[i] = (32 * part + i > row) ? 0.f : ai.x;
-          a[i + 1] = (32 * part + i + 1 > row) ? 0.f : ai.y;
+          const float2 ai = __ffma2_rn(inv2, make_float2(a[i], a[i + 1]), dv2);
+          pa[i >> 1] = pack_bf16((32 * part + i > row) ? 0.f : ai.x, (32 * part + i + 1 > row) ? 0.f : ai.y);
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, 32 * part + 8 * j, kTile), a + 8 * j);
       }
+      wait_mma();
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        st_shared_v4(s_at + sw128_offset(row, 32 * part + 8 * j, kTile), pa[4 * j], pa[4 * j + 1], pa[4 * j + 2],
+                     pa[4 * j + 3]);
+      float v[QD];
+      tmem_ld16(tmem_addr(tb, 32 * q4, kT + QD * part), v);
       if (CS == 2) {
         // this CTA's dV partial -> bf16 in the idle Q tile, for a reduce-add
 #pragma unroll
