@@ -101,7 +101,8 @@ typedef enum {
    * segment in the registered workspace and tags it with k, v, w, the shape
    * and the workspace.  The next slim_attn_bwd with the same k, v, w
    * pointers, shape and workspace, and no other call on that workspace in
-   * between, reads those states instead of recomputing them; any mismatch
+   * between, reads those states (and the bf16 image of w the forward made)
+   * instead of recomputing them; any mismatch
    * recomputes them, so results never depend on the tag.  The caller
    * guarantees that the contents of k, v and w do not change between the two
    * calls (they are not compared).  Carried-state calls (slim_attn_*_carry)

@@ -68,8 +68,6 @@ cudaError_t tc_forward(const Plan &p, const Args &a, cudaStream_t st);
 // CTA's partials into them).
 cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, int zero_grads, const float *init,
                               cudaStream_t st);
-// FAVOR+: W -> the bf16 W^T image the tensor kernels copy (in the workspace).
-cudaError_t tc_prep_w(const Plan &p, const Args &a, cudaStream_t st);
 // Carried states (carry.cu): the caller's e-major [BH][d + 1][M] layout into
 // the tensor path's features-major [BH][M][d + 1], and the sum of one slot of
 // two features-major state arrays ([BH][pa][M][d + 1], b may be NULL) back
@@ -78,9 +76,11 @@ cudaError_t emajor_to_fm(const Plan &p, const float *src, float *dst, cudaStream
 cudaError_t fm_to_emajor(const Plan &p, const float *a, int pa, int sa, const float *b, int pb, int sb, float *out,
                          cudaStream_t st);
 // dK, dV += the terms of the later segments' reverse state (after the backward
-// kernel and the reverse scan of the segment G totals).  g_last: the reverse
-// state arriving from rows after this call (features-major [BH][M][d + 1]),
-// which is also the last segment's G_end, or NULL.
+// kernel; the G_end records come from the segment G totals by a reverse
+// running sum, also written back over totals 1 .. P - 1 when a.g_out is set).
+// g_last: the reverse state arriving from rows after this call
+// (features-major [BH][M][d + 1]), which is also the last segment's G_end, or
+// NULL.
 cudaError_t tc_correction(const Plan &p, const Args &a, const float *g_last, cudaStream_t st);
 // Learnable W (FAVOR+): the later segments' reverse-state terms of dW, added
 // to the per-segment partials (after tc_correction, which builds the G_end

@@ -223,11 +223,14 @@ Plan make_plan(int B, int H, int L, int d, int M, int chunk, bool favor, bool bw
   size_t off = 0;
   p.states_off = off; off += align_floats(state);
   p.states_lo_off = off; if (path == 2) off += align_floats(state);
+  // the W image next: at the same offset in a forward's and a backward's
+  // layout of one shape and segment plan, so a backward on the forward's
+  // states (SLIM_OPT_REUSE_STATES) reads its image too
+  p.wimg_off = off; if (path == 2 && favor) off += align_floats((size_t)std::max(p.wh, 1) * M * 32);
   p.gstates_off = off; if (bwd) off += align_floats(state);
   p.scratch_stride = path == 2 ? 0 : align_floats(generic_scratch_floats(p, bwd));
   p.scratch_off = off; off += p.scratch_stride * p.BH * p.P;
   p.dwpart_off = off; if (bwd && want_dw) off += align_floats((size_t)p.BH * p.P * d * M);
-  p.wimg_off = off; if (path == 2 && favor) off += align_floats((size_t)std::max(p.wh, 1) * M * 32);
   // bf16 G_end images [M][d] and fp32 G_S [M] per (head, segment)
   p.gimg_off = off; if (path == 2 && bwd) off += align_floats((size_t)p.BH * p.P * M * (d / 2 + 1));
   // carried states turned features-major: R'_0 and G (tensor path)

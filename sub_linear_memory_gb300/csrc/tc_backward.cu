@@ -963,12 +963,12 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
   }
   // R' totals of every segment, scanned; with two CTAs per segment the
   // outputs start at zero for the per-CTA reduce-adds.  With the end states
-  // the forward left (same segments, same exact scan) only the W image and
-  // the zeroed outputs remain to be made.
-  cudaError_t e;
+  // the forward left (same segments, same exact scan; its W image sits at
+  // the same workspace offset, made from the same W) only the zeroed
+  // outputs remain to be made.
+  cudaError_t e = cudaSuccess;
   if (a.reuse_states) {
-    e = tc_prep_w(pl, a, st);
-    if (e == cudaSuccess && CS == 2) e = zero_outputs(pl, a, st);
+    if (CS == 2) e = zero_outputs(pl, a, st);
   } else {
     e = tc_segment_states(pl, a, pl.P, CS == 2 ? 7 : 0, init, st);
   }
@@ -1014,13 +1014,8 @@ cudaError_t backward_family(const Plan &pl, const Args &a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   if (pl.P > 1 || g_last) {
-    if (pl.P > 1) {
-      ProfScope ps("scan_states", st);
-      // G_end(s) = G arriving from later rows + sum over s' > s: reverse
-      // inclusive scan over segments 1..P-1
-      e = scan_states_f32_rev(pl, a.ws + pl.gstates_off + (size_t)pl.M * (D + 1), pl.P - 1, g_last, st);
-      if (e != cudaSuccess) return e;
-    }
+    // G_end(s) = G arriving from later rows + sum over s' > s of the
+    // segments' totals, formed by the correction's set-up kernel
     e = tc_correction(pl, a, g_last, st);
     if (e != cudaSuccess) return e;
     // dW's share of the later segments' reverse state

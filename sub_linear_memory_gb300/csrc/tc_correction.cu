@@ -502,28 +502,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
-// G_end(s) = gstates[s + 1] (after the reverse scan) -> per (head, segment)
-// record: bf16 [M][64] swizzled image of columns 0..63, then fp32 column 64.
-// nrec records per head: P - 1, or P when a reverse state g_last
-// (features-major [BH][M][D + 1]) arrives from later rows: it is the last
-// segment's G_end.
-__global__ void prep_g_kernel(const float *__restrict__ gstates, const float *__restrict__ g_last,
-                              unsigned char *__restrict__ grec, int M, int P, int nrec, int BH) {
-  // x: the (feature, column) pairs of one record; y: its (head, segment),
-  // so every division is by a constant or once per thread
+// G_end(s) of every record s < nrec from the segments' G totals (gstates,
+// features-major [BH][P][M][D + 1]) by a running sum from the last segment
+// down: G_end(s) = g_last + sum over s' > s of total(s'), where g_last
+// (features-major [BH][M][D + 1]) is the reverse state arriving from later
+// rows, or zero.  nrec = P - 1, or P with g_last (then it is the last
+// segment's G_end).  A record, per (head, segment): bf16 [M][64] swizzled
+// image of columns 0..63, then fp32 column 64.  One thread per (head,
+// feature, group of 8 columns); group 7 also carries column 64.  With keep
+// the running sums also go back over totals 1 .. P - 1 (the carried-state
+// gradient reads G_end(0) there).
+__global__ void scan_prep_g_kernel(float *__restrict__ gstates, const float *__restrict__ g_last,
+                                   unsigned char *__restrict__ grec, int M, int P, int nrec, int BH, int keep) {
   const int DP = D + 1;
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= M * DP) return;
-  const int f = r / DP, e = r - f * DP;
-  for (int hs = blockIdx.y; hs < BH * nrec; hs += gridDim.y) {
-    const int bh = hs / nrec, s = hs - bh * nrec;
-    const float g = s + 1 < P ? gstates[((size_t)bh * P + s + 1) * (size_t)M * DP + r]
-                              : g_last[(size_t)bh * M * DP + r];
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)BH * M * 8) return;
+  const int c = (int)(i & 7);
+  const long long fm = i >> 3;
+  const int bh = (int)(fm / M), f = (int)(fm - (long long)bh * M);
+  const int n = c == 7 ? 9 : 8;
+  const size_t per = (size_t)M * DP, base = (size_t)f * DP + 8 * c;
+  float acc[9];
+#pragma unroll
+  for (int j = 0; j < 9; ++j) acc[j] = (j < n && g_last) ? g_last[(size_t)bh * per + base + j] : 0.f;
+  for (int s = nrec - 1; s >= 0; --s) {
+    if (s + 1 < P) {
+      float *src = gstates + ((size_t)bh * P + s + 1) * per + base;
+#pragma unroll
+      for (int j = 0; j < 9; ++j)
+        if (j < n) {
+          acc[j] += src[j];
+          if (keep) src[j] = acc[j];
+        }
+    }
     unsigned char *rec = grec + ((size_t)bh * P + s) * (size_t)M * 132u;
-    if (e < D)
-      *reinterpret_cast<__nv_bfloat16 *>(rec + sw128_offset(f, e, M)) = __float2bfloat16_rn(g);
-    else
-      reinterpret_cast<float *>(rec + (size_t)M * 128u)[f] = g;
+    *reinterpret_cast<uint4 *>(rec + sw128_offset(f, 8 * c, M)) =
+        make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]), pack_bf16(acc[4], acc[5]),
+                   pack_bf16(acc[6], acc[7]));
+    if (c == 7) reinterpret_cast<float *>(rec + (size_t)M * 128u)[f] = acc[8];
   }
 }
 
@@ -815,11 +831,11 @@ cudaError_t tc_correction(const Plan &pl, const Args &a, const float *g_last, cu
     return cudaErrorInvalidValue;
   {
     ProfScope ps("prep_g", st);
-    const int rec = pl.M * (tcc::D + 1);
-    const dim3 grid((rec + 255) / 256, (unsigned)std::min(pl.BH * nrec, 65535));
-    tcc::prep_g_kernel<<<grid, 256, 0, st>>>(a.ws + pl.gstates_off, g_last,
-                                               reinterpret_cast<unsigned char *>(a.ws + pl.gimg_off), pl.M, pl.P,
-                                               nrec, pl.BH);
+    const long long threads = (long long)pl.BH * pl.M * 8;
+    const int keep = a.g_out != nullptr && pl.P > 1;
+    tcc::scan_prep_g_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
+        a.ws + pl.gstates_off, g_last, reinterpret_cast<unsigned char *>(a.ws + pl.gimg_off), pl.M, pl.P, nrec,
+        pl.BH, keep);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

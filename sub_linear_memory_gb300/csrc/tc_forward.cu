@@ -1222,8 +1222,6 @@ cudaError_t tc_segment_states(const Plan &p, const Args &a, int nseg, int zero_g
   return cudaErrorInvalidValue;
 }
 
-cudaError_t tc_prep_w(const Plan &p, const Args &a, cudaStream_t st) { return tcf::prep_w(p, a, st); }
-
 cudaError_t tc_forward(const Plan &p, const Args &a, cudaStream_t st) {
   cudaError_t e = tcf::prep_w(p, a, st);
   if (e != cudaSuccess) return e;
