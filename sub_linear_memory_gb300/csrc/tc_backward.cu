@@ -465,7 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row < MC) s_f[row] = hs + ls;
       }
     }
-    tmem_st_wait();
+    // no MMA reads the masters and only this thread rereads its columns (the
+    // next tile), so their stores are waited for later, off this barrier
     fence_async_smem();
     cta_sync();
 
@@ -555,6 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         st_bf16_scalar(smem, lay.ddb + n16_offset(row, 0), dval);
       }
     }
+    tmem_st_wait();  // eq. (19)'s master stores, before the next tile rereads them
     fence_async_smem();
     cta_sync();
 
