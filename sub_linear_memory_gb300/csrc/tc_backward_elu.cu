@@ -311,7 +311,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 16; i += 8) st_bf16x8(s_rb + sw128_offset(row, c + i, D), x + i);
     }
-    tmem_st_wait();
+    // no MMA reads the masters and only this thread rereads its columns (the
+    // next tile): their stores are waited for after dN, off these barriers
     cta_sync();  // the column sums are in
     if (tid < D) {
       const float cs = (dot[tid] + dot[kTile + tid]) + (dot[2 * kTile + tid] + dot[3 * kTile + tid]);
@@ -389,6 +390,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (part == 0) dd[row] = live ? -(dsum * inv) * inv : 0.f;
     }
+    tmem_st_wait();  // eq. (19)'s master stores, before the next tile rereads them
     fence_async_smem();
     cta_sync();
 

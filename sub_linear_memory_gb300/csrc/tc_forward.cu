@@ -997,9 +997,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st16(tmem_addr(tbase, lane_base, t_m + b * NC + D), m);
       }
-      tmem_st_wait();
+      // the increment's loads are complete (each load waits): its columns
+      // are free for the next MMA.  The master's stores are waited for after
+      // the release; only this thread rereads those columns, next tile
       tc_fence_before();
       arrive(S_INCFREE);
+      tmem_st_wait();
       __syncwarp();
       if (lane == 0) mbar_arrive_n(bar + S_EMPTY + slot_idx(2 * i + 1), 2);  // V(t): 4 warps x 2
     }
