@@ -163,8 +163,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *mmb_bar = in_bar + 11;
   // used once, after a timed-out wait: completes when every MMA issued so far has
   uint64_t *drain_bar = in_bar + 12;
-  // dphi_q complete (dphi_k's completion is on mmb_bar)
-  uint64_t *mmc_bar = in_bar + 13;
+  // dphi_q complete (dphi_k's completion is on mmb_bar); the dK MMAs complete
+  uint64_t *mmc_bar = in_bar + 13, *mmd_bar = in_bar + 14;
   float *rx = reinterpret_cast<float *>(smem + lay.rx);
   float *s_f = reinterpret_cast<float *>(smem + lay.s_f);
   float *gs_f = reinterpret_cast<float *>(smem + lay.gs_f);
@@ -200,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(x1_free, 1);
     mbar_init(drain_bar, 1);
     mbar_init(mmc_bar, 1);
+    mbar_init(mmd_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
     const size_t soff = ((size_t)bh * p.P + seg) * (size_t)M * DP + (size_t)fbase * DP;
@@ -272,7 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_at = sb + lay.at, s_gv = sb + lay.gv, s_rb = sb + lay.rb;
   const uint32_t s_ones = sb + lay.ones, s_ddb = sb + lay.ddb;
   const uint32_t tile_bytes = kTile * D * 2;
-  uint32_t in_phase = 0, in2_phase = 0, mma_phase = 0, mmb_phase = 0, mmc_phase = 0, rl_phase = 0, x_phase = 0;
+  uint32_t in_phase = 0, in2_phase = 0, mma_phase = 0, mmb_phase = 0, mmc_phase = 0, mmd_phase = 0, rl_phase = 0,
+           x_phase = 0;
   // the exchange: two fp32 row sums for each of the 128 rows
   constexpr uint32_t kX1Bytes = 2 * kTile * 4;
   const uint32_t peer_x1_full = CS == 2 ? map_peer(smem_u32(x1_full), peer) : 0u;
@@ -305,6 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     go &= mbar_wait(mmc_bar, mmc_phase, p.status, abort_flag);
     mmc_phase ^= 1;
+    tc_fence_after();
+  };
+  auto wait_mmd = [&]() {
+    __syncwarp();
+    go &= mbar_wait(mmd_bar, mmd_phase, p.status, abort_flag);
+    mmd_phase ^= 1;
     tc_fence_after();
   };
   auto cta_sync = [&]() {
@@ -734,6 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t id = make_idesc(128, D, false, true);
         for (int s = 0; s < MC / 16; ++s)
           mma_bf16_ta(tb + kX + 64, tb + kX + 8 * s, desc_mnmajor(s_w, MC, 0, s), id, s > 0);
+        mma_commit(mmd_bar);
       }
     }
     if (kSplitU) wait_mmc();
@@ -783,19 +792,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_done();  // with kSplitU, the dK MMAs issued under u_q too
       }
-      wait_mma();
-      const float sq = (usq[row] + usq[kTile + row]) + (usq[2 * kTile + row] + usq[3 * kTile + row]);
-      const float sk = (usk[row] + usk[kTile + row]) + (usk[2 * kTile + row] + usk[3 * kTile + row]);
-      float a[QD], b[QD];
-      tmem_ld16x2(tmem_addr(tb, 32 * q4, kT + 64 + QD * part), tmem_addr(tb, 32 * q4, kX + 64 + QD * part), a, b);
       uint32_t s_xq = s_q, s_xk = s_k;
       if (CS == 2) {
-        go &= mbar_wait(rl_bar, rl_phase, p.status, abort_flag);
-        rl_phase ^= 1;
         s_xq = sb + lay.at;
         s_xk = sb + lay.at + tile_bytes;
       }
-      if (DW && issue0()) {
+      auto issue_dw = [&]() {
         // dW^T = u_q^T Q + u_k^T K (features on the lanes) -> T: the dQ, dK
         // MMAs have read u's TMEM pairs there
         const uint32_t id_w = make_idesc(128, D, true, true);
@@ -804,24 +806,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kTile / 16; ++s)
           mma_bf16(tb + kT, desc_mnmajor(s_phk, kTile, 0, s), desc_mnmajor(s_xk, kTile, 0, s), id_w, 1);
         mma_commit(mmb_bar);
-      }
+      };
+      auto wait_rl = [&]() {
+        if (CS == 2) {
+          go &= mbar_wait(rl_bar, rl_phase, p.status, abort_flag);
+          rl_phase ^= 1;
+        }
+      };
       // dQ = u_q W^T - q rowsum(u_q), dK likewise (this CTA's features)
       float oq[QD], ok[QD];
+      if constexpr (kSplitU) {
+        // dK first: its MMAs ran under u_q (their own commit), so its
+        // epilogue runs while the dQ MMAs do
+        wait_mmd();
+        {
+          const float sk = (usk[row] + usk[kTile + row]) + (usk[2 * kTile + row] + usk[3 * kTile + row]);
+          float b[QD];
+          tmem_ld16(tmem_addr(tb, 32 * q4, kX + 64 + QD * part), b);
+          wait_rl();
 #pragma unroll
-      for (int j = 0; j < QD / 8; ++j) {
-        float xq[8], xk[8];
-        ld_bf16x8(s_xq + sw128_offset(row, QD * part + 8 * j, kTile), xq);
-        ld_bf16x8(s_xk + sw128_offset(row, QD * part + 8 * j, kTile), xk);
+          for (int j = 0; j < QD / 8; ++j) {
+            float xk[8];
+            ld_bf16x8(s_xk + sw128_offset(row, QD * part + 8 * j, kTile), xk);
 #pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          const float2 q2 = __ffma2_rn(make_float2(-xq[i], -xq[i + 1]), make_float2(sq, sq),
-                                       make_float2(a[8 * j + i], a[8 * j + i + 1]));
-          const float2 k2 = __ffma2_rn(make_float2(-xk[i], -xk[i + 1]), make_float2(sk, sk),
-                                       make_float2(b[8 * j + i], b[8 * j + i + 1]));
-          oq[8 * j + i] = q2.x;
-          oq[8 * j + i + 1] = q2.y;
-          ok[8 * j + i] = k2.x;
-          ok[8 * j + i + 1] = k2.y;
+            for (int i = 0; i < 8; i += 2) {
+              const float2 k2 = __ffma2_rn(make_float2(-xk[i], -xk[i + 1]), make_float2(sk, sk),
+                                           make_float2(b[8 * j + i], b[8 * j + i + 1]));
+              ok[8 * j + i] = k2.x;
+              ok[8 * j + i + 1] = k2.y;
+            }
+          }
+        }
+        wait_mma();
+        if (DW && issue0()) issue_dw();
+        const float sq = (usq[row] + usq[kTile + row]) + (usq[2 * kTile + row] + usq[3 * kTile + row]);
+        float a[QD];
+        tmem_ld16(tmem_addr(tb, 32 * q4, kT + 64 + QD * part), a);
+#pragma unroll
+        for (int j = 0; j < QD / 8; ++j) {
+          float xq[8];
+          ld_bf16x8(s_xq + sw128_offset(row, QD * part + 8 * j, kTile), xq);
+#pragma unroll
+          for (int i = 0; i < 8; i += 2) {
+            const float2 q2 = __ffma2_rn(make_float2(-xq[i], -xq[i + 1]), make_float2(sq, sq),
+                                         make_float2(a[8 * j + i], a[8 * j + i + 1]));
+            oq[8 * j + i] = q2.x;
+            oq[8 * j + i + 1] = q2.y;
+          }
+        }
+      } else {
+        wait_mma();
+        const float sq = (usq[row] + usq[kTile + row]) + (usq[2 * kTile + row] + usq[3 * kTile + row]);
+        const float sk = (usk[row] + usk[kTile + row]) + (usk[2 * kTile + row] + usk[3 * kTile + row]);
+        float a[QD], b[QD];
+        tmem_ld16x2(tmem_addr(tb, 32 * q4, kT + 64 + QD * part), tmem_addr(tb, 32 * q4, kX + 64 + QD * part), a, b);
+        wait_rl();
+        if (DW && issue0()) issue_dw();
+#pragma unroll
+        for (int j = 0; j < QD / 8; ++j) {
+          float xq[8], xk[8];
+          ld_bf16x8(s_xq + sw128_offset(row, QD * part + 8 * j, kTile), xq);
+          ld_bf16x8(s_xk + sw128_offset(row, QD * part + 8 * j, kTile), xk);
+#pragma unroll
+          for (int i = 0; i < 8; i += 2) {
+            const float2 q2 = __ffma2_rn(make_float2(-xq[i], -xq[i + 1]), make_float2(sq, sq),
+                                         make_float2(a[8 * j + i], a[8 * j + i + 1]));
+            const float2 k2 = __ffma2_rn(make_float2(-xk[i], -xk[i + 1]), make_float2(sk, sk),
+                                         make_float2(b[8 * j + i], b[8 * j + i + 1]));
+            oq[8 * j + i] = q2.x;
+            oq[8 * j + i + 1] = q2.y;
+            ok[8 * j + i] = k2.x;
+            ok[8 * j + i + 1] = k2.y;
+          }
         }
       }
       if (CS == 2) {
