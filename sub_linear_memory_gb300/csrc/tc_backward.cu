@@ -139,10 +139,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // MC: features per CTA (<= 128)
   constexpr int QF = MC / kParts;  // feature columns per thread
   constexpr int QD = D / kParts;   // value columns per thread
-  // 128 features: dphi_k and dphi_q complete on barriers of their own, so
-  // u_k and the dK MMAs run under dphi_q's MMAs; with 64 the MMAs are short
+  // 128 features per CTA: the two sides' features, dphi and dQ, dK MMAs
+  // complete on barriers of their own, so one side's CUDA-core work runs
+  // under the other side's MMAs; with 64 the MMAs and exponentials are short
   // and the extra hand-offs cost more than they hide (one commit for both)
-  constexpr bool kSplitU = MC == 128;
+  constexpr bool kSplit = MC == 128;
   const Layout lay(MC);
   const uint32_t sb = smem_u32(smem);
   uint64_t *in_bar = reinterpret_cast<uint64_t *>(smem + lay.bars);
@@ -342,141 +343,283 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_3d(&tmDY, 0, (t - 1) * kTile, bh);
     }
 
-    // (b) features of both sides: F_k -> T, F_q -> X, one commit
-    if (FAVOR) {
+    if constexpr (kSplit) {
+      // (b) features: F_k -> T (its own commit), F_q -> X.  phi_k first, so
+      // the state-increment MMA runs while phi_q is formed
+      float ck = 0.f, cq = 0.f;
+      if (FAVOR) {
+        if (issue0()) {
+          const uint32_t id = make_idesc(128, MC, false, false);
+          for (int s = 0; s < D / 16; ++s)
+            mma_bf16(tb + kT, desc_kmajor(s_k, kTile, 0, s), desc_kmajor(s_w, MC, 0, s), id, s > 0);
+          mma_commit(mmb_bar);
+          for (int s = 0; s < D / 16; ++s)
+            mma_bf16(tb + kX, desc_kmajor(s_q, kTile, 0, s), desc_kmajor(s_w, MC, 0, s), id, s > 0);
+          mma_done();
+        }
+        // |k|^2, |q|^2 of the row while the MMAs run, each part summing a
+        // quarter of the columns (the u row-sum arrays are idle until (i))
+        usq[part * kTile + row] = tile_row_sqnorm_part(s_k, row, QD * part, QD);
+        usk[part * kTile + row] = tile_row_sqnorm_part(s_q, row, QD * part, QD);
+        __syncthreads();
+        const float nk = (usq[row] + usq[kTile + row]) + (usq[2 * kTile + row] + usq[3 * kTile + row]);
+        const float nq = (usk[row] + usk[kTile + row]) + (usk[2 * kTile + row] + usk[3 * kTile + row]);
+        ck = live ? favor_row_const(nk, M) : -INFINITY;
+        cq = live ? favor_row_const(nq, M) : -INFINITY;
+      }
+      // one side's features: FAVOR+ from the TMEM pre-activations (padding
+      // rows: F = 0 from the zero-filled tile and 2^-inf = 0), elu+1 from the
+      // input tile
+      auto features = [&](uint32_t col, float c, uint32_t s_x, uint32_t s_out) {
+        const int c0 = QF * part;
+        if (FAVOR) {
+          float f[QF];
+          if constexpr (QF == 32) {
+            tmem_ld32(tmem_addr(tb, 32 * q4, col + c0), f);
+          } else {
+            tmem_ld16(tmem_addr(tb, 32 * q4, col + c0), f);
+          }
+#pragma unroll
+          for (int i = 0; i < QF; i += 2) favor_feature2(f[i], f[i + 1], c);
+#pragma unroll
+          for (int j = 0; j < QF / 8; ++j) st_bf16x8(s_out + sw128_offset(row, c0 + 8 * j, kTile), f + 8 * j);
+        } else {
+          for (int cc = c0; cc < c0 + QF; cc += 8) {
+            float v[8];
+            ld_bf16x8(s_x + sw128_offset(row, cc, kTile), v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = live ? elu1_feature(v[i]) : 0.f;
+            st_bf16x8(s_out + sw128_offset(row, cc, kTile), v);
+          }
+        }
+      };
+      if (FAVOR) wait_mmb();
+      features(kT, ck, s_k, s_phk);
+      fence_async_smem();
+      cta_sync();
+
+      // (c) eq. (19): R' -= phi_k^T [V, 1], removing exactly the increment the
+      // segment pre-pass added for this tile (increment -> T, its own commit),
+      // while phi_q is formed
+      go &= mbar_wait(in2_bar, in2_phase, p.status, abort_flag);  // V (and dY, read in (f))
+      in2_phase ^= 1;
       if (issue0()) {
-        const uint32_t id = make_idesc(128, MC, false, false);
-        for (int s = 0; s < D / 16; ++s)
-          mma_bf16(tb + kT, desc_kmajor(s_k, kTile, 0, s), desc_kmajor(s_w, MC, 0, s), id, s > 0);
-        for (int s = 0; s < D / 16; ++s)
-          mma_bf16(tb + kX, desc_kmajor(s_q, kTile, 0, s), desc_kmajor(s_w, MC, 0, s), id, s > 0);
+        // last tile's dQ, dK partials (staged in the G_V-copy and R-copy tiles) have
+        // been read by their reduce-adds before this phase's epilogue reuses them
+        if (CS == 2) tma_store_wait_read();
+        issue_state_delta(tb + kT, s_phk, s_v, s_ones, D);
+        mma_commit(mmb_bar);
+      }
+      if (FAVOR) wait_mma();
+      features(kX, cq, s_q, s_phq);
+      fence_async_smem();
+      cta_sync();
+      // my receive slots (in usk) are idle until (i): the peer may send its
+      // row partials there (signalled off the MMA-issuing thread: the
+      // cluster-scope release waits for this thread's earlier stores)
+      if (CS == 2 && tid == 32 && go) mbar_arrive_remote(peer_x1_free);
+
+      // A = phi_q phi_k^T -> X (its own commit: eq. (19) below runs under it)
+      if (issue0()) {
+        const uint32_t id = make_idesc(128, 128, false, false);
+        for (int s = 0; s < MC / 16; ++s)
+          mma_bf16(tb + kX, desc_kmajor(s_phq, kTile, 0, s), desc_kmajor(s_phk, kTile, 0, s), id, s > 0);
         mma_done();
       }
-      // |k|^2, |q|^2 of the row while the MMAs run, each part summing a
-      // quarter of the columns (the u row-sum arrays are idle until (i))
-      usq[part * kTile + row] = tile_row_sqnorm_part(s_k, row, QD * part, QD);
-      usk[part * kTile + row] = tile_row_sqnorm_part(s_q, row, QD * part, QD);
-      __syncthreads();
-      const float nk = (usq[row] + usq[kTile + row]) + (usq[2 * kTile + row] + usq[3 * kTile + row]);
-      const float nq = (usk[row] + usk[kTile + row]) + (usk[2 * kTile + row] + usk[3 * kTile + row]);
-      const float ck = live ? favor_row_const(nk, M) : -INFINITY;
-      const float cq = live ? favor_row_const(nq, M) : -INFINITY;
-      wait_mma();
+      wait_mmb();
+      // eq. (19) on the double-float master, and from the updated values the
+      // bf16 copy of R for the MMAs and fp32 S for the epilogues (R: 16
+      // columns per part; S, column D, on part 3)
       {
-        // both sides' F with one wait, so the two loads' latencies overlap
-        const int c0 = QF * part;
-        float fk[QF], fq[QF];
-        if constexpr (QF == 32) {
-          tmem_ld32x2(tmem_addr(tb, 32 * q4, kT + c0), tmem_addr(tb, 32 * q4, kX + c0), fk, fq);
-        } else {
-          tmem_ld16x2(tmem_addr(tb, 32 * q4, kT + c0), tmem_addr(tb, 32 * q4, kX + c0), fk, fq);
-        }
-        // padding rows: F = 0 (zero-filled tile) and 2^-inf = 0
+        const int c = 16 * part;
+        float x[16], h[16], l[16];
+        tmem_ld16x3(tmem_addr(tb, 32 * q4, kT + c), tmem_addr(tb, 32 * q4, kRhi + c),
+                    tmem_addr(tb, 32 * q4, kRlo + c), x, h, l);
 #pragma unroll
-        for (int i = 0; i < QF; i += 2) {
-          favor_feature2(fk[i], fk[i + 1], ck);
-          favor_feature2(fq[i], fq[i + 1], cq);
+        for (int i = 0; i < 16; i += 2) {
+          float2 h2 = make_float2(h[i], h[i + 1]), l2 = make_float2(l[i], l[i + 1]);
+          df_sub2(h2, l2, make_float2(x[i], x[i + 1]));
+          h[i] = h2.x;
+          h[i + 1] = h2.y;
+          l[i] = l2.x;
+          l[i + 1] = l2.y;
         }
+        tmem_st16(tmem_addr(tb, 32 * q4, kRhi + c), h);
+        tmem_st16(tmem_addr(tb, 32 * q4, kRlo + c), l);
+        if (row < MC) {
 #pragma unroll
-        for (int j = 0; j < QF / 8; ++j) {
-          st_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), fk + 8 * j);
-          st_bf16x8(s_phq + sw128_offset(row, c0 + 8 * j, kTile), fq + 8 * j);
+          for (int i = 0; i < 16; ++i) x[i] = h[i] + l[i];
+#pragma unroll
+          for (int i = 0; i < 16; i += 8) st_bf16x8(s_rb + sw128_offset(row, c + i, MC), x + i);
+        }
+        if (part == kParts - 1) {
+          float xs, hs, ls;
+          tmem_ld1x3(tmem_addr(tb, 32 * q4, kT + D), tmem_addr(tb, 32 * q4, kRhi + D),
+                     tmem_addr(tb, 32 * q4, kRlo + D), xs, hs, ls);
+          df_add(hs, ls, -xs);
+          tmem_st1(tmem_addr(tb, 32 * q4, kRhi + D), hs);
+          tmem_st1(tmem_addr(tb, 32 * q4, kRlo + D), ls);
+          if (row < MC) s_f[row] = hs + ls;
         }
       }
+      wait_mma();
+      // tril(A) (diagonal kept) -> bf16 tile, and this part's row sum of it
+      {
+        float v[32];
+        tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * part), v);
+        // r4[i & 3] sums as two packed pairs: (0, 1), (2, 3)
+        float2 r4[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          if (32 * part + i > row) v[i] = 0.f;
+          if (32 * part + i + 1 > row) v[i + 1] = 0.f;
+          r4[(i >> 1) & 1] = __fadd2_rn(r4[(i >> 1) & 1], make_float2(v[i], v[i + 1]));
+        }
+        asum[part * kTile + row] = (r4[0].x + r4[0].y) + (r4[1].x + r4[1].y);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, 32 * part + 8 * j, kTile), v + 8 * j);
+      }
+      // no MMA reads the masters and only this thread rereads its columns (the
+      // next tile), so their stores are waited for later, off this barrier
+      fence_async_smem();
+      cta_sync();
     } else {
-      for (int side = 0; side < 2; ++side) {
-        const uint32_t s_x = side ? s_q : s_k, s_out = side ? s_phq : s_phk;
-        for (int c0 = QF * part; c0 < QF * (part + 1); c0 += 8) {
-          float v[8];
-          ld_bf16x8(s_x + sw128_offset(row, c0, kTile), v);
+      // (b) features of both sides: F_k -> T, F_q -> X, one commit
+      if (FAVOR) {
+        if (issue0()) {
+          const uint32_t id = make_idesc(128, MC, false, false);
+          for (int s = 0; s < D / 16; ++s)
+            mma_bf16(tb + kT, desc_kmajor(s_k, kTile, 0, s), desc_kmajor(s_w, MC, 0, s), id, s > 0);
+          for (int s = 0; s < D / 16; ++s)
+            mma_bf16(tb + kX, desc_kmajor(s_q, kTile, 0, s), desc_kmajor(s_w, MC, 0, s), id, s > 0);
+          mma_done();
+        }
+        // |k|^2, |q|^2 of the row while the MMAs run, each part summing a
+        // quarter of the columns (the u row-sum arrays are idle until (i))
+        usq[part * kTile + row] = tile_row_sqnorm_part(s_k, row, QD * part, QD);
+        usk[part * kTile + row] = tile_row_sqnorm_part(s_q, row, QD * part, QD);
+        __syncthreads();
+        const float nk = (usq[row] + usq[kTile + row]) + (usq[2 * kTile + row] + usq[3 * kTile + row]);
+        const float nq = (usk[row] + usk[kTile + row]) + (usk[2 * kTile + row] + usk[3 * kTile + row]);
+        const float ck = live ? favor_row_const(nk, M) : -INFINITY;
+        const float cq = live ? favor_row_const(nq, M) : -INFINITY;
+        wait_mma();
+        {
+          // both sides' F with one wait, so the two loads' latencies overlap
+          const int c0 = QF * part;
+          float fk[QF], fq[QF];
+          if constexpr (QF == 32) {
+            tmem_ld32x2(tmem_addr(tb, 32 * q4, kT + c0), tmem_addr(tb, 32 * q4, kX + c0), fk, fq);
+          } else {
+            tmem_ld16x2(tmem_addr(tb, 32 * q4, kT + c0), tmem_addr(tb, 32 * q4, kX + c0), fk, fq);
+          }
+          // padding rows: F = 0 (zero-filled tile) and 2^-inf = 0
 #pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = live ? elu1_feature(v[i]) : 0.f;
-          st_bf16x8(s_out + sw128_offset(row, c0, kTile), v);
+          for (int i = 0; i < QF; i += 2) {
+            favor_feature2(fk[i], fk[i + 1], ck);
+            favor_feature2(fq[i], fq[i + 1], cq);
+          }
+#pragma unroll
+          for (int j = 0; j < QF / 8; ++j) {
+            st_bf16x8(s_phk + sw128_offset(row, c0 + 8 * j, kTile), fk + 8 * j);
+            st_bf16x8(s_phq + sw128_offset(row, c0 + 8 * j, kTile), fq + 8 * j);
+          }
+        }
+      } else {
+        for (int side = 0; side < 2; ++side) {
+          const uint32_t s_x = side ? s_q : s_k, s_out = side ? s_phq : s_phk;
+          for (int c0 = QF * part; c0 < QF * (part + 1); c0 += 8) {
+            float v[8];
+            ld_bf16x8(s_x + sw128_offset(row, c0, kTile), v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = live ? elu1_feature(v[i]) : 0.f;
+            st_bf16x8(s_out + sw128_offset(row, c0, kTile), v);
+          }
         }
       }
-    }
-    fence_async_smem();
-    cta_sync();
-    // my receive slots (in usk) are idle until (i): the peer may send its
-    // row partials there (signalled off the MMA-issuing thread: the
-    // cluster-scope release waits for this thread's earlier stores)
-    if (CS == 2 && tid == 32 && go) mbar_arrive_remote(peer_x1_free);
+      fence_async_smem();
+      cta_sync();
+      // my receive slots (in usk) are idle until (i): the peer may send its
+      // row partials there (signalled off the MMA-issuing thread: the
+      // cluster-scope release waits for this thread's earlier stores)
+      if (CS == 2 && tid == 32 && go) mbar_arrive_remote(peer_x1_free);
 
-    // (c) A = phi_q phi_k^T -> X (its own commit: the mask below overlaps
-    // the next group), and eq. (19): R' -= phi_k^T [V, 1], removing exactly
-    // the increment the segment pre-pass added for this tile (increment -> T)
-    if (issue0()) {
-      // last tile's dQ, dK partials (staged in the G_V-copy and R-copy tiles) have
-      // been read by their reduce-adds before this phase's epilogue reuses them
-      if (CS == 2) tma_store_wait_read();
-      const uint32_t id = make_idesc(128, 128, false, false);
-      for (int s = 0; s < MC / 16; ++s)
-        mma_bf16(tb + kX, desc_kmajor(s_phq, kTile, 0, s), desc_kmajor(s_phk, kTile, 0, s), id, s > 0);
-      mma_commit(mmb_bar);
-    }
-    go &= mbar_wait(in2_bar, in2_phase, p.status, abort_flag);  // V (and dY, read in (f))
-    in2_phase ^= 1;
-    if (issue0()) {
-      issue_state_delta(tb + kT, s_phk, s_v, s_ones, D);
-      mma_done();
-    }
-    wait_mmb();
-    // tril(A) (diagonal kept) -> bf16 tile, and this part's row sum of it
-    {
-      float v[32];
-      tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * part), v);
-      // r4[i & 3] sums as two packed pairs: (0, 1), (2, 3)
-      float2 r4[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        if (32 * part + i > row) v[i] = 0.f;
-        if (32 * part + i + 1 > row) v[i + 1] = 0.f;
-        r4[(i >> 1) & 1] = __fadd2_rn(r4[(i >> 1) & 1], make_float2(v[i], v[i + 1]));
+      // (c) A = phi_q phi_k^T -> X (its own commit: the mask below overlaps
+      // the next group), and eq. (19): R' -= phi_k^T [V, 1], removing exactly
+      // the increment the segment pre-pass added for this tile (increment -> T)
+      if (issue0()) {
+        // last tile's dQ, dK partials (staged in the G_V-copy and R-copy tiles) have
+        // been read by their reduce-adds before this phase's epilogue reuses them
+        if (CS == 2) tma_store_wait_read();
+        const uint32_t id = make_idesc(128, 128, false, false);
+        for (int s = 0; s < MC / 16; ++s)
+          mma_bf16(tb + kX, desc_kmajor(s_phq, kTile, 0, s), desc_kmajor(s_phk, kTile, 0, s), id, s > 0);
+        mma_commit(mmb_bar);
       }
-      asum[part * kTile + row] = (r4[0].x + r4[0].y) + (r4[1].x + r4[1].y);
+      go &= mbar_wait(in2_bar, in2_phase, p.status, abort_flag);  // V (and dY, read in (f))
+      in2_phase ^= 1;
+      if (issue0()) {
+        issue_state_delta(tb + kT, s_phk, s_v, s_ones, D);
+        mma_done();
+      }
+      wait_mmb();
+      // tril(A) (diagonal kept) -> bf16 tile, and this part's row sum of it
+      {
+        float v[32];
+        tmem_ld32(tmem_addr(tb, 32 * q4, kX + 32 * part), v);
+        // r4[i & 3] sums as two packed pairs: (0, 1), (2, 3)
+        float2 r4[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, 32 * part + 8 * j, kTile), v + 8 * j);
+        for (int i = 0; i < 32; i += 2) {
+          if (32 * part + i > row) v[i] = 0.f;
+          if (32 * part + i + 1 > row) v[i + 1] = 0.f;
+          r4[(i >> 1) & 1] = __fadd2_rn(r4[(i >> 1) & 1], make_float2(v[i], v[i + 1]));
+        }
+        asum[part * kTile + row] = (r4[0].x + r4[0].y) + (r4[1].x + r4[1].y);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) st_bf16x8(s_at + sw128_offset(row, 32 * part + 8 * j, kTile), v + 8 * j);
+      }
+      wait_mma();
+      // eq. (19) on the double-float master, and from the updated values the
+      // bf16 copy of R for the MMAs and fp32 S for the epilogues (R: 16
+      // columns per part; S, column D, on part 3)
+      {
+        const int c = 16 * part;
+        float x[16], h[16], l[16];
+        tmem_ld16x3(tmem_addr(tb, 32 * q4, kT + c), tmem_addr(tb, 32 * q4, kRhi + c),
+                    tmem_addr(tb, 32 * q4, kRlo + c), x, h, l);
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          float2 h2 = make_float2(h[i], h[i + 1]), l2 = make_float2(l[i], l[i + 1]);
+          df_sub2(h2, l2, make_float2(x[i], x[i + 1]));
+          h[i] = h2.x;
+          h[i + 1] = h2.y;
+          l[i] = l2.x;
+          l[i + 1] = l2.y;
+        }
+        tmem_st16(tmem_addr(tb, 32 * q4, kRhi + c), h);
+        tmem_st16(tmem_addr(tb, 32 * q4, kRlo + c), l);
+        if (row < MC) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[i] = h[i] + l[i];
+#pragma unroll
+          for (int i = 0; i < 16; i += 8) st_bf16x8(s_rb + sw128_offset(row, c + i, MC), x + i);
+        }
+        if (part == kParts - 1) {
+          float xs, hs, ls;
+          tmem_ld1x3(tmem_addr(tb, 32 * q4, kT + D), tmem_addr(tb, 32 * q4, kRhi + D),
+                     tmem_addr(tb, 32 * q4, kRlo + D), xs, hs, ls);
+          df_add(hs, ls, -xs);
+          tmem_st1(tmem_addr(tb, 32 * q4, kRhi + D), hs);
+          tmem_st1(tmem_addr(tb, 32 * q4, kRlo + D), ls);
+          if (row < MC) s_f[row] = hs + ls;
+        }
+      }
+      // no MMA reads the masters and only this thread rereads its columns (the
+      // next tile), so their stores are waited for later, off this barrier
+      fence_async_smem();
+      cta_sync();
     }
-    wait_mma();
-    // eq. (19) on the double-float master, and from the updated values the
-    // bf16 copy of R for the MMAs and fp32 S for the epilogues (R: 16
-    // columns per part; S, column D, on part 3)
-    {
-      const int c = 16 * part;
-      float x[16], h[16], l[16];
-      tmem_ld16x3(tmem_addr(tb, 32 * q4, kT + c), tmem_addr(tb, 32 * q4, kRhi + c),
-                  tmem_addr(tb, 32 * q4, kRlo + c), x, h, l);
-#pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        float2 h2 = make_float2(h[i], h[i + 1]), l2 = make_float2(l[i], l[i + 1]);
-        df_sub2(h2, l2, make_float2(x[i], x[i + 1]));
-        h[i] = h2.x;
-        h[i + 1] = h2.y;
-        l[i] = l2.x;
-        l[i + 1] = l2.y;
-      }
-      tmem_st16(tmem_addr(tb, 32 * q4, kRhi + c), h);
-      tmem_st16(tmem_addr(tb, 32 * q4, kRlo + c), l);
-      if (row < MC) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = h[i] + l[i];
-#pragma unroll
-        for (int i = 0; i < 16; i += 8) st_bf16x8(s_rb + sw128_offset(row, c + i, MC), x + i);
-      }
-      if (part == kParts - 1) {
-        float xs, hs, ls;
-        tmem_ld1x3(tmem_addr(tb, 32 * q4, kT + D), tmem_addr(tb, 32 * q4, kRhi + D),
-                   tmem_addr(tb, 32 * q4, kRlo + D), xs, hs, ls);
-        df_add(hs, ls, -xs);
-        tmem_st1(tmem_addr(tb, 32 * q4, kRhi + D), hs);
-        tmem_st1(tmem_addr(tb, 32 * q4, kRlo + D), ls);
-        if (row < MC) s_f[row] = hs + ls;
-      }
-    }
-    // no MMA reads the masters and only this thread rereads its columns (the
-    // next tile), so their stores are waited for later, off this barrier
-    fence_async_smem();
-    cta_sync();
 
     // (f) num = A V + phi_q R^T -> T; Y, dN, dD.  den = rowsum(tril A) +
     // phi_q . S comes from the CUDA cores while the MMAs run
@@ -620,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_store_commit();
     }
 
-    // (h) dphi_k -> X (kSplitU: its own commit, u_k starts on it while
+    // (h) dphi_k -> X (kSplit: its own commit, u_k starts on it while
     // dphi_q's MMAs run), dphi_q -> T, then the G update (its own commit:
     // it runs under u, which leaves phi_q, dN and dD, the update's operands,
     // in place)
@@ -631,13 +774,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_bf16(tb + kX, desc_mnmajor(s_at, kTile, 0, s), desc_mnmajor(s_phq, kTile, 0, s), id_k1, s > 0);
       for (int s = 0; s < D / 16; ++s)
         mma_bf16(tb + kX, desc_kmajor(s_v, kTile, 0, s), desc_kmajor(s_gv, MC, 0, s), id_q2, 1);
-      if (kSplitU) mma_commit(mmb_bar);
+      if (kSplit) mma_commit(mmb_bar);
       const uint32_t id_q1 = make_idesc(128, MC, false, true);
       for (int s = 0; s < kTile / 16; ++s)
         mma_bf16(tb + kT, desc_kmajor(s_at, kTile, 0, s), desc_mnmajor(s_phk, kTile, 0, s), id_q1, s > 0);
       for (int s = 0; s < D / 16; ++s)
         mma_bf16(tb + kT, desc_kmajor(s_dy, kTile, 0, s), desc_kmajor(s_rb, MC, 0, s), id_q2, 1);
-      mma_commit(kSplitU ? mmc_bar : mmb_bar);
+      mma_commit(kSplit ? mmc_bar : mmb_bar);
       const uint32_t id_g = make_idesc(128, D, true, true);
       const uint32_t id_g1 = make_idesc(128, 16, true, true);
       for (int s = 0; s < kTile / 16; ++s) {
@@ -667,8 +810,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // (i) u = phi * dphi and its row sums, one side at a time: u_k (with
-    // kSplitU while dphi_q's MMAs run), then u_q.  FAVOR+: u as bf16 pairs
-    // into TMEM over dphi (the A operand of (j)), with kSplitU the dK MMAs
+    // kSplit while dphi_q's MMAs run), then u_q.  FAVOR+: u as bf16 pairs
+    // into TMEM over dphi (the A operand of (j)), with kSplit the dK MMAs
     // issued between the two sides; elu+1 writes dQ, dK here.  With DW, u_k also goes over phi_k
     // once dphi_q has read it, and u_q over phi_q once the G update has
     // read phi_q.  The dphi terms that are not MMAs are added here:
@@ -734,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     uint32_t uq_pairs[QF / 2], uk_pairs[QF / 2];
     u_side(kX, s_phk, gs_f, 1.f, usk, uk_pairs, p.dk);
-    if (FAVOR && kSplitU) {
+    if (FAVOR && kSplit) {
       // dK = u_k W^T (-> X + 64) under u_q
       tmem_st_wait();
       cta_sync();
@@ -745,7 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(mmd_bar);
       }
     }
-    if (kSplitU) wait_mmc();
+    if (kSplit) wait_mmc();
     if (CS == 2) {
       // the dA tile is idle from here: Q and K come back into it for the
       // dQ, dK epilogue (the Q tile holds the dV partial, K the next K)
@@ -788,9 +931,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t id = make_idesc(128, D, false, true);
         for (int s = 0; s < MC / 16; ++s) {
           mma_bf16_ta(tb + kT + 64, tb + kT + 8 * s, desc_mnmajor(s_w, MC, 0, s), id, s > 0);
-          if (!kSplitU) mma_bf16_ta(tb + kX + 64, tb + kX + 8 * s, desc_mnmajor(s_w, MC, 0, s), id, s > 0);
+          if (!kSplit) mma_bf16_ta(tb + kX + 64, tb + kX + 8 * s, desc_mnmajor(s_w, MC, 0, s), id, s > 0);
         }
-        mma_done();  // with kSplitU, the dK MMAs issued under u_q too
+        mma_done();  // with kSplit, the dK MMAs issued under u_q too
       }
       uint32_t s_xq = s_q, s_xk = s_k;
       if (CS == 2) {
@@ -815,7 +958,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // dQ = u_q W^T - q rowsum(u_q), dK likewise (this CTA's features)
       float oq[QD], ok[QD];
-      if constexpr (kSplitU) {
+      if constexpr (kSplit) {
         // dK first: its MMAs ran under u_q (their own commit), so its
         // epilogue runs while the dQ MMAs do
         wait_mmd();
