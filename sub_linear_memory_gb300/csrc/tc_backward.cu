@@ -1060,7 +1060,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 16; i += 4) red_add_v4(dst + i, wv[i], wv[i + 1], wv[i + 2], wv[i + 3]);
         }
       }
-      cta_sync();
+      // this tile's TMEM loads complete before the next tile's MMAs: with a
+      // CTA pair (and no dW) the staging barrier above has ordered them
+      if (CS == 1 || DW) cta_sync();
     }
     x_phase ^= 1;
     if (CS == 1 && issue0() && t > t0) {
