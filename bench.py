@@ -389,17 +389,18 @@ def per_head_redraw_timing(binding, inputs, peaks, steps=20, warmup=3):
             "frac": roof * 1e3 / ms, "steps": steps}
 
 
-def streamed_timings(binding, inputs, exps=(20, 21, 22), window=1 << 18, steps=3, warmup=2):
+def streamed_timings(binding, inputs, exps=(20, 21, 22), window=1 << 18, steps=5, warmup=2):
     """fwd + bwd of the 1M workload's head shape with Q, K, V, dY (and Y, dQ,
     dK, dV) kept in pinned host memory and run window by window (stream.py):
     CUDA-event time per step on the current stream (the host<->device copies
-    are part of the work), the bytes copied, and the peak device memory held
-    against L."""
+    are part of the work; the median of the timed steps), the bytes copied,
+    and the peak device memory held against L."""
     from sub_linear_memory_gb300 import stream
 
     base = inputs.WORKLOADS["l1m"]
     out = {"workload": "l1m head shape (B=1, H=8, d=64, M=64, chunk 256), inputs and outputs in pinned host memory",
-           "window": window, "L": [], "ms_per_step": [], "tokens_per_s": [], "peak_device_bytes": [],
+           "window": window, "timing": "median of %d steps after %d warm-up" % (steps, warmup),
+           "L": [], "ms_per_step": [], "tokens_per_s": [], "peak_device_bytes": [],
            "h2d_bytes_per_step": [], "d2h_bytes_per_step": []}
     for e in exps:
         wl = base.with_(L=1 << e)
@@ -423,14 +424,18 @@ def streamed_timings(binding, inputs, exps=(20, 21, 22), window=1 << 18, steps=3
         for _ in range(warmup):
             step()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
+        # each step timed on its own and the median kept: a step here is
+        # mostly host-link copies, which another process on the host can slow
+        times = []
         for _ in range(steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
             step()
-        e1.record()
-        torch.cuda.synchronize()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
         binding.sync_status()
-        ms = e0.elapsed_time(e1) / steps
+        ms = sorted(times)[len(times) // 2]
         nbytes = q.numel() * q.element_size()
         out["L"].append(wl.L)
         out["ms_per_step"].append(ms)
