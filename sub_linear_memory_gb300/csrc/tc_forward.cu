@@ -510,7 +510,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         arrive(F_EMPTY + s);
       }
       // phi_q . S(t-1) needs S(t-1), written with the bf16 copy of R(t-1)
-      if (side && !wait(F_RBFULL, i & 1)) break;
+      // once the previous tile's last MMAs are done: the first block's
+      // features are formed and stored without it, and its share of the dot
+      // product is taken from the stored bf16 values once S(t-1) is in; later
+      // blocks (after the wait) use their fp32 values.
       // dp[x & 3] sums of phi_q . S(t-1), as two packed pairs: (0, 1), (2, 3)
       float2 dp[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       for (int h = 0; h < nb && ok; ++h) {
@@ -534,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int x = 0; x < 8; ++x) v[8 * j + x] = dead ? 0.f : elu1_feature(v[8 * j + x]);
             }
           }
-          if (side) {
+          if (side && h > 0) {
             const float2 *sh = reinterpret_cast<const float2 *>(ss + 128 * h + 64 * half);
 #pragma unroll
             for (int x = 0; x < 64; x += 2)
@@ -545,6 +548,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 8; ++j) st_bf16x8(s_out + sw128_offset(row, 64 * half + 8 * j, kTile), v + 8 * j);
         }
         if (!ok) break;
+        if (side && h == 0) {
+          // the first block's phi_q . S(t-1), from this row's stored bf16
+          // features, before the MMAs are told the block is in (S(t) then
+          // replaces S(t-1) only after this tile's last MMAs)
+          if (!wait(F_RBFULL, i & 1)) break;
+#pragma unroll 4
+          for (int x0 = 0; x0 < FB; x0 += 8) {
+            float f[8];
+            ld_bf16x8(s_out + sw128_offset(row, x0, kTile), f);
+            const float2 *sh = reinterpret_cast<const float2 *>(ss + x0);
+#pragma unroll
+            for (int x = 0; x < 8; x += 2)
+              dp[(x >> 1) & 1] = __ffma2_rn(make_float2(f[x], f[x + 1]), sh[x >> 1], dp[(x >> 1) & 1]);
+          }
+        }
         fence_async_smem();
         arrive(b_stored);
       }
