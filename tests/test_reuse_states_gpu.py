@@ -99,6 +99,8 @@ def test_backward_reads_forward_states(case, lib):
     print(prof)
     assert prof["tc_forward"][0] == 1 and prof["tc_backward"][0] == 1, prof
     assert prof["tc_segment_state"][0] == 1, prof  # the forward's, read again by the backward
+    # the W image too: the backward reads the forward's, at the same workspace offset
+    assert prof.get("prep_w", (0,))[0] == (1 if feature == "favor" else 0), prof
     qn, kn, vn, dyn = _np(q), _np(k), _np(v), _np(dy)
     wn = None if w is None else _np(w)
     y_ref = oracle.recurrence_forward(qn, kn, vn, wn)
@@ -125,6 +127,7 @@ def test_per_head_w_reuse(lib):
         lib.set_option(lib.OPT_REUSE_STATES, 0)
         lib.set_option(lib.OPT_W_PER_HEAD, 0)
     assert prof["tc_segment_state"][0] == 1, prof
+    assert prof["prep_w"][0] == 1, prof
     qn, kn, vn, dyn, wn = _np(q), _np(k), _np(v), _np(dy), _np(w)
     y_ref = oracle.recurrence_forward(qn, kn, vn, wn)
     ref = oracle.recurrence_backward(qn, kn, vn, wn, dyn, want_dw=True)
@@ -158,6 +161,7 @@ def test_mismatch_recomputes(between, lib):
         lib.set_option(lib.OPT_REUSE_STATES, 0)
     expect = 2 if between != "state_call" else 3  # forward, (state call,) backward
     assert prof["tc_segment_state"][0] == expect, prof
+    assert prof["prep_w"][0] == expect, prof  # each state pass makes its own W image
     qn, kn, vn, dyn, wn = _np(q), _np(kb), _np(v), _np(dy), _np(w)
     ref = oracle.recurrence_backward(qn, kn, vn, wn, dyn, want_dw=False)
     _compare(grads[:3], ref[:3])
